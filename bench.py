@@ -1,0 +1,507 @@
+#!/usr/bin/env python
+"""Benchmark of the speculative-decoding hot path (n-gram draft -> verify ->
+append -> n-gram update) on GB300, through the library's public API.
+
+One step = one pass of the whole path over one batch: ngram_draft,
+spec_verify, spec_append and ngram_update, with the target logits already
+resident in HBM (a rotating set of synthetic batches larger than L2).
+Prints one JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c5]
+    python bench.py --impl reference ...   # the fp64 oracle on the host cores
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from speculative_decoding_draft_ngram_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "spec_verify rows/s (B*(K+1) logit rows)"
+UNIT = "rows/s"
+DESCR = {
+    "c2": "Qwen3-4B-shaped verify: B=1 V=151936 K=4 bf16 N(0,1)*4 logits, draft boosted to rowmax+6 w.p. 0.5, "
+          "T=0.6, history 4096 Zipf(1.05) with 32-token copied spans, n-gram drafts",
+    "c3": "Gemma-4-E2B-shaped continuous batch: B=64 V=262144 K=4 bf16 N(0,1)*8 logits, soft cap 30, T=1, "
+          "histories U[512,8192] Zipf(1.1) with copied spans, n-gram drafts, EMA gate (tau 0.1, thr 0.5), "
+          "boost w.p. U[0.2,0.9] per sequence",
+    "c4": "dense-q verify: B=32 V=151936 K=4 T=0.6 bf16 N(0,1)*4 target, fp32 q = softmax((target+N(0,0.5))/0.6), "
+          "drafts sampled from q, Leviathan accept + residual resampling",
+    "c5": "large batch: B=256 V=151936 k_b~U{0..4} bf16 N(0,1)*4 logits, repetition penalty 1.1 over the last "
+          "64 tokens, T=0.6, histories 32768 Zipf(1.05) with 64-token copied spans, n-gram update each step",
+}
+VERIFY_SRC = os.path.join(ROOT, "speculative_decoding_draft_ngram_gb300", "csrc", "verify.cuh")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="c5", choices=sorted(DESCR))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample", type=int, default=0, help="sequences in the oracle sample (0: auto)")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, bf16 copy)"
+    return 6800.0, "fallback (6.8 TB/s, one earlier GB300 measurement)"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("verify.cuh", "common.cuh"):
+        with open(os.path.join(ROOT, "speculative_decoding_draft_ngram_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", f"verify_stream_{workload}.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("source_hash") != source_hash():
+        return None
+    return d.get("dram_bytes_per_launch_full")
+
+
+class Clocks:
+    """nvidia-smi sampler running during the timed region."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.proc = None
+        self.path = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            ident = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            ident = None
+        self.ident = ident
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "20"]
+            if self.ident:
+                cmd += ["-i", self.ident]
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self, window=None):
+        """Summary of the samples whose timestamps fall in window = (t0, t1)
+        (host wall-clock seconds bracketing the timed region)."""
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 10:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if window is not None:
+            from datetime import datetime
+            keep = []
+            for r in rows:
+                try:
+                    ts = datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    continue
+                if window[0] <= ts <= window[1]:
+                    keep.append(r)
+            rows = keep or rows[-1:]
+        if not rows:
+            return None
+        num = lambda x: x.replace(".", "", 1).isdigit()  # noqa: E731
+        sm = [float(r[2]) for r in rows if num(r[2])]
+        mx = [float(r[3]) for r in rows if num(r[3])]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[6:10]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- our arm
+
+class Path:
+    """Device state of one workload and its step function."""
+
+    def __init__(self, name, steps_total, device, seed_offset=0):
+        import speculative_decoding_draft_ngram_gb300 as sp
+        self.sp = sp
+        cfg = wl.get(name)
+        cfg = wl.get(name, steps=max(cfg.steps, steps_total), data_seed=cfg.data_seed + 7919 * seed_offset,
+                     sampler_seed=cfg.sampler_seed + seed_offset)
+        self.cfg = cfg
+        self.dev = device
+        B, K, V = cfg.B, cfg.K, cfg.V
+        self.hist, self.lens = wl.histories(cfg, device)
+        self.ngram = not cfg.dense
+        if self.ngram:
+            self.table = sp.NgramTable(B, V, B * cfg.hist_cap, device=device)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            sp.ngram_update(self.table, self.hist, self.lens)
+            torch.cuda.synchronize()
+            self.build_ms = (time.perf_counter() - t0) * 1e3
+        g = wl._gen(cfg.data_seed + 1, device)
+        set_bytes = B * (K + 1) * V * (2 if cfg.dtype == "bf16" else 4)
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        self.n_sets = max(3, math.ceil(2 * l2 / set_bytes) + 1)
+        self.set_bytes = set_bytes
+        self.logits = [wl.step_logits(cfg, g, device=device) for _ in range(self.n_sets)]
+        self.q = [None] * self.n_sets
+        self.dsets = [None] * self.n_sets
+        if cfg.dense:
+            for i in range(self.n_sets):
+                self.q[i], self.dsets[i] = wl.dense_draft(cfg, self.logits[i], g)
+        self.limits = (wl.draft_limits(cfg, g, device) if not cfg.k_uniform else
+                       torch.randint(0, K + 1, (steps_total, B), generator=g, device=device, dtype=torch.int32))
+        self.bprob = wl.boost_probs(cfg, device)
+        self.kbuf = torch.zeros((steps_total, B), dtype=torch.int32, device=device)
+        self.drafts = torch.full((B, K), -1, dtype=torch.int32, device=device)
+        self.kfull = torch.full((B,), K, dtype=torch.int32, device=device)
+        self.kv = self.lens.clone()
+        self.ema = torch.ones(B, dtype=torch.float32, device=device)
+        self.out = torch.empty((B, K + 1), dtype=torch.int32, device=device)
+        self.acc = torch.empty((B,), dtype=torch.int32, device=device)
+        self.ws = sp.spec_verify_workspace(B, K, V, device)
+        self.params = sp.VerifyParams(temperature=cfg.temperature, softcap=cfg.softcap, rep_penalty=cfg.rep_penalty,
+                                      rep_window=cfg.rep_window, gate_enabled=cfg.gate, seed=cfg.sampler_seed)
+        self.launches_per_step = (1 if self.ngram else 0) + (2 if cfg.dense and cfg.temperature > 0 else 1) + 1 + \
+            (2 if self.ngram else 0)
+        self.g = g
+
+    def step(self, s, logits, ev=None):
+        """One pass of the hot path; ev = (start, end) events around spec_verify."""
+        sp, cfg = self.sp, self.cfg
+        if self.ngram:
+            lim = self.limits[s] if cfg.k_uniform else None
+            sp.ngram_draft(self.table, self.hist, self.lens, cfg.K, k_limit=lim, out_drafts=self.drafts,
+                           out_k=self.kbuf[s])
+            drafts, k, q = self.drafts, self.kbuf[s], None
+        else:
+            i = s % self.n_sets
+            drafts, k, q = self.dsets[i], self.kfull, self.q[i]
+        saved = None
+        if cfg.boost is not None:
+            # target-model stand-in: it agrees with a draft w.p. rho_b
+            saved = self._boost(logits, drafts, k)
+        self.params.step = s
+        if ev is not None:
+            ev[0].record()
+        sp.spec_verify(logits, drafts, q, k, self.hist, self.lens, self.params, self.kv, self.ema, self.out,
+                       self.acc, self.ws)
+        if ev is not None:
+            ev[1].record()
+        if saved is not None:
+            logits.view(-1)[saved[0]] = saved[1]
+        sp.spec_append(self.hist, self.lens, self.out, self.acc)
+        if self.ngram:
+            sp.ngram_update(self.table, self.hist, self.lens)
+
+    def _boost(self, logits, drafts, k):
+        B, K1, V = logits.shape
+        coin = torch.rand((B, K1 - 1), generator=self.g, device=logits.device) < self.bprob[:, None]
+        j = torch.arange(K1 - 1, device=logits.device)[None, :]
+        ok = coin & (j < k[:, None]) & (drafts >= 0)
+        flat = (torch.arange(B, device=logits.device)[:, None] * K1 + j) * V + drafts.clamp(min=0).long()
+        idx = flat[ok]
+        rowmax = logits[:, :K1 - 1].amax(dim=-1)
+        newv = (rowmax.float() + 6.0).to(logits.dtype)[ok]
+        old = logits.view(-1)[idx].clone()
+        logits.view(-1)[idx] = newv
+        return idx, old
+
+    def rows_read(self, steps):
+        cfg = self.cfg
+        if self.ngram:
+            return int((self.kbuf[:steps] + 1).sum().item())
+        return steps * cfg.B * (cfg.K + 1)
+
+    def verify_bytes(self, steps):
+        cfg = self.cfg
+        elem = 2 if cfg.dtype == "bf16" else 4
+        rows = self.rows_read(steps)
+        small = steps * cfg.B * (4 * (2 * cfg.K + 8))
+        return rows * cfg.V * elem + small
+
+
+def run_ours(args):
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import speculative_decoding_draft_ngram_gb300 as sp
+    sp.load()
+    total_steps = args.warmup + args.steps
+    e2e_steps = 0 if args.no_e2e else min(args.steps, 200)
+    path = Path(args.workload, 2 * total_steps + e2e_steps + 8, dev, seed_offset=rank)
+    cfg = path.cfg
+    stream = torch.cuda.current_stream(dev)
+
+    # ---- device-resident timed loop
+    for s in range(args.warmup):
+        path.step(s, path.logits[s % path.n_sets])
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = Clocks(dev) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    base = args.warmup
+    wall0 = time.time()
+    t_start.record(stream)
+    for i in range(args.steps):
+        s = base + i
+        path.step(s, path.logits[s % path.n_sets], evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    if ws > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop((wall0, wall1)) if clocks else None
+    ms = t_start.elapsed_time(t_end)
+    verify_ms = [a.elapsed_time(b) for a, b in evs]
+    # rows of the timed steps only
+    rows_read = path.rows_read(base + args.steps) - path.rows_read(base)
+    vbytes = path.verify_bytes(base + args.steps) - path.verify_bytes(base)
+    rows_nominal = args.steps * cfg.B * (cfg.K + 1)
+    ms_max = ms
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_max = float(t.item())
+    status = sp.get_status(clear=True)
+
+    # ---- end to end: host logits -> device, step, results -> host
+    e2e = None
+    if e2e_steps:
+        host = [x.cpu().pin_memory() for x in path.logits[:3]]
+        dbuf = torch.empty_like(path.logits[0])
+        out_h = torch.empty(path.out.shape, dtype=torch.int32).pin_memory()
+        acc_h = torch.empty(path.acc.shape, dtype=torch.int32).pin_memory()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        base2 = base + args.steps
+        for i in range(3):  # warm the copy path
+            dbuf.copy_(host[i % 3], non_blocking=True)
+        torch.cuda.synchronize()
+        if ws > 1:
+            torch.distributed.barrier()
+        e0.record(stream)
+        for i in range(e2e_steps):
+            dbuf.copy_(host[i % 3], non_blocking=True)
+            path.step(base2 + i, dbuf)
+            out_h.copy_(path.out, non_blocking=True)
+            acc_h.copy_(path.acc, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1)
+        if ws > 1:
+            t = torch.tensor([ems], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": ws * e2e_steps * cfg.B * (cfg.K + 1) / (ems / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": int(dbuf.numel() * dbuf.element_size()),
+               "d2h_bytes_per_step": int(out_h.numel() * 4 + acc_h.numel() * 4), "steps": e2e_steps,
+               "ms_per_step": ems / e2e_steps}
+        status |= sp.get_status(clear=True)
+
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return
+    peak, peak_src = measured_peaks()
+    v_avg_s = statistics.mean(verify_ms) / 1e3
+    per_launch_bytes = vbytes / args.steps
+    achieved = per_launch_bytes / v_avg_s / 1e9
+    traffic = ncu_traffic(args.workload)
+    line = {
+        "metric": METRIC,
+        "value": ws * rows_nominal / (ms_max / 1e3),
+        "unit": UNIT,
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_max / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{args.workload}: {DESCR[args.workload]}",
+            "B": cfg.B, "K": cfg.K, "V": cfg.V, "logits_dtype": cfg.dtype,
+            "l2": f"inputs larger than L2: {path.n_sets} rotating logit batches of {path.set_bytes / 1e6:.0f} MB",
+            "parallelism": f"dp{ws} (independent sequences per GPU)",
+        },
+        "rows_read_per_s": ws * rows_read / (ms_max / 1e3),
+        "verify_us": v_avg_s * 1e6,
+        "verify_logits_gbs": achieved,
+        "roofline": {
+            "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": traffic, "kernel": "verify_stream_kernel",
+            "peak_source": peak_src,
+            "algorithmic_bytes_per_launch": per_launch_bytes,
+        },
+        "gpu_launches": path.launches_per_step * args.steps,
+        "e2e": e2e,
+        "clocks": clk,
+        "device_status": sp.status_names(status),
+    }
+    if path.ngram:
+        line["ngram_build_ms"] = path.build_ms
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_sample)
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ---------------------------------------------------------------- oracle arm
+
+class OracleState:
+    """A bounded sample of the workload's sequences, stepped by the oracle."""
+
+    def __init__(self, name, nseq):
+        cfg = wl.get(name)
+        cfg = wl.get(name, B=nseq, steps=max(cfg.steps, 64))
+        self.cfg = cfg
+        hist, lens = wl.histories(cfg, "cpu")
+        self.hist = hist.numpy().astype(np.int64)
+        self.lens = lens.numpy().astype(np.int64)
+        self.g = wl._gen(cfg.data_seed + 1, "cpu")
+        self.ema = np.ones(cfg.B)
+        self.kv = self.lens.copy()
+
+    def step(self, s):
+        from oracle import ngram as on
+        from oracle import verify as ov
+        cfg = self.cfg
+        logits = wl.step_logits(cfg, self.g)
+        lim = wl.draft_limits(cfg, self.g).numpy()
+        if cfg.dense:
+            q, d = wl.dense_draft(cfg, logits, self.g)
+            q, d, k = q.numpy(), d.numpy().astype(np.int64), np.full(cfg.B, cfg.K)
+        else:
+            d, k = on.draft_batch(self.hist, self.lens, cfg.K, k_limit=lim)
+            q = None
+        if cfg.boost is not None:
+            logits = wl.apply_boost(cfg, logits, torch.from_numpy(d), torch.from_numpy(k),
+                                    wl.boost_probs(cfg), self.g)
+        p = ov.VerifyParams(temperature=cfg.temperature, softcap=cfg.softcap, rep_penalty=cfg.rep_penalty,
+                            rep_window=cfg.rep_window, gate_enabled=cfg.gate, seed=cfg.sampler_seed, step=s)
+        res = ov.spec_verify(logits.float().numpy(), d, q, k, self.hist, self.lens, p, self.kv,
+                             self.ema.astype(np.float32))
+        for b in range(cfg.B):
+            a = int(res["accept_len"][b])
+            self.hist[b, self.lens[b]:self.lens[b] + a + 1] = res["out_tokens"][b, :a + 1]
+            self.lens[b] += a + 1
+        self.kv = res["kv_len"]
+        self.ema = res["ema"]
+        return cfg.B * (cfg.K + 1)
+
+
+AUTO_SAMPLE = {"c2": 1, "c3": 4, "c4": 6, "c5": 8}
+
+
+def cpu_baseline(name, nseq=0, steps=6):
+    """Time the oracle, as it stands, on a bounded sample of the workload."""
+    nseq = nseq or AUTO_SAMPLE[name]
+    st = OracleState(name, nseq)
+    t0 = time.perf_counter()
+    rows = sum(st.step(s) for s in range(steps))
+    dt = time.perf_counter() - t0
+    return {"value": rows / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{steps} full steps (n-gram draft from the history, fp64 verify, append) of {nseq} "
+                      f"sequences of workload {name}; {rows} nominal rows in {dt:.1f} s; numpy, one thread"}
+
+
+def run_reference(args):
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    nseq = args.cpu_sample or 1   # one sequence per step keeps the run within minutes
+    st = OracleState(args.workload, nseq)
+    for s in range(args.warmup):
+        st.step(s)
+    t0 = time.perf_counter()
+    rows = 0
+    for s in range(args.steps):
+        rows += st.step(args.warmup + s)
+    dt = time.perf_counter() - t0
+    v = rows / dt
+    sample = (f"each step: {nseq} sequences of workload {args.workload} (n-gram draft, fp64 verify, append) "
+              f"on the host; {args.steps} timed steps")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {DESCR[args.workload]}", "sampled_sequences": nseq},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

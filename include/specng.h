@@ -1,0 +1,235 @@
+/*
+ * specng.h -- C ABI of the GB300 (sm_103a) library for the data-parallel hot
+ * path of speculative decoding with n-gram drafts and Leviathan/Chen
+ * verification.
+ *
+ * Sources (page title, section):
+ *  [AX]  "AX Engine: An LLM Inference Engine Built Exclusively for Apple
+ *        Silicon M4+", section "Core Technical Architecture & Methods":
+ *        bigram/trigram tables built at runtime; up to 4 draft tokens per
+ *        step; validation by the target forward; EMA acceptance gate
+ *        (tau = 0.1, threshold = 0.5) that disables speculation; O(1)
+ *        rollback by moving the sequence-length pointer.  Section "Supported
+ *        Model Families" (table): Gemma's logit soft cap.
+ *  [SW]  "SwiftLM: Apple Silicon native MLX Swift LLM inference server",
+ *        paragraph on algorithmic equivalence (Leviathan et al.): accept a
+ *        draft with probability P_target / P_draft and resample from the
+ *        corrected distribution on rejection; M1 Ultra benchmark paragraph:
+ *        --repeat-penalty 1.1, temperature 0.6; DFlash warning paragraph:
+ *        greedy (argmax) verification is the temperature-0 case.
+ *
+ * Conventions shared by every call
+ *  - Every array argument is caller-owned DEVICE memory unless stated
+ *    otherwise; the library never frees it.  int32 arrays are row-major.
+ *  - Every call is asynchronous and ordered on the given stream; none of
+ *    them synchronises except specng_get_status().
+ *  - Return value: SPECNG_OK (0), or a negative code for an error found on
+ *    the host before anything was enqueued (nothing ran in that case).
+ *  - Errors found on the device (full table, out-of-range token, non-finite
+ *    logits, history overflow, out-of-range k) never trap and never hang:
+ *    the kernel skips the offending item and sets a bit in a per-device
+ *    status word read with specng_get_status().
+ *  - No kernel waits for another block: cross-block merges use a
+ *    fence + atomic ticket, and the last block to arrive does the merge.
+ *    Every hash probe loop is bounded by the table capacity.
+ */
+#ifndef SPECNG_H
+#define SPECNG_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPECNG_API_VERSION 1
+
+/* Host-detected return codes. */
+#define SPECNG_OK      0
+#define SPECNG_EINVAL (-1)  /* null pointer, size or parameter out of range   */
+#define SPECNG_EALIGN (-2)  /* pointer alignment below what the call requires */
+#define SPECNG_ECUDA  (-3)  /* a CUDA runtime call failed (message: strerror) */
+#define SPECNG_ENOMEM (-4)  /* device allocation failed (table creation only) */
+#define SPECNG_ESMALL (-5)  /* workspace smaller than spec_verify_workspace_bytes */
+
+/* Logit element types accepted by spec_verify. */
+#define SPECNG_F32  0
+#define SPECNG_BF16 1
+
+/* Device status bits (specng_get_status). */
+#define SPECNG_DEV_TABLE_FULL     0x01u /* a hash probe met no free slot; insert skipped   */
+#define SPECNG_DEV_TOKEN_OOR      0x02u /* a token outside [0, V) was met and skipped      */
+#define SPECNG_DEV_NONFINITE      0x04u /* a logit row read at T > 0 had NaN or +Inf       */
+#define SPECNG_DEV_HIST_OVERFLOW  0x08u /* spec_append would pass the history capacity     */
+#define SPECNG_DEV_BAD_K          0x10u /* k[b] or accept_len[b] outside [0, K]; clamped   */
+#define SPECNG_DEV_COUNT_SAT      0x20u /* an n-gram count passed 2^22 - 1 and saturated   */
+#define SPECNG_DEV_HIST_SHRANK    0x40u /* lens[b] fell below what the table had indexed   */
+
+/* Limits checked on the host. */
+#define SPECNG_MAX_K          16        /* drafts per sequence per call            */
+#define SPECNG_MAX_REP_WINDOW 256       /* repetition-penalty window (tokens)      */
+#define SPECNG_NGRAM_MAX_B    512       /* sequences per n-gram table              */
+#define SPECNG_NGRAM_MAX_V    262144    /* vocabulary of an n-gram table (2^18)    */
+#define SPECNG_NGRAM_MAX_POS  16777216  /* positions per sequence in a table (2^24) */
+
+/* ------------------------------------------------------------------------
+ * N-gram table  [AX]: "builds bigram/trigram tables at runtime, predicts up
+ * to 4 draft tokens per step".
+ *
+ * One opaque object holds four open-addressed hash tables in device memory
+ * (trigram pairs, bigram pairs, trigram contexts, bigram contexts) for B
+ * sequences with token ids in [0, V).  A pair entry counts how often token
+ * c followed a context and the latest position where it did; a context
+ * entry holds its best continuation: the largest count, equal counts going
+ * to the most recent occurrence.  Insertion is order-independent, so the
+ * table is a pure function of the indexed histories (it can be rebuilt
+ * from them after a restart).
+ * --------------------------------------------------------------------- */
+typedef struct specng_ngram specng_ngram;
+
+/* Allocate and clear a table.  max_positions: upper bound on the number of
+ * history positions that will ever be indexed, summed over all B sequences
+ * (each table gets 2 * max_positions slots rounded up to a power of two, 16
+ * bytes each).  B in [1, 512]; V in [1, 2^18].  The object owns its device
+ * memory (allocated with cudaMalloc on the current device) until
+ * specng_ngram_destroy.  Clearing is enqueued on stream s.
+ * Errors: EINVAL, ENOMEM, ECUDA. */
+int specng_ngram_create(specng_ngram** table, int B, int V, int64_t max_positions,
+                        cudaStream_t s);
+
+/* Free the table (synchronises the device first).  NULL is accepted. */
+int specng_ngram_destroy(specng_ngram* table);
+
+/* Remove every entry and mark every sequence as not indexed (stream s). */
+int specng_ngram_reset(specng_ngram* table, cudaStream_t s);
+
+/* Slots per hash table (a power of two). */
+int specng_ngram_capacity(const specng_ngram* table, int64_t* slots);
+
+/* Index the history positions added since the previous call.
+ * history: int32 [B, hist_stride] (token i of sequence b at b*hist_stride+i);
+ * lens: int32 [B], the number of valid tokens per sequence.  For every new
+ * position i in [indexed_b, lens_b) (indexed_b = lens_b of the previous
+ * call, 0 after create/reset) the bigram pair (h[i-1] -> h[i]) and, when
+ * i >= 2, the trigram pair ((h[i-2], h[i-1]) -> h[i]) are counted, then the
+ * contexts' best continuations are refreshed.  Two kernel launches.
+ * Device errors: TABLE_FULL, TOKEN_OOR, COUNT_SAT, HIST_SHRANK. */
+int ngram_update(specng_ngram* table, const int32_t* history, int64_t hist_stride,
+                 const int32_t* lens, cudaStream_t s);
+
+/* Draft up to max_k tokens per sequence by chained lookups: the context is
+ * the last two tokens of history ++ drafts so far; the trigram context is
+ * tried first, then the bigram context; drafting stops at the first miss.
+ * k_limit: optional int32 [B] per-sequence cap (NULL: max_k for all).
+ * out_drafts: int32 [B, max_k], padded with -1; out_k: int32 [B], the count.
+ * The table is read only.  max_k in [0, 16].  One kernel launch. */
+int ngram_draft(const specng_ngram* table, const int32_t* history, int64_t hist_stride,
+                const int32_t* lens, int max_k, const int32_t* k_limit,
+                int32_t* out_drafts, int32_t* out_k, cudaStream_t s);
+
+/* ------------------------------------------------------------------------
+ * Verification  [SW] Leviathan/Chen + [AX] EMA gate and rollback.
+ * --------------------------------------------------------------------- */
+typedef struct {
+    float    temperature;   /* T; 0 selects greedy verification (argmax)          */
+    float    softcap;       /* c: x -> c * tanh(x / c); <= 0 disables             */
+    float    rep_penalty;   /* r > 0: x > 0 -> x / r, else x * r; 1 disables       */
+    int32_t  rep_window;    /* W in [0, 256]: last W tokens of history ++ drafts   */
+    float    ema_tau;       /* EMA rate (0.1 on the page)                          */
+    float    ema_thresh;    /* gate threshold (0.5 on the page)                    */
+    int32_t  gate_enabled;  /* 0: always verify k[b] drafts                        */
+    uint32_t pad_;          /* must be 0                                           */
+    uint64_t seed;          /* Philox key                                          */
+    uint64_t step;          /* decode step (low 32 bits enter the Philox counter)  */
+} specng_verify_params;
+
+/* Bytes of device workspace spec_verify needs for (B, K, V). */
+size_t spec_verify_workspace_bytes(int B, int K, int V);
+
+/* Zero a workspace (stream-ordered).  A workspace must be zero-filled once
+ * before its first spec_verify call; each call leaves it zero-filled. */
+int spec_verify_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t s);
+
+/* One verify call for B sequences with up to K drafts each.
+ *
+ * logits       [B, K+1, V] of logits_dtype (SPECNG_BF16 or SPECNG_F32);
+ *              row j of sequence b is the target's next-token logits after
+ *              history ++ d_1..d_j.  Rows j > k_eff(b) are never read.
+ * drafts       int32 [B, K]: d_1..d_K (may be NULL when K = 0).
+ * draft_probs  fp32 [B, K, V] draft distributions q_j, or NULL for
+ *              point-mass drafts (q = one-hot(d), the n-gram case).
+ * k            int32 [B]: drafts to verify per sequence, in [0, K].
+ * history, hist_stride, lens: int32, as for ngram_update; read only for the
+ *              repetition-penalty window (may be NULL when the penalty is off).
+ * params       host pointer; see specng_verify_params.
+ * kv_len       int32 [B], in/out: on entry the KV length after the verify
+ *              forward (committed + k[b] + 1); on exit kv_len - k[b] + a.
+ * ema          fp32 [B], in/out: acceptance EMA.  Gate (when enabled):
+ *              k_eff = ema >= thresh ? k : 0, read before the update; if
+ *              k_eff > 0, ema <- (1 - tau) * ema + tau * a / k_eff.
+ * out_tokens   int32 [B, K+1]: d_1..d_a, then the residual or bonus sample,
+ *              then -1.
+ * out_accept_len int32 [B]: a.
+ * workspace    device scratch of at least spec_verify_workspace_bytes(B, K, V)
+ *              bytes, 256-byte aligned, zero-filled before its first use
+ *              (spec_verify_workspace_init or any zero fill).  Every call
+ *              leaves it zero-filled again, so later calls of any shape that
+ *              fits may reuse it; one workspace per call in flight.
+ *
+ * Per row: x <- c tanh(x/c) (soft cap), repetition penalty over the window
+ * (each distinct id once), temperature; online max and sum of exponentials.
+ * Accept test for draft i: u_i * q(d_i) <= p(d_i), u_i from Philox4x32-10
+ * keyed by (seed; draft index, step, sequence).  Sample at row a (residual
+ * max(0, p_a - q_a) on a rejection, p_a when all k_eff drafts are accepted)
+ * by Gumbel-max with Philox noise keyed by (seed; vocab id, row, step,
+ * sequence).  T = 0: accept iff d_i is its row's argmax (lowest id on
+ * ties); the emitted token is the argmax of row a.
+ * Launches: one kernel (point-mass drafts or T = 0), two with dense q.
+ * Requirements: logits 16-byte aligned for the vectorised path (any
+ * alignment works, slower); B in [1, 2^20]; K in [0, 16]; V in [1, 2^30].
+ * Errors: EINVAL, ESMALL, ECUDA.  Device: NONFINITE, TOKEN_OOR, BAD_K. */
+int spec_verify(const void* logits, int logits_dtype, int B, int K, int V,
+                const int32_t* drafts, const float* draft_probs, const int32_t* k,
+                const int32_t* history, int64_t hist_stride, const int32_t* lens,
+                const specng_verify_params* params,
+                int32_t* kv_len, float* ema,
+                int32_t* out_tokens, int32_t* out_accept_len,
+                void* workspace, size_t workspace_bytes, cudaStream_t s);
+
+/* Append the emitted tokens: history[b, lens_b + t] = out_tokens[b, t] for
+ * t <= out_accept_len[b], then lens_b += out_accept_len[b] + 1.  A sequence
+ * whose history would pass hist_cap tokens is left unchanged (HIST_OVERFLOW).
+ * In place, one kernel launch. */
+int spec_append(int32_t* history, int64_t hist_stride, int32_t* lens, int64_t hist_cap,
+                const int32_t* out_tokens, const int32_t* out_accept_len, int B, int K,
+                cudaStream_t s);
+
+/* ------------------------------------------------------------------------
+ * Status and diagnostics
+ * --------------------------------------------------------------------- */
+
+/* Copy the current device's status bits to *bits (host pointer);
+ * if clear != 0, reset them to 0.  Synchronises the device. */
+int specng_get_status(uint32_t* bits, int clear);
+
+/* Static description of a return code. */
+const char* specng_strerror(int code);
+
+/* Description of the last host-detected error of the calling thread (names
+ * the call and, for ECUDA, the CUDA error).  Valid until the next error. */
+const char* specng_last_error(void);
+
+/* Philox4x32-10 (Salmon et al., SC'11) on n counters: out[4i..4i+3] =
+ * philox(ctr[4i..4i+3]; key = (seed mod 2^32, seed >> 32)).  The same
+ * device routine keys the accept and Gumbel noise of spec_verify; exported
+ * so that it can be compared bit for bit with an independent
+ * implementation.  ctr, out: uint32 device arrays of 4n words. */
+int specng_philox4x32_10(const uint32_t* ctr, uint64_t seed, uint32_t* out, int64_t n,
+                         cudaStream_t s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPECNG_H */

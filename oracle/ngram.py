@@ -56,6 +56,21 @@ def continuation_stats(tokens: Sequence[int], length: int) -> Tuple[Stats, Stats
     return tri, bi
 
 
+def extend_stats(stats: Tuple[Stats, Stats], tokens: Sequence[int], start: int, length: int):
+    """Add positions [max(start, 1), length) to (tri, bi); equal to a rebuild."""
+    tri, bi = stats
+    for i in range(max(start, 1), length):
+        c = int(tokens[i])
+        e = bi.setdefault(int(tokens[i - 1]), {}).setdefault(c, [0, -1])
+        e[0] += 1
+        e[1] = i
+        if i >= 2:
+            e = tri.setdefault((int(tokens[i - 2]), int(tokens[i - 1])), {}).setdefault(c, [0, -1])
+            e[0] += 1
+            e[1] = i
+    return stats
+
+
 def best_continuation(conts: Dict[int, List[int]]):
     """Most frequent continuation, latest occurrence breaking ties (None if empty)."""
     best = None
@@ -87,15 +102,18 @@ def draft(tokens: Sequence[int], length: int, max_k: int, stats=None) -> List[in
     return out
 
 
-def draft_batch(history, lens, max_k: int, k_limit=None):
-    """Drafts for every sequence: (drafts [B, max_k] padded with -1, counts [B])."""
+def draft_batch(history, lens, max_k: int, k_limit=None, stats=None):
+    """Drafts for every sequence: (drafts [B, max_k] padded with -1, counts [B]).
+
+    ``stats`` optionally holds each sequence's statistics of its whole
+    history (as kept up to date by ``extend_stats``)."""
     import numpy as np
     B = len(lens)
     drafts = np.full((B, max(max_k, 0)), -1, dtype=np.int64)
     counts = np.zeros(B, dtype=np.int64)
     for b in range(B):
-        kb = max_k if k_limit is None else min(max_k, int(k_limit[b]))
-        d = draft(history[b], int(lens[b]), kb)
+        kb = max_k if k_limit is None else max(0, min(max_k, int(k_limit[b])))
+        d = draft(history[b], int(lens[b]), kb, None if stats is None else stats[b])
         drafts[b, :len(d)] = d
         counts[b] = len(d)
     return drafts, counts

@@ -1,0 +1,25 @@
+"""GB300 (sm_103a) library for the hot path of speculative decoding with
+n-gram drafts: device bigram/trigram tables (``ngram_update``,
+``ngram_draft``), a single-pass Leviathan/Chen verifier with Gumbel-max
+residual / bonus sampling, kv_len rollback and an EMA gate
+(``spec_verify``), and the history append (``spec_append``).
+
+The compute runs in hand-written CUDA kernels behind the C ABI of
+``include/specng.h`` (``libspecng.so``); this package is the thin binding.
+"""
+from .capi import (  # noqa: F401
+    NgramTable,
+    SpecngError,
+    VerifyParams,
+    get_status,
+    lib_path,
+    load,
+    ngram_draft,
+    ngram_update,
+    philox4x32_10,
+    spec_append,
+    spec_verify,
+    spec_verify_workspace,
+    spec_verify_workspace_bytes,
+    status_names,
+)

@@ -1,0 +1,330 @@
+// C ABI of libspecng: argument checks, workspace layout, the device status
+// word and the launches.  Declarations and documentation: include/specng.h.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "ngram.cuh"
+#include "verify.cuh"
+
+namespace specng {
+
+__device__ unsigned g_status_word;
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+int fail(int code, const char* what) {
+    std::snprintf(g_last_error, sizeof(g_last_error), "%s", what);
+    return code;
+}
+
+int fail_cuda(cudaError_t e, const char* where) {
+    std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s", where, cudaGetErrorString(e));
+    return SPECNG_ECUDA;
+}
+
+// Device address of the status word, looked up once per device.
+unsigned* status_ptr() {
+    static std::mutex mu;
+    static unsigned* ptrs[128] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (ptrs[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) == cudaSuccess) ptrs[dev] = static_cast<unsigned*>(p);
+    }
+    return ptrs[dev];
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct WsLayout {
+    size_t part, rowres, seqres, part2, tickets, total;
+    size_t row_ticket, seq_ticket, seq_ticket2;
+};
+
+// The f32 chunk is the smaller one, so its chunk count bounds both dtypes.
+int max_chunks(int V) { return (V + chunk_elems<false>() - 1) / chunk_elems<false>(); }
+
+WsLayout ws_layout(int B, int K, int V) {
+    const size_t rows = static_cast<size_t>(B) * (K + 1);
+    const size_t nch = static_cast<size_t>(max_chunks(V));
+    WsLayout L{};
+    size_t off = 0;
+    L.part = off;    off = align256(off + rows * nch * sizeof(Partial));
+    L.rowres = off;  off = align256(off + rows * sizeof(RowRes));
+    L.seqres = off;  off = align256(off + static_cast<size_t>(B) * sizeof(SeqRes));
+    L.part2 = off;   off = align256(off + static_cast<size_t>(B) * nch * sizeof(Partial));
+    L.tickets = off;
+    L.row_ticket = off;   off += rows * sizeof(unsigned);
+    L.seq_ticket = off;   off += static_cast<size_t>(B) * sizeof(unsigned);
+    L.seq_ticket2 = off;  off += static_cast<size_t>(B) * sizeof(unsigned);
+    L.total = align256(off);
+    return L;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace specng
+
+using namespace specng;
+
+struct specng_ngram {
+    NgramDev dev;
+    void* mem;
+    int parity;
+    int grid;
+};
+
+extern "C" {
+
+const char* specng_last_error(void) { return g_last_error; }
+
+const char* specng_strerror(int code) {
+    switch (code) {
+        case SPECNG_OK: return "ok";
+        case SPECNG_EINVAL: return "invalid argument (null pointer, size or parameter out of range)";
+        case SPECNG_EALIGN: return "pointer alignment below what the call requires";
+        case SPECNG_ECUDA: return "CUDA runtime error";
+        case SPECNG_ENOMEM: return "device allocation failed";
+        case SPECNG_ESMALL: return "workspace smaller than spec_verify_workspace_bytes";
+        default: return "unknown error code";
+    }
+}
+
+int specng_get_status(uint32_t* bits, int clear) {
+    if (bits == nullptr) return fail(SPECNG_EINVAL, "specng_get_status: bits is NULL");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail_cuda(e, "specng_get_status");
+    unsigned v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_status_word, sizeof(v));
+    if (e != cudaSuccess) return fail_cuda(e, "specng_get_status");
+    *bits = v;
+    if (clear) {
+        const unsigned z = 0;
+        e = cudaMemcpyToSymbol(g_status_word, &z, sizeof(z));
+        if (e != cudaSuccess) return fail_cuda(e, "specng_get_status");
+    }
+    return SPECNG_OK;
+}
+
+// ------------------------------------------------------------------ n-gram
+
+int specng_ngram_create(specng_ngram** table, int B, int V, int64_t max_positions, cudaStream_t s) {
+    if (table == nullptr) return fail(SPECNG_EINVAL, "specng_ngram_create: table is NULL");
+    *table = nullptr;
+    if (B < 1 || B > SPECNG_NGRAM_MAX_B) return fail(SPECNG_EINVAL, "specng_ngram_create: B outside [1, 512]");
+    if (V < 1 || V > SPECNG_NGRAM_MAX_V) return fail(SPECNG_EINVAL, "specng_ngram_create: V outside [1, 2^18]");
+    if (max_positions < 1 || max_positions > (int64_t(1) << 33))
+        return fail(SPECNG_EINVAL, "specng_ngram_create: max_positions outside [1, 2^33]");
+    uint64_t slots = 1024;
+    while (slots < 2ull * static_cast<uint64_t>(max_positions)) slots <<= 1;
+    const size_t table_bytes = slots * sizeof(ulonglong2);
+    const size_t idx_bytes = align256(2 * static_cast<size_t>(B) * sizeof(int32_t));
+    void* mem = nullptr;
+    cudaError_t e = cudaMalloc(&mem, 4 * table_bytes + idx_bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SPECNG_ENOMEM, "specng_ngram_create: cudaMalloc failed");
+    }
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    specng_ngram* t = new specng_ngram();
+    char* base = static_cast<char*>(mem);
+    t->mem = mem;
+    t->parity = 0;
+    t->grid = 2 * (sms > 0 ? sms : 1);
+    t->dev.tri_pair = reinterpret_cast<ulonglong2*>(base);
+    t->dev.bi_pair = reinterpret_cast<ulonglong2*>(base + table_bytes);
+    t->dev.tri_ctx = reinterpret_cast<ulonglong2*>(base + 2 * table_bytes);
+    t->dev.bi_ctx = reinterpret_cast<ulonglong2*>(base + 3 * table_bytes);
+    t->dev.mask = slots - 1;
+    t->dev.indexed[0] = reinterpret_cast<int32_t*>(base + 4 * table_bytes);
+    t->dev.indexed[1] = t->dev.indexed[0] + B;
+    t->dev.B = B;
+    t->dev.V = V;
+    t->dev.status = status_ptr();
+    e = launch_ngram_clear(t->dev, s);
+    if (e != cudaSuccess) {
+        cudaFree(mem);
+        delete t;
+        return fail_cuda(e, "specng_ngram_create");
+    }
+    *table = t;
+    return SPECNG_OK;
+}
+
+int specng_ngram_destroy(specng_ngram* table) {
+    if (table == nullptr) return SPECNG_OK;
+    cudaError_t e = cudaDeviceSynchronize();
+    cudaError_t f = cudaFree(table->mem);
+    delete table;
+    if (e != cudaSuccess) return fail_cuda(e, "specng_ngram_destroy");
+    if (f != cudaSuccess) return fail_cuda(f, "specng_ngram_destroy");
+    return SPECNG_OK;
+}
+
+int specng_ngram_reset(specng_ngram* table, cudaStream_t s) {
+    if (table == nullptr) return fail(SPECNG_EINVAL, "specng_ngram_reset: table is NULL");
+    const cudaError_t e = launch_ngram_clear(table->dev, s);
+    if (e != cudaSuccess) return fail_cuda(e, "specng_ngram_reset");
+    table->parity = 0;
+    return SPECNG_OK;
+}
+
+int specng_ngram_capacity(const specng_ngram* table, int64_t* slots) {
+    if (table == nullptr || slots == nullptr) return fail(SPECNG_EINVAL, "specng_ngram_capacity: NULL argument");
+    *slots = static_cast<int64_t>(table->dev.mask + 1);
+    return SPECNG_OK;
+}
+
+int ngram_update(specng_ngram* table, const int32_t* history, int64_t hist_stride, const int32_t* lens,
+                 cudaStream_t s) {
+    if (table == nullptr || history == nullptr || lens == nullptr)
+        return fail(SPECNG_EINVAL, "ngram_update: NULL argument");
+    if (hist_stride < 1 || hist_stride > SPECNG_NGRAM_MAX_POS)
+        return fail(SPECNG_EINVAL, "ngram_update: hist_stride outside [1, 2^24]");
+    const cudaError_t e = launch_ngram_update(table->dev, table->parity, history, hist_stride, lens, table->grid, s);
+    if (e != cudaSuccess) return fail_cuda(e, "ngram_update");
+    table->parity ^= 1;
+    return SPECNG_OK;
+}
+
+int ngram_draft(const specng_ngram* table, const int32_t* history, int64_t hist_stride, const int32_t* lens,
+                int max_k, const int32_t* k_limit, int32_t* out_drafts, int32_t* out_k, cudaStream_t s) {
+    if (table == nullptr || history == nullptr || lens == nullptr || out_k == nullptr)
+        return fail(SPECNG_EINVAL, "ngram_draft: NULL argument");
+    if (max_k < 0 || max_k > SPECNG_MAX_K) return fail(SPECNG_EINVAL, "ngram_draft: max_k outside [0, 16]");
+    if (max_k > 0 && out_drafts == nullptr) return fail(SPECNG_EINVAL, "ngram_draft: out_drafts is NULL");
+    if (hist_stride < 1 || hist_stride > SPECNG_NGRAM_MAX_POS)
+        return fail(SPECNG_EINVAL, "ngram_draft: hist_stride outside [1, 2^24]");
+    const cudaError_t e = launch_ngram_draft(table->dev, history, hist_stride, lens, max_k, k_limit, out_drafts,
+                                             out_k, s);
+    if (e != cudaSuccess) return fail_cuda(e, "ngram_draft");
+    return SPECNG_OK;
+}
+
+// ------------------------------------------------------------------ verify
+
+size_t spec_verify_workspace_bytes(int B, int K, int V) {
+    if (B < 1 || K < 0 || K > SPECNG_MAX_K || V < 1) return 0;
+    return ws_layout(B, K, V).total;
+}
+
+int spec_verify_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t s) {
+    if (workspace == nullptr) return fail(SPECNG_EINVAL, "spec_verify_workspace_init: workspace is NULL");
+    const cudaError_t e = cudaMemsetAsync(workspace, 0, workspace_bytes, s);
+    if (e != cudaSuccess) return fail_cuda(e, "spec_verify_workspace_init");
+    return SPECNG_OK;
+}
+
+int spec_verify(const void* logits, int logits_dtype, int B, int K, int V, const int32_t* drafts,
+                const float* draft_probs, const int32_t* k, const int32_t* history, int64_t hist_stride,
+                const int32_t* lens, const specng_verify_params* params, int32_t* kv_len, float* ema,
+                int32_t* out_tokens, int32_t* out_accept_len, void* workspace, size_t workspace_bytes,
+                cudaStream_t s) {
+    if (logits == nullptr || k == nullptr || params == nullptr || kv_len == nullptr || ema == nullptr ||
+        out_tokens == nullptr || out_accept_len == nullptr || workspace == nullptr)
+        return fail(SPECNG_EINVAL, "spec_verify: NULL argument");
+    if (logits_dtype != SPECNG_BF16 && logits_dtype != SPECNG_F32)
+        return fail(SPECNG_EINVAL, "spec_verify: logits_dtype must be SPECNG_BF16 or SPECNG_F32");
+    if (B < 1 || B > (1 << 20)) return fail(SPECNG_EINVAL, "spec_verify: B outside [1, 2^20]");
+    if (K < 0 || K > SPECNG_MAX_K) return fail(SPECNG_EINVAL, "spec_verify: K outside [0, 16]");
+    if (V < 1 || V > (1 << 30)) return fail(SPECNG_EINVAL, "spec_verify: V outside [1, 2^30]");
+    if (K > 0 && drafts == nullptr) return fail(SPECNG_EINVAL, "spec_verify: drafts is NULL with K > 0");
+    const specng_verify_params& p = *params;
+    if (!(p.temperature >= 0.0f) || !std::isfinite(p.temperature))
+        return fail(SPECNG_EINVAL, "spec_verify: temperature must be finite and >= 0");
+    if (!std::isfinite(p.softcap)) return fail(SPECNG_EINVAL, "spec_verify: softcap must be finite");
+    if (!(p.rep_penalty > 0.0f) || !std::isfinite(p.rep_penalty))
+        return fail(SPECNG_EINVAL, "spec_verify: rep_penalty must be finite and > 0");
+    if (p.rep_window < 0 || p.rep_window > SPECNG_MAX_REP_WINDOW)
+        return fail(SPECNG_EINVAL, "spec_verify: rep_window outside [0, 256]");
+    if (p.gate_enabled && (!std::isfinite(p.ema_tau) || !std::isfinite(p.ema_thresh)))
+        return fail(SPECNG_EINVAL, "spec_verify: ema_tau and ema_thresh must be finite");
+    const bool penalty = p.rep_penalty != 1.0f && p.rep_window > 0;
+    if (penalty && (history == nullptr || lens == nullptr || hist_stride < 1))
+        return fail(SPECNG_EINVAL, "spec_verify: history, lens and hist_stride are needed for the penalty");
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(SPECNG_EALIGN, "spec_verify: workspace must be 256-byte aligned");
+    const WsLayout L = ws_layout(B, K, V);
+    if (workspace_bytes < L.total) return fail(SPECNG_ESMALL, "spec_verify: workspace too small");
+    const bool bf16 = logits_dtype == SPECNG_BF16;
+    const int chunk = bf16 ? chunk_elems<true>() : chunk_elems<false>();
+    const int nchunk = (V + chunk - 1) / chunk;
+    if (static_cast<int64_t>(B) * (K + 1) * nchunk > 0x7FFFFFFFLL)
+        return fail(SPECNG_EINVAL, "spec_verify: B * (K + 1) * chunks exceeds the grid limit");
+
+    const bool greedy = p.temperature == 0.0f;
+    const bool softcap = p.softcap > 0.0f;
+    const bool dense = draft_probs != nullptr;
+    const int epv = bf16 ? 8 : 4;
+
+    VerifyDev P{};
+    P.logits = logits;
+    P.B = B; P.K = K; P.V = V; P.nchunk = nchunk;
+    P.drafts = drafts; P.q = draft_probs; P.k = k;
+    P.hist = history; P.hist_stride = hist_stride; P.lens = lens;
+    P.T = p.temperature;
+    P.invT = greedy ? 0.0f : 1.0f / p.temperature;
+    P.sc = greedy ? 0.0f : kLog2e / p.temperature;
+    P.Td = static_cast<double>(p.temperature);
+    P.cap = softcap ? p.softcap : 0.0f;
+    P.invcap = softcap ? 1.0f / p.softcap : 0.0f;
+    P.rep = p.rep_penalty;
+    P.invrep = 1.0f / p.rep_penalty;
+    P.W = penalty ? p.rep_window : 0;
+    P.tau = p.ema_tau;
+    P.thresh = p.ema_thresh;
+    P.gate = p.gate_enabled ? 1 : 0;
+    P.nk.k0 = static_cast<uint32_t>(p.seed);
+    P.nk.k1 = static_cast<uint32_t>(p.seed >> 32);
+    P.nk.step = static_cast<uint32_t>(p.step);
+    P.nk.seq = 0;
+    P.aligned = aligned16(logits) && (V % epv == 0) && (!dense || (aligned16(draft_probs) && V % 4 == 0));
+    P.kv_len = kv_len; P.ema = ema; P.out_tokens = out_tokens; P.out_accept = out_accept_len;
+    char* ws = static_cast<char*>(workspace);
+    P.part = reinterpret_cast<Partial*>(ws + L.part);
+    P.rowres = reinterpret_cast<RowRes*>(ws + L.rowres);
+    P.seqres = reinterpret_cast<SeqRes*>(ws + L.seqres);
+    P.part2 = reinterpret_cast<Partial*>(ws + L.part2);
+    P.row_ticket = reinterpret_cast<unsigned*>(ws + L.row_ticket);
+    P.seq_ticket = reinterpret_cast<unsigned*>(ws + L.seq_ticket);
+    P.seq_ticket2 = reinterpret_cast<unsigned*>(ws + L.seq_ticket2);
+    P.status = status_ptr();
+
+    const cudaError_t e = bf16 ? launch_verify_dtype<true>(P, greedy, softcap, penalty, dense, s)
+                               : launch_verify_dtype<false>(P, greedy, softcap, penalty, dense, s);
+    if (e != cudaSuccess) return fail_cuda(e, "spec_verify");
+    return SPECNG_OK;
+}
+
+int spec_append(int32_t* history, int64_t hist_stride, int32_t* lens, int64_t hist_cap, const int32_t* out_tokens,
+                const int32_t* out_accept_len, int B, int K, cudaStream_t s) {
+    if (history == nullptr || lens == nullptr || out_tokens == nullptr || out_accept_len == nullptr)
+        return fail(SPECNG_EINVAL, "spec_append: NULL argument");
+    if (B < 1 || K < 0 || K > SPECNG_MAX_K) return fail(SPECNG_EINVAL, "spec_append: B or K out of range");
+    if (hist_stride < 1 || hist_cap < 0 || hist_cap > hist_stride)
+        return fail(SPECNG_EINVAL, "spec_append: need 0 <= hist_cap <= hist_stride");
+    const cudaError_t e = launch_spec_append(history, hist_stride, lens, hist_cap, out_tokens, out_accept_len, B, K,
+                                             status_ptr(), s);
+    if (e != cudaSuccess) return fail_cuda(e, "spec_append");
+    return SPECNG_OK;
+}
+
+int specng_philox4x32_10(const uint32_t* ctr, uint64_t seed, uint32_t* out, int64_t n, cudaStream_t s) {
+    if (ctr == nullptr || out == nullptr || n < 0) return fail(SPECNG_EINVAL, "specng_philox4x32_10: bad argument");
+    if (!aligned16(ctr) || !aligned16(out)) return fail(SPECNG_EALIGN, "specng_philox4x32_10: 16-byte alignment");
+    if (n == 0) return SPECNG_OK;
+    const cudaError_t e = launch_philox(ctr, seed, out, n, s);
+    if (e != cudaSuccess) return fail_cuda(e, "specng_philox4x32_10");
+    return SPECNG_OK;
+}
+
+}  // extern "C"

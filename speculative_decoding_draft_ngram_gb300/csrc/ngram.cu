@@ -1,0 +1,261 @@
+// N-gram table update / draft kernels, the history append and the Philox
+// diagnostic kernel (sm_103a).
+#include "ngram.cuh"
+
+namespace specng {
+
+namespace {
+
+constexpr int kNgThreads = 256;
+
+// Exclusive prefix over the per-sequence counts of new positions, shared by
+// both update phases.  Position i of sequence b is new when
+// max(indexed_b, 1) <= i < min(lens_b, stride): position 0 has no context.
+struct NewRange {
+    long long* pref;  // [B + 1]
+    int* lo;          // [B]
+};
+
+__device__ void build_new_range(const NgramDev& T, int parity, const int32_t* lens, int64_t stride,
+                                long long* s_pref, int* s_lo, int* s_hi, bool flag) {
+    __shared__ long long s_warp[kNgThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // each thread owns up to 2 consecutive sequences (B <= 512)
+    long long n[2] = {0, 0};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int b = 2 * tid + h;
+        if (b < T.B) {
+            const int idx = T.indexed[parity][b];
+            int L = lens[b];
+            if (L < 0) L = 0;
+            if (static_cast<int64_t>(L) > stride) L = static_cast<int>(stride);
+            if (flag && L < idx) raise_status(T.status, SPECNG_DEV_HIST_SHRANK);
+            const int lo = idx > 1 ? idx : 1;
+            s_lo[b] = lo;
+            s_hi[b] = L;
+            n[h] = L > lo ? L - lo : 0;
+        }
+    }
+    long long v = n[0] + n[1];
+    long long incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const long long o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    long long base = 0;
+    for (int w = 0; w < warp; ++w) base += s_warp[w];
+    const long long excl = base + incl - v;
+    if (2 * tid < T.B) s_pref[2 * tid] = excl;
+    if (2 * tid + 1 < T.B) s_pref[2 * tid + 1] = excl + n[0];
+    if (tid == kNgThreads - 1) s_pref[T.B] = base + incl;
+    __syncthreads();
+}
+
+__device__ __forceinline__ int seq_of(const long long* s_pref, int B, long long f) {
+    int lo = 0, hi = B;  // largest b with s_pref[b] <= f
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_pref[mid] <= f) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ bool tok_ok(int t, int V) { return t >= 0 && t < V; }
+
+__global__ void __launch_bounds__(kNgThreads) ngram_count_kernel(const NgramDev T, int parity, const int32_t* hist,
+                                                                 int64_t stride, const int32_t* lens) {
+    __shared__ long long s_pref[SPECNG_NGRAM_MAX_B + 1];
+    __shared__ int s_lo[SPECNG_NGRAM_MAX_B], s_hi[SPECNG_NGRAM_MAX_B];
+    build_new_range(T, parity, lens, stride, s_pref, s_lo, s_hi, blockIdx.x == 0);
+    const long long total = s_pref[T.B];
+    for (long long f = static_cast<long long>(blockIdx.x) * kNgThreads + threadIdx.x; f < total;
+         f += static_cast<long long>(gridDim.x) * kNgThreads) {
+        const int b = seq_of(s_pref, T.B, f);
+        const int i = s_lo[b] + static_cast<int>(f - s_pref[b]);
+        const int32_t* h = hist + static_cast<size_t>(b) * stride;
+        const int c = h[i], t1 = h[i - 1];
+        if (!tok_ok(c, T.V) || !tok_ok(t1, T.V)) { raise_status(T.status, SPECNG_DEV_TOKEN_OOR); continue; }
+        int64_t slot = find_or_insert(T.bi_pair, T.mask, key_bi_pair(b, t1, c));
+        if (slot < 0) {
+            raise_status(T.status, SPECNG_DEV_TABLE_FULL);
+        } else {
+            unsigned* v = reinterpret_cast<unsigned*>(&T.bi_pair[slot].y);
+            atomicAdd(v, 1u);
+            atomicMax(v + 1, static_cast<unsigned>(i));
+        }
+        if (i >= 2) {
+            const int t2 = h[i - 2];
+            if (!tok_ok(t2, T.V)) { raise_status(T.status, SPECNG_DEV_TOKEN_OOR); continue; }
+            slot = find_or_insert(T.tri_pair, T.mask, key_tri_pair(b, t2, t1, c));
+            if (slot < 0) {
+                raise_status(T.status, SPECNG_DEV_TABLE_FULL);
+            } else {
+                unsigned* v = reinterpret_cast<unsigned*>(&T.tri_pair[slot].y);
+                atomicAdd(v, 1u);
+                atomicMax(v + 1, static_cast<unsigned>(i));
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void push_best(const NgramDev& T, const ulonglong2* pairs, ulonglong2* ctxs,
+                                          uint64_t pair_key, uint64_t ctx_key, int c) {
+    uint64_t pv;
+    if (!find_value(pairs, T.mask, pair_key, &pv)) return;  // insert failed in the count phase
+    uint64_t count = pv & 0xFFFFFFFFull;
+    const uint64_t last = pv >> 32;
+    if (count > kCountMax) { raise_status(T.status, SPECNG_DEV_COUNT_SAT); count = kCountMax; }
+    const int64_t slot = find_or_insert(ctxs, T.mask, ctx_key);
+    if (slot < 0) { raise_status(T.status, SPECNG_DEV_TABLE_FULL); return; }
+    atomicMax(&ctxs[slot].y, static_cast<unsigned long long>(pack_best(count, last, static_cast<uint64_t>(c))));
+}
+
+__global__ void __launch_bounds__(kNgThreads) ngram_best_kernel(const NgramDev T, int parity, const int32_t* hist,
+                                                                int64_t stride, const int32_t* lens) {
+    __shared__ long long s_pref[SPECNG_NGRAM_MAX_B + 1];
+    __shared__ int s_lo[SPECNG_NGRAM_MAX_B], s_hi[SPECNG_NGRAM_MAX_B];
+    build_new_range(T, parity, lens, stride, s_pref, s_lo, s_hi, false);
+    const long long total = s_pref[T.B];
+    for (long long f = static_cast<long long>(blockIdx.x) * kNgThreads + threadIdx.x; f < total;
+         f += static_cast<long long>(gridDim.x) * kNgThreads) {
+        const int b = seq_of(s_pref, T.B, f);
+        const int i = s_lo[b] + static_cast<int>(f - s_pref[b]);
+        const int32_t* h = hist + static_cast<size_t>(b) * stride;
+        const int c = h[i], t1 = h[i - 1];
+        if (!tok_ok(c, T.V) || !tok_ok(t1, T.V)) continue;
+        push_best(T, T.bi_pair, T.bi_ctx, key_bi_pair(b, t1, c), key_bi_ctx(b, t1), c);
+        if (i >= 2) {
+            const int t2 = h[i - 2];
+            if (!tok_ok(t2, T.V)) continue;
+            push_best(T, T.tri_pair, T.tri_ctx, key_tri_pair(b, t2, t1, c), key_tri_ctx(b, t2, t1), c);
+        }
+    }
+    // the next call starts from the lengths indexed now (other buffer: no
+    // block of this launch reads it)
+    if (blockIdx.x == 0) {
+        for (int b = threadIdx.x; b < T.B; b += kNgThreads) {
+            const int idx = T.indexed[parity][b];
+            T.indexed[parity ^ 1][b] = s_hi[b] > idx ? s_hi[b] : idx;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kNgThreads) ngram_draft_kernel(const NgramDev T, const int32_t* hist, int64_t stride,
+                                                                 const int32_t* lens, int max_k, const int32_t* k_limit,
+                                                                 int32_t* out_drafts, int32_t* out_k) {
+    const int b = blockIdx.x * kNgThreads + threadIdx.x;
+    if (b >= T.B) return;
+    int kmax = max_k;
+    if (k_limit != nullptr) {
+        const int kl = k_limit[b];
+        kmax = kl < 0 ? 0 : (kl < kmax ? kl : kmax);
+    }
+    int L = lens[b];
+    if (L < 0) L = 0;
+    if (static_cast<int64_t>(L) > stride) L = static_cast<int>(stride);
+    const int32_t* h = hist + static_cast<size_t>(b) * stride;
+    int c2 = L >= 2 ? h[L - 2] : -1;
+    int c1 = L >= 1 ? h[L - 1] : -1;
+    if ((L >= 2 && !tok_ok(c2, T.V)) || (L >= 1 && !tok_ok(c1, T.V))) raise_status(T.status, SPECNG_DEV_TOKEN_OOR);
+    if (!tok_ok(c2, T.V)) c2 = -1;
+    if (!tok_ok(c1, T.V)) c1 = -1;
+    int n = 0;
+    int32_t* out = out_drafts + static_cast<size_t>(b) * max_k;
+    while (n < kmax && c1 >= 0) {
+        int tok = -1;
+        uint64_t v;
+        if (c2 >= 0 && find_value(T.tri_ctx, T.mask, key_tri_ctx(b, c2, c1), &v)) tok = best_token(v);
+        if (tok < 0 && find_value(T.bi_ctx, T.mask, key_bi_ctx(b, c1), &v)) tok = best_token(v);
+        if (tok < 0) break;
+        out[n++] = tok;
+        c2 = c1;
+        c1 = tok;
+    }
+    for (int t = n; t < max_k; ++t) out[t] = -1;
+    out_k[b] = n;
+}
+
+__global__ void ngram_clear_kernel(const NgramDev T) {
+    const uint64_t slots = T.mask + 1;
+    const ulonglong2 empty = make_ulonglong2(kEmptyKey, 0ull);
+    for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < slots;
+         i += static_cast<uint64_t>(gridDim.x) * blockDim.x) {
+        T.tri_pair[i] = empty;
+        T.bi_pair[i] = empty;
+        T.tri_ctx[i] = empty;
+        T.bi_ctx[i] = empty;
+    }
+    if (blockIdx.x == 0) {
+        for (int b = threadIdx.x; b < T.B; b += blockDim.x) { T.indexed[0][b] = 0; T.indexed[1][b] = 0; }
+    }
+}
+
+__global__ void spec_append_kernel(int32_t* hist, int64_t stride, int32_t* lens, int64_t cap, const int32_t* out_tokens,
+                                   const int32_t* out_accept, int B, int K, unsigned* status) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    const int a = out_accept[b];
+    if (a < 0 || a > K) { raise_status(status, SPECNG_DEV_BAD_K); return; }
+    const int L = lens[b];
+    if (L < 0 || static_cast<int64_t>(L) + a + 1 > cap) { raise_status(status, SPECNG_DEV_HIST_OVERFLOW); return; }
+    int32_t* h = hist + static_cast<size_t>(b) * stride + L;
+    const int32_t* t = out_tokens + static_cast<size_t>(b) * (K + 1);
+    for (int i = 0; i <= a; ++i) h[i] = t[i];
+    lens[b] = L + a + 1;
+}
+
+__global__ void philox_kernel(const uint4* ctr, uint32_t k0, uint32_t k1, uint4* out, int64_t n) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        out[i] = philox4x32_10(ctr[i], k0, k1);
+}
+
+}  // namespace
+
+cudaError_t launch_ngram_update(const NgramDev& T, int parity, const int32_t* hist, int64_t stride,
+                                const int32_t* lens, int grid, cudaStream_t s) {
+    ngram_count_kernel<<<grid, kNgThreads, 0, s>>>(T, parity, hist, stride, lens);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    ngram_best_kernel<<<grid, kNgThreads, 0, s>>>(T, parity, hist, stride, lens);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ngram_draft(const NgramDev& T, const int32_t* hist, int64_t stride, const int32_t* lens,
+                               int max_k, const int32_t* k_limit, int32_t* out_drafts, int32_t* out_k,
+                               cudaStream_t s) {
+    const int grid = (T.B + kNgThreads - 1) / kNgThreads;
+    ngram_draft_kernel<<<grid, kNgThreads, 0, s>>>(T, hist, stride, lens, max_k, k_limit, out_drafts, out_k);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_ngram_clear(const NgramDev& T, cudaStream_t s) {
+    const uint64_t slots = T.mask + 1;
+    uint64_t blocks = (slots + 255) / 256;
+    if (blocks > 65536) blocks = 65536;
+    ngram_clear_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(T);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_spec_append(int32_t* hist, int64_t stride, int32_t* lens, int64_t cap, const int32_t* out_tokens,
+                               const int32_t* out_accept, int B, int K, unsigned* status, cudaStream_t s) {
+    spec_append_kernel<<<(B + 127) / 128, 128, 0, s>>>(hist, stride, lens, cap, out_tokens, out_accept, B, K, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_philox(const uint32_t* ctr, uint64_t seed, uint32_t* out, int64_t n, cudaStream_t s) {
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    if (blocks < 1) blocks = 1;
+    philox_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(reinterpret_cast<const uint4*>(ctr),
+                                                                static_cast<uint32_t>(seed),
+                                                                static_cast<uint32_t>(seed >> 32),
+                                                                reinterpret_cast<uint4*>(out), n);
+    return cudaGetLastError();
+}
+
+}  // namespace specng

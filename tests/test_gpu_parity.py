@@ -1,0 +1,62 @@
+"""GPU parity of the whole hot path (draft -> verify -> append -> update)
+against the fp64 oracle, in lockstep, on every workload at sizes the oracle
+finishes in seconds.  V = 40000 spans three bf16 chunks (five fp32 chunks)
+with a ragged tail; V = 40001 takes the unaligned (scalar-load) path."""
+import pytest
+import torch
+
+from speculative_decoding_draft_ngram_gb300 import workloads as wl
+
+import lockstep
+
+pytestmark = pytest.mark.gpu
+
+V_SMALL = 40000
+
+CASES = {
+    "c1": (wl.get("c1"), 64, None),
+    "c2_greedy": (wl.get("c2", V=V_SMALL, hist_len=(512, 512), steps=16), 16, 0.0),
+    "c2_t06": (wl.get("c2", V=V_SMALL, hist_len=(512, 512), steps=16), 16, 0.6),
+    "c2_literal_boost": (wl.get("c2", V=V_SMALL, hist_len=(512, 512), boost="literal", steps=8), 8, 0.6),
+    "c3_softcap_gate": (wl.get("c3", B=6, V=V_SMALL, hist_len=(64, 700), steps=16), 16, None),
+    "c3_f32": (wl.get("c3", B=4, V=V_SMALL, hist_len=(64, 700), dtype="f32", steps=8), 8, None),
+    "c3_greedy_softcap": (wl.get("c3", B=4, V=V_SMALL, hist_len=(64, 700), steps=8), 8, 0.0),
+    "c4_dense": (wl.get("c4", B=6, V=V_SMALL, steps=10), 10, None),
+    "c4_dense_f32": (wl.get("c4", B=3, V=V_SMALL, dtype="f32", steps=6), 6, None),
+    "c4_dense_softcap_penalty": (wl.get("c4", B=3, V=V_SMALL, softcap=20.0, rep_penalty=1.3,
+                                        rep_window=32, steps=6), 6, None),
+    "c5_penalty": (wl.get("c5", B=7, V=V_SMALL, hist_len=(1500, 1500), steps=10), 10, None),
+    "c5_f32": (wl.get("c5", B=5, V=V_SMALL, hist_len=(1500, 1500), dtype="f32", steps=6), 6, None),
+    "c5_greedy_penalty": (wl.get("c5", B=5, V=V_SMALL, hist_len=(1500, 1500), steps=6), 6, 0.0),
+    "c5_penalty_below_one": (wl.get("c5", B=4, V=V_SMALL, hist_len=(1500, 1500), rep_penalty=0.8,
+                                    steps=6), 6, None),
+    "unaligned_v": (wl.get("c5", B=4, V=V_SMALL + 1, hist_len=(1500, 1500), steps=6), 6, None),
+    "unaligned_v_dense": (wl.get("c4", B=3, V=V_SMALL + 3, steps=5), 5, None),
+    "tiny_v": (wl.get("c1", V=5, zipf_ids=5, steps=24), 24, None),
+    "k2_many_seqs": (wl.get("c5", B=33, K=2, V=3000, hist_len=(300, 300), steps=8), 8, None),
+    "k0_bonus_only": (wl.get("c5", B=4, K=0, V=V_SMALL, hist_len=(300, 300), steps=5), 5, None),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_lockstep(name):
+    cfg, steps, T = CASES[name]
+    rep = lockstep.run(cfg, steps, T=T)
+    assert rep.steps == steps
+    assert rep.excused == 0, rep.notes
+    if cfg.K > 0 and name not in ("c2_literal_boost",):
+        assert rep.drafted > 0
+    if name in ("c2_t06", "c3_softcap_gate", "c4_dense", "c5_penalty", "c1"):
+        assert rep.accepted > 0
+
+
+def test_gate_turns_sequences_off():
+    cfg = wl.get("c3", B=8, V=8000, hist_len=(64, 400), boost_prob=(0.0, 0.3), steps=20)
+    rep = lockstep.run(cfg, 20)
+    assert rep.gated > 0
+
+
+def test_long_c1_run():
+    # the tiny workload for its full 64 steps with three sampler seeds
+    for seed in (8, 123, 99991):
+        lockstep.run(wl.get("c1"), 64, seed=seed)

@@ -59,6 +59,13 @@ def test_count_invariants():
     tri2, bi2 = ngram.continuation_stats(tokens, 300)
     assert tri2 != tri
     assert ngram.continuation_stats(tokens[:300], 300) == (tri2, bi2)
+    # incremental extension equals the rebuild
+    inc = ngram.continuation_stats(tokens, 0)
+    prev = 0
+    for end in (1, 2, 3, 50, 300, 500):
+        ngram.extend_stats(inc, tokens, prev, end)
+        prev = end
+        assert inc == ngram.continuation_stats(tokens, end)
 
 
 def test_hand_worked_examples():
