@@ -204,6 +204,8 @@ class Path:
         self.limits = (wl.draft_limits(cfg, g, device) if not cfg.k_uniform else
                        torch.randint(0, K + 1, (steps_total, B), generator=g, device=device, dtype=torch.int32))
         self.bprob = wl.boost_probs(cfg, device)
+        zcdf = wl.zipf_cdf(cfg.zipf_ids or cfg.V, cfg.zipf_s, device)
+        self.fallback = [wl.fallback_drafts(cfg, g, device, zcdf) for _ in range(16)] if cfg.topup else None
         self.kbuf = torch.zeros((steps_total, B), dtype=torch.int32, device=device)
         self.drafts = torch.full((B, K), -1, dtype=torch.int32, device=device)
         self.kfull = torch.full((B,), K, dtype=torch.int32, device=device)
@@ -223,8 +225,9 @@ class Path:
         sp, cfg = self.sp, self.cfg
         if self.ngram:
             lim = self.limits[s] if cfg.k_uniform else None
+            fb = self.fallback[s % 16] if self.fallback is not None else None
             sp.ngram_draft(self.table, self.hist, self.lens, cfg.K, k_limit=lim, out_drafts=self.drafts,
-                           out_k=self.kbuf[s])
+                           out_k=self.kbuf[s], fallback=fb)
             drafts, k, q = self.drafts, self.kbuf[s], None
         else:
             i = s % self.n_sets
@@ -432,11 +435,13 @@ class OracleState:
         cfg = self.cfg
         logits = wl.step_logits(cfg, self.g)
         lim = wl.draft_limits(cfg, self.g).numpy()
+        fb = wl.fallback_drafts(cfg, self.g)
         if cfg.dense:
             q, d = wl.dense_draft(cfg, logits, self.g)
             q, d, k = q.numpy(), d.numpy().astype(np.int64), np.full(cfg.B, cfg.K)
         else:
-            d, k = on.draft_batch(self.hist, self.lens, cfg.K, k_limit=lim)
+            d, k = on.draft_batch(self.hist, self.lens, cfg.K, k_limit=lim,
+                                  fallback=None if fb is None else fb.numpy())
             q = None
         if cfg.boost is not None:
             logits = wl.apply_boost(cfg, logits, torch.from_numpy(d), torch.from_numpy(k),

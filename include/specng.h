@@ -123,10 +123,13 @@ int ngram_update(specng_ngram* table, const int32_t* history, int64_t hist_strid
  * the last two tokens of history ++ drafts so far; the trigram context is
  * tried first, then the bigram context; drafting stops at the first miss.
  * k_limit: optional int32 [B] per-sequence cap (NULL: max_k for all).
+ * fallback: optional int32 [B, max_k] proposals of another drafter; when
+ * given, the positions after the first miss (up to the cap) take
+ * fallback[b, t] and are counted in out_k (NULL: drafting just stops).
  * out_drafts: int32 [B, max_k], padded with -1; out_k: int32 [B], the count.
  * The table is read only.  max_k in [0, 16].  One kernel launch. */
 int ngram_draft(const specng_ngram* table, const int32_t* history, int64_t hist_stride,
-                const int32_t* lens, int max_k, const int32_t* k_limit,
+                const int32_t* lens, int max_k, const int32_t* k_limit, const int32_t* fallback,
                 int32_t* out_drafts, int32_t* out_k, cudaStream_t s);
 
 /* ------------------------------------------------------------------------

@@ -102,11 +102,14 @@ def draft(tokens: Sequence[int], length: int, max_k: int, stats=None) -> List[in
     return out
 
 
-def draft_batch(history, lens, max_k: int, k_limit=None, stats=None):
+def draft_batch(history, lens, max_k: int, k_limit=None, stats=None, fallback=None):
     """Drafts for every sequence: (drafts [B, max_k] padded with -1, counts [B]).
 
     ``stats`` optionally holds each sequence's statistics of its whole
-    history (as kept up to date by ``extend_stats``)."""
+    history (as kept up to date by ``extend_stats``).  ``fallback`` [B, max_k]
+    optionally holds another drafter's proposals: the positions after the
+    first miss, up to the per-sequence cap, take them (reading of a
+    fixed per-sequence draft length when the tables run dry)."""
     import numpy as np
     B = len(lens)
     drafts = np.full((B, max(max_k, 0)), -1, dtype=np.int64)
@@ -114,6 +117,8 @@ def draft_batch(history, lens, max_k: int, k_limit=None, stats=None):
     for b in range(B):
         kb = max_k if k_limit is None else max(0, min(max_k, int(k_limit[b])))
         d = draft(history[b], int(lens[b]), kb, None if stats is None else stats[b])
+        if fallback is not None:
+            d = d + [int(t) for t in fallback[b, len(d):kb]]
         drafts[b, :len(d)] = d
         counts[b] = len(d)
     return drafts, counts

@@ -100,7 +100,7 @@ def load() -> ctypes.CDLL:
         "specng_ngram_reset": (I, [P, P]),
         "specng_ngram_capacity": (I, [P, ctypes.POINTER(I64)]),
         "ngram_update": (I, [P, P, I64, P, P]),
-        "ngram_draft": (I, [P, P, I64, P, I, P, P, P, P]),
+        "ngram_draft": (I, [P, P, I64, P, I, P, P, P, P, P]),
         "spec_verify_workspace_bytes": (SZ, [I, I, I]),
         "spec_verify_workspace_init": (I, [P, SZ, P]),
         "spec_verify": (I, [P, I, I, I, I, P, P, P, P, I64, P, ctypes.POINTER(VerifyParamsC),
@@ -186,8 +186,10 @@ def ngram_update(table: NgramTable, history: torch.Tensor, lens: torch.Tensor):
 
 def ngram_draft(table: NgramTable, history: torch.Tensor, lens: torch.Tensor, max_k: int,
                 k_limit: Optional[torch.Tensor] = None, out_drafts: Optional[torch.Tensor] = None,
-                out_k: Optional[torch.Tensor] = None):
-    """Chained trigram -> bigram drafts: returns (out_drafts [B, max_k], out_k [B])."""
+                out_k: Optional[torch.Tensor] = None, fallback: Optional[torch.Tensor] = None):
+    """Chained trigram -> bigram drafts: returns (out_drafts [B, max_k], out_k [B]).
+
+    fallback [B, max_k] (optional) fills the positions after the first miss."""
     B = lens.shape[0]
     if out_drafts is None:
         out_drafts = torch.empty((B, max_k), dtype=torch.int32, device=history.device)
@@ -195,7 +197,8 @@ def ngram_draft(table: NgramTable, history: torch.Tensor, lens: torch.Tensor, ma
         out_k = torch.empty((B,), dtype=torch.int32, device=history.device)
     _check(load().ngram_draft(table._h, _ptr(history, torch.int32, "history"), history.shape[1],
                               _ptr(lens, torch.int32, "lens"), int(max_k),
-                              _ptr(k_limit, torch.int32, "k_limit"), _ptr(out_drafts, torch.int32, "out_drafts"),
+                              _ptr(k_limit, torch.int32, "k_limit"), _ptr(fallback, torch.int32, "fallback"),
+                              _ptr(out_drafts, torch.int32, "out_drafts"),
                               _ptr(out_k, torch.int32, "out_k"), _stream(history.device)), "ngram_draft")
     return out_drafts, out_k
 

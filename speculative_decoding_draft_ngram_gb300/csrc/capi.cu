@@ -44,7 +44,7 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct WsLayout {
     size_t part, rowres, seqres, part2, tickets, total;
-    size_t row_ticket, seq_ticket, seq_ticket2;
+    size_t row_ticket, row_thr, seq_ticket, seq_ticket2;
 };
 
 // The f32 chunk is the smaller one, so its chunk count bounds both dtypes.
@@ -61,6 +61,7 @@ WsLayout ws_layout(int B, int K, int V) {
     L.part2 = off;   off = align256(off + static_cast<size_t>(B) * nch * sizeof(Partial));
     L.tickets = off;
     L.row_ticket = off;   off += rows * sizeof(unsigned);
+    L.row_thr = off;      off += rows * sizeof(unsigned);
     L.seq_ticket = off;   off += static_cast<size_t>(B) * sizeof(unsigned);
     L.seq_ticket2 = off;  off += static_cast<size_t>(B) * sizeof(unsigned);
     L.total = align256(off);
@@ -197,15 +198,16 @@ int ngram_update(specng_ngram* table, const int32_t* history, int64_t hist_strid
 }
 
 int ngram_draft(const specng_ngram* table, const int32_t* history, int64_t hist_stride, const int32_t* lens,
-                int max_k, const int32_t* k_limit, int32_t* out_drafts, int32_t* out_k, cudaStream_t s) {
+                int max_k, const int32_t* k_limit, const int32_t* fallback, int32_t* out_drafts, int32_t* out_k,
+                cudaStream_t s) {
     if (table == nullptr || history == nullptr || lens == nullptr || out_k == nullptr)
         return fail(SPECNG_EINVAL, "ngram_draft: NULL argument");
     if (max_k < 0 || max_k > SPECNG_MAX_K) return fail(SPECNG_EINVAL, "ngram_draft: max_k outside [0, 16]");
     if (max_k > 0 && out_drafts == nullptr) return fail(SPECNG_EINVAL, "ngram_draft: out_drafts is NULL");
     if (hist_stride < 1 || hist_stride > SPECNG_NGRAM_MAX_POS)
         return fail(SPECNG_EINVAL, "ngram_draft: hist_stride outside [1, 2^24]");
-    const cudaError_t e = launch_ngram_draft(table->dev, history, hist_stride, lens, max_k, k_limit, out_drafts,
-                                             out_k, s);
+    const cudaError_t e = launch_ngram_draft(table->dev, history, hist_stride, lens, max_k, k_limit, fallback,
+                                             out_drafts, out_k, s);
     if (e != cudaSuccess) return fail_cuda(e, "ngram_draft");
     return SPECNG_OK;
 }
@@ -295,6 +297,7 @@ int spec_verify(const void* logits, int logits_dtype, int B, int K, int V, const
     P.seqres = reinterpret_cast<SeqRes*>(ws + L.seqres);
     P.part2 = reinterpret_cast<Partial*>(ws + L.part2);
     P.row_ticket = reinterpret_cast<unsigned*>(ws + L.row_ticket);
+    P.row_thr = reinterpret_cast<unsigned*>(ws + L.row_thr);
     P.seq_ticket = reinterpret_cast<unsigned*>(ws + L.seq_ticket);
     P.seq_ticket2 = reinterpret_cast<unsigned*>(ws + L.seq_ticket2);
     P.status = status_ptr();

@@ -146,7 +146,8 @@ __global__ void __launch_bounds__(kNgThreads) ngram_best_kernel(const NgramDev T
 
 __global__ void __launch_bounds__(kNgThreads) ngram_draft_kernel(const NgramDev T, const int32_t* hist, int64_t stride,
                                                                  const int32_t* lens, int max_k, const int32_t* k_limit,
-                                                                 int32_t* out_drafts, int32_t* out_k) {
+                                                                 const int32_t* fallback, int32_t* out_drafts,
+                                                                 int32_t* out_k) {
     const int b = blockIdx.x * kNgThreads + threadIdx.x;
     if (b >= T.B) return;
     int kmax = max_k;
@@ -174,6 +175,10 @@ __global__ void __launch_bounds__(kNgThreads) ngram_draft_kernel(const NgramDev 
         out[n++] = tok;
         c2 = c1;
         c1 = tok;
+    }
+    if (fallback != nullptr) {
+        const int32_t* fb = fallback + static_cast<size_t>(b) * max_k;
+        for (; n < kmax; ++n) out[n] = fb[n];
     }
     for (int t = n; t < max_k; ++t) out[t] = -1;
     out_k[b] = n;
@@ -226,10 +231,11 @@ cudaError_t launch_ngram_update(const NgramDev& T, int parity, const int32_t* hi
 }
 
 cudaError_t launch_ngram_draft(const NgramDev& T, const int32_t* hist, int64_t stride, const int32_t* lens,
-                               int max_k, const int32_t* k_limit, int32_t* out_drafts, int32_t* out_k,
-                               cudaStream_t s) {
+                               int max_k, const int32_t* k_limit, const int32_t* fallback, int32_t* out_drafts,
+                               int32_t* out_k, cudaStream_t s) {
     const int grid = (T.B + kNgThreads - 1) / kNgThreads;
-    ngram_draft_kernel<<<grid, kNgThreads, 0, s>>>(T, hist, stride, lens, max_k, k_limit, out_drafts, out_k);
+    ngram_draft_kernel<<<grid, kNgThreads, 0, s>>>(T, hist, stride, lens, max_k, k_limit, fallback, out_drafts,
+                                                   out_k);
     return cudaGetLastError();
 }
 

@@ -86,8 +86,8 @@ __device__ __forceinline__ bool find_value(const ulonglong2* tab, uint64_t mask,
 cudaError_t launch_ngram_update(const NgramDev& T, int parity, const int32_t* hist, int64_t stride,
                                 const int32_t* lens, int grid, cudaStream_t s);
 cudaError_t launch_ngram_draft(const NgramDev& T, const int32_t* hist, int64_t stride, const int32_t* lens,
-                               int max_k, const int32_t* k_limit, int32_t* out_drafts, int32_t* out_k,
-                               cudaStream_t s);
+                               int max_k, const int32_t* k_limit, const int32_t* fallback, int32_t* out_drafts,
+                               int32_t* out_k, cudaStream_t s);
 cudaError_t launch_ngram_clear(const NgramDev& T, cudaStream_t s);
 cudaError_t launch_spec_append(int32_t* hist, int64_t stride, int32_t* lens, int64_t cap, const int32_t* out_tokens,
                                const int32_t* out_accept, int B, int K, unsigned* status, cudaStream_t s);

@@ -87,6 +87,7 @@ struct VerifyDev {
     RowRes* rowres;
     SeqRes* seqres;
     unsigned* row_ticket;
+    unsigned* row_thr;        // best candidate score published per row (score_key)
     unsigned* seq_ticket;
     Partial* part2;
     unsigned* seq_ticket2;
@@ -208,6 +209,32 @@ __device__ __forceinline__ double warp_sum_f64(double v) {
     return v;
 }
 
+// Order-preserving map of a float score to an unsigned key (0 = "none").
+__device__ __forceinline__ unsigned score_key(float f) {
+    const unsigned u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_score(unsigned k) {
+    if (k == 0u) return -INFINITY;
+    return (k & 0x80000000u) ? __uint_as_float(k & 0x7FFFFFFFu) : __uint_as_float(~k);
+}
+
+// Gumbel variate from a Philox word with hardware log2 (error ~1e-5): a
+// pre-filter only; candidates that pass it are re-scored with gumbel_f32.
+__device__ __forceinline__ float gumbel_fast(uint32_t w) {
+    const float u = static_cast<float>(uniform_numerator(w)) * 0x1p-24f;
+    const float y = 1.0f - u;  // exact
+    float e;
+    if (y < 0.0625f) {
+        e = y * fmaf(y, fmaf(y, fmaf(y, 0.25f, 0.33333334f), 0.5f), 1.0f);  // -log1p(-y) series
+    } else {
+        e = -0.6931472f * __log2f(u);
+    }
+    return -0.6931472f * __log2f(e);
+}
+
+constexpr int kQCap = 32 + 32 * 8;  // per-warp candidate queue: a drained remainder + one push
+
 // Merge (m, s) pairs whose sums are relative to their own maxima.
 __device__ __forceinline__ void ms_merge(float& m, float& s, float mo, float so, float sc) {
     const float M = fmaxf(m, mo);
@@ -261,14 +288,19 @@ __global__ void __launch_bounds__(kThreads, 2) verify_stream_kernel(const Verify
     __shared__ uint32_t s_bm[PENALTY ? CHUNK / 32 : 1];
     __shared__ int s_win[PENALTY ? SPECNG_MAX_REP_WINDOW : 1];
     __shared__ int s_nwin;
-    __shared__ float s_m[kWarps], s_s[kWarps];
+    __shared__ float s_m[kWarps], s_s[kWarps], s_seed[kWarps];
     __shared__ Top2 s_t[kWarps];
     __shared__ int s_last;
+    __shared__ int s_qn[kWarps];
+    __shared__ int2 s_q[GREEDY ? 1 : kWarps * kQCap];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int K1 = P.K + 1;
-    const int row = blockIdx.x / P.nchunk;
-    const int c = blockIdx.x - row * P.nchunk;
+    const int rows = P.B * K1;
+    // chunk-major order: chunk c of every row is scheduled before chunk c + 1,
+    // so later chunks start from the best score the earlier ones published
+    const int c = blockIdx.x / rows;
+    const int row = blockIdx.x - c * rows;
     const int b = row / K1, j = row - b * K1;
 
     int kb = P.k[b];
@@ -351,70 +383,110 @@ __global__ void __launch_bounds__(kThreads, 2) verify_stream_kernel(const Verify
     float m_c = -INFINITY, s_c = 0.0f;
     Top2 tt = top2_empty();
     if constexpr (!GREEDY) {
-        // ---- threshold seed: exact score of the warp's largest element
-        float thr = -INFINITY;
+        // ---- threshold seed: exact score of each warp's largest element; the
+        //      best of them over the CTA and of what earlier chunks published
         {
+            float t0 = -INFINITY;
             float wm = m_t;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, off));
             const unsigned own = __ballot_sync(0xffffffffu, wm > -INFINITY && m_t == wm && arg_t >= 0 && arg_t != excl);
             if (own != 0u) {
                 const int src = __ffs(own) - 1;
-                float t0 = 0.0f;
                 if (lane == src) {
                     const uint4 w = gumbel_block(nk, static_cast<uint32_t>(arg_t) >> 2, static_cast<uint32_t>(j));
                     t0 = m_t * P.invT + gumbel_f32(pick_word(w, static_cast<uint32_t>(arg_t) & 3u));
                 }
                 t0 = __shfl_sync(0xffffffffu, t0, src);
-                thr = t0 - cand_delta(t0);
             }
+            if (lane == 0) { s_seed[warp] = t0; s_qn[warp] = 0; }
         }
-        // ---- pass B: sum of exponentials and Gumbel candidates
+        __syncthreads();
+        float seed = s_seed[0];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) seed = fmaxf(seed, s_seed[w]);
+        const float pub = key_score(__ldcg(&P.row_thr[row]));
+        if (tid == 0 && seed > -INFINITY) atomicMax(&P.row_thr[row], score_key(seed));
+        const float best0 = fmaxf(seed, pub);
+        float thr = best0 > -INFINITY ? best0 - cand_delta(best0) : -INFINITY;
+        float zthr = thr - kGumbelMax;  // an element can reach thr only if z / T >= zthr
+        int2* q = s_q + warp * kQCap;
+        volatile int* qn = s_qn + warp;
+
+        // score one queued candidate (all lanes busy); updates tt / thr
+        auto score_one = [&](int2 ent) {
+            const int v = ent.x;
+            const float zb = __int_as_float(ent.y);
+            if (v == excl || zb + kGumbelMax < thr) return;
+            const uint4 w = gumbel_block(nk, static_cast<uint32_t>(v) >> 2, static_cast<uint32_t>(j));
+            const uint32_t word = pick_word(w, static_cast<uint32_t>(v) & 3u);
+            if (zb + gumbel_fast(word) < thr - 1e-3f) return;
+            const float score = zb + gumbel_f32(word);
+            if (score >= thr) {
+                top2_push(tt, score, v);
+                thr = fmaxf(thr, tt.s1 - cand_delta(tt.s1));
+            }
+        };
+
+        // ---- pass B: sum of exponentials; candidates go to the warp's queue
         const float msc = m_t * P.sc;
-        uint32_t cblk = 0xFFFFFFFFu;
-        uint4 cw = make_uint4(0u, 0u, 0u, 0u);
         float s = 0.0f;
 #pragma unroll
         for (int i = 0; i < kNV; ++i) {
             const int off = (i * kThreads + tid) * EPV;
             const int e0 = v0 + off;
             const int nv = min(EPV, v1 - e0);
-            if (nv <= 0) continue;
-            float x[EPV], z[EPV];
-            unpack<BF16>(raw[i], x);
-            const unsigned pb = pen_bits<PENALTY, EPV>(s_bm, off);
-            if (nv == EPV) {
-                float acc = 0.0f;
+            float z[EPV];
+            if (nv > 0) {
+                float x[EPV];
+                unpack<BF16>(raw[i], x);
+                const unsigned pb = pen_bits<PENALTY, EPV>(s_bm, off);
+                if (nv == EPV) {
+                    float acc = 0.0f;
 #pragma unroll
-                for (int e = 0; e < EPV; ++e) {
-                    z[e] = transform_f32<SOFTCAP, PENALTY>(x[e], (pb >> e) & 1u, P);
-                    acc += ex2_approx(fmaf(z[e], P.sc, -msc));
+                    for (int e = 0; e < EPV; ++e) {
+                        z[e] = transform_f32<SOFTCAP, PENALTY>(x[e], (pb >> e) & 1u, P);
+                        acc += ex2_approx(fmaf(z[e], P.sc, -msc));
+                    }
+                    s += acc;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) {
+                        z[e] = transform_f32<SOFTCAP, PENALTY>(x[e], (pb >> e) & 1u, P);
+                        if (e < nv) s += ex2_approx(fmaf(z[e], P.sc, -msc));
+                    }
                 }
-                s += acc;
-            } else {
+                if (vmax[i] * P.invT >= zthr) {
+                    unsigned msk = 0u;
 #pragma unroll
-                for (int e = 0; e < EPV; ++e) {
-                    z[e] = transform_f32<SOFTCAP, PENALTY>(x[e], (pb >> e) & 1u, P);
-                    if (e < nv) s += ex2_approx(fmaf(z[e], P.sc, -msc));
-                }
-            }
-            if (vmax[i] * P.invT + kGumbelMax >= thr) {
+                    for (int e = 0; e < EPV; ++e)
+                        if (e < nv && z[e] * P.invT >= zthr) msk |= 1u << e;
+                    if (msk != 0u) {
+                        int slot = atomicAdd(&s_qn[warp], __popc(msk));
 #pragma unroll
-                for (int e = 0; e < EPV; ++e) {
-                    if (e >= nv) break;
-                    const float zb = z[e] * P.invT;
-                    const int v = e0 + e;
-                    if (zb + kGumbelMax >= thr && v != excl) {
-                        const uint32_t blk = static_cast<uint32_t>(v) >> 2;
-                        if (blk != cblk) { cw = gumbel_block(nk, blk, static_cast<uint32_t>(j)); cblk = blk; }
-                        const float score = zb + gumbel_f32(pick_word(cw, static_cast<uint32_t>(v) & 3u));
-                        if (score >= thr) {
-                            top2_push(tt, score, v);
-                            thr = fmaxf(thr, tt.s1 - cand_delta(tt.s1));
-                        }
+                        for (int e = 0; e < EPV; ++e)
+                            if ((msk >> e) & 1u) q[slot++] = make_int2(e0 + e, __float_as_int(z[e] * P.invT));
                     }
                 }
             }
+            __syncwarp();
+            int n = *qn;
+            if (n >= 32) {
+                do {
+                    score_one(q[n - 32 + lane]);
+                    n -= 32;
+                } while (n >= 32);
+#pragma unroll
+                for (int off2 = 16; off2 > 0; off2 >>= 1) thr = fmaxf(thr, __shfl_xor_sync(0xffffffffu, thr, off2));
+                zthr = thr - kGumbelMax;
+                __syncwarp();
+                if (lane == 0) *qn = n;
+                __syncwarp();
+            }
+        }
+        {
+            const int n = *qn;
+            if (lane < n) score_one(q[lane]);
         }
         if (!(m_t > -INFINITY)) s = 0.0f;
         // ---- CTA reduction of (max, sum) and candidates
@@ -444,7 +516,8 @@ __global__ void __launch_bounds__(kThreads, 2) verify_stream_kernel(const Verify
             t = top2_merge(t, top2_shfl_xor(t, off));
         }
         if (lane == 0) {
-            st_partial(P.part + blockIdx.x, m, s, t);
+            st_partial(P.part + static_cast<size_t>(row) * P.nchunk + c, m, s, t);
+            if (!GREEDY && t.s1 > -INFINITY) atomicMax(&P.row_thr[row], score_key(t.s1));
             __threadfence();
             const unsigned prev = atomicAdd(&P.row_ticket[row], 1u);
             s_last = prev == static_cast<unsigned>(P.nchunk - 1);
@@ -455,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_stream_kernel(const Verify
     __threadfence();
 
     // ---- last CTA of the row: merge the chunks (warp 0)
-    if (lane == 0) P.row_ticket[row] = 0u;
+    if (lane == 0) { P.row_ticket[row] = 0u; P.row_thr[row] = 0u; }
     const Partial* pr = P.part + static_cast<size_t>(row) * P.nchunk;
     double M = -INFINITY;
     for (int cc = lane; cc < P.nchunk; cc += 32) M = fmax(M, static_cast<double>(__ldcg(&pr[cc].m)));

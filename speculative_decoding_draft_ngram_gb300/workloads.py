@@ -21,6 +21,8 @@ statement; the readings taken where it is open are listed in the design doc.
       repetition penalty 1.1 over the last 64 tokens, T=0.6; histories of
       32768 Zipf(1.05) tokens with 64-token copied spans; n-gram drafts
       capped at k_b.
+  c2, c3 and c5 pad the n-gram drafts with Zipf proposals up to the
+  per-sequence length (K, or k_b for c5) when the tables run dry.
 """
 from __future__ import annotations
 
@@ -54,6 +56,7 @@ class Config:
     boost: Optional[str] = None       # None, "intent", "literal"
     boost_prob: Tuple[float, float] = (0.5, 0.5)   # per-sequence prob ~ U[lo, hi]
     k_uniform: bool = False           # k_b ~ U{0..K} per sequence per step
+    topup: bool = False               # pad n-gram drafts with Zipf proposals up to the cap
     q_noise: float = 0.5
     data_seed: int = 0
     sampler_seed: int = 0
@@ -73,16 +76,16 @@ CONFIGS = {
                  data_seed=1001, sampler_seed=8),
     "c2": Config("c2", B=1, V=151936, K=4, dtype="bf16", temperature=0.6, gate=False, steps=1000,
                  hist_len=(4096, 4096), zipf_s=1.05, span=32, logit_scale=4.0, boost="intent",
-                 data_seed=1002, sampler_seed=9),
+                 topup=True, data_seed=1002, sampler_seed=9),
     "c3": Config("c3", B=64, V=262144, K=4, dtype="bf16", temperature=1.0, softcap=30.0, gate=True,
                  steps=500, hist_len=(512, 8192), zipf_s=1.1, span=32, logit_scale=8.0, boost="intent",
-                 boost_prob=(0.2, 0.9), data_seed=1003, sampler_seed=10),
+                 boost_prob=(0.2, 0.9), topup=True, data_seed=1003, sampler_seed=10),
     "c4": Config("c4", B=32, V=151936, K=4, dtype="bf16", temperature=0.6, dense=True, gate=False,
                  steps=500, hist_len=(1024, 1024), zipf_s=1.05, logit_scale=4.0, data_seed=1004,
                  sampler_seed=11),
     "c5": Config("c5", B=256, V=151936, K=4, dtype="bf16", temperature=0.6, rep_penalty=1.1,
                  rep_window=64, gate=False, steps=200, hist_len=(32768, 32768), zipf_s=1.05, span=64,
-                 logit_scale=4.0, k_uniform=True, data_seed=1005, sampler_seed=12),
+                 logit_scale=4.0, k_uniform=True, topup=True, data_seed=1005, sampler_seed=12),
 }
 
 
@@ -188,6 +191,16 @@ def dense_draft(cfg: Config, logits: torch.Tensor, g: torch.Generator):
     cdf = torch.cumsum(q, dim=-1)
     d = torch.searchsorted(cdf, u * cdf[..., -1:]).clamp_(max=V - 1).squeeze(-1).to(torch.int32)
     return q.contiguous(), d.contiguous()
+
+
+def fallback_drafts(cfg: Config, g: torch.Generator, device="cpu", cdf: Optional[torch.Tensor] = None):
+    """Stand-in for a second drafter: Zipf proposals [B, K] that pad the n-gram
+    drafts up to the per-sequence length (None when cfg.topup is off)."""
+    if not cfg.topup:
+        return None
+    if cdf is None:
+        cdf = zipf_cdf(cfg.zipf_ids or cfg.V, cfg.zipf_s, device)
+    return zipf_tokens(g, (cfg.B, cfg.K), cdf)
 
 
 def draft_limits(cfg: Config, g: torch.Generator, device="cpu") -> torch.Tensor:

@@ -92,15 +92,19 @@ def run(cfg: wl.Config, steps: int, T: float | None = None, device="cuda", seed:
     out_acc = torch.empty((B,), dtype=torch.int32, device=device)
     g = wl._gen(cfg.data_seed + 1, "cpu")
     bprob = wl.boost_probs(cfg, "cpu")
+    zcdf = wl.zipf_cdf(cfg.zipf_ids or cfg.V, cfg.zipf_s)
     sp.get_status(clear=True)
 
     for step in range(steps):
         limits = wl.draft_limits(cfg, g, "cpu")
+        fb = wl.fallback_drafts(cfg, g, "cpu", zcdf)
         logits = wl.step_logits(cfg, g, device="cpu")
         # ---- drafts
         if use_ngram:
-            d_o, k_o = on.draft_batch(hist_o, lens_o, K, k_limit=limits.numpy(), stats=stats)
-            d_g, k_g = sp.ngram_draft(table, hist_g, lens_g, K, k_limit=limits.to(device))
+            d_o, k_o = on.draft_batch(hist_o, lens_o, K, k_limit=limits.numpy(), stats=stats,
+                                      fallback=None if fb is None else fb.numpy())
+            d_g, k_g = sp.ngram_draft(table, hist_g, lens_g, K, k_limit=limits.to(device),
+                                      fallback=None if fb is None else fb.to(device))
             d_g_h, k_g_h = d_g.cpu().numpy(), k_g.cpu().numpy()
             assert np.array_equal(k_g_h, k_o), f"step {step}: draft counts differ\n{k_g_h}\n{k_o}"
             assert np.array_equal(d_g_h, d_o), f"step {step}: drafts differ\n{d_g_h}\n{d_o}"

@@ -44,9 +44,9 @@ def test_lockstep(name):
     rep = lockstep.run(cfg, steps, T=T)
     assert rep.steps == steps
     assert rep.excused == 0, rep.notes
-    if cfg.K > 0 and name not in ("c2_literal_boost",):
+    if cfg.K > 0:
         assert rep.drafted > 0
-    if name in ("c2_t06", "c3_softcap_gate", "c4_dense", "c5_penalty", "c1"):
+    if name in ("c2_t06", "c2_greedy", "c3_softcap_gate", "c1"):
         assert rep.accepted > 0
 
 

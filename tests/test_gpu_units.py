@@ -76,6 +76,24 @@ def test_ngram_matches_oracle_incremental(seed):
     assert torch.equal(a[0], c[0])
 
 
+def test_ngram_fallback_pads_to_the_cap():
+    rng = np.random.default_rng(4)
+    B, V, cap = 40, 7, 200
+    hist, lens = _ngram_case(rng, B, V, 60, cap)
+    t = sp.NgramTable(B, V, B * cap)
+    hg = torch.from_numpy(hist.astype(np.int32)).cuda()
+    lg = torch.from_numpy(lens.astype(np.int32)).cuda()
+    sp.ngram_update(t, hg, lg)
+    fb = rng.integers(0, V, size=(B, 5))
+    lim = rng.integers(0, 6, size=B)
+    d, k = sp.ngram_draft(t, hg, lg, 5, k_limit=torch.from_numpy(lim.astype(np.int32)).cuda(),
+                          fallback=torch.from_numpy(fb.astype(np.int32)).cuda())
+    d_o, k_o = on.draft_batch(hist, lens, 5, k_limit=lim, fallback=fb)
+    np.testing.assert_array_equal(k.cpu().numpy(), lim)
+    np.testing.assert_array_equal(k.cpu().numpy(), k_o)
+    np.testing.assert_array_equal(d.cpu().numpy(), d_o)
+
+
 def test_ngram_large_vocab_keys():
     # ids near 2^18 exercise every key field
     rng = np.random.default_rng(9)
