@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=0, help="sequences in the oracle sample (0: auto)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch size (smaller profiler captures only)")
     return ap.parse_args()
 
 
@@ -172,12 +174,12 @@ class Clocks:
 class Path:
     """Device state of one workload and its step function."""
 
-    def __init__(self, name, steps_total, device, seed_offset=0):
+    def __init__(self, name, steps_total, device, seed_offset=0, batch=0):
         import speculative_decoding_draft_ngram_gb300 as sp
         self.sp = sp
         cfg = wl.get(name)
         cfg = wl.get(name, steps=max(cfg.steps, steps_total), data_seed=cfg.data_seed + 7919 * seed_offset,
-                     sampler_seed=cfg.sampler_seed + seed_offset)
+                     sampler_seed=cfg.sampler_seed + seed_offset, B=batch or cfg.B)
         self.cfg = cfg
         self.dev = device
         B, K, V = cfg.B, cfg.K, cfg.V
@@ -287,7 +289,7 @@ def run_ours(args):
     sp.load()
     total_steps = args.warmup + args.steps
     e2e_steps = 0 if args.no_e2e else min(args.steps, 200)
-    path = Path(args.workload, 2 * total_steps + e2e_steps + 8, dev, seed_offset=rank)
+    path = Path(args.workload, 2 * total_steps + e2e_steps + 8, dev, seed_offset=rank, batch=args.batch)
     cfg = path.cfg
     stream = torch.cuda.current_stream(dev)
 

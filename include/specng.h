@@ -66,6 +66,9 @@ extern "C" {
 #define SPECNG_DEV_BAD_K          0x10u /* k[b] or accept_len[b] outside [0, K]; clamped   */
 #define SPECNG_DEV_COUNT_SAT      0x20u /* an n-gram count passed 2^22 - 1 and saturated   */
 #define SPECNG_DEV_HIST_SHRANK    0x40u /* lens[b] fell below what the table had indexed   */
+#define SPECNG_DEV_TIMEOUT        0x80u /* a bounded wait for a bulk copy gave up; the call's
+                                           outputs are incomplete and its workspace must be
+                                           zeroed again (spec_verify_workspace_init)         */
 
 /* Limits checked on the host. */
 #define SPECNG_MAX_K          16        /* drafts per sequence per call            */

@@ -28,6 +28,7 @@ STATUS_BITS = {
     0x10: "BAD_K",
     0x20: "COUNT_SAT",
     0x40: "HIST_SHRANK",
+    0x80: "TIMEOUT",
 }
 
 # Every symbol include/specng.h declares.

@@ -53,8 +53,63 @@ __device__ __forceinline__ uint4 gumbel_block(const NoiseKey& nk, uint32_t blk, 
     return philox4x32_10(make_uint4(blk, pos | (kPurposeGumbel << 16), nk.step, nk.seq), nk.k0, nk.k1);
 }
 
+// Philox4x32-10 for counters that differ only in word 0 (the vocab block):
+// with words 1..3 fixed, round 1's second product and round 2's first
+// product do not depend on word 0, so they are computed once per row.
+struct RowPhilox {
+    uint32_t c3k1;     // c3 ^ k1 (round 1)
+    uint32_t e2;       // lo(M1 c2) ^ (k0 + W0) (round 2)
+    uint32_t f2;       // hi(M0 c0') ^ (k1 + W1) (round 2)
+    uint32_t d2;       // lo(M0 c0') (round 2, output word 3)
+    uint32_t k0, k1;   // original key
+};
+
+__device__ __forceinline__ RowPhilox row_philox(const NoiseKey& nk, uint32_t pos) {
+    const uint32_t c1 = pos | (kPurposeGumbel << 16), c2 = nk.step, c3 = nk.seq;
+    const uint32_t hi1 = __umulhi(kPhiloxM1, c2), lo1 = kPhiloxM1 * c2;
+    const uint32_t c0p = hi1 ^ c1 ^ nk.k0;  // round-1 output word 0
+    RowPhilox r;
+    r.c3k1 = c3 ^ nk.k1;
+    r.e2 = lo1 ^ (nk.k0 + kPhiloxW0);
+    r.f2 = __umulhi(kPhiloxM0, c0p) ^ (nk.k1 + kPhiloxW1);
+    r.d2 = kPhiloxM0 * c0p;
+    r.k0 = nk.k0;
+    r.k1 = nk.k1;
+    return r;
+}
+
+// Same words as gumbel_block(nk, blk, pos) for the row that rp describes.
+__device__ __forceinline__ uint4 gumbel_block_row(const RowPhilox& rp, uint32_t blk) {
+    // round 1
+    const uint32_t hi0 = __umulhi(kPhiloxM0, blk), lo0 = kPhiloxM0 * blk;
+    const uint32_t c2p = hi0 ^ rp.c3k1;
+    // round 2 (c0' and c1' are row constants folded into e2 / f2 / d2)
+    const uint32_t hi1 = __umulhi(kPhiloxM1, c2p), lo1 = kPhiloxM1 * c2p;
+    uint4 c = make_uint4(hi1 ^ rp.e2, lo1, rp.f2 ^ lo0, rp.d2);
+    uint32_t k0 = rp.k0 + 2u * kPhiloxW0, k1 = rp.k1 + 2u * kPhiloxW1;
+#pragma unroll
+    for (int r = 2; r < 10; ++r) {
+        const uint32_t h0 = __umulhi(kPhiloxM0, c.x);
+        const uint32_t l0 = kPhiloxM0 * c.x;
+        const uint32_t h1 = __umulhi(kPhiloxM1, c.z);
+        const uint32_t l1 = kPhiloxM1 * c.z;
+        c = make_uint4(h1 ^ c.y ^ k0, l1, h0 ^ c.w ^ k1, l0);
+        k0 += kPhiloxW0;
+        k1 += kPhiloxW1;
+    }
+    return c;
+}
+
 __device__ __forceinline__ uint32_t pick_word(const uint4& w, uint32_t lane) {
     return lane == 0 ? w.x : lane == 1 ? w.y : lane == 2 ? w.z : w.w;
+}
+
+// e^-t with the hardware exp2 (relative error ~2^-22).
+__device__ __forceinline__ float exp2f_approx_neg(float t) {
+    float y;
+    const float a = -t * 1.4426950408889634f;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(a));
+    return y;
 }
 
 // u = (2 (w >> 9) + 1) 2^-24: exact in fp32 and fp64, strictly inside (0, 1).
@@ -75,6 +130,17 @@ __device__ __forceinline__ double gumbel_f64(uint32_t w) {
 __device__ __forceinline__ double accept_uniform_f64(const NoiseKey& nk, uint32_t i) {
     const uint4 w = philox4x32_10(make_uint4(0u, i | (kPurposeAccept << 16), nk.step, nk.seq), nk.k0, nk.k1);
     return static_cast<double>(uniform_numerator(w.x)) * 0x1p-24;
+}
+
+// Conservative screen: false only when the Gumbel variate of word w is surely
+// below t (so a score zb + g cannot reach zb + t).  g >= t  <=>  1 - u <= 1 - exp(-e^-t);
+// 1 - u is an exact integer multiple of 2^-24, the right side is computed with
+// the hardware exp2 and widened by a margin far above its error.
+__device__ __forceinline__ bool gumbel_may_reach(uint32_t w, float t) {
+    const float y = exp2f_approx_neg(t);
+    const float c = y < 1e-3f ? y * fmaf(-0.5f, y, 1.0f) : 1.0f - exp2f_approx_neg(y);
+    const float one_minus_u = static_cast<float>(0x1000000u - uniform_numerator(w));  // (1 - u) * 2^24, exact
+    return one_minus_u <= fmaf(c, 16777216.0f * 1.001f, 2.0f);
 }
 
 // Upper bound of a Gumbel draw on the 2^-24 grid (-ln(-ln(1 - 2^-24)) = 16.6355),
@@ -152,6 +218,59 @@ __device__ __forceinline__ Top2 top2_warp_reduce(Top2 t) {
 // Streaming 16-byte load: read once, do not keep in L1.
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {
     return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+
+// ---------------------------------------------------------------- TMA bulk
+// 1-D bulk copies global -> shared completing on an mbarrier (sm_90+ PTX).
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// dst and src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0u;
+}
+
+// Wait for a phase of an mbarrier, giving up after a bounded number of polls
+// (well under a second): a copy that never lands is reported, not waited on.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity) {
+    for (int it = 0; it < (1 << 22); ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (it >= 32) __nanosleep(64);
+    }
+    return false;
 }
 
 // ---------------------------------------------------------------- hashing

@@ -31,6 +31,8 @@
 //     Nothing waits on another CTA.
 #pragma once
 
+#include <cuda_bf16.h>
+
 #include "common.cuh"
 
 namespace specng {
@@ -233,7 +235,34 @@ __device__ __forceinline__ float gumbel_fast(uint32_t w) {
     return -0.6931472f * __log2f(e);
 }
 
-constexpr int kQCap = 32 + 32 * 8;  // per-warp candidate queue: a drained remainder + one push
+constexpr int kQCap = 32 + 32 * 32;  // per-warp candidate queue (chunk offsets): a remainder + one stage
+
+// Largest bf16 value <= f, as a packed pair (both halves).  NaN maps to +inf.
+__device__ __forceinline__ uint32_t bf16x2_floor(float f) {
+    uint32_t u = __float_as_uint(f);
+    if (f != f) u = 0x7F800000u;
+    uint32_t h = u >> 16;
+    if ((u & 0x80000000u) && (u & 0xFFFFu) && (u & 0x7FFFFFFFu) < 0x7F800000u) h += 1u;  // negative: away from 0
+    return h | (h << 16);
+}
+
+__device__ __forceinline__ __nv_bfloat162 as_bf162(uint32_t w) { return *reinterpret_cast<__nv_bfloat162*>(&w); }
+
+// Maximum of the 8 bf16 values of a 16-byte vector (packed compares).
+__device__ __forceinline__ float bf16x8_max(const uint4& r) {
+    const __nv_bfloat162 a = __hmax2(__hmax2(as_bf162(r.x), as_bf162(r.y)), __hmax2(as_bf162(r.z), as_bf162(r.w)));
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(&a);
+    return fmaxf(bf16lo(w), bf16hi(w));
+}
+
+// Bit e set when element e of the vector is >= the (packed) threshold t.
+__device__ __forceinline__ unsigned bf16x8_ge_mask(const uint4& r, uint32_t t) {
+    const __nv_bfloat162 th = as_bf162(t);
+    const unsigned m0 = __hge2_mask(as_bf162(r.x), th), m1 = __hge2_mask(as_bf162(r.y), th);
+    const unsigned m2 = __hge2_mask(as_bf162(r.z), th), m3 = __hge2_mask(as_bf162(r.w), th);
+    return (m0 & 1u) | ((m0 >> 15) & 2u) | ((m1 & 1u) << 2) | ((m1 >> 13) & 8u) | ((m2 & 1u) << 4) |
+           ((m2 >> 11) & 32u) | ((m3 & 1u) << 6) | ((m3 >> 9) & 128u);
+}
 
 // Merge (m, s) pairs whose sums are relative to their own maxima.
 __device__ __forceinline__ void ms_merge(float& m, float& s, float mo, float so, float sc) {
@@ -280,318 +309,696 @@ __device__ __forceinline__ unsigned pen_bits(const uint32_t* s_bm, int off) {
 }
 
 // ---------------------------------------------------------------- K1
+// Persistent, warp-specialised streaming kernel.  One CTA per SM; the active
+// row-chunks of the call (rows 0..k_eff of every sequence, V-chunks of
+// CHUNK elements) are laid out row-major and split into equal contiguous
+// ranges, one per CTA.  A producer warp walks its CTA's range and keeps up to
+// kStages chunks in flight with cp.async.bulk into a shared-memory ring
+// (full / empty mbarriers, bounded waits); sixteen consumer warps each take
+// a 2 KB slice of every chunk.  A consumer warp keeps its Gumbel threshold
+// across the consecutive chunks of one row, so only a row's first chunk
+// needs a seed.  Each chunk leaves one partial (max, sum of exponentials,
+// top-two candidates) in the workspace; the merge kernel combines them.
+
+constexpr int kCWarps = 16;                    // consumer warps
+constexpr int kPWarp = kCWarps;                // producer warp index
+constexpr int kPThreads = (kCWarps + 1) * 32;  // 544
+constexpr int kStages = 5;
+constexpr int kVL = 4;                         // 16-byte vectors per lane per chunk
+
+template <bool BF16>
+__host__ __device__ constexpr int stage_bytes() { return chunk_elems<BF16>() * ElemTraits<BF16>::SIZE; }
+
+template <bool PENALTY>
+__host__ __device__ constexpr size_t k1_dyn_smem() {
+    return static_cast<size_t>(kStages) * 32768 + static_cast<size_t>(kCWarps) * kQCap * sizeof(uint16_t) +
+           (PENALTY ? static_cast<size_t>(kStages) * 2048 : 0);
+}
+
+// Penalty window of row j: the last W tokens of history ++ d_1..d_j, read
+// from the history tail and the drafts (shared or global memory).
+struct WindowView {
+    const int* hwin;    // last nh history tokens
+    const int* drafts;  // d_1..d_k
+    int nh, W;
+
+    __device__ __forceinline__ int count(int j) const {
+        const int total = nh + j;
+        return total < W ? total : W;
+    }
+    __device__ __forceinline__ int token(int j, int t) const {  // t-th token of row j's window
+        const int total = nh + j;
+        const int idx = total - count(j) + t;
+        return idx < nh ? hwin[idx] : drafts[idx - nh];
+    }
+    // whole warp calls it
+    __device__ __forceinline__ bool warp_has(int j, int id) const {
+        bool f = false;
+        const int n = count(j);
+        for (int t = threadIdx.x & 31; t < n; t += 32) f |= token(j, t) == id;
+        return __any_sync(0xffffffffu, f);
+    }
+};
+
+// Bitmap of the penalised ids of row j that fall in [v0, v1); one warp builds it.
+template <int CHUNK>
+__device__ __forceinline__ void warp_build_bitmap(uint32_t* bm, const WindowView& wv, int j, int v0, int v1) {
+    const int lane = threadIdx.x & 31;
+    for (int t = lane; t < CHUNK / 32; t += 32) bm[t] = 0u;
+    __syncwarp();
+    const int n = wv.count(j);
+    for (int t = lane; t < n; t += 32) {
+        const int tok = wv.token(j, t);
+        if (tok >= v0 && tok < v1) atomicOr(&bm[(tok - v0) >> 5], 1u << ((tok - v0) & 31));
+    }
+    __syncwarp();
+}
+
+__device__ __forceinline__ int gate_keff(const VerifyDev& P, int b, int* kb_out, bool flag) {
+    int kb = P.k[b];
+    if (kb < 0 || kb > P.K) {
+        if (flag) raise_status(P.status, SPECNG_DEV_BAD_K);
+        kb = kb < 0 ? 0 : P.K;
+    }
+    if (kb_out) *kb_out = kb;
+    if (P.gate && kb > 0 && !(P.ema[b] >= P.thresh)) return 0;
+    return kb;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+struct StageMeta {
+    int b, j, c, excl, seg_end;  // seg_end: the last chunk of this row in the CTA's range
+};
+
+struct WarpPart {
+    float m, s;
+    Top2 t;
+};
 
 template <bool BF16, bool GREEDY, bool SOFTCAP, bool PENALTY>
-__global__ void __launch_bounds__(kThreads, 2) verify_stream_kernel(const VerifyDev P) {
+__global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const VerifyDev P) {
     constexpr int EPV = ElemTraits<BF16>::EPV;
     constexpr int CHUNK = chunk_elems<BF16>();
-    __shared__ uint32_t s_bm[PENALTY ? CHUNK / 32 : 1];
-    __shared__ int s_win[PENALTY ? SPECNG_MAX_REP_WINDOW : 1];
-    __shared__ int s_nwin;
-    __shared__ float s_m[kWarps], s_s[kWarps], s_seed[kWarps];
-    __shared__ Top2 s_t[kWarps];
-    __shared__ int s_last;
-    __shared__ int s_qn[kWarps];
-    __shared__ int2 s_q[GREEDY ? 1 : kWarps * kQCap];
+    constexpr int SB = stage_bytes<BF16>();
+    static_assert(SB == 32768 && SB == kCWarps * 32 * kVL * 16, "stage layout");
+    extern __shared__ __align__(128) uint8_t s_dyn[];
+    uint8_t* s_stage = s_dyn;
+    uint16_t* s_q = reinterpret_cast<uint16_t*>(s_dyn + kStages * SB);
+    uint32_t* s_bm = reinterpret_cast<uint32_t*>(s_dyn + kStages * SB + kCWarps * kQCap * sizeof(uint16_t));
+    __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages];
+    __shared__ StageMeta s_meta[kStages];
+    __shared__ WarpPart s_slot[kStages][kCWarps];
+    __shared__ int s_cnt[kStages];
+    __shared__ unsigned s_rthr[kStages + 1];  // per-segment shared threshold (score_key; 0 = none)
+    __shared__ int s_qn[kCWarps];
+    __shared__ long long s_wsum[kPThreads / 32];
+    __shared__ int s_start[3];
+    __shared__ int s_hwin[PENALTY ? SPECNG_MAX_REP_WINDOW : 1];
+    __shared__ int s_pdrafts[SPECNG_MAX_K + 1];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int K1 = P.K + 1;
-    const int rows = P.B * K1;
-    // chunk-major order: chunk c of every row is scheduled before chunk c + 1,
-    // so later chunks start from the best score the earlier ones published
-    const int c = blockIdx.x / rows;
-    const int row = blockIdx.x - c * rows;
-    const int b = row / K1, j = row - b * K1;
-
-    int kb = P.k[b];
-    if (kb < 0 || kb > P.K) {
-        if (j == 0 && c == 0 && tid == 0) raise_status(P.status, SPECNG_DEV_BAD_K);
-        kb = kb < 0 ? 0 : P.K;
-    }
-    if (j > kb) return;
-    int keff = kb;
-    if (P.gate && kb > 0 && !(P.ema[b] >= P.thresh)) keff = 0;
-    if (j > keff) return;
-
     const bool dense = P.q != nullptr;
-    const int dnext = j < keff ? P.drafts[b * P.K + j] : -1;  // d_{j+1}
-    const bool dvalid = dnext >= 0 && dnext < P.V;
-    if (j < keff && !dvalid && c == 0 && tid == 0) raise_status(P.status, SPECNG_DEV_TOKEN_OOR);
-    const int excl = (!GREEDY && !dense && j < keff && dvalid) ? dnext : -1;
-    const int v0 = c * CHUNK;
-    const int v1 = min(P.V, v0 + CHUNK);
-    const char* rowp = static_cast<const char*>(P.logits) +
-                       static_cast<size_t>(row) * P.V * ElemTraits<BF16>::SIZE;
-    NoiseKey nk = P.nk;
-    nk.seq = static_cast<uint32_t>(b);
 
-    if constexpr (PENALTY) build_window<CHUNK>(P, b, j, v0, v1, s_bm, s_win, &s_nwin);
-
-    // ---- load the chunk into registers (one HBM read of every byte)
-    uint4 raw[kNV];
+    // ---- prologue: count the active row-chunks and find this CTA's range
+    const int per = (P.B + kPThreads - 1) / kPThreads;
+    const int bb0 = tid * per;
+    long long mine = 0;
+    for (int b = bb0; b < bb0 + per && b < P.B; ++b) mine += static_cast<long long>(gate_keff(P, b, nullptr, false) + 1) * P.nchunk;
+    long long incl = mine;
 #pragma unroll
-    for (int i = 0; i < kNV; ++i) {
-        const int e0 = v0 + (i * kThreads + tid) * EPV;
-        raw[i] = e0 < v1 ? load_vec<BF16>(rowp, e0, v1, P.aligned) : make_uint4(0u, 0u, 0u, 0u);
+    for (int off = 1; off < 32; off <<= 1) {
+        const long long o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
     }
+    if (lane == 31) s_wsum[warp] = incl;
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], kCWarps);
+            s_cnt[i] = 0;
+        }
+        for (int i = 0; i <= kStages; ++i) s_rthr[i] = 0u;
+        mbar_init_fence();
+    }
+    __syncthreads();
+    long long base = 0, total = 0;
+    for (int w = 0; w < kPThreads / 32; ++w) {
+        if (w < warp) base += s_wsum[w];
+        total += s_wsum[w];
+    }
+    const long long G = gridDim.x;
+    const long long w0 = total * blockIdx.x / G, w1 = total * (blockIdx.x + 1) / G;
+    const long long ex = base + incl - mine;  // first row-chunk index of my sequences
+    if (w0 < w1 && w0 >= ex && w0 < ex + mine) {
+        long long acc = ex;
+        for (int b = bb0; b < bb0 + per && b < P.B; ++b) {
+            const long long nb = static_cast<long long>(gate_keff(P, b, nullptr, false) + 1) * P.nchunk;
+            if (w0 < acc + nb) {
+                const long long r = w0 - acc;
+                s_start[0] = b;
+                s_start[1] = static_cast<int>(r / P.nchunk);
+                s_start[2] = static_cast<int>(r % P.nchunk);
+                break;
+            }
+            acc += nb;
+        }
+    }
+    __syncthreads();
+    const int nwork = static_cast<int>(w1 - w0);
+    if (nwork <= 0) return;
 
-    // ---- pass A: per-vector maximum of the transformed values
-    float vmax[kNV];
-    float m_t = -INFINITY;
-    int arg_t = -1;
-    Top2 gt = top2_empty();
-#pragma unroll
-    for (int i = 0; i < kNV; ++i) {
-        const int off = (i * kThreads + tid) * EPV;
-        const int e0 = v0 + off;
-        const int nv = min(EPV, v1 - e0);
-        vmax[i] = -INFINITY;
-        if (nv <= 0) continue;
-        float x[EPV];
-        unpack<BF16>(raw[i], x);
-        const unsigned pb = pen_bits<PENALTY, EPV>(s_bm, off);
-        float zm = -INFINITY;
-        int am = -1;
-        if (nv == EPV && pb == 0u) {
-            float mx = x[0];
-            int ax = 0;
-#pragma unroll
-            for (int e = 1; e < EPV; ++e) if (x[e] > mx) { mx = x[e]; ax = e; }
-            zm = SOFTCAP ? transform_f32<true, false>(mx, false, P) : mx;
-            am = ax;
-        } else {
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) {
-                if (e >= nv) break;
-                const float z = transform_f32<SOFTCAP, PENALTY>(x[e], (pb >> e) & 1u, P);
-                if (z > zm || am < 0) { zm = z; am = e; }
+    if (warp == kPWarp) {
+        // ================= producer =================
+        int b = s_start[0], j = s_start[1], c = s_start[2];
+        int kb = 0;
+        int keff = 0;
+        int nh = 0;
+        auto load_seq = [&](int bq) {
+            keff = gate_keff(P, bq, &kb, true);
+            if (lane < keff) {
+                const int d = P.drafts[bq * P.K + lane];
+                s_pdrafts[lane] = d;
+                if (!(d >= 0 && d < P.V)) raise_status(P.status, SPECNG_DEV_TOKEN_OOR);
+            }
+            if constexpr (PENALTY) {
+                int L = P.lens[bq];
+                L = L < 0 ? 0 : (static_cast<int64_t>(L) > P.hist_stride ? static_cast<int>(P.hist_stride) : L);
+                nh = L < P.W ? L : P.W;
+                for (int t = lane; t < nh; t += 32) s_hwin[t] = P.hist[static_cast<size_t>(bq) * P.hist_stride + (L - nh) + t];
+            }
+            __syncwarp();
+        };
+        load_seq(b);
+        bool ok = true;
+        for (int n = 0; n < nwork && ok; ++n) {
+            const int st = n % kStages;
+            const int use = n / kStages;
+            if (use >= 1) ok = mbar_wait_bounded(&s_empty[st], static_cast<unsigned>((use - 1) & 1));
+            if (!ok) { if (lane == 0) raise_status(P.status, SPECNG_DEV_TIMEOUT); break; }
+            const int v0 = c * CHUNK;
+            const int v1 = min(P.V, v0 + CHUNK);
+            if (lane == 0) {
+                int excl = -1;
+                if (!GREEDY && !dense && j < keff) {
+                    const int d = s_pdrafts[j];
+                    if (d >= 0 && d < P.V) excl = d;
+                }
+                s_meta[st] = StageMeta{b, j, c, excl, (c == P.nchunk - 1 || n == nwork - 1) ? 1 : 0};
+            }
+            if constexpr (PENALTY) {
+                const WindowView wv{s_hwin, s_pdrafts, nh, P.W};
+                warp_build_bitmap<CHUNK>(s_bm + st * (CHUNK / 32), wv, j, v0, v1);
+            }
+            __syncwarp();
+            const char* src = static_cast<const char*>(P.logits) +
+                              ((static_cast<size_t>(b) * K1 + j) * P.V + v0) * ElemTraits<BF16>::SIZE;
+            if (P.aligned) {
+                if (lane == 0) {
+                    // the empty barrier already orders the consumers' reads of this stage
+                    // before the copy that overwrites it
+                    mbar_expect_tx(&s_full[st], static_cast<unsigned>(v1 - v0) * ElemTraits<BF16>::SIZE);
+                    bulk_g2s(s_stage + st * SB, src, static_cast<unsigned>(v1 - v0) * ElemTraits<BF16>::SIZE, &s_full[st]);
+                }
+            } else {
+                uint8_t* dst = s_stage + st * SB;
+                for (int e = lane; e < v1 - v0; e += 32) {
+                    if constexpr (BF16) reinterpret_cast<uint16_t*>(dst)[e] = reinterpret_cast<const uint16_t*>(src)[e];
+                    else reinterpret_cast<uint32_t*>(dst)[e] = reinterpret_cast<const uint32_t*>(src)[e];
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_full[st]);
+            }
+            // advance to the next row-chunk
+            if (++c == P.nchunk) {
+                c = 0;
+                if (++j > keff) {
+                    j = 0;
+                    ++b;
+                    if (n + 1 < nwork) load_seq(b);
+                }
             }
         }
-        vmax[i] = zm;
-        if (zm > m_t) { m_t = zm; arg_t = e0 + am; }
+        // the CTA stays resident until every issued copy has landed
+        if (P.aligned && lane == 0) {
+            const int lo = nwork > kStages ? nwork - kStages : 0;
+            for (int n = lo; n < nwork; ++n) mbar_wait_bounded(&s_full[n % kStages], static_cast<unsigned>((n / kStages) & 1));
+        }
+        return;
+    }
+
+    // ================= consumers =================
+    // Per-lane accumulators live across the chunks of one row (a segment of
+    // the CTA's range); warps combine them once, at the segment's last chunk.
+    // The candidate threshold of a segment is shared by the CTA's consumer
+    // warps through a small ring of shared-memory slots (order-preserving
+    // keys, atomicMax): every warp prunes with the best score any warp found.
+    float thr = -INFINITY;
+    float m = -INFINITY, s = 0.0f, msc = 0.0f;
+    Top2 tt = top2_empty();
+    bool fresh = true;
+    int seg = 0;
+    uint16_t* q = s_q + warp * kQCap;
+    if (lane == 0) s_qn[warp] = 0;
+    __syncwarp();
+    for (int n = 0; n < nwork; ++n) {
+        const int st = n % kStages;
+        if (!mbar_wait_bounded(&s_full[st], static_cast<unsigned>((n / kStages) & 1))) {
+            if (lane == 0) raise_status(P.status, SPECNG_DEV_TIMEOUT);
+            break;
+        }
+        const StageMeta mt = s_meta[st];
+        const int row = mt.b * K1 + mt.j;
+        const int j = mt.j;
+        const int excl = mt.excl;
+        const int v0 = mt.c * CHUNK;
+        const int v1 = min(P.V, v0 + CHUNK);
+        const uint4* stage = reinterpret_cast<const uint4*>(s_stage + st * SB);
+        const uint32_t* bm = s_bm + (PENALTY ? st * (CHUNK / 32) : 0);
+        NoiseKey nk = P.nk;
+        nk.seq = static_cast<uint32_t>(mt.b);
+        const int ubase = warp * (32 * kVL);  // first 16-byte vector of my slice
+        unsigned* rth = &s_rthr[seg % (kStages + 1)];
+
         if constexpr (GREEDY) {
-            if (zm >= gt.s2) {
+            // top two transformed values (lower id on ties) within cand_delta of
+            // the best value any warp of the CTA has seen in this segment
+            float gth = fmaxf(tt.s1, key_score(*reinterpret_cast<volatile unsigned*>(rth)));
+            gth = gth > -INFINITY ? gth - cand_delta(gth) : -INFINITY;
+#pragma unroll
+            for (int i = 0; i < kVL; ++i) {
+                const int u = ubase + i * 32 + lane;
+                const int off = u * EPV;
+                const int e0 = v0 + off;
+                const int nv = min(EPV, v1 - e0);
+                if (nv <= 0) continue;
+                const uint4 r = stage[u];
+                const unsigned pb = pen_bits<PENALTY, EPV>(bm, off);
+                if (BF16 && nv == EPV && pb == 0u) {
+                    float vm = bf16x8_max(r);
+                    if constexpr (SOFTCAP) vm = transform_f32<true, false>(vm, false, P);
+                    if (!(vm >= gth)) continue;
+                }
+                float x[EPV];
+                unpack<BF16>(r, x);
 #pragma unroll
                 for (int e = 0; e < EPV; ++e) {
                     if (e >= nv) break;
-                    top2_push(gt, transform_f32<SOFTCAP, PENALTY>(x[e], (pb >> e) & 1u, P), e0 + e);
+                    const float z = transform_f32<SOFTCAP, PENALTY>(x[e], (pb >> e) & 1u, P);
+                    if (z >= gth) top2_push(tt, z, e0 + e);
                 }
+                gth = fmaxf(gth, tt.s1 - cand_delta(tt.s1));
             }
-        }
-    }
-
-    float m_c = -INFINITY, s_c = 0.0f;
-    Top2 tt = top2_empty();
-    if constexpr (!GREEDY) {
-        // ---- threshold seed: exact score of each warp's largest element; the
-        //      best of them over the CTA and of what earlier chunks published
-        {
-            float t0 = -INFINITY;
-            float wm = m_t;
+            if (tt.s1 > -INFINITY) atomicMax(rth, score_key(tt.s1));
+        } else {
+            int seeded = -1;  // element already scored as this lane's seed
+            if (fresh) {
+                // ---- seed: every lane scores the largest element of its slice
+                float zm = -INFINITY;
+                int am = -1;
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, off));
-            const unsigned own = __ballot_sync(0xffffffffu, wm > -INFINITY && m_t == wm && arg_t >= 0 && arg_t != excl);
-            if (own != 0u) {
-                const int src = __ffs(own) - 1;
-                if (lane == src) {
-                    const uint4 w = gumbel_block(nk, static_cast<uint32_t>(arg_t) >> 2, static_cast<uint32_t>(j));
-                    t0 = m_t * P.invT + gumbel_f32(pick_word(w, static_cast<uint32_t>(arg_t) & 3u));
-                }
-                t0 = __shfl_sync(0xffffffffu, t0, src);
-            }
-            if (lane == 0) { s_seed[warp] = t0; s_qn[warp] = 0; }
-        }
-        __syncthreads();
-        float seed = s_seed[0];
-#pragma unroll
-        for (int w = 1; w < kWarps; ++w) seed = fmaxf(seed, s_seed[w]);
-        const float pub = key_score(__ldcg(&P.row_thr[row]));
-        if (tid == 0 && seed > -INFINITY) atomicMax(&P.row_thr[row], score_key(seed));
-        const float best0 = fmaxf(seed, pub);
-        float thr = best0 > -INFINITY ? best0 - cand_delta(best0) : -INFINITY;
-        float zthr = thr - kGumbelMax;  // an element can reach thr only if z / T >= zthr
-        int2* q = s_q + warp * kQCap;
-        volatile int* qn = s_qn + warp;
-
-        // score one queued candidate (all lanes busy); updates tt / thr
-        auto score_one = [&](int2 ent) {
-            const int v = ent.x;
-            const float zb = __int_as_float(ent.y);
-            if (v == excl || zb + kGumbelMax < thr) return;
-            const uint4 w = gumbel_block(nk, static_cast<uint32_t>(v) >> 2, static_cast<uint32_t>(j));
-            const uint32_t word = pick_word(w, static_cast<uint32_t>(v) & 3u);
-            if (zb + gumbel_fast(word) < thr - 1e-3f) return;
-            const float score = zb + gumbel_f32(word);
-            if (score >= thr) {
-                top2_push(tt, score, v);
-                thr = fmaxf(thr, tt.s1 - cand_delta(tt.s1));
-            }
-        };
-
-        // ---- pass B: sum of exponentials; candidates go to the warp's queue
-        const float msc = m_t * P.sc;
-        float s = 0.0f;
-#pragma unroll
-        for (int i = 0; i < kNV; ++i) {
-            const int off = (i * kThreads + tid) * EPV;
-            const int e0 = v0 + off;
-            const int nv = min(EPV, v1 - e0);
-            float z[EPV];
-            if (nv > 0) {
-                float x[EPV];
-                unpack<BF16>(raw[i], x);
-                const unsigned pb = pen_bits<PENALTY, EPV>(s_bm, off);
-                if (nv == EPV) {
-                    float acc = 0.0f;
+                for (int i = 0; i < kVL; ++i) {
+                    const int u = ubase + i * 32 + lane;
+                    const int off = u * EPV;
+                    const int e0 = v0 + off;
+                    const int nv = min(EPV, v1 - e0);
+                    if (nv <= 0) continue;
+                    float x[EPV];
+                    unpack<BF16>(stage[u], x);
+                    const unsigned pb = pen_bits<PENALTY, EPV>(bm, off);
 #pragma unroll
                     for (int e = 0; e < EPV; ++e) {
-                        z[e] = transform_f32<SOFTCAP, PENALTY>(x[e], (pb >> e) & 1u, P);
-                        acc += ex2_approx(fmaf(z[e], P.sc, -msc));
+                        if (e >= nv) break;
+                        const float z = transform_f32<SOFTCAP, PENALTY>(x[e], (pb >> e) & 1u, P);
+                        if (z > zm && e0 + e != excl) { zm = z; am = e0 + e; }
                     }
-                    s += acc;
+                }
+                float t0 = -INFINITY;
+                if (am >= 0) {
+                    const uint4 w = gumbel_block(nk, static_cast<uint32_t>(am) >> 2, static_cast<uint32_t>(j));
+                    t0 = zm * P.invT + gumbel_f32(pick_word(w, static_cast<uint32_t>(am) & 3u));
+                    top2_push(tt, t0, am);
+                    seeded = am;
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, off));
+                if (t0 > -INFINITY) {
+                    thr = t0 - cand_delta(t0);
+                    if (lane == 0) atomicMax(rth, score_key(t0));
+                }
+            }
+            // candidate threshold in raw-logit units: z / T >= thr - g_max  <=>  x >= xt
+            float xt;
+            uint32_t xt2;
+            auto set_xt = [&]() {
+                const float zt = (thr - kGumbelMax) * P.T;
+                if constexpr (SOFTCAP) {
+                    // shrink u by more than the fp32 error of c * tanh(x / c) before inverting:
+                    // atanh is steep near |u| = 1
+                    float u = zt * P.invcap;
+                    u -= 1e-6f * fabsf(u) + 1e-7f;
+                    xt = u > 1.0f ? INFINITY : (u <= -1.0f ? -INFINITY : P.cap * atanhf(fminf(u, 1.0f - 1e-7f)));
                 } else {
+                    xt = zt;
+                }
+                xt -= 1e-5f * (1.0f + fabsf(xt));  // slack for the rounding of the transform
+                xt2 = bf16x2_floor(xt);
+            };
+            // adopt the best score another warp published for this segment
+            auto sync_thr = [&]() {
+                const float best = key_score(*reinterpret_cast<volatile unsigned*>(rth));
+                if (best > -INFINITY) {
+                    const float t1 = best - cand_delta(best);
+                    if (t1 > thr) { thr = t1; set_xt(); }
+                }
+            };
+            set_xt();
+            sync_thr();
+            // score one queued candidate (offset in the chunk; all lanes busy); updates tt / thr
+            const RowPhilox rp = row_philox(nk, static_cast<uint32_t>(j));
+            auto score_one = [&](int loc) {
+                float x;
+                if constexpr (BF16) {
+                    x = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(stage)[loc]) << 16);
+                } else {
+                    x = reinterpret_cast<const float*>(stage)[loc];
+                }
+                const bool pen = PENALTY && ((bm[loc >> 5] >> (loc & 31)) & 1u);
+                const float zb = transform_f32<SOFTCAP, PENALTY>(x, pen, P) * P.invT;
+                const int v = v0 + loc;
+                if (v == excl || zb + kGumbelMax < thr) return;
+                const uint32_t word = pick_word(gumbel_block_row(rp, static_cast<uint32_t>(v) >> 2),
+                                                static_cast<uint32_t>(v) & 3u);
+                if (!gumbel_may_reach(word, thr - zb)) return;
+                const float score = zb + gumbel_f32(word);
+                if (score >= thr) {
+                    top2_push(tt, score, v);
+                    thr = fmaxf(thr, tt.s1 - cand_delta(tt.s1));
+                }
+            };
+            // ---- one pass over the slice: all four 16-byte vectors are loaded first, the
+            //      online maximum and the 32 exponentials form one independent block, the
+            //      candidates of the whole slice are queued once and scored 32 at a time
+            uint4 rv[kVL];
+#pragma unroll
+            for (int i = 0; i < kVL; ++i) rv[i] = stage[ubase + i * 32 + lane];
+            const int off0 = ubase * EPV + lane * EPV;  // chunk offset of vector 0's element 0
+            const bool fast = v0 + (ubase + (kVL - 1) * 32 + lane) * EPV + EPV <= v1;  // four full vectors
+            unsigned pmk = 0u;  // penalised elements of the slice (bit 8 i + e)
+            if constexpr (PENALTY) {
+#pragma unroll
+                for (int i = 0; i < kVL; ++i) pmk |= pen_bits<PENALTY, EPV>(bm, off0 + i * 32 * EPV) << (8 * i);
+            }
+            unsigned msk = 0u;  // bit 8 i + e: element e of vector i
+            if (fast) {
+                float vm = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < kVL; ++i) {
+                    if constexpr (BF16) {
+                        vm = fmaxf(vm, bf16x8_max(rv[i]));
+                    } else {
+                        vm = fmaxf(vm, fmaxf(fmaxf(__uint_as_float(rv[i].x), __uint_as_float(rv[i].y)),
+                                             fmaxf(__uint_as_float(rv[i].z), __uint_as_float(rv[i].w))));
+                    }
+                }
+                if constexpr (SOFTCAP) vm = transform_f32<true, false>(vm, false, P);
+                if (vm > m) {
+                    s = m > -INFINITY ? s * ex2_approx((m - vm) * P.sc) : 0.0f;
+                    m = vm;
+                    msc = m * P.sc;
+                }
+                float acc[kVL];
+#pragma unroll
+                for (int i = 0; i < kVL; ++i) {
+                    float x[EPV];
+                    unpack<BF16>(rv[i], x);
+                    float a = 0.0f;
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) a += ex2_approx(fmaf(transform_f32<SOFTCAP, false>(x[e], false, P), P.sc, -msc));
+                    acc[i] = a;
+                    unsigned mi;
+                    if constexpr (BF16) {
+                        mi = bf16x8_ge_mask(rv[i], xt2);
+                    } else {
+                        mi = 0u;
+#pragma unroll
+                        for (int e = 0; e < EPV; ++e) mi |= static_cast<unsigned>(x[e] >= xt) << e;
+                    }
+                    msk |= mi << (8 * i);
+                }
+                s += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                if constexpr (PENALTY) {
+                    // the few penalised elements: replace their terms by the penalised ones
+                    // (and raise the maximum if a penalty below 1 lifted one above it); they
+                    // are always queued, so scoring sees their exact values
+                    unsigned pw = pmk;
+                    while (pw != 0u) {
+                        const int bit = __ffs(pw) - 1;
+                        pw &= pw - 1u;
+                        const int loc = off0 + (bit >> 3) * 32 * EPV + (bit & 7);
+                        float xe;
+                        if constexpr (BF16) {
+                            xe = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(stage)[loc]) << 16);
+                        } else {
+                            xe = reinterpret_cast<const float*>(stage)[loc];
+                        }
+                        const float zu = transform_f32<SOFTCAP, false>(xe, false, P);
+                        const float zp = transform_f32<SOFTCAP, true>(xe, true, P);
+                        if (zp > m) {
+                            s *= ex2_approx((m - zp) * P.sc);
+                            m = zp;
+                            msc = m * P.sc;
+                        }
+                        s += ex2_approx(fmaf(zp, P.sc, -msc)) - ex2_approx(fmaf(zu, P.sc, -msc));
+                    }
+                    msk |= pmk;
+                }
+            } else {
+                // partial vectors (a row's last chunk): exact transform element by element
+#pragma unroll
+                for (int i = 0; i < kVL; ++i) {
+                    const int off = off0 + i * 32 * EPV;
+                    const int e0 = v0 + off;
+                    const int nv = min(EPV, v1 - e0);
+                    if (nv <= 0) continue;
+                    float x[EPV], z[EPV];
+                    unpack<BF16>(rv[i], x);
+                    const unsigned pb = pen_bits<PENALTY, EPV>(bm, off);
+                    float vm = -INFINITY;
 #pragma unroll
                     for (int e = 0; e < EPV; ++e) {
                         z[e] = transform_f32<SOFTCAP, PENALTY>(x[e], (pb >> e) & 1u, P);
-                        if (e < nv) s += ex2_approx(fmaf(z[e], P.sc, -msc));
+                        if (e < nv) vm = fmaxf(vm, z[e]);
                     }
-                }
-                if (vmax[i] * P.invT >= zthr) {
-                    unsigned msk = 0u;
+                    if (vm > m) {
+                        s = m > -INFINITY ? s * ex2_approx((m - vm) * P.sc) : 0.0f;
+                        m = vm;
+                        msc = m * P.sc;
+                    }
+                    const float zthr = thr - kGumbelMax;
 #pragma unroll
-                    for (int e = 0; e < EPV; ++e)
-                        if (e < nv && z[e] * P.invT >= zthr) msk |= 1u << e;
-                    if (msk != 0u) {
-                        int slot = atomicAdd(&s_qn[warp], __popc(msk));
-#pragma unroll
-                        for (int e = 0; e < EPV; ++e)
-                            if ((msk >> e) & 1u) q[slot++] = make_int2(e0 + e, __float_as_int(z[e] * P.invT));
+                    for (int e = 0; e < EPV; ++e) {
+                        if (e < nv) {
+                            if (m > -INFINITY) s += ex2_approx(fmaf(z[e], P.sc, -msc));
+                            msk |= static_cast<unsigned>(z[e] * P.invT >= zthr) << (8 * i + e);
+                        }
                     }
                 }
             }
-            __syncwarp();
-            int n = *qn;
-            if (n >= 32) {
-                do {
-                    score_one(q[n - 32 + lane]);
-                    n -= 32;
-                } while (n >= 32);
-#pragma unroll
-                for (int off2 = 16; off2 > 0; off2 >>= 1) thr = fmaxf(thr, __shfl_xor_sync(0xffffffffu, thr, off2));
-                zthr = thr - kGumbelMax;
+            if (seeded >= 0) {
+                const int so = seeded - v0 - off0;  // position of the seed in the slice
+                const int si = so / (32 * EPV), se = so - si * 32 * EPV;
+                if (se >= 0 && se < EPV) msk &= ~(1u << (8 * si + se));
+            }
+            // queue the slice's candidates (chunk offsets)
+            const unsigned cnt = __popc(msk);
+            int nq = static_cast<int>(__reduce_add_sync(0xffffffffu, cnt));
+            if (nq != 0) {
+                if (msk != 0u) {
+                    int slot = atomicAdd(&s_qn[warp], static_cast<int>(cnt));
+                    while (msk != 0u) {
+                        const int bit = __ffs(msk) - 1;
+                        msk &= msk - 1u;
+                        q[slot++] = static_cast<uint16_t>(off0 + (bit >> 3) * 32 * EPV + (bit & 7));
+                    }
+                }
                 __syncwarp();
-                if (lane == 0) *qn = n;
+                while (nq >= 32) {
+                    score_one(q[nq - 32 + lane]);
+                    nq -= 32;
+                    // share the warp's best score with the CTA
+                    float bw = tt.s1;
+#pragma unroll
+                    for (int off2 = 16; off2 > 0; off2 >>= 1) bw = fmaxf(bw, __shfl_xor_sync(0xffffffffu, bw, off2));
+                    if (bw > -INFINITY) {
+                        thr = fmaxf(thr, bw - cand_delta(bw));
+                        if (lane == 0) atomicMax(rth, score_key(bw));
+                    }
+                    sync_thr();
+                }
+                if (lane < nq) score_one(q[lane]);
+                __syncwarp();
+                if (lane == 0) s_qn[warp] = 0;
                 __syncwarp();
             }
+            if (tt.s1 > -INFINITY) atomicMax(rth, score_key(tt.s1));
         }
-        {
-            const int n = *qn;
-            if (lane < n) score_one(q[lane]);
-        }
-        if (!(m_t > -INFINITY)) s = 0.0f;
-        // ---- CTA reduction of (max, sum) and candidates
-        m_c = m_t;
-        s_c = s;
+        fresh = mt.seg_end != 0;
+        if (fresh) {
+            // ---- end of this row's segment: one partial for the segment
+            float pm = m, ps = s;
+            Top2 pt = tt;
+            if constexpr (!GREEDY) {
+                if (!(pm > -INFINITY)) ps = 0.0f;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float mo = __shfl_xor_sync(0xffffffffu, m_c, off);
-            const float so = __shfl_xor_sync(0xffffffffu, s_c, off);
-            ms_merge(m_c, s_c, mo, so, P.sc);
-        }
-        tt = top2_warp_reduce(tt);
-    } else {
-        tt = top2_warp_reduce(gt);
-    }
-    if (lane == 0) { s_m[warp] = m_c; s_s[warp] = s_c; s_t[warp] = tt; }
-    __syncthreads();
-    if (warp == 0) {
-        float m = lane < kWarps ? s_m[lane] : -INFINITY;
-        float s = lane < kWarps ? s_s[lane] : 0.0f;
-        Top2 t = lane < kWarps ? s_t[lane] : top2_empty();
+                for (int off = 16; off > 0; off >>= 1) {
+                    const float mo = __shfl_xor_sync(0xffffffffu, pm, off);
+                    const float so = __shfl_xor_sync(0xffffffffu, ps, off);
+                    ms_merge(pm, ps, mo, so, P.sc);
+                }
+            }
+            pt = top2_warp_reduce(pt);
+            int last = 0;
+            if (lane == 0) {
+                s_slot[st][warp] = WarpPart{pm, ps, pt};
+                __threadfence_block();
+                last = atomicAdd(&s_cnt[st], 1) == kCWarps - 1;
+            }
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (last) {
+                __threadfence_block();
+                WarpPart wp = lane < kCWarps ? s_slot[st][lane] : WarpPart{-INFINITY, 0.0f, top2_empty()};
+                float cm = wp.m, cs = wp.s;
+                Top2 ct = wp.t;
 #pragma unroll
-        for (int off = 4; off > 0; off >>= 1) {
-            const float mo = __shfl_xor_sync(0xffffffffu, m, off);
-            const float so = __shfl_xor_sync(0xffffffffu, s, off);
-            ms_merge(m, s, mo, so, P.sc);
-            t = top2_merge(t, top2_shfl_xor(t, off));
+                for (int off = 16; off > 0; off >>= 1) {
+                    const float mo = __shfl_xor_sync(0xffffffffu, cm, off);
+                    const float so = __shfl_xor_sync(0xffffffffu, cs, off);
+                    ms_merge(cm, cs, mo, so, P.sc);
+                    ct = top2_merge(ct, top2_shfl_xor(ct, off));
+                }
+                if (lane == 0) {
+                    // keyed by the segment's last chunk; a written partial is never all-zero
+                    st_partial(P.part + static_cast<size_t>(row) * P.nchunk + mt.c, GREEDY ? 0.0f : cm,
+                               GREEDY ? 1.0f : cs, ct);
+                    s_cnt[st] = 0;
+                    *rth = 0u;  // every warp is past this segment: the slot is free
+                }
+            }
+            m = -INFINITY;
+            s = 0.0f;
+            msc = 0.0f;
+            tt = top2_empty();
+            thr = -INFINITY;
+            ++seg;
         }
-        if (lane == 0) {
-            st_partial(P.part + static_cast<size_t>(row) * P.nchunk + c, m, s, t);
-            if (!GREEDY && t.s1 > -INFINITY) atomicMax(&P.row_thr[row], score_key(t.s1));
-            __threadfence();
-            const unsigned prev = atomicAdd(&P.row_ticket[row], 1u);
-            s_last = prev == static_cast<unsigned>(P.nchunk - 1);
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_empty[st]);
     }
-    __syncthreads();
-    if (!s_last || warp != 0) return;
-    __threadfence();
+}
 
-    // ---- last CTA of the row: merge the chunks (warp 0)
-    if (lane == 0) { P.row_ticket[row] = 0u; P.row_thr[row] = 0u; }
-    const Partial* pr = P.part + static_cast<size_t>(row) * P.nchunk;
-    double M = -INFINITY;
-    for (int cc = lane; cc < P.nchunk; cc += 32) M = fmax(M, static_cast<double>(__ldcg(&pr[cc].m)));
-    M = warp_max_f64(M);
+// ---------------------------------------------------------------- K3
+// One warp per row: combine the row's chunk partials (log-sum-exp, sampled
+// candidate), run the accept test of the draft it verifies; the last row of
+// a sequence to finish runs the epilogue (tokens, kv_len, EMA).
+
+template <bool BF16, bool GREEDY, bool SOFTCAP, bool PENALTY>
+__global__ void __launch_bounds__(256) verify_merge_kernel(const VerifyDev P) {
+    const int lane = threadIdx.x & 31;
+    const int K1 = P.K + 1;
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (row >= P.B * K1) return;
+    const int b = row / K1, j = row - b * K1;
+    int kb;
+    const int keff = gate_keff(P, b, &kb, false);
+    if (j > keff) return;
+    const bool dense = P.q != nullptr;
+    NoiseKey nk = P.nk;
+    nk.seq = static_cast<uint32_t>(b);
+    int nh = 0, L = 0;
+    if constexpr (PENALTY) {
+        L = P.lens[b];
+        L = L < 0 ? 0 : (static_cast<int64_t>(L) > P.hist_stride ? static_cast<int>(P.hist_stride) : L);
+        nh = L < P.W ? L : P.W;
+    }
+    const WindowView wv{PENALTY ? P.hist + static_cast<size_t>(b) * P.hist_stride + (L - nh) : nullptr,
+                        P.drafts + static_cast<size_t>(b) * P.K, nh, PENALTY ? P.W : 0};
+
+    // one partial per row segment, stored at the segment's last chunk; the
+    // other slots are all-zero (a written partial never is)
+    Partial* pr = P.part + static_cast<size_t>(row) * P.nchunk;
+    float mf = -INFINITY;
+    for (int cc = lane; cc < P.nchunk; cc += 32) {
+        const Partial p = ldcg_partial(pr + cc);
+        if (p.s != 0.0f || __float_as_uint(p.m) != 0u) mf = fmaxf(mf, p.m);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mf = fmaxf(mf, __shfl_xor_sync(0xffffffffu, mf, off));
     double S = 0.0;
     Top2 t = top2_empty();
     for (int cc = lane; cc < P.nchunk; cc += 32) {
         const Partial p = ldcg_partial(pr + cc);
-        if (!GREEDY && p.m > -INFINITY) S += static_cast<double>(p.s) * exp((static_cast<double>(p.m) - M) / P.Td);
+        if (p.s == 0.0f && __float_as_uint(p.m) == 0u) continue;
+        if (!GREEDY && p.m > -INFINITY) S += static_cast<double>(p.s) * static_cast<double>(expf((p.m - mf) * P.invT));
         t = top2_merge(t, p.t);
     }
     S = warp_sum_f64(S);
     t = top2_warp_reduce(t);
-    // leave the workspace zeroed for the next call (any shape may reuse it)
     __syncwarp();
-    for (int cc = lane; cc < P.nchunk; cc += 32) st_zero(const_cast<Partial*>(pr) + cc);
-    const double lse = GREEDY ? 0.0 : M / P.Td + log(S);
-    if (!GREEDY && !(S > 0.0 && S < INFINITY && M < INFINITY) && lane == 0)
+    for (int cc = lane; cc < P.nchunk; cc += 32) st_zero(pr + cc);  // leave the workspace zeroed
+    const double lse = GREEDY ? 0.0 : static_cast<double>(mf) / P.Td + log(S);
+    if (!GREEDY && !(S > 0.0 && S < INFINITY && mf < INFINITY) && lane == 0)
         raise_status(P.status, SPECNG_DEV_NONFINITE);
 
-    // fp64 re-score of the (up to) two candidates from the raw logits
-    const int nw = PENALTY ? s_nwin : 0;
-    const bool pen1 = PENALTY && t.i1 >= 0 ? warp_in_window(t.i1, s_win, nw) : false;
-    const bool pen2 = PENALTY && t.i2 >= 0 ? warp_in_window(t.i2, s_win, nw) : false;
+    // winner: fp32 order unless the two best are within the fp32 error, then fp64
     int winner = t.i1;
-    if (lane == 0 && t.i1 >= 0) {
-        const bool second = t.i2 >= 0 && t.s2 >= t.s1 - cand_delta(t.s1);
-        double sc1, sc2 = -INFINITY;
-        {
-            const double z = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, t.i1), pen1, P);
-            if constexpr (GREEDY) {
-                sc1 = z;
-            } else {
-                const uint4 w = gumbel_block(nk, static_cast<uint32_t>(t.i1) >> 2, static_cast<uint32_t>(j));
-                sc1 = z / P.Td + gumbel_f64(pick_word(w, static_cast<uint32_t>(t.i1) & 3u));
+    const bool close = t.i2 >= 0 && t.s2 >= t.s1 - cand_delta(t.s1);
+    if (close) {
+        const bool pen1 = PENALTY ? wv.warp_has(j, t.i1) : false;
+        const bool pen2 = PENALTY ? wv.warp_has(j, t.i2) : false;
+        if (lane == 0) {
+            double sc[2];
+            for (int h = 0; h < 2; ++h) {
+                const int id = h == 0 ? t.i1 : t.i2;
+                const double z = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, id),
+                                                                 h == 0 ? pen1 : pen2, P);
+                if constexpr (GREEDY) {
+                    sc[h] = z;
+                } else {
+                    const uint4 w = gumbel_block(nk, static_cast<uint32_t>(id) >> 2, static_cast<uint32_t>(j));
+                    sc[h] = z / P.Td + gumbel_f64(pick_word(w, static_cast<uint32_t>(id) & 3u));
+                }
             }
+            if (better64(sc[1], t.i2, sc[0], t.i1)) winner = t.i2;
         }
-        if (second) {
-            const double z = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, t.i2), pen2, P);
-            if constexpr (GREEDY) {
-                sc2 = z;
-            } else {
-                const uint4 w = gumbel_block(nk, static_cast<uint32_t>(t.i2) >> 2, static_cast<uint32_t>(j));
-                sc2 = z / P.Td + gumbel_f64(pick_word(w, static_cast<uint32_t>(t.i2) & 3u));
-            }
-            if (better64(sc2, t.i2, sc1, t.i1)) winner = t.i2;
-        }
+        winner = __shfl_sync(0xffffffffu, winner, 0);
     }
-    winner = __shfl_sync(0xffffffffu, winner, 0);
 
-    // accept test of the draft this row verifies, in fp64
+    // accept test of d_{j+1}: fp32 unless within 1e-4 of the boundary, then fp64
     int accepted = 0;
-    if (j < keff && dvalid) {
+    const int dnext = j < keff ? wv.drafts[j] : -1;
+    if (j < keff && dnext >= 0 && dnext < P.V) {
         if constexpr (GREEDY) {
             accepted = dnext == winner;
         } else {
-            const bool pend = PENALTY ? warp_in_window(dnext, s_win, nw) : false;
+            const bool pend = PENALTY ? wv.warp_has(j, dnext) : false;
             if (lane == 0) {
-                const double zd = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, dnext), pend, P);
-                const double p = exp(zd / P.Td - lse);
-                const double q = dense ? static_cast<double>(P.q[(static_cast<size_t>(b) * P.K + j) * P.V + dnext]) : 1.0;
                 const double u = accept_uniform_f64(nk, static_cast<uint32_t>(j + 1));
-                accepted = u * q <= p;
+                const double q = dense ? static_cast<double>(P.q[(static_cast<size_t>(b) * P.K + j) * P.V + dnext]) : 1.0;
+                const float xd = static_cast<float>(raw_logit_f64<BF16>(P.logits, row, P.V, dnext));
+                const float lp = transform_f32<SOFTCAP, PENALTY>(xd, pend, P) * P.invT - static_cast<float>(lse);
+                const float lr = logf(static_cast<float>(u)) + logf(static_cast<float>(q));
+                if (lr < lp - 1e-4f * (1.0f + fabsf(lp))) {
+                    accepted = 1;
+                } else if (lr > lp + 1e-4f * (1.0f + fabsf(lp))) {
+                    accepted = 0;
+                } else {
+                    const double zd = transform_f64<SOFTCAP, PENALTY>(static_cast<double>(xd), pend, P);
+                    accepted = u * q <= exp(zd / P.Td - lse);
+                }
             }
             accepted = __shfl_sync(0xffffffffu, accepted, 0);
         }
@@ -612,21 +1019,21 @@ __global__ void __launch_bounds__(kThreads, 2) verify_stream_kernel(const Verify
     if (!last_row) return;
     __threadfence();
 
-    // ---- last row of the sequence: epilogue (warp 0)
+    // ---- last row of the sequence: epilogue
     if (lane == 0) P.seq_ticket[b] = 0u;
-    const RowRes* rs = P.rowres + static_cast<size_t>(b) * K1;
+    RowRes* rs = P.rowres + static_cast<size_t>(b) * K1;
     int acc = 1;
     if (lane < keff) acc = __ldcg(&rs[lane].accepted);
     const unsigned rej = __ballot_sync(0xffffffffu, lane < keff && !acc);
     const int a = rej ? __ffs(rej) - 1 : keff;
     // a rejected draft outside [0, V) leaves the residual equal to p: the
     // row's own candidate (over all ids) is then the sample
-    const int da = a < keff ? P.drafts[b * P.K + a] : -1;
+    const int da = a < keff ? wv.drafts[a] : -1;
     const bool need = dense && !GREEDY && a < keff && da >= 0 && da < P.V;
     const int y = need ? -1 : __ldcg(&rs[a].winner);
     __syncwarp();
-    if (lane <= keff && !(need && lane == a)) st_zero(const_cast<RowRes*>(rs) + lane);
-    if (lane < K1) P.out_tokens[static_cast<size_t>(b) * K1 + lane] = lane < a ? P.drafts[b * P.K + lane] : (lane == a ? y : -1);
+    if (lane <= keff && !(need && lane == a)) st_zero(rs + lane);
+    if (lane < K1) P.out_tokens[static_cast<size_t>(b) * K1 + lane] = lane < a ? wv.drafts[lane] : (lane == a ? y : -1);
     if (lane == 0) {
         P.out_accept[b] = a;
         P.kv_len[b] = P.kv_len[b] - kb + a;
