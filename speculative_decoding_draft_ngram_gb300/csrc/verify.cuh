@@ -221,6 +221,10 @@ __device__ __forceinline__ float key_score(unsigned k) {
     return (k & 0x80000000u) ? __uint_as_float(k & 0x7FFFFFFFu) : __uint_as_float(~k);
 }
 
+__device__ __forceinline__ unsigned warp_best_key(float best) {
+    return __reduce_max_sync(0xffffffffu, best > -INFINITY ? score_key(best) : 0u);
+}
+
 // Gumbel variate from a Philox word with hardware log2 (error ~1e-5): a
 // pre-filter only; candidates that pass it are re-scored with gumbel_f32.
 __device__ __forceinline__ float gumbel_fast(uint32_t w) {
@@ -612,7 +616,8 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                 }
                 gth = fmaxf(gth, tt.s1 - cand_delta(tt.s1));
             }
-            if (tt.s1 > -INFINITY) atomicMax(rth, score_key(tt.s1));
+            const unsigned kw = warp_best_key(tt.s1);
+            if (lane == 0 && kw != 0u) atomicMax(rth, kw);
         } else {
             int seeded = -1;  // element already scored as this lane's seed
             if (fresh) {
@@ -643,11 +648,11 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                     top2_push(tt, t0, am);
                     seeded = am;
                 }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) t0 = fmaxf(t0, __shfl_xor_sync(0xffffffffu, t0, off));
-                if (t0 > -INFINITY) {
+                const unsigned k0 = warp_best_key(t0);
+                if (k0 != 0u) {
+                    t0 = key_score(k0);
                     thr = t0 - cand_delta(t0);
-                    if (lane == 0) atomicMax(rth, score_key(t0));
+                    if (lane == 0) atomicMax(rth, k0);
                 }
             }
             // candidate threshold in raw-logit units: z / T >= thr - g_max  <=>  x >= xt
@@ -830,12 +835,11 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                     score_one(q[nq - 32 + lane]);
                     nq -= 32;
                     // share the warp's best score with the CTA
-                    float bw = tt.s1;
-#pragma unroll
-                    for (int off2 = 16; off2 > 0; off2 >>= 1) bw = fmaxf(bw, __shfl_xor_sync(0xffffffffu, bw, off2));
-                    if (bw > -INFINITY) {
+                    const unsigned kb = warp_best_key(tt.s1);
+                    if (kb != 0u) {
+                        const float bw = key_score(kb);
                         thr = fmaxf(thr, bw - cand_delta(bw));
-                        if (lane == 0) atomicMax(rth, score_key(bw));
+                        if (lane == 0) atomicMax(rth, kb);
                     }
                     sync_thr();
                 }
@@ -844,7 +848,8 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                 if (lane == 0) s_qn[warp] = 0;
                 __syncwarp();
             }
-            if (tt.s1 > -INFINITY) atomicMax(rth, score_key(tt.s1));
+            const unsigned kw = warp_best_key(tt.s1);
+            if (lane == 0 && kw != 0u) atomicMax(rth, kw);
         }
         fresh = mt.seg_end != 0;
         if (fresh) {
