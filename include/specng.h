@@ -76,6 +76,7 @@ extern "C" {
 #define SPECNG_NGRAM_MAX_B    512       /* sequences per n-gram table              */
 #define SPECNG_NGRAM_MAX_V    262144    /* vocabulary of an n-gram table (2^18)    */
 #define SPECNG_NGRAM_MAX_POS  16777216  /* positions per sequence in a table (2^24) */
+#define SPECNG_STATIC_SCRATCH_BYTES 4194304  /* scratch of spec_verify_noalloc (4 MiB) */
 
 /* ------------------------------------------------------------------------
  * N-gram table  [AX]: "builds bigram/trigram tables at runtime, predicts up
@@ -203,6 +204,38 @@ int spec_verify(const void* logits, int logits_dtype, int B, int K, int V,
                 int32_t* kv_len, float* ema,
                 int32_t* out_tokens, int32_t* out_accept_len,
                 void* workspace, size_t workspace_bytes, cudaStream_t s);
+
+/* spec_verify without a caller workspace.  The pages have no counterpart of
+ * this call: it is an interface addition, for callers that cannot allocate
+ * device memory where they verify -- a runtime whose allocator reserved the
+ * device's memory up front and refuses requests while decoding, or a decode
+ * loop that must not stall on cudaMalloc / cudaFree (both synchronise the
+ * device) and has no buffer of its own to lend.
+ *
+ * Arguments, results, launches and errors as for spec_verify, minus the
+ * workspace.  The scratch is a static device array of
+ * SPECNG_STATIC_SCRATCH_BYTES inside the library, one per device; the call
+ * allocates nothing (no cudaMalloc / cudaFree, no allocating library
+ * routine).
+ *   - Limit: spec_verify_workspace_bytes(B, K, V) must not exceed
+ *     SPECNG_STATIC_SCRATCH_BYTES (e.g. B = 512, K = 4, V = 262144 fits);
+ *     a larger shape returns SPECNG_ESMALL, with the sizes in
+ *     specng_last_error(), and nothing is enqueued.  spec_verify with a
+ *     caller workspace has no such limit.
+ *   - Each call first zero-fills the part of the scratch it uses
+ *     (cudaMemsetAsync on s), then enqueues the verify kernels on s.
+ *   - The first call on a device looks the scratch address up
+ *     (cudaGetSymbolAddress) and caches it; make that first call before any
+ *     stream capture starts on that device.
+ *   - All calls on one device share the scratch: calls whose executions
+ *     overlap (unordered streams, or several host threads) race and give
+ *     wrong results.  Order them, e.g. on one stream. */
+int spec_verify_noalloc(const void* logits, int logits_dtype, int B, int K, int V,
+                        const int32_t* drafts, const float* draft_probs, const int32_t* k,
+                        const int32_t* history, int64_t hist_stride, const int32_t* lens,
+                        const specng_verify_params* params,
+                        int32_t* kv_len, float* ema,
+                        int32_t* out_tokens, int32_t* out_accept_len, cudaStream_t s);
 
 /* Append the emitted tokens: history[b, lens_b + t] = out_tokens[b, t] for
  * t <= out_accept_len[b], then lens_b += out_accept_len[b] + 1.  A sequence

@@ -19,6 +19,7 @@ from .capi import (  # noqa: F401
     philox4x32_10,
     spec_append,
     spec_verify,
+    spec_verify_noalloc,
     spec_verify_workspace,
     spec_verify_workspace_bytes,
     status_names,

@@ -35,8 +35,8 @@ STATUS_BITS = {
 EXPORTED = (
     "specng_ngram_create", "specng_ngram_destroy", "specng_ngram_reset", "specng_ngram_capacity",
     "ngram_update", "ngram_draft", "spec_verify_workspace_bytes", "spec_verify_workspace_init",
-    "spec_verify", "spec_append", "specng_get_status", "specng_strerror", "specng_last_error",
-    "specng_philox4x32_10",
+    "spec_verify", "spec_verify_noalloc", "spec_append", "specng_get_status", "specng_strerror",
+    "specng_last_error", "specng_philox4x32_10",
 )
 
 
@@ -106,6 +106,8 @@ def load() -> ctypes.CDLL:
         "spec_verify_workspace_init": (I, [P, SZ, P]),
         "spec_verify": (I, [P, I, I, I, I, P, P, P, P, I64, P, ctypes.POINTER(VerifyParamsC),
                             P, P, P, P, P, SZ, P]),
+        "spec_verify_noalloc": (I, [P, I, I, I, I, P, P, P, P, I64, P, ctypes.POINTER(VerifyParamsC),
+                                    P, P, P, P, P]),
         "spec_append": (I, [P, I64, P, I64, P, P, I, I, P]),
         "specng_get_status": (I, [ctypes.POINTER(ctypes.c_uint32), I]),
         "specng_strerror": (ctypes.c_char_p, [I]),
@@ -240,6 +242,35 @@ def spec_verify(logits: torch.Tensor, drafts: Optional[torch.Tensor], draft_prob
         _ptr(out_tokens, torch.int32, "out_tokens"), _ptr(out_accept_len, torch.int32, "out_accept_len"),
         _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
         _stream(logits.device)), "spec_verify")
+
+
+def spec_verify_noalloc(logits: torch.Tensor, drafts: Optional[torch.Tensor], draft_probs: Optional[torch.Tensor],
+                        k: torch.Tensor, history: Optional[torch.Tensor], lens: Optional[torch.Tensor],
+                        params: VerifyParams, kv_len: torch.Tensor, ema: torch.Tensor, out_tokens: torch.Tensor,
+                        out_accept_len: torch.Tensor):
+    """spec_verify on the library's static scratch (no workspace, nothing allocated).
+
+    For callers that cannot allocate device memory where they verify; shapes
+    are limited to spec_verify_workspace_bytes(B, K, V) <= 4 MiB, and calls
+    on one device must not overlap (they share the scratch)."""
+    if logits.dim() != 3:
+        raise SpecngError("logits must be [B, K+1, V]")
+    B, K1, V = logits.shape
+    if logits.dtype == torch.bfloat16:
+        dt = SPECNG_BF16
+    elif logits.dtype == torch.float32:
+        dt = SPECNG_F32
+    else:
+        raise SpecngError(f"logits dtype {logits.dtype} unsupported (bfloat16 or float32)")
+    pc = params.to_c()
+    _check(load().spec_verify_noalloc(
+        _ptr(logits, None, "logits"), dt, B, K1 - 1, V,
+        _ptr(drafts, torch.int32, "drafts"), _ptr(draft_probs, torch.float32, "draft_probs"),
+        _ptr(k, torch.int32, "k"), _ptr(history, torch.int32, "history"),
+        history.shape[1] if history is not None else 0, _ptr(lens, torch.int32, "lens"),
+        ctypes.byref(pc), _ptr(kv_len, torch.int32, "kv_len"), _ptr(ema, torch.float32, "ema"),
+        _ptr(out_tokens, torch.int32, "out_tokens"), _ptr(out_accept_len, torch.int32, "out_accept_len"),
+        _stream(logits.device)), "spec_verify_noalloc")
 
 
 def spec_append(history: torch.Tensor, lens: torch.Tensor, out_tokens: torch.Tensor,

@@ -12,6 +12,11 @@ namespace specng {
 
 __device__ unsigned g_status_word;
 
+// Scratch of spec_verify_noalloc: part of the library's device image, one
+// per device, so that callers without an allocator (see the header) can
+// verify.  Each call zero-fills the part it uses before its kernels run.
+static __device__ __align__(256) unsigned char g_verify_scratch[SPECNG_STATIC_SCRATCH_BYTES];
+
 namespace {
 
 thread_local char g_last_error[256] = "";
@@ -36,6 +41,21 @@ unsigned* status_ptr() {
     if (ptrs[dev] == nullptr) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_status_word) == cudaSuccess) ptrs[dev] = static_cast<unsigned*>(p);
+    }
+    return ptrs[dev];
+}
+
+// Device address of the static verify scratch, looked up once per device
+// (the lookup may load the module, so it belongs to set-up, before capture).
+void* static_scratch_ptr() {
+    static std::mutex mu;
+    static void* ptrs[128] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (ptrs[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_verify_scratch) == cudaSuccess) ptrs[dev] = p;
     }
     return ptrs[dev];
 }
@@ -306,6 +326,27 @@ int spec_verify(const void* logits, int logits_dtype, int B, int K, int V, const
                                : launch_verify_dtype<false>(P, greedy, softcap, penalty, dense, s);
     if (e != cudaSuccess) return fail_cuda(e, "spec_verify");
     return SPECNG_OK;
+}
+
+int spec_verify_noalloc(const void* logits, int logits_dtype, int B, int K, int V, const int32_t* drafts,
+                        const float* draft_probs, const int32_t* k, const int32_t* history, int64_t hist_stride,
+                        const int32_t* lens, const specng_verify_params* params, int32_t* kv_len, float* ema,
+                        int32_t* out_tokens, int32_t* out_accept_len, cudaStream_t s) {
+    const size_t need = spec_verify_workspace_bytes(B, K, V);
+    if (need == 0) return fail(SPECNG_EINVAL, "spec_verify_noalloc: B, K or V out of range");
+    if (need > static_cast<size_t>(SPECNG_STATIC_SCRATCH_BYTES)) {
+        std::snprintf(g_last_error, sizeof(g_last_error),
+                      "spec_verify_noalloc: B=%d K=%d V=%d needs %zu bytes of scratch but the static scratch "
+                      "holds %d; call spec_verify with a workspace instead", B, K, V, need,
+                      SPECNG_STATIC_SCRATCH_BYTES);
+        return SPECNG_ESMALL;
+    }
+    void* scratch = static_scratch_ptr();
+    if (scratch == nullptr) return fail(SPECNG_ECUDA, "spec_verify_noalloc: scratch address lookup failed");
+    const cudaError_t e = cudaMemsetAsync(scratch, 0, need, s);
+    if (e != cudaSuccess) return fail_cuda(e, "spec_verify_noalloc");
+    return spec_verify(logits, logits_dtype, B, K, V, drafts, draft_probs, k, history, hist_stride, lens, params,
+                       kv_len, ema, out_tokens, out_accept_len, scratch, SPECNG_STATIC_SCRATCH_BYTES, s);
 }
 
 int spec_append(int32_t* history, int64_t hist_stride, int32_t* lens, int64_t hist_cap, const int32_t* out_tokens,
