@@ -71,6 +71,24 @@ def dist_env():
     return ws, rank, local
 
 
+def rank_config(name: str, steps_total: int, rank: int, batch: int = 0) -> wl.Config:
+    """The workload of one rank: same shapes on every rank, its own data and
+    sampler seeds (weak scaling: each rank verifies an independent batch)."""
+    cfg = wl.get(name)
+    return wl.get(name, steps=max(cfg.steps, steps_total), data_seed=cfg.data_seed + 7919 * rank,
+                  sampler_seed=cfg.sampler_seed + rank, B=batch or cfg.B)
+
+
+def max_over_ranks(x: float, device) -> float:
+    """Maximum of a per-rank value over all ranks (x itself on one rank)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -177,9 +195,7 @@ class Path:
     def __init__(self, name, steps_total, device, seed_offset=0, batch=0):
         import speculative_decoding_draft_ngram_gb300 as sp
         self.sp = sp
-        cfg = wl.get(name)
-        cfg = wl.get(name, steps=max(cfg.steps, steps_total), data_seed=cfg.data_seed + 7919 * seed_offset,
-                     sampler_seed=cfg.sampler_seed + seed_offset, B=batch or cfg.B)
+        cfg = rank_config(name, steps_total, seed_offset, batch)
         self.cfg = cfg
         self.dev = device
         B, K, V = cfg.B, cfg.K, cfg.V
@@ -328,11 +344,7 @@ def run_ours(args):
     rows_read = path.rows_read(base + args.steps) - path.rows_read(base)
     vbytes = path.verify_bytes(base + args.steps) - path.verify_bytes(base)
     rows_nominal = args.steps * cfg.B * (cfg.K + 1)
-    ms_max = ms
-    if ws > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms, dev)
     status = sp.get_status(clear=True)
 
     # ---- end to end: host logits -> device, step, results -> host
@@ -357,11 +369,7 @@ def run_ours(args):
             acc_h.copy_(path.acc, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize()
-        ems = e0.elapsed_time(e1)
-        if ws > 1:
-            t = torch.tensor([ems], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ems = float(t.item())
+        ems = max_over_ranks(e0.elapsed_time(e1), dev)
         e2e = {"value": ws * e2e_steps * cfg.B * (cfg.K + 1) / (ems / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": int(dbuf.numel() * dbuf.element_size()),
                "d2h_bytes_per_step": int(out_h.numel() * 4 + acc_h.numel() * 4), "steps": e2e_steps,

@@ -193,7 +193,9 @@ int spec_verify_workspace_init(void* workspace, size_t workspace_bytes, cudaStre
  * by Gumbel-max with Philox noise keyed by (seed; vocab id, row, step,
  * sequence).  T = 0: accept iff d_i is its row's argmax (lowest id on
  * ties); the emitted token is the argmax of row a.
- * Launches: one kernel (point-mass drafts or T = 0), two with dense q.
+ * Launches: two kernels (the streaming pass over the rows, then a per-row
+ * merge that also runs each sequence's epilogue); three with dense q at
+ * T > 0 (a residual pass over row a of the rejected sequences).
  * Requirements: logits 16-byte aligned for the vectorised path (any
  * alignment works, slower); B in [1, 2^20]; K in [0, 16]; V in [1, 2^30].
  * Errors: EINVAL, ESMALL, ECUDA.  Device: NONFINITE, TOKEN_OOR, BAD_K. */

@@ -64,6 +64,132 @@ def oracle_verify(logits, drafts, q, k, hist, lens, params, kv, ema, chunk=16):
     return {key: np.concatenate([p[key] for p in parts]) for key in parts[0]}
 
 
+def compare(step, a_g, t_g, kv_gh, ema_gh, res, rep: Report, ids=None):
+    """Compare one step's GPU outputs with the oracle's (rows of the same
+    sequences); raise on a mismatch that the margin rule does not excuse.
+    Returns the mask of (excused) mismatching sequences."""
+    a_o = res["accept_len"]
+    t_o = res["out_tokens"]
+    bad = (a_g != a_o) | (t_g != t_o).any(axis=1) | (kv_gh != res["kv_len"]) | \
+          (np.abs(ema_gh - res["ema"]) > EMA_TOL)
+    for b in np.nonzero(bad)[0]:
+        excusable = False
+        if a_g[b] != a_o[b]:
+            i = min(a_g[b], a_o[b])
+            excusable = res["accept_margin"][b, i] < MARGIN
+        elif (t_g[b] != t_o[b]).any():
+            excusable = res["sample_margin"][b] < MARGIN
+        if res["ema_margin"][b] < EMA_TOL:
+            excusable = True
+        sb = b if ids is None else int(ids[b])
+        msg = (f"step {step} seq {sb}: gpu a={a_g[b]} tok={t_g[b].tolist()} kv={kv_gh[b]} ema={ema_gh[b]!r}; "
+               f"oracle a={a_o[b]} tok={t_o[b].tolist()} kv={res['kv_len'][b]} ema={res['ema'][b]!r} "
+               f"acc_margin={res['accept_margin'][b].tolist()} sample_margin={res['sample_margin'][b]!r}")
+        assert excusable, "parity failure: " + msg
+        rep.excused += 1
+        rep.notes.append(msg)
+    return bad
+
+
+def run_sampled(cfg: wl.Config, steps: int, sample: int, T: float | None = None, device="cuda",
+                seed: int | None = None) -> Report:
+    """Full-size steps on the GPU (the whole batch, in the launch configuration
+    the benchmark uses); the oracle checks a seeded sample of ``sample``
+    sequences one by one (sequences are independent; their Philox streams are
+    keyed by their own index)."""
+    T = cfg.temperature if T is None else T
+    seed = cfg.sampler_seed if seed is None else seed
+    rep = Report()
+    B, K, V = cfg.B, cfg.K, cfg.V
+    hist_full, lens_full = wl.histories(cfg, "cpu")
+    ids = np.sort(np.random.default_rng(cfg.data_seed).choice(B, size=min(sample, B), replace=False))
+    hist_o = hist_full.numpy()[ids].astype(np.int64)
+    lens_o = lens_full.numpy()[ids].astype(np.int64)
+    hist_g = hist_full.to(device)
+    lens_g = lens_full.to(device)
+    ema_o = np.ones(len(ids), dtype=np.float64)
+    ema_g = torch.ones(B, dtype=torch.float32, device=device)
+    kv_g = lens_g.clone()
+    use_ngram = not cfg.dense
+    table = stats = None
+    if use_ngram:
+        table = sp.NgramTable(B, V, B * cfg.hist_cap, device=device)
+        sp.ngram_update(table, hist_g, lens_g)
+        stats = [on.continuation_stats(hist_o[i], int(lens_o[i])) for i in range(len(ids))]
+    ws = sp.spec_verify_workspace(B, K, V, device)
+    out_tok = torch.empty((B, K + 1), dtype=torch.int32, device=device)
+    out_acc = torch.empty((B,), dtype=torch.int32, device=device)
+    g = wl._gen(cfg.data_seed + 1, "cpu")
+    bprob = wl.boost_probs(cfg, "cpu")
+    zcdf = wl.zipf_cdf(cfg.zipf_ids or cfg.V, cfg.zipf_s)
+    sp.get_status(clear=True)
+    for step in range(steps):
+        limits = wl.draft_limits(cfg, g, "cpu")
+        fb = wl.fallback_drafts(cfg, g, "cpu", zcdf)
+        logits = wl.step_logits(cfg, g, device="cpu")
+        if use_ngram:
+            d_g, k_g = sp.ngram_draft(table, hist_g, lens_g, K, k_limit=limits.to(device),
+                                      fallback=None if fb is None else fb.to(device))
+            d_o, k_o = on.draft_batch(hist_o, lens_o, K, k_limit=limits.numpy()[ids], stats=stats,
+                                      fallback=None if fb is None else fb.numpy()[ids])
+            d_gh, k_gh = d_g.cpu().numpy(), k_g.cpu().numpy()
+            assert np.array_equal(k_gh[ids], k_o), f"step {step}: draft counts differ"
+            assert np.array_equal(d_gh[ids], d_o), f"step {step}: drafts differ"
+            drafts, k, q = torch.from_numpy(d_gh), torch.from_numpy(k_gh), None
+        else:
+            q, drafts = wl.dense_draft(cfg, logits, g)
+            k = torch.full((B,), K, dtype=torch.int32)
+        logits = wl.apply_boost(cfg, logits, drafts, k, bprob, g)
+        kv_all = lens_g.cpu().numpy().astype(np.int64) + k.numpy()
+        kv_g.copy_(torch.from_numpy(kv_all.astype(np.int32)))
+        sp.spec_verify(logits.to(device), drafts.to(device), None if q is None else q.to(device), k.to(device),
+                       hist_g, lens_g, _gpu_params(cfg, T, step, seed), kv_g, ema_g, out_tok, out_acc, ws)
+        res = ov.spec_verify(logits[ids].double().numpy(), drafts.numpy()[ids].astype(np.int64),
+                             None if q is None else q[ids].numpy(), k.numpy()[ids].astype(np.int64), hist_o,
+                             lens_o, _oracle_params(cfg, T, step, seed), kv_all[ids],
+                             ema_o.astype(np.float32), seq_ids=ids)
+        a_g = out_acc.cpu().numpy()[ids]
+        t_g = out_tok.cpu().numpy()[ids]
+        kv_gh = kv_g.cpu().numpy()[ids]
+        ema_gh = ema_g.cpu().numpy()[ids].astype(np.float64)
+        rep.rows += len(ids) * (K + 1)
+        rep.rows_read += int((res["k_eff"] + 1).sum())
+        rep.accepted += int(res["accept_len"].sum())
+        rep.drafted += int(res["k_eff"].sum())
+        bad = compare(step, a_g, t_g, kv_gh, ema_gh, res, rep, ids)
+        sp.spec_append(hist_g, lens_g, out_tok, out_acc)
+        for i in range(len(ids)):
+            a = int(res["accept_len"][i])
+            hist_o[i, lens_o[i]:lens_o[i] + a + 1] = res["out_tokens"][i, :a + 1]
+            if stats is not None:
+                on.extend_stats(stats[i], hist_o[i], int(lens_o[i]), int(lens_o[i]) + a + 1)
+            lens_o[i] += a + 1
+        ema_o = res["ema"].astype(np.float32).astype(np.float64)
+        if bad.any():  # put the oracle's state into the sampled sequences
+            h = hist_g.cpu()
+            h[torch.from_numpy(ids)] = torch.from_numpy(hist_o.astype(np.int32))
+            hist_g.copy_(h)
+            ln = lens_g.cpu()
+            ln[torch.from_numpy(ids)] = torch.from_numpy(lens_o.astype(np.int32))
+            lens_g.copy_(ln)
+            e = ema_g.cpu()
+            e[torch.from_numpy(ids)] = torch.from_numpy(ema_o.astype(np.float32))
+            ema_g.copy_(e)
+            if use_ngram:
+                table.reset()
+        else:
+            assert np.array_equal(lens_g.cpu().numpy()[ids], lens_o)
+        if use_ngram:
+            sp.ngram_update(table, hist_g, lens_g)
+        rep.steps += 1
+    status = sp.get_status(clear=True)
+    assert status == 0, f"device status bits set: {sp.status_names(status)}"
+    assert rep.excused <= max(1, EXCUSE_RATE * rep.rows), "\n".join(rep.notes)
+    if table is not None:
+        table.close()
+    return rep
+
+
 def run(cfg: wl.Config, steps: int, T: float | None = None, device="cuda", seed: int | None = None,
         oracle_chunk: int = 16) -> Report:
     """Run ``steps`` lockstep steps of cfg; raise AssertionError on a parity failure."""
@@ -136,23 +262,7 @@ def run(cfg: wl.Config, steps: int, T: float | None = None, device="cuda", seed:
         rep.accepted += int(a_o.sum())
         rep.drafted += int(k_eff.sum())
         rep.gated += int(((k.numpy() > 0) & (k_eff == 0)).sum())
-        bad = (a_g != a_o) | (t_g != t_o).any(axis=1) | (kv_gh != res["kv_len"]) | \
-              (np.abs(ema_gh - res["ema"]) > EMA_TOL)
-        for b in np.nonzero(bad)[0]:
-            excusable = False
-            if a_g[b] != a_o[b]:
-                i = min(a_g[b], a_o[b])
-                excusable = res["accept_margin"][b, i] < MARGIN
-            elif (t_g[b] != t_o[b]).any():
-                excusable = res["sample_margin"][b] < MARGIN
-            if res["ema_margin"][b] < EMA_TOL:
-                excusable = True
-            msg = (f"step {step} seq {b}: gpu a={a_g[b]} tok={t_g[b].tolist()} kv={kv_gh[b]} ema={ema_gh[b]!r}; "
-                   f"oracle a={a_o[b]} tok={t_o[b].tolist()} kv={res['kv_len'][b]} ema={res['ema'][b]!r} "
-                   f"acc_margin={res['accept_margin'][b].tolist()} sample_margin={res['sample_margin'][b]!r}")
-            assert excusable, "parity failure: " + msg
-            rep.excused += 1
-            rep.notes.append(msg)
+        bad = compare(step, a_g, t_g, kv_gh, ema_gh, res, rep)
         # ---- commit: both sides append their own tokens
         sp.spec_append(hist_g, lens_g, out_tok, out_acc)
         for b in range(B):

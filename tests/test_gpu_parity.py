@@ -60,3 +60,21 @@ def test_long_c1_run():
     # the tiny workload for its full 64 steps with three sampler seeds
     for seed in (8, 123, 99991):
         lockstep.run(wl.get("c1"), 64, seed=seed)
+
+
+FULL = {
+    # the benchmark's workloads at full size; the oracle checks sampled sequences
+    "c5_full": (wl.get("c5"), 2, 8),
+    "c3_full": (wl.get("c3"), 2, 6),
+    "c4_full": (wl.get("c4"), 2, 4),
+    "c2_full_greedy": (wl.get("c2"), 3, 1),
+}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_full_size_sampled(name):
+    cfg, steps, sample = FULL[name]
+    T = 0.0 if name.endswith("greedy") else None
+    rep = lockstep.run_sampled(cfg, steps, sample, T=T)
+    assert rep.steps == steps and rep.excused <= 1
+    assert rep.drafted > 0
