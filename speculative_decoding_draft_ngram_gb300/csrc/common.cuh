@@ -81,19 +81,21 @@ __device__ __forceinline__ RowPhilox row_philox(const NoiseKey& nk, uint32_t pos
 // Same words as gumbel_block(nk, blk, pos) for the row that rp describes.
 __device__ __forceinline__ uint4 gumbel_block_row(const RowPhilox& rp, uint32_t blk) {
     // round 1
-    const uint32_t hi0 = __umulhi(kPhiloxM0, blk), lo0 = kPhiloxM0 * blk;
+    const uint64_t q0 = static_cast<uint64_t>(kPhiloxM0) * blk;
+    const uint32_t hi0 = static_cast<uint32_t>(q0 >> 32), lo0 = static_cast<uint32_t>(q0);
     const uint32_t c2p = hi0 ^ rp.c3k1;
     // round 2 (c0' and c1' are row constants folded into e2 / f2 / d2)
-    const uint32_t hi1 = __umulhi(kPhiloxM1, c2p), lo1 = kPhiloxM1 * c2p;
+    const uint64_t q1 = static_cast<uint64_t>(kPhiloxM1) * c2p;
+    const uint32_t hi1 = static_cast<uint32_t>(q1 >> 32), lo1 = static_cast<uint32_t>(q1);
     uint4 c = make_uint4(hi1 ^ rp.e2, lo1, rp.f2 ^ lo0, rp.d2);
     uint32_t k0 = rp.k0 + 2u * kPhiloxW0, k1 = rp.k1 + 2u * kPhiloxW1;
 #pragma unroll
     for (int r = 2; r < 10; ++r) {
-        const uint32_t h0 = __umulhi(kPhiloxM0, c.x);
-        const uint32_t l0 = kPhiloxM0 * c.x;
-        const uint32_t h1 = __umulhi(kPhiloxM1, c.z);
-        const uint32_t l1 = kPhiloxM1 * c.z;
-        c = make_uint4(h1 ^ c.y ^ k0, l1, h0 ^ c.w ^ k1, l0);
+        // one 32 x 32 -> 64-bit product per multiplier gives both halves
+        const uint64_t p0 = static_cast<uint64_t>(kPhiloxM0) * c.x;
+        const uint64_t p1 = static_cast<uint64_t>(kPhiloxM1) * c.z;
+        c = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ c.y ^ k0, static_cast<uint32_t>(p1),
+                       static_cast<uint32_t>(p0 >> 32) ^ c.w ^ k1, static_cast<uint32_t>(p0));
         k0 += kPhiloxW0;
         k1 += kPhiloxW1;
     }

@@ -268,6 +268,19 @@ __device__ __forceinline__ unsigned bf16x8_ge_mask(const uint4& r, uint32_t t) {
            ((m2 >> 11) & 32u) | ((m3 & 1u) << 6) | ((m3 >> 9) & 128u);
 }
 
+// The same mask with fewer instructions: the high byte of each compared half
+// is gathered with byte permutes, and the four 0xFF / 0x00 bytes of a word are
+// turned into four bits by one multiply (the partial products of distinct
+// bytes land on distinct bit positions, so nothing carries into bits 24..27).
+__device__ __forceinline__ unsigned bf16x8_ge_bits(const uint4& r, uint32_t t) {
+    const __nv_bfloat162 th = as_bf162(t);
+    const unsigned m0 = __hge2_mask(as_bf162(r.x), th), m1 = __hge2_mask(as_bf162(r.y), th);
+    const unsigned m2 = __hge2_mask(as_bf162(r.z), th), m3 = __hge2_mask(as_bf162(r.w), th);
+    const unsigned b03 = __byte_perm(m0, m1, 0x7531u) & 0x01010101u;  // elements 0..3, one byte each
+    const unsigned b47 = __byte_perm(m2, m3, 0x7531u) & 0x01010101u;  // elements 4..7
+    return ((b03 * 0x01020408u) >> 24) | (((b47 * 0x01020408u) >> 24) << 4);
+}
+
 // Merge (m, s) pairs whose sums are relative to their own maxima.
 __device__ __forceinline__ void ms_merge(float& m, float& s, float mo, float so, float sc) {
     const float M = fmaxf(m, mo);
@@ -395,6 +408,7 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 
 struct StageMeta {
     int b, j, c, excl, seg_end;  // seg_end: the last chunk of this row in the CTA's range
+    int cand;                    // the row's Gumbel candidates can be the emitted token
 };
 
 struct WarpPart {
@@ -418,6 +432,8 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
     __shared__ int s_cnt[kStages];
     __shared__ unsigned s_rthr[kStages + 1];  // per-segment shared threshold (score_key; 0 = none)
     __shared__ int s_qn[kCWarps];
+    __shared__ float s_cz[GREEDY ? 1 : kCWarps * 32];  // carried candidates: z / T
+    __shared__ int s_cv[GREEDY ? 1 : kCWarps * 32];    // carried candidates: vocab id
     __shared__ long long s_wsum[kPThreads / 32];
     __shared__ int s_start[3];
     __shared__ int s_hwin[PENALTY ? SPECNG_MAX_REP_WINDOW : 1];
@@ -507,11 +523,16 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
             const int v1 = min(P.V, v0 + CHUNK);
             if (lane == 0) {
                 int excl = -1;
-                if (!GREEDY && !dense && j < keff) {
+                // with dense q, row j < k_eff is sampled by the residual pass unless
+                // its draft is invalid (the residual is then p itself)
+                int cand = 1;
+                if (!GREEDY && j < keff) {
                     const int d = s_pdrafts[j];
-                    if (d >= 0 && d < P.V) excl = d;
+                    const bool valid = d >= 0 && d < P.V;
+                    if (!dense && valid) excl = d;
+                    if (dense && valid) cand = 0;
                 }
-                s_meta[st] = StageMeta{b, j, c, excl, (c == P.nchunk - 1 || n == nwork - 1) ? 1 : 0};
+                s_meta[st] = StageMeta{b, j, c, excl, (c == P.nchunk - 1 || n == nwork - 1) ? 1 : 0, cand};
             }
             if constexpr (PENALTY) {
                 const WindowView wv{s_hwin, s_pdrafts, nh, P.W};
@@ -566,6 +587,7 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
     bool fresh = true;
     int seg = 0;
     uint16_t* q = s_q + warp * kQCap;
+    int cn = 0;  // candidates carried from the segment's previous stage (s_cz / s_cv)
     if (lane == 0) s_qn[warp] = 0;
     __syncwarp();
     for (int n = 0; n < nwork; ++n) {
@@ -586,11 +608,39 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
         nk.seq = static_cast<uint32_t>(mt.b);
         const int ubase = warp * (32 * kVL);  // first 16-byte vector of my slice
         unsigned* rth = &s_rthr[seg % (kStages + 1)];
+        const RowPhilox rp = row_philox(nk, static_cast<uint32_t>(j));
 
         if constexpr (GREEDY) {
             // top two transformed values (lower id on ties) within cand_delta of
-            // the best value any warp of the CTA has seen in this segment
-            float gth = fmaxf(tt.s1, key_score(*reinterpret_cast<volatile unsigned*>(rth)));
+            // the best value any warp of the CTA has seen in this segment.  The
+            // slice's maxima come first (packed compares), so the threshold is
+            // already the warp's best before any element is pushed.
+            uint4 rv[kVL];
+            float vmx[kVL];
+            float lmax = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < kVL; ++i) {
+                const int u = ubase + i * 32 + lane;
+                const int off = u * EPV;
+                const int nv = min(EPV, v1 - (v0 + off));
+                rv[i] = stage[u];
+                const unsigned pb = pen_bits<PENALTY, EPV>(bm, off);
+                float vm = -INFINITY;
+                if (BF16 && nv == EPV && pb == 0u) {
+                    vm = bf16x8_max(rv[i]);
+                    if constexpr (SOFTCAP) vm = transform_f32<true, false>(vm, false, P);
+                } else if (nv > 0) {
+                    float x[EPV];
+                    unpack<BF16>(rv[i], x);
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e)
+                        if (e < nv) vm = fmaxf(vm, transform_f32<SOFTCAP, PENALTY>(x[e], (pb >> e) & 1u, P));
+                }
+                vmx[i] = vm;
+                lmax = fmaxf(lmax, vm);
+            }
+            const unsigned wk = warp_best_key(lmax);
+            float gth = fmaxf(fmaxf(tt.s1, key_score(wk)), key_score(*reinterpret_cast<volatile unsigned*>(rth)));
             gth = gth > -INFINITY ? gth - cand_delta(gth) : -INFINITY;
 #pragma unroll
             for (int i = 0; i < kVL; ++i) {
@@ -598,16 +648,10 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                 const int off = u * EPV;
                 const int e0 = v0 + off;
                 const int nv = min(EPV, v1 - e0);
-                if (nv <= 0) continue;
-                const uint4 r = stage[u];
+                if (nv <= 0 || !(vmx[i] >= gth)) continue;
                 const unsigned pb = pen_bits<PENALTY, EPV>(bm, off);
-                if (BF16 && nv == EPV && pb == 0u) {
-                    float vm = bf16x8_max(r);
-                    if constexpr (SOFTCAP) vm = transform_f32<true, false>(vm, false, P);
-                    if (!(vm >= gth)) continue;
-                }
                 float x[EPV];
-                unpack<BF16>(r, x);
+                unpack<BF16>(rv[i], x);
 #pragma unroll
                 for (int e = 0; e < EPV; ++e) {
                     if (e >= nv) break;
@@ -619,8 +663,9 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
             const unsigned kw = warp_best_key(tt.s1);
             if (lane == 0 && kw != 0u) atomicMax(rth, kw);
         } else {
+            const bool cand = mt.cand != 0;
             int seeded = -1;  // element already scored as this lane's seed
-            if (fresh) {
+            if (fresh && cand && !(BF16 && !PENALTY && v0 + (ubase + (kVL - 1) * 32 + lane) * EPV + EPV <= v1)) {
                 // ---- seed: every lane scores the largest element of its slice
                 float zm = -INFINITY;
                 int am = -1;
@@ -643,7 +688,7 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                 }
                 float t0 = -INFINITY;
                 if (am >= 0) {
-                    const uint4 w = gumbel_block(nk, static_cast<uint32_t>(am) >> 2, static_cast<uint32_t>(j));
+                    const uint4 w = gumbel_block_row(rp, static_cast<uint32_t>(am) >> 2);
                     t0 = zm * P.invT + gumbel_f32(pick_word(w, static_cast<uint32_t>(am) & 3u));
                     top2_push(tt, t0, am);
                     seeded = am;
@@ -682,31 +727,10 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
             };
             set_xt();
             sync_thr();
-            // score one queued candidate (offset in the chunk; all lanes busy); updates tt / thr
-            const RowPhilox rp = row_philox(nk, static_cast<uint32_t>(j));
-            auto score_one = [&](int loc) {
-                float x;
-                if constexpr (BF16) {
-                    x = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(stage)[loc]) << 16);
-                } else {
-                    x = reinterpret_cast<const float*>(stage)[loc];
-                }
-                const bool pen = PENALTY && ((bm[loc >> 5] >> (loc & 31)) & 1u);
-                const float zb = transform_f32<SOFTCAP, PENALTY>(x, pen, P) * P.invT;
-                const int v = v0 + loc;
-                if (v == excl || zb + kGumbelMax < thr) return;
-                const uint32_t word = pick_word(gumbel_block_row(rp, static_cast<uint32_t>(v) >> 2),
-                                                static_cast<uint32_t>(v) & 3u);
-                if (!gumbel_may_reach(word, thr - zb)) return;
-                const float score = zb + gumbel_f32(word);
-                if (score >= thr) {
-                    top2_push(tt, score, v);
-                    thr = fmaxf(thr, tt.s1 - cand_delta(tt.s1));
-                }
-            };
-            // ---- one pass over the slice: all four 16-byte vectors are loaded first, the
-            //      online maximum and the 32 exponentials form one independent block, the
-            //      candidates of the whole slice are queued once and scored 32 at a time
+            // ---- one pass over the slice: all four 16-byte vectors are loaded first; the
+            //      online maximum and the 32 exponentials (packed fp32x2 arithmetic) form one
+            //      independent block; candidate masks are formed only for the vectors whose
+            //      maximum reaches the threshold
             uint4 rv[kVL];
 #pragma unroll
             for (int i = 0; i < kVL; ++i) rv[i] = stage[ubase + i * 32 + lane];
@@ -719,14 +743,49 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
             }
             unsigned msk = 0u;  // bit 8 i + e: element e of vector i
             if (fast) {
-                float vm = -INFINITY;
+                float rmx[kVL];  // raw maxima
 #pragma unroll
                 for (int i = 0; i < kVL; ++i) {
                     if constexpr (BF16) {
-                        vm = fmaxf(vm, bf16x8_max(rv[i]));
+                        rmx[i] = bf16x8_max(rv[i]);
                     } else {
-                        vm = fmaxf(vm, fmaxf(fmaxf(__uint_as_float(rv[i].x), __uint_as_float(rv[i].y)),
-                                             fmaxf(__uint_as_float(rv[i].z), __uint_as_float(rv[i].w))));
+                        rmx[i] = fmaxf(fmaxf(__uint_as_float(rv[i].x), __uint_as_float(rv[i].y)),
+                                       fmaxf(__uint_as_float(rv[i].z), __uint_as_float(rv[i].w)));
+                    }
+                }
+                float vm = fmaxf(fmaxf(rmx[0], rmx[1]), fmaxf(rmx[2], rmx[3]));
+                if constexpr (BF16 && !PENALTY) {
+                    if (fresh && cand) {
+                        // seed: score the slice's largest element (lowest id among equals); the
+                        // transform is monotone, so it is also the largest transformed value
+                        int am = -1;
+#pragma unroll
+                        for (int i = kVL - 1; i >= 0; --i) {
+                            if (rmx[i] == vm) {
+                                float x[EPV];
+                                unpack<BF16>(rv[i], x);
+                                int e = EPV - 1;
+#pragma unroll
+                                for (int k = EPV - 2; k >= 0; --k) e = x[k] == vm ? k : e;
+                                am = v0 + off0 + i * 32 * EPV + e;
+                            }
+                        }
+                        float t0 = -INFINITY;
+                        if (am >= 0 && am != excl) {
+                            const uint4 w = gumbel_block_row(rp, static_cast<uint32_t>(am) >> 2);
+                            t0 = transform_f32<SOFTCAP, false>(vm, false, P) * P.invT +
+                                 gumbel_f32(pick_word(w, static_cast<uint32_t>(am) & 3u));
+                            top2_push(tt, t0, am);
+                            seeded = am;
+                        }
+                        const unsigned k0 = warp_best_key(t0);
+                        if (k0 != 0u) {
+                            t0 = key_score(k0);
+                            thr = t0 - cand_delta(t0);
+                            if (lane == 0) atomicMax(rth, k0);
+                            set_xt();
+                        }
+                        sync_thr();  // and adopt the best seed any warp has published
                     }
                 }
                 if constexpr (SOFTCAP) vm = transform_f32<true, false>(vm, false, P);
@@ -735,26 +794,38 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                     m = vm;
                     msc = m * P.sc;
                 }
-                float acc[kVL];
+                float2 acc2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+                const float2 sc2 = make_float2(P.sc, P.sc), nm2 = make_float2(-msc, -msc);
 #pragma unroll
                 for (int i = 0; i < kVL; ++i) {
                     float x[EPV];
                     unpack<BF16>(rv[i], x);
-                    float a = 0.0f;
 #pragma unroll
-                    for (int e = 0; e < EPV; ++e) a += ex2_approx(fmaf(transform_f32<SOFTCAP, false>(x[e], false, P), P.sc, -msc));
-                    acc[i] = a;
-                    unsigned mi;
-                    if constexpr (BF16) {
-                        mi = bf16x8_ge_mask(rv[i], xt2);
-                    } else {
-                        mi = 0u;
-#pragma unroll
-                        for (int e = 0; e < EPV; ++e) mi |= static_cast<unsigned>(x[e] >= xt) << e;
+                    for (int e = 0; e < EPV; e += 2) {
+                        const float2 t = __ffma2_rn(make_float2(transform_f32<SOFTCAP, false>(x[e], false, P),
+                                                                transform_f32<SOFTCAP, false>(x[e + 1], false, P)),
+                                                    sc2, nm2);
+                        acc2[i & 1] = __fadd2_rn(acc2[i & 1], make_float2(ex2_approx(t.x), ex2_approx(t.y)));
                     }
-                    msk |= mi << (8 * i);
                 }
-                s += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                s += (acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y);
+                if (cand) {
+#pragma unroll
+                    for (int i = 0; i < kVL; ++i) {
+                        if (!(rmx[i] >= xt)) continue;
+                        unsigned mi;
+                        if constexpr (BF16) {
+                            mi = bf16x8_ge_bits(rv[i], xt2);
+                        } else {
+                            mi = 0u;
+                            mi |= static_cast<unsigned>(__uint_as_float(rv[i].x) >= xt);
+                            mi |= static_cast<unsigned>(__uint_as_float(rv[i].y) >= xt) << 1;
+                            mi |= static_cast<unsigned>(__uint_as_float(rv[i].z) >= xt) << 2;
+                            mi |= static_cast<unsigned>(__uint_as_float(rv[i].w) >= xt) << 3;
+                        }
+                        msk |= mi << (8 * i);
+                    }
+                }
                 if constexpr (PENALTY) {
                     // the few penalised elements: replace their terms by the penalised ones
                     // (and raise the maximum if a penalty below 1 lifted one above it); they
@@ -779,7 +850,7 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                         }
                         s += ex2_approx(fmaf(zp, P.sc, -msc)) - ex2_approx(fmaf(zu, P.sc, -msc));
                     }
-                    msk |= pmk;
+                    if (cand) msk |= pmk;
                 }
             } else {
                 // partial vectors (a row's last chunk): exact transform element by element
@@ -792,15 +863,15 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                     float x[EPV], z[EPV];
                     unpack<BF16>(rv[i], x);
                     const unsigned pb = pen_bits<PENALTY, EPV>(bm, off);
-                    float vm = -INFINITY;
+                    float vmx = -INFINITY;
 #pragma unroll
                     for (int e = 0; e < EPV; ++e) {
                         z[e] = transform_f32<SOFTCAP, PENALTY>(x[e], (pb >> e) & 1u, P);
-                        if (e < nv) vm = fmaxf(vm, z[e]);
+                        if (e < nv) vmx = fmaxf(vmx, z[e]);
                     }
-                    if (vm > m) {
-                        s = m > -INFINITY ? s * ex2_approx((m - vm) * P.sc) : 0.0f;
-                        m = vm;
+                    if (vmx > m) {
+                        s = m > -INFINITY ? s * ex2_approx((m - vmx) * P.sc) : 0.0f;
+                        m = vmx;
                         msc = m * P.sc;
                     }
                     const float zthr = thr - kGumbelMax;
@@ -808,7 +879,7 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                     for (int e = 0; e < EPV; ++e) {
                         if (e < nv) {
                             if (m > -INFINITY) s += ex2_approx(fmaf(z[e], P.sc, -msc));
-                            msk |= static_cast<unsigned>(z[e] * P.invT >= zthr) << (8 * i + e);
+                            if (cand) msk |= static_cast<unsigned>(z[e] * P.invT >= zthr) << (8 * i + e);
                         }
                     }
                 }
@@ -818,38 +889,83 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                 const int si = so / (32 * EPV), se = so - si * 32 * EPV;
                 if (se >= 0 && se < EPV) msk &= ~(1u << (8 * si + se));
             }
-            // queue the slice's candidates (chunk offsets)
+            // ---- queue the slice's candidates (chunk offsets of this stage)
             const unsigned cnt = __popc(msk);
-            int nq = static_cast<int>(__reduce_add_sync(0xffffffffu, cnt));
-            if (nq != 0) {
-                if (msk != 0u) {
-                    int slot = atomicAdd(&s_qn[warp], static_cast<int>(cnt));
-                    while (msk != 0u) {
-                        const int bit = __ffs(msk) - 1;
-                        msk &= msk - 1u;
-                        q[slot++] = static_cast<uint16_t>(off0 + (bit >> 3) * 32 * EPV + (bit & 7));
-                    }
+            const int nq = static_cast<int>(__reduce_add_sync(0xffffffffu, cnt));
+            if (msk != 0u) {
+                int slot = atomicAdd(&s_qn[warp], static_cast<int>(cnt));
+                while (msk != 0u) {
+                    const int bit = __ffs(msk) - 1;
+                    msk &= msk - 1u;
+                    q[slot++] = static_cast<uint16_t>(off0 + (bit >> 3) * 32 * EPV + (bit & 7));
                 }
-                __syncwarp();
-                while (nq >= 32) {
-                    score_one(q[nq - 32 + lane]);
-                    nq -= 32;
-                    // share the warp's best score with the CTA
-                    const unsigned kb = warp_best_key(tt.s1);
-                    if (kb != 0u) {
-                        const float bw = key_score(kb);
-                        thr = fmaxf(thr, bw - cand_delta(bw));
-                        if (lane == 0) atomicMax(rth, kb);
-                    }
-                    sync_thr();
-                }
-                if (lane < nq) score_one(q[lane]);
-                __syncwarp();
-                if (lane == 0) s_qn[warp] = 0;
-                __syncwarp();
             }
+            __syncwarp();
+            // ---- score full batches of 32 from [carried ++ queued]; the remainder is carried to
+            //      the segment's next stage (as transformed value and id), and scored at its end
+            const bool flush = mt.seg_end != 0;
+            const int total = cn + nq;
+            float* cz = s_cz + warp * 32;
+            int* cv = s_cv + warp * 32;
+            auto fetch = [&](int idx, float& zb, int& v) {
+                if (idx < cn) {
+                    zb = cz[idx];
+                    v = cv[idx];
+                } else {
+                    const int loc = static_cast<int>(q[idx - cn]);
+                    float x;
+                    if constexpr (BF16) {
+                        x = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(stage)[loc]) << 16);
+                    } else {
+                        x = reinterpret_cast<const float*>(stage)[loc];
+                    }
+                    const bool pen = PENALTY && ((bm[loc >> 5] >> (loc & 31)) & 1u);
+                    zb = transform_f32<SOFTCAP, PENALTY>(x, pen, P) * P.invT;
+                    v = v0 + loc;
+                }
+            };
+            int base = 0;
+            while (total - base >= 32 || (flush && base < total)) {
+                const int idx = base + lane;
+                float zb = -INFINITY;
+                int v = 0;
+                if (idx < total) fetch(idx, zb, v);
+                const bool live = idx < total && v != excl && zb + kGumbelMax >= thr;
+                if (__any_sync(0xffffffffu, live)) {
+                    const uint32_t word = pick_word(gumbel_block_row(rp, static_cast<uint32_t>(v) >> 2),
+                                                    static_cast<uint32_t>(v) & 3u);
+                    if (live && gumbel_may_reach(word, thr - zb)) {
+                        const float score = zb + gumbel_f32(word);
+                        if (score >= thr) {
+                            top2_push(tt, score, v);
+                            thr = fmaxf(thr, tt.s1 - cand_delta(tt.s1));
+                        }
+                    }
+                }
+                base += 32;
+            }
+            const int rem = total - base;  // < 32; 0 after a flush
+            if (rem > 0) {
+                float zc = 0.0f;
+                int vc = 0;
+                if (lane < rem) fetch(base + lane, zc, vc);
+                __syncwarp();
+                if (lane < rem) {
+                    cz[lane] = zc;
+                    cv[lane] = vc;
+                }
+            }
+            cn = rem > 0 ? rem : 0;
+            __syncwarp();
+            if (lane == 0) s_qn[warp] = 0;
+            __syncwarp();
+            // share the warp's best score with the CTA, adopt the CTA's best
             const unsigned kw = warp_best_key(tt.s1);
-            if (lane == 0 && kw != 0u) atomicMax(rth, kw);
+            if (kw != 0u) {
+                const float bw = key_score(kw);
+                thr = fmaxf(thr, bw - cand_delta(bw));
+                if (lane == 0) atomicMax(rth, kw);
+            }
         }
         fresh = mt.seg_end != 0;
         if (fresh) {
