@@ -234,20 +234,30 @@ class Path:
         self.ws = sp.spec_verify_workspace(B, K, V, device)
         self.params = sp.VerifyParams(temperature=cfg.temperature, softcap=cfg.softcap, rep_penalty=cfg.rep_penalty,
                                       rep_window=cfg.rep_window, gate_enabled=cfg.gate, seed=cfg.sampler_seed)
-        # library kernels per step: ngram_draft (1), spec_verify (stream + merge; + residual with dense q at
-        # T > 0), spec_append (1), ngram_update (count + best)
-        self.launches_per_step = (1 if self.ngram else 0) + (3 if cfg.dense and cfg.temperature > 0 else 2) + 1 + \
-            (2 if self.ngram else 0)
+        # library kernels per step: spec_verify (stream + merge; + residual with dense q at T > 0), then
+        # spec_commit (append + index + next drafts) or, without n-gram drafts, spec_append
+        self.launches_per_step = (3 if cfg.dense and cfg.temperature > 0 else 2) + 1
         self.g = g
 
+    def _limits(self, s):
+        cfg = self.cfg
+        lim = self.limits[s] if cfg.k_uniform else None
+        fb = self.fallback[s % 16] if self.fallback is not None else None
+        return lim, fb
+
+    def first_drafts(self, s):
+        """Drafts of step s from the table (the steps after it get theirs from spec_commit)."""
+        if self.ngram:
+            lim, fb = self._limits(s)
+            self.sp.ngram_draft(self.table, self.hist, self.lens, self.cfg.K, k_limit=lim, out_drafts=self.drafts,
+                                out_k=self.kbuf[s], fallback=fb)
+
     def step(self, s, logits, ev=None):
-        """One pass of the hot path; ev = (start, end) events around spec_verify."""
+        """One pass of the hot path: verify step s's drafts, then commit (append the
+        emitted tokens, index them, draft step s + 1); ev = (start, end) events
+        around spec_verify."""
         sp, cfg = self.sp, self.cfg
         if self.ngram:
-            lim = self.limits[s] if cfg.k_uniform else None
-            fb = self.fallback[s % 16] if self.fallback is not None else None
-            sp.ngram_draft(self.table, self.hist, self.lens, cfg.K, k_limit=lim, out_drafts=self.drafts,
-                           out_k=self.kbuf[s], fallback=fb)
             drafts, k, q = self.drafts, self.kbuf[s], None
         else:
             i = s % self.n_sets
@@ -265,9 +275,12 @@ class Path:
             ev[1].record()
         if saved is not None:
             logits.view(-1)[saved[0]] = saved[1]
-        sp.spec_append(self.hist, self.lens, self.out, self.acc)
         if self.ngram:
-            sp.ngram_update(self.table, self.hist, self.lens)
+            lim, fb = self._limits(s + 1)
+            sp.spec_commit(self.table, self.hist, self.lens, self.out, self.acc, cfg.K, k_limit=lim, fallback=fb,
+                           out_drafts=self.drafts, out_k=self.kbuf[s + 1])
+        else:
+            sp.spec_append(self.hist, self.lens, self.out, self.acc)
 
     def _boost(self, logits, drafts, k):
         B, K1, V = logits.shape
@@ -312,6 +325,7 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
 
     # ---- device-resident timed loop
+    path.first_drafts(0)
     for s in range(args.warmup):
         path.step(s, path.logits[s % path.n_sets])
     torch.cuda.synchronize()

@@ -207,6 +207,21 @@ int spec_verify(const void* logits, int logits_dtype, int B, int K, int V,
                 int32_t* out_tokens, int32_t* out_accept_len,
                 void* workspace, size_t workspace_bytes, cudaStream_t s);
 
+/* One step's commit in one kernel launch: exactly spec_append, then
+ * ngram_update, then ngram_draft for the next step, with the same arguments
+ * and results as those three calls made in that order (B must be the
+ * table's B).  One warp per sequence: a sequence's history, lengths and
+ * table keys belong to it alone, so no other sequence's work is waited for.
+ * The fusion is an implementation choice, not a step of the pages; it
+ * removes three of the four launches of the per-step bookkeeping, which are
+ * bound by launch and memory latency rather than by bandwidth.
+ * Errors: EINVAL, ECUDA.  Device: HIST_OVERFLOW, BAD_K, TABLE_FULL,
+ * TOKEN_OOR, COUNT_SAT, HIST_SHRANK. */
+int spec_commit(specng_ngram* table, int32_t* history, int64_t hist_stride, int32_t* lens,
+                int64_t hist_cap, const int32_t* out_tokens, const int32_t* out_accept_len,
+                int B, int K, int max_k, const int32_t* k_limit, const int32_t* fallback,
+                int32_t* out_drafts, int32_t* out_k, cudaStream_t s);
+
 /* spec_verify without a caller workspace.  The pages have no counterpart of
  * this call: it is an interface addition, for callers that cannot allocate
  * device memory where they verify -- a runtime whose allocator reserved the

@@ -18,6 +18,7 @@ from .capi import (  # noqa: F401
     ngram_update,
     philox4x32_10,
     spec_append,
+    spec_commit,
     spec_verify,
     spec_verify_noalloc,
     spec_verify_workspace,

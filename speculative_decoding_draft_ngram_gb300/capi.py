@@ -35,7 +35,7 @@ STATUS_BITS = {
 EXPORTED = (
     "specng_ngram_create", "specng_ngram_destroy", "specng_ngram_reset", "specng_ngram_capacity",
     "ngram_update", "ngram_draft", "spec_verify_workspace_bytes", "spec_verify_workspace_init",
-    "spec_verify", "spec_verify_noalloc", "spec_append", "specng_get_status", "specng_strerror",
+    "spec_verify", "spec_verify_noalloc", "spec_append", "spec_commit", "specng_get_status", "specng_strerror",
     "specng_last_error", "specng_philox4x32_10",
 )
 
@@ -109,6 +109,7 @@ def load() -> ctypes.CDLL:
         "spec_verify_noalloc": (I, [P, I, I, I, I, P, P, P, P, I64, P, ctypes.POINTER(VerifyParamsC),
                                     P, P, P, P, P]),
         "spec_append": (I, [P, I64, P, I64, P, P, I, I, P]),
+        "spec_commit": (I, [P, P, I64, P, I64, P, P, I, I, I, P, P, P, P, P]),
         "specng_get_status": (I, [ctypes.POINTER(ctypes.c_uint32), I]),
         "specng_strerror": (ctypes.c_char_p, [I]),
         "specng_last_error": (ctypes.c_char_p, []),
@@ -282,6 +283,27 @@ def spec_append(history: torch.Tensor, lens: torch.Tensor, out_tokens: torch.Ten
                               _ptr(lens, torch.int32, "lens"), cap, _ptr(out_tokens, torch.int32, "out_tokens"),
                               _ptr(out_accept_len, torch.int32, "out_accept_len"), B, K1 - 1,
                               _stream(history.device)), "spec_append")
+
+
+def spec_commit(table: NgramTable, history: torch.Tensor, lens: torch.Tensor, out_tokens: torch.Tensor,
+                out_accept_len: torch.Tensor, max_k: int, k_limit: Optional[torch.Tensor] = None,
+                fallback: Optional[torch.Tensor] = None, out_drafts: Optional[torch.Tensor] = None,
+                out_k: Optional[torch.Tensor] = None, hist_cap: Optional[int] = None):
+    """spec_append + ngram_update + ngram_draft (next step) in one launch;
+    returns (out_drafts [B, max_k], out_k [B])."""
+    B, K1 = out_tokens.shape
+    if out_drafts is None:
+        out_drafts = torch.empty((B, max_k), dtype=torch.int32, device=history.device)
+    if out_k is None:
+        out_k = torch.empty((B,), dtype=torch.int32, device=history.device)
+    cap = history.shape[1] if hist_cap is None else int(hist_cap)
+    _check(load().spec_commit(table._h, _ptr(history, torch.int32, "history"), history.shape[1],
+                              _ptr(lens, torch.int32, "lens"), cap, _ptr(out_tokens, torch.int32, "out_tokens"),
+                              _ptr(out_accept_len, torch.int32, "out_accept_len"), B, K1 - 1, int(max_k),
+                              _ptr(k_limit, torch.int32, "k_limit"), _ptr(fallback, torch.int32, "fallback"),
+                              _ptr(out_drafts, torch.int32, "out_drafts"), _ptr(out_k, torch.int32, "out_k"),
+                              _stream(history.device)), "spec_commit")
+    return out_drafts, out_k
 
 
 # ---------------------------------------------------------------- diagnostics

@@ -362,6 +362,27 @@ int spec_append(int32_t* history, int64_t hist_stride, int32_t* lens, int64_t hi
     return SPECNG_OK;
 }
 
+int spec_commit(specng_ngram* table, int32_t* history, int64_t hist_stride, int32_t* lens, int64_t hist_cap,
+                const int32_t* out_tokens, const int32_t* out_accept_len, int B, int K, int max_k,
+                const int32_t* k_limit, const int32_t* fallback, int32_t* out_drafts, int32_t* out_k,
+                cudaStream_t s) {
+    if (table == nullptr || history == nullptr || lens == nullptr || out_tokens == nullptr ||
+        out_accept_len == nullptr || out_k == nullptr)
+        return fail(SPECNG_EINVAL, "spec_commit: NULL argument");
+    if (B != table->dev.B) return fail(SPECNG_EINVAL, "spec_commit: B differs from the table's B");
+    if (K < 0 || K > SPECNG_MAX_K) return fail(SPECNG_EINVAL, "spec_commit: K outside [0, 16]");
+    if (max_k < 0 || max_k > SPECNG_MAX_K) return fail(SPECNG_EINVAL, "spec_commit: max_k outside [0, 16]");
+    if (max_k > 0 && out_drafts == nullptr) return fail(SPECNG_EINVAL, "spec_commit: out_drafts is NULL");
+    if (hist_stride < 1 || hist_stride > SPECNG_NGRAM_MAX_POS)
+        return fail(SPECNG_EINVAL, "spec_commit: hist_stride outside [1, 2^24]");
+    if (hist_cap < 0 || hist_cap > hist_stride) return fail(SPECNG_EINVAL, "spec_commit: need 0 <= hist_cap <= hist_stride");
+    const cudaError_t e = launch_spec_commit(table->dev, table->parity, history, hist_stride, lens, hist_cap, out_tokens,
+                                             out_accept_len, K, max_k, k_limit, fallback, out_drafts, out_k, s);
+    if (e != cudaSuccess) return fail_cuda(e, "spec_commit");
+    table->parity ^= 1;
+    return SPECNG_OK;
+}
+
 int specng_philox4x32_10(const uint32_t* ctr, uint64_t seed, uint32_t* out, int64_t n, cudaStream_t s) {
     if (ctr == nullptr || out == nullptr || n < 0) return fail(SPECNG_EINVAL, "specng_philox4x32_10: bad argument");
     if (!aligned16(ctr) || !aligned16(out)) return fail(SPECNG_EALIGN, "specng_philox4x32_10: 16-byte alignment");

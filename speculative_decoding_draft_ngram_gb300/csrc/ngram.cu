@@ -144,44 +144,19 @@ __global__ void __launch_bounds__(kNgThreads) ngram_best_kernel(const NgramDev T
     }
 }
 
+__device__ void draft_one(const NgramDev& T, int b, const int32_t* h, int L, int max_k, const int32_t* k_limit,
+                          const int32_t* fallback, int32_t* out_drafts, int32_t* out_k);
+
 __global__ void __launch_bounds__(kNgThreads) ngram_draft_kernel(const NgramDev T, const int32_t* hist, int64_t stride,
                                                                  const int32_t* lens, int max_k, const int32_t* k_limit,
                                                                  const int32_t* fallback, int32_t* out_drafts,
                                                                  int32_t* out_k) {
     const int b = blockIdx.x * kNgThreads + threadIdx.x;
     if (b >= T.B) return;
-    int kmax = max_k;
-    if (k_limit != nullptr) {
-        const int kl = k_limit[b];
-        kmax = kl < 0 ? 0 : (kl < kmax ? kl : kmax);
-    }
     int L = lens[b];
     if (L < 0) L = 0;
     if (static_cast<int64_t>(L) > stride) L = static_cast<int>(stride);
-    const int32_t* h = hist + static_cast<size_t>(b) * stride;
-    int c2 = L >= 2 ? h[L - 2] : -1;
-    int c1 = L >= 1 ? h[L - 1] : -1;
-    if ((L >= 2 && !tok_ok(c2, T.V)) || (L >= 1 && !tok_ok(c1, T.V))) raise_status(T.status, SPECNG_DEV_TOKEN_OOR);
-    if (!tok_ok(c2, T.V)) c2 = -1;
-    if (!tok_ok(c1, T.V)) c1 = -1;
-    int n = 0;
-    int32_t* out = out_drafts + static_cast<size_t>(b) * max_k;
-    while (n < kmax && c1 >= 0) {
-        int tok = -1;
-        uint64_t v;
-        if (c2 >= 0 && find_value(T.tri_ctx, T.mask, key_tri_ctx(b, c2, c1), &v)) tok = best_token(v);
-        if (tok < 0 && find_value(T.bi_ctx, T.mask, key_bi_ctx(b, c1), &v)) tok = best_token(v);
-        if (tok < 0) break;
-        out[n++] = tok;
-        c2 = c1;
-        c1 = tok;
-    }
-    if (fallback != nullptr) {
-        const int32_t* fb = fallback + static_cast<size_t>(b) * max_k;
-        for (; n < kmax; ++n) out[n] = fb[n];
-    }
-    for (int t = n; t < max_k; ++t) out[t] = -1;
-    out_k[b] = n;
+    draft_one(T, b, hist + static_cast<size_t>(b) * stride, L, max_k, k_limit, fallback, out_drafts, out_k);
 }
 
 __global__ void ngram_clear_kernel(const NgramDev T) {
@@ -211,6 +186,116 @@ __global__ void spec_append_kernel(int32_t* hist, int64_t stride, int32_t* lens,
     const int32_t* t = out_tokens + static_cast<size_t>(b) * (K + 1);
     for (int i = 0; i <= a; ++i) h[i] = t[i];
     lens[b] = L + a + 1;
+}
+
+// Chained trigram -> bigram drafts of sequence b (one thread), as ngram_draft_kernel.
+__device__ void draft_one(const NgramDev& T, int b, const int32_t* h, int L, int max_k, const int32_t* k_limit,
+                          const int32_t* fallback, int32_t* out_drafts, int32_t* out_k) {
+    int kmax = max_k;
+    if (k_limit != nullptr) {
+        const int kl = k_limit[b];
+        kmax = kl < 0 ? 0 : (kl < kmax ? kl : kmax);
+    }
+    int c2 = L >= 2 ? h[L - 2] : -1;
+    int c1 = L >= 1 ? h[L - 1] : -1;
+    if ((L >= 2 && !tok_ok(c2, T.V)) || (L >= 1 && !tok_ok(c1, T.V))) raise_status(T.status, SPECNG_DEV_TOKEN_OOR);
+    if (!tok_ok(c2, T.V)) c2 = -1;
+    if (!tok_ok(c1, T.V)) c1 = -1;
+    int n = 0;
+    int32_t* out = out_drafts + static_cast<size_t>(b) * max_k;
+    while (n < kmax && c1 >= 0) {
+        int tok = -1;
+        uint64_t v;
+        if (c2 >= 0 && find_value(T.tri_ctx, T.mask, key_tri_ctx(b, c2, c1), &v)) tok = best_token(v);
+        if (tok < 0 && find_value(T.bi_ctx, T.mask, key_bi_ctx(b, c1), &v)) tok = best_token(v);
+        if (tok < 0) break;
+        out[n++] = tok;
+        c2 = c1;
+        c1 = tok;
+    }
+    if (fallback != nullptr) {
+        const int32_t* fb = fallback + static_cast<size_t>(b) * max_k;
+        for (; n < kmax; ++n) out[n] = fb[n];
+    }
+    for (int t = n; t < max_k; ++t) out[t] = -1;
+    out_k[b] = n;
+}
+
+// One step's commit for every sequence, one warp per sequence: append the
+// emitted tokens (spec_append), index the new positions (ngram_update: pair
+// counts, then the contexts' best continuations) and draft the next step
+// (ngram_draft).  A sequence's keys belong to it alone, so the warp needs no
+// other sequence's work: __syncwarp orders its phases.
+__global__ void __launch_bounds__(kNgThreads) spec_commit_kernel(const NgramDev T, int parity, int32_t* hist,
+                                                                 int64_t stride, int32_t* lens, int64_t cap,
+                                                                 const int32_t* out_tokens, const int32_t* out_accept,
+                                                                 int K, int max_k, const int32_t* k_limit,
+                                                                 const int32_t* fallback, int32_t* out_drafts,
+                                                                 int32_t* out_k) {
+    const int lane = threadIdx.x & 31;
+    const int b = blockIdx.x * (kNgThreads / 32) + (threadIdx.x >> 5);
+    if (b >= T.B) return;
+    int32_t* h = hist + static_cast<size_t>(b) * stride;
+    // ---- append
+    int L = lens[b];
+    const int a = out_accept[b];
+    if (a < 0 || a > K) {
+        if (lane == 0) raise_status(T.status, SPECNG_DEV_BAD_K);
+    } else if (L < 0 || static_cast<int64_t>(L) + a + 1 > cap) {
+        if (lane == 0) raise_status(T.status, SPECNG_DEV_HIST_OVERFLOW);
+    } else {
+        if (lane <= a) h[L + lane] = out_tokens[static_cast<size_t>(b) * (K + 1) + lane];
+        L += a + 1;
+        if (lane == 0) lens[b] = L;
+    }
+    __syncwarp();
+    // ---- index positions [max(indexed, 1), L)
+    if (L < 0) L = 0;
+    if (static_cast<int64_t>(L) > stride) L = static_cast<int>(stride);
+    const int idx = T.indexed[parity][b];
+    if (L < idx && lane == 0) raise_status(T.status, SPECNG_DEV_HIST_SHRANK);
+    const int lo = idx > 1 ? idx : 1;
+    for (int i = lo + lane; i < L; i += 32) {
+        const int c = h[i], t1 = h[i - 1];
+        if (!tok_ok(c, T.V) || !tok_ok(t1, T.V)) { raise_status(T.status, SPECNG_DEV_TOKEN_OOR); continue; }
+        int64_t slot = find_or_insert(T.bi_pair, T.mask, key_bi_pair(b, t1, c));
+        if (slot < 0) {
+            raise_status(T.status, SPECNG_DEV_TABLE_FULL);
+        } else {
+            unsigned* v = reinterpret_cast<unsigned*>(&T.bi_pair[slot].y);
+            atomicAdd(v, 1u);
+            atomicMax(v + 1, static_cast<unsigned>(i));
+        }
+        if (i >= 2) {
+            const int t2 = h[i - 2];
+            if (!tok_ok(t2, T.V)) { raise_status(T.status, SPECNG_DEV_TOKEN_OOR); continue; }
+            slot = find_or_insert(T.tri_pair, T.mask, key_tri_pair(b, t2, t1, c));
+            if (slot < 0) {
+                raise_status(T.status, SPECNG_DEV_TABLE_FULL);
+            } else {
+                unsigned* v = reinterpret_cast<unsigned*>(&T.tri_pair[slot].y);
+                atomicAdd(v, 1u);
+                atomicMax(v + 1, static_cast<unsigned>(i));
+            }
+        }
+    }
+    __syncwarp();
+    for (int i = lo + lane; i < L; i += 32) {
+        const int c = h[i], t1 = h[i - 1];
+        if (!tok_ok(c, T.V) || !tok_ok(t1, T.V)) continue;
+        push_best(T, T.bi_pair, T.bi_ctx, key_bi_pair(b, t1, c), key_bi_ctx(b, t1), c);
+        if (i >= 2) {
+            const int t2 = h[i - 2];
+            if (!tok_ok(t2, T.V)) continue;
+            push_best(T, T.tri_pair, T.tri_ctx, key_tri_pair(b, t2, t1, c), key_tri_ctx(b, t2, t1), c);
+        }
+    }
+    __syncwarp();
+    if (lane == 0) {
+        T.indexed[parity ^ 1][b] = L > idx ? L : idx;
+        // ---- the next step's drafts
+        draft_one(T, b, h, L, max_k, k_limit, fallback, out_drafts, out_k);
+    }
 }
 
 __global__ void philox_kernel(const uint4* ctr, uint32_t k0, uint32_t k1, uint4* out, int64_t n) {
@@ -250,6 +335,17 @@ cudaError_t launch_ngram_clear(const NgramDev& T, cudaStream_t s) {
 cudaError_t launch_spec_append(int32_t* hist, int64_t stride, int32_t* lens, int64_t cap, const int32_t* out_tokens,
                                const int32_t* out_accept, int B, int K, unsigned* status, cudaStream_t s) {
     spec_append_kernel<<<(B + 127) / 128, 128, 0, s>>>(hist, stride, lens, cap, out_tokens, out_accept, B, K, status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_spec_commit(const NgramDev& T, int parity, int32_t* hist, int64_t stride, int32_t* lens,
+                               int64_t cap, const int32_t* out_tokens, const int32_t* out_accept, int K, int max_k,
+                               const int32_t* k_limit, const int32_t* fallback, int32_t* out_drafts, int32_t* out_k,
+                               cudaStream_t s) {
+    const int per = kNgThreads / 32;
+    spec_commit_kernel<<<(T.B + per - 1) / per, kNgThreads, 0, s>>>(T, parity, hist, stride, lens, cap, out_tokens,
+                                                                   out_accept, K, max_k, k_limit, fallback,
+                                                                   out_drafts, out_k);
     return cudaGetLastError();
 }
 

@@ -91,6 +91,10 @@ cudaError_t launch_ngram_draft(const NgramDev& T, const int32_t* hist, int64_t s
 cudaError_t launch_ngram_clear(const NgramDev& T, cudaStream_t s);
 cudaError_t launch_spec_append(int32_t* hist, int64_t stride, int32_t* lens, int64_t cap, const int32_t* out_tokens,
                                const int32_t* out_accept, int B, int K, unsigned* status, cudaStream_t s);
+cudaError_t launch_spec_commit(const NgramDev& T, int parity, int32_t* hist, int64_t stride, int32_t* lens,
+                               int64_t cap, const int32_t* out_tokens, const int32_t* out_accept, int K, int max_k,
+                               const int32_t* k_limit, const int32_t* fallback, int32_t* out_drafts, int32_t* out_k,
+                               cudaStream_t s);
 cudaError_t launch_philox(const uint32_t* ctr, uint64_t seed, uint32_t* out, int64_t n, cudaStream_t s);
 
 }  // namespace specng

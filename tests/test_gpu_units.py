@@ -250,3 +250,38 @@ def test_all_gated_reads_only_row_zero():
                          np.zeros((B, 1), int), np.zeros(B, int),
                          ov.VerifyParams(temperature=1.0, gate_enabled=False, seed=1), np.zeros(B), np.ones(B))
     np.testing.assert_array_equal(out.cpu().numpy()[:, 0], res["out_tokens"][:, 0])
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_commit_equals_append_update_draft(seed):
+    # spec_commit against the three calls it fuses, over several steps, and the
+    # drafts against the oracle on the resulting histories
+    rng = np.random.default_rng(100 + seed)
+    B, V, K, cap = 29, 9, 4, 300
+    hist, lens = _ngram_case(rng, B, V, 80, cap)
+    t1, t2 = sp.NgramTable(B, V, B * cap), sp.NgramTable(B, V, B * cap)
+    h1 = torch.from_numpy(hist.astype(np.int32)).cuda()
+    l1 = torch.from_numpy(lens.astype(np.int32)).cuda()
+    h2, l2 = h1.clone(), l1.clone()
+    sp.ngram_update(t1, h1, l1)
+    sp.ngram_update(t2, h2, l2)
+    for step in range(8):
+        a = torch.from_numpy(rng.integers(0, K + 1, size=B).astype(np.int32)).cuda()
+        if step == 5:
+            a.fill_(K)  # the longest history cannot take K + 1 more tokens below this step's cap
+        tok = torch.from_numpy(rng.integers(0, V, size=(B, K + 1)).astype(np.int32)).cuda()
+        lim = torch.from_numpy(rng.integers(0, K + 1, size=B).astype(np.int32)).cuda() if step % 2 else None
+        fb = torch.from_numpy(rng.integers(0, V, size=(B, K)).astype(np.int32)).cuda() if step % 3 == 0 else None
+        cap_now = cap if step != 5 else int(l1.max().item()) + 2   # some sequences overflow at step 5
+        sp.spec_append(h1, l1, tok, a, hist_cap=cap_now)
+        sp.ngram_update(t1, h1, l1)
+        d1, k1 = sp.ngram_draft(t1, h1, l1, K, k_limit=lim, fallback=fb)
+        d2, k2 = sp.spec_commit(t2, h2, l2, tok, a, K, k_limit=lim, fallback=fb, hist_cap=cap_now)
+        assert torch.equal(h1, h2) and torch.equal(l1, l2)
+        assert torch.equal(d1, d2) and torch.equal(k1, k2)
+        d_o, k_o = on.draft_batch(h2.cpu().numpy().astype(np.int64), l2.cpu().numpy().astype(np.int64), K,
+                                  k_limit=None if lim is None else lim.cpu().numpy(),
+                                  fallback=None if fb is None else fb.cpu().numpy())
+        np.testing.assert_array_equal(d2.cpu().numpy(), d_o)
+        np.testing.assert_array_equal(k2.cpu().numpy(), k_o)
+    assert sp.status_names(sp.get_status()) == ["HIST_OVERFLOW"]
