@@ -295,18 +295,50 @@ class Path:
         logits.view(-1)[idx] = newv
         return idx, old
 
+    def time_verify(self, calls: int = 60):
+        """Device time of spec_verify alone (its two or three kernels), on the
+        workload's current state.  Before each call a 1 GB memset flushes L2 and
+        keeps the GPU busy while the host enqueues the call, so the events
+        around it measure kernel time, not launch gaps.  kv_len / ema are
+        restored before every call: each call reads the same rows.
+        Returns (mean seconds per call, rows read per call)."""
+        sp, cfg = self.sp, self.cfg
+        kv0, ema0 = self.kv.clone(), self.ema.clone()
+        flush = torch.empty(1 << 30, dtype=torch.uint8, device=self.dev)
+        s0 = self.n_sets * 1000
+        drafts, k, q = (self.drafts, self.kbuf[s0 % self.kbuf.shape[0]], None) if self.ngram else (None, self.kfull, None)
+        if self.ngram:
+            self.first_drafts(s0 % self.kbuf.shape[0])
+        keff = k.clone()
+        if cfg.gate:
+            keff = torch.where((k > 0) & ~(ema0 >= self.params.ema_thresh), torch.zeros_like(k), k)
+        rows = int((keff + 1).sum().item())
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(calls)]
+        for i in range(calls + 3):
+            j = i % self.n_sets
+            if not self.ngram:
+                drafts, q = self.dsets[j], self.q[j]
+            self.kv.copy_(kv0)
+            self.ema.copy_(ema0)
+            flush.zero_()
+            self.params.step = s0 + i
+            if i >= 3:
+                evs[i - 3][0].record()
+            sp.spec_verify(self.logits[j], drafts, q, k, self.hist, self.lens, self.params, self.kv, self.ema,
+                           self.out, self.acc, self.ws)
+            if i >= 3:
+                evs[i - 3][1].record()
+        torch.cuda.synchronize()
+        self.kv.copy_(kv0)
+        self.ema.copy_(ema0)
+        t = [a.elapsed_time(b) / 1e3 for a, b in evs]
+        return statistics.mean(t), rows
+
     def rows_read(self, steps):
         cfg = self.cfg
         if self.ngram:
             return int((self.kbuf[:steps] + 1).sum().item())
         return steps * cfg.B * (cfg.K + 1)
-
-    def verify_bytes(self, steps):
-        cfg = self.cfg
-        elem = 2 if cfg.dtype == "bf16" else 4
-        rows = self.rows_read(steps)
-        small = steps * cfg.B * (4 * (2 * cfg.K + 8))
-        return rows * cfg.V * elem + small
 
 
 def run_ours(args):
@@ -356,7 +388,6 @@ def run_ours(args):
     verify_ms = [a.elapsed_time(b) for a, b in evs]
     # rows of the timed steps only
     rows_read = path.rows_read(base + args.steps) - path.rows_read(base)
-    vbytes = path.verify_bytes(base + args.steps) - path.verify_bytes(base)
     rows_nominal = args.steps * cfg.B * (cfg.K + 1)
     ms_max = max_over_ranks(ms, dev)
     status = sp.get_status(clear=True)
@@ -395,9 +426,12 @@ def run_ours(args):
             torch.distributed.destroy_process_group()
         return
     peak, peak_src = measured_peaks()
-    v_avg_s = statistics.mean(verify_ms) / 1e3
-    per_launch_bytes = vbytes / args.steps
+    # the kernels' own time (no launch gaps), for the roofline
+    v_avg_s, v_rows = path.time_verify()
+    elem = 2 if cfg.dtype == "bf16" else 4
+    per_launch_bytes = v_rows * cfg.V * elem + cfg.B * 4 * (2 * cfg.K + 8)
     achieved = per_launch_bytes / v_avg_s / 1e9
+    step_verify_us = statistics.mean(verify_ms) * 1e3
     traffic = ncu_traffic(args.workload)
     line = {
         "metric": METRIC,
@@ -420,11 +454,15 @@ def run_ours(args):
         },
         "rows_read_per_s": ws * rows_read / (ms_max / 1e3),
         "verify_us": v_avg_s * 1e6,
+        "verify_us_in_step": step_verify_us,
         "verify_logits_gbs": achieved,
         "roofline": {
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "traffic": traffic,
-            "kernel": "spec_verify call: verify_stream_kernel + verify_merge_kernel, timed together",
+            "kernel": "spec_verify call: verify_stream_kernel + verify_merge_kernel (+ verify_residual_kernel "
+                      "with dense q), timed together; CUDA events around each call after an L2-flushing memset, "
+                      "60 calls",
+            "rows_per_launch": v_rows,
             "peak_source": peak_src,
             "algorithmic_bytes_per_launch": per_launch_bytes,
         },

@@ -1178,8 +1178,23 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const VerifyDev P) {
 
 // ---------------------------------------------------------------- K2
 // Dense draft distributions: after a rejection at row a, sample from the
-// residual max(0, p_a - q_a) by Gumbel-max over row a (logits and q read once
-// more, for the rejected sequences only).
+// residual max(0, p_a - q_a) by Gumbel-max over row a (the logits of row a
+// read once more and q_a read at the candidates only, for the rejected
+// sequences).  log r_v <= log p_v = z_v / T - lse, so an element can beat
+// the threshold only if z_v / T - lse + g_max reaches it.  The threshold
+// starts from the exact residual score of the row's bonus sample (when its
+// residual is positive) and is shared by the CTA's warps and, through the
+// workspace, by the CTAs of the row.
+
+// log max(0, p - q) for log p = lp, in fp32 without cancellation: for q > 0,
+// p - q = q (e^(lp - ln q) - 1), and expm1 keeps the relative accuracy when
+// p and q are close.  -inf when the residual is zero.
+__device__ __forceinline__ float log_residual(float lp, float q) {
+    if (!(q > 0.0f)) return lp;
+    const float d = lp - logf(q);
+    if (!(d > 0.0f)) return -INFINITY;
+    return logf(q) + logf(expm1f(d));
+}
 
 template <bool BF16, bool SOFTCAP, bool PENALTY>
 __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const VerifyDev P) {
@@ -1190,6 +1205,8 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const Veri
     __shared__ int s_nwin;
     __shared__ Top2 s_t[kWarps];
     __shared__ int s_last;
+    __shared__ unsigned s_thr;
+    __shared__ uint16_t s_q2[kWarps * 32 * kNV * EPV];  // per-warp candidate queues (chunk offsets)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int K1 = P.K + 1;
@@ -1199,7 +1216,8 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const Veri
     if (!need) return;
     const int a = __ldcg(&P.seqres[b].a);
     const int row = b * K1 + a;
-    const float lse_f = static_cast<float>(__ldcg(&P.rowres[row].lse));
+    const double lse = __ldcg(&P.rowres[row].lse);
+    const float lse_f = static_cast<float>(lse);
     const int v0 = c * CHUNK;
     const int v1 = min(P.V, v0 + CHUNK);
     const char* rowp = static_cast<const char*>(P.logits) +
@@ -1207,49 +1225,127 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const Veri
     const float* qrow = P.q + (static_cast<size_t>(b) * P.K + a) * P.V;
     NoiseKey nk = P.nk;
     nk.seq = static_cast<uint32_t>(b);
+    const RowPhilox rp = row_philox(nk, static_cast<uint32_t>(a));
 
+    if (tid == 0) s_thr = 0u;
     if constexpr (PENALTY) build_window<CHUNK>(P, b, a, v0, v1, s_bm, s_win, &s_nwin);
-
+    __syncthreads();
+    // the chunk in registers: every thread's eight 16-byte vectors, loaded together
+    uint4 rv[kNV];
+#pragma unroll
+    for (int i = 0; i < kNV; ++i) {
+        const int e0 = v0 + (i * kThreads + tid) * EPV;
+        rv[i] = e0 < v1 ? load_vec<BF16>(rowp, e0, v1, P.aligned) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    auto lp_of = [&](float x, bool pen) { return transform_f32<SOFTCAP, PENALTY>(x, pen, P) * P.invT - lse_f; };
+    // ---- seed: each lane scores the residual of its largest p; the CTA and the row
+    //      share the best (any element's exact score bounds the best from below)
     Top2 tt = top2_empty();
+    int seeded = -1;
+    {
+        float lm = -INFINITY;
+        int im = -1;
+#pragma unroll
+        for (int i = 0; i < kNV; ++i) {
+            const int off = (i * kThreads + tid) * EPV;
+            const int nv = min(EPV, v1 - (v0 + off));
+            if (nv <= 0) continue;
+            float x[EPV];
+            unpack<BF16>(rv[i], x);
+            const unsigned pb = pen_bits<PENALTY, EPV>(s_bm, off);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) {
+                if (e >= nv) break;
+                const float lp = lp_of(x[e], (pb >> e) & 1u);
+                if (lp > lm) { lm = lp; im = v0 + off + e; }
+            }
+        }
+        float t0 = -INFINITY;
+        if (im >= 0) {
+            const float lr = log_residual(lm, __ldcs(qrow + im));
+            if (lr > -INFINITY) {
+                t0 = lr + gumbel_f32(pick_word(gumbel_block_row(rp, static_cast<uint32_t>(im) >> 2),
+                                               static_cast<uint32_t>(im) & 3u));
+                top2_push(tt, t0, im);
+                seeded = im;
+            }
+        }
+        const unsigned kw = warp_best_key(t0);
+        if (kw != 0u && lane == 0) atomicMax(&s_thr, kw);
+    }
+    __syncthreads();
+    if (tid == 0 && s_thr != 0u) atomicMax(&P.row_thr[row], s_thr);
     float thr = -INFINITY;
-    uint32_t cblk = 0xFFFFFFFFu;
-    uint4 cw = make_uint4(0u, 0u, 0u, 0u);
-    const float l2 = kLog2e;
-#pragma unroll 2
+    {
+        const unsigned kb = max(s_thr, __ldcg(&P.row_thr[row]));
+        if (kb != 0u) {
+            const float bw = key_score(kb);
+            thr = bw - cand_delta(bw);
+        }
+    }
+    // ---- candidates: log r_v <= lp_v, so lp_v + g_max must reach the threshold.  They
+    //      are compacted per warp (chunk offsets), then scored 32 at a time, so the
+    //      loads of a batch (the logit, from L2, and q) are issued together
+    uint16_t* qw = s_q2 + warp * (32 * kNV * EPV);
+    int nq = 0;
+#pragma unroll
     for (int i = 0; i < kNV; ++i) {
         const int off = (i * kThreads + tid) * EPV;
-        const int e0 = v0 + off;
-        const int nv = min(EPV, v1 - e0);
-        if (nv <= 0) continue;
-        const uint4 r = load_vec<BF16>(rowp, e0, v1, P.aligned);
-        float x[EPV], qv[EPV];
-        unpack<BF16>(r, x);
-        if (P.aligned) {
+        const int nv = min(EPV, v1 - (v0 + off));
+        unsigned mi = 0u;
+        if (nv > 0) {
+            float x[EPV];
+            unpack<BF16>(rv[i], x);
+            const unsigned pb = pen_bits<PENALTY, EPV>(s_bm, off);
 #pragma unroll
-            for (int h = 0; h < EPV / 4; ++h) {
-                const float4 q4 = __ldcs(reinterpret_cast<const float4*>(qrow + e0) + h);
-                qv[4 * h + 0] = q4.x; qv[4 * h + 1] = q4.y; qv[4 * h + 2] = q4.z; qv[4 * h + 3] = q4.w;
-            }
-        } else {
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) qv[e] = e < nv ? qrow[e0 + e] : 0.0f;
+            for (int e = 0; e < EPV; ++e)
+                if (e < nv && !(lp_of(x[e], (pb >> e) & 1u) + kGumbelMax < thr) && v0 + off + e != seeded) mi |= 1u << e;
         }
-        const unsigned pb = pen_bits<PENALTY, EPV>(s_bm, off);
+        const unsigned cnt = __popc(mi);
+        unsigned incl = cnt;
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-            if (e >= nv) break;
-            const float lp = transform_f32<SOFTCAP, PENALTY>(x[e], (pb >> e) & 1u, P) * P.invT - lse_f;
-            if (lp + kGumbelMax < thr) continue;
-            const float rsd = ex2_approx(lp * l2) - qv[e];
-            if (!(rsd > 0.0f)) continue;
-            const int v = e0 + e;
-            const uint32_t blk = static_cast<uint32_t>(v) >> 2;
-            if (blk != cblk) { cw = gumbel_block(nk, blk, static_cast<uint32_t>(a)); cblk = blk; }
-            const float score = logf(rsd) + gumbel_f32(pick_word(cw, static_cast<uint32_t>(v) & 3u));
-            if (score >= thr) {
-                top2_push(tt, score, v);
-                thr = fmaxf(thr, tt.s1 - cand_delta(tt.s1));
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        int slot = nq + static_cast<int>(incl - cnt);
+        while (mi != 0u) {
+            const int e = __ffs(mi) - 1;
+            mi &= mi - 1u;
+            qw[slot++] = static_cast<uint16_t>(off + e);
+        }
+        nq += static_cast<int>(__shfl_sync(0xffffffffu, incl, 31));
+    }
+    __syncwarp();
+    for (int base = 0; base < nq; base += 32) {
+        const int idx = base + lane;
+        const bool in = idx < nq;
+        const int loc = in ? static_cast<int>(qw[idx]) : 0;
+        const int v = v0 + loc;
+        const float x = in ? static_cast<float>(raw_logit_f64<BF16>(P.logits, row, P.V, v)) : 0.0f;
+        const float qv = in ? __ldcs(qrow + v) : 0.0f;
+        const bool pen = PENALTY && ((s_bm[loc >> 5] >> (loc & 31)) & 1u);
+        const float lp = lp_of(x, pen);
+        const float lr = in && !(lp + kGumbelMax < thr) ? log_residual(lp, qv) : -INFINITY;
+        const bool live = lr > -INFINITY;
+        if (__any_sync(0xffffffffu, live)) {
+            const uint32_t word = pick_word(gumbel_block_row(rp, static_cast<uint32_t>(v) >> 2),
+                                            static_cast<uint32_t>(v) & 3u);
+            if (live && gumbel_may_reach(word, thr - lr - 1e-4f)) {
+                const float score = lr + gumbel_f32(word);
+                if (score >= thr) {
+                    top2_push(tt, score, v);
+                    thr = fmaxf(thr, tt.s1 - cand_delta(tt.s1));
+                }
             }
+        }
+        // share the warp's best with the CTA, adopt the CTA's
+        const unsigned kw = warp_best_key(tt.s1);
+        if (kw != 0u && lane == 0) atomicMax(&s_thr, kw);
+        const unsigned kb = max(*reinterpret_cast<volatile unsigned*>(&s_thr), kw);
+        if (kb != 0u) {
+            const float bw = key_score(kb);
+            thr = fmaxf(thr, bw - cand_delta(bw));
         }
     }
     tt = top2_warp_reduce(tt);
@@ -1269,7 +1365,10 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const Veri
     __syncthreads();
     if (!s_last || warp != 0) return;
     __threadfence();
-    if (lane == 0) P.seq_ticket2[b] = 0u;
+    if (lane == 0) {
+        P.seq_ticket2[b] = 0u;
+        P.row_thr[row] = 0u;  // leave the workspace zeroed
+    }
     const Partial* pr = P.part2 + static_cast<size_t>(b) * P.nchunk;
     Top2 t = top2_empty();
     for (int cc = lane; cc < P.nchunk; cc += 32) t = top2_merge(t, ldcg_partial(pr + cc).t);
@@ -1280,7 +1379,6 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const Veri
     const bool pen1 = PENALTY && t.i1 >= 0 ? warp_in_window(t.i1, s_win, nw) : false;
     const bool pen2 = PENALTY && t.i2 >= 0 ? warp_in_window(t.i2, s_win, nw) : false;
     if (lane != 0) return;
-    const double lse = __ldcg(&P.rowres[row].lse);
     const int bonus = __ldcg(&P.rowres[row].winner);
     st_zero(P.rowres + row);
     st_zero(P.seqres + b);
