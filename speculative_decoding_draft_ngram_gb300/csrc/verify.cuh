@@ -1048,11 +1048,29 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const VerifyDev P) {
     const WindowView wv{PENALTY ? P.hist + static_cast<size_t>(b) * P.hist_stride + (L - nh) : nullptr,
                         P.drafts + static_cast<size_t>(b) * P.K, nh, PENALTY ? P.W : 0};
 
+    // the draft's logit (and q) are loaded first: their latency overlaps the partials'
+    const int dnext = j < keff ? wv.drafts[j] : -1;
+    const bool dvalid = dnext >= 0 && dnext < P.V;
+    float xd = 0.0f, qd = 1.0f;
+    if (!GREEDY && lane == 0 && dvalid) {
+        xd = static_cast<float>(raw_logit_f64<BF16>(P.logits, row, P.V, dnext));
+        if (dense) qd = P.q[(static_cast<size_t>(b) * P.K + j) * P.V + dnext];
+    }
+
     // one partial per row segment, stored at the segment's last chunk; the
-    // other slots are all-zero (a written partial never is)
+    // other slots are all-zero (a written partial never is).  A lane holds at
+    // most a few of them (chunks <= 32 for V <= 2^18 bf16 / 2^17 fp32).
     Partial* pr = P.part + static_cast<size_t>(row) * P.nchunk;
+    constexpr int kHeld = 2;
+    Partial held[kHeld];
     float mf = -INFINITY;
-    for (int cc = lane; cc < P.nchunk; cc += 32) {
+#pragma unroll
+    for (int h = 0; h < kHeld; ++h) {
+        const int cc = lane + 32 * h;
+        held[h] = cc < P.nchunk ? ldcg_partial(pr + cc) : Partial{0.0f, 0.0f, top2_empty(), {0, 0}};
+        if (cc < P.nchunk && (held[h].s != 0.0f || __float_as_uint(held[h].m) != 0u)) mf = fmaxf(mf, held[h].m);
+    }
+    for (int cc = lane + 32 * kHeld; cc < P.nchunk; cc += 32) {
         const Partial p = ldcg_partial(pr + cc);
         if (p.s != 0.0f || __float_as_uint(p.m) != 0u) mf = fmaxf(mf, p.m);
     }
@@ -1060,7 +1078,14 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const VerifyDev P) {
     for (int off = 16; off > 0; off >>= 1) mf = fmaxf(mf, __shfl_xor_sync(0xffffffffu, mf, off));
     double S = 0.0;
     Top2 t = top2_empty();
-    for (int cc = lane; cc < P.nchunk; cc += 32) {
+#pragma unroll
+    for (int h = 0; h < kHeld; ++h) {
+        const Partial& p = held[h];
+        if (lane + 32 * h >= P.nchunk || (p.s == 0.0f && __float_as_uint(p.m) == 0u)) continue;
+        if (!GREEDY && p.m > -INFINITY) S += static_cast<double>(p.s) * static_cast<double>(expf((p.m - mf) * P.invT));
+        t = top2_merge(t, p.t);
+    }
+    for (int cc = lane + 32 * kHeld; cc < P.nchunk; cc += 32) {
         const Partial p = ldcg_partial(pr + cc);
         if (p.s == 0.0f && __float_as_uint(p.m) == 0u) continue;
         if (!GREEDY && p.m > -INFINITY) S += static_cast<double>(p.s) * static_cast<double>(expf((p.m - mf) * P.invT));
@@ -1100,16 +1125,14 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const VerifyDev P) {
 
     // accept test of d_{j+1}: fp32 unless within 1e-4 of the boundary, then fp64
     int accepted = 0;
-    const int dnext = j < keff ? wv.drafts[j] : -1;
-    if (j < keff && dnext >= 0 && dnext < P.V) {
+    if (j < keff && dvalid) {
         if constexpr (GREEDY) {
             accepted = dnext == winner;
         } else {
             const bool pend = PENALTY ? wv.warp_has(j, dnext) : false;
             if (lane == 0) {
                 const double u = accept_uniform_f64(nk, static_cast<uint32_t>(j + 1));
-                const double q = dense ? static_cast<double>(P.q[(static_cast<size_t>(b) * P.K + j) * P.V + dnext]) : 1.0;
-                const float xd = static_cast<float>(raw_logit_f64<BF16>(P.logits, row, P.V, dnext));
+                const double q = dense ? static_cast<double>(qd) : 1.0;
                 const float lp = transform_f32<SOFTCAP, PENALTY>(xd, pend, P) * P.invT - static_cast<float>(lse);
                 const float lr = logf(static_cast<float>(u)) + logf(static_cast<float>(q));
                 if (lr < lp - 1e-4f * (1.0f + fabsf(lp))) {
