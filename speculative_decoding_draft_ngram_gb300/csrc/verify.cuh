@@ -725,8 +725,13 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                     if (t1 > thr) { thr = t1; set_xt(); }
                 }
             };
-            set_xt();
-            sync_thr();
+            if (cand) {
+                set_xt();
+                sync_thr();
+            } else {
+                xt = INFINITY;
+                xt2 = 0x7F807F80u;
+            }
             // ---- one pass over the slice: all four 16-byte vectors are loaded first; the
             //      online maximum and the 32 exponentials (packed fp32x2 arithmetic) form one
             //      independent block; candidate masks are formed only for the vectors whose
@@ -889,6 +894,7 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                 const int si = so / (32 * EPV), se = so - si * 32 * EPV;
                 if (se >= 0 && se < EPV) msk &= ~(1u << (8 * si + se));
             }
+            if (cand) {
             // ---- queue the slice's candidates (chunk offsets of this stage)
             const unsigned cnt = __popc(msk);
             const int nq = static_cast<int>(__reduce_add_sync(0xffffffffu, cnt));
@@ -966,6 +972,7 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                 thr = fmaxf(thr, bw - cand_delta(bw));
                 if (lane == 0) atomicMax(rth, kw);
             }
+            }  // cand
         }
         fresh = mt.seg_end != 0;
         if (fresh) {
