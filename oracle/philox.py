@@ -12,17 +12,42 @@ Shaw, "Parallel random numbers: as easy as 1, 2, 3" (SC'11), keyed by the
 step, sequence).  This module is written from that paper's definition and
 shares no code with the GPU library, which has its own implementation.
 
+Sampling noise.  The sampler takes argmax_v (log w_v - ln E_v) with E_v
+i.i.d. Exp(1), i.e. Gumbel-max with g_v = -ln E_v.  The E_v of the 1024
+vocab ids of one block (ids 1024 b .. 1024 b + 1023) are drawn through the
+Renyi representation of exponential order statistics: the smallest of n
+i.i.d. Exp(1) variates is Exp(n); its position is uniform on the n slots
+and independent of it; and, the distribution being memoryless, the other
+n - 1 exceed it by i.i.d. Exp(1) amounts.  So with one block draw
+(M ~ Exp(1024), I uniform on 0..1023) and one draw F_v ~ Exp(1) per id,
+
+    E_v = M          if v mod 1024 == I
+    E_v = M + F_v    otherwise,
+
+the E_v are exactly i.i.d. Exp(1), and every score of the block is bounded
+by log w_v - ln M.  (Ids beyond the vocabulary fill the last block; their
+weight is zero, so they never win.)  An Exp(1) variate is E = -ln u for a
+Philox uniform u, taken as -log1p(u - 1) when u > 1/2, where u - 1 is exact.
+
 Counter layout (both sides follow it):
 
-    GUMBEL draw for vocab id v at row ``pos``:
+    element draw F_v for vocab id v at row ``pos``:
         counter = (v >> 2, pos | 0 << 16, step mod 2**32, seq), word v & 3
+    block draw (M, I) for block b = v >> 10 at row ``pos``:
+        counter = (b, pos | 2 << 16, step mod 2**32, seq);
+        M = E(word 0) / 1024, I = word 1 & 1023
     ACCEPT draw for draft i (1-based):
         counter = (0, i | 1 << 16, step mod 2**32, seq), word 0
     key = (seed mod 2**32, seed >> 32)
 
+With u on the 2**-24 grid, g_v lies in about [-2.82, 23.57] (the top end is
+-ln of the smallest M); the truncation is a bias of order 2**-24 per draw.
+
 Pinned by: tests/test_oracle_philox.py (against Triton's independent
 Philox implementation run on the CPU interpreter, uniformity chi-square,
-and the exactness of the uniform grid).
+the exactness of the uniform grid, and the block construction: the law of
+the block minimum and of its position, the Exp(1) marginals, and
+Gumbel-max against softmax over several blocks).
 """
 from __future__ import annotations
 
@@ -37,6 +62,10 @@ PHILOX_ROUNDS = 10
 
 PURPOSE_GUMBEL = 0
 PURPOSE_ACCEPT = 1
+PURPOSE_BLOCK = 2
+
+NOISE_BLOCK = 1024          # vocab ids per block draw (a power of two)
+NOISE_BLOCK_SHIFT = 10
 
 _MASK32 = np.uint64(0xFFFFFFFF)
 
@@ -86,46 +115,88 @@ def uniform_from_word(w) -> np.ndarray:
     return (2.0 * m + 1.0) * 2.0 ** -24
 
 
-def gumbel_from_uniform(u) -> np.ndarray:
-    """Standard Gumbel variate g = -ln(-ln u).
+def exp_from_uniform(u) -> np.ndarray:
+    """Exp(1) variate E = -ln u.
 
-    For u > 1/2 the inner logarithm is taken as log1p(u - 1): u - 1 is exact
-    there, which keeps the upper tail (where the winners of a Gumbel-max
-    come from) accurate.  With u on the 2**-24 grid, g lies in about
-    [-2.81, 16.64]; the truncation is a bias of order 2**-24 per draw.
+    For u > 1/2 the logarithm is taken as log1p(u - 1): u - 1 is exact
+    there, which keeps small E (the large Gumbel values that win a
+    Gumbel-max) accurate.
     """
     u = np.asarray(u, dtype=np.float64)
-    e = np.where(u > 0.5, -np.log1p(u - 1.0), -np.log(u))
-    return -np.log(e)
+    return np.where(u > 0.5, -np.log1p(u - 1.0), -np.log(u))
+
+
+def gumbel_from_uniform(u) -> np.ndarray:
+    """Standard Gumbel variate -ln(-ln u) of one uniform (a single Exp(1) draw)."""
+    return -np.log(exp_from_uniform(u))
+
+
+def _ctr(step, seq, pos, purpose):
+    pos = np.asarray(pos, dtype=np.uint64)
+    return (pos | np.uint64(purpose << 16), np.uint64(int(step) & 0xFFFFFFFF),
+            np.asarray(seq, dtype=np.uint64))
+
+
+def block_draw(seed: int, seq, step: int, pos, blk):
+    """(M, I) of vocab block ``blk`` at row ``pos``: M ~ Exp(1024), I uniform on 0..1023."""
+    k0, k1 = seed_key(seed)
+    c1, c2, c3 = _ctr(step, seq, pos, PURPOSE_BLOCK)
+    w0, w1, _, _ = philox4x32_10(np.asarray(blk, dtype=np.uint64), c1, c2, c3, k0, k1)
+    M = exp_from_uniform(uniform_from_word(w0)) / NOISE_BLOCK
+    I = (w1 & np.uint64(NOISE_BLOCK - 1)).astype(np.int64)
+    return M, I
+
+
+def element_exp(seed: int, seq, step: int, pos, v) -> np.ndarray:
+    """F_v ~ Exp(1), the per-id draw (before the block minimum is added)."""
+    k0, k1 = seed_key(seed)
+    v = np.asarray(v, dtype=np.uint64)
+    c1, c2, c3 = _ctr(step, seq, pos, PURPOSE_GUMBEL)
+    words = philox4x32_10(v >> np.uint64(2), c1, c2, c3, k0, k1)
+    lane = (v & np.uint64(3)).astype(np.int64)
+    w = np.choose(np.broadcast_to(lane, words[0].shape), words)
+    return exp_from_uniform(uniform_from_word(w))
+
+
+def exp_noise(seed: int, seq, step: int, pos, v) -> np.ndarray:
+    """E_v ~ Exp(1) for (seq, step, pos, vocab id v); arguments broadcast."""
+    v = np.asarray(v, dtype=np.int64)
+    M, I = block_draw(seed, seq, step, pos, v >> NOISE_BLOCK_SHIFT)
+    F = element_exp(seed, seq, step, pos, v)
+    return np.where((v & (NOISE_BLOCK - 1)) == I, M, M + F)
 
 
 def gumbel_noise(seed: int, seq, step: int, pos, v) -> np.ndarray:
-    """Gumbel noise g for (seq, step, pos, vocab id v); arguments broadcast."""
-    k0, k1 = seed_key(seed)
-    v = np.asarray(v, dtype=np.uint64)
-    pos = np.asarray(pos, dtype=np.uint64)
-    seq = np.asarray(seq, dtype=np.uint64)
-    c1 = pos | np.uint64(PURPOSE_GUMBEL << 16)
-    words = philox4x32_10(v >> np.uint64(2), c1, np.uint64(int(step) & 0xFFFFFFFF), seq, k0, k1)
-    lane = (v & np.uint64(3)).astype(np.int64)
-    w = np.choose(np.broadcast_to(lane, words[0].shape), words)
-    return gumbel_from_uniform(uniform_from_word(w))
+    """Gumbel noise g_v = -ln E_v for (seq, step, pos, vocab id v); arguments broadcast."""
+    return -np.log(exp_noise(seed, seq, step, pos, v))
 
 
-def gumbel_row(seed: int, seq, step: int, pos, V: int) -> np.ndarray:
-    """Gumbel noise for vocab ids 0..V-1 of row ``pos``: shape broadcast(seq, pos) + (V,).
+def exp_row(seed: int, seq, step: int, pos, V: int) -> np.ndarray:
+    """E_v for vocab ids 0..V-1 of row ``pos``: shape broadcast(seq, pos) + (V,).
 
-    Same values as ``gumbel_noise(..., v=arange(V))``; each Philox block is
-    evaluated once and its four words serve four consecutive ids.
+    Same values as ``exp_noise(..., v=arange(V))``; each Philox block is
+    evaluated once: four words serve four consecutive ids, one block draw
+    serves 1024 ids.
     """
     k0, k1 = seed_key(seed)
     seq = np.asarray(seq, dtype=np.uint64)[..., None]
     pos = np.asarray(pos, dtype=np.uint64)[..., None]
-    blocks = np.arange((V + 3) // 4, dtype=np.uint64)
-    c1 = pos | np.uint64(PURPOSE_GUMBEL << 16)
-    words = philox4x32_10(blocks, c1, np.uint64(int(step) & 0xFFFFFFFF), seq, k0, k1)
+    c1, c2, c3 = _ctr(step, seq, pos, PURPOSE_GUMBEL)
+    quads = np.arange((V + 3) // 4, dtype=np.uint64)
+    words = philox4x32_10(quads, c1, c2, c3, k0, k1)
     w = np.stack(words, axis=-1).reshape(words[0].shape[:-1] + (-1,))[..., :V]
-    return gumbel_from_uniform(uniform_from_word(w))
+    F = exp_from_uniform(uniform_from_word(w))
+    nblk = (V + NOISE_BLOCK - 1) // NOISE_BLOCK
+    M, I = block_draw(seed, seq, step, pos, np.arange(nblk, dtype=np.uint64))
+    v = np.arange(V)
+    Mv = np.repeat(M, NOISE_BLOCK, axis=-1)[..., :V]
+    Iv = np.repeat(I, NOISE_BLOCK, axis=-1)[..., :V]
+    return np.where((v & (NOISE_BLOCK - 1)) == Iv, Mv, Mv + F)
+
+
+def gumbel_row(seed: int, seq, step: int, pos, V: int) -> np.ndarray:
+    """Gumbel noise -ln E_v for vocab ids 0..V-1 of row ``pos`` (see ``exp_row``)."""
+    return -np.log(exp_row(seed, seq, step, pos, V))
 
 
 def accept_uniform(seed: int, seq, step: int, i) -> np.ndarray:
