@@ -13,15 +13,15 @@ step, sequence).  This module is written from that paper's definition and
 shares no code with the GPU library, which has its own implementation.
 
 Sampling noise.  The sampler takes argmax_v (log w_v - ln E_v) with E_v
-i.i.d. Exp(1), i.e. Gumbel-max with g_v = -ln E_v.  The E_v of the 1024
-vocab ids of one block (ids 1024 b .. 1024 b + 1023) are drawn through the
+i.i.d. Exp(1), i.e. Gumbel-max with g_v = -ln E_v.  The E_v of the 256
+vocab ids of one block (ids 256 b .. 256 b + 255) are drawn through the
 Renyi representation of exponential order statistics: the smallest of n
 i.i.d. Exp(1) variates is Exp(n); its position is uniform on the n slots
 and independent of it; and, the distribution being memoryless, the other
 n - 1 exceed it by i.i.d. Exp(1) amounts.  So with one block draw
-(M ~ Exp(1024), I uniform on 0..1023) and one draw F_v ~ Exp(1) per id,
+(M ~ Exp(256), I uniform on 0..255) and one draw F_v ~ Exp(1) per id,
 
-    E_v = M          if v mod 1024 == I
+    E_v = M          if v mod 256 == I
     E_v = M + F_v    otherwise,
 
 the E_v are exactly i.i.d. Exp(1), and every score of the block is bounded
@@ -33,14 +33,14 @@ Counter layout (both sides follow it):
 
     element draw F_v for vocab id v at row ``pos``:
         counter = (v >> 2, pos | 0 << 16, step mod 2**32, seq), word v & 3
-    block draw (M, I) for block b = v >> 10 at row ``pos``:
+    block draw (M, I) for block b = v >> 8 at row ``pos``:
         counter = (b, pos | 2 << 16, step mod 2**32, seq);
-        M = E(word 0) / 1024, I = word 1 & 1023
+        M = E(word 0) / 256, I = word 1 & 255
     ACCEPT draw for draft i (1-based):
         counter = (0, i | 1 << 16, step mod 2**32, seq), word 0
     key = (seed mod 2**32, seed >> 32)
 
-With u on the 2**-24 grid, g_v lies in about [-2.82, 23.57] (the top end is
+With u on the 2**-24 grid, g_v lies in about [-2.82, 22.18] (the top end is
 -ln of the smallest M); the truncation is a bias of order 2**-24 per draw.
 
 Pinned by: tests/test_oracle_philox.py (against Triton's independent
@@ -64,8 +64,8 @@ PURPOSE_GUMBEL = 0
 PURPOSE_ACCEPT = 1
 PURPOSE_BLOCK = 2
 
-NOISE_BLOCK = 1024          # vocab ids per block draw (a power of two)
-NOISE_BLOCK_SHIFT = 10
+NOISE_BLOCK = 256           # vocab ids per block draw (a power of two)
+NOISE_BLOCK_SHIFT = 8
 
 _MASK32 = np.uint64(0xFFFFFFFF)
 
@@ -138,7 +138,7 @@ def _ctr(step, seq, pos, purpose):
 
 
 def block_draw(seed: int, seq, step: int, pos, blk):
-    """(M, I) of vocab block ``blk`` at row ``pos``: M ~ Exp(1024), I uniform on 0..1023."""
+    """(M, I) of vocab block ``blk`` at row ``pos``: M ~ Exp(256), I uniform on 0..255."""
     k0, k1 = seed_key(seed)
     c1, c2, c3 = _ctr(step, seq, pos, PURPOSE_BLOCK)
     w0, w1, _, _ = philox4x32_10(np.asarray(blk, dtype=np.uint64), c1, c2, c3, k0, k1)
@@ -176,7 +176,7 @@ def exp_row(seed: int, seq, step: int, pos, V: int) -> np.ndarray:
 
     Same values as ``exp_noise(..., v=arange(V))``; each Philox block is
     evaluated once: four words serve four consecutive ids, one block draw
-    serves 1024 ids.
+    serves 256 ids.
     """
     k0, k1 = seed_key(seed)
     seq = np.asarray(seq, dtype=np.uint64)[..., None]

@@ -106,27 +106,18 @@ __device__ __forceinline__ uint32_t pick_word(const uint4& w, uint32_t lane) {
     return lane == 0 ? w.x : lane == 1 ? w.y : lane == 2 ? w.z : w.w;
 }
 
-// e^-t with the hardware exp2 (relative error ~2^-22).
-__device__ __forceinline__ float exp2f_approx_neg(float t) {
-    float y;
-    const float a = -t * 1.4426950408889634f;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(a));
-    return y;
-}
-
 // u = (2 (w >> 9) + 1) 2^-24: exact in fp32 and fp64, strictly inside (0, 1).
 __device__ __forceinline__ uint32_t uniform_numerator(uint32_t w) { return ((w >> 9) << 1) | 1u; }
 
-__device__ __forceinline__ float gumbel_f32(uint32_t w) {
+// Exp(1) variate -ln u of a Philox word; -log1p(u - 1) above 1/2, where u - 1
+// is exact, keeps small values (the large Gumbel values) accurate.
+__device__ __forceinline__ float exp_of_word(uint32_t w) {
     const float u = static_cast<float>(uniform_numerator(w)) * 0x1p-24f;
-    const float e = u > 0.5f ? -log1pf(u - 1.0f) : -logf(u);
-    return -logf(e);
+    return u > 0.5f ? -log1pf(u - 1.0f) : -logf(u);
 }
-
-__device__ __forceinline__ double gumbel_f64(uint32_t w) {
+__device__ __forceinline__ double exp_of_word_f64(uint32_t w) {
     const double u = static_cast<double>(uniform_numerator(w)) * 0x1p-24;
-    const double e = u > 0.5 ? -log1p(u - 1.0) : -log(u);
-    return -log(e);
+    return u > 0.5 ? -log1p(u - 1.0) : -log(u);
 }
 
 __device__ __forceinline__ double accept_uniform_f64(const NoiseKey& nk, uint32_t i) {
@@ -134,20 +125,73 @@ __device__ __forceinline__ double accept_uniform_f64(const NoiseKey& nk, uint32_
     return static_cast<double>(uniform_numerator(w.x)) * 0x1p-24;
 }
 
-// Conservative screen: false only when the Gumbel variate of word w is surely
-// below t (so a score zb + g cannot reach zb + t).  g >= t  <=>  1 - u <= 1 - exp(-e^-t);
-// 1 - u is an exact integer multiple of 2^-24, the right side is computed with
-// the hardware exp2 and widened by a margin far above its error.
-__device__ __forceinline__ bool gumbel_may_reach(uint32_t w, float t) {
-    const float y = exp2f_approx_neg(t);
-    const float c = y < 1e-3f ? y * fmaf(-0.5f, y, 1.0f) : 1.0f - exp2f_approx_neg(y);
-    const float one_minus_u = static_cast<float>(0x1000000u - uniform_numerator(w));  // (1 - u) * 2^24, exact
-    return one_minus_u <= fmaf(c, 16777216.0f * 1.001f, 2.0f);
+// ---------------------------------------------------------------- sampling noise
+// The sampler's noise is g_v = -ln E_v with E_v i.i.d. Exp(1), drawn per block
+// of 256 vocab ids through the Renyi representation of exponential order
+// statistics: one block draw gives the block minimum M ~ Exp(256) (word 0,
+// scaled by 2^-8) and the slot I of the id holding it (word 1, low 8 bits,
+// uniform); every other id adds its own Exp(1) draw F_v, E_v = M + F_v.  Any
+// score of the block is therefore at most log w_v - ln M, which prunes whole
+// blocks before a single per-id draw is made.
+
+constexpr uint32_t kPurposeBlock = 2u;
+constexpr int kNoiseBlockShift = 8;
+constexpr uint32_t kNoiseBlockMask = (1u << kNoiseBlockShift) - 1u;
+
+__device__ __forceinline__ uint4 block_words(const NoiseKey& nk, uint32_t blk, uint32_t pos) {
+    return philox4x32_10(make_uint4(blk, pos | (kPurposeBlock << 16), nk.step, nk.seq), nk.k0, nk.k1);
 }
 
-// Upper bound of a Gumbel draw on the 2^-24 grid (-ln(-ln(1 - 2^-24)) = 16.6355),
-// with slack for fp32 rounding.
-constexpr float kGumbelMax = 16.7f;
+struct BlockNoise {
+    float M, lnM;  // block minimum and its logarithm (fp32)
+    int I;         // slot (v & 255) of the id whose E is M
+    int pad;
+};
+
+__device__ __forceinline__ BlockNoise block_noise(const NoiseKey& nk, uint32_t blk, uint32_t pos) {
+    const uint4 w = block_words(nk, blk, pos);
+    BlockNoise r;
+    r.M = exp_of_word(w.x) * 0x1p-8f;
+    r.lnM = logf(r.M);  // exact to an ulp: it bounds every score of the block
+    r.I = static_cast<int>(w.y & kNoiseBlockMask);
+    r.pad = 0;
+    return r;
+}
+
+// Screening precision (fp32 scores that only order candidates; every final
+// decision between close scores is re-taken in fp64).  -ln u for a Philox
+// word: above 1/2, with x = u - 1 (exact) and s = x / (2 + x),
+// -ln u = -log1p(x) = -2 atanh(s) = -2 s (1 + s^2/3 + s^4/5 + s^6/7 + s^8/9 + ...),
+// |s| <= 1/3, truncated after s^8/9 (relative error below 2e-6); below 1/2,
+// -ln u >= ln 2 and the hardware logarithm's error is relative to it.
+__device__ __forceinline__ float exp_of_word_fast(uint32_t w) {
+    const float u = static_cast<float>(uniform_numerator(w)) * 0x1p-24f;
+    if (u > 0.5f) {
+        const float x = u - 1.0f;
+        const float sv = __fdividef(x, 2.0f + x);
+        const float s2 = sv * sv;
+        const float poly = fmaf(s2, fmaf(s2, fmaf(s2, fmaf(s2, 1.0f / 9.0f, 1.0f / 7.0f), 0.2f), 1.0f / 3.0f), 1.0f);
+        return -2.0f * sv * poly;
+    }
+    return -__logf(u);
+}
+
+// E_v in fp32 for an id of a block with minimum M and argmin slot I (rp: the row's element draws).
+__device__ __forceinline__ float noise_exp_f32(const RowPhilox& rp, float M, int I, uint32_t v) {
+    if (static_cast<int>(v & kNoiseBlockMask) == I) return M;
+    return M + exp_of_word_fast(pick_word(gumbel_block_row(rp, v >> 2), v & 3u));
+}
+
+// ln E at screening precision: 3 ulp of |ln E| (hardware logarithm).
+__device__ __forceinline__ float ln_fast(float e) { return __logf(e); }
+
+// E_v in fp64, the oracle's arithmetic, for the final decisions.
+__device__ __forceinline__ double noise_exp_f64(const NoiseKey& nk, uint32_t v, uint32_t pos) {
+    const uint4 bw = block_words(nk, v >> kNoiseBlockShift, pos);
+    const double M = exp_of_word_f64(bw.x) * 0x1p-8;
+    if ((v & kNoiseBlockMask) == (bw.y & kNoiseBlockMask)) return M;
+    return M + exp_of_word_f64(pick_word(gumbel_block(nk, v >> 2, pos), v & 3u));
+}
 
 // Candidates whose fp32 score is below (best - delta) cannot win once the
 // final choice is re-scored in fp64: delta is far above the fp32 error of a
@@ -244,6 +288,16 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, unsigned bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
+}
+
+// Raise the expected transaction bytes of the current phase without arriving.
+__device__ __forceinline__ void mbar_add_tx(uint64_t* bar, unsigned bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // dst and src 16-byte aligned, bytes a multiple of 16.

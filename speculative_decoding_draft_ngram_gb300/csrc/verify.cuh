@@ -1,5 +1,6 @@
-// spec_verify kernels (sm_103a): the streaming pass over the logit rows, the
-// dense-q residual pass, and the per-row / per-sequence epilogues.
+// spec_verify kernels (sm_103a): the streaming pass over the logit rows with
+// the row merges and sequence epilogues folded in, and the dense-q residual
+// pass.
 //
 // Method (SwiftLM page, paragraph on algorithmic equivalence after Leviathan
 // et al.; AX Engine page, "Core Technical Architecture & Methods"):
@@ -7,28 +8,14 @@
 //   p_j = softmax(x_j / T); accept draft i iff u_i q(d_i) <= p(d_i)
 //   a = number accepted before the first rejection (<= k_eff, EMA gate)
 //   sample at row a: residual max(0, p_a - q_a) on a rejection, p_a (bonus)
-//   otherwise, by Gumbel-max with Philox noise; T = 0: argmax matching
+//   otherwise, by Gumbel-max argmax_v (log w_v - ln E_v); T = 0: argmax
 //   epilogue: tokens, kv_len <- kv_len - k + a, EMA update.
 //
-// Design (one GPU, HBM-bound):
-//   * grid = (sequence, row, V-chunk); a CTA of 256 threads owns one chunk
-//     of one row; each thread keeps its 8 x 16-byte vectors in registers, so
-//     the chunk is read from HBM exactly once with coalesced 16-byte loads;
-//   * pass A over the registers: per-vector maximum (the soft cap is
-//     monotone, so it is applied to the vector maximum only);
-//   * pass B: sum of exponentials against the thread's own maximum (no
-//     rescaling in the loop) and Gumbel candidates.  A vector is skipped
-//     unless max(x)/T + g_max can still reach the current threshold, and
-//     Philox runs only for the few elements that pass; the threshold is seeded
-//     per warp by the exact score of the warp's largest element;
-//   * candidates are kept as the top two by fp32 score; the last CTA of a
-//     row merges the chunk partials (max / sum in fp64, candidates), re-scores
-//     the two candidates in fp64 from the raw logits and takes the accept
-//     test in fp64, so the integer decisions are taken in the oracle's
-//     precision;
-//   * cross-CTA merges use the fence + atomic ticket pattern: the last CTA of
-//     a row merges the row; the last row of a sequence runs the epilogue.
-//     Nothing waits on another CTA.
+// The noise E_v is drawn per block of 256 ids (block minimum M and its slot,
+// then E_v = M + F_v for the others; see common.cuh), so a score of a block is
+// at most log w_v - ln M.  The streaming pass keeps, per row, the running
+// best score; a block whose largest logit cannot reach it under that bound
+// is skipped without a single per-id draw.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -37,20 +24,19 @@
 
 namespace specng {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kNV = 8;  // 16-byte vectors per thread per chunk
-
 template <bool BF16> struct ElemTraits;
 template <> struct ElemTraits<true> { static constexpr int EPV = 8; static constexpr int SIZE = 2; };
 template <> struct ElemTraits<false> { static constexpr int EPV = 4; static constexpr int SIZE = 4; };
 
+// One chunk of a row = one 32 KB stage of the streaming ring = one CTA of the
+// residual pass.
+constexpr int kChunkBytes = 32768;
 template <bool BF16>
-__host__ __device__ constexpr int chunk_elems() { return kThreads * kNV * ElemTraits<BF16>::EPV; }
+__host__ __device__ constexpr int chunk_elems() { return kChunkBytes / ElemTraits<BF16>::SIZE; }
 
 // Workspace records.
 struct __align__(32) Partial {
-    float m, s;  // chunk maximum (transformed units) and sum of exp((z - m) / T)
+    float m, s;  // maximum (transformed units) and sum of exp((z - m) / T) of a row segment
     Top2 t;      // top-two candidates (fp32 scores)
     int pad[2];
 };
@@ -79,7 +65,7 @@ struct VerifyDev {
     int W;                    // penalty window
     float tau, thresh;
     int gate;
-    NoiseKey nk;              // seq filled per CTA
+    NoiseKey nk;              // seq filled per row
     int aligned;              // logits (and q) allow 16-byte vector loads
     int32_t* kv_len;
     float* ema;
@@ -89,7 +75,7 @@ struct VerifyDev {
     RowRes* rowres;
     SeqRes* seqres;
     unsigned* row_ticket;
-    unsigned* row_thr;        // best candidate score published per row (score_key)
+    unsigned* row_thr;        // best residual score published per row (score_key)
     unsigned* seq_ticket;
     Partial* part2;
     unsigned* seq_ticket2;
@@ -136,6 +122,15 @@ __device__ __forceinline__ double raw_logit_f64(const void* logits, size_t row, 
         return static_cast<double>(__uint_as_float(static_cast<uint32_t>(h) << 16));
     } else {
         return static_cast<double>(reinterpret_cast<const float*>(logits)[row * V + id]);
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ float elem_of_stage(const uint4* stage, int loc) {
+    if constexpr (BF16) {
+        return __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(stage)[loc]) << 16);
+    } else {
+        return reinterpret_cast<const float*>(stage)[loc];
     }
 }
 
@@ -200,11 +195,6 @@ __device__ __forceinline__ void st_zero(R* p) {
     for (int i = 0; i < static_cast<int>(sizeof(R) / 16); ++i) reinterpret_cast<uint4*>(p)[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
-__device__ __forceinline__ double warp_max_f64(double v) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v = fmax(v, __shfl_xor_sync(0xffffffffu, v, off));
-    return v;
-}
 __device__ __forceinline__ double warp_sum_f64(double v) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
@@ -225,22 +215,6 @@ __device__ __forceinline__ unsigned warp_best_key(float best) {
     return __reduce_max_sync(0xffffffffu, best > -INFINITY ? score_key(best) : 0u);
 }
 
-// Gumbel variate from a Philox word with hardware log2 (error ~1e-5): a
-// pre-filter only; candidates that pass it are re-scored with gumbel_f32.
-__device__ __forceinline__ float gumbel_fast(uint32_t w) {
-    const float u = static_cast<float>(uniform_numerator(w)) * 0x1p-24f;
-    const float y = 1.0f - u;  // exact
-    float e;
-    if (y < 0.0625f) {
-        e = y * fmaf(y, fmaf(y, fmaf(y, 0.25f, 0.33333334f), 0.5f), 1.0f);  // -log1p(-y) series
-    } else {
-        e = -0.6931472f * __log2f(u);
-    }
-    return -0.6931472f * __log2f(e);
-}
-
-constexpr int kQCap = 32 + 32 * 32;  // per-warp candidate queue (chunk offsets): a remainder + one stage
-
 // Largest bf16 value <= f, as a packed pair (both halves).  NaN maps to +inf.
 __device__ __forceinline__ uint32_t bf16x2_floor(float f) {
     uint32_t u = __float_as_uint(f);
@@ -251,27 +225,18 @@ __device__ __forceinline__ uint32_t bf16x2_floor(float f) {
 }
 
 __device__ __forceinline__ __nv_bfloat162 as_bf162(uint32_t w) { return *reinterpret_cast<__nv_bfloat162*>(&w); }
+__device__ __forceinline__ uint32_t as_u32(__nv_bfloat162 h) { return *reinterpret_cast<uint32_t*>(&h); }
 
-// Maximum of the 8 bf16 values of a 16-byte vector (packed compares).
-__device__ __forceinline__ float bf16x8_max(const uint4& r) {
-    const __nv_bfloat162 a = __hmax2(__hmax2(as_bf162(r.x), as_bf162(r.y)), __hmax2(as_bf162(r.z), as_bf162(r.w)));
-    const uint32_t w = *reinterpret_cast<const uint32_t*>(&a);
-    return fmaxf(bf16lo(w), bf16hi(w));
+// Packed maximum of the 8 bf16 values of a 16-byte vector (both halves hold a partial maximum).
+__device__ __forceinline__ __nv_bfloat162 bf16x8_max2(const uint4& r) {
+    return __hmax2(__hmax2(as_bf162(r.x), as_bf162(r.y)), __hmax2(as_bf162(r.z), as_bf162(r.w)));
 }
 
-// Bit e set when element e of the vector is >= the (packed) threshold t.
-__device__ __forceinline__ unsigned bf16x8_ge_mask(const uint4& r, uint32_t t) {
-    const __nv_bfloat162 th = as_bf162(t);
-    const unsigned m0 = __hge2_mask(as_bf162(r.x), th), m1 = __hge2_mask(as_bf162(r.y), th);
-    const unsigned m2 = __hge2_mask(as_bf162(r.z), th), m3 = __hge2_mask(as_bf162(r.w), th);
-    return (m0 & 1u) | ((m0 >> 15) & 2u) | ((m1 & 1u) << 2) | ((m1 >> 13) & 8u) | ((m2 & 1u) << 4) |
-           ((m2 >> 11) & 32u) | ((m3 & 1u) << 6) | ((m3 >> 9) & 128u);
-}
-
-// The same mask with fewer instructions: the high byte of each compared half
-// is gathered with byte permutes, and the four 0xFF / 0x00 bytes of a word are
-// turned into four bits by one multiply (the partial products of distinct
-// bytes land on distinct bit positions, so nothing carries into bits 24..27).
+// Bit e set when element e of the vector is >= the (packed) threshold t: the
+// high byte of each compared half is gathered with byte permutes, and the four
+// 0xFF / 0x00 bytes of a word become four bits by one multiply (the partial
+// products of distinct bytes land on distinct bit positions, so nothing
+// carries into bits 24..27).
 __device__ __forceinline__ unsigned bf16x8_ge_bits(const uint4& r, uint32_t t) {
     const __nv_bfloat162 th = as_bf162(t);
     const unsigned m0 = __hge2_mask(as_bf162(r.x), th), m1 = __hge2_mask(as_bf162(r.y), th);
@@ -289,67 +254,6 @@ __device__ __forceinline__ void ms_merge(float& m, float& s, float mo, float so,
     if (mo > -INFINITY) r += so * ex2_approx((mo - M) * sc);
     m = M;
     s = r;
-}
-
-// Penalty window of row j of sequence b: the last W tokens of
-// history[:lens] ++ d_1..d_j.  Fills s_win / s_nwin and, for the chunk
-// [v0, v1), the bitmap s_bm.  Whole CTA calls it.
-template <int CHUNK>
-__device__ __forceinline__ void build_window(const VerifyDev& P, int b, int j, int v0, int v1,
-                                             uint32_t* s_bm, int* s_win, int* s_nwin) {
-    const int tid = threadIdx.x;
-    int L = P.lens[b];
-    L = L < 0 ? 0 : (static_cast<int64_t>(L) > P.hist_stride ? static_cast<int>(P.hist_stride) : L);
-    const int total = L + j;
-    const int start = total - P.W > 0 ? total - P.W : 0;
-    const int nw = total - start;
-    for (int t = tid; t < CHUNK / 32; t += kThreads) s_bm[t] = 0u;
-    int tok = -1;
-    if (tid < nw) {
-        const int idx = start + tid;
-        tok = idx < L ? P.hist[static_cast<size_t>(b) * P.hist_stride + idx] : P.drafts[b * P.K + (idx - L)];
-        s_win[tid] = tok;
-    }
-    if (tid == 0) *s_nwin = nw;
-    __syncthreads();
-    if (tok >= v0 && tok < v1) atomicOr(&s_bm[(tok - v0) >> 5], 1u << ((tok - v0) & 31));
-    __syncthreads();
-}
-
-template <bool PENALTY, int EPV>
-__device__ __forceinline__ unsigned pen_bits(const uint32_t* s_bm, int off) {
-    if constexpr (!PENALTY) {
-        return 0u;
-    } else {
-        return (s_bm[off >> 5] >> (off & 31)) & ((1u << EPV) - 1u);
-    }
-}
-
-// ---------------------------------------------------------------- K1
-// Persistent, warp-specialised streaming kernel.  One CTA per SM; the active
-// row-chunks of the call (rows 0..k_eff of every sequence, V-chunks of
-// CHUNK elements) are laid out row-major and split into equal contiguous
-// ranges, one per CTA.  A producer warp walks its CTA's range and keeps up to
-// kStages chunks in flight with cp.async.bulk into a shared-memory ring
-// (full / empty mbarriers, bounded waits); sixteen consumer warps each take
-// a 2 KB slice of every chunk.  A consumer warp keeps its Gumbel threshold
-// across the consecutive chunks of one row, so only a row's first chunk
-// needs a seed.  Each chunk leaves one partial (max, sum of exponentials,
-// top-two candidates) in the workspace; the merge kernel combines them.
-
-constexpr int kCWarps = 16;                    // consumer warps
-constexpr int kPWarp = kCWarps;                // producer warp index
-constexpr int kPThreads = (kCWarps + 1) * 32;  // 544
-constexpr int kStages = 5;
-constexpr int kVL = 4;                         // 16-byte vectors per lane per chunk
-
-template <bool BF16>
-__host__ __device__ constexpr int stage_bytes() { return chunk_elems<BF16>() * ElemTraits<BF16>::SIZE; }
-
-template <bool PENALTY>
-__host__ __device__ constexpr size_t k1_dyn_smem() {
-    return static_cast<size_t>(kStages) * 32768 + static_cast<size_t>(kCWarps) * kQCap * sizeof(uint16_t) +
-           (PENALTY ? static_cast<size_t>(kStages) * 2048 : 0);
 }
 
 // Penalty window of row j: the last W tokens of history ++ d_1..d_j, read
@@ -377,20 +281,6 @@ struct WindowView {
     }
 };
 
-// Bitmap of the penalised ids of row j that fall in [v0, v1); one warp builds it.
-template <int CHUNK>
-__device__ __forceinline__ void warp_build_bitmap(uint32_t* bm, const WindowView& wv, int j, int v0, int v1) {
-    const int lane = threadIdx.x & 31;
-    for (int t = lane; t < CHUNK / 32; t += 32) bm[t] = 0u;
-    __syncwarp();
-    const int n = wv.count(j);
-    for (int t = lane; t < n; t += 32) {
-        const int tok = wv.token(j, t);
-        if (tok >= v0 && tok < v1) atomicOr(&bm[(tok - v0) >> 5], 1u << ((tok - v0) & 31));
-    }
-    __syncwarp();
-}
-
 __device__ __forceinline__ int gate_keff(const VerifyDev& P, int b, int* kb_out, bool flag) {
     int kb = P.k[b];
     if (kb < 0 || kb > P.K) {
@@ -402,647 +292,21 @@ __device__ __forceinline__ int gate_keff(const VerifyDev& P, int b, int* kb_out,
     return kb;
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
+// Slack of the block bound: covers the fp32 rounding of z / T and ln M.
+__device__ __forceinline__ float bound_slack(float z) { return 1e-5f * (1.0f + fabsf(z)); }
 
-struct StageMeta {
-    int b, j, c, excl, seg_end;  // seg_end: the last chunk of this row in the CTA's range
-    int cand;                    // the row's Gumbel candidates can be the emitted token
-};
-
-struct WarpPart {
-    float m, s;
-    Top2 t;
-};
+// ---------------------------------------------------------------- row merge
+// One warp: combine the row's segment partials (log-sum-exp, sampled
+// candidate), run the accept test of the draft the row verifies; the last
+// row of a sequence to finish runs the epilogue (tokens, kv_len, EMA).
 
 template <bool BF16, bool GREEDY, bool SOFTCAP, bool PENALTY>
-__global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const VerifyDev P) {
-    constexpr int EPV = ElemTraits<BF16>::EPV;
-    constexpr int CHUNK = chunk_elems<BF16>();
-    constexpr int SB = stage_bytes<BF16>();
-    static_assert(SB == 32768 && SB == kCWarps * 32 * kVL * 16, "stage layout");
-    extern __shared__ __align__(128) uint8_t s_dyn[];
-    uint8_t* s_stage = s_dyn;
-    uint16_t* s_q = reinterpret_cast<uint16_t*>(s_dyn + kStages * SB);
-    uint32_t* s_bm = reinterpret_cast<uint32_t*>(s_dyn + kStages * SB + kCWarps * kQCap * sizeof(uint16_t));
-    __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages];
-    __shared__ StageMeta s_meta[kStages];
-    __shared__ WarpPart s_slot[kStages][kCWarps];
-    __shared__ int s_cnt[kStages];
-    __shared__ unsigned s_rthr[kStages + 1];  // per-segment shared threshold (score_key; 0 = none)
-    __shared__ int s_qn[kCWarps];
-    __shared__ float s_cz[GREEDY ? 1 : kCWarps * 32];  // carried candidates: z / T
-    __shared__ int s_cv[GREEDY ? 1 : kCWarps * 32];    // carried candidates: vocab id
-    __shared__ long long s_wsum[kPThreads / 32];
-    __shared__ int s_start[3];
-    __shared__ int s_hwin[PENALTY ? SPECNG_MAX_REP_WINDOW : 1];
-    __shared__ int s_pdrafts[SPECNG_MAX_K + 1];
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int K1 = P.K + 1;
-    const bool dense = P.q != nullptr;
-
-    // ---- prologue: count the active row-chunks and find this CTA's range
-    const int per = (P.B + kPThreads - 1) / kPThreads;
-    const int bb0 = tid * per;
-    long long mine = 0;
-    for (int b = bb0; b < bb0 + per && b < P.B; ++b) mine += static_cast<long long>(gate_keff(P, b, nullptr, false) + 1) * P.nchunk;
-    long long incl = mine;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const long long o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
-    }
-    if (lane == 31) s_wsum[warp] = incl;
-    if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init(&s_full[i], 1);
-            mbar_init(&s_empty[i], kCWarps);
-            s_cnt[i] = 0;
-        }
-        for (int i = 0; i <= kStages; ++i) s_rthr[i] = 0u;
-        mbar_init_fence();
-    }
-    __syncthreads();
-    long long base = 0, total = 0;
-    for (int w = 0; w < kPThreads / 32; ++w) {
-        if (w < warp) base += s_wsum[w];
-        total += s_wsum[w];
-    }
-    const long long G = gridDim.x;
-    const long long w0 = total * blockIdx.x / G, w1 = total * (blockIdx.x + 1) / G;
-    const long long ex = base + incl - mine;  // first row-chunk index of my sequences
-    if (w0 < w1 && w0 >= ex && w0 < ex + mine) {
-        long long acc = ex;
-        for (int b = bb0; b < bb0 + per && b < P.B; ++b) {
-            const long long nb = static_cast<long long>(gate_keff(P, b, nullptr, false) + 1) * P.nchunk;
-            if (w0 < acc + nb) {
-                const long long r = w0 - acc;
-                s_start[0] = b;
-                s_start[1] = static_cast<int>(r / P.nchunk);
-                s_start[2] = static_cast<int>(r % P.nchunk);
-                break;
-            }
-            acc += nb;
-        }
-    }
-    __syncthreads();
-    const int nwork = static_cast<int>(w1 - w0);
-    if (nwork <= 0) return;
-
-    if (warp == kPWarp) {
-        // ================= producer =================
-        int b = s_start[0], j = s_start[1], c = s_start[2];
-        int kb = 0;
-        int keff = 0;
-        int nh = 0;
-        auto load_seq = [&](int bq) {
-            keff = gate_keff(P, bq, &kb, true);
-            if (lane < keff) {
-                const int d = P.drafts[bq * P.K + lane];
-                s_pdrafts[lane] = d;
-                if (!(d >= 0 && d < P.V)) raise_status(P.status, SPECNG_DEV_TOKEN_OOR);
-            }
-            if constexpr (PENALTY) {
-                int L = P.lens[bq];
-                L = L < 0 ? 0 : (static_cast<int64_t>(L) > P.hist_stride ? static_cast<int>(P.hist_stride) : L);
-                nh = L < P.W ? L : P.W;
-                for (int t = lane; t < nh; t += 32) s_hwin[t] = P.hist[static_cast<size_t>(bq) * P.hist_stride + (L - nh) + t];
-            }
-            __syncwarp();
-        };
-        load_seq(b);
-        bool ok = true;
-        for (int n = 0; n < nwork && ok; ++n) {
-            const int st = n % kStages;
-            const int use = n / kStages;
-            if (use >= 1) ok = mbar_wait_bounded(&s_empty[st], static_cast<unsigned>((use - 1) & 1));
-            if (!ok) { if (lane == 0) raise_status(P.status, SPECNG_DEV_TIMEOUT); break; }
-            const int v0 = c * CHUNK;
-            const int v1 = min(P.V, v0 + CHUNK);
-            if (lane == 0) {
-                int excl = -1;
-                // with dense q, row j < k_eff is sampled by the residual pass unless
-                // its draft is invalid (the residual is then p itself)
-                int cand = 1;
-                if (!GREEDY && j < keff) {
-                    const int d = s_pdrafts[j];
-                    const bool valid = d >= 0 && d < P.V;
-                    if (!dense && valid) excl = d;
-                    if (dense && valid) cand = 0;
-                }
-                s_meta[st] = StageMeta{b, j, c, excl, (c == P.nchunk - 1 || n == nwork - 1) ? 1 : 0, cand};
-            }
-            if constexpr (PENALTY) {
-                const WindowView wv{s_hwin, s_pdrafts, nh, P.W};
-                warp_build_bitmap<CHUNK>(s_bm + st * (CHUNK / 32), wv, j, v0, v1);
-            }
-            __syncwarp();
-            const char* src = static_cast<const char*>(P.logits) +
-                              ((static_cast<size_t>(b) * K1 + j) * P.V + v0) * ElemTraits<BF16>::SIZE;
-            if (P.aligned) {
-                if (lane == 0) {
-                    // the empty barrier already orders the consumers' reads of this stage
-                    // before the copy that overwrites it
-                    mbar_expect_tx(&s_full[st], static_cast<unsigned>(v1 - v0) * ElemTraits<BF16>::SIZE);
-                    bulk_g2s(s_stage + st * SB, src, static_cast<unsigned>(v1 - v0) * ElemTraits<BF16>::SIZE, &s_full[st]);
-                }
-            } else {
-                uint8_t* dst = s_stage + st * SB;
-                for (int e = lane; e < v1 - v0; e += 32) {
-                    if constexpr (BF16) reinterpret_cast<uint16_t*>(dst)[e] = reinterpret_cast<const uint16_t*>(src)[e];
-                    else reinterpret_cast<uint32_t*>(dst)[e] = reinterpret_cast<const uint32_t*>(src)[e];
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s_full[st]);
-            }
-            // advance to the next row-chunk
-            if (++c == P.nchunk) {
-                c = 0;
-                if (++j > keff) {
-                    j = 0;
-                    ++b;
-                    if (n + 1 < nwork) load_seq(b);
-                }
-            }
-        }
-        // the CTA stays resident until every issued copy has landed
-        if (P.aligned && lane == 0) {
-            const int lo = nwork > kStages ? nwork - kStages : 0;
-            for (int n = lo; n < nwork; ++n) mbar_wait_bounded(&s_full[n % kStages], static_cast<unsigned>((n / kStages) & 1));
-        }
-        return;
-    }
-
-    // ================= consumers =================
-    // Per-lane accumulators live across the chunks of one row (a segment of
-    // the CTA's range); warps combine them once, at the segment's last chunk.
-    // The candidate threshold of a segment is shared by the CTA's consumer
-    // warps through a small ring of shared-memory slots (order-preserving
-    // keys, atomicMax): every warp prunes with the best score any warp found.
-    float thr = -INFINITY;
-    float m = -INFINITY, s = 0.0f, msc = 0.0f;
-    Top2 tt = top2_empty();
-    bool fresh = true;
-    int seg = 0;
-    uint16_t* q = s_q + warp * kQCap;
-    int cn = 0;  // candidates carried from the segment's previous stage (s_cz / s_cv)
-    if (lane == 0) s_qn[warp] = 0;
-    __syncwarp();
-    for (int n = 0; n < nwork; ++n) {
-        const int st = n % kStages;
-        if (!mbar_wait_bounded(&s_full[st], static_cast<unsigned>((n / kStages) & 1))) {
-            if (lane == 0) raise_status(P.status, SPECNG_DEV_TIMEOUT);
-            break;
-        }
-        const StageMeta mt = s_meta[st];
-        const int row = mt.b * K1 + mt.j;
-        const int j = mt.j;
-        const int excl = mt.excl;
-        const int v0 = mt.c * CHUNK;
-        const int v1 = min(P.V, v0 + CHUNK);
-        const uint4* stage = reinterpret_cast<const uint4*>(s_stage + st * SB);
-        const uint32_t* bm = s_bm + (PENALTY ? st * (CHUNK / 32) : 0);
-        NoiseKey nk = P.nk;
-        nk.seq = static_cast<uint32_t>(mt.b);
-        const int ubase = warp * (32 * kVL);  // first 16-byte vector of my slice
-        unsigned* rth = &s_rthr[seg % (kStages + 1)];
-        const RowPhilox rp = row_philox(nk, static_cast<uint32_t>(j));
-
-        if constexpr (GREEDY) {
-            // top two transformed values (lower id on ties) within cand_delta of
-            // the best value any warp of the CTA has seen in this segment.  The
-            // slice's maxima come first (packed compares), so the threshold is
-            // already the warp's best before any element is pushed.
-            uint4 rv[kVL];
-            float vmx[kVL];
-            float lmax = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < kVL; ++i) {
-                const int u = ubase + i * 32 + lane;
-                const int off = u * EPV;
-                const int nv = min(EPV, v1 - (v0 + off));
-                rv[i] = stage[u];
-                const unsigned pb = pen_bits<PENALTY, EPV>(bm, off);
-                float vm = -INFINITY;
-                if (BF16 && nv == EPV && pb == 0u) {
-                    vm = bf16x8_max(rv[i]);
-                    if constexpr (SOFTCAP) vm = transform_f32<true, false>(vm, false, P);
-                } else if (nv > 0) {
-                    float x[EPV];
-                    unpack<BF16>(rv[i], x);
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e)
-                        if (e < nv) vm = fmaxf(vm, transform_f32<SOFTCAP, PENALTY>(x[e], (pb >> e) & 1u, P));
-                }
-                vmx[i] = vm;
-                lmax = fmaxf(lmax, vm);
-            }
-            const unsigned wk = warp_best_key(lmax);
-            float gth = fmaxf(fmaxf(tt.s1, key_score(wk)), key_score(*reinterpret_cast<volatile unsigned*>(rth)));
-            gth = gth > -INFINITY ? gth - cand_delta(gth) : -INFINITY;
-#pragma unroll
-            for (int i = 0; i < kVL; ++i) {
-                const int u = ubase + i * 32 + lane;
-                const int off = u * EPV;
-                const int e0 = v0 + off;
-                const int nv = min(EPV, v1 - e0);
-                if (nv <= 0 || !(vmx[i] >= gth)) continue;
-                const unsigned pb = pen_bits<PENALTY, EPV>(bm, off);
-                float x[EPV];
-                unpack<BF16>(rv[i], x);
-#pragma unroll
-                for (int e = 0; e < EPV; ++e) {
-                    if (e >= nv) break;
-                    const float z = transform_f32<SOFTCAP, PENALTY>(x[e], (pb >> e) & 1u, P);
-                    if (z >= gth) top2_push(tt, z, e0 + e);
-                }
-                gth = fmaxf(gth, tt.s1 - cand_delta(tt.s1));
-            }
-            const unsigned kw = warp_best_key(tt.s1);
-            if (lane == 0 && kw != 0u) atomicMax(rth, kw);
-        } else {
-            const bool cand = mt.cand != 0;
-            int seeded = -1;  // element already scored as this lane's seed
-            if (fresh && cand && !(BF16 && !PENALTY && v0 + (ubase + (kVL - 1) * 32 + lane) * EPV + EPV <= v1)) {
-                // ---- seed: every lane scores the largest element of its slice
-                float zm = -INFINITY;
-                int am = -1;
-#pragma unroll
-                for (int i = 0; i < kVL; ++i) {
-                    const int u = ubase + i * 32 + lane;
-                    const int off = u * EPV;
-                    const int e0 = v0 + off;
-                    const int nv = min(EPV, v1 - e0);
-                    if (nv <= 0) continue;
-                    float x[EPV];
-                    unpack<BF16>(stage[u], x);
-                    const unsigned pb = pen_bits<PENALTY, EPV>(bm, off);
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e) {
-                        if (e >= nv) break;
-                        const float z = transform_f32<SOFTCAP, PENALTY>(x[e], (pb >> e) & 1u, P);
-                        if (z > zm && e0 + e != excl) { zm = z; am = e0 + e; }
-                    }
-                }
-                float t0 = -INFINITY;
-                if (am >= 0) {
-                    const uint4 w = gumbel_block_row(rp, static_cast<uint32_t>(am) >> 2);
-                    t0 = zm * P.invT + gumbel_f32(pick_word(w, static_cast<uint32_t>(am) & 3u));
-                    top2_push(tt, t0, am);
-                    seeded = am;
-                }
-                const unsigned k0 = warp_best_key(t0);
-                if (k0 != 0u) {
-                    t0 = key_score(k0);
-                    thr = t0 - cand_delta(t0);
-                    if (lane == 0) atomicMax(rth, k0);
-                }
-            }
-            // candidate threshold in raw-logit units: z / T >= thr - g_max  <=>  x >= xt
-            float xt;
-            uint32_t xt2;
-            auto set_xt = [&]() {
-                const float zt = (thr - kGumbelMax) * P.T;
-                if constexpr (SOFTCAP) {
-                    // shrink u by more than the fp32 error of c * tanh(x / c) before inverting:
-                    // atanh is steep near |u| = 1
-                    float u = zt * P.invcap;
-                    u -= 1e-6f * fabsf(u) + 1e-7f;
-                    xt = u > 1.0f ? INFINITY : (u <= -1.0f ? -INFINITY : P.cap * atanhf(fminf(u, 1.0f - 1e-7f)));
-                } else {
-                    xt = zt;
-                }
-                xt -= 1e-5f * (1.0f + fabsf(xt));  // slack for the rounding of the transform
-                xt2 = bf16x2_floor(xt);
-            };
-            // adopt the best score another warp published for this segment
-            auto sync_thr = [&]() {
-                const float best = key_score(*reinterpret_cast<volatile unsigned*>(rth));
-                if (best > -INFINITY) {
-                    const float t1 = best - cand_delta(best);
-                    if (t1 > thr) { thr = t1; set_xt(); }
-                }
-            };
-            if (cand) {
-                set_xt();
-                sync_thr();
-            } else {
-                xt = INFINITY;
-                xt2 = 0x7F807F80u;
-            }
-            // ---- one pass over the slice: all four 16-byte vectors are loaded first; the
-            //      online maximum and the 32 exponentials (packed fp32x2 arithmetic) form one
-            //      independent block; candidate masks are formed only for the vectors whose
-            //      maximum reaches the threshold
-            uint4 rv[kVL];
-#pragma unroll
-            for (int i = 0; i < kVL; ++i) rv[i] = stage[ubase + i * 32 + lane];
-            const int off0 = ubase * EPV + lane * EPV;  // chunk offset of vector 0's element 0
-            const bool fast = v0 + (ubase + (kVL - 1) * 32 + lane) * EPV + EPV <= v1;  // four full vectors
-            unsigned pmk = 0u;  // penalised elements of the slice (bit 8 i + e)
-            if constexpr (PENALTY) {
-#pragma unroll
-                for (int i = 0; i < kVL; ++i) pmk |= pen_bits<PENALTY, EPV>(bm, off0 + i * 32 * EPV) << (8 * i);
-            }
-            unsigned msk = 0u;  // bit 8 i + e: element e of vector i
-            if (fast) {
-                float rmx[kVL];  // raw maxima
-#pragma unroll
-                for (int i = 0; i < kVL; ++i) {
-                    if constexpr (BF16) {
-                        rmx[i] = bf16x8_max(rv[i]);
-                    } else {
-                        rmx[i] = fmaxf(fmaxf(__uint_as_float(rv[i].x), __uint_as_float(rv[i].y)),
-                                       fmaxf(__uint_as_float(rv[i].z), __uint_as_float(rv[i].w)));
-                    }
-                }
-                float vm = fmaxf(fmaxf(rmx[0], rmx[1]), fmaxf(rmx[2], rmx[3]));
-                if constexpr (BF16 && !PENALTY) {
-                    if (fresh && cand) {
-                        // seed: score the slice's largest element (lowest id among equals); the
-                        // transform is monotone, so it is also the largest transformed value
-                        int am = -1;
-#pragma unroll
-                        for (int i = kVL - 1; i >= 0; --i) {
-                            if (rmx[i] == vm) {
-                                float x[EPV];
-                                unpack<BF16>(rv[i], x);
-                                int e = EPV - 1;
-#pragma unroll
-                                for (int k = EPV - 2; k >= 0; --k) e = x[k] == vm ? k : e;
-                                am = v0 + off0 + i * 32 * EPV + e;
-                            }
-                        }
-                        float t0 = -INFINITY;
-                        if (am >= 0 && am != excl) {
-                            const uint4 w = gumbel_block_row(rp, static_cast<uint32_t>(am) >> 2);
-                            t0 = transform_f32<SOFTCAP, false>(vm, false, P) * P.invT +
-                                 gumbel_f32(pick_word(w, static_cast<uint32_t>(am) & 3u));
-                            top2_push(tt, t0, am);
-                            seeded = am;
-                        }
-                        const unsigned k0 = warp_best_key(t0);
-                        if (k0 != 0u) {
-                            t0 = key_score(k0);
-                            thr = t0 - cand_delta(t0);
-                            if (lane == 0) atomicMax(rth, k0);
-                            set_xt();
-                        }
-                        sync_thr();  // and adopt the best seed any warp has published
-                    }
-                }
-                if constexpr (SOFTCAP) vm = transform_f32<true, false>(vm, false, P);
-                if (vm > m) {
-                    s = m > -INFINITY ? s * ex2_approx((m - vm) * P.sc) : 0.0f;
-                    m = vm;
-                    msc = m * P.sc;
-                }
-                float2 acc2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
-                const float2 sc2 = make_float2(P.sc, P.sc), nm2 = make_float2(-msc, -msc);
-#pragma unroll
-                for (int i = 0; i < kVL; ++i) {
-                    float x[EPV];
-                    unpack<BF16>(rv[i], x);
-#pragma unroll
-                    for (int e = 0; e < EPV; e += 2) {
-                        const float2 t = __ffma2_rn(make_float2(transform_f32<SOFTCAP, false>(x[e], false, P),
-                                                                transform_f32<SOFTCAP, false>(x[e + 1], false, P)),
-                                                    sc2, nm2);
-                        acc2[i & 1] = __fadd2_rn(acc2[i & 1], make_float2(ex2_approx(t.x), ex2_approx(t.y)));
-                    }
-                }
-                s += (acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y);
-                if (cand) {
-#pragma unroll
-                    for (int i = 0; i < kVL; ++i) {
-                        if (!(rmx[i] >= xt)) continue;
-                        unsigned mi;
-                        if constexpr (BF16) {
-                            mi = bf16x8_ge_bits(rv[i], xt2);
-                        } else {
-                            mi = 0u;
-                            mi |= static_cast<unsigned>(__uint_as_float(rv[i].x) >= xt);
-                            mi |= static_cast<unsigned>(__uint_as_float(rv[i].y) >= xt) << 1;
-                            mi |= static_cast<unsigned>(__uint_as_float(rv[i].z) >= xt) << 2;
-                            mi |= static_cast<unsigned>(__uint_as_float(rv[i].w) >= xt) << 3;
-                        }
-                        msk |= mi << (8 * i);
-                    }
-                }
-                if constexpr (PENALTY) {
-                    // the few penalised elements: replace their terms by the penalised ones
-                    // (and raise the maximum if a penalty below 1 lifted one above it); they
-                    // are always queued, so scoring sees their exact values
-                    unsigned pw = pmk;
-                    while (pw != 0u) {
-                        const int bit = __ffs(pw) - 1;
-                        pw &= pw - 1u;
-                        const int loc = off0 + (bit >> 3) * 32 * EPV + (bit & 7);
-                        float xe;
-                        if constexpr (BF16) {
-                            xe = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(stage)[loc]) << 16);
-                        } else {
-                            xe = reinterpret_cast<const float*>(stage)[loc];
-                        }
-                        const float zu = transform_f32<SOFTCAP, false>(xe, false, P);
-                        const float zp = transform_f32<SOFTCAP, true>(xe, true, P);
-                        if (zp > m) {
-                            s *= ex2_approx((m - zp) * P.sc);
-                            m = zp;
-                            msc = m * P.sc;
-                        }
-                        s += ex2_approx(fmaf(zp, P.sc, -msc)) - ex2_approx(fmaf(zu, P.sc, -msc));
-                    }
-                    if (cand) msk |= pmk;
-                }
-            } else {
-                // partial vectors (a row's last chunk): exact transform element by element
-#pragma unroll
-                for (int i = 0; i < kVL; ++i) {
-                    const int off = off0 + i * 32 * EPV;
-                    const int e0 = v0 + off;
-                    const int nv = min(EPV, v1 - e0);
-                    if (nv <= 0) continue;
-                    float x[EPV], z[EPV];
-                    unpack<BF16>(rv[i], x);
-                    const unsigned pb = pen_bits<PENALTY, EPV>(bm, off);
-                    float vmx = -INFINITY;
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e) {
-                        z[e] = transform_f32<SOFTCAP, PENALTY>(x[e], (pb >> e) & 1u, P);
-                        if (e < nv) vmx = fmaxf(vmx, z[e]);
-                    }
-                    if (vmx > m) {
-                        s = m > -INFINITY ? s * ex2_approx((m - vmx) * P.sc) : 0.0f;
-                        m = vmx;
-                        msc = m * P.sc;
-                    }
-                    const float zthr = thr - kGumbelMax;
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e) {
-                        if (e < nv) {
-                            if (m > -INFINITY) s += ex2_approx(fmaf(z[e], P.sc, -msc));
-                            if (cand) msk |= static_cast<unsigned>(z[e] * P.invT >= zthr) << (8 * i + e);
-                        }
-                    }
-                }
-            }
-            if (seeded >= 0) {
-                const int so = seeded - v0 - off0;  // position of the seed in the slice
-                const int si = so / (32 * EPV), se = so - si * 32 * EPV;
-                if (se >= 0 && se < EPV) msk &= ~(1u << (8 * si + se));
-            }
-            if (cand) {
-            // ---- queue the slice's candidates (chunk offsets of this stage)
-            const unsigned cnt = __popc(msk);
-            const int nq = static_cast<int>(__reduce_add_sync(0xffffffffu, cnt));
-            if (msk != 0u) {
-                int slot = atomicAdd(&s_qn[warp], static_cast<int>(cnt));
-                while (msk != 0u) {
-                    const int bit = __ffs(msk) - 1;
-                    msk &= msk - 1u;
-                    q[slot++] = static_cast<uint16_t>(off0 + (bit >> 3) * 32 * EPV + (bit & 7));
-                }
-            }
-            __syncwarp();
-            // ---- score full batches of 32 from [carried ++ queued]; the remainder is carried to
-            //      the segment's next stage (as transformed value and id), and scored at its end
-            const bool flush = mt.seg_end != 0;
-            const int total = cn + nq;
-            float* cz = s_cz + warp * 32;
-            int* cv = s_cv + warp * 32;
-            auto fetch = [&](int idx, float& zb, int& v) {
-                if (idx < cn) {
-                    zb = cz[idx];
-                    v = cv[idx];
-                } else {
-                    const int loc = static_cast<int>(q[idx - cn]);
-                    float x;
-                    if constexpr (BF16) {
-                        x = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(stage)[loc]) << 16);
-                    } else {
-                        x = reinterpret_cast<const float*>(stage)[loc];
-                    }
-                    const bool pen = PENALTY && ((bm[loc >> 5] >> (loc & 31)) & 1u);
-                    zb = transform_f32<SOFTCAP, PENALTY>(x, pen, P) * P.invT;
-                    v = v0 + loc;
-                }
-            };
-            int base = 0;
-            while (total - base >= 32 || (flush && base < total)) {
-                const int idx = base + lane;
-                float zb = -INFINITY;
-                int v = 0;
-                if (idx < total) fetch(idx, zb, v);
-                const bool live = idx < total && v != excl && zb + kGumbelMax >= thr;
-                if (__any_sync(0xffffffffu, live)) {
-                    const uint32_t word = pick_word(gumbel_block_row(rp, static_cast<uint32_t>(v) >> 2),
-                                                    static_cast<uint32_t>(v) & 3u);
-                    if (live && gumbel_may_reach(word, thr - zb)) {
-                        const float score = zb + gumbel_f32(word);
-                        if (score >= thr) {
-                            top2_push(tt, score, v);
-                            thr = fmaxf(thr, tt.s1 - cand_delta(tt.s1));
-                        }
-                    }
-                }
-                base += 32;
-            }
-            const int rem = total - base;  // < 32; 0 after a flush
-            if (rem > 0) {
-                float zc = 0.0f;
-                int vc = 0;
-                if (lane < rem) fetch(base + lane, zc, vc);
-                __syncwarp();
-                if (lane < rem) {
-                    cz[lane] = zc;
-                    cv[lane] = vc;
-                }
-            }
-            cn = rem > 0 ? rem : 0;
-            __syncwarp();
-            if (lane == 0) s_qn[warp] = 0;
-            __syncwarp();
-            // share the warp's best score with the CTA, adopt the CTA's best
-            const unsigned kw = warp_best_key(tt.s1);
-            if (kw != 0u) {
-                const float bw = key_score(kw);
-                thr = fmaxf(thr, bw - cand_delta(bw));
-                if (lane == 0) atomicMax(rth, kw);
-            }
-            }  // cand
-        }
-        fresh = mt.seg_end != 0;
-        if (fresh) {
-            // ---- end of this row's segment: one partial for the segment
-            float pm = m, ps = s;
-            Top2 pt = tt;
-            if constexpr (!GREEDY) {
-                if (!(pm > -INFINITY)) ps = 0.0f;
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    const float mo = __shfl_xor_sync(0xffffffffu, pm, off);
-                    const float so = __shfl_xor_sync(0xffffffffu, ps, off);
-                    ms_merge(pm, ps, mo, so, P.sc);
-                }
-            }
-            pt = top2_warp_reduce(pt);
-            int last = 0;
-            if (lane == 0) {
-                s_slot[st][warp] = WarpPart{pm, ps, pt};
-                __threadfence_block();
-                last = atomicAdd(&s_cnt[st], 1) == kCWarps - 1;
-            }
-            last = __shfl_sync(0xffffffffu, last, 0);
-            if (last) {
-                __threadfence_block();
-                WarpPart wp = lane < kCWarps ? s_slot[st][lane] : WarpPart{-INFINITY, 0.0f, top2_empty()};
-                float cm = wp.m, cs = wp.s;
-                Top2 ct = wp.t;
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    const float mo = __shfl_xor_sync(0xffffffffu, cm, off);
-                    const float so = __shfl_xor_sync(0xffffffffu, cs, off);
-                    ms_merge(cm, cs, mo, so, P.sc);
-                    ct = top2_merge(ct, top2_shfl_xor(ct, off));
-                }
-                if (lane == 0) {
-                    // keyed by the segment's last chunk; a written partial is never all-zero
-                    st_partial(P.part + static_cast<size_t>(row) * P.nchunk + mt.c, GREEDY ? 0.0f : cm,
-                               GREEDY ? 1.0f : cs, ct);
-                    s_cnt[st] = 0;
-                    *rth = 0u;  // every warp is past this segment: the slot is free
-                }
-            }
-            m = -INFINITY;
-            s = 0.0f;
-            msc = 0.0f;
-            tt = top2_empty();
-            thr = -INFINITY;
-            ++seg;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_empty[st]);
-    }
-}
-
-// ---------------------------------------------------------------- K3
-// One warp per row: combine the row's chunk partials (log-sum-exp, sampled
-// candidate), run the accept test of the draft it verifies; the last row of
-// a sequence to finish runs the epilogue (tokens, kv_len, EMA).
-
-template <bool BF16, bool GREEDY, bool SOFTCAP, bool PENALTY>
-__global__ void __launch_bounds__(256) verify_merge_kernel(const VerifyDev P) {
+__device__ __noinline__ void merge_row(const VerifyDev& P, int row) {
     const int lane = threadIdx.x & 31;
     const int K1 = P.K + 1;
-    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (row >= P.B * K1) return;
     const int b = row / K1, j = row - b * K1;
     int kb;
     const int keff = gate_keff(P, b, &kb, false);
-    if (j > keff) return;
     const bool dense = P.q != nullptr;
     NoiseKey nk = P.nk;
     nk.seq = static_cast<uint32_t>(b);
@@ -1065,8 +329,7 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const VerifyDev P) {
     }
 
     // one partial per row segment, stored at the segment's last chunk; the
-    // other slots are all-zero (a written partial never is).  A lane holds at
-    // most a few of them (chunks <= 32 for V <= 2^18 bf16 / 2^17 fp32).
+    // other slots are all-zero (a written partial never is)
     Partial* pr = P.part + static_cast<size_t>(row) * P.nchunk;
     constexpr int kHeld = 2;
     Partial held[kHeld];
@@ -1102,6 +365,7 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const VerifyDev P) {
     t = top2_warp_reduce(t);
     __syncwarp();
     for (int cc = lane; cc < P.nchunk; cc += 32) st_zero(pr + cc);  // leave the workspace zeroed
+    if (lane == 0) P.row_ticket[row] = 0u;
     const double lse = GREEDY ? 0.0 : static_cast<double>(mf) / P.Td + log(S);
     if (!GREEDY && !(S > 0.0 && S < INFINITY && mf < INFINITY) && lane == 0)
         raise_status(P.status, SPECNG_DEV_NONFINITE);
@@ -1121,8 +385,7 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const VerifyDev P) {
                 if constexpr (GREEDY) {
                     sc[h] = z;
                 } else {
-                    const uint4 w = gumbel_block(nk, static_cast<uint32_t>(id) >> 2, static_cast<uint32_t>(j));
-                    sc[h] = z / P.Td + gumbel_f64(pick_word(w, static_cast<uint32_t>(id) & 3u));
+                    sc[h] = z / P.Td - log(noise_exp_f64(nk, static_cast<uint32_t>(id), static_cast<uint32_t>(j)));
                 }
             }
             if (better64(sc[1], t.i2, sc[0], t.i1)) winner = t.i2;
@@ -1206,15 +469,696 @@ __global__ void __launch_bounds__(256) verify_merge_kernel(const VerifyDev P) {
     }
 }
 
+// ---------------------------------------------------------------- K1
+// Persistent, warp-specialised streaming kernel.  One CTA per SM; the active
+// row-chunks of the call (rows 0..k_eff of every sequence, chunks of 32 KB)
+// are laid out row-major and split into equal contiguous ranges, one per CTA.
+//   * A producer warp walks the CTA's range and keeps up to kStages chunks in
+//     flight with cp.async.bulk into a shared-memory ring (full / empty
+//     mbarriers, bounded waits).  While a copy is in flight it publishes the
+//     row's metadata, the penalty bitmap of the chunk and the noise of the
+//     chunk's 256-id blocks (one Philox draw per two blocks, by its lanes).
+//   * Sixteen streaming warps each own a 2 KB slice of every chunk.  A lane's
+//     16-byte vector i of a bf16 chunk covers 8 ids of noise block 4 w + i, so
+//     its packed maximum gives the block test z / T - ln M >= best for its
+//     eight ids at once.  Per slice: packed maxima, the exponentials of the
+//     sum, the block tests; only the vectors that pass compare their elements,
+//     and each lane scores its few survivors (per-id Philox draw, E_v, score)
+//     in step with the warp.  At the first chunk of a row segment each lane
+//     scores its largest element, which starts the segment's best; the warps
+//     of the CTA share the best through shared memory.
+//   * A merge warp runs the row merges: the CTA that completes a row (atomic
+//     ticket over the row's chunks) queues it, and the merge warp combines the
+//     row's partials, takes the accept test and, for the last row of a
+//     sequence (second ticket), runs the epilogue.  Nothing waits on another
+//     CTA.
+
+constexpr int kCWarps = 16;                    // streaming warps
+constexpr int kPWarp = kCWarps;                // producer warp index
+constexpr int kMWarp = kCWarps + 1;            // merge warp index
+constexpr int kPThreads = (kCWarps + 2) * 32;  // 576
+constexpr int kStages = 5;
+constexpr int kVL = 4;                         // 16-byte vectors per lane per chunk
+constexpr int kMaxBlk = kChunkBytes / 2 >> kNoiseBlockShift;  // noise blocks per chunk (bf16: 64)
+constexpr int kMQ = 16;                        // merge-queue entries per streaming warp
+static_assert(kChunkBytes == kCWarps * 32 * kVL * 16, "stage layout");
+static_assert((32 * 8) == (1 << kNoiseBlockShift), "a bf16 vector row of a warp is one noise block");
+
+template <bool PENALTY>
+__host__ __device__ constexpr size_t k1_dyn_smem() {
+    return static_cast<size_t>(kStages) * kChunkBytes + (PENALTY ? static_cast<size_t>(kStages) * 2048 : 0);
+}
+
+struct StageMeta {
+    int b, j, c, excl, seg_end;  // seg_end: the last chunk of this row in the CTA's range
+    int cand;                    // the row's Gumbel candidates can be the emitted token
+    unsigned penw;               // bit w: warp w's slice holds a penalised id
+    int pad;
+    BlockNoise bn[kMaxBlk];      // noise of the chunk's 256-id blocks
+};
+
+struct WarpPart {
+    float m, s;
+    Top2 t;
+};
+
+template <bool BF16, bool GREEDY, bool SOFTCAP, bool PENALTY>
+__global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const VerifyDev P) {
+    constexpr int EPV = ElemTraits<BF16>::EPV;
+    constexpr int CHUNK = chunk_elems<BF16>();
+    constexpr int SB = kChunkBytes;
+    constexpr int SL = 32 * kVL * EPV;  // ids per streaming slice
+    constexpr int NB = CHUNK >> kNoiseBlockShift;
+    extern __shared__ __align__(128) uint8_t s_dyn[];
+    uint8_t* s_stage = s_dyn;
+    uint32_t* s_bm = reinterpret_cast<uint32_t*>(s_dyn + kStages * SB);
+    __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages];
+    __shared__ StageMeta s_meta[kStages];
+    __shared__ WarpPart s_slot[kStages][kCWarps];
+    __shared__ int s_cnt[kStages];
+    __shared__ unsigned s_rthr[kStages + 1];  // per-segment best score (score_key; 0 = none)
+    __shared__ long long s_wsum[kPThreads / 32];
+    __shared__ int s_start[3];
+    __shared__ int s_hwin[PENALTY ? SPECNG_MAX_REP_WINDOW : 1];
+    __shared__ int s_pdrafts[SPECNG_MAX_K + 1];
+    __shared__ volatile int s_mq[kCWarps][kMQ];  // rows to merge, per streaming warp (single producer / consumer)
+    __shared__ volatile int s_mq_tail[kCWarps];
+    __shared__ volatile int s_mq_head[kCWarps];
+    __shared__ int s_done;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int K1 = P.K + 1;
+    const bool dense = P.q != nullptr;
+
+    // ---- prologue: count the active row-chunks and find this CTA's range
+    const int per = (P.B + kPThreads - 1) / kPThreads;
+    const int bb0 = tid * per;
+    long long mine = 0;
+    for (int b = bb0; b < bb0 + per && b < P.B; ++b) mine += static_cast<long long>(gate_keff(P, b, nullptr, false) + 1) * P.nchunk;
+    long long incl = mine;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const long long o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], kCWarps);
+            s_cnt[i] = 0;
+        }
+        for (int i = 0; i <= kStages; ++i) s_rthr[i] = 0u;
+        s_done = 0;
+        mbar_init_fence();
+    }
+    if (tid < kCWarps) {
+        s_mq_tail[tid] = 0;
+        s_mq_head[tid] = 0;
+    }
+    __syncthreads();
+    long long base = 0, total = 0;
+    for (int w = 0; w < kPThreads / 32; ++w) {
+        if (w < warp) base += s_wsum[w];
+        total += s_wsum[w];
+    }
+    const long long G = gridDim.x;
+    const long long w0 = total * blockIdx.x / G, w1 = total * (blockIdx.x + 1) / G;
+    const long long ex = base + incl - mine;  // first row-chunk index of my sequences
+    if (w0 < w1 && w0 >= ex && w0 < ex + mine) {
+        long long acc = ex;
+        for (int b = bb0; b < bb0 + per && b < P.B; ++b) {
+            const long long nb = static_cast<long long>(gate_keff(P, b, nullptr, false) + 1) * P.nchunk;
+            if (w0 < acc + nb) {
+                const long long r = w0 - acc;
+                s_start[0] = b;
+                s_start[1] = static_cast<int>(r / P.nchunk);
+                s_start[2] = static_cast<int>(r % P.nchunk);
+                break;
+            }
+            acc += nb;
+        }
+    }
+    __syncthreads();
+    const int nwork = static_cast<int>(w1 - w0);
+    if (nwork <= 0) return;
+
+    if (warp == kPWarp) {
+        // ================= producer =================
+        int b = s_start[0], j = s_start[1], c = s_start[2];
+        int kb = 0;
+        int keff = 0;
+        int nh = 0;
+        auto load_seq = [&](int bq) {
+            keff = gate_keff(P, bq, &kb, true);
+            if (lane < keff) {
+                const int d = P.drafts[bq * P.K + lane];
+                s_pdrafts[lane] = d;
+                if (!(d >= 0 && d < P.V)) raise_status(P.status, SPECNG_DEV_TOKEN_OOR);
+            }
+            if constexpr (PENALTY) {
+                int L = P.lens[bq];
+                L = L < 0 ? 0 : (static_cast<int64_t>(L) > P.hist_stride ? static_cast<int>(P.hist_stride) : L);
+                nh = L < P.W ? L : P.W;
+                for (int t = lane; t < nh; t += 32) s_hwin[t] = P.hist[static_cast<size_t>(bq) * P.hist_stride + (L - nh) + t];
+            }
+            __syncwarp();
+        };
+        load_seq(b);
+        NoiseKey nk = P.nk;
+        bool ok = true;
+        for (int n = 0; n < nwork && ok; ++n) {
+            const int st = n % kStages;
+            const int use = n / kStages;
+            if (use >= 1) ok = mbar_wait_bounded(&s_empty[st], static_cast<unsigned>((use - 1) & 1));
+            if (!ok) { if (lane == 0) raise_status(P.status, SPECNG_DEV_TIMEOUT); break; }
+            const int v0 = c * CHUNK;
+            const int v1 = min(P.V, v0 + CHUNK);
+            const char* src = static_cast<const char*>(P.logits) +
+                              ((static_cast<size_t>(b) * K1 + j) * P.V + v0) * ElemTraits<BF16>::SIZE;
+            // the copy goes first; the metadata is written while it is in flight, and the
+            // phase completes once both the bytes and the arrive below are in
+            if (P.aligned && lane == 0) {
+                // the empty barrier already orders the consumers' reads of this stage
+                // before the copy that overwrites it
+                mbar_add_tx(&s_full[st], static_cast<unsigned>(v1 - v0) * ElemTraits<BF16>::SIZE);
+                bulk_g2s(s_stage + st * SB, src, static_cast<unsigned>(v1 - v0) * ElemTraits<BF16>::SIZE, &s_full[st]);
+            }
+            StageMeta& mt = s_meta[st];
+            // with dense q, row j < k_eff is sampled by the residual pass unless
+            // its draft is invalid (the residual is then p itself)
+            int excl = -1, cand = 1;
+            if (!GREEDY && j < keff) {
+                const int d = s_pdrafts[j];
+                const bool valid = d >= 0 && d < P.V;
+                if (!dense && valid) excl = d;
+                if (dense && valid) cand = 0;
+            }
+            if (lane == 0) {
+                mt.b = b; mt.j = j; mt.c = c; mt.excl = excl;
+                mt.seg_end = (c == P.nchunk - 1 || n == nwork - 1) ? 1 : 0;
+                mt.cand = cand;
+            }
+            if (!GREEDY && cand) {
+                // noise of the chunk's blocks: one Philox draw serves two blocks
+                // (words 0, 1 the even block, words 2, 3 the odd one)
+                nk.seq = static_cast<uint32_t>(b);
+                for (int q = lane; q < NB; q += 32) {
+                    mt.bn[q] = block_noise(nk, static_cast<uint32_t>((v0 >> kNoiseBlockShift) + q), static_cast<uint32_t>(j));
+                }
+            }
+            if constexpr (PENALTY) {
+                // bitmap of the penalised ids of row j in [v0, v1), and which slices hold one
+                uint32_t* bm = s_bm + st * (CHUNK / 32);
+                for (int t = lane; t < CHUNK / 32; t += 32) bm[t] = 0u;
+                __syncwarp();
+                const WindowView wv{s_hwin, s_pdrafts, nh, P.W};
+                const int nwin = wv.count(j);
+                unsigned pw = 0u;
+                for (int t = lane; t < nwin; t += 32) {
+                    const int tok = wv.token(j, t);
+                    if (tok >= v0 && tok < v1) {
+                        atomicOr(&bm[(tok - v0) >> 5], 1u << ((tok - v0) & 31));
+                        pw |= 1u << ((tok - v0) / SL);
+                    }
+                }
+                pw = __reduce_or_sync(0xffffffffu, pw);
+                if (lane == 0) mt.penw = pw;
+            } else {
+                if (lane == 0) mt.penw = 0u;
+            }
+            if (!P.aligned) {
+                uint8_t* dst = s_stage + st * SB;
+                for (int e = lane; e < v1 - v0; e += 32) {
+                    if constexpr (BF16) reinterpret_cast<uint16_t*>(dst)[e] = reinterpret_cast<const uint16_t*>(src)[e];
+                    else reinterpret_cast<uint32_t*>(dst)[e] = reinterpret_cast<const uint32_t*>(src)[e];
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_full[st]);
+            // advance to the next row-chunk
+            if (++c == P.nchunk) {
+                c = 0;
+                if (++j > keff) {
+                    j = 0;
+                    ++b;
+                    if (n + 1 < nwork) load_seq(b);
+                }
+            }
+        }
+        // the CTA stays resident until every issued copy has landed
+        if (P.aligned && lane == 0) {
+            const int lo = nwork > kStages ? nwork - kStages : 0;
+            for (int n = lo; n < nwork; ++n) mbar_wait_bounded(&s_full[n % kStages], static_cast<unsigned>((n / kStages) & 1));
+        }
+        return;
+    }
+
+    if (warp == kMWarp) {
+        // ================= merge warp =================
+        // Polls the streaming warps' queues (lane q watches queue q) until every
+        // streaming warp has finished and every queue is drained.  The wait is bounded.
+        unsigned idle = 0;
+        while (true) {
+            const bool has = lane < kCWarps && s_mq_head[lane] != s_mq_tail[lane];
+            const unsigned qs = __ballot_sync(0xffffffffu, has);
+            if (qs != 0u) {
+                idle = 0;
+                const int q = __ffs(qs) - 1;
+                const int h = s_mq_head[q];
+                const int row = s_mq[q][h % kMQ];
+                __syncwarp();
+                merge_row<BF16, GREEDY, SOFTCAP, PENALTY>(P, row);
+                __syncwarp();
+                if (lane == 0) s_mq_head[q] = h + 1;
+                __syncwarp();
+                continue;
+            }
+            if (*reinterpret_cast<volatile int*>(&s_done) == kCWarps) {
+                // every push happened before its warp's increment of s_done
+                __threadfence_block();
+                const bool again = lane < kCWarps && s_mq_head[lane] != s_mq_tail[lane];
+                if (!__any_sync(0xffffffffu, again)) break;
+                continue;
+            }
+            if (++idle > (1u << 22)) {
+                if (lane == 0) raise_status(P.status, SPECNG_DEV_TIMEOUT);
+                break;
+            }
+            __nanosleep(idle < 64 ? 32 : 256);
+        }
+        return;
+    }
+
+    // ================= streaming warps =================
+    // Per-lane accumulators live across the chunks of one row (a segment of
+    // the CTA's range); warps combine them once, at the segment's last chunk.
+    const int ubase = warp * (32 * kVL);        // first 16-byte vector of my slice
+    const int off0 = ubase * EPV + lane * EPV;  // chunk offset of vector 0's element 0
+    float thr = -INFINITY;
+    float m = -INFINITY, s = 0.0f, msc = 0.0f;
+    Top2 tt = top2_empty();
+    int seg = 0, cfirst = 0;
+    int row = 0, excl = -1;
+    bool cand = false;
+    RowPhilox rp{};
+    bool fresh = true;
+    for (int n = 0; n < nwork; ++n) {
+        const int st = n % kStages;
+        if (!mbar_wait_bounded(&s_full[st], static_cast<unsigned>((n / kStages) & 1))) {
+            if (lane == 0) raise_status(P.status, SPECNG_DEV_TIMEOUT);
+            break;
+        }
+        const StageMeta& mt = s_meta[st];
+        const int c = mt.c;
+        unsigned* rth = &s_rthr[seg % (kStages + 1)];
+        const bool seg_start = fresh;
+        if (seg_start) {
+            const int b = mt.b, j = mt.j;
+            row = b * K1 + j;
+            excl = mt.excl;
+            cand = !GREEDY && mt.cand != 0;
+            cfirst = c;
+            if (cand) {
+                NoiseKey nk = P.nk;
+                nk.seq = static_cast<uint32_t>(b);
+                rp = row_philox(nk, static_cast<uint32_t>(j));
+            }
+        }
+        const int v0 = c * CHUNK;
+        const int v1 = min(P.V, v0 + CHUNK);
+        const uint4* stage = reinterpret_cast<const uint4*>(s_stage + st * SB);
+        const uint32_t* bm = s_bm + (PENALTY ? st * (CHUNK / 32) : 0);
+        const bool full = v0 + off0 + (kVL - 1) * 32 * EPV + EPV <= v1;  // my four vectors are whole
+        uint4 rv[kVL];
+#pragma unroll
+        for (int i = 0; i < kVL; ++i) rv[i] = stage[ubase + i * 32 + lane];
+        // penalised elements of my lane (bit 8 i + e), only where the slice holds one
+        unsigned pmk = 0u;
+        if constexpr (PENALTY) {
+            if ((mt.penw >> warp) & 1u) {
+#pragma unroll
+                for (int i = 0; i < kVL; ++i) {
+                    const int off = off0 + i * 32 * EPV;
+                    pmk |= ((bm[off >> 5] >> (off & 31)) & ((1u << EPV) - 1u)) << (8 * i);
+                }
+            }
+        }
+
+        // ---- streaming: vector maxima, sum of exponentials; zv[i] bounds the transformed
+        //      values of vector i (penalised ones included)
+        float vmx[kVL];  // raw maxima of my vectors (-inf where empty)
+        float zv[kVL];
+        float lraw = -INFINITY;
+        if (full) {
+#pragma unroll
+            for (int i = 0; i < kVL; ++i) {
+                if constexpr (BF16) {
+                    const __nv_bfloat162 h = bf16x8_max2(rv[i]);
+                    vmx[i] = fmaxf(bf16lo(as_u32(h)), bf16hi(as_u32(h)));
+                } else {
+                    vmx[i] = fmaxf(fmaxf(__uint_as_float(rv[i].x), __uint_as_float(rv[i].y)),
+                                   fmaxf(__uint_as_float(rv[i].z), __uint_as_float(rv[i].w)));
+                }
+            }
+            lraw = fmaxf(fmaxf(vmx[0], vmx[1]), fmaxf(vmx[2], vmx[3]));
+            const float zl = SOFTCAP ? transform_f32<true, false>(lraw, false, P) : lraw;
+#pragma unroll
+            for (int i = 0; i < kVL; ++i) zv[i] = SOFTCAP ? transform_f32<true, false>(vmx[i], false, P) : vmx[i];
+            if constexpr (GREEDY) {
+                if (zl > m) m = zl;
+            } else {
+                if (zl > m) {
+                    s = m > -INFINITY ? s * ex2_approx((m - zl) * P.sc) : 0.0f;
+                    m = zl;
+                    msc = m * P.sc;
+                }
+                float2 acc2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+                const float2 sc2 = make_float2(P.sc, P.sc), nm2 = make_float2(-msc, -msc);
+#pragma unroll
+                for (int i = 0; i < kVL; ++i) {
+                    float x[EPV];
+                    unpack<BF16>(rv[i], x);
+#pragma unroll
+                    for (int e = 0; e < EPV; e += 2) {
+                        const float2 t = __ffma2_rn(make_float2(transform_f32<SOFTCAP, false>(x[e], false, P),
+                                                                transform_f32<SOFTCAP, false>(x[e + 1], false, P)),
+                                                    sc2, nm2);
+                        acc2[i & 1] = __fadd2_rn(acc2[i & 1], make_float2(ex2_approx(t.x), ex2_approx(t.y)));
+                    }
+                }
+                s += (acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y);
+            }
+            if constexpr (PENALTY) {
+                // the few penalised elements: replace their terms by the penalised ones (and
+                // raise the maximum if a penalty below 1 lifted one above it)
+                unsigned pw = pmk;
+                while (pw != 0u) {
+                    const int bit = __ffs(pw) - 1;
+                    pw &= pw - 1u;
+                    const float xe = elem_of_stage<BF16>(stage, off0 + (bit >> 3) * 32 * EPV + (bit & 7));
+                    const float zu = transform_f32<SOFTCAP, false>(xe, false, P);
+                    const float zp = transform_f32<SOFTCAP, true>(xe, true, P);
+#pragma unroll
+                    for (int i = 0; i < kVL; ++i)
+                        if ((bit >> 3) == i) zv[i] = fmaxf(zv[i], zp);
+                    if constexpr (GREEDY) {
+                        m = fmaxf(m, zp);
+                    } else {
+                        if (zp > m) {
+                            s *= ex2_approx((m - zp) * P.sc);
+                            m = zp;
+                            msc = m * P.sc;
+                        }
+                        s += ex2_approx(fmaf(zp, P.sc, -msc)) - ex2_approx(fmaf(zu, P.sc, -msc));
+                    }
+                }
+            }
+        } else {
+            // partial vectors (a row's last chunk): exact transform element by element
+#pragma unroll
+            for (int i = 0; i < kVL; ++i) {
+                vmx[i] = -INFINITY;
+                zv[i] = -INFINITY;
+                const int off = off0 + i * 32 * EPV;
+                const int nv = min(EPV, v1 - (v0 + off));
+                if (nv <= 0) continue;
+                float x[EPV];
+                unpack<BF16>(rv[i], x);
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) {
+                    if (e >= nv) break;
+                    const float z = transform_f32<SOFTCAP, PENALTY>(x[e], (pmk >> (8 * i + e)) & 1u, P);
+                    vmx[i] = fmaxf(vmx[i], x[e]);
+                    zv[i] = fmaxf(zv[i], z);
+                    if constexpr (GREEDY) {
+                        m = fmaxf(m, z);
+                    } else {
+                        if (z > m) {
+                            s = m > -INFINITY ? s * ex2_approx((m - z) * P.sc) : 0.0f;
+                            m = z;
+                            msc = m * P.sc;
+                        }
+                        s += ex2_approx(fmaf(z, P.sc, -msc));
+                    }
+                }
+                lraw = fmaxf(lraw, vmx[i]);
+            }
+        }
+
+        // ---- candidates
+        if constexpr (GREEDY) {
+            // top two transformed values (lower id on ties) within cand_delta of the best
+            // value any warp of the CTA has reached in this segment.  Without a penalty the
+            // lane maximum is itself a value of the row (the transform is monotone)
+            const float zl = fmaxf(fmaxf(zv[0], zv[1]), fmaxf(zv[2], zv[3]));
+            float gth = fmaxf(tt.s1, key_score(*reinterpret_cast<volatile unsigned*>(rth)));
+            if constexpr (!PENALTY) gth = fmaxf(gth, key_score(warp_best_key(zl)));
+            gth = gth > -INFINITY ? gth - cand_delta(gth) : -INFINITY;
+            if (zl >= gth) {
+#pragma unroll
+                for (int i = 0; i < kVL; ++i) {
+                    const int off = off0 + i * 32 * EPV;
+                    const int nv = min(EPV, v1 - (v0 + off));
+                    if (nv <= 0 || !(zv[i] >= gth)) continue;
+                    float x[EPV];
+                    unpack<BF16>(rv[i], x);
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) {
+                        if (e >= nv) break;
+                        const float z = transform_f32<SOFTCAP, PENALTY>(x[e], (pmk >> (8 * i + e)) & 1u, P);
+                        if (z >= gth) {
+                            top2_push(tt, z, v0 + off + e);
+                            gth = fmaxf(gth, tt.s1 - cand_delta(tt.s1));
+                        }
+                    }
+                }
+            }
+            const unsigned kw = warp_best_key(tt.s1);
+            if (lane == 0 && kw != 0u) atomicMax(rth, kw);
+        } else if (cand) {
+            // noise blocks of my four vectors
+            BlockNoise bn[kVL];
+#pragma unroll
+            for (int i = 0; i < kVL; ++i) bn[i] = mt.bn[(off0 + i * 32 * EPV) >> kNoiseBlockShift];
+            int seeded = -1;
+            if (seg_start) {
+                // seed: every lane scores its largest raw element (any exact score bounds the
+                // best from below); the CTA's warps share the best seed
+                int am = -1, ai = 0;
+#pragma unroll
+                for (int i = kVL - 1; i >= 0; --i) {
+                    const int off = off0 + i * 32 * EPV;
+                    const int nv = min(EPV, v1 - (v0 + off));
+                    float x[EPV];
+                    unpack<BF16>(rv[i], x);
+#pragma unroll
+                    for (int e = EPV - 1; e >= 0; --e)
+                        if (e < nv && x[e] == lraw) { am = off + e; ai = i; }
+                }
+                float t0 = -INFINITY;
+                if (am >= 0 && v0 + am != excl) {
+                    const float z = transform_f32<SOFTCAP, PENALTY>(elem_of_stage<BF16>(stage, am),
+                                                                    PENALTY && ((bm[am >> 5] >> (am & 31)) & 1u), P);
+                    const uint32_t v = static_cast<uint32_t>(v0 + am);
+                    float M = bn[0].M;
+                    int I = bn[0].I;
+#pragma unroll
+                    for (int i = 1; i < kVL; ++i)
+                        if (ai == i) { M = bn[i].M; I = bn[i].I; }
+                    t0 = z * P.invT - ln_fast(noise_exp_f32(rp, M, I, v));
+                    top2_push(tt, t0, static_cast<int>(v));
+                    seeded = static_cast<int>(v);
+                }
+                const unsigned k0 = warp_best_key(t0);
+                if (k0 != 0u) {
+                    const float b0 = key_score(k0);
+                    thr = fmaxf(thr, b0 - cand_delta(b0));
+                    if (lane == 0) atomicMax(rth, k0);
+                }
+            }
+            {
+                // adopt the best score another warp published for this segment
+                const float best = key_score(*reinterpret_cast<volatile unsigned*>(rth));
+                if (best > -INFINITY) thr = fmaxf(thr, best - cand_delta(best));
+            }
+            // block tests: every score of vector i is at most z / T - ln M_i
+            unsigned pv = 0u;
+#pragma unroll
+            for (int i = 0; i < kVL; ++i) {
+                const float zb = zv[i] * P.invT;
+                if (zb - bn[i].lnM + bound_slack(zb) >= thr) pv |= 1u << i;
+            }
+            if (__any_sync(0xffffffffu, pv != 0u)) {
+                // elements of the passing vectors that can reach the best
+                unsigned msk = 0u;
+#pragma unroll
+                for (int i = 0; i < kVL; ++i) {
+                    if (!((pv >> i) & 1u)) continue;
+                    const int off = off0 + i * 32 * EPV;
+                    if (full) {
+                        // z >= T (thr + ln M), in raw units
+                        const float zt = (thr + bn[i].lnM) * P.T;
+                        float xt = zt;
+                        if constexpr (SOFTCAP) {
+                            // shrink by more than the fp32 error of c tanh(x / c) before
+                            // inverting: atanh is steep near |u| = 1
+                            float u = zt * P.invcap;
+                            u -= 1e-6f * fabsf(u) + 1e-7f;
+                            xt = u > 1.0f ? INFINITY : (u <= -1.0f ? -INFINITY : P.cap * atanhf(fminf(u, 1.0f - 1e-7f)));
+                        }
+                        xt -= 1e-5f * (1.0f + fabsf(xt));  // slack for the rounding of the transform
+                        unsigned mi;
+                        if constexpr (BF16) {
+                            mi = bf16x8_ge_bits(rv[i], bf16x2_floor(xt));
+                        } else {
+                            mi = static_cast<unsigned>(__uint_as_float(rv[i].x) >= xt);
+                            mi |= static_cast<unsigned>(__uint_as_float(rv[i].y) >= xt) << 1;
+                            mi |= static_cast<unsigned>(__uint_as_float(rv[i].z) >= xt) << 2;
+                            mi |= static_cast<unsigned>(__uint_as_float(rv[i].w) >= xt) << 3;
+                        }
+                        msk |= (mi | ((pmk >> (8 * i)) & 0xFFu)) << (8 * i);  // penalised: decided exactly below
+                    } else {
+                        const int nv = min(EPV, v1 - (v0 + off));
+                        if (nv > 0) msk |= ((1u << nv) - 1u) << (8 * i);
+                    }
+                }
+                if (seeded >= 0) {
+                    const int so = seeded - v0 - off0;
+                    const int si = so / (32 * EPV), se = so - si * 32 * EPV;
+                    if (se >= 0 && se < EPV) msk &= ~(1u << (8 * si + se));
+                }
+                // score the lane's candidates one per iteration, the warp in step
+                while (__any_sync(0xffffffffu, msk != 0u)) {
+                    int v = -1, bi = 0;
+                    float zb = -INFINITY;
+                    if (msk != 0u) {
+                        const int bit = __ffs(msk) - 1;
+                        msk &= msk - 1u;
+                        bi = bit >> 3;
+                        const int loc = off0 + bi * 32 * EPV + (bit & 7);
+                        const bool pen = PENALTY && ((pmk >> bit) & 1u);
+                        zb = transform_f32<SOFTCAP, PENALTY>(elem_of_stage<BF16>(stage, loc), pen, P) * P.invT;
+                        v = v0 + loc;
+                    }
+                    float M = bn[0].M, lnM = bn[0].lnM;
+                    int I = bn[0].I;
+#pragma unroll
+                    for (int i = 1; i < kVL; ++i)
+                        if (bi == i) { M = bn[i].M; lnM = bn[i].lnM; I = bn[i].I; }
+                    const bool live = v >= 0 && v != excl && zb - lnM + bound_slack(zb) >= thr;
+                    if (__any_sync(0xffffffffu, live)) {
+                        const float E = noise_exp_f32(rp, M, I, static_cast<uint32_t>(v < 0 ? 0 : v));
+                        if (live) {
+                            const float score = zb - ln_fast(E);
+                            if (score >= thr) {
+                                top2_push(tt, score, v);
+                                thr = fmaxf(thr, tt.s1 - cand_delta(tt.s1));
+                            }
+                        }
+                    }
+                }
+                // share the warp's best score with the CTA
+                const unsigned kw = warp_best_key(tt.s1);
+                if (kw != 0u) {
+                    const float bw = key_score(kw);
+                    thr = fmaxf(thr, bw - cand_delta(bw));
+                    if (lane == 0) atomicMax(rth, kw);
+                }
+            }
+        }
+
+        fresh = mt.seg_end != 0;
+        if (fresh) {
+            // ---- end of this row's segment: one partial for the segment
+            float pm = m, ps = s;
+            Top2 pt = tt;
+            if constexpr (!GREEDY) {
+                if (!(pm > -INFINITY)) ps = 0.0f;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    const float mo = __shfl_xor_sync(0xffffffffu, pm, off);
+                    const float so = __shfl_xor_sync(0xffffffffu, ps, off);
+                    ms_merge(pm, ps, mo, so, P.sc);
+                }
+            }
+            pt = top2_warp_reduce(pt);
+            int last = 0;
+            if (lane == 0) {
+                s_slot[st][warp] = WarpPart{pm, ps, pt};
+                __threadfence_block();
+                last = atomicAdd(&s_cnt[st], 1) == kCWarps - 1;
+            }
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (last) {
+                __threadfence_block();
+                WarpPart wp = lane < kCWarps ? s_slot[st][lane] : WarpPart{-INFINITY, 0.0f, top2_empty()};
+                float cm = wp.m, cs = wp.s;
+                Top2 ct = wp.t;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    const float mo = __shfl_xor_sync(0xffffffffu, cm, off);
+                    const float so = __shfl_xor_sync(0xffffffffu, cs, off);
+                    ms_merge(cm, cs, mo, so, P.sc);
+                    ct = top2_merge(ct, top2_shfl_xor(ct, off));
+                }
+                int merge_now = 0;
+                if (lane == 0) {
+                    // keyed by the segment's last chunk; a written partial is never all-zero
+                    st_partial(P.part + static_cast<size_t>(row) * P.nchunk + c, GREEDY ? 0.0f : cm,
+                               GREEDY ? 1.0f : cs, ct);
+                    s_cnt[st] = 0;
+                    *rth = 0u;  // every warp is past this segment: the slot is free
+                    // the CTA that completes the row's chunks merges it
+                    __threadfence();
+                    const unsigned nseg = static_cast<unsigned>(c - cfirst + 1);
+                    const unsigned prev = atomicAdd(&P.row_ticket[row], nseg);
+                    if (prev + nseg == static_cast<unsigned>(P.nchunk)) {
+                        __threadfence();
+                        const int tl = s_mq_tail[warp];
+                        if (tl - s_mq_head[warp] < kMQ) {
+                            s_mq[warp][tl % kMQ] = row;
+                            __threadfence_block();
+                            s_mq_tail[warp] = tl + 1;
+                        } else {
+                            merge_now = 1;  // queue full: merge here
+                        }
+                    }
+                }
+                merge_now = __shfl_sync(0xffffffffu, merge_now, 0);
+                if (merge_now) merge_row<BF16, GREEDY, SOFTCAP, PENALTY>(P, row);
+            }
+            m = -INFINITY;
+            s = 0.0f;
+            msc = 0.0f;
+            tt = top2_empty();
+            thr = -INFINITY;
+            ++seg;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_empty[st]);
+    }
+    __syncwarp();
+    if (lane == 0) {
+        __threadfence_block();
+        atomicAdd(&s_done, 1);
+    }
+}
+
 // ---------------------------------------------------------------- K2
 // Dense draft distributions: after a rejection at row a, sample from the
 // residual max(0, p_a - q_a) by Gumbel-max over row a (the logits of row a
 // read once more and q_a read at the candidates only, for the rejected
-// sequences).  log r_v <= log p_v = z_v / T - lse, so an element can beat
-// the threshold only if z_v / T - lse + g_max reaches it.  The threshold
-// starts from the exact residual score of the row's bonus sample (when its
-// residual is positive) and is shared by the CTA's warps and, through the
-// workspace, by the CTAs of the row.
+// sequences).  log r_v <= log p_v = z_v / T - lse and E_v >= M of its block,
+// so an element can beat the best score only if z_v / T - lse - ln M reaches
+// it.  The best starts from the exact residual score of each lane's largest p
+// and is shared by the CTA's warps and, through the workspace, by the CTAs of
+// the row.
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kNV = 8;  // 16-byte vectors per thread per chunk
+static_assert(kChunkBytes == kThreads * kNV * 16, "residual chunk layout");
 
 // log max(0, p - q) for log p = lp, in fp32 without cancellation: for q > 0,
 // p - q = q (e^(lp - ln q) - 1), and expm1 keeps the relative accuracy when
@@ -1226,16 +1170,43 @@ __device__ __forceinline__ float log_residual(float lp, float q) {
     return logf(q) + logf(expm1f(d));
 }
 
+// Penalty window of row j of sequence b: the last W tokens of
+// history[:lens] ++ d_1..d_j.  Fills s_win / s_nwin and, for the chunk
+// [v0, v1), the bitmap s_bm.  Whole CTA calls it.
+template <int CHUNK>
+__device__ __forceinline__ void build_window(const VerifyDev& P, int b, int j, int v0, int v1,
+                                             uint32_t* s_bm, int* s_win, int* s_nwin) {
+    const int tid = threadIdx.x;
+    int L = P.lens[b];
+    L = L < 0 ? 0 : (static_cast<int64_t>(L) > P.hist_stride ? static_cast<int>(P.hist_stride) : L);
+    const int total = L + j;
+    const int start = total - P.W > 0 ? total - P.W : 0;
+    const int nw = total - start;
+    for (int t = tid; t < CHUNK / 32; t += kThreads) s_bm[t] = 0u;
+    int tok = -1;
+    if (tid < nw) {
+        const int idx = start + tid;
+        tok = idx < L ? P.hist[static_cast<size_t>(b) * P.hist_stride + idx] : P.drafts[b * P.K + (idx - L)];
+        s_win[tid] = tok;
+    }
+    if (tid == 0) *s_nwin = nw;
+    __syncthreads();
+    if (tok >= v0 && tok < v1) atomicOr(&s_bm[(tok - v0) >> 5], 1u << ((tok - v0) & 31));
+    __syncthreads();
+}
+
 template <bool BF16, bool SOFTCAP, bool PENALTY>
 __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const VerifyDev P) {
     constexpr int EPV = ElemTraits<BF16>::EPV;
     constexpr int CHUNK = chunk_elems<BF16>();
+    constexpr int NB = CHUNK >> kNoiseBlockShift;
     __shared__ uint32_t s_bm[PENALTY ? CHUNK / 32 : 1];
     __shared__ int s_win[PENALTY ? SPECNG_MAX_REP_WINDOW : 1];
     __shared__ int s_nwin;
     __shared__ Top2 s_t[kWarps];
     __shared__ int s_last;
     __shared__ unsigned s_thr;
+    __shared__ BlockNoise s_bn[NB];
     __shared__ uint16_t s_q2[kWarps * 32 * kNV * EPV];  // per-warp candidate queues (chunk offsets)
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1258,6 +1229,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const Veri
     const RowPhilox rp = row_philox(nk, static_cast<uint32_t>(a));
 
     if (tid == 0) s_thr = 0u;
+    if (tid < NB) s_bn[tid] = block_noise(nk, static_cast<uint32_t>((v0 >> kNoiseBlockShift) + tid), static_cast<uint32_t>(a));
     if constexpr (PENALTY) build_window<CHUNK>(P, b, a, v0, v1, s_bm, s_win, &s_nwin);
     __syncthreads();
     // the chunk in registers: every thread's eight 16-byte vectors, loaded together
@@ -1268,6 +1240,10 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const Veri
         rv[i] = e0 < v1 ? load_vec<BF16>(rowp, e0, v1, P.aligned) : make_uint4(0u, 0u, 0u, 0u);
     }
     auto lp_of = [&](float x, bool pen) { return transform_f32<SOFTCAP, PENALTY>(x, pen, P) * P.invT - lse_f; };
+    auto pen_at = [&](int off) -> unsigned {
+        if constexpr (PENALTY) return (s_bm[off >> 5] >> (off & 31)) & ((1u << EPV) - 1u);
+        return 0u;
+    };
     // ---- seed: each lane scores the residual of its largest p; the CTA and the row
     //      share the best (any element's exact score bounds the best from below)
     Top2 tt = top2_empty();
@@ -1282,7 +1258,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const Veri
             if (nv <= 0) continue;
             float x[EPV];
             unpack<BF16>(rv[i], x);
-            const unsigned pb = pen_bits<PENALTY, EPV>(s_bm, off);
+            const unsigned pb = pen_at(off);
 #pragma unroll
             for (int e = 0; e < EPV; ++e) {
                 if (e >= nv) break;
@@ -1294,8 +1270,8 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const Veri
         if (im >= 0) {
             const float lr = log_residual(lm, __ldcs(qrow + im));
             if (lr > -INFINITY) {
-                t0 = lr + gumbel_f32(pick_word(gumbel_block_row(rp, static_cast<uint32_t>(im) >> 2),
-                                               static_cast<uint32_t>(im) & 3u));
+                const BlockNoise bn = s_bn[(im - v0) >> kNoiseBlockShift];
+                t0 = lr - ln_fast(noise_exp_f32(rp, bn.M, bn.I, static_cast<uint32_t>(im)));
                 top2_push(tt, t0, im);
                 seeded = im;
             }
@@ -1313,8 +1289,8 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const Veri
             thr = bw - cand_delta(bw);
         }
     }
-    // ---- candidates: log r_v <= lp_v, so lp_v + g_max must reach the threshold.  They
-    //      are compacted per warp (chunk offsets), then scored 32 at a time, so the
+    // ---- candidates: log r_v - ln E_v <= lp_v - ln M, so that bound must reach the best.
+    //      They are compacted per warp (chunk offsets), then scored 32 at a time, so the
     //      loads of a batch (the logit, from L2, and q) are issued together
     uint16_t* qw = s_q2 + warp * (32 * kNV * EPV);
     int nq = 0;
@@ -1326,10 +1302,14 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const Veri
         if (nv > 0) {
             float x[EPV];
             unpack<BF16>(rv[i], x);
-            const unsigned pb = pen_bits<PENALTY, EPV>(s_bm, off);
+            const unsigned pb = pen_at(off);
+            const float lnM = s_bn[off >> kNoiseBlockShift].lnM;
 #pragma unroll
-            for (int e = 0; e < EPV; ++e)
-                if (e < nv && !(lp_of(x[e], (pb >> e) & 1u) + kGumbelMax < thr) && v0 + off + e != seeded) mi |= 1u << e;
+            for (int e = 0; e < EPV; ++e) {
+                if (e >= nv) break;
+                const float bnd = lp_of(x[e], (pb >> e) & 1u) - lnM;
+                if (bnd + bound_slack(bnd) >= thr && v0 + off + e != seeded) mi |= 1u << e;
+            }
         }
         const unsigned cnt = __popc(mi);
         unsigned incl = cnt;
@@ -1355,14 +1335,14 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const Veri
         const float x = in ? static_cast<float>(raw_logit_f64<BF16>(P.logits, row, P.V, v)) : 0.0f;
         const float qv = in ? __ldcs(qrow + v) : 0.0f;
         const bool pen = PENALTY && ((s_bm[loc >> 5] >> (loc & 31)) & 1u);
+        const BlockNoise bn = s_bn[loc >> kNoiseBlockShift];
         const float lp = lp_of(x, pen);
-        const float lr = in && !(lp + kGumbelMax < thr) ? log_residual(lp, qv) : -INFINITY;
-        const bool live = lr > -INFINITY;
+        const float lr = in && lp - bn.lnM + bound_slack(lp) >= thr ? log_residual(lp, qv) : -INFINITY;
+        const bool live = lr > -INFINITY && lr - bn.lnM + bound_slack(lr) >= thr;
         if (__any_sync(0xffffffffu, live)) {
-            const uint32_t word = pick_word(gumbel_block_row(rp, static_cast<uint32_t>(v) >> 2),
-                                            static_cast<uint32_t>(v) & 3u);
-            if (live && gumbel_may_reach(word, thr - lr - 1e-4f)) {
-                const float score = lr + gumbel_f32(word);
+            const float E = noise_exp_f32(rp, bn.M, bn.I, static_cast<uint32_t>(v));
+            if (live) {
+                const float score = lr - ln_fast(E);
                 if (score >= thr) {
                     top2_push(tt, score, v);
                     thr = fmaxf(thr, tt.s1 - cand_delta(tt.s1));
@@ -1421,8 +1401,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const Veri
         const double z = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, id), h == 0 ? pen1 : pen2, P);
         const double rsd = exp(z / P.Td - lse) - static_cast<double>(qrow[id]);
         if (!(rsd > 0.0)) continue;
-        const uint4 w = gumbel_block(nk, static_cast<uint32_t>(id) >> 2, static_cast<uint32_t>(a));
-        const double score = log(rsd) + gumbel_f64(pick_word(w, static_cast<uint32_t>(id) & 3u));
+        const double score = log(rsd) - log(noise_exp_f64(nk, static_cast<uint32_t>(id), static_cast<uint32_t>(a)));
         if (winner < 0 || better64(score, id, best, winner)) { best = score; winner = id; }
     }
     // all-zero residual (p <= q everywhere): sample from p, the row's bonus candidate
@@ -1430,9 +1409,62 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const Veri
     P.out_tokens[static_cast<size_t>(b) * K1 + a] = winner;
 }
 
-// Host-side launch of one dtype (defined in verify_bf16.cu / verify_f32.cu).
+// ---------------------------------------------------------------- launch
+
+__host__ inline int sm_count_cached() {
+    static int cached[128] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 1;
+    if (cached[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = n > 0 ? n : 1;
+    }
+    return cached[dev];
+}
+
+template <bool BF16, bool G, bool C, bool R>
+cudaError_t launch_stream(const VerifyDev& P, cudaStream_t s) {
+    // one persistent CTA per SM; the staging ring lives in dynamic shared memory
+    constexpr size_t smem = k1_dyn_smem<R>();
+    static bool configured = false;
+    if (!configured) {
+        const cudaError_t e = cudaFuncSetAttribute(verify_stream_kernel<BF16, G, C, R>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    verify_stream_kernel<BF16, G, C, R><<<sm_count_cached(), kPThreads, smem, s>>>(P);
+    return cudaGetLastError();
+}
+
+template <bool BF16, bool C, bool R>
+cudaError_t launch_residual(const VerifyDev& P, cudaStream_t s) {
+    const unsigned grid = static_cast<unsigned>(P.B) * static_cast<unsigned>(P.nchunk);
+    verify_residual_kernel<BF16, C, R><<<grid, kThreads, 0, s>>>(P);
+    return cudaGetLastError();
+}
+
+template <bool BF16, bool G>
+cudaError_t launch_stream_cr(const VerifyDev& P, bool c, bool r, cudaStream_t s) {
+    if (c) return r ? launch_stream<BF16, G, true, true>(P, s) : launch_stream<BF16, G, true, false>(P, s);
+    return r ? launch_stream<BF16, G, false, true>(P, s) : launch_stream<BF16, G, false, false>(P, s);
+}
+
+// The kernels of one spec_verify call for one logits dtype: the streaming
+// kernel (with the merges), then, for dense q at T > 0, the residual pass.
 template <bool BF16>
 cudaError_t launch_verify_dtype(const VerifyDev& P, bool greedy, bool softcap, bool penalty, bool dense,
                                 cudaStream_t s);
+
+template <bool BF16>
+cudaError_t launch_verify_impl(const VerifyDev& P, bool greedy, bool softcap, bool penalty, bool dense,
+                               cudaStream_t s) {
+    cudaError_t e = greedy ? launch_stream_cr<BF16, true>(P, softcap, penalty, s)
+                           : launch_stream_cr<BF16, false>(P, softcap, penalty, s);
+    if (e != cudaSuccess || !dense || greedy) return e;
+    if (softcap) return penalty ? launch_residual<BF16, true, true>(P, s) : launch_residual<BF16, true, false>(P, s);
+    return penalty ? launch_residual<BF16, false, true>(P, s) : launch_residual<BF16, false, false>(P, s);
+}
 
 }  // namespace specng

@@ -108,13 +108,13 @@ def test_uniformity_chisq():
 
 def test_counter_layout_lanes():
     # four consecutive vocab ids share one Philox block for their element draws and take its four
-    # words; 1024 consecutive ids share one block draw (M = E(word 0) / 1024, I = word 1 & 1023)
+    # words; 256 consecutive ids share one block draw (M = E(word 0) / 256, I = word 1 & 255)
     k0, k1 = philox.seed_key(77)
     words = philox.philox4x32_10(5, 3, 8, 2, k0, k1)
     F = philox.exp_from_uniform(philox.uniform_from_word(np.array([int(w) for w in words], dtype=np.uint64)))
     b0, b1, _, _ = philox.philox4x32_10(0, 3 | (2 << 16), 8, 2, k0, k1)
-    M = philox.exp_from_uniform(philox.uniform_from_word(np.uint64(int(b0)))) / 1024
-    I = int(b1) & 1023
+    M = philox.exp_from_uniform(philox.uniform_from_word(np.uint64(int(b0)))) / 256
+    I = int(b1) & 255
     ids = np.arange(20, 24)
     E = np.where(ids == I, M, M + F)
     np.testing.assert_array_equal(philox.exp_noise(77, 2, 8, 3, ids), E)
@@ -129,7 +129,7 @@ def test_counter_layout_lanes():
 def test_gumbel_row_equals_per_id_noise():
     seq = np.array([0, 5, 9])
     pos = np.array([0, 2, 4])
-    for V in (1, 7, 8, 33, 1024, 2500):
+    for V in (1, 7, 8, 33, 256, 1100):
         row = philox.gumbel_row(3, seq, 11, pos, V)
         ref = philox.gumbel_noise(3, seq[:, None], 11, pos[:, None], np.arange(V)[None, :])
         np.testing.assert_array_equal(row, ref)
@@ -144,25 +144,28 @@ def test_exp_map_closed_form():
     assert E[2] == -np.log1p(-2.0 ** -24) and abs(E[3] - 24 * np.log(2.0)) < 1e-13
 
 
-def _block_rows(n, V=2048, seed=2718, step=5, pos=1):
+NB = philox.NOISE_BLOCK
+
+
+def _block_rows(n, V=2 * NB, seed=2718, step=5, pos=1):
     return philox.exp_row(seed, np.arange(n), step, pos, V)
 
 
 def _block_law_pvalues(E):
-    """p-values of the order-statistics laws of the first two 1024-id blocks of
-    rows E [n, >= 2048] and of the Exp(1) marginals of a few ids."""
+    """p-values of the order-statistics laws of the first two blocks of rows
+    E [n, >= 2 NB] and of the Exp(1) marginals of a few ids."""
     n = E.shape[0]
     pv = []
     for blk in (0, 1):
-        sl = E[:, blk * 1024:(blk + 1) * 1024]
+        sl = E[:, blk * NB:(blk + 1) * NB]
         e = np.sort(sl, axis=1)
-        pv.append(stats.kstest(1024 * e[:, 0], "expon").pvalue)              # minimum ~ Exp(1024)
-        pv.append(stats.kstest(1023 * (e[:, 1] - e[:, 0]), "expon").pvalue)  # next gap ~ Exp(1023)
-        counts = np.bincount(np.argmin(sl, axis=1) >> 4, minlength=64)        # argmin uniform
+        pv.append(stats.kstest(NB * e[:, 0], "expon").pvalue)                # minimum ~ Exp(NB)
+        pv.append(stats.kstest((NB - 1) * (e[:, 1] - e[:, 0]), "expon").pvalue)  # next gap ~ Exp(NB - 1)
+        counts = np.bincount(np.argmin(sl, axis=1) * 64 // NB, minlength=64)  # argmin uniform
         pv.append(stats.chisquare(counts).pvalue)
-    for v in (0, 1, 511, 1023, 1024, 2047):
+    for v in (0, 1, NB // 2 - 1, NB - 1, NB, 2 * NB - 1):
         pv.append(stats.kstest(E[:, v], "expon").pvalue)
-    c = np.corrcoef(E[:, [0, 1, 700, 1023, 1024]].T)
+    c = np.corrcoef(E[:, [0, 1, NB // 2 + 5, NB - 1, NB]].T)
     pv.append(1.0 if np.abs(c[~np.eye(5, dtype=bool)]).max() < 5 / np.sqrt(n) else 0.0)
     return np.array(pv)
 
@@ -179,18 +182,18 @@ def test_block_construction_laws():
 def test_block_pins_catch_planted_mistakes(mistake):
     """Each plausible slip in the block construction, planted in a copy built
     from the oracle's own draws, fails the law checks above."""
-    n, V = 3000, 2048
+    n, V = 3000, 2 * NB
     seq = np.arange(n)[:, None]
     v = np.arange(V)[None, :]
-    M, I = philox.block_draw(11, seq, 3, 0, v >> 10)
+    M, I = philox.block_draw(11, seq, 3, 0, v // NB)
     F = philox.element_exp(11, seq, 3, 0, v)
-    slot = v & 1023
+    slot = v % NB
     if mistake == "no_min_added":
         E = np.where(slot == I, M, F)
     elif mistake == "argmin_on_half":
-        E = np.where(slot == (I & 511), M, M + F)
+        E = np.where(slot == (I % (NB // 2)), M, M + F)
     elif mistake == "min_rate_1":
-        E = np.where(slot == I, M * 1024, M * 1024 + F)
+        E = np.where(slot == I, M * NB, M * NB + F)
     else:
         E = M + F
     assert _block_law_pvalues(E).min() < 1e-6
@@ -202,9 +205,9 @@ def test_block_pins_catch_planted_mistakes(mistake):
 def test_gumbel_max_over_blocks_matches_softmax():
     """argmax_v (log p_v - ln E_v) is distributed as p, with the mass spread
     across the boundary of two blocks."""
-    V = 2048
+    V = 4 * NB
     v = np.arange(V)
-    x = -np.abs(v - 1023.5) / 3.0
+    x = -np.abs(v - (2 * NB - 0.5)) / 3.0
     logp = x - (x.max() + np.log(np.sum(np.exp(x - x.max()))))
     n = 20000
     g = -np.log(_block_rows(n, V, seed=99, step=1, pos=0))
