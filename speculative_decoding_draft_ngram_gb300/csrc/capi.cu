@@ -67,8 +67,9 @@ struct WsLayout {
     size_t row_ticket, row_thr, seq_ticket, seq_ticket2;
 };
 
-// The f32 chunk is the smaller one, so its chunk count bounds both dtypes.
+// The f32 chunks are the smaller ones, so their counts bound both dtypes.
 int max_chunks(int V) { return (V + chunk_elems<false>() - 1) / chunk_elems<false>(); }
+int max_chunks2(int V) { return (V + res_chunk_elems<false>() - 1) / res_chunk_elems<false>(); }
 
 WsLayout ws_layout(int B, int K, int V) {
     const size_t rows = static_cast<size_t>(B) * (K + 1);
@@ -78,7 +79,7 @@ WsLayout ws_layout(int B, int K, int V) {
     L.part = off;    off = align256(off + rows * nch * sizeof(Partial));
     L.rowres = off;  off = align256(off + rows * sizeof(RowRes));
     L.seqres = off;  off = align256(off + static_cast<size_t>(B) * sizeof(SeqRes));
-    L.part2 = off;   off = align256(off + static_cast<size_t>(B) * nch * sizeof(Partial));
+    L.part2 = off;   off = align256(off + static_cast<size_t>(B) * static_cast<size_t>(max_chunks2(V)) * sizeof(Partial));
     L.tickets = off;
     L.row_ticket = off;   off += rows * sizeof(unsigned);
     L.row_thr = off;      off += rows * sizeof(unsigned);
@@ -280,7 +281,9 @@ int spec_verify(const void* logits, int logits_dtype, int B, int K, int V, const
     const bool bf16 = logits_dtype == SPECNG_BF16;
     const int chunk = bf16 ? chunk_elems<true>() : chunk_elems<false>();
     const int nchunk = (V + chunk - 1) / chunk;
-    if (static_cast<int64_t>(B) * (K + 1) * nchunk > 0x7FFFFFFFLL)
+    const int chunk2 = bf16 ? res_chunk_elems<true>() : res_chunk_elems<false>();
+    const int nchunk2 = (V + chunk2 - 1) / chunk2;
+    if (static_cast<int64_t>(B) * (K + 1) * nchunk2 > 0x7FFFFFFFLL)
         return fail(SPECNG_EINVAL, "spec_verify: B * (K + 1) * chunks exceeds the grid limit");
 
     const bool greedy = p.temperature == 0.0f;
@@ -290,7 +293,7 @@ int spec_verify(const void* logits, int logits_dtype, int B, int K, int V, const
 
     VerifyDev P{};
     P.logits = logits;
-    P.B = B; P.K = K; P.V = V; P.nchunk = nchunk;
+    P.B = B; P.K = K; P.V = V; P.nchunk = nchunk; P.nchunk2 = nchunk2;
     P.drafts = drafts; P.q = draft_probs; P.k = k;
     P.hist = history; P.hist_stride = hist_stride; P.lens = lens;
     P.T = p.temperature;

@@ -148,15 +148,6 @@ struct BlockNoise {
     int pad;
 };
 
-__device__ __forceinline__ BlockNoise block_noise(const NoiseKey& nk, uint32_t blk, uint32_t pos) {
-    const uint4 w = block_words(nk, blk, pos);
-    BlockNoise r;
-    r.M = exp_of_word(w.x) * 0x1p-8f;
-    r.lnM = logf(r.M);  // exact to an ulp: it bounds every score of the block
-    r.I = static_cast<int>(w.y & kNoiseBlockMask);
-    r.pad = 0;
-    return r;
-}
 
 // Screening precision (fp32 scores that only order candidates; every final
 // decision between close scores is re-taken in fp64).  -ln u for a Philox
@@ -184,6 +175,18 @@ __device__ __forceinline__ float noise_exp_f32(const RowPhilox& rp, float M, int
 
 // ln E at screening precision: 3 ulp of |ln E| (hardware logarithm).
 __device__ __forceinline__ float ln_fast(float e) { return __logf(e); }
+
+// A block's draw at screening precision (the bound ln M is off by a few ulp at
+// most, far inside the slack every comparison with it carries).
+__device__ __forceinline__ BlockNoise block_noise(const NoiseKey& nk, uint32_t blk, uint32_t pos) {
+    const uint4 w = block_words(nk, blk, pos);
+    BlockNoise r;
+    r.M = exp_of_word_fast(w.x) * 0x1p-8f;
+    r.lnM = ln_fast(r.M);
+    r.I = static_cast<int>(w.y & kNoiseBlockMask);
+    r.pad = 0;
+    return r;
+}
 
 // E_v in fp64, the oracle's arithmetic, for the final decisions.
 __device__ __forceinline__ double noise_exp_f64(const NoiseKey& nk, uint32_t v, uint32_t pos) {

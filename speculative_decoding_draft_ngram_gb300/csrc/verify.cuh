@@ -28,11 +28,14 @@ template <bool BF16> struct ElemTraits;
 template <> struct ElemTraits<true> { static constexpr int EPV = 8; static constexpr int SIZE = 2; };
 template <> struct ElemTraits<false> { static constexpr int EPV = 4; static constexpr int SIZE = 4; };
 
-// One chunk of a row = one 32 KB stage of the streaming ring = one CTA of the
-// residual pass.
-constexpr int kChunkBytes = 32768;
+// One chunk of a row = one 64 KB stage of the streaming ring; the residual
+// pass takes 32 KB chunks, one per CTA.
+constexpr int kChunkBytes = 65536;
+constexpr int kResChunkBytes = 32768;
 template <bool BF16>
 __host__ __device__ constexpr int chunk_elems() { return kChunkBytes / ElemTraits<BF16>::SIZE; }
+template <bool BF16>
+__host__ __device__ constexpr int res_chunk_elems() { return kResChunkBytes / ElemTraits<BF16>::SIZE; }
 
 // Workspace records.
 struct __align__(32) Partial {
@@ -51,7 +54,8 @@ struct __align__(16) SeqRes {
 
 struct VerifyDev {
     const void* logits;
-    int B, K, V, nchunk;
+    int B, K, V, nchunk;      // nchunk: streaming chunks per row
+    int nchunk2;              // residual-pass chunks per row
     const int32_t* drafts;
     const float* q;
     const int32_t* k;
@@ -471,22 +475,24 @@ __device__ __noinline__ void merge_row(const VerifyDev& P, int row) {
 
 // ---------------------------------------------------------------- K1
 // Persistent, warp-specialised streaming kernel.  One CTA per SM; the active
-// row-chunks of the call (rows 0..k_eff of every sequence, chunks of 32 KB)
+// row-chunks of the call (rows 0..k_eff of every sequence, chunks of 64 KB)
 // are laid out row-major and split into equal contiguous ranges, one per CTA.
 //   * A producer warp walks the CTA's range and keeps up to kStages chunks in
 //     flight with cp.async.bulk into a shared-memory ring (full / empty
-//     mbarriers, bounded waits).  While a copy is in flight it publishes the
-//     row's metadata, the penalty bitmap of the chunk and the noise of the
-//     chunk's 256-id blocks (one Philox draw per two blocks, by its lanes).
-//   * Sixteen streaming warps each own a 2 KB slice of every chunk.  A lane's
-//     16-byte vector i of a bf16 chunk covers 8 ids of noise block 4 w + i, so
+//     mbarriers, bounded waits).  It draws the noise of a chunk's 256-id
+//     blocks before the chunk's ring slot is free, and writes the row's
+//     metadata, the penalty bitmap and the noise while the copy is in flight.
+//   * Sixteen streaming warps each own a 4 KB slice of every chunk.  A lane's
+//     16-byte vector i of a bf16 chunk covers 8 ids of noise block 8 w + i, so
 //     its packed maximum gives the block test z / T - ln M >= best for its
-//     eight ids at once.  Per slice: packed maxima, the exponentials of the
-//     sum, the block tests; only the vectors that pass compare their elements,
-//     and each lane scores its few survivors (per-id Philox draw, E_v, score)
-//     in step with the warp.  At the first chunk of a row segment each lane
-//     scores its largest element, which starts the segment's best; the warps
-//     of the CTA share the best through shared memory.
+//     eight ids at once; a single test of the lane's maximum against the
+//     smallest ln M of the slice gates them.  Per slice: packed maxima, the
+//     exponentials of the sum, the block tests; only the vectors that pass
+//     compare their elements, and each lane scores its few survivors
+//     (per-id Philox draw, E_v, score) in step with the warp.  At the first
+//     chunk of a row segment each lane scores its largest element, which
+//     starts the segment's best; the warps of the CTA share the best through
+//     shared memory.
 //   * A merge warp runs the row merges: the CTA that completes a row (atomic
 //     ticket over the row's chunks) queues it, and the merge warp combines the
 //     row's partials, takes the accept test and, for the last row of a
@@ -497,16 +503,17 @@ constexpr int kCWarps = 16;                    // streaming warps
 constexpr int kPWarp = kCWarps;                // producer warp index
 constexpr int kMWarp = kCWarps + 1;            // merge warp index
 constexpr int kPThreads = (kCWarps + 2) * 32;  // 576
-constexpr int kStages = 5;
-constexpr int kVL = 4;                         // 16-byte vectors per lane per chunk
-constexpr int kMaxBlk = kChunkBytes / 2 >> kNoiseBlockShift;  // noise blocks per chunk (bf16: 64)
+constexpr int kStages = 3;
+constexpr int kVL = 8;                         // 16-byte vectors per lane per chunk
+constexpr int kMaxBlk = kChunkBytes / 2 >> kNoiseBlockShift;  // noise blocks per chunk (bf16: 128)
 constexpr int kMQ = 16;                        // merge-queue entries per streaming warp
 static_assert(kChunkBytes == kCWarps * 32 * kVL * 16, "stage layout");
 static_assert((32 * 8) == (1 << kNoiseBlockShift), "a bf16 vector row of a warp is one noise block");
 
 template <bool PENALTY>
 __host__ __device__ constexpr size_t k1_dyn_smem() {
-    return static_cast<size_t>(kStages) * kChunkBytes + (PENALTY ? static_cast<size_t>(kStages) * 2048 : 0);
+    return static_cast<size_t>(kStages) * kChunkBytes +
+           (PENALTY ? static_cast<size_t>(kStages) * (kChunkBytes / 2 / 8) : 0);
 }
 
 struct StageMeta {
@@ -514,6 +521,7 @@ struct StageMeta {
     int cand;                    // the row's Gumbel candidates can be the emitted token
     unsigned penw;               // bit w: warp w's slice holds a penalised id
     int pad;
+    float wmin[kCWarps];         // smallest ln M of each warp's slice
     BlockNoise bn[kMaxBlk];      // noise of the chunk's 256-id blocks
 };
 
@@ -529,6 +537,7 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
     constexpr int SB = kChunkBytes;
     constexpr int SL = 32 * kVL * EPV;  // ids per streaming slice
     constexpr int NB = CHUNK >> kNoiseBlockShift;
+    constexpr int BPW = NB / kCWarps;   // noise blocks per slice
     extern __shared__ __align__(128) uint8_t s_dyn[];
     uint8_t* s_stage = s_dyn;
     uint32_t* s_bm = reinterpret_cast<uint32_t*>(s_dyn + kStages * SB);
@@ -605,46 +614,73 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
 
     if (warp == kPWarp) {
         // ================= producer =================
+        // The data of the next sequence (k, EMA, drafts, the tail of its history
+        // for the penalty window) is fetched into registers one sequence ahead,
+        // and its history length two ahead, so no global round trip stalls the
+        // copies at a sequence change.
+        constexpr int kHW = PENALTY ? SPECNG_MAX_REP_WINDOW / 32 : 1;
+        struct SeqData {
+            int k, draft, L;
+            float ema;
+            int hw[kHW];
+        };
+        auto clampL = [&](int L) {
+            return L < 0 ? 0 : (static_cast<int64_t>(L) > P.hist_stride ? static_cast<int>(P.hist_stride) : L);
+        };
+        auto fetch = [&](int bq, int L, SeqData& d) {  // issues the loads; nothing waits here
+            d.k = bq < P.B ? P.k[bq] : 0;
+            d.ema = (P.gate && bq < P.B) ? P.ema[bq] : 1.0f;
+            d.draft = (bq < P.B && lane < P.K) ? P.drafts[bq * P.K + lane] : -1;
+            d.L = L;
+            if constexpr (PENALTY) {
+                const int nh = L < P.W ? L : P.W;
+#pragma unroll
+                for (int i = 0; i < kHW; ++i) {
+                    const int t = lane + 32 * i;
+                    d.hw[i] = (bq < P.B && t < nh) ? P.hist[static_cast<size_t>(bq) * P.hist_stride + (L - nh) + t] : 0;
+                }
+            }
+        };
         int b = s_start[0], j = s_start[1], c = s_start[2];
-        int kb = 0;
-        int keff = 0;
-        int nh = 0;
-        auto load_seq = [&](int bq) {
-            keff = gate_keff(P, bq, &kb, true);
+        int kb = 0, keff = 0, nh = 0;
+        auto install = [&](const SeqData& d) {
+            kb = d.k;
+            if (kb < 0 || kb > P.K) {
+                if (lane == 0) raise_status(P.status, SPECNG_DEV_BAD_K);
+                kb = kb < 0 ? 0 : P.K;
+            }
+            keff = (P.gate && kb > 0 && !(d.ema >= P.thresh)) ? 0 : kb;
             if (lane < keff) {
-                const int d = P.drafts[bq * P.K + lane];
-                s_pdrafts[lane] = d;
-                if (!(d >= 0 && d < P.V)) raise_status(P.status, SPECNG_DEV_TOKEN_OOR);
+                s_pdrafts[lane] = d.draft;
+                if (!(d.draft >= 0 && d.draft < P.V)) raise_status(P.status, SPECNG_DEV_TOKEN_OOR);
             }
             if constexpr (PENALTY) {
-                int L = P.lens[bq];
-                L = L < 0 ? 0 : (static_cast<int64_t>(L) > P.hist_stride ? static_cast<int>(P.hist_stride) : L);
-                nh = L < P.W ? L : P.W;
-                for (int t = lane; t < nh; t += 32) s_hwin[t] = P.hist[static_cast<size_t>(bq) * P.hist_stride + (L - nh) + t];
+                nh = d.L < P.W ? d.L : P.W;
+#pragma unroll
+                for (int i = 0; i < kHW; ++i)
+                    if (lane + 32 * i < nh) s_hwin[lane + 32 * i] = d.hw[i];
             }
             __syncwarp();
         };
-        load_seq(b);
+        SeqData cur, nxt;
+        int Lnext2 = 0;
+        {
+            const int L0 = PENALTY ? clampL(P.lens[b]) : 0;
+            const int L1 = (PENALTY && b + 1 < P.B) ? clampL(P.lens[b + 1]) : 0;
+            fetch(b, L0, cur);
+            install(cur);
+            fetch(b + 1, L1, nxt);
+            if (PENALTY && b + 2 < P.B) Lnext2 = P.lens[b + 2];
+        }
         NoiseKey nk = P.nk;
         bool ok = true;
+        int st = 0;
+        unsigned eph = 0u;  // parity of the empty barrier phase to wait for
         for (int n = 0; n < nwork && ok; ++n) {
-            const int st = n % kStages;
-            const int use = n / kStages;
-            if (use >= 1) ok = mbar_wait_bounded(&s_empty[st], static_cast<unsigned>((use - 1) & 1));
-            if (!ok) { if (lane == 0) raise_status(P.status, SPECNG_DEV_TIMEOUT); break; }
             const int v0 = c * CHUNK;
             const int v1 = min(P.V, v0 + CHUNK);
             const char* src = static_cast<const char*>(P.logits) +
                               ((static_cast<size_t>(b) * K1 + j) * P.V + v0) * ElemTraits<BF16>::SIZE;
-            // the copy goes first; the metadata is written while it is in flight, and the
-            // phase completes once both the bytes and the arrive below are in
-            if (P.aligned && lane == 0) {
-                // the empty barrier already orders the consumers' reads of this stage
-                // before the copy that overwrites it
-                mbar_add_tx(&s_full[st], static_cast<unsigned>(v1 - v0) * ElemTraits<BF16>::SIZE);
-                bulk_g2s(s_stage + st * SB, src, static_cast<unsigned>(v1 - v0) * ElemTraits<BF16>::SIZE, &s_full[st]);
-            }
-            StageMeta& mt = s_meta[st];
             // with dense q, row j < k_eff is sampled by the residual pass unless
             // its draft is invalid (the residual is then p itself)
             int excl = -1, cand = 1;
@@ -654,17 +690,43 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                 if (!dense && valid) excl = d;
                 if (dense && valid) cand = 0;
             }
+            // the noise of the chunk's blocks (lane q: blocks q, q + 32, ...), before the
+            // ring slot is free
+            constexpr int NBL = (NB + 31) / 32;
+            BlockNoise bnl[NBL];
+            if (!GREEDY && cand) {
+                nk.seq = static_cast<uint32_t>(b);
+                const uint32_t blk0 = static_cast<uint32_t>(v0 >> kNoiseBlockShift);
+#pragma unroll
+                for (int r = 0; r < NBL; ++r)
+                    if (lane + 32 * r < NB) bnl[r] = block_noise(nk, blk0 + lane + 32 * r, static_cast<uint32_t>(j));
+            }
+            if (n >= kStages) ok = mbar_wait_bounded(&s_empty[st], eph);
+            if (!ok) { if (lane == 0) raise_status(P.status, SPECNG_DEV_TIMEOUT); break; }
+            // the copy goes first; the metadata is written while it is in flight, and the
+            // phase completes once both the bytes and the arrive below are in
+            if (P.aligned && lane == 0) {
+                // the empty barrier already orders the consumers' reads of this stage
+                // before the copy that overwrites it
+                mbar_add_tx(&s_full[st], static_cast<unsigned>(v1 - v0) * ElemTraits<BF16>::SIZE);
+                bulk_g2s(s_stage + st * SB, src, static_cast<unsigned>(v1 - v0) * ElemTraits<BF16>::SIZE, &s_full[st]);
+            }
+            StageMeta& mt = s_meta[st];
             if (lane == 0) {
                 mt.b = b; mt.j = j; mt.c = c; mt.excl = excl;
                 mt.seg_end = (c == P.nchunk - 1 || n == nwork - 1) ? 1 : 0;
                 mt.cand = cand;
             }
             if (!GREEDY && cand) {
-                // noise of the chunk's blocks: one Philox draw serves two blocks
-                // (words 0, 1 the even block, words 2, 3 the odd one)
-                nk.seq = static_cast<uint32_t>(b);
-                for (int q = lane; q < NB; q += 32) {
-                    mt.bn[q] = block_noise(nk, static_cast<uint32_t>((v0 >> kNoiseBlockShift) + q), static_cast<uint32_t>(j));
+#pragma unroll
+                for (int r = 0; r < NBL; ++r)
+                    if (lane + 32 * r < NB) mt.bn[lane + 32 * r] = bnl[r];
+                __syncwarp();
+                if (lane < kCWarps) {
+                    float mn = INFINITY;
+#pragma unroll
+                    for (int q = 0; q < BPW; ++q) mn = fminf(mn, mt.bn[lane * BPW + q].lnM);
+                    mt.wmin[lane] = mn;
                 }
             }
             if constexpr (PENALTY) {
@@ -696,13 +758,22 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&s_full[st]);
+            if (++st == kStages) {
+                st = 0;
+                if (n >= kStages) eph ^= 1u;  // the waits of ring cycle u (>= 1) are for phase u - 1
+            }
             // advance to the next row-chunk
             if (++c == P.nchunk) {
                 c = 0;
                 if (++j > keff) {
                     j = 0;
                     ++b;
-                    if (n + 1 < nwork) load_seq(b);
+                    if (n + 1 < nwork) {
+                        install(nxt);
+                        const int L2 = PENALTY ? clampL(Lnext2) : 0;
+                        fetch(b + 1, L2, nxt);
+                        if (PENALTY && b + 2 < P.B) Lnext2 = P.lens[b + 2];
+                    }
                 }
             }
         }
@@ -763,9 +834,10 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
     bool cand = false;
     RowPhilox rp{};
     bool fresh = true;
+    int st = 0;
+    unsigned fph = 0u;  // parity of the full barrier phase to wait for
     for (int n = 0; n < nwork; ++n) {
-        const int st = n % kStages;
-        if (!mbar_wait_bounded(&s_full[st], static_cast<unsigned>((n / kStages) & 1))) {
+        if (!mbar_wait_bounded(&s_full[st], fph)) {
             if (lane == 0) raise_status(P.status, SPECNG_DEV_TIMEOUT);
             break;
         }
@@ -789,42 +861,44 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
         const int v1 = min(P.V, v0 + CHUNK);
         const uint4* stage = reinterpret_cast<const uint4*>(s_stage + st * SB);
         const uint32_t* bm = s_bm + (PENALTY ? st * (CHUNK / 32) : 0);
-        const bool full = v0 + off0 + (kVL - 1) * 32 * EPV + EPV <= v1;  // my four vectors are whole
+        const bool full = v0 + off0 + (kVL - 1) * 32 * EPV + EPV <= v1;  // my vectors are whole
         uint4 rv[kVL];
 #pragma unroll
         for (int i = 0; i < kVL; ++i) rv[i] = stage[ubase + i * 32 + lane];
         // penalised elements of my lane (bit 8 i + e), only where the slice holds one
-        unsigned pmk = 0u;
+        uint64_t pmk = 0u;
         if constexpr (PENALTY) {
             if ((mt.penw >> warp) & 1u) {
 #pragma unroll
                 for (int i = 0; i < kVL; ++i) {
                     const int off = off0 + i * 32 * EPV;
-                    pmk |= ((bm[off >> 5] >> (off & 31)) & ((1u << EPV) - 1u)) << (8 * i);
+                    pmk |= static_cast<uint64_t>((bm[off >> 5] >> (off & 31)) & ((1u << EPV) - 1u)) << (8 * i);
                 }
             }
         }
 
-        // ---- streaming: vector maxima, sum of exponentials; zv[i] bounds the transformed
-        //      values of vector i (penalised ones included)
-        float vmx[kVL];  // raw maxima of my vectors (-inf where empty)
-        float zv[kVL];
+        // ---- streaming: lane maximum zl (bounds my transformed values, penalised ones
+        //      included), sum of exponentials
+        float zl = -INFINITY;
         float lraw = -INFINITY;
+        uint32_t hv[kVL];  // packed vector maxima (bf16), or the fp32 maxima
         if (full) {
+            if constexpr (BF16) {
 #pragma unroll
-            for (int i = 0; i < kVL; ++i) {
-                if constexpr (BF16) {
-                    const __nv_bfloat162 h = bf16x8_max2(rv[i]);
-                    vmx[i] = fmaxf(bf16lo(as_u32(h)), bf16hi(as_u32(h)));
-                } else {
-                    vmx[i] = fmaxf(fmaxf(__uint_as_float(rv[i].x), __uint_as_float(rv[i].y)),
-                                   fmaxf(__uint_as_float(rv[i].z), __uint_as_float(rv[i].w)));
+                for (int i = 0; i < kVL; ++i) hv[i] = as_u32(bf16x8_max2(rv[i]));
+                __nv_bfloat162 h = __hmax2(__hmax2(__hmax2(as_bf162(hv[0]), as_bf162(hv[1])), __hmax2(as_bf162(hv[2]), as_bf162(hv[3]))),
+                                           __hmax2(__hmax2(as_bf162(hv[4]), as_bf162(hv[5])), __hmax2(as_bf162(hv[6]), as_bf162(hv[7]))));
+                lraw = fmaxf(bf16lo(as_u32(h)), bf16hi(as_u32(h)));
+            } else {
+#pragma unroll
+                for (int i = 0; i < kVL; ++i) {
+                    const float f = fmaxf(fmaxf(__uint_as_float(rv[i].x), __uint_as_float(rv[i].y)),
+                                          fmaxf(__uint_as_float(rv[i].z), __uint_as_float(rv[i].w)));
+                    hv[i] = __float_as_uint(f);
+                    lraw = fmaxf(lraw, f);
                 }
             }
-            lraw = fmaxf(fmaxf(vmx[0], vmx[1]), fmaxf(vmx[2], vmx[3]));
-            const float zl = SOFTCAP ? transform_f32<true, false>(lraw, false, P) : lraw;
-#pragma unroll
-            for (int i = 0; i < kVL; ++i) zv[i] = SOFTCAP ? transform_f32<true, false>(vmx[i], false, P) : vmx[i];
+            zl = SOFTCAP ? transform_f32<true, false>(lraw, false, P) : lraw;
             if constexpr (GREEDY) {
                 if (zl > m) m = zl;
             } else {
@@ -833,7 +907,8 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                     m = zl;
                     msc = m * P.sc;
                 }
-                float2 acc2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+                float2 acc2[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                                  make_float2(0.0f, 0.0f)};
                 const float2 sc2 = make_float2(P.sc, P.sc), nm2 = make_float2(-msc, -msc);
 #pragma unroll
                 for (int i = 0; i < kVL; ++i) {
@@ -844,24 +919,22 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                         const float2 t = __ffma2_rn(make_float2(transform_f32<SOFTCAP, false>(x[e], false, P),
                                                                 transform_f32<SOFTCAP, false>(x[e + 1], false, P)),
                                                     sc2, nm2);
-                        acc2[i & 1] = __fadd2_rn(acc2[i & 1], make_float2(ex2_approx(t.x), ex2_approx(t.y)));
+                        acc2[i & 3] = __fadd2_rn(acc2[i & 3], make_float2(ex2_approx(t.x), ex2_approx(t.y)));
                     }
                 }
-                s += (acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y);
+                s += ((acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y)) + ((acc2[2].x + acc2[2].y) + (acc2[3].x + acc2[3].y));
             }
             if constexpr (PENALTY) {
                 // the few penalised elements: replace their terms by the penalised ones (and
                 // raise the maximum if a penalty below 1 lifted one above it)
-                unsigned pw = pmk;
+                uint64_t pw = pmk;
                 while (pw != 0u) {
-                    const int bit = __ffs(pw) - 1;
+                    const int bit = __ffsll(static_cast<long long>(pw)) - 1;
                     pw &= pw - 1u;
                     const float xe = elem_of_stage<BF16>(stage, off0 + (bit >> 3) * 32 * EPV + (bit & 7));
                     const float zu = transform_f32<SOFTCAP, false>(xe, false, P);
                     const float zp = transform_f32<SOFTCAP, true>(xe, true, P);
-#pragma unroll
-                    for (int i = 0; i < kVL; ++i)
-                        if ((bit >> 3) == i) zv[i] = fmaxf(zv[i], zp);
+                    zl = fmaxf(zl, zp);
                     if constexpr (GREEDY) {
                         m = fmaxf(m, zp);
                     } else {
@@ -878,8 +951,7 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
             // partial vectors (a row's last chunk): exact transform element by element
 #pragma unroll
             for (int i = 0; i < kVL; ++i) {
-                vmx[i] = -INFINITY;
-                zv[i] = -INFINITY;
+                hv[i] = BF16 ? 0xFF80FF80u : __float_as_uint(-INFINITY);
                 const int off = off0 + i * 32 * EPV;
                 const int nv = min(EPV, v1 - (v0 + off));
                 if (nv <= 0) continue;
@@ -889,8 +961,8 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                 for (int e = 0; e < EPV; ++e) {
                     if (e >= nv) break;
                     const float z = transform_f32<SOFTCAP, PENALTY>(x[e], (pmk >> (8 * i + e)) & 1u, P);
-                    vmx[i] = fmaxf(vmx[i], x[e]);
-                    zv[i] = fmaxf(zv[i], z);
+                    lraw = fmaxf(lraw, x[e]);
+                    zl = fmaxf(zl, z);
                     if constexpr (GREEDY) {
                         m = fmaxf(m, z);
                     } else {
@@ -902,7 +974,6 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                         s += ex2_approx(fmaf(z, P.sc, -msc));
                     }
                 }
-                lraw = fmaxf(lraw, vmx[i]);
             }
         }
 
@@ -911,7 +982,6 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
             // top two transformed values (lower id on ties) within cand_delta of the best
             // value any warp of the CTA has reached in this segment.  Without a penalty the
             // lane maximum is itself a value of the row (the transform is monotone)
-            const float zl = fmaxf(fmaxf(zv[0], zv[1]), fmaxf(zv[2], zv[3]));
             float gth = fmaxf(tt.s1, key_score(*reinterpret_cast<volatile unsigned*>(rth)));
             if constexpr (!PENALTY) gth = fmaxf(gth, key_score(warp_best_key(zl)));
             gth = gth > -INFINITY ? gth - cand_delta(gth) : -INFINITY;
@@ -920,7 +990,7 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                 for (int i = 0; i < kVL; ++i) {
                     const int off = off0 + i * 32 * EPV;
                     const int nv = min(EPV, v1 - (v0 + off));
-                    if (nv <= 0 || !(zv[i] >= gth)) continue;
+                    if (nv <= 0) continue;
                     float x[EPV];
                     unpack<BF16>(rv[i], x);
 #pragma unroll
@@ -937,15 +1007,11 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
             const unsigned kw = warp_best_key(tt.s1);
             if (lane == 0 && kw != 0u) atomicMax(rth, kw);
         } else if (cand) {
-            // noise blocks of my four vectors
-            BlockNoise bn[kVL];
-#pragma unroll
-            for (int i = 0; i < kVL; ++i) bn[i] = mt.bn[(off0 + i * 32 * EPV) >> kNoiseBlockShift];
             int seeded = -1;
             if (seg_start) {
                 // seed: every lane scores its largest raw element (any exact score bounds the
                 // best from below); the CTA's warps share the best seed
-                int am = -1, ai = 0;
+                int am = -1;
 #pragma unroll
                 for (int i = kVL - 1; i >= 0; --i) {
                     const int off = off0 + i * 32 * EPV;
@@ -954,19 +1020,15 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                     unpack<BF16>(rv[i], x);
 #pragma unroll
                     for (int e = EPV - 1; e >= 0; --e)
-                        if (e < nv && x[e] == lraw) { am = off + e; ai = i; }
+                        if (e < nv && x[e] == lraw) am = off + e;
                 }
                 float t0 = -INFINITY;
                 if (am >= 0 && v0 + am != excl) {
                     const float z = transform_f32<SOFTCAP, PENALTY>(elem_of_stage<BF16>(stage, am),
                                                                     PENALTY && ((bm[am >> 5] >> (am & 31)) & 1u), P);
                     const uint32_t v = static_cast<uint32_t>(v0 + am);
-                    float M = bn[0].M;
-                    int I = bn[0].I;
-#pragma unroll
-                    for (int i = 1; i < kVL; ++i)
-                        if (ai == i) { M = bn[i].M; I = bn[i].I; }
-                    t0 = z * P.invT - ln_fast(noise_exp_f32(rp, M, I, v));
+                    const BlockNoise bk = mt.bn[am >> kNoiseBlockShift];
+                    t0 = z * P.invT - ln_fast(noise_exp_f32(rp, bk.M, bk.I, v));
                     top2_push(tt, t0, static_cast<int>(v));
                     seeded = static_cast<int>(v);
                 }
@@ -982,73 +1044,75 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                 const float best = key_score(*reinterpret_cast<volatile unsigned*>(rth));
                 if (best > -INFINITY) thr = fmaxf(thr, best - cand_delta(best));
             }
-            // block tests: every score of vector i is at most z / T - ln M_i
-            unsigned pv = 0u;
-#pragma unroll
-            for (int i = 0; i < kVL; ++i) {
-                const float zb = zv[i] * P.invT;
-                if (zb - bn[i].lnM + bound_slack(zb) >= thr) pv |= 1u << i;
-            }
-            if (__any_sync(0xffffffffu, pv != 0u)) {
+            // gate: no score of my lane exceeds zl / T - (smallest ln M of the slice)
+            const float zlb = zl * P.invT;
+            const bool lpass = zlb - mt.wmin[warp] + bound_slack(zlb) >= thr;
+            if (__any_sync(0xffffffffu, lpass)) {
+                // block tests: every score of vector i is at most z / T - ln M_i; then the
                 // elements of the passing vectors that can reach the best
-                unsigned msk = 0u;
+                uint64_t msk = 0u;
+                if (lpass) {
 #pragma unroll
-                for (int i = 0; i < kVL; ++i) {
-                    if (!((pv >> i) & 1u)) continue;
-                    const int off = off0 + i * 32 * EPV;
-                    if (full) {
-                        // z >= T (thr + ln M), in raw units
-                        const float zt = (thr + bn[i].lnM) * P.T;
-                        float xt = zt;
-                        if constexpr (SOFTCAP) {
-                            // shrink by more than the fp32 error of c tanh(x / c) before
-                            // inverting: atanh is steep near |u| = 1
-                            float u = zt * P.invcap;
-                            u -= 1e-6f * fabsf(u) + 1e-7f;
-                            xt = u > 1.0f ? INFINITY : (u <= -1.0f ? -INFINITY : P.cap * atanhf(fminf(u, 1.0f - 1e-7f)));
-                        }
-                        xt -= 1e-5f * (1.0f + fabsf(xt));  // slack for the rounding of the transform
+                    for (int i = 0; i < kVL; ++i) {
+                        const int off = off0 + i * 32 * EPV;
+                        const float lnM = mt.bn[off >> kNoiseBlockShift].lnM;
+                        float zv;
+                        if constexpr (BF16) zv = fmaxf(bf16lo(hv[i]), bf16hi(hv[i]));
+                        else zv = __uint_as_float(hv[i]);
+                        if (SOFTCAP && full) zv = transform_f32<true, false>(zv, false, P);
+                        const unsigned pb = static_cast<unsigned>(pmk >> (8 * i)) & 0xFFu;
+                        const float zvb = zv * P.invT;
+                        if (!(pb != 0u || !full || zvb - lnM + bound_slack(zvb) >= thr)) continue;
                         unsigned mi;
-                        if constexpr (BF16) {
-                            mi = bf16x8_ge_bits(rv[i], bf16x2_floor(xt));
+                        if (full) {
+                            // z >= T (thr + ln M), in raw units
+                            const float zt = (thr + lnM) * P.T;
+                            float xt = zt;
+                            if constexpr (SOFTCAP) {
+                                // shrink by more than the fp32 error of c tanh(x / c) before
+                                // inverting: atanh is steep near |u| = 1
+                                float u = zt * P.invcap;
+                                u -= 1e-6f * fabsf(u) + 1e-7f;
+                                xt = u > 1.0f ? INFINITY : (u <= -1.0f ? -INFINITY : P.cap * atanhf(fminf(u, 1.0f - 1e-7f)));
+                            }
+                            xt -= 1e-5f * (1.0f + fabsf(xt));  // slack for the rounding of the transform
+                            if constexpr (BF16) {
+                                mi = bf16x8_ge_bits(rv[i], bf16x2_floor(xt));
+                            } else {
+                                mi = static_cast<unsigned>(__uint_as_float(rv[i].x) >= xt);
+                                mi |= static_cast<unsigned>(__uint_as_float(rv[i].y) >= xt) << 1;
+                                mi |= static_cast<unsigned>(__uint_as_float(rv[i].z) >= xt) << 2;
+                                mi |= static_cast<unsigned>(__uint_as_float(rv[i].w) >= xt) << 3;
+                            }
+                            mi |= pb;  // penalised: decided exactly below
                         } else {
-                            mi = static_cast<unsigned>(__uint_as_float(rv[i].x) >= xt);
-                            mi |= static_cast<unsigned>(__uint_as_float(rv[i].y) >= xt) << 1;
-                            mi |= static_cast<unsigned>(__uint_as_float(rv[i].z) >= xt) << 2;
-                            mi |= static_cast<unsigned>(__uint_as_float(rv[i].w) >= xt) << 3;
+                            const int nv = min(EPV, v1 - (v0 + off));
+                            mi = nv > 0 ? (1u << nv) - 1u : 0u;
                         }
-                        msk |= (mi | ((pmk >> (8 * i)) & 0xFFu)) << (8 * i);  // penalised: decided exactly below
-                    } else {
-                        const int nv = min(EPV, v1 - (v0 + off));
-                        if (nv > 0) msk |= ((1u << nv) - 1u) << (8 * i);
+                        msk |= static_cast<uint64_t>(mi) << (8 * i);
                     }
-                }
-                if (seeded >= 0) {
-                    const int so = seeded - v0 - off0;
-                    const int si = so / (32 * EPV), se = so - si * 32 * EPV;
-                    if (se >= 0 && se < EPV) msk &= ~(1u << (8 * si + se));
+                    if (seeded >= 0) {
+                        const int so = seeded - v0 - off0;
+                        const int si = so / (32 * EPV), se = so - si * 32 * EPV;
+                        if (se >= 0 && se < EPV) msk &= ~(static_cast<uint64_t>(1) << (8 * si + se));
+                    }
                 }
                 // score the lane's candidates one per iteration, the warp in step
                 while (__any_sync(0xffffffffu, msk != 0u)) {
-                    int v = -1, bi = 0;
+                    int v = -1, loc = 0;
                     float zb = -INFINITY;
                     if (msk != 0u) {
-                        const int bit = __ffs(msk) - 1;
+                        const int bit = __ffsll(static_cast<long long>(msk)) - 1;
                         msk &= msk - 1u;
-                        bi = bit >> 3;
-                        const int loc = off0 + bi * 32 * EPV + (bit & 7);
+                        loc = off0 + (bit >> 3) * 32 * EPV + (bit & 7);
                         const bool pen = PENALTY && ((pmk >> bit) & 1u);
                         zb = transform_f32<SOFTCAP, PENALTY>(elem_of_stage<BF16>(stage, loc), pen, P) * P.invT;
                         v = v0 + loc;
                     }
-                    float M = bn[0].M, lnM = bn[0].lnM;
-                    int I = bn[0].I;
-#pragma unroll
-                    for (int i = 1; i < kVL; ++i)
-                        if (bi == i) { M = bn[i].M; lnM = bn[i].lnM; I = bn[i].I; }
-                    const bool live = v >= 0 && v != excl && zb - lnM + bound_slack(zb) >= thr;
+                    const BlockNoise bk = mt.bn[loc >> kNoiseBlockShift];
+                    const bool live = v >= 0 && v != excl && zb - bk.lnM + bound_slack(zb) >= thr;
                     if (__any_sync(0xffffffffu, live)) {
-                        const float E = noise_exp_f32(rp, M, I, static_cast<uint32_t>(v < 0 ? 0 : v));
+                        const float E = noise_exp_f32(rp, bk.M, bk.I, static_cast<uint32_t>(v < 0 ? 0 : v));
                         if (live) {
                             const float score = zb - ln_fast(E);
                             if (score >= thr) {
@@ -1137,6 +1201,10 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_empty[st]);
+        if (++st == kStages) {
+            st = 0;
+            fph ^= 1u;
+        }
     }
     __syncwarp();
     if (lane == 0) {
@@ -1158,7 +1226,7 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kNV = 8;  // 16-byte vectors per thread per chunk
-static_assert(kChunkBytes == kThreads * kNV * 16, "residual chunk layout");
+static_assert(kResChunkBytes == kThreads * kNV * 16, "residual chunk layout");
 
 // log max(0, p - q) for log p = lp, in fp32 without cancellation: for q > 0,
 // p - q = q (e^(lp - ln q) - 1), and expm1 keeps the relative accuracy when
@@ -1198,7 +1266,7 @@ __device__ __forceinline__ void build_window(const VerifyDev& P, int b, int j, i
 template <bool BF16, bool SOFTCAP, bool PENALTY>
 __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const VerifyDev P) {
     constexpr int EPV = ElemTraits<BF16>::EPV;
-    constexpr int CHUNK = chunk_elems<BF16>();
+    constexpr int CHUNK = res_chunk_elems<BF16>();
     constexpr int NB = CHUNK >> kNoiseBlockShift;
     __shared__ uint32_t s_bm[PENALTY ? CHUNK / 32 : 1];
     __shared__ int s_win[PENALTY ? SPECNG_MAX_REP_WINDOW : 1];
@@ -1211,8 +1279,8 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const Veri
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int K1 = P.K + 1;
-    const int b = blockIdx.x / P.nchunk;
-    const int c = blockIdx.x - b * P.nchunk;
+    const int b = blockIdx.x / P.nchunk2;
+    const int c = blockIdx.x - b * P.nchunk2;
     const int need = __ldcg(&P.seqres[b].need_residual);
     if (!need) return;
     const int a = __ldcg(&P.seqres[b].a);
@@ -1369,7 +1437,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const Veri
             st_partial(P.part2 + blockIdx.x, 0.0f, 0.0f, t);
             __threadfence();
             const unsigned prev = atomicAdd(&P.seq_ticket2[b], 1u);
-            s_last = prev == static_cast<unsigned>(P.nchunk - 1);
+            s_last = prev == static_cast<unsigned>(P.nchunk2 - 1);
         }
     }
     __syncthreads();
@@ -1379,12 +1447,12 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const Veri
         P.seq_ticket2[b] = 0u;
         P.row_thr[row] = 0u;  // leave the workspace zeroed
     }
-    const Partial* pr = P.part2 + static_cast<size_t>(b) * P.nchunk;
+    const Partial* pr = P.part2 + static_cast<size_t>(b) * P.nchunk2;
     Top2 t = top2_empty();
-    for (int cc = lane; cc < P.nchunk; cc += 32) t = top2_merge(t, ldcg_partial(pr + cc).t);
+    for (int cc = lane; cc < P.nchunk2; cc += 32) t = top2_merge(t, ldcg_partial(pr + cc).t);
     t = top2_warp_reduce(t);
     __syncwarp();
-    for (int cc = lane; cc < P.nchunk; cc += 32) st_zero(const_cast<Partial*>(pr) + cc);
+    for (int cc = lane; cc < P.nchunk2; cc += 32) st_zero(const_cast<Partial*>(pr) + cc);
     const int nw = PENALTY ? s_nwin : 0;
     const bool pen1 = PENALTY && t.i1 >= 0 ? warp_in_window(t.i1, s_win, nw) : false;
     const bool pen2 = PENALTY && t.i2 >= 0 ? warp_in_window(t.i2, s_win, nw) : false;
@@ -1440,7 +1508,7 @@ cudaError_t launch_stream(const VerifyDev& P, cudaStream_t s) {
 
 template <bool BF16, bool C, bool R>
 cudaError_t launch_residual(const VerifyDev& P, cudaStream_t s) {
-    const unsigned grid = static_cast<unsigned>(P.B) * static_cast<unsigned>(P.nchunk);
+    const unsigned grid = static_cast<unsigned>(P.B) * static_cast<unsigned>(P.nchunk2);
     verify_residual_kernel<BF16, C, R><<<grid, kThreads, 0, s>>>(P);
     return cudaGetLastError();
 }
