@@ -474,424 +474,160 @@ __device__ __noinline__ void merge_row(const VerifyDev& P, int row) {
 }
 
 // ---------------------------------------------------------------- K1
-// Persistent, warp-specialised streaming kernel.  One CTA per SM; the active
-// row-chunks of the call (rows 0..k_eff of every sequence, chunks of 64 KB)
-// are laid out row-major and split into equal contiguous ranges, one per CTA.
-//   * A producer warp walks the CTA's range and keeps up to kStages chunks in
-//     flight with cp.async.bulk into a shared-memory ring (full / empty
-//     mbarriers, bounded waits).  It draws the noise of a chunk's 256-id
-//     blocks before the chunk's ring slot is free, and writes the row's
-//     metadata, the penalty bitmap and the noise while the copy is in flight.
-//   * Sixteen streaming warps each own a 4 KB slice of every chunk.  A lane's
-//     16-byte vector i of a bf16 chunk covers 8 ids of noise block 8 w + i, so
-//     its packed maximum gives the block test z / T - ln M >= best for its
-//     eight ids at once; a single test of the lane's maximum against the
-//     smallest ln M of the slice gates them.  Per slice: packed maxima, the
-//     exponentials of the sum, the block tests; only the vectors that pass
-//     compare their elements, and each lane scores its few survivors
-//     (per-id Philox draw, E_v, score) in step with the warp.  At the first
-//     chunk of a row segment each lane scores its largest element, which
-//     starts the segment's best; the warps of the CTA share the best through
-//     shared memory.
-//   * A merge warp runs the row merges: the CTA that completes a row (atomic
-//     ticket over the row's chunks) queues it, and the merge warp combines the
-//     row's partials, takes the accept test and, for the last row of a
-//     sequence (second ticket), runs the epilogue.  Nothing waits on another
-//     CTA.
+// One warp per piece of a row.  The active rows of the call (rows 0..k_eff of
+// every sequence) are cut into pieces of 16 KB; each warp streams its piece
+// once with 16-byte loads (the next iteration's loads in flight while the
+// current one is computed) and leaves one partial (maximum, sum of
+// exponentials, top-two sampling candidates).  The warp that finishes a row's
+// last piece (atomic ticket) merges the row at once; the last row of a
+// sequence (second ticket) runs the epilogue.  Warps never wait on each other.
+//   * Noise: a bf16 piece holds 32 blocks of 256 ids, one per lane; each lane
+//     draws its block's minimum (one Philox call).  A lane's vector i of
+//     iteration it covers 8 ids of block 4 it + i, so its packed maximum gives
+//     the block test z / T - ln M >= best for its eight ids at once; only the
+//     vectors that pass compare their elements, and each lane scores its few
+//     survivors (per-id Philox draw, E_v, score) in step with the warp.
+//   * The best score of a row is shared by the row's warps through a global
+//     atomic maximum (read one iteration ahead, so its latency is hidden); at
+//     its first iteration a warp scores its largest element to start it.
+//   * The sum of exponentials is kept against a reference maximum fixed at the
+//     piece's first iteration, raised only when a value passes it by more than
+//     2^32 in the sum's units, so the exponentials never wait for a maximum.
 
-constexpr int kCWarps = 16;                    // streaming warps
-constexpr int kPWarp = kCWarps;                // producer warp index
-constexpr int kMWarp = kCWarps + 1;            // merge warp index
-constexpr int kPThreads = (kCWarps + 2) * 32;  // 576
-constexpr int kStages = 3;
-constexpr int kVL = 8;                         // 16-byte vectors per lane per chunk
-constexpr int kMaxBlk = kChunkBytes / 2 >> kNoiseBlockShift;  // noise blocks per chunk (bf16: 128)
-constexpr int kMQ = 16;                        // merge-queue entries per streaming warp
-static_assert(kChunkBytes == kCWarps * 32 * kVL * 16, "stage layout");
-static_assert((32 * 8) == (1 << kNoiseBlockShift), "a bf16 vector row of a warp is one noise block");
+constexpr int kPieceBytes = 16384;
+constexpr int kPW = 8;           // warps per CTA
+constexpr int kPT = kPW * 32;    // threads per CTA
+constexpr int kIV = 4;           // 16-byte vectors per lane per iteration
 
-template <bool PENALTY>
-__host__ __device__ constexpr size_t k1_dyn_smem() {
-    return static_cast<size_t>(kStages) * kChunkBytes +
-           (PENALTY ? static_cast<size_t>(kStages) * (kChunkBytes / 2 / 8) : 0);
-}
-
-struct StageMeta {
-    int b, j, c, excl, seg_end;  // seg_end: the last chunk of this row in the CTA's range
-    int cand;                    // the row's Gumbel candidates can be the emitted token
-    unsigned penw;               // bit w: warp w's slice holds a penalised id
-    int pad;
-    float wmin[kCWarps];         // smallest ln M of each warp's slice
-    BlockNoise bn[kMaxBlk];      // noise of the chunk's 256-id blocks
-};
-
-struct WarpPart {
-    float m, s;
-    Top2 t;
-};
+template <bool BF16>
+__host__ __device__ constexpr int piece_elems() { return kPieceBytes / ElemTraits<BF16>::SIZE; }
 
 template <bool BF16, bool GREEDY, bool SOFTCAP, bool PENALTY>
-__global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const VerifyDev P) {
+__global__ void __launch_bounds__(kPT, 2) verify_piece_kernel(const VerifyDev P) {
     constexpr int EPV = ElemTraits<BF16>::EPV;
-    constexpr int CHUNK = chunk_elems<BF16>();
-    constexpr int SB = kChunkBytes;
-    constexpr int SL = 32 * kVL * EPV;  // ids per streaming slice
-    constexpr int NB = CHUNK >> kNoiseBlockShift;
-    constexpr int BPW = NB / kCWarps;   // noise blocks per slice
-    extern __shared__ __align__(128) uint8_t s_dyn[];
-    uint8_t* s_stage = s_dyn;
-    uint32_t* s_bm = reinterpret_cast<uint32_t*>(s_dyn + kStages * SB);
-    __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages];
-    __shared__ StageMeta s_meta[kStages];
-    __shared__ WarpPart s_slot[kStages][kCWarps];
-    __shared__ int s_cnt[kStages];
-    __shared__ unsigned s_rthr[kStages + 1];  // per-segment best score (score_key; 0 = none)
-    __shared__ long long s_wsum[kPThreads / 32];
-    __shared__ int s_start[3];
-    __shared__ int s_hwin[PENALTY ? SPECNG_MAX_REP_WINDOW : 1];
-    __shared__ int s_pdrafts[SPECNG_MAX_K + 1];
-    __shared__ volatile int s_mq[kCWarps][kMQ];  // rows to merge, per streaming warp (single producer / consumer)
-    __shared__ volatile int s_mq_tail[kCWarps];
-    __shared__ volatile int s_mq_head[kCWarps];
-    __shared__ int s_done;
+    constexpr int PIECE = piece_elems<BF16>();
+    constexpr int ITV = 32 * kIV;                // vectors per warp per iteration
+    constexpr int NIT = PIECE / (ITV * EPV);     // iterations per piece (8)
+    constexpr int NBP = PIECE >> kNoiseBlockShift;  // noise blocks per piece (bf16 32, fp32 16)
+    constexpr int VPB = (1 << kNoiseBlockShift) / (32 * EPV);  // vector rows per block (bf16 1, fp32 2)
+    static_assert(NIT * ITV * EPV == PIECE && NBP <= 32, "piece layout");
+    __shared__ uint32_t s_pbm[PENALTY ? kPW * (PIECE / 32) : 1];  // per-warp penalty bitmap of the piece
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int K1 = P.K + 1;
+    const long long item = static_cast<long long>(blockIdx.x) * kPW + warp;
+    const int row = static_cast<int>(item / P.nchunk);
+    const int p = static_cast<int>(item - static_cast<long long>(row) * P.nchunk);
+    if (row >= P.B * K1) return;
+    const int b = row / K1, j = row - b * K1;
+    int kb;
+    const int keff = gate_keff(P, b, &kb, j == 0 && p == 0);
+    if (j > keff) return;
     const bool dense = P.q != nullptr;
+    const int v0 = p * PIECE;
+    const int v1 = min(P.V, v0 + PIECE);
+    const char* rowp = static_cast<const char*>(P.logits) + static_cast<size_t>(row) * P.V * ElemTraits<BF16>::SIZE;
 
-    // ---- prologue: count the active row-chunks and find this CTA's range
-    const int per = (P.B + kPThreads - 1) / kPThreads;
-    const int bb0 = tid * per;
-    long long mine = 0;
-    for (int b = bb0; b < bb0 + per && b < P.B; ++b) mine += static_cast<long long>(gate_keff(P, b, nullptr, false) + 1) * P.nchunk;
-    long long incl = mine;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const long long o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
+    // the draft this row verifies: excluded from the point-mass residual; with dense q
+    // the residual pass samples the row (unless the draft is invalid: the residual is p)
+    int excl = -1;
+    bool cand = !GREEDY;
+    if (!GREEDY && j < keff) {
+        const int d = P.drafts[b * P.K + j];
+        const bool valid = d >= 0 && d < P.V;
+        if (!valid && p == 0 && lane == 0) raise_status(P.status, SPECNG_DEV_TOKEN_OOR);
+        if (!dense && valid) excl = d;
+        if (dense && valid) cand = false;
     }
-    if (lane == 31) s_wsum[warp] = incl;
-    if (tid == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init(&s_full[i], 1);
-            mbar_init(&s_empty[i], kCWarps);
-            s_cnt[i] = 0;
-        }
-        for (int i = 0; i <= kStages; ++i) s_rthr[i] = 0u;
-        s_done = 0;
-        mbar_init_fence();
-    }
-    if (tid < kCWarps) {
-        s_mq_tail[tid] = 0;
-        s_mq_head[tid] = 0;
-    }
-    __syncthreads();
-    long long base = 0, total = 0;
-    for (int w = 0; w < kPThreads / 32; ++w) {
-        if (w < warp) base += s_wsum[w];
-        total += s_wsum[w];
-    }
-    const long long G = gridDim.x;
-    const long long w0 = total * blockIdx.x / G, w1 = total * (blockIdx.x + 1) / G;
-    const long long ex = base + incl - mine;  // first row-chunk index of my sequences
-    if (w0 < w1 && w0 >= ex && w0 < ex + mine) {
-        long long acc = ex;
-        for (int b = bb0; b < bb0 + per && b < P.B; ++b) {
-            const long long nb = static_cast<long long>(gate_keff(P, b, nullptr, false) + 1) * P.nchunk;
-            if (w0 < acc + nb) {
-                const long long r = w0 - acc;
-                s_start[0] = b;
-                s_start[1] = static_cast<int>(r / P.nchunk);
-                s_start[2] = static_cast<int>(r % P.nchunk);
-                break;
-            }
-            acc += nb;
-        }
-    }
-    __syncthreads();
-    const int nwork = static_cast<int>(w1 - w0);
-    if (nwork <= 0) return;
+    NoiseKey nk = P.nk;
+    nk.seq = static_cast<uint32_t>(b);
 
-    if (warp == kPWarp) {
-        // ================= producer =================
-        // The data of the next sequence (k, EMA, drafts, the tail of its history
-        // for the penalty window) is fetched into registers one sequence ahead,
-        // and its history length two ahead, so no global round trip stalls the
-        // copies at a sequence change.
-        constexpr int kHW = PENALTY ? SPECNG_MAX_REP_WINDOW / 32 : 1;
-        struct SeqData {
-            int k, draft, L;
-            float ema;
-            int hw[kHW];
-        };
-        auto clampL = [&](int L) {
-            return L < 0 ? 0 : (static_cast<int64_t>(L) > P.hist_stride ? static_cast<int>(P.hist_stride) : L);
-        };
-        auto fetch = [&](int bq, int L, SeqData& d) {  // issues the loads; nothing waits here
-            d.k = bq < P.B ? P.k[bq] : 0;
-            d.ema = (P.gate && bq < P.B) ? P.ema[bq] : 1.0f;
-            d.draft = (bq < P.B && lane < P.K) ? P.drafts[bq * P.K + lane] : -1;
-            d.L = L;
-            if constexpr (PENALTY) {
-                const int nh = L < P.W ? L : P.W;
+    // the first iteration's loads go out before anything else
+    const int ebase = v0 + lane * EPV;  // id of element 0 of my vector (it, 0)
+    auto load_it = [&](int it, uint4* dst) {
 #pragma unroll
-                for (int i = 0; i < kHW; ++i) {
-                    const int t = lane + 32 * i;
-                    d.hw[i] = (bq < P.B && t < nh) ? P.hist[static_cast<size_t>(bq) * P.hist_stride + (L - nh) + t] : 0;
-                }
-            }
-        };
-        int b = s_start[0], j = s_start[1], c = s_start[2];
-        int kb = 0, keff = 0, nh = 0;
-        auto install = [&](const SeqData& d) {
-            kb = d.k;
-            if (kb < 0 || kb > P.K) {
-                if (lane == 0) raise_status(P.status, SPECNG_DEV_BAD_K);
-                kb = kb < 0 ? 0 : P.K;
-            }
-            keff = (P.gate && kb > 0 && !(d.ema >= P.thresh)) ? 0 : kb;
-            if (lane < keff) {
-                s_pdrafts[lane] = d.draft;
-                if (!(d.draft >= 0 && d.draft < P.V)) raise_status(P.status, SPECNG_DEV_TOKEN_OOR);
-            }
-            if constexpr (PENALTY) {
-                nh = d.L < P.W ? d.L : P.W;
-#pragma unroll
-                for (int i = 0; i < kHW; ++i)
-                    if (lane + 32 * i < nh) s_hwin[lane + 32 * i] = d.hw[i];
-            }
-            __syncwarp();
-        };
-        SeqData cur, nxt;
-        int Lnext2 = 0;
-        {
-            const int L0 = PENALTY ? clampL(P.lens[b]) : 0;
-            const int L1 = (PENALTY && b + 1 < P.B) ? clampL(P.lens[b + 1]) : 0;
-            fetch(b, L0, cur);
-            install(cur);
-            fetch(b + 1, L1, nxt);
-            if (PENALTY && b + 2 < P.B) Lnext2 = P.lens[b + 2];
+        for (int i = 0; i < kIV; ++i) {
+            const int e0 = ebase + (it * kIV + i) * 32 * EPV;
+            dst[i] = e0 < v1 ? load_vec<BF16>(rowp, e0, v1, P.aligned) : make_uint4(0u, 0u, 0u, 0u);
         }
-        NoiseKey nk = P.nk;
-        bool ok = true;
-        int st = 0;
-        unsigned eph = 0u;  // parity of the empty barrier phase to wait for
-        for (int n = 0; n < nwork && ok; ++n) {
-            const int v0 = c * CHUNK;
-            const int v1 = min(P.V, v0 + CHUNK);
-            const char* src = static_cast<const char*>(P.logits) +
-                              ((static_cast<size_t>(b) * K1 + j) * P.V + v0) * ElemTraits<BF16>::SIZE;
-            // with dense q, row j < k_eff is sampled by the residual pass unless
-            // its draft is invalid (the residual is then p itself)
-            int excl = -1, cand = 1;
-            if (!GREEDY && j < keff) {
-                const int d = s_pdrafts[j];
-                const bool valid = d >= 0 && d < P.V;
-                if (!dense && valid) excl = d;
-                if (dense && valid) cand = 0;
-            }
-            // the noise of the chunk's blocks (lane q: blocks q, q + 32, ...), before the
-            // ring slot is free
-            constexpr int NBL = (NB + 31) / 32;
-            BlockNoise bnl[NBL];
-            if (!GREEDY && cand) {
-                nk.seq = static_cast<uint32_t>(b);
-                const uint32_t blk0 = static_cast<uint32_t>(v0 >> kNoiseBlockShift);
-#pragma unroll
-                for (int r = 0; r < NBL; ++r)
-                    if (lane + 32 * r < NB) bnl[r] = block_noise(nk, blk0 + lane + 32 * r, static_cast<uint32_t>(j));
-            }
-            if (n >= kStages) ok = mbar_wait_bounded(&s_empty[st], eph);
-            if (!ok) { if (lane == 0) raise_status(P.status, SPECNG_DEV_TIMEOUT); break; }
-            // the copy goes first; the metadata is written while it is in flight, and the
-            // phase completes once both the bytes and the arrive below are in
-            if (P.aligned && lane == 0) {
-                // the empty barrier already orders the consumers' reads of this stage
-                // before the copy that overwrites it
-                mbar_add_tx(&s_full[st], static_cast<unsigned>(v1 - v0) * ElemTraits<BF16>::SIZE);
-                bulk_g2s(s_stage + st * SB, src, static_cast<unsigned>(v1 - v0) * ElemTraits<BF16>::SIZE, &s_full[st]);
-            }
-            StageMeta& mt = s_meta[st];
-            if (lane == 0) {
-                mt.b = b; mt.j = j; mt.c = c; mt.excl = excl;
-                mt.seg_end = (c == P.nchunk - 1 || n == nwork - 1) ? 1 : 0;
-                mt.cand = cand;
-            }
-            if (!GREEDY && cand) {
-#pragma unroll
-                for (int r = 0; r < NBL; ++r)
-                    if (lane + 32 * r < NB) mt.bn[lane + 32 * r] = bnl[r];
-                __syncwarp();
-                if (lane < kCWarps) {
-                    float mn = INFINITY;
-#pragma unroll
-                    for (int q = 0; q < BPW; ++q) mn = fminf(mn, mt.bn[lane * BPW + q].lnM);
-                    mt.wmin[lane] = mn;
-                }
-            }
-            if constexpr (PENALTY) {
-                // bitmap of the penalised ids of row j in [v0, v1), and which slices hold one
-                uint32_t* bm = s_bm + st * (CHUNK / 32);
-                for (int t = lane; t < CHUNK / 32; t += 32) bm[t] = 0u;
-                __syncwarp();
-                const WindowView wv{s_hwin, s_pdrafts, nh, P.W};
-                const int nwin = wv.count(j);
-                unsigned pw = 0u;
-                for (int t = lane; t < nwin; t += 32) {
-                    const int tok = wv.token(j, t);
-                    if (tok >= v0 && tok < v1) {
-                        atomicOr(&bm[(tok - v0) >> 5], 1u << ((tok - v0) & 31));
-                        pw |= 1u << ((tok - v0) / SL);
-                    }
-                }
-                pw = __reduce_or_sync(0xffffffffu, pw);
-                if (lane == 0) mt.penw = pw;
-            } else {
-                if (lane == 0) mt.penw = 0u;
-            }
-            if (!P.aligned) {
-                uint8_t* dst = s_stage + st * SB;
-                for (int e = lane; e < v1 - v0; e += 32) {
-                    if constexpr (BF16) reinterpret_cast<uint16_t*>(dst)[e] = reinterpret_cast<const uint16_t*>(src)[e];
-                    else reinterpret_cast<uint32_t*>(dst)[e] = reinterpret_cast<const uint32_t*>(src)[e];
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_full[st]);
-            if (++st == kStages) {
-                st = 0;
-                if (n >= kStages) eph ^= 1u;  // the waits of ring cycle u (>= 1) are for phase u - 1
-            }
-            // advance to the next row-chunk
-            if (++c == P.nchunk) {
-                c = 0;
-                if (++j > keff) {
-                    j = 0;
-                    ++b;
-                    if (n + 1 < nwork) {
-                        install(nxt);
-                        const int L2 = PENALTY ? clampL(Lnext2) : 0;
-                        fetch(b + 1, L2, nxt);
-                        if (PENALTY && b + 2 < P.B) Lnext2 = P.lens[b + 2];
-                    }
-                }
-            }
-        }
-        // the CTA stays resident until every issued copy has landed
-        if (P.aligned && lane == 0) {
-            const int lo = nwork > kStages ? nwork - kStages : 0;
-            for (int n = lo; n < nwork; ++n) mbar_wait_bounded(&s_full[n % kStages], static_cast<unsigned>((n / kStages) & 1));
-        }
-        return;
-    }
+    };
+    uint4 rv[kIV], rn[kIV];
+    load_it(0, rn);
 
-    if (warp == kMWarp) {
-        // ================= merge warp =================
-        // Polls the streaming warps' queues (lane q watches queue q) until every
-        // streaming warp has finished and every queue is drained.  The wait is bounded.
-        unsigned idle = 0;
-        while (true) {
-            const bool has = lane < kCWarps && s_mq_head[lane] != s_mq_tail[lane];
-            const unsigned qs = __ballot_sync(0xffffffffu, has);
-            if (qs != 0u) {
-                idle = 0;
-                const int q = __ffs(qs) - 1;
-                const int h = s_mq_head[q];
-                const int row = s_mq[q][h % kMQ];
-                __syncwarp();
-                merge_row<BF16, GREEDY, SOFTCAP, PENALTY>(P, row);
-                __syncwarp();
-                if (lane == 0) s_mq_head[q] = h + 1;
-                __syncwarp();
-                continue;
-            }
-            if (*reinterpret_cast<volatile int*>(&s_done) == kCWarps) {
-                // every push happened before its warp's increment of s_done
-                __threadfence_block();
-                const bool again = lane < kCWarps && s_mq_head[lane] != s_mq_tail[lane];
-                if (!__any_sync(0xffffffffu, again)) break;
-                continue;
-            }
-            if (++idle > (1u << 22)) {
-                if (lane == 0) raise_status(P.status, SPECNG_DEV_TIMEOUT);
-                break;
-            }
-            __nanosleep(idle < 64 ? 32 : 256);
-        }
-        return;
-    }
-
-    // ================= streaming warps =================
-    // Per-lane accumulators live across the chunks of one row (a segment of
-    // the CTA's range); warps combine them once, at the segment's last chunk.
-    const int ubase = warp * (32 * kVL);        // first 16-byte vector of my slice
-    const int off0 = ubase * EPV + lane * EPV;  // chunk offset of vector 0's element 0
-    float thr = -INFINITY;
-    float m = -INFINITY, s = 0.0f, msc = 0.0f;
-    Top2 tt = top2_empty();
-    int seg = 0, cfirst = 0;
-    int row = 0, excl = -1;
-    bool cand = false;
+    // noise of my block (lane q: block q of the piece)
+    BlockNoise bn{};
     RowPhilox rp{};
-    bool fresh = true;
-    int st = 0;
-    unsigned fph = 0u;  // parity of the full barrier phase to wait for
-    for (int n = 0; n < nwork; ++n) {
-        if (!mbar_wait_bounded(&s_full[st], fph)) {
-            if (lane == 0) raise_status(P.status, SPECNG_DEV_TIMEOUT);
-            break;
-        }
-        const StageMeta& mt = s_meta[st];
-        const int c = mt.c;
-        unsigned* rth = &s_rthr[seg % (kStages + 1)];
-        const bool seg_start = fresh;
-        if (seg_start) {
-            const int b = mt.b, j = mt.j;
-            row = b * K1 + j;
-            excl = mt.excl;
-            cand = !GREEDY && mt.cand != 0;
-            cfirst = c;
-            if (cand) {
-                NoiseKey nk = P.nk;
-                nk.seq = static_cast<uint32_t>(b);
-                rp = row_philox(nk, static_cast<uint32_t>(j));
+    if (cand) {
+        if (lane < NBP) bn = block_noise(nk, static_cast<uint32_t>((v0 >> kNoiseBlockShift) + lane), static_cast<uint32_t>(j));
+        rp = row_philox(nk, static_cast<uint32_t>(j));
+    }
+    // penalty window of row j: the last W tokens of history ++ d_1..d_j, as a bitmap of the piece
+    uint32_t* pbm = s_pbm + (PENALTY ? warp * (PIECE / 32) : 0);
+    bool anypen = false;
+    if constexpr (PENALTY) {
+        for (int t = lane; t < PIECE / 32; t += 32) pbm[t] = 0u;
+        int L = P.lens[b];
+        L = L < 0 ? 0 : (static_cast<int64_t>(L) > P.hist_stride ? static_cast<int>(P.hist_stride) : L);
+        const int total = L + j;
+        const int nw = total < P.W ? total : P.W;
+        __syncwarp();
+        bool mine = false;
+        for (int t = lane; t < nw; t += 32) {
+            const int idx = total - nw + t;
+            const int tok = idx < L ? P.hist[static_cast<size_t>(b) * P.hist_stride + idx] : P.drafts[b * P.K + (idx - L)];
+            if (tok >= v0 && tok < v1) {
+                atomicOr(&pbm[(tok - v0) >> 5], 1u << ((tok - v0) & 31));
+                mine = true;
             }
         }
-        const int v0 = c * CHUNK;
-        const int v1 = min(P.V, v0 + CHUNK);
-        const uint4* stage = reinterpret_cast<const uint4*>(s_stage + st * SB);
-        const uint32_t* bm = s_bm + (PENALTY ? st * (CHUNK / 32) : 0);
-        const bool full = v0 + off0 + (kVL - 1) * 32 * EPV + EPV <= v1;  // my vectors are whole
-        uint4 rv[kVL];
+        anypen = __any_sync(0xffffffffu, mine);
+        __syncwarp();
+    }
+
+    unsigned* gthr = P.row_thr + row;  // the row's best score (score_key; 0 = none)
+    float thr = -INFINITY;
+    float mref = -INFINITY, s = 0.0f, m = -INFINITY;
+    Top2 tt = top2_empty();
+    unsigned pub = 0u;           // best key this warp has published
+    unsigned gk = 0u;            // the row's best, read one iteration ahead
+
+    for (int it = 0; it < NIT; ++it) {
 #pragma unroll
-        for (int i = 0; i < kVL; ++i) rv[i] = stage[ubase + i * 32 + lane];
-        // penalised elements of my lane (bit 8 i + e), only where the slice holds one
-        uint64_t pmk = 0u;
+        for (int i = 0; i < kIV; ++i) rv[i] = rn[i];
+        if (it + 1 < NIT) load_it(it + 1, rn);
+        if (!GREEDY && cand && it > 0) {
+            const float best = key_score(gk);
+            if (best > -INFINITY) thr = fmaxf(thr, best - cand_delta(best));
+        }
+        if (!GREEDY && cand && lane == 0) gk = __ldcg(gthr);  // used next iteration
+        gk = __shfl_sync(0xffffffffu, gk, 0);
+        const int ib = ebase + it * kIV * 32 * EPV;  // id of element 0 of my vector (it, 0)
+        const bool full = ib + (kIV - 1) * 32 * EPV + EPV <= v1;
+        // penalised elements of my lane in this iteration (bit 8 i + e)
+        unsigned pmk = 0u;
         if constexpr (PENALTY) {
-            if ((mt.penw >> warp) & 1u) {
+            if (anypen) {
 #pragma unroll
-                for (int i = 0; i < kVL; ++i) {
-                    const int off = off0 + i * 32 * EPV;
-                    pmk |= static_cast<uint64_t>((bm[off >> 5] >> (off & 31)) & ((1u << EPV) - 1u)) << (8 * i);
+                for (int i = 0; i < kIV; ++i) {
+                    const int off = ib + i * 32 * EPV - v0;
+                    if (off < PIECE) pmk |= ((pbm[off >> 5] >> (off & 31)) & ((1u << EPV) - 1u)) << (8 * i);
                 }
             }
         }
 
-        // ---- streaming: lane maximum zl (bounds my transformed values, penalised ones
-        //      included), sum of exponentials
-        float zl = -INFINITY;
-        float lraw = -INFINITY;
-        uint32_t hv[kVL];  // packed vector maxima (bf16), or the fp32 maxima
+        // ---- streaming
+        float zl = -INFINITY, lraw = -INFINITY;
+        uint32_t hv[kIV];
         if (full) {
             if constexpr (BF16) {
 #pragma unroll
-                for (int i = 0; i < kVL; ++i) hv[i] = as_u32(bf16x8_max2(rv[i]));
-                __nv_bfloat162 h = __hmax2(__hmax2(__hmax2(as_bf162(hv[0]), as_bf162(hv[1])), __hmax2(as_bf162(hv[2]), as_bf162(hv[3]))),
-                                           __hmax2(__hmax2(as_bf162(hv[4]), as_bf162(hv[5])), __hmax2(as_bf162(hv[6]), as_bf162(hv[7]))));
-                lraw = fmaxf(bf16lo(as_u32(h)), bf16hi(as_u32(h)));
+                for (int i = 0; i < kIV; ++i) hv[i] = as_u32(bf16x8_max2(rv[i]));
+                const uint32_t h = as_u32(__hmax2(__hmax2(as_bf162(hv[0]), as_bf162(hv[1])),
+                                                  __hmax2(as_bf162(hv[2]), as_bf162(hv[3]))));
+                lraw = fmaxf(bf16lo(h), bf16hi(h));
             } else {
 #pragma unroll
-                for (int i = 0; i < kVL; ++i) {
+                for (int i = 0; i < kIV; ++i) {
                     const float f = fmaxf(fmaxf(__uint_as_float(rv[i].x), __uint_as_float(rv[i].y)),
                                           fmaxf(__uint_as_float(rv[i].z), __uint_as_float(rv[i].w)));
                     hv[i] = __float_as_uint(f);
@@ -899,19 +635,14 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                 }
             }
             zl = SOFTCAP ? transform_f32<true, false>(lraw, false, P) : lraw;
-            if constexpr (GREEDY) {
-                if (zl > m) m = zl;
-            } else {
-                if (zl > m) {
-                    s = m > -INFINITY ? s * ex2_approx((m - zl) * P.sc) : 0.0f;
-                    m = zl;
-                    msc = m * P.sc;
-                }
-                float2 acc2[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
-                                  make_float2(0.0f, 0.0f)};
+            m = fmaxf(m, zl);
+            if constexpr (!GREEDY) {
+                if (!(mref > -INFINITY)) mref = zl;
+                const float msc = mref * P.sc;
+                float2 acc2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
                 const float2 sc2 = make_float2(P.sc, P.sc), nm2 = make_float2(-msc, -msc);
 #pragma unroll
-                for (int i = 0; i < kVL; ++i) {
+                for (int i = 0; i < kIV; ++i) {
                     float x[EPV];
                     unpack<BF16>(rv[i], x);
 #pragma unroll
@@ -919,41 +650,64 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                         const float2 t = __ffma2_rn(make_float2(transform_f32<SOFTCAP, false>(x[e], false, P),
                                                                 transform_f32<SOFTCAP, false>(x[e + 1], false, P)),
                                                     sc2, nm2);
-                        acc2[i & 3] = __fadd2_rn(acc2[i & 3], make_float2(ex2_approx(t.x), ex2_approx(t.y)));
+                        acc2[i & 1] = __fadd2_rn(acc2[i & 1], make_float2(ex2_approx(t.x), ex2_approx(t.y)));
                     }
                 }
-                s += ((acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y)) + ((acc2[2].x + acc2[2].y) + (acc2[3].x + acc2[3].y));
+                float add = (acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y);
+                if ((zl - mref) * P.sc > 32.0f) {
+                    // a value far above the reference: raise it and take the iteration again
+                    s *= ex2_approx((mref - zl) * P.sc);
+                    mref = zl;
+                    const float msc2 = mref * P.sc;
+                    add = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < kIV; ++i) {
+                        float x[EPV];
+                        unpack<BF16>(rv[i], x);
+#pragma unroll
+                        for (int e = 0; e < EPV; ++e)
+                            add += ex2_approx(fmaf(transform_f32<SOFTCAP, false>(x[e], false, P), P.sc, -msc2));
+                    }
+                }
+                s += add;
             }
             if constexpr (PENALTY) {
-                // the few penalised elements: replace their terms by the penalised ones (and
-                // raise the maximum if a penalty below 1 lifted one above it)
-                uint64_t pw = pmk;
+                // the few penalised elements: replace their terms by the penalised ones
+                unsigned pw = pmk;
                 while (pw != 0u) {
-                    const int bit = __ffsll(static_cast<long long>(pw)) - 1;
+                    const int bit = __ffs(pw) - 1;
                     pw &= pw - 1u;
-                    const float xe = elem_of_stage<BF16>(stage, off0 + (bit >> 3) * 32 * EPV + (bit & 7));
+                    float xx[EPV];
+                    uint4 r = rv[0];
+#pragma unroll
+                    for (int i = 1; i < kIV; ++i)
+                        if ((bit >> 3) == i) r = rv[i];
+                    unpack<BF16>(r, xx);
+                    float xe = xx[0];
+#pragma unroll
+                    for (int e = 1; e < EPV; ++e)
+                        if ((bit & 7) == e) xe = xx[e];
                     const float zu = transform_f32<SOFTCAP, false>(xe, false, P);
                     const float zp = transform_f32<SOFTCAP, true>(xe, true, P);
                     zl = fmaxf(zl, zp);
-                    if constexpr (GREEDY) {
-                        m = fmaxf(m, zp);
-                    } else {
-                        if (zp > m) {
-                            s *= ex2_approx((m - zp) * P.sc);
-                            m = zp;
-                            msc = m * P.sc;
+                    m = fmaxf(m, zp);
+                    if constexpr (!GREEDY) {
+                        if ((zp - mref) * P.sc > 32.0f) {
+                            s *= ex2_approx((mref - zp) * P.sc);
+                            mref = zp;
                         }
+                        const float msc = mref * P.sc;
                         s += ex2_approx(fmaf(zp, P.sc, -msc)) - ex2_approx(fmaf(zu, P.sc, -msc));
                     }
                 }
             }
         } else {
-            // partial vectors (a row's last chunk): exact transform element by element
+            // partial vectors (a row's last piece): exact transform element by element
 #pragma unroll
-            for (int i = 0; i < kVL; ++i) {
+            for (int i = 0; i < kIV; ++i) {
                 hv[i] = BF16 ? 0xFF80FF80u : __float_as_uint(-INFINITY);
-                const int off = off0 + i * 32 * EPV;
-                const int nv = min(EPV, v1 - (v0 + off));
+                const int e0 = ib + i * 32 * EPV;
+                const int nv = min(EPV, v1 - e0);
                 if (nv <= 0) continue;
                 float x[EPV];
                 unpack<BF16>(rv[i], x);
@@ -963,15 +717,13 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                     const float z = transform_f32<SOFTCAP, PENALTY>(x[e], (pmk >> (8 * i + e)) & 1u, P);
                     lraw = fmaxf(lraw, x[e]);
                     zl = fmaxf(zl, z);
-                    if constexpr (GREEDY) {
-                        m = fmaxf(m, z);
-                    } else {
-                        if (z > m) {
-                            s = m > -INFINITY ? s * ex2_approx((m - z) * P.sc) : 0.0f;
-                            m = z;
-                            msc = m * P.sc;
+                    m = fmaxf(m, z);
+                    if constexpr (!GREEDY) {
+                        if (!(mref > -INFINITY) || (z - mref) * P.sc > 32.0f) {
+                            s = mref > -INFINITY ? s * ex2_approx((mref - z) * P.sc) : 0.0f;
+                            mref = z;
                         }
-                        s += ex2_approx(fmaf(z, P.sc, -msc));
+                        s += ex2_approx(fmaf(z, P.sc, -mref * P.sc));
                     }
                 }
             }
@@ -980,16 +732,15 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
         // ---- candidates
         if constexpr (GREEDY) {
             // top two transformed values (lower id on ties) within cand_delta of the best
-            // value any warp of the CTA has reached in this segment.  Without a penalty the
-            // lane maximum is itself a value of the row (the transform is monotone)
-            float gth = fmaxf(tt.s1, key_score(*reinterpret_cast<volatile unsigned*>(rth)));
+            // value seen; without a penalty the lane maximum is itself a value of the row
+            float gth = tt.s1;
             if constexpr (!PENALTY) gth = fmaxf(gth, key_score(warp_best_key(zl)));
             gth = gth > -INFINITY ? gth - cand_delta(gth) : -INFINITY;
             if (zl >= gth) {
 #pragma unroll
-                for (int i = 0; i < kVL; ++i) {
-                    const int off = off0 + i * 32 * EPV;
-                    const int nv = min(EPV, v1 - (v0 + off));
+                for (int i = 0; i < kIV; ++i) {
+                    const int e0 = ib + i * 32 * EPV;
+                    const int nv = min(EPV, v1 - e0);
                     if (nv <= 0) continue;
                     float x[EPV];
                     unpack<BF16>(rv[i], x);
@@ -998,72 +749,82 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                         if (e >= nv) break;
                         const float z = transform_f32<SOFTCAP, PENALTY>(x[e], (pmk >> (8 * i + e)) & 1u, P);
                         if (z >= gth) {
-                            top2_push(tt, z, v0 + off + e);
+                            top2_push(tt, z, e0 + e);
                             gth = fmaxf(gth, tt.s1 - cand_delta(tt.s1));
                         }
                     }
                 }
             }
-            const unsigned kw = warp_best_key(tt.s1);
-            if (lane == 0 && kw != 0u) atomicMax(rth, kw);
         } else if (cand) {
             int seeded = -1;
-            if (seg_start) {
-                // seed: every lane scores its largest raw element (any exact score bounds the
-                // best from below); the CTA's warps share the best seed
-                int am = -1;
+            if (it == 0) {
+                // seed: the lane holding the warp's largest raw element scores it (any exact
+                // score bounds the best from below); lowest position among equal maxima
+                const unsigned ku = lraw > -INFINITY ? score_key(lraw) : 0u;
+                const unsigned kmax = __reduce_max_sync(0xffffffffu, ku);
+                const unsigned own = __ballot_sync(0xffffffffu, kmax != 0u && ku == kmax);
+                const int sl = own != 0u ? __ffs(own) - 1 : 0;
+                int am = -1;  // 8 i + e of the maximum in lane sl
+                if (own != 0u && lane == sl) {
 #pragma unroll
-                for (int i = kVL - 1; i >= 0; --i) {
-                    const int off = off0 + i * 32 * EPV;
-                    const int nv = min(EPV, v1 - (v0 + off));
-                    float x[EPV];
-                    unpack<BF16>(rv[i], x);
+                    for (int i = kIV - 1; i >= 0; --i) {
+                        const int nv = min(EPV, v1 - (ib + i * 32 * EPV));
+                        float x[EPV];
+                        unpack<BF16>(rv[i], x);
 #pragma unroll
-                    for (int e = EPV - 1; e >= 0; --e)
-                        if (e < nv && x[e] == lraw) am = off + e;
+                        for (int e = EPV - 1; e >= 0; --e)
+                            if (e < nv && x[e] == lraw) am = i * 8 + e;
+                    }
                 }
+                am = __shfl_sync(0xffffffffu, am, sl);
+                int sv = am >= 0 ? v0 + sl * EPV + (am >> 3) * 32 * EPV + (am & 7) : -1;
+                if (sv == excl) sv = -1;
                 float t0 = -INFINITY;
-                if (am >= 0 && v0 + am != excl) {
-                    const float z = transform_f32<SOFTCAP, PENALTY>(elem_of_stage<BF16>(stage, am),
-                                                                    PENALTY && ((bm[am >> 5] >> (am & 31)) & 1u), P);
-                    const uint32_t v = static_cast<uint32_t>(v0 + am);
-                    const BlockNoise bk = mt.bn[am >> kNoiseBlockShift];
-                    t0 = z * P.invT - ln_fast(noise_exp_f32(rp, bk.M, bk.I, v));
-                    top2_push(tt, t0, static_cast<int>(v));
-                    seeded = static_cast<int>(v);
+                if (sv >= 0) {
+                    const int q = ((sv - v0) >> kNoiseBlockShift);
+                    const float Mq = __shfl_sync(0xffffffffu, bn.M, q);
+                    const int Iq = __shfl_sync(0xffffffffu, bn.I, q);
+                    if (lane == sl) {
+                        float xx[EPV];
+                        uint4 r = rv[0];
+#pragma unroll
+                        for (int i = 1; i < kIV; ++i)
+                            if ((am >> 3) == i) r = rv[i];
+                        unpack<BF16>(r, xx);
+                        float xe = xx[0];
+#pragma unroll
+                        for (int e = 1; e < EPV; ++e)
+                            if ((am & 7) == e) xe = xx[e];
+                        const float z = transform_f32<SOFTCAP, PENALTY>(xe, (pmk >> am) & 1u, P);
+                        t0 = z * P.invT - ln_fast(noise_exp_f32(rp, Mq, Iq, static_cast<uint32_t>(sv)));
+                        top2_push(tt, t0, sv);
+                        seeded = sv;
+                    }
                 }
                 const unsigned k0 = warp_best_key(t0);
                 if (k0 != 0u) {
                     const float b0 = key_score(k0);
                     thr = fmaxf(thr, b0 - cand_delta(b0));
-                    if (lane == 0) atomicMax(rth, k0);
+                    if (lane == 0 && k0 > pub) atomicMax(gthr, k0);
+                    pub = max(pub, k0);
                 }
             }
-            {
-                // adopt the best score another warp published for this segment
-                const float best = key_score(*reinterpret_cast<volatile unsigned*>(rth));
-                if (best > -INFINITY) thr = fmaxf(thr, best - cand_delta(best));
-            }
-            // gate: no score of my lane exceeds zl / T - (smallest ln M of the slice)
-            const float zlb = zl * P.invT;
-            const bool lpass = zlb - mt.wmin[warp] + bound_slack(zlb) >= thr;
-            if (__any_sync(0xffffffffu, lpass)) {
-                // block tests: every score of vector i is at most z / T - ln M_i; then the
-                // elements of the passing vectors that can reach the best
-                uint64_t msk = 0u;
-                if (lpass) {
+            // block tests: every score of vector i is at most z / T - ln M of its block
+            unsigned msk = 0u;
 #pragma unroll
-                    for (int i = 0; i < kVL; ++i) {
-                        const int off = off0 + i * 32 * EPV;
-                        const float lnM = mt.bn[off >> kNoiseBlockShift].lnM;
-                        float zv;
-                        if constexpr (BF16) zv = fmaxf(bf16lo(hv[i]), bf16hi(hv[i]));
-                        else zv = __uint_as_float(hv[i]);
-                        if (SOFTCAP && full) zv = transform_f32<true, false>(zv, false, P);
-                        const unsigned pb = static_cast<unsigned>(pmk >> (8 * i)) & 0xFFu;
-                        const float zvb = zv * P.invT;
-                        if (!(pb != 0u || !full || zvb - lnM + bound_slack(zvb) >= thr)) continue;
-                        unsigned mi;
+            for (int i = 0; i < kIV; ++i) {
+                const int q = (it * kIV + i) / VPB;  // block of vector i (warp-uniform)
+                const float lnM = __shfl_sync(0xffffffffu, bn.lnM, q);
+                float zv;
+                if constexpr (BF16) zv = fmaxf(bf16lo(hv[i]), bf16hi(hv[i]));
+                else zv = __uint_as_float(hv[i]);
+                if (SOFTCAP && full) zv = transform_f32<true, false>(zv, false, P);
+                const unsigned pb = (pmk >> (8 * i)) & 0xFFu;
+                const float zvb = zv * P.invT;
+                const bool vp = pb != 0u || !full || zvb - lnM + bound_slack(zvb) >= thr;
+                if (__any_sync(0xffffffffu, vp)) {
+                    unsigned mi = 0u;
+                    if (vp) {
                         if (full) {
                             // z >= T (thr + ln M), in raw units
                             const float zt = (thr + lnM) * P.T;
@@ -1084,133 +845,97 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                                 mi |= static_cast<unsigned>(__uint_as_float(rv[i].z) >= xt) << 2;
                                 mi |= static_cast<unsigned>(__uint_as_float(rv[i].w) >= xt) << 3;
                             }
-                            mi |= pb;  // penalised: decided exactly below
+                            mi |= pb;  // penalised: tested exactly below
                         } else {
-                            const int nv = min(EPV, v1 - (v0 + off));
+                            const int nv = min(EPV, v1 - (ib + i * 32 * EPV));
                             mi = nv > 0 ? (1u << nv) - 1u : 0u;
                         }
-                        msk |= static_cast<uint64_t>(mi) << (8 * i);
                     }
-                    if (seeded >= 0) {
-                        const int so = seeded - v0 - off0;
-                        const int si = so / (32 * EPV), se = so - si * 32 * EPV;
-                        if (se >= 0 && se < EPV) msk &= ~(static_cast<uint64_t>(1) << (8 * si + se));
-                    }
+                    msk |= mi << (8 * i);
                 }
-                // score the lane's candidates one per iteration, the warp in step
-                while (__any_sync(0xffffffffu, msk != 0u)) {
-                    int v = -1, loc = 0;
-                    float zb = -INFINITY;
-                    if (msk != 0u) {
-                        const int bit = __ffsll(static_cast<long long>(msk)) - 1;
-                        msk &= msk - 1u;
-                        loc = off0 + (bit >> 3) * 32 * EPV + (bit & 7);
-                        const bool pen = PENALTY && ((pmk >> bit) & 1u);
-                        zb = transform_f32<SOFTCAP, PENALTY>(elem_of_stage<BF16>(stage, loc), pen, P) * P.invT;
-                        v = v0 + loc;
-                    }
-                    const BlockNoise bk = mt.bn[loc >> kNoiseBlockShift];
-                    const bool live = v >= 0 && v != excl && zb - bk.lnM + bound_slack(zb) >= thr;
-                    if (__any_sync(0xffffffffu, live)) {
-                        const float E = noise_exp_f32(rp, bk.M, bk.I, static_cast<uint32_t>(v < 0 ? 0 : v));
-                        if (live) {
-                            const float score = zb - ln_fast(E);
-                            if (score >= thr) {
-                                top2_push(tt, score, v);
-                                thr = fmaxf(thr, tt.s1 - cand_delta(tt.s1));
-                            }
+            }
+            if (seeded >= 0) {
+                const int so = seeded - ib;
+                const int si = so / (32 * EPV), se = so - si * 32 * EPV;
+                if (so >= 0 && se >= 0 && se < EPV) msk &= ~(1u << (8 * si + se));
+            }
+            if (excl >= ib && excl < ib + kIV * 32 * EPV) {
+                const int so = excl - ib;
+                const int si = so / (32 * EPV), se = so - si * 32 * EPV;
+                if (se >= 0 && se < EPV) msk &= ~(1u << (8 * si + se));
+            }
+            // score the lane's candidates one per iteration, the warp in step
+            while (__any_sync(0xffffffffu, msk != 0u)) {
+                int v = -1, bi = 0;
+                float zb = -INFINITY;
+                if (msk != 0u) {
+                    const int bit = __ffs(msk) - 1;
+                    msk &= msk - 1u;
+                    bi = bit >> 3;
+                    float xx[EPV];
+                    uint4 r = rv[0];
+#pragma unroll
+                    for (int i = 1; i < kIV; ++i)
+                        if (bi == i) r = rv[i];
+                    unpack<BF16>(r, xx);
+                    float xe = xx[0];
+#pragma unroll
+                    for (int e = 1; e < EPV; ++e)
+                        if ((bit & 7) == e) xe = xx[e];
+                    zb = transform_f32<SOFTCAP, PENALTY>(xe, (pmk >> bit) & 1u, P) * P.invT;
+                    v = ib + bi * 32 * EPV + (bit & 7);
+                }
+                const int q = (it * kIV + bi) / VPB;  // my candidate's block (per lane)
+                const float Mq = __shfl_sync(0xffffffffu, bn.M, q);
+                const float lnMq = __shfl_sync(0xffffffffu, bn.lnM, q);
+                const int Iq = __shfl_sync(0xffffffffu, bn.I, q);
+                const bool live = v >= 0 && v != excl && zb - lnMq + bound_slack(zb) >= thr;
+                if (__any_sync(0xffffffffu, live)) {
+                    const float E = noise_exp_f32(rp, Mq, Iq, static_cast<uint32_t>(v < 0 ? 0 : v));
+                    if (live) {
+                        const float score = zb - ln_fast(E);
+                        if (score >= thr) {
+                            top2_push(tt, score, v);
+                            thr = fmaxf(thr, tt.s1 - cand_delta(tt.s1));
                         }
                     }
                 }
-                // share the warp's best score with the CTA
-                const unsigned kw = warp_best_key(tt.s1);
-                if (kw != 0u) {
-                    const float bw = key_score(kw);
-                    thr = fmaxf(thr, bw - cand_delta(bw));
-                    if (lane == 0) atomicMax(rth, kw);
-                }
+            }
+            // publish the warp's best when it improved
+            const unsigned kw = warp_best_key(tt.s1);
+            if (kw > pub) {
+                const float bw = key_score(kw);
+                thr = fmaxf(thr, bw - cand_delta(bw));
+                if (lane == 0) atomicMax(gthr, kw);
+                pub = kw;
             }
         }
+    }
 
-        fresh = mt.seg_end != 0;
-        if (fresh) {
-            // ---- end of this row's segment: one partial for the segment
-            float pm = m, ps = s;
-            Top2 pt = tt;
-            if constexpr (!GREEDY) {
-                if (!(pm > -INFINITY)) ps = 0.0f;
+    // ---- the piece's partial, then the row merge if this warp completes the row
+    float pm = GREEDY ? m : mref, ps = s;
+    if constexpr (!GREEDY) {
+        if (!(pm > -INFINITY)) ps = 0.0f;
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    const float mo = __shfl_xor_sync(0xffffffffu, pm, off);
-                    const float so = __shfl_xor_sync(0xffffffffu, ps, off);
-                    ms_merge(pm, ps, mo, so, P.sc);
-                }
-            }
-            pt = top2_warp_reduce(pt);
-            int last = 0;
-            if (lane == 0) {
-                s_slot[st][warp] = WarpPart{pm, ps, pt};
-                __threadfence_block();
-                last = atomicAdd(&s_cnt[st], 1) == kCWarps - 1;
-            }
-            last = __shfl_sync(0xffffffffu, last, 0);
-            if (last) {
-                __threadfence_block();
-                WarpPart wp = lane < kCWarps ? s_slot[st][lane] : WarpPart{-INFINITY, 0.0f, top2_empty()};
-                float cm = wp.m, cs = wp.s;
-                Top2 ct = wp.t;
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    const float mo = __shfl_xor_sync(0xffffffffu, cm, off);
-                    const float so = __shfl_xor_sync(0xffffffffu, cs, off);
-                    ms_merge(cm, cs, mo, so, P.sc);
-                    ct = top2_merge(ct, top2_shfl_xor(ct, off));
-                }
-                int merge_now = 0;
-                if (lane == 0) {
-                    // keyed by the segment's last chunk; a written partial is never all-zero
-                    st_partial(P.part + static_cast<size_t>(row) * P.nchunk + c, GREEDY ? 0.0f : cm,
-                               GREEDY ? 1.0f : cs, ct);
-                    s_cnt[st] = 0;
-                    *rth = 0u;  // every warp is past this segment: the slot is free
-                    // the CTA that completes the row's chunks merges it
-                    __threadfence();
-                    const unsigned nseg = static_cast<unsigned>(c - cfirst + 1);
-                    const unsigned prev = atomicAdd(&P.row_ticket[row], nseg);
-                    if (prev + nseg == static_cast<unsigned>(P.nchunk)) {
-                        __threadfence();
-                        const int tl = s_mq_tail[warp];
-                        if (tl - s_mq_head[warp] < kMQ) {
-                            s_mq[warp][tl % kMQ] = row;
-                            __threadfence_block();
-                            s_mq_tail[warp] = tl + 1;
-                        } else {
-                            merge_now = 1;  // queue full: merge here
-                        }
-                    }
-                }
-                merge_now = __shfl_sync(0xffffffffu, merge_now, 0);
-                if (merge_now) merge_row<BF16, GREEDY, SOFTCAP, PENALTY>(P, row);
-            }
-            m = -INFINITY;
-            s = 0.0f;
-            msc = 0.0f;
-            tt = top2_empty();
-            thr = -INFINITY;
-            ++seg;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_empty[st]);
-        if (++st == kStages) {
-            st = 0;
-            fph ^= 1u;
+        for (int off = 16; off > 0; off >>= 1) {
+            const float mo = __shfl_xor_sync(0xffffffffu, pm, off);
+            const float so = __shfl_xor_sync(0xffffffffu, ps, off);
+            ms_merge(pm, ps, mo, so, P.sc);
         }
     }
-    __syncwarp();
+    const Top2 pt = top2_warp_reduce(tt);
+    int last = 0;
     if (lane == 0) {
-        __threadfence_block();
-        atomicAdd(&s_done, 1);
+        // a written partial is never all-zero
+        st_partial(P.part + static_cast<size_t>(row) * P.nchunk + p, GREEDY ? 0.0f : pm, GREEDY ? 1.0f : ps, pt);
+        __threadfence();
+        last = atomicAdd(&P.row_ticket[row], 1u) == static_cast<unsigned>(P.nchunk - 1);
     }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (!last) return;
+    __threadfence();
+    if (lane == 0) P.row_thr[row] = 0u;  // every piece of the row is done
+    merge_row<BF16, GREEDY, SOFTCAP, PENALTY>(P, row);
 }
 
 // ---------------------------------------------------------------- K2
@@ -1493,16 +1218,10 @@ __host__ inline int sm_count_cached() {
 
 template <bool BF16, bool G, bool C, bool R>
 cudaError_t launch_stream(const VerifyDev& P, cudaStream_t s) {
-    // one persistent CTA per SM; the staging ring lives in dynamic shared memory
-    constexpr size_t smem = k1_dyn_smem<R>();
-    static bool configured = false;
-    if (!configured) {
-        const cudaError_t e = cudaFuncSetAttribute(verify_stream_kernel<BF16, G, C, R>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
-    verify_stream_kernel<BF16, G, C, R><<<sm_count_cached(), kPThreads, smem, s>>>(P);
+    // one warp per piece of every row that may be active; warps of inactive rows exit at once
+    const long long warps = static_cast<long long>(P.B) * (P.K + 1) * P.nchunk;
+    const unsigned grid = static_cast<unsigned>((warps + kPW - 1) / kPW);
+    verify_piece_kernel<BF16, G, C, R><<<grid, kPT, 0, s>>>(P);
     return cudaGetLastError();
 }
 
@@ -1519,8 +1238,8 @@ cudaError_t launch_stream_cr(const VerifyDev& P, bool c, bool r, cudaStream_t s)
     return r ? launch_stream<BF16, G, false, true>(P, s) : launch_stream<BF16, G, false, false>(P, s);
 }
 
-// The kernels of one spec_verify call for one logits dtype: the streaming
-// kernel (with the merges), then, for dense q at T > 0, the residual pass.
+// The kernels of one spec_verify call for one logits dtype: the piece kernel
+// (with the merges), then, for dense q at T > 0, the residual pass.
 template <bool BF16>
 cudaError_t launch_verify_dtype(const VerifyDev& P, bool greedy, bool softcap, bool penalty, bool dense,
                                 cudaStream_t s);
