@@ -475,42 +475,52 @@ __device__ __noinline__ void merge_row(const VerifyDev& P, int row) {
 
 // ---------------------------------------------------------------- K1
 // One warp per piece of a row.  The active rows of the call (rows 0..k_eff of
-// every sequence) are cut into pieces of 16 KB; each warp streams its piece
-// once with 16-byte loads (the next iteration's loads in flight while the
-// current one is computed) and leaves one partial (maximum, sum of
-// exponentials, top-two sampling candidates).  The warp that finishes a row's
-// last piece (atomic ticket) merges the row at once; the last row of a
-// sequence (second ticket) runs the epilogue.  Warps never wait on each other.
-//   * Noise: a bf16 piece holds 32 blocks of 256 ids, one per lane; each lane
-//     draws its block's minimum (one Philox call).  A lane's vector i of
-//     iteration it covers 8 ids of block 4 it + i, so its packed maximum gives
-//     the block test z / T - ln M >= best for its eight ids at once; only the
-//     vectors that pass compare their elements, and each lane scores its few
-//     survivors (per-id Philox draw, E_v, score) in step with the warp.
-//   * The best score of a row is shared by the row's warps through a global
-//     atomic maximum (read one iteration ahead, so its latency is hidden); at
-//     its first iteration a warp scores its largest element to start it.
-//   * The sum of exponentials is kept against a reference maximum fixed at the
-//     piece's first iteration, raised only when a value passes it by more than
-//     2^32 in the sum's units, so the exponentials never wait for a maximum.
+// every sequence) are cut into pieces of 16 KB; each warp reads its piece from
+// HBM once and leaves one partial (maximum, sum of exponentials, top-two
+// sampling candidates).  The warp that finishes a row's last piece (atomic
+// ticket) merges the row at once; the last row of a sequence (second ticket)
+// runs the epilogue.  Warps never wait on each other.
+//
+// Sampling in two phases per warp.  A piece holds 32 noise blocks of 256 ids
+// (bf16; 16 for fp32); lane q draws block q's minimum M_q and its slot I_q.
+//   A  streams the piece with 16-byte loads (the next iteration's in flight):
+//      sum of exponentials, and the maximum of every 16-byte vector, kept in
+//      registers as bf16 (rounded up for fp32 data).  Meanwhile each block's
+//      argmin element is loaded: its score z / T - ln M_q is exact without a
+//      per-id draw.  After the stream the lanes holding the warp's four largest
+//      values score them.  The best of these exact scores is published to the
+//      row's shared best (global atomic maximum) and read back.
+//   B  every score of a vector is at most (its maximum) / T - ln M of its block,
+//      so the vector maxima in registers are tested against the best without
+//      touching the data; the few vectors that pass are reloaded (from L2) and
+//      their surviving elements scored (per-id Philox draw, E_v = M + F_v).
 
 constexpr int kPieceBytes = 16384;
 constexpr int kPW = 8;           // warps per CTA
 constexpr int kPT = kPW * 32;    // threads per CTA
 constexpr int kIV = 4;           // 16-byte vectors per lane per iteration
+constexpr int kTop = 4;          // largest values scored after phase A
 
 template <bool BF16>
 __host__ __device__ constexpr int piece_elems() { return kPieceBytes / ElemTraits<BF16>::SIZE; }
+
+// Smallest bf16 value >= f (an upper bound in bf16), as the low 16 bits.
+__device__ __forceinline__ uint32_t bf16_ceil_bits(float f) {
+    const uint32_t u = __float_as_uint(f);
+    uint32_t h = u >> 16;
+    if ((u & 0xFFFFu) != 0u && !(u & 0x80000000u) && (u & 0x7FFFFFFFu) < 0x7F800000u) h += 1u;  // positive: up
+    return h;
+}
 
 template <bool BF16, bool GREEDY, bool SOFTCAP, bool PENALTY>
 __global__ void __launch_bounds__(kPT, 2) verify_piece_kernel(const VerifyDev P) {
     constexpr int EPV = ElemTraits<BF16>::EPV;
     constexpr int PIECE = piece_elems<BF16>();
-    constexpr int ITV = 32 * kIV;                // vectors per warp per iteration
-    constexpr int NIT = PIECE / (ITV * EPV);     // iterations per piece (8)
+    constexpr int RV = 32 * EPV;                  // ids per vector row of the warp
+    constexpr int NIT = PIECE / (kIV * RV);       // iterations per piece (8)
+    constexpr int NV = NIT * kIV;                 // vectors per lane per piece (32)
     constexpr int NBP = PIECE >> kNoiseBlockShift;  // noise blocks per piece (bf16 32, fp32 16)
-    constexpr int VPB = (1 << kNoiseBlockShift) / (32 * EPV);  // vector rows per block (bf16 1, fp32 2)
-    static_assert(NIT * ITV * EPV == PIECE && NBP <= 32, "piece layout");
+    static_assert(NIT * kIV * RV == PIECE && NBP <= 32 && NV == 32, "piece layout");
     __shared__ uint32_t s_pbm[PENALTY ? kPW * (PIECE / 32) : 1];  // per-warp penalty bitmap of the piece
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -543,22 +553,29 @@ __global__ void __launch_bounds__(kPT, 2) verify_piece_kernel(const VerifyDev P)
     nk.seq = static_cast<uint32_t>(b);
 
     // the first iteration's loads go out before anything else
-    const int ebase = v0 + lane * EPV;  // id of element 0 of my vector (it, 0)
+    const int ebase = v0 + lane * EPV;  // id of element 0 of my vector 0
     auto load_it = [&](int it, uint4* dst) {
 #pragma unroll
         for (int i = 0; i < kIV; ++i) {
-            const int e0 = ebase + (it * kIV + i) * 32 * EPV;
+            const int e0 = ebase + (it * kIV + i) * RV;
             dst[i] = e0 < v1 ? load_vec<BF16>(rowp, e0, v1, P.aligned) : make_uint4(0u, 0u, 0u, 0u);
         }
     };
     uint4 rv[kIV], rn[kIV];
     load_it(0, rn);
 
-    // noise of my block (lane q: block q of the piece)
+    // noise of block q (lane q) and its argmin element, loaded now and scored after phase A
     BlockNoise bn{};
     RowPhilox rp{};
+    float xI = 0.0f;
+    int vI = -1;
     if (cand) {
-        if (lane < NBP) bn = block_noise(nk, static_cast<uint32_t>((v0 >> kNoiseBlockShift) + lane), static_cast<uint32_t>(j));
+        if (lane < NBP) {
+            bn = block_noise(nk, static_cast<uint32_t>((v0 >> kNoiseBlockShift) + lane), static_cast<uint32_t>(j));
+            vI = v0 + (lane << kNoiseBlockShift) + bn.I;
+            if (vI < v1) xI = static_cast<float>(raw_logit_f64<BF16>(P.logits, row, P.V, vI));
+            else vI = -1;
+        }
         rp = row_philox(nk, static_cast<uint32_t>(j));
     }
     // penalty window of row j: the last W tokens of history ++ d_1..d_j, as a bitmap of the piece
@@ -583,59 +600,55 @@ __global__ void __launch_bounds__(kPT, 2) verify_piece_kernel(const VerifyDev P)
         anypen = __any_sync(0xffffffffu, mine);
         __syncwarp();
     }
+    auto pen_at = [&](int v) -> bool {  // is id v (inside the piece) penalised?
+        if constexpr (PENALTY) {
+            const int o = v - v0;
+            return anypen && ((pbm[o >> 5] >> (o & 31)) & 1u);
+        }
+        return false;
+    };
 
-    unsigned* gthr = P.row_thr + row;  // the row's best score (score_key; 0 = none)
-    float thr = -INFINITY;
     float mref = -INFINITY, s = 0.0f, m = -INFINITY;
     Top2 tt = top2_empty();
-    unsigned pub = 0u;           // best key this warp has published
-    unsigned gk = 0u;            // the row's best, read one iteration ahead
+    float gth = -INFINITY;         // greedy: the best value so far, less the tie margin
+    uint32_t vmx[NV / 2];          // phase A: bf16 maxima of my vectors, two per register
+    unsigned penv = 0u;            // my vectors that hold a penalised element
+    float lbest = -INFINITY;       // my largest raw value and the vector holding it
+    int lbk = -1;
 
+    // ================= phase A =================
+#pragma unroll 1
     for (int it = 0; it < NIT; ++it) {
 #pragma unroll
         for (int i = 0; i < kIV; ++i) rv[i] = rn[i];
         if (it + 1 < NIT) load_it(it + 1, rn);
-        if (!GREEDY && cand && it > 0) {
-            const float best = key_score(gk);
-            if (best > -INFINITY) thr = fmaxf(thr, best - cand_delta(best));
-        }
-        if (!GREEDY && cand && lane == 0) gk = __ldcg(gthr);  // used next iteration
-        gk = __shfl_sync(0xffffffffu, gk, 0);
-        const int ib = ebase + it * kIV * 32 * EPV;  // id of element 0 of my vector (it, 0)
-        const bool full = ib + (kIV - 1) * 32 * EPV + EPV <= v1;
-        // penalised elements of my lane in this iteration (bit 8 i + e)
-        unsigned pmk = 0u;
+        const int ib = ebase + it * kIV * RV;
+        const bool full = ib + (kIV - 1) * RV + EPV <= v1;
+        unsigned pmk = 0u;  // penalised elements of this iteration (bit 8 i + e)
         if constexpr (PENALTY) {
             if (anypen) {
 #pragma unroll
                 for (int i = 0; i < kIV; ++i) {
-                    const int off = ib + i * 32 * EPV - v0;
+                    const int off = ib + i * RV - v0;
                     if (off < PIECE) pmk |= ((pbm[off >> 5] >> (off & 31)) & ((1u << EPV) - 1u)) << (8 * i);
                 }
             }
         }
-
-        // ---- streaming
-        float zl = -INFINITY, lraw = -INFINITY;
-        uint32_t hv[kIV];
+        float vm[kIV];
+        float zl = -INFINITY;
         if (full) {
-            if constexpr (BF16) {
 #pragma unroll
-                for (int i = 0; i < kIV; ++i) hv[i] = as_u32(bf16x8_max2(rv[i]));
-                const uint32_t h = as_u32(__hmax2(__hmax2(as_bf162(hv[0]), as_bf162(hv[1])),
-                                                  __hmax2(as_bf162(hv[2]), as_bf162(hv[3]))));
-                lraw = fmaxf(bf16lo(h), bf16hi(h));
-            } else {
-#pragma unroll
-                for (int i = 0; i < kIV; ++i) {
-                    const float f = fmaxf(fmaxf(__uint_as_float(rv[i].x), __uint_as_float(rv[i].y)),
-                                          fmaxf(__uint_as_float(rv[i].z), __uint_as_float(rv[i].w)));
-                    hv[i] = __float_as_uint(f);
-                    lraw = fmaxf(lraw, f);
+            for (int i = 0; i < kIV; ++i) {
+                if constexpr (BF16) {
+                    const uint32_t h = as_u32(bf16x8_max2(rv[i]));
+                    vm[i] = fmaxf(bf16lo(h), bf16hi(h));
+                } else {
+                    vm[i] = fmaxf(fmaxf(__uint_as_float(rv[i].x), __uint_as_float(rv[i].y)),
+                                  fmaxf(__uint_as_float(rv[i].z), __uint_as_float(rv[i].w)));
                 }
             }
+            const float lraw = fmaxf(fmaxf(vm[0], vm[1]), fmaxf(vm[2], vm[3]));
             zl = SOFTCAP ? transform_f32<true, false>(lraw, false, P) : lraw;
-            m = fmaxf(m, zl);
             if constexpr (!GREEDY) {
                 if (!(mref > -INFINITY)) mref = zl;
                 const float msc = mref * P.sc;
@@ -677,20 +690,10 @@ __global__ void __launch_bounds__(kPT, 2) verify_piece_kernel(const VerifyDev P)
                 while (pw != 0u) {
                     const int bit = __ffs(pw) - 1;
                     pw &= pw - 1u;
-                    float xx[EPV];
-                    uint4 r = rv[0];
-#pragma unroll
-                    for (int i = 1; i < kIV; ++i)
-                        if ((bit >> 3) == i) r = rv[i];
-                    unpack<BF16>(r, xx);
-                    float xe = xx[0];
-#pragma unroll
-                    for (int e = 1; e < EPV; ++e)
-                        if ((bit & 7) == e) xe = xx[e];
+                    const float xe = static_cast<float>(raw_logit_f64<BF16>(P.logits, row, P.V, ib + (bit >> 3) * RV + (bit & 7)));
                     const float zu = transform_f32<SOFTCAP, false>(xe, false, P);
                     const float zp = transform_f32<SOFTCAP, true>(xe, true, P);
                     zl = fmaxf(zl, zp);
-                    m = fmaxf(m, zp);
                     if constexpr (!GREEDY) {
                         if ((zp - mref) * P.sc > 32.0f) {
                             s *= ex2_approx((mref - zp) * P.sc);
@@ -705,8 +708,8 @@ __global__ void __launch_bounds__(kPT, 2) verify_piece_kernel(const VerifyDev P)
             // partial vectors (a row's last piece): exact transform element by element
 #pragma unroll
             for (int i = 0; i < kIV; ++i) {
-                hv[i] = BF16 ? 0xFF80FF80u : __float_as_uint(-INFINITY);
-                const int e0 = ib + i * 32 * EPV;
+                vm[i] = -INFINITY;
+                const int e0 = ib + i * RV;
                 const int nv = min(EPV, v1 - e0);
                 if (nv <= 0) continue;
                 float x[EPV];
@@ -715,9 +718,8 @@ __global__ void __launch_bounds__(kPT, 2) verify_piece_kernel(const VerifyDev P)
                 for (int e = 0; e < EPV; ++e) {
                     if (e >= nv) break;
                     const float z = transform_f32<SOFTCAP, PENALTY>(x[e], (pmk >> (8 * i + e)) & 1u, P);
-                    lraw = fmaxf(lraw, x[e]);
+                    vm[i] = fmaxf(vm[i], x[e]);
                     zl = fmaxf(zl, z);
-                    m = fmaxf(m, z);
                     if constexpr (!GREEDY) {
                         if (!(mref > -INFINITY) || (z - mref) * P.sc > 32.0f) {
                             s = mref > -INFINITY ? s * ex2_approx((mref - z) * P.sc) : 0.0f;
@@ -728,18 +730,36 @@ __global__ void __launch_bounds__(kPT, 2) verify_piece_kernel(const VerifyDev P)
                 }
             }
         }
-
-        // ---- candidates
+        m = fmaxf(m, zl);
+        // bookkeeping of the vectors for phase B: bf16 upper bounds of the raw maxima,
+        // the vectors with a penalised element, my largest value and its vector
+#pragma unroll
+        for (int i = 0; i < kIV; i += 2) {
+            const uint32_t lo = BF16 ? (__float_as_uint(vm[i]) >> 16) : bf16_ceil_bits(vm[i]);
+            const uint32_t hi = BF16 ? (__float_as_uint(vm[i + 1]) >> 16) : bf16_ceil_bits(vm[i + 1]);
+            vmx[(it * kIV + i) >> 1] = lo | (hi << 16);
+        }
+#pragma unroll
+        for (int i = 0; i < kIV; ++i) {
+            if ((pmk >> (8 * i)) & 0xFFu) penv |= 1u << (it * kIV + i);
+            if (vm[i] > lbest) {
+                lbest = vm[i];
+                lbk = it * kIV + i;
+            }
+        }
         if constexpr (GREEDY) {
             // top two transformed values (lower id on ties) within cand_delta of the best
             // value seen; without a penalty the lane maximum is itself a value of the row
-            float gth = tt.s1;
-            if constexpr (!PENALTY) gth = fmaxf(gth, key_score(warp_best_key(zl)));
-            gth = gth > -INFINITY ? gth - cand_delta(gth) : -INFINITY;
+            float g = fmaxf(gth, tt.s1 > -INFINITY ? tt.s1 - cand_delta(tt.s1) : -INFINITY);
+            if constexpr (!PENALTY) {
+                const float wb = key_score(warp_best_key(zl));
+                if (wb > -INFINITY) g = fmaxf(g, wb - cand_delta(wb));
+            }
+            gth = g;
             if (zl >= gth) {
 #pragma unroll
                 for (int i = 0; i < kIV; ++i) {
-                    const int e0 = ib + i * 32 * EPV;
+                    const int e0 = ib + i * RV;
                     const int nv = min(EPV, v1 - e0);
                     if (nv <= 0) continue;
                     float x[EPV];
@@ -755,141 +775,128 @@ __global__ void __launch_bounds__(kPT, 2) verify_piece_kernel(const VerifyDev P)
                     }
                 }
             }
-        } else if (cand) {
-            int seeded = -1;
-            if (it == 0) {
-                // seed: the lane holding the warp's largest raw element scores it (any exact
-                // score bounds the best from below); lowest position among equal maxima
-                const unsigned ku = lraw > -INFINITY ? score_key(lraw) : 0u;
+        }
+    }
+
+    if (!GREEDY && cand) {
+        // ---- exact scores that need no per-id draw: each block's argmin element
+        if (vI >= 0 && vI != excl) {
+            const float zb = transform_f32<SOFTCAP, PENALTY>(xI, pen_at(vI), P) * P.invT;
+            top2_push(tt, zb - bn.lnM, vI);
+        }
+        // ---- the warp's four largest values (their lanes score them)
+        int sv = -1;  // the id this lane scored
+        {
+            unsigned ku = lbest > -INFINITY ? score_key(lbest) : 0u;
+            bool pick = false;
+#pragma unroll
+            for (int r = 0; r < kTop; ++r) {
                 const unsigned kmax = __reduce_max_sync(0xffffffffu, ku);
-                const unsigned own = __ballot_sync(0xffffffffu, kmax != 0u && ku == kmax);
-                const int sl = own != 0u ? __ffs(own) - 1 : 0;
-                int am = -1;  // 8 i + e of the maximum in lane sl
-                if (own != 0u && lane == sl) {
-#pragma unroll
-                    for (int i = kIV - 1; i >= 0; --i) {
-                        const int nv = min(EPV, v1 - (ib + i * 32 * EPV));
-                        float x[EPV];
-                        unpack<BF16>(rv[i], x);
-#pragma unroll
-                        for (int e = EPV - 1; e >= 0; --e)
-                            if (e < nv && x[e] == lraw) am = i * 8 + e;
-                    }
+                if (kmax == 0u) break;
+                const unsigned own = __ballot_sync(0xffffffffu, ku == kmax);
+                if (lane == __ffs(own) - 1) {
+                    pick = true;
+                    ku = 0u;
                 }
-                am = __shfl_sync(0xffffffffu, am, sl);
-                int sv = am >= 0 ? v0 + sl * EPV + (am >> 3) * 32 * EPV + (am & 7) : -1;
+            }
+            int q = 0;
+            float M = 0.0f;
+            int I = 0;
+            if (pick) {
+                // locate the value in its vector (lowest id among equal values), then score it
+                const int e0 = ebase + lbk * RV;
+                const uint4 r = load_vec<BF16>(rowp, e0, v1, P.aligned);
+                float x[EPV];
+                unpack<BF16>(r, x);
+                int e = -1;
+#pragma unroll
+                for (int k = EPV - 1; k >= 0; --k)
+                    if (e0 + k < v1 && x[k] == lbest) e = k;
+                sv = e >= 0 ? e0 + e : -1;
                 if (sv == excl) sv = -1;
-                float t0 = -INFINITY;
+                q = sv >= 0 ? (sv - v0) >> kNoiseBlockShift : 0;
+            }
+            M = __shfl_sync(0xffffffffu, bn.M, q);
+            I = __shfl_sync(0xffffffffu, bn.I, q);
+            if (__any_sync(0xffffffffu, sv >= 0)) {
+                const float E = noise_exp_f32(rp, M, I, static_cast<uint32_t>(sv < 0 ? 0 : sv));
                 if (sv >= 0) {
-                    const int q = ((sv - v0) >> kNoiseBlockShift);
-                    const float Mq = __shfl_sync(0xffffffffu, bn.M, q);
-                    const int Iq = __shfl_sync(0xffffffffu, bn.I, q);
-                    if (lane == sl) {
-                        float xx[EPV];
-                        uint4 r = rv[0];
-#pragma unroll
-                        for (int i = 1; i < kIV; ++i)
-                            if ((am >> 3) == i) r = rv[i];
-                        unpack<BF16>(r, xx);
-                        float xe = xx[0];
-#pragma unroll
-                        for (int e = 1; e < EPV; ++e)
-                            if ((am & 7) == e) xe = xx[e];
-                        const float z = transform_f32<SOFTCAP, PENALTY>(xe, (pmk >> am) & 1u, P);
-                        t0 = z * P.invT - ln_fast(noise_exp_f32(rp, Mq, Iq, static_cast<uint32_t>(sv)));
-                        top2_push(tt, t0, sv);
-                        seeded = sv;
-                    }
-                }
-                const unsigned k0 = warp_best_key(t0);
-                if (k0 != 0u) {
-                    const float b0 = key_score(k0);
-                    thr = fmaxf(thr, b0 - cand_delta(b0));
-                    if (lane == 0 && k0 > pub) atomicMax(gthr, k0);
-                    pub = max(pub, k0);
+                    const float zb = transform_f32<SOFTCAP, PENALTY>(lbest, pen_at(sv), P) * P.invT;
+                    // the argmin element is already in; its score here is the same
+                    if (static_cast<int>(static_cast<uint32_t>(sv) & kNoiseBlockMask) != I)
+                        top2_push(tt, zb - ln_fast(E), sv);
+                    else
+                        sv = -1;
                 }
             }
-            // block tests: every score of vector i is at most z / T - ln M of its block
-            unsigned msk = 0u;
+        }
+        // ---- publish the warp's best to the row, read back the row's best
+        unsigned* gthr = P.row_thr + row;
+        const unsigned kw = warp_best_key(tt.s1);
+        unsigned kg = 0u;
+        if (lane == 0) {
+            if (kw != 0u) atomicMax(gthr, kw);
+            kg = __ldcg(gthr);
+        }
+        kg = __shfl_sync(0xffffffffu, max(kg, kw), 0);
+        const float best = key_score(kg);
+        float thr = best > -INFINITY ? best - cand_delta(best) : -INFINITY;
+
+        // ================= phase B =================
+        // lane q (block q) turns the best into a raw-value bound for its block, packed
+        // twice: element x of block q can reach the best only if x >= xt_q
+        uint32_t xt2 = 0u;
+        {
+            const float zt = (thr + bn.lnM) * P.T;
+            float xt = zt;
+            if constexpr (SOFTCAP) {
+                // shrink by more than the fp32 error of c tanh(x / c) before inverting:
+                // atanh is steep near |u| = 1
+                float u = zt * P.invcap;
+                u -= 1e-6f * fabsf(u) + 1e-7f;
+                xt = u > 1.0f ? INFINITY : (u <= -1.0f ? -INFINITY : P.cap * atanhf(fminf(u, 1.0f - 1e-7f)));
+            }
+            xt -= 1e-5f * (1.0f + fabsf(xt));  // slack for the rounding of the transform
+            if (!(thr > -INFINITY)) xt = -INFINITY;
+            xt2 = bf16x2_floor(xt);
+        }
+        // vector k of a lane lies in block k * EPV / 8; two vectors per test
+        unsigned pv = penv;
 #pragma unroll
-            for (int i = 0; i < kIV; ++i) {
-                const int q = (it * kIV + i) / VPB;  // block of vector i (warp-uniform)
-                const float lnM = __shfl_sync(0xffffffffu, bn.lnM, q);
-                float zv;
-                if constexpr (BF16) zv = fmaxf(bf16lo(hv[i]), bf16hi(hv[i]));
-                else zv = __uint_as_float(hv[i]);
-                if (SOFTCAP && full) zv = transform_f32<true, false>(zv, false, P);
-                const unsigned pb = (pmk >> (8 * i)) & 0xFFu;
-                const float zvb = zv * P.invT;
-                const bool vp = pb != 0u || !full || zvb - lnM + bound_slack(zvb) >= thr;
-                if (__any_sync(0xffffffffu, vp)) {
-                    unsigned mi = 0u;
-                    if (vp) {
-                        if (full) {
-                            // z >= T (thr + ln M), in raw units
-                            const float zt = (thr + lnM) * P.T;
-                            float xt = zt;
-                            if constexpr (SOFTCAP) {
-                                // shrink by more than the fp32 error of c tanh(x / c) before
-                                // inverting: atanh is steep near |u| = 1
-                                float u = zt * P.invcap;
-                                u -= 1e-6f * fabsf(u) + 1e-7f;
-                                xt = u > 1.0f ? INFINITY : (u <= -1.0f ? -INFINITY : P.cap * atanhf(fminf(u, 1.0f - 1e-7f)));
-                            }
-                            xt -= 1e-5f * (1.0f + fabsf(xt));  // slack for the rounding of the transform
-                            if constexpr (BF16) {
-                                mi = bf16x8_ge_bits(rv[i], bf16x2_floor(xt));
-                            } else {
-                                mi = static_cast<unsigned>(__uint_as_float(rv[i].x) >= xt);
-                                mi |= static_cast<unsigned>(__uint_as_float(rv[i].y) >= xt) << 1;
-                                mi |= static_cast<unsigned>(__uint_as_float(rv[i].z) >= xt) << 2;
-                                mi |= static_cast<unsigned>(__uint_as_float(rv[i].w) >= xt) << 3;
-                            }
-                            mi |= pb;  // penalised: tested exactly below
-                        } else {
-                            const int nv = min(EPV, v1 - (ib + i * 32 * EPV));
-                            mi = nv > 0 ? (1u << nv) - 1u : 0u;
-                        }
-                    }
-                    msk |= mi << (8 * i);
-                }
+        for (int k2 = 0; k2 < NV / 2; ++k2) {
+            const int q0 = (2 * k2) * EPV / 8, q1 = (2 * k2 + 1) * EPV / 8;
+            const uint32_t t0 = __shfl_sync(0xffffffffu, xt2, q0), t1 = __shfl_sync(0xffffffffu, xt2, q1);
+            const uint32_t th = (t0 & 0xFFFFu) | (t1 & 0xFFFF0000u);
+            const unsigned mk = __hge2_mask(as_bf162(vmx[k2]), as_bf162(th));
+            pv |= ((mk & 1u) | ((mk >> 15) & 2u)) << (2 * k2);
+        }
+        pv &= (ebase < v1 ? 0xFFFFFFFFu : 0u);  // (a lane wholly past the end has nothing)
+        // the passing vectors: reload, bound each element exactly, score the survivors
+        while (__any_sync(0xffffffffu, pv != 0u)) {
+            int k = -1;
+            uint4 r = make_uint4(0u, 0u, 0u, 0u);
+            if (pv != 0u) {
+                k = __ffs(pv) - 1;
+                pv &= pv - 1u;
+                const int e0 = ebase + k * RV;
+                if (e0 < v1) r = load_vec<BF16>(rowp, e0, v1, P.aligned);
+                else k = -1;
             }
-            if (seeded >= 0) {
-                const int so = seeded - ib;
-                const int si = so / (32 * EPV), se = so - si * 32 * EPV;
-                if (so >= 0 && se >= 0 && se < EPV) msk &= ~(1u << (8 * si + se));
-            }
-            if (excl >= ib && excl < ib + kIV * 32 * EPV) {
-                const int so = excl - ib;
-                const int si = so / (32 * EPV), se = so - si * 32 * EPV;
-                if (se >= 0 && se < EPV) msk &= ~(1u << (8 * si + se));
-            }
-            // score the lane's candidates one per iteration, the warp in step
-            while (__any_sync(0xffffffffu, msk != 0u)) {
-                int v = -1, bi = 0;
+            float x[EPV];
+            unpack<BF16>(r, x);
+            const int q = k >= 0 ? (k * EPV) >> 3 : 0;
+            const float Mq = __shfl_sync(0xffffffffu, bn.M, q);
+            const float lnq = __shfl_sync(0xffffffffu, bn.lnM, q);
+            const int Iq = __shfl_sync(0xffffffffu, bn.I, q);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) {
+                const int v = k >= 0 ? ebase + k * RV + e : -1;
+                bool live = false;
                 float zb = -INFINITY;
-                if (msk != 0u) {
-                    const int bit = __ffs(msk) - 1;
-                    msk &= msk - 1u;
-                    bi = bit >> 3;
-                    float xx[EPV];
-                    uint4 r = rv[0];
-#pragma unroll
-                    for (int i = 1; i < kIV; ++i)
-                        if (bi == i) r = rv[i];
-                    unpack<BF16>(r, xx);
-                    float xe = xx[0];
-#pragma unroll
-                    for (int e = 1; e < EPV; ++e)
-                        if ((bit & 7) == e) xe = xx[e];
-                    zb = transform_f32<SOFTCAP, PENALTY>(xe, (pmk >> bit) & 1u, P) * P.invT;
-                    v = ib + bi * 32 * EPV + (bit & 7);
+                if (v >= 0 && v < v1 && v != excl && v != sv && static_cast<int>(static_cast<uint32_t>(v) & kNoiseBlockMask) != Iq) {
+                    zb = transform_f32<SOFTCAP, PENALTY>(x[e], pen_at(v), P) * P.invT;
+                    live = zb - lnq + bound_slack(zb) >= thr;
                 }
-                const int q = (it * kIV + bi) / VPB;  // my candidate's block (per lane)
-                const float Mq = __shfl_sync(0xffffffffu, bn.M, q);
-                const float lnMq = __shfl_sync(0xffffffffu, bn.lnM, q);
-                const int Iq = __shfl_sync(0xffffffffu, bn.I, q);
-                const bool live = v >= 0 && v != excl && zb - lnMq + bound_slack(zb) >= thr;
                 if (__any_sync(0xffffffffu, live)) {
                     const float E = noise_exp_f32(rp, Mq, Iq, static_cast<uint32_t>(v < 0 ? 0 : v));
                     if (live) {
@@ -901,15 +908,9 @@ __global__ void __launch_bounds__(kPT, 2) verify_piece_kernel(const VerifyDev P)
                     }
                 }
             }
-            // publish the warp's best when it improved
-            const unsigned kw = warp_best_key(tt.s1);
-            if (kw > pub) {
-                const float bw = key_score(kw);
-                thr = fmaxf(thr, bw - cand_delta(bw));
-                if (lane == 0) atomicMax(gthr, kw);
-                pub = kw;
-            }
         }
+        const unsigned kw2 = warp_best_key(tt.s1);
+        if (lane == 0 && kw2 > kw) atomicMax(gthr, kw2);
     }
 
     // ---- the piece's partial, then the row merge if this warp completes the row
