@@ -68,7 +68,7 @@ struct WsLayout {
 };
 
 // The f32 chunks are the smaller ones, so their counts bound both dtypes.
-int max_chunks(int V) { return (V + piece_elems<false>() - 1) / piece_elems<false>(); }
+int max_chunks(int V) { return (V + chunk_elems<false>() - 1) / chunk_elems<false>(); }
 int max_chunks2(int V) { return (V + res_chunk_elems<false>() - 1) / res_chunk_elems<false>(); }
 
 WsLayout ws_layout(int B, int K, int V) {
@@ -279,12 +279,11 @@ int spec_verify(const void* logits, int logits_dtype, int B, int K, int V, const
     const WsLayout L = ws_layout(B, K, V);
     if (workspace_bytes < L.total) return fail(SPECNG_ESMALL, "spec_verify: workspace too small");
     const bool bf16 = logits_dtype == SPECNG_BF16;
-    const int chunk = bf16 ? piece_elems<true>() : piece_elems<false>();
+    const int chunk = bf16 ? chunk_elems<true>() : chunk_elems<false>();
     const int nchunk = (V + chunk - 1) / chunk;
     const int chunk2 = bf16 ? res_chunk_elems<true>() : res_chunk_elems<false>();
     const int nchunk2 = (V + chunk2 - 1) / chunk2;
-    if (static_cast<int64_t>(B) * (K + 1) * nchunk2 > 0x7FFFFFFFLL ||
-        (static_cast<int64_t>(B) * (K + 1) * nchunk + kPW - 1) / kPW > 0x7FFFFFFFLL)
+    if (static_cast<int64_t>(B) * (K + 1) * nchunk2 > 0x7FFFFFFFLL)
         return fail(SPECNG_EINVAL, "spec_verify: B * (K + 1) * chunks exceeds the grid limit");
 
     const bool greedy = p.temperature == 0.0f;

@@ -30,7 +30,7 @@ template <> struct ElemTraits<false> { static constexpr int EPV = 4; static cons
 
 // One chunk of a row = one 64 KB stage of the streaming ring; the residual
 // pass takes 32 KB chunks, one per CTA.
-constexpr int kChunkBytes = 65536;
+constexpr int kChunkBytes = 32768;
 constexpr int kResChunkBytes = 32768;
 template <bool BF16>
 __host__ __device__ constexpr int chunk_elems() { return kChunkBytes / ElemTraits<BF16>::SIZE; }
@@ -474,188 +474,451 @@ __device__ __noinline__ void merge_row(const VerifyDev& P, int row) {
 }
 
 // ---------------------------------------------------------------- K1
-// One warp per piece of a row.  The active rows of the call (rows 0..k_eff of
-// every sequence) are cut into pieces of 16 KB; each warp reads its piece from
-// HBM once and leaves one partial (maximum, sum of exponentials, top-two
-// sampling candidates).  The warp that finishes a row's last piece (atomic
-// ticket) merges the row at once; the last row of a sequence (second ticket)
-// runs the epilogue.  Warps never wait on each other.
-//
-// Sampling in two phases per warp.  A piece holds 32 noise blocks of 256 ids
-// (bf16; 16 for fp32); lane q draws block q's minimum M_q and its slot I_q.
-//   A  streams the piece with 16-byte loads (the next iteration's in flight):
-//      sum of exponentials, and the maximum of every 16-byte vector, kept in
-//      registers as bf16 (rounded up for fp32 data).  Meanwhile each block's
-//      argmin element is loaded: its score z / T - ln M_q is exact without a
-//      per-id draw.  After the stream the lanes holding the warp's four largest
-//      values score them.  The best of these exact scores is published to the
-//      row's shared best (global atomic maximum) and read back.
-//   B  every score of a vector is at most (its maximum) / T - ln M of its block,
-//      so the vector maxima in registers are tested against the best without
-//      touching the data; the few vectors that pass are reloaded (from L2) and
-//      their surviving elements scored (per-id Philox draw, E_v = M + F_v).
+// Persistent, warp-specialised streaming kernel.  One CTA per SM; the active
+// row-chunks of the call (rows 0..k_eff of every sequence, chunks of 64 KB)
+// are laid out row-major and split into equal contiguous ranges, one per CTA.
+//   * A producer warp walks the CTA's range and keeps up to kStages chunks in
+//     flight with cp.async.bulk into a shared-memory ring (full / empty
+//     mbarriers, bounded waits).  It draws the noise of a chunk's 256-id
+//     blocks before the chunk's ring slot is free, and writes the row's
+//     metadata, the penalty bitmap and the noise while the copy is in flight.
+//   * Sixteen streaming warps each own a 4 KB slice of every chunk.  A lane's
+//     16-byte vector i of a bf16 chunk covers 8 ids of noise block 8 w + i, so
+//     its packed maximum gives the block test z / T - ln M >= best for its
+//     eight ids at once; a single test of the lane's maximum against the
+//     smallest ln M of the slice gates them.  Per slice: packed maxima, the
+//     exponentials of the sum, the block tests; only the vectors that pass
+//     compare their elements, and each lane scores its few survivors
+//     (per-id Philox draw, E_v, score) in step with the warp.  At the first
+//     chunk of a row segment each lane scores its largest element, which
+//     starts the segment's best; the warps of the CTA share the best through
+//     shared memory.
+//   * A merge warp runs the row merges: the CTA that completes a row (atomic
+//     ticket over the row's chunks) queues it, and the merge warp combines the
+//     row's partials, takes the accept test and, for the last row of a
+//     sequence (second ticket), runs the epilogue.  Nothing waits on another
+//     CTA.
 
-constexpr int kPieceBytes = 16384;
-constexpr int kPW = 8;           // warps per CTA
-constexpr int kPT = kPW * 32;    // threads per CTA
-constexpr int kIV = 4;           // 16-byte vectors per lane per iteration
-constexpr int kTop = 4;          // largest values scored after phase A
+constexpr int kCWarps = 16;                    // streaming warps
+constexpr int kPWarp = kCWarps;                // producer warp index
+constexpr int kMWarp = kCWarps + 1;            // merge warp index
+constexpr int kPThreads = (kCWarps + 2) * 32;  // 576
+constexpr int kStages = 6;
+constexpr int kVL = 4;                         // 16-byte vectors per lane per chunk
+constexpr int kMaxBlk = kChunkBytes / 2 >> kNoiseBlockShift;  // noise blocks per chunk (bf16: 128)
+constexpr int kMQ = 16;                        // merge-queue entries per streaming warp
+static_assert(kChunkBytes == kCWarps * 32 * kVL * 16, "stage layout");
+static_assert((32 * 8) == (1 << kNoiseBlockShift), "a bf16 vector row of a warp is one noise block");
 
-template <bool BF16>
-__host__ __device__ constexpr int piece_elems() { return kPieceBytes / ElemTraits<BF16>::SIZE; }
-
-// Smallest bf16 value >= f (an upper bound in bf16), as the low 16 bits.
-__device__ __forceinline__ uint32_t bf16_ceil_bits(float f) {
-    const uint32_t u = __float_as_uint(f);
-    uint32_t h = u >> 16;
-    if ((u & 0xFFFFu) != 0u && !(u & 0x80000000u) && (u & 0x7FFFFFFFu) < 0x7F800000u) h += 1u;  // positive: up
-    return h;
+template <bool PENALTY>
+__host__ __device__ constexpr size_t k1_dyn_smem() {
+    return static_cast<size_t>(kStages) * kChunkBytes +
+           (PENALTY ? static_cast<size_t>(kStages) * (kChunkBytes / 2 / 8) : 0);
 }
 
+struct StageMeta {
+    int b, j, c, excl, seg_end;  // seg_end: the last chunk of this row in the CTA's range
+    int cand;                    // the row's Gumbel candidates can be the emitted token
+    unsigned penw;               // bit w: warp w's slice holds a penalised id
+    int pad;
+    float wmin[kCWarps];         // smallest ln M of each warp's slice
+    BlockNoise bn[kMaxBlk];      // noise of the chunk's 256-id blocks
+};
+
+struct WarpPart {
+    float m, s;
+    Top2 t;
+};
+
 template <bool BF16, bool GREEDY, bool SOFTCAP, bool PENALTY>
-__global__ void __launch_bounds__(kPT, 2) verify_piece_kernel(const VerifyDev P) {
+__global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const VerifyDev P) {
     constexpr int EPV = ElemTraits<BF16>::EPV;
-    constexpr int PIECE = piece_elems<BF16>();
-    constexpr int RV = 32 * EPV;                  // ids per vector row of the warp
-    constexpr int NIT = PIECE / (kIV * RV);       // iterations per piece (8)
-    constexpr int NV = NIT * kIV;                 // vectors per lane per piece (32)
-    constexpr int NBP = PIECE >> kNoiseBlockShift;  // noise blocks per piece (bf16 32, fp32 16)
-    static_assert(NIT * kIV * RV == PIECE && NBP <= 32 && NV == 32, "piece layout");
-    __shared__ uint32_t s_pbm[PENALTY ? kPW * (PIECE / 32) : 1];  // per-warp penalty bitmap of the piece
+    constexpr int CHUNK = chunk_elems<BF16>();
+    constexpr int SB = kChunkBytes;
+    constexpr int SL = 32 * kVL * EPV;  // ids per streaming slice
+    constexpr int NB = CHUNK >> kNoiseBlockShift;
+    constexpr int BPW = NB / kCWarps;   // noise blocks per slice
+    extern __shared__ __align__(128) uint8_t s_dyn[];
+    uint8_t* s_stage = s_dyn;
+    uint32_t* s_bm = reinterpret_cast<uint32_t*>(s_dyn + kStages * SB);
+    __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages];
+    __shared__ StageMeta s_meta[kStages];
+    __shared__ WarpPart s_slot[kStages][kCWarps];
+    __shared__ int s_cnt[kStages];
+    __shared__ unsigned s_rthr[kStages + 1];  // per-segment best score (score_key; 0 = none)
+    __shared__ long long s_wsum[kPThreads / 32];
+    __shared__ int s_start[3];
+    __shared__ int s_hwin[PENALTY ? SPECNG_MAX_REP_WINDOW : 1];
+    __shared__ int s_pdrafts[SPECNG_MAX_K + 1];
+    __shared__ volatile int s_mq[kCWarps][kMQ];  // rows to merge, per streaming warp (single producer / consumer)
+    __shared__ volatile int s_mq_tail[kCWarps];
+    __shared__ volatile int s_mq_head[kCWarps];
+    __shared__ int s_done;
 
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int K1 = P.K + 1;
-    const long long item = static_cast<long long>(blockIdx.x) * kPW + warp;
-    const int row = static_cast<int>(item / P.nchunk);
-    const int p = static_cast<int>(item - static_cast<long long>(row) * P.nchunk);
-    if (row >= P.B * K1) return;
-    const int b = row / K1, j = row - b * K1;
-    int kb;
-    const int keff = gate_keff(P, b, &kb, j == 0 && p == 0);
-    if (j > keff) return;
     const bool dense = P.q != nullptr;
-    const int v0 = p * PIECE;
-    const int v1 = min(P.V, v0 + PIECE);
-    const char* rowp = static_cast<const char*>(P.logits) + static_cast<size_t>(row) * P.V * ElemTraits<BF16>::SIZE;
 
-    // the draft this row verifies: excluded from the point-mass residual; with dense q
-    // the residual pass samples the row (unless the draft is invalid: the residual is p)
-    int excl = -1;
-    bool cand = !GREEDY;
-    if (!GREEDY && j < keff) {
-        const int d = P.drafts[b * P.K + j];
-        const bool valid = d >= 0 && d < P.V;
-        if (!valid && p == 0 && lane == 0) raise_status(P.status, SPECNG_DEV_TOKEN_OOR);
-        if (!dense && valid) excl = d;
-        if (dense && valid) cand = false;
-    }
-    NoiseKey nk = P.nk;
-    nk.seq = static_cast<uint32_t>(b);
-
-    // the first iteration's loads go out before anything else
-    const int ebase = v0 + lane * EPV;  // id of element 0 of my vector 0
-    auto load_it = [&](int it, uint4* dst) {
+    // ---- prologue: count the active row-chunks and find this CTA's range
+    const int per = (P.B + kPThreads - 1) / kPThreads;
+    const int bb0 = tid * per;
+    long long mine = 0;
+    for (int b = bb0; b < bb0 + per && b < P.B; ++b) mine += static_cast<long long>(gate_keff(P, b, nullptr, false) + 1) * P.nchunk;
+    long long incl = mine;
 #pragma unroll
-        for (int i = 0; i < kIV; ++i) {
-            const int e0 = ebase + (it * kIV + i) * RV;
-            dst[i] = e0 < v1 ? load_vec<BF16>(rowp, e0, v1, P.aligned) : make_uint4(0u, 0u, 0u, 0u);
-        }
-    };
-    uint4 rv[kIV], rn[kIV];
-    load_it(0, rn);
-
-    // noise of block q (lane q) and its argmin element, loaded now and scored after phase A
-    BlockNoise bn{};
-    RowPhilox rp{};
-    float xI = 0.0f;
-    int vI = -1;
-    if (cand) {
-        if (lane < NBP) {
-            bn = block_noise(nk, static_cast<uint32_t>((v0 >> kNoiseBlockShift) + lane), static_cast<uint32_t>(j));
-            vI = v0 + (lane << kNoiseBlockShift) + bn.I;
-            if (vI < v1) xI = static_cast<float>(raw_logit_f64<BF16>(P.logits, row, P.V, vI));
-            else vI = -1;
-        }
-        rp = row_philox(nk, static_cast<uint32_t>(j));
+    for (int off = 1; off < 32; off <<= 1) {
+        const long long o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
     }
-    // penalty window of row j: the last W tokens of history ++ d_1..d_j, as a bitmap of the piece
-    uint32_t* pbm = s_pbm + (PENALTY ? warp * (PIECE / 32) : 0);
-    bool anypen = false;
-    if constexpr (PENALTY) {
-        for (int t = lane; t < PIECE / 32; t += 32) pbm[t] = 0u;
-        int L = P.lens[b];
-        L = L < 0 ? 0 : (static_cast<int64_t>(L) > P.hist_stride ? static_cast<int>(P.hist_stride) : L);
-        const int total = L + j;
-        const int nw = total < P.W ? total : P.W;
-        __syncwarp();
-        bool mine = false;
-        for (int t = lane; t < nw; t += 32) {
-            const int idx = total - nw + t;
-            const int tok = idx < L ? P.hist[static_cast<size_t>(b) * P.hist_stride + idx] : P.drafts[b * P.K + (idx - L)];
-            if (tok >= v0 && tok < v1) {
-                atomicOr(&pbm[(tok - v0) >> 5], 1u << ((tok - v0) & 31));
-                mine = true;
+    if (lane == 31) s_wsum[warp] = incl;
+    if (tid == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], kCWarps);
+            s_cnt[i] = 0;
+        }
+        for (int i = 0; i <= kStages; ++i) s_rthr[i] = 0u;
+        s_done = 0;
+        mbar_init_fence();
+    }
+    if (tid < kCWarps) {
+        s_mq_tail[tid] = 0;
+        s_mq_head[tid] = 0;
+    }
+    __syncthreads();
+    long long base = 0, total = 0;
+    for (int w = 0; w < kPThreads / 32; ++w) {
+        if (w < warp) base += s_wsum[w];
+        total += s_wsum[w];
+    }
+    const long long G = gridDim.x;
+    const long long w0 = total * blockIdx.x / G, w1 = total * (blockIdx.x + 1) / G;
+    const long long ex = base + incl - mine;  // first row-chunk index of my sequences
+    if (w0 < w1 && w0 >= ex && w0 < ex + mine) {
+        long long acc = ex;
+        for (int b = bb0; b < bb0 + per && b < P.B; ++b) {
+            const long long nb = static_cast<long long>(gate_keff(P, b, nullptr, false) + 1) * P.nchunk;
+            if (w0 < acc + nb) {
+                const long long r = w0 - acc;
+                s_start[0] = b;
+                s_start[1] = static_cast<int>(r / P.nchunk);
+                s_start[2] = static_cast<int>(r % P.nchunk);
+                break;
+            }
+            acc += nb;
+        }
+    }
+    __syncthreads();
+    const int nwork = static_cast<int>(w1 - w0);
+    if (nwork <= 0) return;
+
+    if (warp == kPWarp) {
+        // ================= producer =================
+        // The data of the next sequence (k, EMA, drafts, the tail of its history
+        // for the penalty window) is fetched into registers one sequence ahead,
+        // and its history length two ahead, so no global round trip stalls the
+        // copies at a sequence change.
+        constexpr int kHW = PENALTY ? SPECNG_MAX_REP_WINDOW / 32 : 1;
+        struct SeqData {
+            int k, draft, L;
+            float ema;
+            int hw[kHW];
+        };
+        auto clampL = [&](int L) {
+            return L < 0 ? 0 : (static_cast<int64_t>(L) > P.hist_stride ? static_cast<int>(P.hist_stride) : L);
+        };
+        auto fetch = [&](int bq, int L, SeqData& d) {  // issues the loads; nothing waits here
+            d.k = bq < P.B ? P.k[bq] : 0;
+            d.ema = (P.gate && bq < P.B) ? P.ema[bq] : 1.0f;
+            d.draft = (bq < P.B && lane < P.K) ? P.drafts[bq * P.K + lane] : -1;
+            d.L = L;
+            if constexpr (PENALTY) {
+                const int nh = L < P.W ? L : P.W;
+#pragma unroll
+                for (int i = 0; i < kHW; ++i) {
+                    const int t = lane + 32 * i;
+                    d.hw[i] = (bq < P.B && t < nh) ? P.hist[static_cast<size_t>(bq) * P.hist_stride + (L - nh) + t] : 0;
+                }
+            }
+        };
+        int b = s_start[0], j = s_start[1], c = s_start[2];
+        int kb = 0, keff = 0, nh = 0;
+        auto install = [&](const SeqData& d) {
+            kb = d.k;
+            if (kb < 0 || kb > P.K) {
+                if (lane == 0) raise_status(P.status, SPECNG_DEV_BAD_K);
+                kb = kb < 0 ? 0 : P.K;
+            }
+            keff = (P.gate && kb > 0 && !(d.ema >= P.thresh)) ? 0 : kb;
+            if (lane < keff) {
+                s_pdrafts[lane] = d.draft;
+                if (!(d.draft >= 0 && d.draft < P.V)) raise_status(P.status, SPECNG_DEV_TOKEN_OOR);
+            }
+            if constexpr (PENALTY) {
+                nh = d.L < P.W ? d.L : P.W;
+#pragma unroll
+                for (int i = 0; i < kHW; ++i)
+                    if (lane + 32 * i < nh) s_hwin[lane + 32 * i] = d.hw[i];
+            }
+            __syncwarp();
+        };
+        SeqData cur, nxt;
+        int Lnext2 = 0;
+        {
+            const int L0 = PENALTY ? clampL(P.lens[b]) : 0;
+            const int L1 = (PENALTY && b + 1 < P.B) ? clampL(P.lens[b + 1]) : 0;
+            fetch(b, L0, cur);
+            install(cur);
+            fetch(b + 1, L1, nxt);
+            if (PENALTY && b + 2 < P.B) Lnext2 = P.lens[b + 2];
+        }
+        NoiseKey nk = P.nk;
+        bool ok = true;
+        int st = 0;
+        unsigned eph = 0u;  // parity of the empty barrier phase to wait for
+        for (int n = 0; n < nwork && ok; ++n) {
+            const int v0 = c * CHUNK;
+            const int v1 = min(P.V, v0 + CHUNK);
+            const char* src = static_cast<const char*>(P.logits) +
+                              ((static_cast<size_t>(b) * K1 + j) * P.V + v0) * ElemTraits<BF16>::SIZE;
+            // with dense q, row j < k_eff is sampled by the residual pass unless
+            // its draft is invalid (the residual is then p itself)
+            int excl = -1, cand = 1;
+            if (!GREEDY && j < keff) {
+                const int d = s_pdrafts[j];
+                const bool valid = d >= 0 && d < P.V;
+                if (!dense && valid) excl = d;
+                if (dense && valid) cand = 0;
+            }
+            // the noise of the chunk's blocks (lane q: blocks q, q + 32, ...), before the
+            // ring slot is free
+            constexpr int NBL = (NB + 31) / 32;
+            BlockNoise bnl[NBL];
+            if (!GREEDY && cand) {
+                nk.seq = static_cast<uint32_t>(b);
+                const uint32_t blk0 = static_cast<uint32_t>(v0 >> kNoiseBlockShift);
+#pragma unroll
+                for (int r = 0; r < NBL; ++r)
+                    if (lane + 32 * r < NB) bnl[r] = block_noise(nk, blk0 + lane + 32 * r, static_cast<uint32_t>(j));
+            }
+            if (n >= kStages) ok = mbar_wait_bounded(&s_empty[st], eph);
+            if (!ok) { if (lane == 0) raise_status(P.status, SPECNG_DEV_TIMEOUT); break; }
+            // the copy goes first; the metadata is written while it is in flight, and the
+            // phase completes once both the bytes and the arrive below are in
+            if (P.aligned && lane == 0) {
+                // the empty barrier already orders the consumers' reads of this stage
+                // before the copy that overwrites it
+                mbar_add_tx(&s_full[st], static_cast<unsigned>(v1 - v0) * ElemTraits<BF16>::SIZE);
+                bulk_g2s(s_stage + st * SB, src, static_cast<unsigned>(v1 - v0) * ElemTraits<BF16>::SIZE, &s_full[st]);
+            }
+            StageMeta& mt = s_meta[st];
+            if (lane == 0) {
+                mt.b = b; mt.j = j; mt.c = c; mt.excl = excl;
+                mt.seg_end = (c == P.nchunk - 1 || n == nwork - 1) ? 1 : 0;
+                mt.cand = cand;
+            }
+            if (!GREEDY && cand) {
+#pragma unroll
+                for (int r = 0; r < NBL; ++r)
+                    if (lane + 32 * r < NB) mt.bn[lane + 32 * r] = bnl[r];
+                __syncwarp();
+                if (lane < kCWarps) {
+                    float mn = INFINITY;
+#pragma unroll
+                    for (int q = 0; q < BPW; ++q) mn = fminf(mn, mt.bn[lane * BPW + q].lnM);
+                    mt.wmin[lane] = mn;
+                }
+            }
+            if constexpr (PENALTY) {
+                // bitmap of the penalised ids of row j in [v0, v1), and which slices hold one
+                uint32_t* bm = s_bm + st * (CHUNK / 32);
+                for (int t = lane; t < CHUNK / 32; t += 32) bm[t] = 0u;
+                __syncwarp();
+                const WindowView wv{s_hwin, s_pdrafts, nh, P.W};
+                const int nwin = wv.count(j);
+                unsigned pw = 0u;
+                for (int t = lane; t < nwin; t += 32) {
+                    const int tok = wv.token(j, t);
+                    if (tok >= v0 && tok < v1) {
+                        atomicOr(&bm[(tok - v0) >> 5], 1u << ((tok - v0) & 31));
+                        pw |= 1u << ((tok - v0) / SL);
+                    }
+                }
+                pw = __reduce_or_sync(0xffffffffu, pw);
+                if (lane == 0) mt.penw = pw;
+            } else {
+                if (lane == 0) mt.penw = 0u;
+            }
+            if (!P.aligned) {
+                uint8_t* dst = s_stage + st * SB;
+                for (int e = lane; e < v1 - v0; e += 32) {
+                    if constexpr (BF16) reinterpret_cast<uint16_t*>(dst)[e] = reinterpret_cast<const uint16_t*>(src)[e];
+                    else reinterpret_cast<uint32_t*>(dst)[e] = reinterpret_cast<const uint32_t*>(src)[e];
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_full[st]);
+            if (++st == kStages) {
+                st = 0;
+                if (n >= kStages) eph ^= 1u;  // the waits of ring cycle u (>= 1) are for phase u - 1
+            }
+            // advance to the next row-chunk
+            if (++c == P.nchunk) {
+                c = 0;
+                if (++j > keff) {
+                    j = 0;
+                    ++b;
+                    if (n + 1 < nwork) {
+                        install(nxt);
+                        const int L2 = PENALTY ? clampL(Lnext2) : 0;
+                        fetch(b + 1, L2, nxt);
+                        if (PENALTY && b + 2 < P.B) Lnext2 = P.lens[b + 2];
+                    }
+                }
             }
         }
-        anypen = __any_sync(0xffffffffu, mine);
-        __syncwarp();
-    }
-    auto pen_at = [&](int v) -> bool {  // is id v (inside the piece) penalised?
-        if constexpr (PENALTY) {
-            const int o = v - v0;
-            return anypen && ((pbm[o >> 5] >> (o & 31)) & 1u);
+        // the CTA stays resident until every issued copy has landed
+        if (P.aligned && lane == 0) {
+            const int lo = nwork > kStages ? nwork - kStages : 0;
+            for (int n = lo; n < nwork; ++n) mbar_wait_bounded(&s_full[n % kStages], static_cast<unsigned>((n / kStages) & 1));
         }
-        return false;
-    };
+        return;
+    }
 
-    float mref = -INFINITY, s = 0.0f, m = -INFINITY;
+    if (warp == kMWarp) {
+        // ================= merge warp =================
+        // Polls the streaming warps' queues (lane q watches queue q) until every
+        // streaming warp has finished and every queue is drained.  The wait is bounded.
+        unsigned idle = 0;
+        while (true) {
+            const bool has = lane < kCWarps && s_mq_head[lane] != s_mq_tail[lane];
+            const unsigned qs = __ballot_sync(0xffffffffu, has);
+            if (qs != 0u) {
+                idle = 0;
+                const int q = __ffs(qs) - 1;
+                const int h = s_mq_head[q];
+                const int row = s_mq[q][h % kMQ];
+                __syncwarp();
+                merge_row<BF16, GREEDY, SOFTCAP, PENALTY>(P, row);
+                __syncwarp();
+                if (lane == 0) s_mq_head[q] = h + 1;
+                __syncwarp();
+                continue;
+            }
+            if (*reinterpret_cast<volatile int*>(&s_done) == kCWarps) {
+                // every push happened before its warp's increment of s_done
+                __threadfence_block();
+                const bool again = lane < kCWarps && s_mq_head[lane] != s_mq_tail[lane];
+                if (!__any_sync(0xffffffffu, again)) break;
+                continue;
+            }
+            if (++idle > (1u << 22)) {
+                if (lane == 0) raise_status(P.status, SPECNG_DEV_TIMEOUT);
+                break;
+            }
+            __nanosleep(idle < 64 ? 32 : 256);
+        }
+        return;
+    }
+
+    // ================= streaming warps =================
+    // Per-lane accumulators live across the chunks of one row (a segment of
+    // the CTA's range); warps combine them once, at the segment's last chunk.
+    const int ubase = warp * (32 * kVL);        // first 16-byte vector of my slice
+    const int off0 = ubase * EPV + lane * EPV;  // chunk offset of vector 0's element 0
+    float thr = -INFINITY;
+    float m = -INFINITY, s = 0.0f, msc = 0.0f;
     Top2 tt = top2_empty();
-    float gth = -INFINITY;         // greedy: the best value so far, less the tie margin
-    uint32_t vmx[NV / 2];          // phase A: bf16 maxima of my vectors, two per register
-    unsigned penv = 0u;            // my vectors that hold a penalised element
-    float lbest = -INFINITY;       // my largest raw value and the vector holding it
-    int lbk = -1;
-
-    // ================= phase A =================
-#pragma unroll 1
-    for (int it = 0; it < NIT; ++it) {
+    int seg = 0, cfirst = 0;
+    int row = 0, excl = -1;
+    bool cand = false;
+    RowPhilox rp{};
+    bool fresh = true;
+    int st = 0;
+    unsigned fph = 0u;  // parity of the full barrier phase to wait for
+    for (int n = 0; n < nwork; ++n) {
+        if (!mbar_wait_bounded(&s_full[st], fph)) {
+            if (lane == 0) raise_status(P.status, SPECNG_DEV_TIMEOUT);
+            break;
+        }
+        const StageMeta& mt = s_meta[st];
+        const int c = mt.c;
+        unsigned* rth = &s_rthr[seg % (kStages + 1)];
+        const bool seg_start = fresh;
+        if (seg_start) {
+            const int b = mt.b, j = mt.j;
+            row = b * K1 + j;
+            excl = mt.excl;
+            cand = !GREEDY && mt.cand != 0;
+            cfirst = c;
+            if (cand) {
+                NoiseKey nk = P.nk;
+                nk.seq = static_cast<uint32_t>(b);
+                rp = row_philox(nk, static_cast<uint32_t>(j));
+            }
+        }
+        const int v0 = c * CHUNK;
+        const int v1 = min(P.V, v0 + CHUNK);
+        const uint4* stage = reinterpret_cast<const uint4*>(s_stage + st * SB);
+        const uint32_t* bm = s_bm + (PENALTY ? st * (CHUNK / 32) : 0);
+        const bool full = v0 + off0 + (kVL - 1) * 32 * EPV + EPV <= v1;  // my vectors are whole
+        uint4 rv[kVL];
 #pragma unroll
-        for (int i = 0; i < kIV; ++i) rv[i] = rn[i];
-        if (it + 1 < NIT) load_it(it + 1, rn);
-        const int ib = ebase + it * kIV * RV;
-        const bool full = ib + (kIV - 1) * RV + EPV <= v1;
-        unsigned pmk = 0u;  // penalised elements of this iteration (bit 8 i + e)
+        for (int i = 0; i < kVL; ++i) rv[i] = stage[ubase + i * 32 + lane];
+        // penalised elements of my lane (bit 8 i + e), only where the slice holds one
+        uint64_t pmk = 0u;
         if constexpr (PENALTY) {
-            if (anypen) {
+            if ((mt.penw >> warp) & 1u) {
 #pragma unroll
-                for (int i = 0; i < kIV; ++i) {
-                    const int off = ib + i * RV - v0;
-                    if (off < PIECE) pmk |= ((pbm[off >> 5] >> (off & 31)) & ((1u << EPV) - 1u)) << (8 * i);
+                for (int i = 0; i < kVL; ++i) {
+                    const int off = off0 + i * 32 * EPV;
+                    pmk |= static_cast<uint64_t>((bm[off >> 5] >> (off & 31)) & ((1u << EPV) - 1u)) << (8 * i);
                 }
             }
         }
-        float vm[kIV];
+
+        // ---- streaming: lane maximum zl (bounds my transformed values, penalised ones
+        //      included), sum of exponentials
         float zl = -INFINITY;
+        float lraw = -INFINITY;
+        uint32_t hv[kVL];  // packed vector maxima (bf16), or the fp32 maxima
         if (full) {
+            if constexpr (BF16) {
 #pragma unroll
-            for (int i = 0; i < kIV; ++i) {
-                if constexpr (BF16) {
-                    const uint32_t h = as_u32(bf16x8_max2(rv[i]));
-                    vm[i] = fmaxf(bf16lo(h), bf16hi(h));
-                } else {
-                    vm[i] = fmaxf(fmaxf(__uint_as_float(rv[i].x), __uint_as_float(rv[i].y)),
-                                  fmaxf(__uint_as_float(rv[i].z), __uint_as_float(rv[i].w)));
+                for (int i = 0; i < kVL; ++i) hv[i] = as_u32(bf16x8_max2(rv[i]));
+                uint32_t hr[kVL];
+#pragma unroll
+                for (int i = 0; i < kVL; ++i) hr[i] = hv[i];
+#pragma unroll
+                for (int w2 = kVL / 2; w2 > 0; w2 >>= 1)
+#pragma unroll
+                    for (int i = 0; i < w2; ++i) hr[i] = as_u32(__hmax2(as_bf162(hr[i]), as_bf162(hr[i + w2])));
+                lraw = fmaxf(bf16lo(hr[0]), bf16hi(hr[0]));
+            } else {
+#pragma unroll
+                for (int i = 0; i < kVL; ++i) {
+                    const float f = fmaxf(fmaxf(__uint_as_float(rv[i].x), __uint_as_float(rv[i].y)),
+                                          fmaxf(__uint_as_float(rv[i].z), __uint_as_float(rv[i].w)));
+                    hv[i] = __float_as_uint(f);
+                    lraw = fmaxf(lraw, f);
                 }
             }
-            const float lraw = fmaxf(fmaxf(vm[0], vm[1]), fmaxf(vm[2], vm[3]));
             zl = SOFTCAP ? transform_f32<true, false>(lraw, false, P) : lraw;
-            if constexpr (!GREEDY) {
-                if (!(mref > -INFINITY)) mref = zl;
-                const float msc = mref * P.sc;
-                float2 acc2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+            if constexpr (GREEDY) {
+                if (zl > m) m = zl;
+            } else {
+                // m is the segment's reference: fixed at its first value and raised only when a
+                // value passes it by more than 2^32 in the sum's units, so the exponentials of a
+                // chunk do not wait for the chunk's maximum
+                if (!(m > -INFINITY)) {
+                    m = zl;
+                    msc = m * P.sc;
+                }
+                float2 acc2[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                                  make_float2(0.0f, 0.0f)};
                 const float2 sc2 = make_float2(P.sc, P.sc), nm2 = make_float2(-msc, -msc);
 #pragma unroll
-                for (int i = 0; i < kIV; ++i) {
+                for (int i = 0; i < kVL; ++i) {
                     float x[EPV];
                     unpack<BF16>(rv[i], x);
 #pragma unroll
@@ -663,54 +926,57 @@ __global__ void __launch_bounds__(kPT, 2) verify_piece_kernel(const VerifyDev P)
                         const float2 t = __ffma2_rn(make_float2(transform_f32<SOFTCAP, false>(x[e], false, P),
                                                                 transform_f32<SOFTCAP, false>(x[e + 1], false, P)),
                                                     sc2, nm2);
-                        acc2[i & 1] = __fadd2_rn(acc2[i & 1], make_float2(ex2_approx(t.x), ex2_approx(t.y)));
+                        acc2[i & 3] = __fadd2_rn(acc2[i & 3], make_float2(ex2_approx(t.x), ex2_approx(t.y)));
                     }
                 }
-                float add = (acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y);
-                if ((zl - mref) * P.sc > 32.0f) {
-                    // a value far above the reference: raise it and take the iteration again
-                    s *= ex2_approx((mref - zl) * P.sc);
-                    mref = zl;
-                    const float msc2 = mref * P.sc;
+                float add = ((acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y)) + ((acc2[2].x + acc2[2].y) + (acc2[3].x + acc2[3].y));
+                if ((zl - m) * P.sc > 32.0f) {
+                    // far above the reference: raise it and take the chunk again
+                    s *= ex2_approx((m - zl) * P.sc);
+                    m = zl;
+                    msc = m * P.sc;
                     add = 0.0f;
 #pragma unroll
-                    for (int i = 0; i < kIV; ++i) {
+                    for (int i = 0; i < kVL; ++i) {
                         float x[EPV];
                         unpack<BF16>(rv[i], x);
 #pragma unroll
                         for (int e = 0; e < EPV; ++e)
-                            add += ex2_approx(fmaf(transform_f32<SOFTCAP, false>(x[e], false, P), P.sc, -msc2));
+                            add += ex2_approx(fmaf(transform_f32<SOFTCAP, false>(x[e], false, P), P.sc, -msc));
                     }
                 }
                 s += add;
             }
             if constexpr (PENALTY) {
-                // the few penalised elements: replace their terms by the penalised ones
-                unsigned pw = pmk;
+                // the few penalised elements: replace their terms by the penalised ones (and
+                // raise the maximum if a penalty below 1 lifted one above it)
+                uint64_t pw = pmk;
                 while (pw != 0u) {
-                    const int bit = __ffs(pw) - 1;
+                    const int bit = __ffsll(static_cast<long long>(pw)) - 1;
                     pw &= pw - 1u;
-                    const float xe = static_cast<float>(raw_logit_f64<BF16>(P.logits, row, P.V, ib + (bit >> 3) * RV + (bit & 7)));
+                    const float xe = elem_of_stage<BF16>(stage, off0 + (bit >> 3) * 32 * EPV + (bit & 7));
                     const float zu = transform_f32<SOFTCAP, false>(xe, false, P);
                     const float zp = transform_f32<SOFTCAP, true>(xe, true, P);
                     zl = fmaxf(zl, zp);
-                    if constexpr (!GREEDY) {
-                        if ((zp - mref) * P.sc > 32.0f) {
-                            s *= ex2_approx((mref - zp) * P.sc);
-                            mref = zp;
+                    if constexpr (GREEDY) {
+                        m = fmaxf(m, zp);
+                    } else {
+                        if ((zp - m) * P.sc > 32.0f) {
+                            s *= ex2_approx((m - zp) * P.sc);
+                            m = zp;
+                            msc = m * P.sc;
                         }
-                        const float msc = mref * P.sc;
                         s += ex2_approx(fmaf(zp, P.sc, -msc)) - ex2_approx(fmaf(zu, P.sc, -msc));
                     }
                 }
             }
         } else {
-            // partial vectors (a row's last piece): exact transform element by element
+            // partial vectors (a row's last chunk): exact transform element by element
 #pragma unroll
-            for (int i = 0; i < kIV; ++i) {
-                vm[i] = -INFINITY;
-                const int e0 = ib + i * RV;
-                const int nv = min(EPV, v1 - e0);
+            for (int i = 0; i < kVL; ++i) {
+                hv[i] = BF16 ? 0xFF80FF80u : __float_as_uint(-INFINITY);
+                const int off = off0 + i * 32 * EPV;
+                const int nv = min(EPV, v1 - (v0 + off));
                 if (nv <= 0) continue;
                 float x[EPV];
                 unpack<BF16>(rv[i], x);
@@ -718,49 +984,35 @@ __global__ void __launch_bounds__(kPT, 2) verify_piece_kernel(const VerifyDev P)
                 for (int e = 0; e < EPV; ++e) {
                     if (e >= nv) break;
                     const float z = transform_f32<SOFTCAP, PENALTY>(x[e], (pmk >> (8 * i + e)) & 1u, P);
-                    vm[i] = fmaxf(vm[i], x[e]);
+                    lraw = fmaxf(lraw, x[e]);
                     zl = fmaxf(zl, z);
-                    if constexpr (!GREEDY) {
-                        if (!(mref > -INFINITY) || (z - mref) * P.sc > 32.0f) {
-                            s = mref > -INFINITY ? s * ex2_approx((mref - z) * P.sc) : 0.0f;
-                            mref = z;
+                    if constexpr (GREEDY) {
+                        m = fmaxf(m, z);
+                    } else {
+                        if (!(m > -INFINITY) || (z - m) * P.sc > 32.0f) {
+                            s = m > -INFINITY ? s * ex2_approx((m - z) * P.sc) : 0.0f;
+                            m = z;
+                            msc = m * P.sc;
                         }
-                        s += ex2_approx(fmaf(z, P.sc, -mref * P.sc));
+                        s += ex2_approx(fmaf(z, P.sc, -msc));
                     }
                 }
             }
         }
-        m = fmaxf(m, zl);
-        // bookkeeping of the vectors for phase B: bf16 upper bounds of the raw maxima,
-        // the vectors with a penalised element, my largest value and its vector
-#pragma unroll
-        for (int i = 0; i < kIV; i += 2) {
-            const uint32_t lo = BF16 ? (__float_as_uint(vm[i]) >> 16) : bf16_ceil_bits(vm[i]);
-            const uint32_t hi = BF16 ? (__float_as_uint(vm[i + 1]) >> 16) : bf16_ceil_bits(vm[i + 1]);
-            vmx[(it * kIV + i) >> 1] = lo | (hi << 16);
-        }
-#pragma unroll
-        for (int i = 0; i < kIV; ++i) {
-            if ((pmk >> (8 * i)) & 0xFFu) penv |= 1u << (it * kIV + i);
-            if (vm[i] > lbest) {
-                lbest = vm[i];
-                lbk = it * kIV + i;
-            }
-        }
+
+        // ---- candidates
         if constexpr (GREEDY) {
             // top two transformed values (lower id on ties) within cand_delta of the best
-            // value seen; without a penalty the lane maximum is itself a value of the row
-            float g = fmaxf(gth, tt.s1 > -INFINITY ? tt.s1 - cand_delta(tt.s1) : -INFINITY);
-            if constexpr (!PENALTY) {
-                const float wb = key_score(warp_best_key(zl));
-                if (wb > -INFINITY) g = fmaxf(g, wb - cand_delta(wb));
-            }
-            gth = g;
+            // value any warp of the CTA has reached in this segment.  Without a penalty the
+            // lane maximum is itself a value of the row (the transform is monotone)
+            float gth = fmaxf(tt.s1, key_score(*reinterpret_cast<volatile unsigned*>(rth)));
+            if constexpr (!PENALTY) gth = fmaxf(gth, key_score(warp_best_key(zl)));
+            gth = gth > -INFINITY ? gth - cand_delta(gth) : -INFINITY;
             if (zl >= gth) {
 #pragma unroll
-                for (int i = 0; i < kIV; ++i) {
-                    const int e0 = ib + i * RV;
-                    const int nv = min(EPV, v1 - e0);
+                for (int i = 0; i < kVL; ++i) {
+                    const int off = off0 + i * 32 * EPV;
+                    const int nv = min(EPV, v1 - (v0 + off));
                     if (nv <= 0) continue;
                     float x[EPV];
                     unpack<BF16>(rv[i], x);
@@ -769,174 +1021,219 @@ __global__ void __launch_bounds__(kPT, 2) verify_piece_kernel(const VerifyDev P)
                         if (e >= nv) break;
                         const float z = transform_f32<SOFTCAP, PENALTY>(x[e], (pmk >> (8 * i + e)) & 1u, P);
                         if (z >= gth) {
-                            top2_push(tt, z, e0 + e);
+                            top2_push(tt, z, v0 + off + e);
                             gth = fmaxf(gth, tt.s1 - cand_delta(tt.s1));
                         }
                     }
                 }
             }
-        }
-    }
-
-    if (!GREEDY && cand) {
-        // ---- exact scores that need no per-id draw: each block's argmin element
-        if (vI >= 0 && vI != excl) {
-            const float zb = transform_f32<SOFTCAP, PENALTY>(xI, pen_at(vI), P) * P.invT;
-            top2_push(tt, zb - bn.lnM, vI);
-        }
-        // ---- the warp's four largest values (their lanes score them)
-        int sv = -1;  // the id this lane scored
-        {
-            unsigned ku = lbest > -INFINITY ? score_key(lbest) : 0u;
-            bool pick = false;
+            const unsigned kw = warp_best_key(tt.s1);
+            if (lane == 0 && kw != 0u) atomicMax(rth, kw);
+        } else if (cand) {
+            int seeded = -1;
+            if (seg_start) {
+                // seed: every lane scores its largest raw element (any exact score bounds the
+                // best from below); the CTA's warps share the best seed
+                int am = -1;
 #pragma unroll
-            for (int r = 0; r < kTop; ++r) {
-                const unsigned kmax = __reduce_max_sync(0xffffffffu, ku);
-                if (kmax == 0u) break;
-                const unsigned own = __ballot_sync(0xffffffffu, ku == kmax);
-                if (lane == __ffs(own) - 1) {
-                    pick = true;
-                    ku = 0u;
+                for (int i = kVL - 1; i >= 0; --i) {
+                    const int off = off0 + i * 32 * EPV;
+                    const int nv = min(EPV, v1 - (v0 + off));
+                    float x[EPV];
+                    unpack<BF16>(rv[i], x);
+#pragma unroll
+                    for (int e = EPV - 1; e >= 0; --e)
+                        if (e < nv && x[e] == lraw) am = off + e;
+                }
+                float t0 = -INFINITY;
+                if (am >= 0 && v0 + am != excl) {
+                    const float z = transform_f32<SOFTCAP, PENALTY>(elem_of_stage<BF16>(stage, am),
+                                                                    PENALTY && ((bm[am >> 5] >> (am & 31)) & 1u), P);
+                    const uint32_t v = static_cast<uint32_t>(v0 + am);
+                    const BlockNoise bk = mt.bn[am >> kNoiseBlockShift];
+                    t0 = z * P.invT - ln_fast(noise_exp_f32(rp, bk.M, bk.I, v));
+                    top2_push(tt, t0, static_cast<int>(v));
+                    seeded = static_cast<int>(v);
+                }
+                const unsigned k0 = warp_best_key(t0);
+                if (k0 != 0u) {
+                    const float b0 = key_score(k0);
+                    thr = fmaxf(thr, b0 - cand_delta(b0));
+                    if (lane == 0) atomicMax(rth, k0);
                 }
             }
-            int q = 0;
-            float M = 0.0f;
-            int I = 0;
-            if (pick) {
-                // locate the value in its vector (lowest id among equal values), then score it
-                const int e0 = ebase + lbk * RV;
-                const uint4 r = load_vec<BF16>(rowp, e0, v1, P.aligned);
-                float x[EPV];
-                unpack<BF16>(r, x);
-                int e = -1;
-#pragma unroll
-                for (int k = EPV - 1; k >= 0; --k)
-                    if (e0 + k < v1 && x[k] == lbest) e = k;
-                sv = e >= 0 ? e0 + e : -1;
-                if (sv == excl) sv = -1;
-                q = sv >= 0 ? (sv - v0) >> kNoiseBlockShift : 0;
+            {
+                // adopt the best score another warp published for this segment
+                const float best = key_score(*reinterpret_cast<volatile unsigned*>(rth));
+                if (best > -INFINITY) thr = fmaxf(thr, best - cand_delta(best));
             }
-            M = __shfl_sync(0xffffffffu, bn.M, q);
-            I = __shfl_sync(0xffffffffu, bn.I, q);
-            if (__any_sync(0xffffffffu, sv >= 0)) {
-                const float E = noise_exp_f32(rp, M, I, static_cast<uint32_t>(sv < 0 ? 0 : sv));
-                if (sv >= 0) {
-                    const float zb = transform_f32<SOFTCAP, PENALTY>(lbest, pen_at(sv), P) * P.invT;
-                    // the argmin element is already in; its score here is the same
-                    if (static_cast<int>(static_cast<uint32_t>(sv) & kNoiseBlockMask) != I)
-                        top2_push(tt, zb - ln_fast(E), sv);
-                    else
-                        sv = -1;
+            // gate: no score of my lane exceeds zl / T - (smallest ln M of the slice)
+            const float zlb = zl * P.invT;
+            const bool lpass = zlb - mt.wmin[warp] + bound_slack(zlb) >= thr;
+            if (__any_sync(0xffffffffu, lpass)) {
+                // block tests: every score of vector i is at most z / T - ln M_i; then the
+                // elements of the passing vectors that can reach the best
+                uint64_t msk = 0u;
+                if (lpass) {
+#pragma unroll
+                    for (int i = 0; i < kVL; ++i) {
+                        const int off = off0 + i * 32 * EPV;
+                        const float lnM = mt.bn[off >> kNoiseBlockShift].lnM;
+                        float zv;
+                        if constexpr (BF16) zv = fmaxf(bf16lo(hv[i]), bf16hi(hv[i]));
+                        else zv = __uint_as_float(hv[i]);
+                        if (SOFTCAP && full) zv = transform_f32<true, false>(zv, false, P);
+                        const unsigned pb = static_cast<unsigned>(pmk >> (8 * i)) & 0xFFu;
+                        const float zvb = zv * P.invT;
+                        if (!(pb != 0u || !full || zvb - lnM + bound_slack(zvb) >= thr)) continue;
+                        unsigned mi;
+                        if (full) {
+                            // z >= T (thr + ln M), in raw units
+                            const float zt = (thr + lnM) * P.T;
+                            float xt = zt;
+                            if constexpr (SOFTCAP) {
+                                // shrink by more than the fp32 error of c tanh(x / c) before
+                                // inverting: atanh is steep near |u| = 1
+                                float u = zt * P.invcap;
+                                u -= 1e-6f * fabsf(u) + 1e-7f;
+                                xt = u > 1.0f ? INFINITY : (u <= -1.0f ? -INFINITY : P.cap * atanhf(fminf(u, 1.0f - 1e-7f)));
+                            }
+                            xt -= 1e-5f * (1.0f + fabsf(xt));  // slack for the rounding of the transform
+                            if constexpr (BF16) {
+                                mi = bf16x8_ge_bits(rv[i], bf16x2_floor(xt));
+                            } else {
+                                mi = static_cast<unsigned>(__uint_as_float(rv[i].x) >= xt);
+                                mi |= static_cast<unsigned>(__uint_as_float(rv[i].y) >= xt) << 1;
+                                mi |= static_cast<unsigned>(__uint_as_float(rv[i].z) >= xt) << 2;
+                                mi |= static_cast<unsigned>(__uint_as_float(rv[i].w) >= xt) << 3;
+                            }
+                            mi |= pb;  // penalised: decided exactly below
+                        } else {
+                            const int nv = min(EPV, v1 - (v0 + off));
+                            mi = nv > 0 ? (1u << nv) - 1u : 0u;
+                        }
+                        msk |= static_cast<uint64_t>(mi) << (8 * i);
+                    }
+                    if (seeded >= 0) {
+                        const int so = seeded - v0 - off0;
+                        const int si = so / (32 * EPV), se = so - si * 32 * EPV;
+                        if (se >= 0 && se < EPV) msk &= ~(static_cast<uint64_t>(1) << (8 * si + se));
+                    }
                 }
-            }
-        }
-        // ---- publish the warp's best to the row, read back the row's best
-        unsigned* gthr = P.row_thr + row;
-        const unsigned kw = warp_best_key(tt.s1);
-        unsigned kg = 0u;
-        if (lane == 0) {
-            if (kw != 0u) atomicMax(gthr, kw);
-            kg = __ldcg(gthr);
-        }
-        kg = __shfl_sync(0xffffffffu, max(kg, kw), 0);
-        const float best = key_score(kg);
-        float thr = best > -INFINITY ? best - cand_delta(best) : -INFINITY;
-
-        // ================= phase B =================
-        // lane q (block q) turns the best into a raw-value bound for its block, packed
-        // twice: element x of block q can reach the best only if x >= xt_q
-        uint32_t xt2 = 0u;
-        {
-            const float zt = (thr + bn.lnM) * P.T;
-            float xt = zt;
-            if constexpr (SOFTCAP) {
-                // shrink by more than the fp32 error of c tanh(x / c) before inverting:
-                // atanh is steep near |u| = 1
-                float u = zt * P.invcap;
-                u -= 1e-6f * fabsf(u) + 1e-7f;
-                xt = u > 1.0f ? INFINITY : (u <= -1.0f ? -INFINITY : P.cap * atanhf(fminf(u, 1.0f - 1e-7f)));
-            }
-            xt -= 1e-5f * (1.0f + fabsf(xt));  // slack for the rounding of the transform
-            if (!(thr > -INFINITY)) xt = -INFINITY;
-            xt2 = bf16x2_floor(xt);
-        }
-        // vector k of a lane lies in block k * EPV / 8; two vectors per test
-        unsigned pv = penv;
-#pragma unroll
-        for (int k2 = 0; k2 < NV / 2; ++k2) {
-            const int q0 = (2 * k2) * EPV / 8, q1 = (2 * k2 + 1) * EPV / 8;
-            const uint32_t t0 = __shfl_sync(0xffffffffu, xt2, q0), t1 = __shfl_sync(0xffffffffu, xt2, q1);
-            const uint32_t th = (t0 & 0xFFFFu) | (t1 & 0xFFFF0000u);
-            const unsigned mk = __hge2_mask(as_bf162(vmx[k2]), as_bf162(th));
-            pv |= ((mk & 1u) | ((mk >> 15) & 2u)) << (2 * k2);
-        }
-        pv &= (ebase < v1 ? 0xFFFFFFFFu : 0u);  // (a lane wholly past the end has nothing)
-        // the passing vectors: reload, bound each element exactly, score the survivors
-        while (__any_sync(0xffffffffu, pv != 0u)) {
-            int k = -1;
-            uint4 r = make_uint4(0u, 0u, 0u, 0u);
-            if (pv != 0u) {
-                k = __ffs(pv) - 1;
-                pv &= pv - 1u;
-                const int e0 = ebase + k * RV;
-                if (e0 < v1) r = load_vec<BF16>(rowp, e0, v1, P.aligned);
-                else k = -1;
-            }
-            float x[EPV];
-            unpack<BF16>(r, x);
-            const int q = k >= 0 ? (k * EPV) >> 3 : 0;
-            const float Mq = __shfl_sync(0xffffffffu, bn.M, q);
-            const float lnq = __shfl_sync(0xffffffffu, bn.lnM, q);
-            const int Iq = __shfl_sync(0xffffffffu, bn.I, q);
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) {
-                const int v = k >= 0 ? ebase + k * RV + e : -1;
-                bool live = false;
-                float zb = -INFINITY;
-                if (v >= 0 && v < v1 && v != excl && v != sv && static_cast<int>(static_cast<uint32_t>(v) & kNoiseBlockMask) != Iq) {
-                    zb = transform_f32<SOFTCAP, PENALTY>(x[e], pen_at(v), P) * P.invT;
-                    live = zb - lnq + bound_slack(zb) >= thr;
-                }
-                if (__any_sync(0xffffffffu, live)) {
-                    const float E = noise_exp_f32(rp, Mq, Iq, static_cast<uint32_t>(v < 0 ? 0 : v));
-                    if (live) {
-                        const float score = zb - ln_fast(E);
-                        if (score >= thr) {
-                            top2_push(tt, score, v);
-                            thr = fmaxf(thr, tt.s1 - cand_delta(tt.s1));
+                // score the lane's candidates one per iteration, the warp in step
+                while (__any_sync(0xffffffffu, msk != 0u)) {
+                    int v = -1, loc = 0;
+                    float zb = -INFINITY;
+                    if (msk != 0u) {
+                        const int bit = __ffsll(static_cast<long long>(msk)) - 1;
+                        msk &= msk - 1u;
+                        loc = off0 + (bit >> 3) * 32 * EPV + (bit & 7);
+                        const bool pen = PENALTY && ((pmk >> bit) & 1u);
+                        zb = transform_f32<SOFTCAP, PENALTY>(elem_of_stage<BF16>(stage, loc), pen, P) * P.invT;
+                        v = v0 + loc;
+                    }
+                    const BlockNoise bk = mt.bn[loc >> kNoiseBlockShift];
+                    const bool live = v >= 0 && v != excl && zb - bk.lnM + bound_slack(zb) >= thr;
+                    if (__any_sync(0xffffffffu, live)) {
+                        const float E = noise_exp_f32(rp, bk.M, bk.I, static_cast<uint32_t>(v < 0 ? 0 : v));
+                        if (live) {
+                            const float score = zb - ln_fast(E);
+                            if (score >= thr) {
+                                top2_push(tt, score, v);
+                                thr = fmaxf(thr, tt.s1 - cand_delta(tt.s1));
+                            }
                         }
                     }
                 }
+                // share the warp's best score with the CTA
+                const unsigned kw = warp_best_key(tt.s1);
+                if (kw != 0u) {
+                    const float bw = key_score(kw);
+                    thr = fmaxf(thr, bw - cand_delta(bw));
+                    if (lane == 0) atomicMax(rth, kw);
+                }
             }
         }
-        const unsigned kw2 = warp_best_key(tt.s1);
-        if (lane == 0 && kw2 > kw) atomicMax(gthr, kw2);
-    }
 
-    // ---- the piece's partial, then the row merge if this warp completes the row
-    float pm = GREEDY ? m : mref, ps = s;
-    if constexpr (!GREEDY) {
-        if (!(pm > -INFINITY)) ps = 0.0f;
+        fresh = mt.seg_end != 0;
+        if (fresh) {
+            // ---- end of this row's segment: one partial for the segment
+            float pm = m, ps = s;
+            Top2 pt = tt;
+            if constexpr (!GREEDY) {
+                if (!(pm > -INFINITY)) ps = 0.0f;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float mo = __shfl_xor_sync(0xffffffffu, pm, off);
-            const float so = __shfl_xor_sync(0xffffffffu, ps, off);
-            ms_merge(pm, ps, mo, so, P.sc);
+                for (int off = 16; off > 0; off >>= 1) {
+                    const float mo = __shfl_xor_sync(0xffffffffu, pm, off);
+                    const float so = __shfl_xor_sync(0xffffffffu, ps, off);
+                    ms_merge(pm, ps, mo, so, P.sc);
+                }
+            }
+            pt = top2_warp_reduce(pt);
+            int last = 0;
+            if (lane == 0) {
+                s_slot[st][warp] = WarpPart{pm, ps, pt};
+                __threadfence_block();
+                last = atomicAdd(&s_cnt[st], 1) == kCWarps - 1;
+            }
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (last) {
+                __threadfence_block();
+                WarpPart wp = lane < kCWarps ? s_slot[st][lane] : WarpPart{-INFINITY, 0.0f, top2_empty()};
+                float cm = wp.m, cs = wp.s;
+                Top2 ct = wp.t;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    const float mo = __shfl_xor_sync(0xffffffffu, cm, off);
+                    const float so = __shfl_xor_sync(0xffffffffu, cs, off);
+                    ms_merge(cm, cs, mo, so, P.sc);
+                    ct = top2_merge(ct, top2_shfl_xor(ct, off));
+                }
+                int merge_now = 0;
+                if (lane == 0) {
+                    // keyed by the segment's last chunk; a written partial is never all-zero
+                    st_partial(P.part + static_cast<size_t>(row) * P.nchunk + c, GREEDY ? 0.0f : cm,
+                               GREEDY ? 1.0f : cs, ct);
+                    s_cnt[st] = 0;
+                    *rth = 0u;  // every warp is past this segment: the slot is free
+                    // the CTA that completes the row's chunks merges it
+                    __threadfence();
+                    const unsigned nseg = static_cast<unsigned>(c - cfirst + 1);
+                    const unsigned prev = atomicAdd(&P.row_ticket[row], nseg);
+                    if (prev + nseg == static_cast<unsigned>(P.nchunk)) {
+                        __threadfence();
+                        const int tl = s_mq_tail[warp];
+                        if (tl - s_mq_head[warp] < kMQ) {
+                            s_mq[warp][tl % kMQ] = row;
+                            __threadfence_block();
+                            s_mq_tail[warp] = tl + 1;
+                        } else {
+                            merge_now = 1;  // queue full: merge here
+                        }
+                    }
+                }
+                merge_now = __shfl_sync(0xffffffffu, merge_now, 0);
+                if (merge_now) merge_row<BF16, GREEDY, SOFTCAP, PENALTY>(P, row);
+            }
+            m = -INFINITY;
+            s = 0.0f;
+            msc = 0.0f;
+            tt = top2_empty();
+            thr = -INFINITY;
+            ++seg;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_empty[st]);
+        if (++st == kStages) {
+            st = 0;
+            fph ^= 1u;
         }
     }
-    const Top2 pt = top2_warp_reduce(tt);
-    int last = 0;
+    __syncwarp();
     if (lane == 0) {
-        // a written partial is never all-zero
-        st_partial(P.part + static_cast<size_t>(row) * P.nchunk + p, GREEDY ? 0.0f : pm, GREEDY ? 1.0f : ps, pt);
-        __threadfence();
-        last = atomicAdd(&P.row_ticket[row], 1u) == static_cast<unsigned>(P.nchunk - 1);
+        __threadfence_block();
+        atomicAdd(&s_done, 1);
     }
-    last = __shfl_sync(0xffffffffu, last, 0);
-    if (!last) return;
-    __threadfence();
-    if (lane == 0) P.row_thr[row] = 0u;  // every piece of the row is done
-    merge_row<BF16, GREEDY, SOFTCAP, PENALTY>(P, row);
 }
 
 // ---------------------------------------------------------------- K2
@@ -1219,10 +1516,16 @@ __host__ inline int sm_count_cached() {
 
 template <bool BF16, bool G, bool C, bool R>
 cudaError_t launch_stream(const VerifyDev& P, cudaStream_t s) {
-    // one warp per piece of every row that may be active; warps of inactive rows exit at once
-    const long long warps = static_cast<long long>(P.B) * (P.K + 1) * P.nchunk;
-    const unsigned grid = static_cast<unsigned>((warps + kPW - 1) / kPW);
-    verify_piece_kernel<BF16, G, C, R><<<grid, kPT, 0, s>>>(P);
+    // one persistent CTA per SM; the staging ring lives in dynamic shared memory
+    constexpr size_t smem = k1_dyn_smem<R>();
+    static bool configured = false;
+    if (!configured) {
+        const cudaError_t e = cudaFuncSetAttribute(verify_stream_kernel<BF16, G, C, R>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    verify_stream_kernel<BF16, G, C, R><<<sm_count_cached(), kPThreads, smem, s>>>(P);
     return cudaGetLastError();
 }
 
@@ -1239,8 +1542,8 @@ cudaError_t launch_stream_cr(const VerifyDev& P, bool c, bool r, cudaStream_t s)
     return r ? launch_stream<BF16, G, false, true>(P, s) : launch_stream<BF16, G, false, false>(P, s);
 }
 
-// The kernels of one spec_verify call for one logits dtype: the piece kernel
-// (with the merges), then, for dense q at T > 0, the residual pass.
+// The kernels of one spec_verify call for one logits dtype: the streaming
+// kernel (with the merges), then, for dense q at T > 0, the residual pass.
 template <bool BF16>
 cudaError_t launch_verify_dtype(const VerifyDev& P, bool greedy, bool softcap, bool penalty, bool dense,
                                 cudaStream_t s);
