@@ -76,7 +76,7 @@ extern "C" {
 #define SPECNG_NGRAM_MAX_B    512       /* sequences per n-gram table              */
 #define SPECNG_NGRAM_MAX_V    262144    /* vocabulary of an n-gram table (2^18)    */
 #define SPECNG_NGRAM_MAX_POS  16777216  /* positions per sequence in a table (2^24) */
-#define SPECNG_STATIC_SCRATCH_BYTES 4194304  /* scratch of spec_verify_noalloc (4 MiB) */
+#define SPECNG_STATIC_SCRATCH_BYTES 16777216 /* scratch of spec_verify_noalloc (16 MiB) */
 
 /* ------------------------------------------------------------------------
  * N-gram table  [AX]: "builds bigram/trigram tables at runtime, predicts up

@@ -63,8 +63,8 @@ void* static_scratch_ptr() {
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct WsLayout {
-    size_t part, rowres, seqres, part2, tickets, total;
-    size_t row_ticket, row_thr, seq_ticket, seq_ticket2;
+    size_t part, bmax, blkws, rowres, seqres, part2, tickets, total;
+    size_t row_thr, seq_ticket2;
 };
 
 // The f32 chunks are the smaller ones, so their counts bound both dtypes.
@@ -74,16 +74,18 @@ int max_chunks2(int V) { return (V + res_chunk_elems<false>() - 1) / res_chunk_e
 WsLayout ws_layout(int B, int K, int V) {
     const size_t rows = static_cast<size_t>(B) * (K + 1);
     const size_t nch = static_cast<size_t>(max_chunks(V));
+    const size_t nblk = static_cast<size_t>(noise_blocks(V));
     WsLayout L{};
     size_t off = 0;
-    L.part = off;    off = align256(off + rows * nch * sizeof(Partial));
+    L.part = off;    off = align256(off + rows * nch * sizeof(SegSum));
+    L.bmax = off;    off = align256(off + rows * nblk * sizeof(float));
+    L.blkws = off;
+    if (nblk > static_cast<size_t>(kSmemBlkCap)) off = align256(off + static_cast<size_t>(B) * nblk * kBlkScratchBytes);
     L.rowres = off;  off = align256(off + rows * sizeof(RowRes));
     L.seqres = off;  off = align256(off + static_cast<size_t>(B) * sizeof(SeqRes));
     L.part2 = off;   off = align256(off + static_cast<size_t>(B) * static_cast<size_t>(max_chunks2(V)) * sizeof(Partial));
     L.tickets = off;
-    L.row_ticket = off;   off += rows * sizeof(unsigned);
     L.row_thr = off;      off += rows * sizeof(unsigned);
-    L.seq_ticket = off;   off += static_cast<size_t>(B) * sizeof(unsigned);
     L.seq_ticket2 = off;  off += static_cast<size_t>(B) * sizeof(unsigned);
     L.total = align256(off);
     return L;
@@ -294,6 +296,7 @@ int spec_verify(const void* logits, int logits_dtype, int B, int K, int V, const
     VerifyDev P{};
     P.logits = logits;
     P.B = B; P.K = K; P.V = V; P.nchunk = nchunk; P.nchunk2 = nchunk2;
+    P.nblk = noise_blocks(V);
     P.drafts = drafts; P.q = draft_probs; P.k = k;
     P.hist = history; P.hist_stride = hist_stride; P.lens = lens;
     P.T = p.temperature;
@@ -315,13 +318,13 @@ int spec_verify(const void* logits, int logits_dtype, int B, int K, int V, const
     P.aligned = aligned16(logits) && (V % epv == 0) && (!dense || (aligned16(draft_probs) && V % 4 == 0));
     P.kv_len = kv_len; P.ema = ema; P.out_tokens = out_tokens; P.out_accept = out_accept_len;
     char* ws = static_cast<char*>(workspace);
-    P.part = reinterpret_cast<Partial*>(ws + L.part);
+    P.part = reinterpret_cast<SegSum*>(ws + L.part);
+    P.bmax = reinterpret_cast<float*>(ws + L.bmax);
+    P.blkws = reinterpret_cast<uint8_t*>(ws + L.blkws);
     P.rowres = reinterpret_cast<RowRes*>(ws + L.rowres);
     P.seqres = reinterpret_cast<SeqRes*>(ws + L.seqres);
     P.part2 = reinterpret_cast<Partial*>(ws + L.part2);
-    P.row_ticket = reinterpret_cast<unsigned*>(ws + L.row_ticket);
     P.row_thr = reinterpret_cast<unsigned*>(ws + L.row_thr);
-    P.seq_ticket = reinterpret_cast<unsigned*>(ws + L.seq_ticket);
     P.seq_ticket2 = reinterpret_cast<unsigned*>(ws + L.seq_ticket2);
     P.status = status_ptr();
 

@@ -1,6 +1,5 @@
-// spec_verify kernels (sm_103a): the streaming pass over the logit rows with
-// the row merges and sequence epilogues folded in, and the dense-q residual
-// pass.
+// spec_verify kernels (sm_103a): the streaming pass over the logit rows, the
+// per-sequence decision kernel, and the dense-q residual pass.
 //
 // Method (SwiftLM page, paragraph on algorithmic equivalence after Leviathan
 // et al.; AX Engine page, "Core Technical Architecture & Methods"):
@@ -13,9 +12,11 @@
 //
 // The noise E_v is drawn per block of 256 ids (block minimum M and its slot,
 // then E_v = M + F_v for the others; see common.cuh), so a score of a block is
-// at most log w_v - ln M.  The streaming pass keeps, per row, the running
-// best score; a block whose largest logit cannot reach it under that bound
-// is skipped without a single per-id draw.
+// at most z_max / T - ln M with z_max the block's largest transformed logit.
+// The streaming pass (bandwidth only) leaves, per row, the segment sums of
+// the softmax and every block's z_max; the decision kernel takes the accept
+// tests from the sums, and only then samples, at row a alone, reading again
+// just the blocks whose bound reaches the best score found.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -28,7 +29,7 @@ template <bool BF16> struct ElemTraits;
 template <> struct ElemTraits<true> { static constexpr int EPV = 8; static constexpr int SIZE = 2; };
 template <> struct ElemTraits<false> { static constexpr int EPV = 4; static constexpr int SIZE = 4; };
 
-// One chunk of a row = one 64 KB stage of the streaming ring; the residual
+// One chunk of a row = one 32 KB stage of the streaming ring; the residual
 // pass takes 32 KB chunks, one per CTA.
 constexpr int kChunkBytes = 32768;
 constexpr int kResChunkBytes = 32768;
@@ -37,25 +38,38 @@ __host__ __device__ constexpr int chunk_elems() { return kChunkBytes / ElemTrait
 template <bool BF16>
 __host__ __device__ constexpr int res_chunk_elems() { return kResChunkBytes / ElemTraits<BF16>::SIZE; }
 
+// Noise blocks of a row of V ids.
+__host__ __device__ constexpr int noise_blocks(int V) { return (V + (1 << kNoiseBlockShift) - 1) >> kNoiseBlockShift; }
+
 // Workspace records.
+struct __align__(8) SegSum {
+    float m, s;  // reference (transformed units) and sum of exp((z - m) / T) of a row segment
+};
 struct __align__(32) Partial {
-    float m, s;  // maximum (transformed units) and sum of exp((z - m) / T) of a row segment
+    float m, s;
     Top2 t;      // top-two candidates (fp32 scores)
     int pad[2];
 };
 struct __align__(16) RowRes {
     double lse;    // log-sum-exp of row / T (T > 0)
-    int winner;    // sampled id of this row (residual or bonus candidate); argmax at T = 0
-    int accepted;  // accept decision for the draft this row verifies
+    int winner;    // sampled id of this row over p (the fallback of an all-zero residual)
+    int accepted;
 };
 struct __align__(16) SeqRes {
     int a, keff, need_residual, pad;
 };
 
+// Per-block scratch of the decision kernel (bound, M, slot, list entry).
+constexpr int kBlkScratchBytes = 16;
+// Blocks whose scratch the decision kernel keeps in shared memory (64 KB);
+// longer rows keep it in the workspace.
+constexpr int kSmemBlkCap = 4096;
+
 struct VerifyDev {
     const void* logits;
     int B, K, V, nchunk;      // nchunk: streaming chunks per row
     int nchunk2;              // residual-pass chunks per row
+    int nblk;                 // noise blocks per row
     const int32_t* drafts;
     const float* q;
     const int32_t* k;
@@ -75,17 +89,16 @@ struct VerifyDev {
     float* ema;
     int32_t* out_tokens;
     int32_t* out_accept;
-    Partial* part;
+    SegSum* part;             // [B (K + 1)][nchunk] segment sums, at each segment's last chunk
+    float* bmax;              // [B (K + 1)][nblk] largest transformed logit of each noise block
+    uint8_t* blkws;           // [B][nblk][16] decision-kernel block scratch (rows past kSmemBlkCap blocks)
     RowRes* rowres;
     SeqRes* seqres;
-    unsigned* row_ticket;
     unsigned* row_thr;        // best residual score published per row (score_key)
-    unsigned* seq_ticket;
     Partial* part2;
     unsigned* seq_ticket2;
     unsigned* status;
 };
-
 // ---------------------------------------------------------------- helpers
 
 template <bool BF16>
@@ -299,214 +312,29 @@ __device__ __forceinline__ int gate_keff(const VerifyDev& P, int b, int* kb_out,
 // Slack of the block bound: covers the fp32 rounding of z / T and ln M.
 __device__ __forceinline__ float bound_slack(float z) { return 1e-5f * (1.0f + fabsf(z)); }
 
-// ---------------------------------------------------------------- row merge
-// One warp: combine the row's segment partials (log-sum-exp, sampled
-// candidate), run the accept test of the draft the row verifies; the last
-// row of a sequence to finish runs the epilogue (tokens, kv_len, EMA).
-
-template <bool BF16, bool GREEDY, bool SOFTCAP, bool PENALTY>
-__device__ __noinline__ void merge_row(const VerifyDev& P, int row) {
-    const int lane = threadIdx.x & 31;
-    const int K1 = P.K + 1;
-    const int b = row / K1, j = row - b * K1;
-    int kb;
-    const int keff = gate_keff(P, b, &kb, false);
-    const bool dense = P.q != nullptr;
-    NoiseKey nk = P.nk;
-    nk.seq = static_cast<uint32_t>(b);
-    int nh = 0, L = 0;
-    if constexpr (PENALTY) {
-        L = P.lens[b];
-        L = L < 0 ? 0 : (static_cast<int64_t>(L) > P.hist_stride ? static_cast<int>(P.hist_stride) : L);
-        nh = L < P.W ? L : P.W;
-    }
-    const WindowView wv{PENALTY ? P.hist + static_cast<size_t>(b) * P.hist_stride + (L - nh) : nullptr,
-                        P.drafts + static_cast<size_t>(b) * P.K, nh, PENALTY ? P.W : 0};
-
-    // the draft's logit (and q) are loaded first: their latency overlaps the partials'
-    const int dnext = j < keff ? wv.drafts[j] : -1;
-    const bool dvalid = dnext >= 0 && dnext < P.V;
-    float xd = 0.0f, qd = 1.0f;
-    if (!GREEDY && lane == 0 && dvalid) {
-        xd = static_cast<float>(raw_logit_f64<BF16>(P.logits, row, P.V, dnext));
-        if (dense) qd = P.q[(static_cast<size_t>(b) * P.K + j) * P.V + dnext];
-    }
-
-    // one partial per row segment, stored at the segment's last chunk; the
-    // other slots are all-zero (a written partial never is)
-    Partial* pr = P.part + static_cast<size_t>(row) * P.nchunk;
-    constexpr int kHeld = 2;
-    Partial held[kHeld];
-    float mf = -INFINITY;
-#pragma unroll
-    for (int h = 0; h < kHeld; ++h) {
-        const int cc = lane + 32 * h;
-        held[h] = cc < P.nchunk ? ldcg_partial(pr + cc) : Partial{0.0f, 0.0f, top2_empty(), {0, 0}};
-        if (cc < P.nchunk && (held[h].s != 0.0f || __float_as_uint(held[h].m) != 0u)) mf = fmaxf(mf, held[h].m);
-    }
-    for (int cc = lane + 32 * kHeld; cc < P.nchunk; cc += 32) {
-        const Partial p = ldcg_partial(pr + cc);
-        if (p.s != 0.0f || __float_as_uint(p.m) != 0u) mf = fmaxf(mf, p.m);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mf = fmaxf(mf, __shfl_xor_sync(0xffffffffu, mf, off));
-    double S = 0.0;
-    Top2 t = top2_empty();
-#pragma unroll
-    for (int h = 0; h < kHeld; ++h) {
-        const Partial& p = held[h];
-        if (lane + 32 * h >= P.nchunk || (p.s == 0.0f && __float_as_uint(p.m) == 0u)) continue;
-        if (!GREEDY && p.m > -INFINITY) S += static_cast<double>(p.s) * static_cast<double>(expf((p.m - mf) * P.invT));
-        t = top2_merge(t, p.t);
-    }
-    for (int cc = lane + 32 * kHeld; cc < P.nchunk; cc += 32) {
-        const Partial p = ldcg_partial(pr + cc);
-        if (p.s == 0.0f && __float_as_uint(p.m) == 0u) continue;
-        if (!GREEDY && p.m > -INFINITY) S += static_cast<double>(p.s) * static_cast<double>(expf((p.m - mf) * P.invT));
-        t = top2_merge(t, p.t);
-    }
-    S = warp_sum_f64(S);
-    t = top2_warp_reduce(t);
-    __syncwarp();
-    for (int cc = lane; cc < P.nchunk; cc += 32) st_zero(pr + cc);  // leave the workspace zeroed
-    if (lane == 0) P.row_ticket[row] = 0u;
-    const double lse = GREEDY ? 0.0 : static_cast<double>(mf) / P.Td + log(S);
-    if (!GREEDY && !(S > 0.0 && S < INFINITY && mf < INFINITY) && lane == 0)
-        raise_status(P.status, SPECNG_DEV_NONFINITE);
-
-    // winner: fp32 order unless the two best are within the fp32 error, then fp64
-    int winner = t.i1;
-    const bool close = t.i2 >= 0 && t.s2 >= t.s1 - cand_delta(t.s1);
-    if (close) {
-        const bool pen1 = PENALTY ? wv.warp_has(j, t.i1) : false;
-        const bool pen2 = PENALTY ? wv.warp_has(j, t.i2) : false;
-        if (lane == 0) {
-            double sc[2];
-            for (int h = 0; h < 2; ++h) {
-                const int id = h == 0 ? t.i1 : t.i2;
-                const double z = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, id),
-                                                                 h == 0 ? pen1 : pen2, P);
-                if constexpr (GREEDY) {
-                    sc[h] = z;
-                } else {
-                    sc[h] = z / P.Td - log(noise_exp_f64(nk, static_cast<uint32_t>(id), static_cast<uint32_t>(j)));
-                }
-            }
-            if (better64(sc[1], t.i2, sc[0], t.i1)) winner = t.i2;
-        }
-        winner = __shfl_sync(0xffffffffu, winner, 0);
-    }
-
-    // accept test of d_{j+1}: fp32 unless within 1e-4 of the boundary, then fp64
-    int accepted = 0;
-    if (j < keff && dvalid) {
-        if constexpr (GREEDY) {
-            accepted = dnext == winner;
-        } else {
-            const bool pend = PENALTY ? wv.warp_has(j, dnext) : false;
-            if (lane == 0) {
-                const double u = accept_uniform_f64(nk, static_cast<uint32_t>(j + 1));
-                const double q = dense ? static_cast<double>(qd) : 1.0;
-                const float lp = transform_f32<SOFTCAP, PENALTY>(xd, pend, P) * P.invT - static_cast<float>(lse);
-                const float lr = logf(static_cast<float>(u)) + logf(static_cast<float>(q));
-                if (lr < lp - 1e-4f * (1.0f + fabsf(lp))) {
-                    accepted = 1;
-                } else if (lr > lp + 1e-4f * (1.0f + fabsf(lp))) {
-                    accepted = 0;
-                } else {
-                    const double zd = transform_f64<SOFTCAP, PENALTY>(static_cast<double>(xd), pend, P);
-                    accepted = u * q <= exp(zd / P.Td - lse);
-                }
-            }
-            accepted = __shfl_sync(0xffffffffu, accepted, 0);
-        }
-    }
-
-    int last_row = 0;
-    if (lane == 0) {
-        RowRes rr;
-        rr.lse = lse;
-        rr.winner = winner;
-        rr.accepted = accepted;
-        P.rowres[row] = rr;
-        __threadfence();
-        const unsigned prev = atomicAdd(&P.seq_ticket[b], 1u);
-        last_row = prev == static_cast<unsigned>(keff);
-    }
-    last_row = __shfl_sync(0xffffffffu, last_row, 0);
-    if (!last_row) return;
-    __threadfence();
-
-    // ---- last row of the sequence: epilogue
-    if (lane == 0) P.seq_ticket[b] = 0u;
-    RowRes* rs = P.rowres + static_cast<size_t>(b) * K1;
-    int acc = 1;
-    if (lane < keff) acc = __ldcg(&rs[lane].accepted);
-    const unsigned rej = __ballot_sync(0xffffffffu, lane < keff && !acc);
-    const int a = rej ? __ffs(rej) - 1 : keff;
-    // a rejected draft outside [0, V) leaves the residual equal to p: the
-    // row's own candidate (over all ids) is then the sample
-    const int da = a < keff ? wv.drafts[a] : -1;
-    const bool need = dense && !GREEDY && a < keff && da >= 0 && da < P.V;
-    const int y = need ? -1 : __ldcg(&rs[a].winner);
-    __syncwarp();
-    if (lane <= keff && !(need && lane == a)) st_zero(rs + lane);
-    if (lane < K1) P.out_tokens[static_cast<size_t>(b) * K1 + lane] = lane < a ? wv.drafts[lane] : (lane == a ? y : -1);
-    if (lane == 0) {
-        P.out_accept[b] = a;
-        P.kv_len[b] = P.kv_len[b] - kb + a;
-        if (keff > 0) {
-            // (1 - tau) * ema + tau * a / k_eff, rounded step by step (no contraction)
-            const double tau = static_cast<double>(P.tau);
-            const double rate = static_cast<double>(a) / static_cast<double>(keff);
-            P.ema[b] = static_cast<float>(
-                __dadd_rn(__dmul_rn(1.0 - tau, static_cast<double>(P.ema[b])), __dmul_rn(tau, rate)));
-        }
-        if (need) {
-            SeqRes sr;
-            sr.a = a;
-            sr.keff = keff;
-            sr.need_residual = 1;
-            sr.pad = 0;
-            P.seqres[b] = sr;
-        }
-    }
-}
-
 // ---------------------------------------------------------------- K1
-// Persistent, warp-specialised streaming kernel.  One CTA per SM; the active
-// row-chunks of the call (rows 0..k_eff of every sequence, chunks of 64 KB)
-// are laid out row-major and split into equal contiguous ranges, one per CTA.
+// Streaming kernel: bandwidth only.  Persistent and warp-specialised, one CTA
+// per SM; the active row-chunks of the call (rows 0..k_eff of every sequence,
+// chunks of 32 KB) are laid out row-major and split into equal contiguous
+// ranges, one per CTA.
 //   * A producer warp walks the CTA's range and keeps up to kStages chunks in
 //     flight with cp.async.bulk into a shared-memory ring (full / empty
-//     mbarriers, bounded waits).  It draws the noise of a chunk's 256-id
-//     blocks before the chunk's ring slot is free, and writes the row's
-//     metadata, the penalty bitmap and the noise while the copy is in flight.
-//   * Sixteen streaming warps each own a 4 KB slice of every chunk.  A lane's
-//     16-byte vector i of a bf16 chunk covers 8 ids of noise block 8 w + i, so
-//     its packed maximum gives the block test z / T - ln M >= best for its
-//     eight ids at once; a single test of the lane's maximum against the
-//     smallest ln M of the slice gates them.  Per slice: packed maxima, the
-//     exponentials of the sum, the block tests; only the vectors that pass
-//     compare their elements, and each lane scores its few survivors
-//     (per-id Philox draw, E_v, score) in step with the warp.  At the first
-//     chunk of a row segment each lane scores its largest element, which
-//     starts the segment's best; the warps of the CTA share the best through
-//     shared memory.
-//   * A merge warp runs the row merges: the CTA that completes a row (atomic
-//     ticket over the row's chunks) queues it, and the merge warp combines the
-//     row's partials, takes the accept test and, for the last row of a
-//     sequence (second ticket), runs the epilogue.  Nothing waits on another
-//     CTA.
+//     mbarriers, bounded waits), with each chunk's row metadata and penalty
+//     bitmap.  The next sequence's drafts and history tail are fetched into
+//     registers one sequence ahead, so no global round trip stalls the copies.
+//   * Sixteen streaming warps each own a 2 KB slice of every chunk.  A warp's
+//     vector row (32 lanes x one 16-byte vector) of a bf16 chunk is one noise
+//     block (two rows for fp32): its largest transformed value goes to the
+//     workspace.  The rows that carry an accept test (j < k_eff, T > 0) also
+//     add their exponentials to a sum kept against a segment reference (so
+//     the sum does not wait for each chunk's maximum); at the last chunk of a
+//     row segment the warps combine their sums into one record.
 
 constexpr int kCWarps = 16;                    // streaming warps
 constexpr int kPWarp = kCWarps;                // producer warp index
-constexpr int kMWarp = kCWarps + 1;            // merge warp index
-constexpr int kPThreads = (kCWarps + 2) * 32;  // 576
+constexpr int kPThreads = (kCWarps + 1) * 32;  // 544
 constexpr int kStages = 6;
 constexpr int kVL = 4;                         // 16-byte vectors per lane per chunk
-constexpr int kMaxBlk = kChunkBytes / 2 >> kNoiseBlockShift;  // noise blocks per chunk (bf16: 128)
-constexpr int kMQ = 16;                        // merge-queue entries per streaming warp
 static_assert(kChunkBytes == kCWarps * 32 * kVL * 16, "stage layout");
 static_assert((32 * 8) == (1 << kNoiseBlockShift), "a bf16 vector row of a warp is one noise block");
 
@@ -517,17 +345,11 @@ __host__ __device__ constexpr size_t k1_dyn_smem() {
 }
 
 struct StageMeta {
-    int b, j, c, excl, seg_end;  // seg_end: the last chunk of this row in the CTA's range
-    int cand;                    // the row's Gumbel candidates can be the emitted token
-    unsigned penw;               // bit w: warp w's slice holds a penalised id
-    int pad;
-    float wmin[kCWarps];         // smallest ln M of each warp's slice
-    BlockNoise bn[kMaxBlk];      // noise of the chunk's 256-id blocks
-};
-
-struct WarpPart {
-    float m, s;
-    Top2 t;
+    int b, j, c;
+    int seg_end;   // the last chunk of this row in the CTA's range
+    int sum;       // the row's softmax sum is needed (accept test)
+    unsigned penw; // bit w: warp w's slice holds a penalised id
+    int pad[2];
 };
 
 template <bool BF16, bool GREEDY, bool SOFTCAP, bool PENALTY>
@@ -535,29 +357,22 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
     constexpr int EPV = ElemTraits<BF16>::EPV;
     constexpr int CHUNK = chunk_elems<BF16>();
     constexpr int SB = kChunkBytes;
-    constexpr int SL = 32 * kVL * EPV;  // ids per streaming slice
-    constexpr int NB = CHUNK >> kNoiseBlockShift;
-    constexpr int BPW = NB / kCWarps;   // noise blocks per slice
+    constexpr int SL = 32 * kVL * EPV;                          // ids per streaming slice
+    constexpr int VPB = (1 << kNoiseBlockShift) / (32 * EPV);   // vector rows per noise block (bf16 1, fp32 2)
     extern __shared__ __align__(128) uint8_t s_dyn[];
     uint8_t* s_stage = s_dyn;
     uint32_t* s_bm = reinterpret_cast<uint32_t*>(s_dyn + kStages * SB);
     __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages];
     __shared__ StageMeta s_meta[kStages];
-    __shared__ WarpPart s_slot[kStages][kCWarps];
+    __shared__ SegSum s_slot[kStages][kCWarps];
     __shared__ int s_cnt[kStages];
-    __shared__ unsigned s_rthr[kStages + 1];  // per-segment best score (score_key; 0 = none)
     __shared__ long long s_wsum[kPThreads / 32];
     __shared__ int s_start[3];
     __shared__ int s_hwin[PENALTY ? SPECNG_MAX_REP_WINDOW : 1];
     __shared__ int s_pdrafts[SPECNG_MAX_K + 1];
-    __shared__ volatile int s_mq[kCWarps][kMQ];  // rows to merge, per streaming warp (single producer / consumer)
-    __shared__ volatile int s_mq_tail[kCWarps];
-    __shared__ volatile int s_mq_head[kCWarps];
-    __shared__ int s_done;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int K1 = P.K + 1;
-    const bool dense = P.q != nullptr;
 
     // ---- prologue: count the active row-chunks and find this CTA's range
     const int per = (P.B + kPThreads - 1) / kPThreads;
@@ -577,13 +392,7 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
             mbar_init(&s_empty[i], kCWarps);
             s_cnt[i] = 0;
         }
-        for (int i = 0; i <= kStages; ++i) s_rthr[i] = 0u;
-        s_done = 0;
         mbar_init_fence();
-    }
-    if (tid < kCWarps) {
-        s_mq_tail[tid] = 0;
-        s_mq_head[tid] = 0;
     }
     __syncthreads();
     long long base = 0, total = 0;
@@ -614,10 +423,6 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
 
     if (warp == kPWarp) {
         // ================= producer =================
-        // The data of the next sequence (k, EMA, drafts, the tail of its history
-        // for the penalty window) is fetched into registers one sequence ahead,
-        // and its history length two ahead, so no global round trip stalls the
-        // copies at a sequence change.
         constexpr int kHW = PENALTY ? SPECNG_MAX_REP_WINDOW / 32 : 1;
         struct SeqData {
             int k, draft, L;
@@ -642,18 +447,12 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
             }
         };
         int b = s_start[0], j = s_start[1], c = s_start[2];
-        int kb = 0, keff = 0, nh = 0;
+        int keff = 0, nh = 0;
         auto install = [&](const SeqData& d) {
-            kb = d.k;
-            if (kb < 0 || kb > P.K) {
-                if (lane == 0) raise_status(P.status, SPECNG_DEV_BAD_K);
-                kb = kb < 0 ? 0 : P.K;
-            }
+            int kb = d.k;
+            if (kb < 0 || kb > P.K) kb = kb < 0 ? 0 : P.K;
             keff = (P.gate && kb > 0 && !(d.ema >= P.thresh)) ? 0 : kb;
-            if (lane < keff) {
-                s_pdrafts[lane] = d.draft;
-                if (!(d.draft >= 0 && d.draft < P.V)) raise_status(P.status, SPECNG_DEV_TOKEN_OOR);
-            }
+            if (lane < keff) s_pdrafts[lane] = d.draft;
             if constexpr (PENALTY) {
                 nh = d.L < P.W ? d.L : P.W;
 #pragma unroll
@@ -672,7 +471,6 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
             fetch(b + 1, L1, nxt);
             if (PENALTY && b + 2 < P.B) Lnext2 = P.lens[b + 2];
         }
-        NoiseKey nk = P.nk;
         bool ok = true;
         int st = 0;
         unsigned eph = 0u;  // parity of the empty barrier phase to wait for
@@ -681,26 +479,6 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
             const int v1 = min(P.V, v0 + CHUNK);
             const char* src = static_cast<const char*>(P.logits) +
                               ((static_cast<size_t>(b) * K1 + j) * P.V + v0) * ElemTraits<BF16>::SIZE;
-            // with dense q, row j < k_eff is sampled by the residual pass unless
-            // its draft is invalid (the residual is then p itself)
-            int excl = -1, cand = 1;
-            if (!GREEDY && j < keff) {
-                const int d = s_pdrafts[j];
-                const bool valid = d >= 0 && d < P.V;
-                if (!dense && valid) excl = d;
-                if (dense && valid) cand = 0;
-            }
-            // the noise of the chunk's blocks (lane q: blocks q, q + 32, ...), before the
-            // ring slot is free
-            constexpr int NBL = (NB + 31) / 32;
-            BlockNoise bnl[NBL];
-            if (!GREEDY && cand) {
-                nk.seq = static_cast<uint32_t>(b);
-                const uint32_t blk0 = static_cast<uint32_t>(v0 >> kNoiseBlockShift);
-#pragma unroll
-                for (int r = 0; r < NBL; ++r)
-                    if (lane + 32 * r < NB) bnl[r] = block_noise(nk, blk0 + lane + 32 * r, static_cast<uint32_t>(j));
-            }
             if (n >= kStages) ok = mbar_wait_bounded(&s_empty[st], eph);
             if (!ok) { if (lane == 0) raise_status(P.status, SPECNG_DEV_TIMEOUT); break; }
             // the copy goes first; the metadata is written while it is in flight, and the
@@ -713,21 +491,9 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
             }
             StageMeta& mt = s_meta[st];
             if (lane == 0) {
-                mt.b = b; mt.j = j; mt.c = c; mt.excl = excl;
+                mt.b = b; mt.j = j; mt.c = c;
                 mt.seg_end = (c == P.nchunk - 1 || n == nwork - 1) ? 1 : 0;
-                mt.cand = cand;
-            }
-            if (!GREEDY && cand) {
-#pragma unroll
-                for (int r = 0; r < NBL; ++r)
-                    if (lane + 32 * r < NB) mt.bn[lane + 32 * r] = bnl[r];
-                __syncwarp();
-                if (lane < kCWarps) {
-                    float mn = INFINITY;
-#pragma unroll
-                    for (int q = 0; q < BPW; ++q) mn = fminf(mn, mt.bn[lane * BPW + q].lnM);
-                    mt.wmin[lane] = mn;
-                }
+                mt.sum = (!GREEDY && j < keff) ? 1 : 0;
             }
             if constexpr (PENALTY) {
                 // bitmap of the penalised ids of row j in [v0, v1), and which slices hold one
@@ -785,55 +551,13 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
         return;
     }
 
-    if (warp == kMWarp) {
-        // ================= merge warp =================
-        // Polls the streaming warps' queues (lane q watches queue q) until every
-        // streaming warp has finished and every queue is drained.  The wait is bounded.
-        unsigned idle = 0;
-        while (true) {
-            const bool has = lane < kCWarps && s_mq_head[lane] != s_mq_tail[lane];
-            const unsigned qs = __ballot_sync(0xffffffffu, has);
-            if (qs != 0u) {
-                idle = 0;
-                const int q = __ffs(qs) - 1;
-                const int h = s_mq_head[q];
-                const int row = s_mq[q][h % kMQ];
-                __syncwarp();
-                merge_row<BF16, GREEDY, SOFTCAP, PENALTY>(P, row);
-                __syncwarp();
-                if (lane == 0) s_mq_head[q] = h + 1;
-                __syncwarp();
-                continue;
-            }
-            if (*reinterpret_cast<volatile int*>(&s_done) == kCWarps) {
-                // every push happened before its warp's increment of s_done
-                __threadfence_block();
-                const bool again = lane < kCWarps && s_mq_head[lane] != s_mq_tail[lane];
-                if (!__any_sync(0xffffffffu, again)) break;
-                continue;
-            }
-            if (++idle > (1u << 22)) {
-                if (lane == 0) raise_status(P.status, SPECNG_DEV_TIMEOUT);
-                break;
-            }
-            __nanosleep(idle < 64 ? 32 : 256);
-        }
-        return;
-    }
-
     // ================= streaming warps =================
-    // Per-lane accumulators live across the chunks of one row (a segment of
-    // the CTA's range); warps combine them once, at the segment's last chunk.
+    // The sum of exponentials of a segment is kept against a reference m, fixed
+    // at the segment's first value and raised only when a value passes it by
+    // more than 2^32 in the sum's units.
     const int ubase = warp * (32 * kVL);        // first 16-byte vector of my slice
     const int off0 = ubase * EPV + lane * EPV;  // chunk offset of vector 0's element 0
-    float thr = -INFINITY;
     float m = -INFINITY, s = 0.0f, msc = 0.0f;
-    Top2 tt = top2_empty();
-    int seg = 0, cfirst = 0;
-    int row = 0, excl = -1;
-    bool cand = false;
-    RowPhilox rp{};
-    bool fresh = true;
     int st = 0;
     unsigned fph = 0u;  // parity of the full barrier phase to wait for
     for (int n = 0; n < nwork; ++n) {
@@ -843,20 +567,8 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
         }
         const StageMeta& mt = s_meta[st];
         const int c = mt.c;
-        unsigned* rth = &s_rthr[seg % (kStages + 1)];
-        const bool seg_start = fresh;
-        if (seg_start) {
-            const int b = mt.b, j = mt.j;
-            row = b * K1 + j;
-            excl = mt.excl;
-            cand = !GREEDY && mt.cand != 0;
-            cfirst = c;
-            if (cand) {
-                NoiseKey nk = P.nk;
-                nk.seq = static_cast<uint32_t>(b);
-                rp = row_philox(nk, static_cast<uint32_t>(j));
-            }
-        }
+        const int row = mt.b * K1 + mt.j;
+        const bool dosum = !GREEDY && mt.sum != 0;
         const int v0 = c * CHUNK;
         const int v1 = min(P.V, v0 + CHUNK);
         const uint4* stage = reinterpret_cast<const uint4*>(s_stage + st * SB);
@@ -866,50 +578,34 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
 #pragma unroll
         for (int i = 0; i < kVL; ++i) rv[i] = stage[ubase + i * 32 + lane];
         // penalised elements of my lane (bit 8 i + e), only where the slice holds one
-        uint64_t pmk = 0u;
+        unsigned pmk = 0u;
         if constexpr (PENALTY) {
             if ((mt.penw >> warp) & 1u) {
 #pragma unroll
                 for (int i = 0; i < kVL; ++i) {
                     const int off = off0 + i * 32 * EPV;
-                    pmk |= static_cast<uint64_t>((bm[off >> 5] >> (off & 31)) & ((1u << EPV) - 1u)) << (8 * i);
+                    pmk |= ((bm[off >> 5] >> (off & 31)) & ((1u << EPV) - 1u)) << (8 * i);
                 }
             }
         }
-
-        // ---- streaming: lane maximum zl (bounds my transformed values, penalised ones
-        //      included), sum of exponentials
-        float zl = -INFINITY;
-        float lraw = -INFINITY;
-        uint32_t hv[kVL];  // packed vector maxima (bf16), or the fp32 maxima
+        float zv[kVL];  // largest transformed value of each of my vectors (an upper bound)
         if (full) {
-            if constexpr (BF16) {
+            float lraw = -INFINITY;
 #pragma unroll
-                for (int i = 0; i < kVL; ++i) hv[i] = as_u32(bf16x8_max2(rv[i]));
-                uint32_t hr[kVL];
-#pragma unroll
-                for (int i = 0; i < kVL; ++i) hr[i] = hv[i];
-#pragma unroll
-                for (int w2 = kVL / 2; w2 > 0; w2 >>= 1)
-#pragma unroll
-                    for (int i = 0; i < w2; ++i) hr[i] = as_u32(__hmax2(as_bf162(hr[i]), as_bf162(hr[i + w2])));
-                lraw = fmaxf(bf16lo(hr[0]), bf16hi(hr[0]));
-            } else {
-#pragma unroll
-                for (int i = 0; i < kVL; ++i) {
-                    const float f = fmaxf(fmaxf(__uint_as_float(rv[i].x), __uint_as_float(rv[i].y)),
-                                          fmaxf(__uint_as_float(rv[i].z), __uint_as_float(rv[i].w)));
-                    hv[i] = __float_as_uint(f);
-                    lraw = fmaxf(lraw, f);
+            for (int i = 0; i < kVL; ++i) {
+                float vm;
+                if constexpr (BF16) {
+                    const uint32_t h = as_u32(bf16x8_max2(rv[i]));
+                    vm = fmaxf(bf16lo(h), bf16hi(h));
+                } else {
+                    vm = fmaxf(fmaxf(__uint_as_float(rv[i].x), __uint_as_float(rv[i].y)),
+                               fmaxf(__uint_as_float(rv[i].z), __uint_as_float(rv[i].w)));
                 }
+                zv[i] = SOFTCAP ? transform_f32<true, false>(vm, false, P) : vm;
+                lraw = fmaxf(lraw, vm);
             }
-            zl = SOFTCAP ? transform_f32<true, false>(lraw, false, P) : lraw;
-            if constexpr (GREEDY) {
-                if (zl > m) m = zl;
-            } else {
-                // m is the segment's reference: fixed at its first value and raised only when a
-                // value passes it by more than 2^32 in the sum's units, so the exponentials of a
-                // chunk do not wait for the chunk's maximum
+            if (dosum) {
+                const float zl = SOFTCAP ? transform_f32<true, false>(lraw, false, P) : lraw;
                 if (!(m > -INFINITY)) {
                     m = zl;
                     msc = m * P.sc;
@@ -929,7 +625,8 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                         acc2[i & 3] = __fadd2_rn(acc2[i & 3], make_float2(ex2_approx(t.x), ex2_approx(t.y)));
                     }
                 }
-                float add = ((acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y)) + ((acc2[2].x + acc2[2].y) + (acc2[3].x + acc2[3].y));
+                float add = ((acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y)) +
+                            ((acc2[2].x + acc2[2].y) + (acc2[3].x + acc2[3].y));
                 if ((zl - m) * P.sc > 32.0f) {
                     // far above the reference: raise it and take the chunk again
                     s *= ex2_approx((m - zl) * P.sc);
@@ -948,19 +645,19 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                 s += add;
             }
             if constexpr (PENALTY) {
-                // the few penalised elements: replace their terms by the penalised ones (and
-                // raise the maximum if a penalty below 1 lifted one above it)
-                uint64_t pw = pmk;
+                // the few penalised elements: their penalised values join the vector's bound,
+                // and their terms of the sum are replaced by the penalised ones
+                unsigned pw = pmk;
                 while (pw != 0u) {
-                    const int bit = __ffsll(static_cast<long long>(pw)) - 1;
+                    const int bit = __ffs(pw) - 1;
                     pw &= pw - 1u;
                     const float xe = elem_of_stage<BF16>(stage, off0 + (bit >> 3) * 32 * EPV + (bit & 7));
                     const float zu = transform_f32<SOFTCAP, false>(xe, false, P);
                     const float zp = transform_f32<SOFTCAP, true>(xe, true, P);
-                    zl = fmaxf(zl, zp);
-                    if constexpr (GREEDY) {
-                        m = fmaxf(m, zp);
-                    } else {
+#pragma unroll
+                    for (int i = 0; i < kVL; ++i)
+                        if ((bit >> 3) == i) zv[i] = fmaxf(zv[i], zp);
+                    if (dosum) {
                         if ((zp - m) * P.sc > 32.0f) {
                             s *= ex2_approx((m - zp) * P.sc);
                             m = zp;
@@ -974,7 +671,7 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
             // partial vectors (a row's last chunk): exact transform element by element
 #pragma unroll
             for (int i = 0; i < kVL; ++i) {
-                hv[i] = BF16 ? 0xFF80FF80u : __float_as_uint(-INFINITY);
+                zv[i] = -INFINITY;
                 const int off = off0 + i * 32 * EPV;
                 const int nv = min(EPV, v1 - (v0 + off));
                 if (nv <= 0) continue;
@@ -984,11 +681,8 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                 for (int e = 0; e < EPV; ++e) {
                     if (e >= nv) break;
                     const float z = transform_f32<SOFTCAP, PENALTY>(x[e], (pmk >> (8 * i + e)) & 1u, P);
-                    lraw = fmaxf(lraw, x[e]);
-                    zl = fmaxf(zl, z);
-                    if constexpr (GREEDY) {
-                        m = fmaxf(m, z);
-                    } else {
+                    zv[i] = fmaxf(zv[i], z);
+                    if (dosum) {
                         if (!(m > -INFINITY) || (z - m) * P.sc > 32.0f) {
                             s = m > -INFINITY ? s * ex2_approx((m - z) * P.sc) : 0.0f;
                             m = z;
@@ -999,228 +693,56 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                 }
             }
         }
-
-        // ---- candidates
-        if constexpr (GREEDY) {
-            // top two transformed values (lower id on ties) within cand_delta of the best
-            // value any warp of the CTA has reached in this segment.  Without a penalty the
-            // lane maximum is itself a value of the row (the transform is monotone)
-            float gth = fmaxf(tt.s1, key_score(*reinterpret_cast<volatile unsigned*>(rth)));
-            if constexpr (!PENALTY) gth = fmaxf(gth, key_score(warp_best_key(zl)));
-            gth = gth > -INFINITY ? gth - cand_delta(gth) : -INFINITY;
-            if (zl >= gth) {
+        // ---- block maxima: vector row i of the warp (rows i, i + 1 for fp32) is one noise block
 #pragma unroll
-                for (int i = 0; i < kVL; ++i) {
-                    const int off = off0 + i * 32 * EPV;
-                    const int nv = min(EPV, v1 - (v0 + off));
-                    if (nv <= 0) continue;
-                    float x[EPV];
-                    unpack<BF16>(rv[i], x);
+        for (int i = 0; i < kVL; i += VPB) {
+            float zb = zv[i];
 #pragma unroll
-                    for (int e = 0; e < EPV; ++e) {
-                        if (e >= nv) break;
-                        const float z = transform_f32<SOFTCAP, PENALTY>(x[e], (pmk >> (8 * i + e)) & 1u, P);
-                        if (z >= gth) {
-                            top2_push(tt, z, v0 + off + e);
-                            gth = fmaxf(gth, tt.s1 - cand_delta(tt.s1));
-                        }
-                    }
-                }
-            }
-            const unsigned kw = warp_best_key(tt.s1);
-            if (lane == 0 && kw != 0u) atomicMax(rth, kw);
-        } else if (cand) {
-            int seeded = -1;
-            if (seg_start) {
-                // seed: every lane scores its largest raw element (any exact score bounds the
-                // best from below); the CTA's warps share the best seed
-                int am = -1;
-#pragma unroll
-                for (int i = kVL - 1; i >= 0; --i) {
-                    const int off = off0 + i * 32 * EPV;
-                    const int nv = min(EPV, v1 - (v0 + off));
-                    float x[EPV];
-                    unpack<BF16>(rv[i], x);
-#pragma unroll
-                    for (int e = EPV - 1; e >= 0; --e)
-                        if (e < nv && x[e] == lraw) am = off + e;
-                }
-                float t0 = -INFINITY;
-                if (am >= 0 && v0 + am != excl) {
-                    const float z = transform_f32<SOFTCAP, PENALTY>(elem_of_stage<BF16>(stage, am),
-                                                                    PENALTY && ((bm[am >> 5] >> (am & 31)) & 1u), P);
-                    const uint32_t v = static_cast<uint32_t>(v0 + am);
-                    const BlockNoise bk = mt.bn[am >> kNoiseBlockShift];
-                    t0 = z * P.invT - ln_fast(noise_exp_f32(rp, bk.M, bk.I, v));
-                    top2_push(tt, t0, static_cast<int>(v));
-                    seeded = static_cast<int>(v);
-                }
-                const unsigned k0 = warp_best_key(t0);
-                if (k0 != 0u) {
-                    const float b0 = key_score(k0);
-                    thr = fmaxf(thr, b0 - cand_delta(b0));
-                    if (lane == 0) atomicMax(rth, k0);
-                }
-            }
-            {
-                // adopt the best score another warp published for this segment
-                const float best = key_score(*reinterpret_cast<volatile unsigned*>(rth));
-                if (best > -INFINITY) thr = fmaxf(thr, best - cand_delta(best));
-            }
-            // gate: no score of my lane exceeds zl / T - (smallest ln M of the slice)
-            const float zlb = zl * P.invT;
-            const bool lpass = zlb - mt.wmin[warp] + bound_slack(zlb) >= thr;
-            if (__any_sync(0xffffffffu, lpass)) {
-                // block tests: every score of vector i is at most z / T - ln M_i; then the
-                // elements of the passing vectors that can reach the best
-                uint64_t msk = 0u;
-                if (lpass) {
-#pragma unroll
-                    for (int i = 0; i < kVL; ++i) {
-                        const int off = off0 + i * 32 * EPV;
-                        const float lnM = mt.bn[off >> kNoiseBlockShift].lnM;
-                        float zv;
-                        if constexpr (BF16) zv = fmaxf(bf16lo(hv[i]), bf16hi(hv[i]));
-                        else zv = __uint_as_float(hv[i]);
-                        if (SOFTCAP && full) zv = transform_f32<true, false>(zv, false, P);
-                        const unsigned pb = static_cast<unsigned>(pmk >> (8 * i)) & 0xFFu;
-                        const float zvb = zv * P.invT;
-                        if (!(pb != 0u || !full || zvb - lnM + bound_slack(zvb) >= thr)) continue;
-                        unsigned mi;
-                        if (full) {
-                            // z >= T (thr + ln M), in raw units
-                            const float zt = (thr + lnM) * P.T;
-                            float xt = zt;
-                            if constexpr (SOFTCAP) {
-                                // shrink by more than the fp32 error of c tanh(x / c) before
-                                // inverting: atanh is steep near |u| = 1
-                                float u = zt * P.invcap;
-                                u -= 1e-6f * fabsf(u) + 1e-7f;
-                                xt = u > 1.0f ? INFINITY : (u <= -1.0f ? -INFINITY : P.cap * atanhf(fminf(u, 1.0f - 1e-7f)));
-                            }
-                            xt -= 1e-5f * (1.0f + fabsf(xt));  // slack for the rounding of the transform
-                            if constexpr (BF16) {
-                                mi = bf16x8_ge_bits(rv[i], bf16x2_floor(xt));
-                            } else {
-                                mi = static_cast<unsigned>(__uint_as_float(rv[i].x) >= xt);
-                                mi |= static_cast<unsigned>(__uint_as_float(rv[i].y) >= xt) << 1;
-                                mi |= static_cast<unsigned>(__uint_as_float(rv[i].z) >= xt) << 2;
-                                mi |= static_cast<unsigned>(__uint_as_float(rv[i].w) >= xt) << 3;
-                            }
-                            mi |= pb;  // penalised: decided exactly below
-                        } else {
-                            const int nv = min(EPV, v1 - (v0 + off));
-                            mi = nv > 0 ? (1u << nv) - 1u : 0u;
-                        }
-                        msk |= static_cast<uint64_t>(mi) << (8 * i);
-                    }
-                    if (seeded >= 0) {
-                        const int so = seeded - v0 - off0;
-                        const int si = so / (32 * EPV), se = so - si * 32 * EPV;
-                        if (se >= 0 && se < EPV) msk &= ~(static_cast<uint64_t>(1) << (8 * si + se));
-                    }
-                }
-                // score the lane's candidates one per iteration, the warp in step
-                while (__any_sync(0xffffffffu, msk != 0u)) {
-                    int v = -1, loc = 0;
-                    float zb = -INFINITY;
-                    if (msk != 0u) {
-                        const int bit = __ffsll(static_cast<long long>(msk)) - 1;
-                        msk &= msk - 1u;
-                        loc = off0 + (bit >> 3) * 32 * EPV + (bit & 7);
-                        const bool pen = PENALTY && ((pmk >> bit) & 1u);
-                        zb = transform_f32<SOFTCAP, PENALTY>(elem_of_stage<BF16>(stage, loc), pen, P) * P.invT;
-                        v = v0 + loc;
-                    }
-                    const BlockNoise bk = mt.bn[loc >> kNoiseBlockShift];
-                    const bool live = v >= 0 && v != excl && zb - bk.lnM + bound_slack(zb) >= thr;
-                    if (__any_sync(0xffffffffu, live)) {
-                        const float E = noise_exp_f32(rp, bk.M, bk.I, static_cast<uint32_t>(v < 0 ? 0 : v));
-                        if (live) {
-                            const float score = zb - ln_fast(E);
-                            if (score >= thr) {
-                                top2_push(tt, score, v);
-                                thr = fmaxf(thr, tt.s1 - cand_delta(tt.s1));
-                            }
-                        }
-                    }
-                }
-                // share the warp's best score with the CTA
-                const unsigned kw = warp_best_key(tt.s1);
-                if (kw != 0u) {
-                    const float bw = key_score(kw);
-                    thr = fmaxf(thr, bw - cand_delta(bw));
-                    if (lane == 0) atomicMax(rth, kw);
-                }
-            }
+            for (int u = 1; u < VPB; ++u) zb = fmaxf(zb, zv[i + u]);
+            const unsigned key = __reduce_max_sync(0xffffffffu, zb > -INFINITY ? score_key(zb) : 0u);
+            const int e0 = v0 + (ubase + i * 32) * EPV;
+            if (lane == 0 && e0 < v1)
+                P.bmax[static_cast<size_t>(row) * P.nblk + (e0 >> kNoiseBlockShift)] = key_score(key);
         }
 
-        fresh = mt.seg_end != 0;
-        if (fresh) {
-            // ---- end of this row's segment: one partial for the segment
+        if (mt.seg_end && dosum) {
+            // ---- end of this row's segment: one record for the segment
             float pm = m, ps = s;
-            Top2 pt = tt;
-            if constexpr (!GREEDY) {
-                if (!(pm > -INFINITY)) ps = 0.0f;
+            if (!(pm > -INFINITY)) ps = 0.0f;
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    const float mo = __shfl_xor_sync(0xffffffffu, pm, off);
-                    const float so = __shfl_xor_sync(0xffffffffu, ps, off);
-                    ms_merge(pm, ps, mo, so, P.sc);
-                }
+            for (int off = 16; off > 0; off >>= 1) {
+                const float mo = __shfl_xor_sync(0xffffffffu, pm, off);
+                const float so = __shfl_xor_sync(0xffffffffu, ps, off);
+                ms_merge(pm, ps, mo, so, P.sc);
             }
-            pt = top2_warp_reduce(pt);
             int last = 0;
             if (lane == 0) {
-                s_slot[st][warp] = WarpPart{pm, ps, pt};
+                s_slot[st][warp] = SegSum{pm, ps};
                 __threadfence_block();
                 last = atomicAdd(&s_cnt[st], 1) == kCWarps - 1;
             }
             last = __shfl_sync(0xffffffffu, last, 0);
             if (last) {
                 __threadfence_block();
-                WarpPart wp = lane < kCWarps ? s_slot[st][lane] : WarpPart{-INFINITY, 0.0f, top2_empty()};
+                const SegSum wp = lane < kCWarps ? s_slot[st][lane] : SegSum{-INFINITY, 0.0f};
                 float cm = wp.m, cs = wp.s;
-                Top2 ct = wp.t;
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) {
                     const float mo = __shfl_xor_sync(0xffffffffu, cm, off);
                     const float so = __shfl_xor_sync(0xffffffffu, cs, off);
                     ms_merge(cm, cs, mo, so, P.sc);
-                    ct = top2_merge(ct, top2_shfl_xor(ct, off));
                 }
-                int merge_now = 0;
                 if (lane == 0) {
-                    // keyed by the segment's last chunk; a written partial is never all-zero
-                    st_partial(P.part + static_cast<size_t>(row) * P.nchunk + c, GREEDY ? 0.0f : cm,
-                               GREEDY ? 1.0f : cs, ct);
+                    // keyed by the segment's last chunk; a written record is never all-zero
+                    P.part[static_cast<size_t>(row) * P.nchunk + c] = SegSum{cm, cs};
                     s_cnt[st] = 0;
-                    *rth = 0u;  // every warp is past this segment: the slot is free
-                    // the CTA that completes the row's chunks merges it
-                    __threadfence();
-                    const unsigned nseg = static_cast<unsigned>(c - cfirst + 1);
-                    const unsigned prev = atomicAdd(&P.row_ticket[row], nseg);
-                    if (prev + nseg == static_cast<unsigned>(P.nchunk)) {
-                        __threadfence();
-                        const int tl = s_mq_tail[warp];
-                        if (tl - s_mq_head[warp] < kMQ) {
-                            s_mq[warp][tl % kMQ] = row;
-                            __threadfence_block();
-                            s_mq_tail[warp] = tl + 1;
-                        } else {
-                            merge_now = 1;  // queue full: merge here
-                        }
-                    }
                 }
-                merge_now = __shfl_sync(0xffffffffu, merge_now, 0);
-                if (merge_now) merge_row<BF16, GREEDY, SOFTCAP, PENALTY>(P, row);
             }
+        }
+        if (mt.seg_end) {
             m = -INFINITY;
             s = 0.0f;
             msc = 0.0f;
-            tt = top2_empty();
-            thr = -INFINITY;
-            ++seg;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_empty[st]);
@@ -1229,10 +751,512 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
             fph ^= 1u;
         }
     }
-    __syncwarp();
-    if (lane == 0) {
-        __threadfence_block();
-        atomicAdd(&s_done, 1);
+}
+
+// ---------------------------------------------------------------- K2
+// Decision kernel: one CTA of four warps per sequence.
+//   1. The accept tests (T > 0): warp w takes rows w, w + 4, ... < k_eff; the
+//      log-sum-exp of a row comes from its segment sums (fp64), and the test
+//      of d_{j+1} is taken in fp32 unless it is within 1e-4 of the boundary,
+//      then in fp64.  At T = 0 every row 0..k_eff gets its argmax instead:
+//      the blocks whose largest value is within the tie margin of the best
+//      value found are read again.
+//   2. a = the first rejection (k_eff when none).
+//   3. The token at row a (T > 0): Gumbel-max over the row, draft d_{a+1}
+//      left out for a point-mass draft.  Each block's draw gives M and its
+//      slot; the bound z_max / T - ln M of every block goes to shared memory.
+//      Each warp reads again the block with its largest bound and each lane
+//      scores its largest element there, which starts the best; then only the
+//      blocks whose bound reaches the best are read again (eight per warp at
+//      once), and the elements whose own bound z / T - ln M reaches it are
+//      scored (per-id draw, E_v = M + F_v).  The two best fp32 scores are
+//      re-scored in fp64 when they are within the fp32 error of each other.
+//      With dense q the residual pass samples row a instead; this sample is
+//      its fallback for an all-zero residual.
+//   4. Epilogue: tokens, accept length, kv_len, EMA.
+
+constexpr int kSW = 8;                          // warps per sequence
+constexpr int kST = kSW * 32;
+constexpr int kBatch = 8;                       // blocks a warp reads again at once
+constexpr int kQCap = 320;                      // candidate queue entries per warp (>= 31 + 256)
+constexpr int kPenSlots = 2 * SPECNG_MAX_REP_WINDOW;
+constexpr int kPenBits = 9;
+static_assert((1 << kPenBits) == kPenSlots, "penalty table size");
+static_assert(SPECNG_MAX_K + 1 <= kST, "one thread per output token");
+
+// Dynamic shared memory of the decision kernel at T > 0: the block scratch
+// (when it fits), each warp's staging of a batch of blocks, and each warp's
+// candidate queue (id, staging index).
+__host__ __device__ constexpr size_t k2_stage_bytes(bool bf16) { return static_cast<size_t>(kSW) * kBatch * 32 * (bf16 ? 1 : 2) * 16; }
+__host__ __device__ inline size_t k2_blk_bytes(int nblk) {
+    return nblk <= kSmemBlkCap ? (static_cast<size_t>(nblk) * kBlkScratchBytes + 15) / 16 * 16 : 0;
+}
+__host__ __device__ inline size_t k2_dyn_smem(int nblk, bool bf16) {
+    return k2_blk_bytes(nblk) + k2_stage_bytes(bf16) + static_cast<size_t>(kSW) * kQCap * 8;
+}
+
+// Open-addressed table of the history tail of the penalty window: the token
+// and its latest position in the tail (-1 = empty slot).
+__device__ __forceinline__ uint32_t pen_hash(int v) { return (static_cast<uint32_t>(v) * 2654435761u) >> (32 - kPenBits); }
+
+// Is id v in the penalty window of row j (the last W tokens of the history
+// tail ++ d_1..d_j)?  key / pos: the table above; d: the drafts; nh: the
+// tail's length.  Out of line: it is called from several places.
+static __device__ __noinline__ bool pen_lookup(const int* key, const int* pos, const int* d, int nh, int W, int v, int j) {
+    const int total = nh + j;
+    const int start = total - (total < W ? total : W);
+    uint32_t h = pen_hash(v);
+    for (int probe = 0; probe < kPenSlots; ++probe) {
+        const int k = key[h];
+        if (k == v) {
+            if (pos[h] >= start) return true;
+            break;
+        }
+        if (k == -1) break;
+        h = (h + 1u) & (kPenSlots - 1u);
+    }
+    for (int i = start > nh ? start - nh : 0; i < j; ++i)
+        if (d[i] == v) return true;
+    return false;
+}
+
+template <bool BF16, bool GREEDY, bool SOFTCAP, bool PENALTY>
+__global__ void __launch_bounds__(kST) verify_seq_kernel(const VerifyDev P) {
+    constexpr int EPV = ElemTraits<BF16>::EPV;
+    constexpr int BLK = 1 << kNoiseBlockShift;
+    constexpr int VPL = BLK / (32 * EPV);  // 16-byte vectors per lane per block (bf16 1, fp32 2)
+    constexpr int NE = VPL * EPV;          // elements per lane per block
+    extern __shared__ __align__(128) uint8_t s_dyn[];
+    __shared__ int s_pkey[PENALTY ? kPenSlots : 1];
+    __shared__ int s_ppos[PENALTY ? kPenSlots : 1];
+    __shared__ int s_d[SPECNG_MAX_K + 1];
+    __shared__ double s_lse[SPECNG_MAX_K + 1];
+    __shared__ int s_acc[SPECNG_MAX_K + 1];
+    __shared__ int s_arg[SPECNG_MAX_K + 1];
+    __shared__ Top2 s_top[kSW];
+    __shared__ unsigned s_thr;
+    __shared__ int s_nl;
+    __shared__ int s_y;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b = blockIdx.x;
+    const int K1 = P.K + 1;
+    int kb;
+    const int keff = gate_keff(P, b, &kb, tid == 0);
+    const bool dense = P.q != nullptr;
+    NoiseKey nk = P.nk;
+    nk.seq = static_cast<uint32_t>(b);
+    int nh = 0;
+    if (tid < keff) {
+        const int d = P.drafts[b * P.K + tid];
+        s_d[tid] = d;
+        if (!(d >= 0 && d < P.V)) raise_status(P.status, SPECNG_DEV_TOKEN_OOR);
+    }
+    if (tid == 0) {
+        s_thr = 0u;
+        s_nl = 0;
+    }
+    if constexpr (PENALTY) {
+        int L = P.lens[b];
+        L = L < 0 ? 0 : (static_cast<int64_t>(L) > P.hist_stride ? static_cast<int>(P.hist_stride) : L);
+        nh = L < P.W ? L : P.W;
+        for (int t = tid; t < kPenSlots; t += kST) {
+            s_pkey[t] = -1;
+            s_ppos[t] = -1;
+        }
+        __syncthreads();
+        const int* tail = P.hist + static_cast<size_t>(b) * P.hist_stride + (L - nh);
+        for (int t = tid; t < nh; t += kST) {
+            const int v = tail[t];
+            if (v < 0) continue;  // matches no id
+            uint32_t h = pen_hash(v);
+            for (int probe = 0; probe < kPenSlots; ++probe) {
+                const int old = atomicCAS(&s_pkey[h], -1, v);
+                if (old == -1 || old == v) {
+                    atomicMax(&s_ppos[h], t);
+                    break;
+                }
+                h = (h + 1u) & (kPenSlots - 1u);
+            }
+        }
+    }
+    __syncthreads();
+
+    auto pen_of = [&](int v, int j) -> bool {
+        if constexpr (!PENALTY) return false;
+        return pen_lookup(s_pkey, s_ppos, s_d, nh, P.W, v, j);
+    };
+    auto rowp_of = [&](int row) {
+        return static_cast<const char*>(P.logits) + static_cast<size_t>(row) * P.V * ElemTraits<BF16>::SIZE;
+    };
+    // lane's vectors of block q of a row
+    auto load_block = [&](const char* rowp, int q, uint4* r) {
+#pragma unroll
+        for (int u = 0; u < VPL; ++u) {
+            const int e0 = q * BLK + (u * 32 + lane) * EPV;
+            r[u] = e0 < P.V ? load_vec<BF16>(rowp, e0, P.V, P.aligned) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    };
+    auto elem_id = [&](int q, int k) { return q * BLK + ((k / EPV) * 32 + lane) * EPV + (k % EPV); };
+
+    // ---- 1. accept tests (T > 0) / argmax of every row (T = 0)
+    for (int j = warp; j <= keff; j += kSW) {
+        const int row = b * K1 + j;
+        if constexpr (GREEDY) {
+            // the block with the largest value first, then every block within the tie margin
+            const float* bmx = P.bmax + static_cast<size_t>(row) * P.nblk;
+            const char* rowp = rowp_of(row);
+            float lb = -INFINITY;
+            int lq = -1;
+            for (int q = lane; q < P.nblk; q += 32) {
+                const float x = bmx[q];
+                if (x > lb || lq < 0) { lb = x; lq = q; }
+            }
+            const unsigned kq = __reduce_max_sync(0xffffffffu, score_key(lb));
+            const unsigned own = __ballot_sync(0xffffffffu, score_key(lb) == kq);
+            const int q0 = __shfl_sync(0xffffffffu, lq, __ffs(own) - 1);
+            Top2 t = top2_empty();
+            auto scan = [&](int q, float gth) {
+                uint4 r[VPL];
+                load_block(rowp, q, r);
+#pragma unroll
+                for (int u = 0; u < VPL; ++u) {
+                    float x[EPV];
+                    unpack<BF16>(r[u], x);
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) {
+                        const int v = elem_id(q, u * EPV + e);
+                        if (v >= P.V) continue;
+                        const float z = transform_f32<SOFTCAP, PENALTY>(x[e], PENALTY && pen_of(v, j), P);
+                        if (z >= gth) top2_push(t, z, v);
+                    }
+                }
+            };
+            scan(q0, -INFINITY);
+            const unsigned kw = warp_best_key(t.s1);
+            const float gth = kw ? key_score(kw) - cand_delta(key_score(kw)) : -INFINITY;
+            for (int qb = 0; qb < P.nblk; qb += 32) {
+                const int q = qb + lane;
+                unsigned pass = __ballot_sync(0xffffffffu, q < P.nblk && q != q0 && bmx[q] >= gth);
+                while (pass != 0u) {
+                    const int qq = qb + __ffs(pass) - 1;
+                    pass &= pass - 1u;
+                    scan(qq, gth);
+                }
+            }
+            t = top2_warp_reduce(t);
+            int y = t.i1;
+            if (t.i2 >= 0 && t.s2 >= t.s1 - cand_delta(t.s1)) {
+                if (lane == 0) {
+                    const double z1 = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, t.i1),
+                                                                      PENALTY && pen_of(t.i1, j), P);
+                    const double z2 = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, t.i2),
+                                                                      PENALTY && pen_of(t.i2, j), P);
+                    if (better64(z2, t.i2, z1, t.i1)) y = t.i2;
+                }
+                y = __shfl_sync(0xffffffffu, y, 0);
+            }
+            if (lane == 0) {
+                s_arg[j] = y;
+                s_acc[j] = j < keff && s_d[j] >= 0 && s_d[j] < P.V && s_d[j] == y;
+            }
+        } else {
+            if (j == keff) break;
+            // the draft's logit and q first: their latency overlaps the sums'
+            const int d = s_d[j];
+            const bool dv = d >= 0 && d < P.V;
+            float xd = 0.0f, qdf = 1.0f;
+            if (lane == 0 && dv) {
+                xd = static_cast<float>(raw_logit_f64<BF16>(P.logits, row, P.V, d));
+                if (dense) qdf = P.q[(static_cast<size_t>(b) * P.K + j) * P.V + d];
+            }
+            SegSum* pr = P.part + static_cast<size_t>(row) * P.nchunk;
+            float mf = -INFINITY;
+            for (int cc = lane; cc < P.nchunk; cc += 32) {
+                const float2 p = __ldcg(reinterpret_cast<const float2*>(pr + cc));
+                if (p.y != 0.0f || __float_as_uint(p.x) != 0u) mf = fmaxf(mf, p.x);
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mf = fmaxf(mf, __shfl_xor_sync(0xffffffffu, mf, off));
+            double S = 0.0;
+            for (int cc = lane; cc < P.nchunk; cc += 32) {
+                const float2 p = __ldcg(reinterpret_cast<const float2*>(pr + cc));
+                if ((p.y != 0.0f || __float_as_uint(p.x) != 0u) && p.x > -INFINITY)
+                    S += static_cast<double>(p.y) * static_cast<double>(expf((p.x - mf) * P.invT));
+            }
+            S = warp_sum_f64(S);
+            __syncwarp();
+            for (int cc = lane; cc < P.nchunk; cc += 32) pr[cc] = SegSum{0.0f, 0.0f};  // leave the workspace zeroed
+            const double lse = static_cast<double>(mf) / P.Td + log(S);
+            if (lane == 0) {
+                if (!(S > 0.0 && S < INFINITY && mf < INFINITY)) raise_status(P.status, SPECNG_DEV_NONFINITE);
+                int accepted = 0;
+                if (dv) {
+                    const double qd = static_cast<double>(qdf);
+                    const bool pend = pen_of(d, j);
+                    const double u = accept_uniform_f64(nk, static_cast<uint32_t>(j + 1));
+                    const float lp = transform_f32<SOFTCAP, PENALTY>(xd, pend, P) * P.invT - static_cast<float>(lse);
+                    const float lr = logf(static_cast<float>(u)) + logf(static_cast<float>(qd));
+                    if (lr < lp - 1e-4f * (1.0f + fabsf(lp))) {
+                        accepted = 1;
+                    } else if (lr > lp + 1e-4f * (1.0f + fabsf(lp))) {
+                        accepted = 0;
+                    } else {
+                        const double zd = transform_f64<SOFTCAP, PENALTY>(static_cast<double>(xd), pend, P);
+                        accepted = u * qd <= exp(zd / P.Td - lse);
+                    }
+                }
+                s_acc[j] = accepted;
+                s_lse[j] = lse;
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- 2. acceptance length
+    int a = keff;
+    for (int i = 0; i < keff; ++i)
+        if (!s_acc[i]) { a = i; break; }
+    const int da = a < keff ? s_d[a] : -1;
+    const bool dvalid = da >= 0 && da < P.V;
+    const bool need = dense && !GREEDY && a < keff && dvalid;
+
+    // ---- 3. the token at row a
+    int y;
+    if constexpr (GREEDY) {
+        y = s_arg[a];
+    } else {
+        const int row = b * K1 + a;
+        const int excl = (!dense && a < keff && dvalid) ? da : -1;
+        const float* bmx = P.bmax + static_cast<size_t>(row) * P.nblk;
+        const char* rowp = rowp_of(row);
+        const int nblk = P.nblk;
+        uint8_t* scr = nblk <= kSmemBlkCap ? s_dyn : P.blkws + static_cast<size_t>(b) * nblk * kBlkScratchBytes;
+        float* s_bnd = reinterpret_cast<float*>(scr);
+        float* s_M = s_bnd + nblk;
+        int* s_I = reinterpret_cast<int*>(s_M + nblk);
+        int* s_list = s_I + nblk;
+        uint4* stg = reinterpret_cast<uint4*>(s_dyn + k2_blk_bytes(nblk)) + warp * (kBatch * 32 * VPL);
+        int2* que = reinterpret_cast<int2*>(s_dyn + k2_blk_bytes(nblk) + k2_stage_bytes(BF16)) + warp * kQCap;
+        const RowPhilox rp = row_philox(nk, static_cast<uint32_t>(a));
+        // block draws and bounds (the blocks' values are loaded first, so their
+        // latencies overlap); each warp's block with the largest value (a large
+        // bound more often comes from a small M, whose block rarely holds the best)
+        float lb = -INFINITY;
+        int lq = -1;
+        for (int q0 = tid; q0 < nblk; q0 += 4 * kST) {
+            float zq[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) zq[i] = q0 + i * kST < nblk ? bmx[q0 + i * kST] : -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int q = q0 + i * kST;
+                if (q >= nblk) break;
+                const BlockNoise bn = block_noise(nk, static_cast<uint32_t>(q), static_cast<uint32_t>(a));
+                s_bnd[q] = zq[i] * P.invT - bn.lnM;
+                s_M[q] = bn.M;
+                s_I[q] = bn.I;
+                if (zq[i] > lb) { lb = zq[i]; lq = q; }
+            }
+        }
+        __syncwarp();
+        // seed: each lane scores its largest element of the warp's seed block
+        {
+            const unsigned kq = warp_best_key(lb);
+            const unsigned own = __ballot_sync(0xffffffffu, kq != 0u && lb > -INFINITY && score_key(lb) == kq);
+            const int q = own ? __shfl_sync(0xffffffffu, lq, __ffs(own) - 1) : -1;
+            float sc = -INFINITY;
+            if (q >= 0) {
+                uint4 r[VPL];
+                load_block(rowp, q, r);
+                float xb = -INFINITY;
+                int vb = -1;
+#pragma unroll
+                for (int u = 0; u < VPL; ++u) {
+                    float x[EPV];
+                    unpack<BF16>(r[u], x);
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) {
+                        const int v = elem_id(q, u * EPV + e);
+                        if (v < P.V && v != excl && (vb < 0 || x[e] > xb)) { xb = x[e]; vb = v; }
+                    }
+                }
+                if (vb >= 0) {
+                    const float zb = transform_f32<SOFTCAP, PENALTY>(xb, PENALTY && pen_of(vb, a), P) * P.invT;
+                    sc = zb - ln_fast(noise_exp_f32(rp, s_M[q], s_I[q], static_cast<uint32_t>(vb)));
+                }
+            }
+            const unsigned kw = warp_best_key(sc);
+            if (kw != 0u && lane == 0) atomicMax(&s_thr, kw);
+        }
+        __syncthreads();
+        float thr = -INFINITY;
+        if (s_thr != 0u) thr = key_score(s_thr) - cand_delta(key_score(s_thr));
+        // the blocks whose bound reaches the best
+        for (int qb = warp * 32; qb < nblk; qb += kST) {
+            const int q = qb + lane;
+            const bool pass = q < nblk && s_bnd[q] + bound_slack(s_bnd[q]) >= thr;
+            const unsigned bal = __ballot_sync(0xffffffffu, pass);
+            int at = 0;
+            if (lane == 0 && bal) at = atomicAdd(&s_nl, __popc(bal));
+            at = __shfl_sync(0xffffffffu, at, 0);
+            if (pass) s_list[at + __popc(bal & ((1u << lane) - 1u))] = q;
+        }
+        __syncthreads();
+        const int nl = s_nl;
+        Top2 t = top2_empty();
+        // score the queued candidates, one per lane per round: the exact value
+        // (penalty) and the element's own draw
+        auto flush = [&](int qn) {
+            __syncwarp();
+            for (int i0 = 0; i0 < qn; i0 += 32) {
+                const int i = i0 + lane;
+                if (i < qn) {
+                    const int2 en = que[i];
+                    const int v = en.x;
+                    const int q = v >> kNoiseBlockShift;
+                    const float xv = elem_of_stage<BF16>(stg, en.y);
+                    const float zb = transform_f32<SOFTCAP, PENALTY>(xv, PENALTY && pen_of(v, a), P) * P.invT;
+                    const float Mq = s_M[q];
+                    const float lnMq = ln_fast(Mq);
+                    if (zb - lnMq + bound_slack(zb - lnMq) >= thr) {
+                        const float score = zb - ln_fast(noise_exp_f32(rp, Mq, s_I[q], static_cast<uint32_t>(v)));
+                        if (score >= thr) {
+                            top2_push(t, score, v);
+                            thr = fmaxf(thr, t.s1 - cand_delta(t.s1));
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            const unsigned kw = warp_best_key(t.s1);
+            if (kw != 0u) thr = fmaxf(thr, key_score(kw) - cand_delta(key_score(kw)));
+        };
+        for (int l0 = warp * kBatch; l0 < nl; l0 += kSW * kBatch) {
+            // blocks whose bound no longer reaches the best found so far are skipped;
+            // lane h < kBatch holds block h of the batch
+            const unsigned kc0 = __shfl_sync(0xffffffffu, max(*reinterpret_cast<volatile unsigned*>(&s_thr), warp_best_key(t.s1)), 0);
+            const float thw = kc0 != 0u ? key_score(kc0) - cand_delta(key_score(kc0)) : -INFINITY;
+            thr = fmaxf(thr, thw);
+            int myq = -1;
+            if (lane < kBatch && l0 + lane < nl) {
+                const int q = s_list[l0 + lane];
+                if (s_bnd[q] + bound_slack(s_bnd[q]) >= thw) myq = q;
+            }
+            // the batch's blocks into the warp's staging, all loads in flight together
+#pragma unroll
+            for (int h = 0; h < kBatch; ++h) {
+                const int q = __shfl_sync(0xffffffffu, myq, h);
+                if (q >= 0) {
+#pragma unroll
+                    for (int u = 0; u < VPL; ++u) {
+                        const int e0 = q * BLK + (u * 32 + lane) * EPV;
+                        stg[(h * VPL + u) * 32 + lane] =
+                            e0 < P.V ? load_vec<BF16>(rowp, e0, P.V, P.aligned) : make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+            }
+            __syncwarp();
+            // the elements whose bound z / T - ln M reaches the best go to the queue (a
+            // bound of z first: a penalty above 1 only lowers it)
+            int qn = 0;
+#pragma unroll 1
+            for (int h = 0; h < kBatch; ++h) {
+                const int q = __shfl_sync(0xffffffffu, myq, h);
+                if (q < 0) continue;  // warp-uniform
+                const float lnMq = ln_fast(s_M[q]);
+                unsigned ce = 0u;
+#pragma unroll
+                for (int u = 0; u < VPL; ++u) {
+                    float x[EPV];
+                    unpack<BF16>(stg[(h * VPL + u) * 32 + lane], x);
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) {
+                        const int k = u * EPV + e;
+                        const int v = elem_id(q, k);
+                        float zb = transform_f32<SOFTCAP, false>(x[e], false, P);
+                        if (PENALTY && P.rep < 1.0f) zb = fmaxf(zb, transform_f32<SOFTCAP, true>(x[e], true, P));
+                        zb *= P.invT;
+                        if (v < P.V && v != excl && zb - lnMq + bound_slack(zb - lnMq) >= thr) ce |= 1u << k;
+                    }
+                }
+                const int c = __popc(ce);
+                int incl = c;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y2 = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y2;
+                }
+                int at = qn + incl - c;
+                while (ce != 0u) {
+                    const int k = __ffs(ce) - 1;
+                    ce &= ce - 1u;
+                    que[at++] = make_int2(elem_id(q, k), ((h * VPL + k / EPV) * 32 + lane) * EPV + k % EPV);
+                }
+                qn += __shfl_sync(0xffffffffu, incl, 31);
+                if (qn >= 32) {
+                    flush(qn);
+                    qn = 0;
+                }
+            }
+            if (qn > 0) flush(qn);
+            __syncwarp();  // the staging is read before the next batch overwrites it
+            // share the best with the other warps
+            const unsigned kw = warp_best_key(t.s1);
+            if (kw != 0u && lane == 0) atomicMax(&s_thr, kw);
+            const unsigned kc = max(*reinterpret_cast<volatile unsigned*>(&s_thr), kw);
+            if (kc != 0u) thr = fmaxf(thr, key_score(kc) - cand_delta(key_score(kc)));
+        }
+        t = top2_warp_reduce(t);
+        if (lane == 0) s_top[warp] = t;
+        __syncthreads();
+        if (warp == 0) {
+            Top2 tw = lane < kSW ? s_top[lane] : top2_empty();
+#pragma unroll
+            for (int off = kSW / 2; off > 0; off >>= 1) tw = top2_merge(tw, top2_shfl_xor(tw, off));
+            int w = tw.i1;
+            if (lane == 0 && tw.i2 >= 0 && tw.s2 >= tw.s1 - cand_delta(tw.s1)) {
+                double sc[2];
+                for (int h = 0; h < 2; ++h) {
+                    const int id = h == 0 ? tw.i1 : tw.i2;
+                    const double z = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, id),
+                                                                     PENALTY && pen_of(id, a), P);
+                    sc[h] = z / P.Td - log(noise_exp_f64(nk, static_cast<uint32_t>(id), static_cast<uint32_t>(a)));
+                }
+                if (better64(sc[1], tw.i2, sc[0], tw.i1)) w = tw.i2;
+            }
+            if (lane == 0) s_y = w;
+        }
+        __syncthreads();
+        y = s_y;
+    }
+
+    // ---- 4. epilogue (with dense q the residual pass writes the token at row a)
+    if (tid < K1)
+        P.out_tokens[static_cast<size_t>(b) * K1 + tid] = tid < a ? s_d[tid] : (tid == a && !need ? y : -1);
+    if (tid == 0) {
+        P.out_accept[b] = a;
+        P.kv_len[b] = P.kv_len[b] - kb + a;
+        if (keff > 0) {
+            // (1 - tau) * ema + tau * a / k_eff, rounded step by step (no contraction)
+            const double tau = static_cast<double>(P.tau);
+            const double rate = static_cast<double>(a) / static_cast<double>(keff);
+            P.ema[b] = static_cast<float>(
+                __dadd_rn(__dmul_rn(1.0 - tau, static_cast<double>(P.ema[b])), __dmul_rn(tau, rate)));
+        }
+        if (need) {
+            RowRes rr;
+            rr.lse = s_lse[a];
+            rr.winner = y;
+            rr.accepted = 0;
+            P.rowres[b * K1 + a] = rr;
+            SeqRes sr;
+            sr.a = a;
+            sr.keff = keff;
+            sr.need_residual = 1;
+            sr.pad = 0;
+            P.seqres[b] = sr;
+        }
     }
 }
 
@@ -1529,6 +1553,22 @@ cudaError_t launch_stream(const VerifyDev& P, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+template <bool BF16, bool G, bool C, bool R>
+cudaError_t launch_seq(const VerifyDev& P, cudaStream_t s) {
+    // block scratch of the sampled row (when it fits), staging and candidate queues
+    const size_t smem = G ? 0 : k2_dyn_smem(P.nblk, BF16);
+    static bool configured = false;
+    if (!G && !configured) {
+        const cudaError_t e = cudaFuncSetAttribute(verify_seq_kernel<BF16, G, C, R>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(k2_dyn_smem(kSmemBlkCap, BF16)));
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    verify_seq_kernel<BF16, G, C, R><<<static_cast<unsigned>(P.B), kST, smem, s>>>(P);
+    return cudaGetLastError();
+}
+
 template <bool BF16, bool C, bool R>
 cudaError_t launch_residual(const VerifyDev& P, cudaStream_t s) {
     const unsigned grid = static_cast<unsigned>(P.B) * static_cast<unsigned>(P.nchunk2);
@@ -1536,14 +1576,23 @@ cudaError_t launch_residual(const VerifyDev& P, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+template <bool BF16, bool G, bool C, bool R>
+cudaError_t launch_all(const VerifyDev& P, bool dense, cudaStream_t s) {
+    cudaError_t e = launch_stream<BF16, G, C, R>(P, s);
+    if (e != cudaSuccess) return e;
+    e = launch_seq<BF16, G, C, R>(P, s);
+    if (e != cudaSuccess || !dense || G) return e;
+    return launch_residual<BF16, C, R>(P, s);
+}
+
 template <bool BF16, bool G>
-cudaError_t launch_stream_cr(const VerifyDev& P, bool c, bool r, cudaStream_t s) {
-    if (c) return r ? launch_stream<BF16, G, true, true>(P, s) : launch_stream<BF16, G, true, false>(P, s);
-    return r ? launch_stream<BF16, G, false, true>(P, s) : launch_stream<BF16, G, false, false>(P, s);
+cudaError_t launch_all_cr(const VerifyDev& P, bool c, bool r, bool dense, cudaStream_t s) {
+    if (c) return r ? launch_all<BF16, G, true, true>(P, dense, s) : launch_all<BF16, G, true, false>(P, dense, s);
+    return r ? launch_all<BF16, G, false, true>(P, dense, s) : launch_all<BF16, G, false, false>(P, dense, s);
 }
 
 // The kernels of one spec_verify call for one logits dtype: the streaming
-// kernel (with the merges), then, for dense q at T > 0, the residual pass.
+// kernel, the decision kernel and, for dense q at T > 0, the residual pass.
 template <bool BF16>
 cudaError_t launch_verify_dtype(const VerifyDev& P, bool greedy, bool softcap, bool penalty, bool dense,
                                 cudaStream_t s);
@@ -1551,11 +1600,8 @@ cudaError_t launch_verify_dtype(const VerifyDev& P, bool greedy, bool softcap, b
 template <bool BF16>
 cudaError_t launch_verify_impl(const VerifyDev& P, bool greedy, bool softcap, bool penalty, bool dense,
                                cudaStream_t s) {
-    cudaError_t e = greedy ? launch_stream_cr<BF16, true>(P, softcap, penalty, s)
-                           : launch_stream_cr<BF16, false>(P, softcap, penalty, s);
-    if (e != cudaSuccess || !dense || greedy) return e;
-    if (softcap) return penalty ? launch_residual<BF16, true, true>(P, s) : launch_residual<BF16, true, false>(P, s);
-    return penalty ? launch_residual<BF16, false, true>(P, s) : launch_residual<BF16, false, false>(P, s);
+    return greedy ? launch_all_cr<BF16, true>(P, softcap, penalty, dense, s)
+                  : launch_all_cr<BF16, false>(P, softcap, penalty, dense, s);
 }
 
 }  // namespace specng
