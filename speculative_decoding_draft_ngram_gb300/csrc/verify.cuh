@@ -12,7 +12,8 @@
 //
 // The noise E_v is drawn per block of 256 ids (block minimum M and its slot,
 // then E_v = M + F_v for the others; see common.cuh), so a score of a block is
-// at most z_max / T - ln M with z_max the block's largest transformed logit.
+// at most z_max / T - ln M, with z_max the transform of the block's largest
+// logit (a bound of the block's transformed logits).
 // The streaming pass (bandwidth only) leaves, per row, the segment sums of
 // the softmax and every block's z_max; the decision kernel takes the accept
 // tests from the sums, and only then samples, at row a alone, reading again
@@ -90,7 +91,7 @@ struct VerifyDev {
     int32_t* out_tokens;
     int32_t* out_accept;
     SegSum* part;             // [B (K + 1)][nchunk] segment sums, at each segment's last chunk
-    float* bmax;              // [B (K + 1)][nblk] largest transformed logit of each noise block
+    float* bmax;              // [B (K + 1)][nblk] largest raw logit of each noise block
     uint8_t* blkws;           // [B][nblk][16] decision-kernel block scratch (rows past kSmemBlkCap blocks)
     RowRes* rowres;
     SeqRes* seqres;
@@ -312,6 +313,22 @@ __device__ __forceinline__ int gate_keff(const VerifyDev& P, int b, int* kb_out,
 // Slack of the block bound: covers the fp32 rounding of z / T and ln M.
 __device__ __forceinline__ float bound_slack(float z) { return 1e-5f * (1.0f + fabsf(z)); }
 
+// Elements n.. of a 16-byte vector set to -inf (n <= 0: all of them).
+template <bool BF16>
+__device__ __forceinline__ uint4 mask_tail(uint4 r, int n) {
+    uint32_t w[4] = {r.x, r.y, r.z, r.w};
+    if constexpr (BF16) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            if (e >= n) w[e >> 1] = (e & 1) ? ((w[e >> 1] & 0x0000FFFFu) | 0xFF800000u) : ((w[e >> 1] & 0xFFFF0000u) | 0xFF80u);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (e >= n) w[e] = 0xFF800000u;
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // ---------------------------------------------------------------- K1
 // Streaming kernel: bandwidth only.  Persistent and warp-specialised, one CTA
 // per SM; the active row-chunks of the call (rows 0..k_eff of every sequence,
@@ -324,11 +341,12 @@ __device__ __forceinline__ float bound_slack(float z) { return 1e-5f * (1.0f + f
 //     registers one sequence ahead, so no global round trip stalls the copies.
 //   * Sixteen streaming warps each own a 2 KB slice of every chunk.  A warp's
 //     vector row (32 lanes x one 16-byte vector) of a bf16 chunk is one noise
-//     block (two rows for fp32): its largest transformed value goes to the
-//     workspace.  The rows that carry an accept test (j < k_eff, T > 0) also
-//     add their exponentials to a sum kept against a segment reference (so
-//     the sum does not wait for each chunk's maximum); at the last chunk of a
-//     row segment the warps combine their sums into one record.
+//     block (two rows for fp32): its largest raw logit goes to the workspace
+//     (packed maxima reduced across the warp).  The rows that carry an accept
+//     test (j < k_eff, T > 0) also add their exponentials to a sum kept against
+//     a segment reference (so the sum does not wait for each chunk's maximum);
+//     at the last chunk of a row segment the warps combine their sums into one
+//     record.
 
 constexpr int kCWarps = 16;                    // streaming warps
 constexpr int kPWarp = kCWarps;                // producer warp index
@@ -588,101 +606,106 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                 }
             }
         }
-        float zv[kVL];  // largest transformed value of each of my vectors (an upper bound)
-        if (full) {
-            float lraw = -INFINITY;
+        // packed maxima of my vectors (bf16: both halves of a word hold partial maxima;
+        // fp32: the maximum); elements past the row's end count as -inf
+        uint32_t hv[kVL];
 #pragma unroll
-            for (int i = 0; i < kVL; ++i) {
-                float vm;
-                if constexpr (BF16) {
-                    const uint32_t h = as_u32(bf16x8_max2(rv[i]));
-                    vm = fmaxf(bf16lo(h), bf16hi(h));
-                } else {
-                    vm = fmaxf(fmaxf(__uint_as_float(rv[i].x), __uint_as_float(rv[i].y)),
-                               fmaxf(__uint_as_float(rv[i].z), __uint_as_float(rv[i].w)));
-                }
-                zv[i] = SOFTCAP ? transform_f32<true, false>(vm, false, P) : vm;
-                lraw = fmaxf(lraw, vm);
+        for (int i = 0; i < kVL; ++i) {
+            uint4 r = rv[i];
+            if (!full) {
+                const int nv = v1 - (v0 + off0 + i * 32 * EPV);
+                r = mask_tail<BF16>(r, nv);
             }
-            if (dosum) {
+            if constexpr (BF16) {
+                hv[i] = as_u32(bf16x8_max2(r));
+            } else {
+                hv[i] = __float_as_uint(fmaxf(fmaxf(__uint_as_float(r.x), __uint_as_float(r.y)),
+                                              fmaxf(__uint_as_float(r.z), __uint_as_float(r.w))));
+            }
+        }
+        if (dosum) {
+            if (full) {
+                float lraw;
+                if constexpr (BF16) {
+                    uint32_t h = hv[0];
+#pragma unroll
+                    for (int i = 1; i < kVL; ++i) h = as_u32(__hmax2(as_bf162(h), as_bf162(hv[i])));
+                    lraw = fmaxf(bf16lo(h), bf16hi(h));
+                } else {
+                    lraw = __uint_as_float(hv[0]);
+#pragma unroll
+                    for (int i = 1; i < kVL; ++i) lraw = fmaxf(lraw, __uint_as_float(hv[i]));
+                }
                 const float zl = SOFTCAP ? transform_f32<true, false>(lraw, false, P) : lraw;
                 if (!(m > -INFINITY)) {
                     m = zl;
                     msc = m * P.sc;
                 }
-                float2 acc2[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
-                                  make_float2(0.0f, 0.0f)};
-                const float2 sc2 = make_float2(P.sc, P.sc), nm2 = make_float2(-msc, -msc);
-#pragma unroll
-                for (int i = 0; i < kVL; ++i) {
-                    float x[EPV];
-                    unpack<BF16>(rv[i], x);
-#pragma unroll
-                    for (int e = 0; e < EPV; e += 2) {
-                        const float2 t = __ffma2_rn(make_float2(transform_f32<SOFTCAP, false>(x[e], false, P),
-                                                                transform_f32<SOFTCAP, false>(x[e + 1], false, P)),
-                                                    sc2, nm2);
-                        acc2[i & 3] = __fadd2_rn(acc2[i & 3], make_float2(ex2_approx(t.x), ex2_approx(t.y)));
-                    }
-                }
-                float add = ((acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y)) +
-                            ((acc2[2].x + acc2[2].y) + (acc2[3].x + acc2[3].y));
-                if ((zl - m) * P.sc > 32.0f) {
-                    // far above the reference: raise it and take the chunk again
-                    s *= ex2_approx((m - zl) * P.sc);
-                    m = zl;
-                    msc = m * P.sc;
-                    add = 0.0f;
+                if (m > -INFINITY) {
+                    float2 acc2[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                                      make_float2(0.0f, 0.0f)};
+                    const float2 sc2 = make_float2(P.sc, P.sc), nm2 = make_float2(-msc, -msc);
 #pragma unroll
                     for (int i = 0; i < kVL; ++i) {
                         float x[EPV];
                         unpack<BF16>(rv[i], x);
 #pragma unroll
-                        for (int e = 0; e < EPV; ++e)
-                            add += ex2_approx(fmaf(transform_f32<SOFTCAP, false>(x[e], false, P), P.sc, -msc));
+                        for (int e = 0; e < EPV; e += 2) {
+                            const float2 t = __ffma2_rn(make_float2(transform_f32<SOFTCAP, false>(x[e], false, P),
+                                                                    transform_f32<SOFTCAP, false>(x[e + 1], false, P)),
+                                                        sc2, nm2);
+                            acc2[i & 3] = __fadd2_rn(acc2[i & 3], make_float2(ex2_approx(t.x), ex2_approx(t.y)));
+                        }
                     }
-                }
-                s += add;
-            }
-            if constexpr (PENALTY) {
-                // the few penalised elements: their penalised values join the vector's bound,
-                // and their terms of the sum are replaced by the penalised ones
-                unsigned pw = pmk;
-                while (pw != 0u) {
-                    const int bit = __ffs(pw) - 1;
-                    pw &= pw - 1u;
-                    const float xe = elem_of_stage<BF16>(stage, off0 + (bit >> 3) * 32 * EPV + (bit & 7));
-                    const float zu = transform_f32<SOFTCAP, false>(xe, false, P);
-                    const float zp = transform_f32<SOFTCAP, true>(xe, true, P);
+                    float add = ((acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y)) +
+                                ((acc2[2].x + acc2[2].y) + (acc2[3].x + acc2[3].y));
+                    if ((zl - m) * P.sc > 32.0f) {
+                        // far above the reference: raise it and take the chunk again
+                        s *= ex2_approx((m - zl) * P.sc);
+                        m = zl;
+                        msc = m * P.sc;
+                        add = 0.0f;
 #pragma unroll
-                    for (int i = 0; i < kVL; ++i)
-                        if ((bit >> 3) == i) zv[i] = fmaxf(zv[i], zp);
-                    if (dosum) {
+                        for (int i = 0; i < kVL; ++i) {
+                            float x[EPV];
+                            unpack<BF16>(rv[i], x);
+#pragma unroll
+                            for (int e = 0; e < EPV; ++e)
+                                add += ex2_approx(fmaf(transform_f32<SOFTCAP, false>(x[e], false, P), P.sc, -msc));
+                        }
+                    }
+                    s += add;
+                }
+                if constexpr (PENALTY) {
+                    // the few penalised elements: their terms are replaced by the penalised ones
+                    unsigned pw = pmk;
+                    while (pw != 0u) {
+                        const int bit = __ffs(pw) - 1;
+                        pw &= pw - 1u;
+                        const float xe = elem_of_stage<BF16>(stage, off0 + (bit >> 3) * 32 * EPV + (bit & 7));
+                        const float zu = transform_f32<SOFTCAP, false>(xe, false, P);
+                        const float zp = transform_f32<SOFTCAP, true>(xe, true, P);
                         if ((zp - m) * P.sc > 32.0f) {
-                            s *= ex2_approx((m - zp) * P.sc);
+                            s = m > -INFINITY ? s * ex2_approx((m - zp) * P.sc) : 0.0f;
                             m = zp;
                             msc = m * P.sc;
                         }
                         s += ex2_approx(fmaf(zp, P.sc, -msc)) - ex2_approx(fmaf(zu, P.sc, -msc));
                     }
                 }
-            }
-        } else {
-            // partial vectors (a row's last chunk): exact transform element by element
+            } else {
+                // partial vectors (a row's last chunk): exact transform element by element
 #pragma unroll
-            for (int i = 0; i < kVL; ++i) {
-                zv[i] = -INFINITY;
-                const int off = off0 + i * 32 * EPV;
-                const int nv = min(EPV, v1 - (v0 + off));
-                if (nv <= 0) continue;
-                float x[EPV];
-                unpack<BF16>(rv[i], x);
+                for (int i = 0; i < kVL; ++i) {
+                    const int off = off0 + i * 32 * EPV;
+                    const int nv = min(EPV, v1 - (v0 + off));
+                    if (nv <= 0) continue;
+                    float x[EPV];
+                    unpack<BF16>(rv[i], x);
 #pragma unroll
-                for (int e = 0; e < EPV; ++e) {
-                    if (e >= nv) break;
-                    const float z = transform_f32<SOFTCAP, PENALTY>(x[e], (pmk >> (8 * i + e)) & 1u, P);
-                    zv[i] = fmaxf(zv[i], z);
-                    if (dosum) {
+                    for (int e = 0; e < EPV; ++e) {
+                        if (e >= nv) break;
+                        const float z = transform_f32<SOFTCAP, PENALTY>(x[e], (pmk >> (8 * i + e)) & 1u, P);
                         if (!(m > -INFINITY) || (z - m) * P.sc > 32.0f) {
                             s = m > -INFINITY ? s * ex2_approx((m - z) * P.sc) : 0.0f;
                             m = z;
@@ -693,16 +716,47 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
                 }
             }
         }
-        // ---- block maxima: vector row i of the warp (rows i, i + 1 for fp32) is one noise block
+        // ---- block maxima (raw logits): vector row i of the warp (rows i, i + 1 for
+        //      fp32) is one noise block; the warp's four (two) blocks are contiguous
+        {
+            const int blk0 = (v0 >> kNoiseBlockShift) + warp * (kVL / VPB);
+            float* dst = P.bmax + static_cast<size_t>(row) * P.nblk + blk0;
+            const int nb = min(kVL / VPB, P.nblk - blk0);
+            if constexpr (BF16) {
+                // the maximum of each vector in one half, two vectors per word
+                uint32_t bw[kVL / 2];
 #pragma unroll
-        for (int i = 0; i < kVL; i += VPB) {
-            float zb = zv[i];
+                for (int p = 0; p < kVL / 2; ++p)
+                    bw[p] = as_u32(__hmax2(as_bf162(__byte_perm(hv[2 * p], hv[2 * p + 1], 0x5410)),
+                                           as_bf162(__byte_perm(hv[2 * p], hv[2 * p + 1], 0x7632))));
 #pragma unroll
-            for (int u = 1; u < VPB; ++u) zb = fmaxf(zb, zv[i + u]);
-            const unsigned key = __reduce_max_sync(0xffffffffu, zb > -INFINITY ? score_key(zb) : 0u);
-            const int e0 = v0 + (ubase + i * 32) * EPV;
-            if (lane == 0 && e0 < v1)
-                P.bmax[static_cast<size_t>(row) * P.nblk + (e0 >> kNoiseBlockShift)] = key_score(key);
+                for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+                    for (int p = 0; p < kVL / 2; ++p)
+                        bw[p] = as_u32(__hmax2(as_bf162(bw[p]), as_bf162(__shfl_xor_sync(0xffffffffu, bw[p], off))));
+                if (lane == 0) {
+#pragma unroll
+                    for (int i = 0; i < kVL; ++i)
+                        if (i < nb) dst[i] = (i & 1) ? bf16hi(bw[i >> 1]) : bf16lo(bw[i >> 1]);
+                }
+            } else {
+                float bm[kVL / VPB];
+#pragma unroll
+                for (int p = 0; p < kVL / VPB; ++p) {
+                    bm[p] = __uint_as_float(hv[VPB * p]);
+#pragma unroll
+                    for (int u = 1; u < VPB; ++u) bm[p] = fmaxf(bm[p], __uint_as_float(hv[VPB * p + u]));
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+                    for (int p = 0; p < kVL / VPB; ++p) bm[p] = fmaxf(bm[p], __shfl_xor_sync(0xffffffffu, bm[p], off));
+                if (lane == 0) {
+#pragma unroll
+                    for (int p = 0; p < kVL / VPB; ++p)
+                        if (p < nb) dst[p] = bm[p];
+                }
+            }
         }
 
         if (mt.seg_end && dosum) {
@@ -798,6 +852,16 @@ __host__ __device__ inline size_t k2_dyn_smem(int nblk, bool bf16) {
 // Open-addressed table of the history tail of the penalty window: the token
 // and its latest position in the tail (-1 = empty slot).
 __device__ __forceinline__ uint32_t pen_hash(int v) { return (static_cast<uint32_t>(v) * 2654435761u) >> (32 - kPenBits); }
+
+// Bound of the transformed logits of a block from its largest raw logit: the
+// soft cap is increasing, and a penalty r >= 1 only lowers a value (r < 1 may
+// raise it: then the larger of the two).
+template <bool SOFTCAP, bool PENALTY>
+__device__ __forceinline__ float block_zmax(float xmax, const VerifyDev& P) {
+    float z = transform_f32<SOFTCAP, false>(xmax, false, P);
+    if (PENALTY && P.rep < 1.0f) z = fmaxf(z, transform_f32<SOFTCAP, true>(xmax, true, P));
+    return z;
+}
 
 // Is id v in the penalty window of row j (the last W tokens of the history
 // tail ++ d_1..d_j)?  key / pos: the table above; d: the drafts; nh: the
@@ -937,7 +1001,7 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const VerifyDev P) {
             const float gth = kw ? key_score(kw) - cand_delta(key_score(kw)) : -INFINITY;
             for (int qb = 0; qb < P.nblk; qb += 32) {
                 const int q = qb + lane;
-                unsigned pass = __ballot_sync(0xffffffffu, q < P.nblk && q != q0 && bmx[q] >= gth);
+                unsigned pass = __ballot_sync(0xffffffffu, q < P.nblk && q != q0 && block_zmax<SOFTCAP, PENALTY>(bmx[q], P) >= gth);
                 while (pass != 0u) {
                     const int qq = qb + __ffs(pass) - 1;
                     pass &= pass - 1u;
@@ -1053,7 +1117,7 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const VerifyDev P) {
                 const int q = q0 + i * kST;
                 if (q >= nblk) break;
                 const BlockNoise bn = block_noise(nk, static_cast<uint32_t>(q), static_cast<uint32_t>(a));
-                s_bnd[q] = zq[i] * P.invT - bn.lnM;
+                s_bnd[q] = block_zmax<SOFTCAP, PENALTY>(zq[i], P) * P.invT - bn.lnM;
                 s_M[q] = bn.M;
                 s_I[q] = bn.I;
                 if (zq[i] > lb) { lb = zq[i]; lq = q; }
