@@ -234,10 +234,10 @@ class Path:
         self.ws = sp.spec_verify_workspace(B, K, V, device)
         self.params = sp.VerifyParams(temperature=cfg.temperature, softcap=cfg.softcap, rep_penalty=cfg.rep_penalty,
                                       rep_window=cfg.rep_window, gate_enabled=cfg.gate, seed=cfg.sampler_seed)
-        # library kernels per step: spec_verify (the streaming kernel with the row merges; + the residual
-        # pass with dense q at T > 0), then spec_commit (append + index + next drafts) or, without n-gram
-        # drafts, spec_append
-        self.launches_per_step = (2 if cfg.dense and cfg.temperature > 0 else 1) + 1
+        # library kernels per step: spec_verify (the streaming kernel and the per-sequence decision
+        # kernel; + the residual pass with dense q at T > 0), then spec_commit (append + index + next
+        # drafts) or, without n-gram drafts, spec_append
+        self.launches_per_step = (3 if cfg.dense and cfg.temperature > 0 else 2) + 1
         self.g = g
 
     def _limits(self, s):
@@ -471,7 +471,7 @@ def run_ours(args):
         "roofline": {
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "traffic": traffic,
-            "kernel": "spec_verify call: verify_stream_kernel (row merges folded in; + verify_residual_kernel "
+            "kernel": "spec_verify call: verify_stream_kernel + verify_seq_kernel (+ verify_residual_kernel "
                       "with dense q); 60 back-to-back calls on rotating logit batches larger than L2 together, "
                       "CUDA events around the loop",
             "rows_per_launch": v_rows,
