@@ -14,6 +14,35 @@ __device__ __forceinline__ void raise_status(unsigned* status, unsigned bit) {
     if (status != nullptr) atomicOr(status, bit);
 }
 
+// ---------------------------------------------------------------- launch chaining
+// Programmatic dependent launch (sm_90+): a kernel launched with the
+// programmatic-serialisation attribute may start before the previous kernel
+// of its stream has finished.  It does the work that depends on nothing the
+// previous kernel writes, then waits in pdl_wait() until that kernel has
+// completed and its writes are visible.  pdl_trigger() lets the next kernel
+// launch early (its own pdl_wait() still waits for this kernel's completion).
+// Both are no-ops for a kernel launched without the attribute.
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch `kernel` on stream s with programmatic stream serialisation.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                  Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // ---------------------------------------------------------------- Philox
 // Philox4x32-10 as defined by Salmon, Moraes, Dror and Shaw, "Parallel random
 // numbers: as easy as 1, 2, 3" (SC'11): per round the two multiplier products

@@ -176,6 +176,8 @@ __global__ void ngram_clear_kernel(const NgramDev T) {
 
 __global__ void spec_append_kernel(int32_t* hist, int64_t stride, int32_t* lens, int64_t cap, const int32_t* out_tokens,
                                    const int32_t* out_accept, int B, int K, unsigned* status) {
+    pdl_wait();  // the verify kernels' tokens
+    pdl_trigger();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= B) return;
     const int a = out_accept[b];
@@ -232,6 +234,8 @@ __global__ void __launch_bounds__(kNgThreads) spec_commit_kernel(const NgramDev 
                                                                  int K, int max_k, const int32_t* k_limit,
                                                                  const int32_t* fallback, int32_t* out_drafts,
                                                                  int32_t* out_k) {
+    pdl_wait();  // the verify kernels' tokens
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int b = blockIdx.x * (kNgThreads / 32) + (threadIdx.x >> 5);
     if (b >= T.B) return;
@@ -334,8 +338,8 @@ cudaError_t launch_ngram_clear(const NgramDev& T, cudaStream_t s) {
 
 cudaError_t launch_spec_append(int32_t* hist, int64_t stride, int32_t* lens, int64_t cap, const int32_t* out_tokens,
                                const int32_t* out_accept, int B, int K, unsigned* status, cudaStream_t s) {
-    spec_append_kernel<<<(B + 127) / 128, 128, 0, s>>>(hist, stride, lens, cap, out_tokens, out_accept, B, K, status);
-    return cudaGetLastError();
+    return launch_chained(spec_append_kernel, dim3((B + 127) / 128), dim3(128), 0, s, hist, stride, lens, cap, out_tokens,
+                          out_accept, B, K, status);
 }
 
 cudaError_t launch_spec_commit(const NgramDev& T, int parity, int32_t* hist, int64_t stride, int32_t* lens,
@@ -343,10 +347,8 @@ cudaError_t launch_spec_commit(const NgramDev& T, int parity, int32_t* hist, int
                                const int32_t* k_limit, const int32_t* fallback, int32_t* out_drafts, int32_t* out_k,
                                cudaStream_t s) {
     const int per = kNgThreads / 32;
-    spec_commit_kernel<<<(T.B + per - 1) / per, kNgThreads, 0, s>>>(T, parity, hist, stride, lens, cap, out_tokens,
-                                                                   out_accept, K, max_k, k_limit, fallback,
-                                                                   out_drafts, out_k);
-    return cudaGetLastError();
+    return launch_chained(spec_commit_kernel, dim3((T.B + per - 1) / per), dim3(kNgThreads), 0, s, T, parity, hist, stride,
+                          lens, cap, out_tokens, out_accept, K, max_k, k_limit, fallback, out_drafts, out_k);
 }
 
 cudaError_t launch_philox(const uint32_t* ctr, uint64_t seed, uint32_t* out, int64_t n, cudaStream_t s) {

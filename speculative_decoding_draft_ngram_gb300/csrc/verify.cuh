@@ -313,6 +313,28 @@ __device__ __forceinline__ int gate_keff(const VerifyDev& P, int b, int* kb_out,
 // Slack of the block bound: covers the fp32 rounding of z / T and ln M.
 __device__ __forceinline__ float bound_slack(float z) { return 1e-5f * (1.0f + fabsf(z)); }
 
+// A raw logit x_t such that every element whose block bound passes the best,
+// z / T - ln M + bound_slack(.) >= thr with z the (unpenalised) transform of x,
+// has x >= x_t.  The margins keep the screen a superset of the exact test in
+// spite of fp32 rounding: 2e-5 (1 + |thr|) in score units, then 1e-5 relative
+// in z, then (soft cap) 2e-5 c in z before the inverse map and 1e-4 relative
+// after it, which covers the error of tanhf amplified by the steep atanh.
+// Used only where the penalty cannot raise a value (r >= 1).
+template <bool SOFTCAP>
+__device__ __forceinline__ float raw_screen(float thr, float lnM, const VerifyDev& P) {
+    if (!(thr > -INFINITY)) return -INFINITY;
+    float zt = (thr + lnM - 2e-5f * (1.0f + fabsf(thr))) * P.T;
+    zt -= 1e-5f * (1.0f + fabsf(zt));
+    if constexpr (SOFTCAP) {
+        zt -= 2e-5f * P.cap;
+        if (zt <= -P.cap) return -INFINITY;
+        if (zt >= P.cap) return INFINITY;  // the transform never exceeds c
+        const float xr = P.cap * atanhf(zt * P.invcap);
+        return xr - 1e-4f * (1.0f + fabsf(xr));
+    }
+    return zt;
+}
+
 // Elements n.. of a 16-byte vector set to -inf (n <= 0: all of them).
 template <bool BF16>
 __device__ __forceinline__ uint4 mask_tail(uint4 r, int n) {
@@ -351,7 +373,8 @@ __device__ __forceinline__ uint4 mask_tail(uint4 r, int n) {
 constexpr int kCWarps = 16;                    // streaming warps
 constexpr int kPWarp = kCWarps;                // producer warp index
 constexpr int kPThreads = (kCWarps + 1) * 32;  // 544
-constexpr int kStages = 6;
+constexpr int kK1PerSM = 2;                    // resident streaming CTAs per SM
+constexpr int kStages = 3;                     // ring stages per CTA
 constexpr int kVL = 4;                         // 16-byte vectors per lane per chunk
 static_assert(kChunkBytes == kCWarps * 32 * kVL * 16, "stage layout");
 static_assert((32 * 8) == (1 << kNoiseBlockShift), "a bf16 vector row of a warp is one noise block");
@@ -371,7 +394,7 @@ struct StageMeta {
 };
 
 template <bool BF16, bool GREEDY, bool SOFTCAP, bool PENALTY>
-__global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const VerifyDev P) {
+__global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(const VerifyDev P) {
     constexpr int EPV = ElemTraits<BF16>::EPV;
     constexpr int CHUNK = chunk_elems<BF16>();
     constexpr int SB = kChunkBytes;
@@ -391,6 +414,10 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int K1 = P.K + 1;
+    // k and ema come from the kernels before this one; once they are visible the
+    // decision kernel may be launched (its own wait holds it until this one ends)
+    pdl_wait();
+    pdl_trigger();
 
     // ---- prologue: count the active row-chunks and find this CTA's range
     const int per = (P.B + kPThreads - 1) / kPThreads;
@@ -832,21 +859,19 @@ __global__ void __launch_bounds__(kPThreads, 1) verify_stream_kernel(const Verif
 constexpr int kSW = 8;                          // warps per sequence
 constexpr int kST = kSW * 32;
 constexpr int kBatch = 8;                       // blocks a warp reads again at once
-constexpr int kQCap = 320;                      // candidate queue entries per warp (>= 31 + 256)
 constexpr int kPenSlots = 2 * SPECNG_MAX_REP_WINDOW;
 constexpr int kPenBits = 9;
 static_assert((1 << kPenBits) == kPenSlots, "penalty table size");
 static_assert(SPECNG_MAX_K + 1 <= kST, "one thread per output token");
 
 // Dynamic shared memory of the decision kernel at T > 0: the block scratch
-// (when it fits), each warp's staging of a batch of blocks, and each warp's
-// candidate queue (id, staging index).
+// (when it fits) and each warp's staging of a batch of blocks.
 __host__ __device__ constexpr size_t k2_stage_bytes(bool bf16) { return static_cast<size_t>(kSW) * kBatch * 32 * (bf16 ? 1 : 2) * 16; }
 __host__ __device__ inline size_t k2_blk_bytes(int nblk) {
     return nblk <= kSmemBlkCap ? (static_cast<size_t>(nblk) * kBlkScratchBytes + 15) / 16 * 16 : 0;
 }
 __host__ __device__ inline size_t k2_dyn_smem(int nblk, bool bf16) {
-    return k2_blk_bytes(nblk) + k2_stage_bytes(bf16) + static_cast<size_t>(kSW) * kQCap * 8;
+    return k2_blk_bytes(nblk) + k2_stage_bytes(bf16);
 }
 
 // Open-addressed table of the history tail of the penalty window: the token
@@ -901,10 +926,12 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const VerifyDev P) {
     __shared__ unsigned s_thr;
     __shared__ int s_nl;
     __shared__ int s_y;
+    __shared__ int s_bq[kSW][kBatch];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = blockIdx.x;
     const int K1 = P.K + 1;
+    pdl_trigger();  // the next kernel may launch; it waits for this one's end itself
     int kb;
     const int keff = gate_keff(P, b, &kb, tid == 0);
     const bool dense = P.q != nullptr;
@@ -945,6 +972,8 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const VerifyDev P) {
         }
     }
     __syncthreads();
+    // everything above reads the call's inputs only; the stream kernel's records from here on
+    pdl_wait();
 
     auto pen_of = [&](int v, int j) -> bool {
         if constexpr (!PENALTY) return false;
@@ -1034,32 +1063,49 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const VerifyDev P) {
                 xd = static_cast<float>(raw_logit_f64<BF16>(P.logits, row, P.V, d));
                 if (dense) qdf = P.q[(static_cast<size_t>(b) * P.K + j) * P.V + d];
             }
+            // one pass over the segment sums: a lane keeps its first kPr records in registers
+            constexpr int kPr = 4;
             SegSum* pr = P.part + static_cast<size_t>(row) * P.nchunk;
+            float2 pv[kPr];
             float mf = -INFINITY;
-            for (int cc = lane; cc < P.nchunk; cc += 32) {
+#pragma unroll
+            for (int i = 0; i < kPr; ++i) {
+                const int cc = lane + 32 * i;
+                pv[i] = cc < P.nchunk ? __ldcg(reinterpret_cast<const float2*>(pr + cc)) : make_float2(0.0f, 0.0f);
+            }
+            for (int cc = lane + 32 * kPr; cc < P.nchunk; cc += 32) {
                 const float2 p = __ldcg(reinterpret_cast<const float2*>(pr + cc));
                 if (p.y != 0.0f || __float_as_uint(p.x) != 0u) mf = fmaxf(mf, p.x);
             }
 #pragma unroll
+            for (int i = 0; i < kPr; ++i)
+                if (pv[i].y != 0.0f || __float_as_uint(pv[i].x) != 0u) mf = fmaxf(mf, pv[i].x);
+#pragma unroll
             for (int off = 16; off > 0; off >>= 1) mf = fmaxf(mf, __shfl_xor_sync(0xffffffffu, mf, off));
-            double S = 0.0;
-            for (int cc = lane; cc < P.nchunk; cc += 32) {
-                const float2 p = __ldcg(reinterpret_cast<const float2*>(pr + cc));
-                if ((p.y != 0.0f || __float_as_uint(p.x) != 0u) && p.x > -INFINITY)
-                    S += static_cast<double>(p.y) * static_cast<double>(expf((p.x - mf) * P.invT));
-            }
-            S = warp_sum_f64(S);
-            __syncwarp();
+            // the records' sums relative to mf (each term <= its record's sum; fp32 keeps 2^-24
+            // relative per term, far inside the accept test's margin)
+            float Sf = 0.0f;
+            auto term = [&](float2 p) {
+                return ((p.y != 0.0f || __float_as_uint(p.x) != 0u) && p.x > -INFINITY)
+                           ? p.y * ex2_approx((p.x - mf) * P.sc) : 0.0f;
+            };
+#pragma unroll
+            for (int i = 0; i < kPr; ++i) Sf += term(pv[i]);
+            for (int cc = lane + 32 * kPr; cc < P.nchunk; cc += 32) Sf += term(__ldcg(reinterpret_cast<const float2*>(pr + cc)));
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) Sf += __shfl_xor_sync(0xffffffffu, Sf, off);
             for (int cc = lane; cc < P.nchunk; cc += 32) pr[cc] = SegSum{0.0f, 0.0f};  // leave the workspace zeroed
-            const double lse = static_cast<double>(mf) / P.Td + log(S);
             if (lane == 0) {
-                if (!(S > 0.0 && S < INFINITY && mf < INFINITY)) raise_status(P.status, SPECNG_DEV_NONFINITE);
+                if (!(Sf > 0.0f && Sf < INFINITY && mf < INFINITY)) raise_status(P.status, SPECNG_DEV_NONFINITE);
+                const float lsef = mf * P.invT + logf(Sf);
+                // the log-sum-exp in fp64 (the oracle's precision), only where it is used
+                auto lse64 = [&]() { return static_cast<double>(mf) / P.Td + log(static_cast<double>(Sf)); };
                 int accepted = 0;
                 if (dv) {
                     const double qd = static_cast<double>(qdf);
                     const bool pend = pen_of(d, j);
                     const double u = accept_uniform_f64(nk, static_cast<uint32_t>(j + 1));
-                    const float lp = transform_f32<SOFTCAP, PENALTY>(xd, pend, P) * P.invT - static_cast<float>(lse);
+                    const float lp = transform_f32<SOFTCAP, PENALTY>(xd, pend, P) * P.invT - lsef;
                     const float lr = logf(static_cast<float>(u)) + logf(static_cast<float>(qd));
                     if (lr < lp - 1e-4f * (1.0f + fabsf(lp))) {
                         accepted = 1;
@@ -1067,11 +1113,11 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const VerifyDev P) {
                         accepted = 0;
                     } else {
                         const double zd = transform_f64<SOFTCAP, PENALTY>(static_cast<double>(xd), pend, P);
-                        accepted = u * qd <= exp(zd / P.Td - lse);
+                        accepted = u * qd <= exp(zd / P.Td - lse64());
                     }
                 }
                 s_acc[j] = accepted;
-                s_lse[j] = lse;
+                s_lse[j] = (dense && !accepted) ? lse64() : 0.0;
             }
         }
     }
@@ -1089,9 +1135,11 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const VerifyDev P) {
     int y;
     if constexpr (GREEDY) {
         y = s_arg[a];
+    } else if (need) {
+        y = -1;  // the residual pass samples row a (CTA-uniform branch)
     } else {
         const int row = b * K1 + a;
-        const int excl = (!dense && a < keff && dvalid) ? da : -1;
+        const int excl = (a < keff && dvalid) ? da : -1;  // point mass here: dense rejections took the branch above
         const float* bmx = P.bmax + static_cast<size_t>(row) * P.nblk;
         const char* rowp = rowp_of(row);
         const int nblk = P.nblk;
@@ -1101,13 +1149,22 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const VerifyDev P) {
         int* s_I = reinterpret_cast<int*>(s_M + nblk);
         int* s_list = s_I + nblk;
         uint4* stg = reinterpret_cast<uint4*>(s_dyn + k2_blk_bytes(nblk)) + warp * (kBatch * 32 * VPL);
-        int2* que = reinterpret_cast<int2*>(s_dyn + k2_blk_bytes(nblk) + k2_stage_bytes(BF16)) + warp * kQCap;
         const RowPhilox rp = row_philox(nk, static_cast<uint32_t>(a));
-        // block draws and bounds (the blocks' values are loaded first, so their
-        // latencies overlap); each warp's block with the largest value (a large
-        // bound more often comes from a small M, whose block rarely holds the best)
+        // each warp's seed: its block with the largest value (the blocks' maxima are
+        // loaded first); the seed block's load is issued before the block draws, so
+        // its latency overlaps them
         float lb = -INFINITY;
         int lq = -1;
+        for (int q = tid; q < nblk; q += kST) {
+            const float zq = bmx[q];
+            if (zq > lb) { lb = zq; lq = q; }
+        }
+        const unsigned kq = warp_best_key(lb);
+        const unsigned own = __ballot_sync(0xffffffffu, kq != 0u && lb > -INFINITY && score_key(lb) == kq);
+        const int qs = own ? __shfl_sync(0xffffffffu, lq, __ffs(own) - 1) : -1;
+        uint4 rs[VPL];
+        if (qs >= 0) load_block(rowp, qs, rs);
+        // block draws and bounds
         for (int q0 = tid; q0 < nblk; q0 += 4 * kST) {
             float zq[4];
 #pragma unroll
@@ -1120,34 +1177,29 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const VerifyDev P) {
                 s_bnd[q] = block_zmax<SOFTCAP, PENALTY>(zq[i], P) * P.invT - bn.lnM;
                 s_M[q] = bn.M;
                 s_I[q] = bn.I;
-                if (zq[i] > lb) { lb = zq[i]; lq = q; }
             }
         }
-        __syncwarp();
-        // seed: each lane scores its largest element of the warp's seed block
+        // seed: each lane scores its largest element of the warp's seed block (the
+        // seed block's draw is the same function of (row, block) as above)
         {
-            const unsigned kq = warp_best_key(lb);
-            const unsigned own = __ballot_sync(0xffffffffu, kq != 0u && lb > -INFINITY && score_key(lb) == kq);
-            const int q = own ? __shfl_sync(0xffffffffu, lq, __ffs(own) - 1) : -1;
             float sc = -INFINITY;
-            if (q >= 0) {
-                uint4 r[VPL];
-                load_block(rowp, q, r);
+            if (qs >= 0) {
                 float xb = -INFINITY;
                 int vb = -1;
 #pragma unroll
                 for (int u = 0; u < VPL; ++u) {
                     float x[EPV];
-                    unpack<BF16>(r[u], x);
+                    unpack<BF16>(rs[u], x);
 #pragma unroll
                     for (int e = 0; e < EPV; ++e) {
-                        const int v = elem_id(q, u * EPV + e);
+                        const int v = elem_id(qs, u * EPV + e);
                         if (v < P.V && v != excl && (vb < 0 || x[e] > xb)) { xb = x[e]; vb = v; }
                     }
                 }
                 if (vb >= 0) {
+                    const BlockNoise bn = block_noise(nk, static_cast<uint32_t>(qs), static_cast<uint32_t>(a));
                     const float zb = transform_f32<SOFTCAP, PENALTY>(xb, PENALTY && pen_of(vb, a), P) * P.invT;
-                    sc = zb - ln_fast(noise_exp_f32(rp, s_M[q], s_I[q], static_cast<uint32_t>(vb)));
+                    sc = zb - ln_fast(noise_exp_f32(rp, bn.M, bn.I, static_cast<uint32_t>(vb)));
                 }
             }
             const unsigned kw = warp_best_key(sc);
@@ -1169,33 +1221,10 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const VerifyDev P) {
         __syncthreads();
         const int nl = s_nl;
         Top2 t = top2_empty();
-        // score the queued candidates, one per lane per round: the exact value
-        // (penalty) and the element's own draw
-        auto flush = [&](int qn) {
-            __syncwarp();
-            for (int i0 = 0; i0 < qn; i0 += 32) {
-                const int i = i0 + lane;
-                if (i < qn) {
-                    const int2 en = que[i];
-                    const int v = en.x;
-                    const int q = v >> kNoiseBlockShift;
-                    const float xv = elem_of_stage<BF16>(stg, en.y);
-                    const float zb = transform_f32<SOFTCAP, PENALTY>(xv, PENALTY && pen_of(v, a), P) * P.invT;
-                    const float Mq = s_M[q];
-                    const float lnMq = ln_fast(Mq);
-                    if (zb - lnMq + bound_slack(zb - lnMq) >= thr) {
-                        const float score = zb - ln_fast(noise_exp_f32(rp, Mq, s_I[q], static_cast<uint32_t>(v)));
-                        if (score >= thr) {
-                            top2_push(t, score, v);
-                            thr = fmaxf(thr, t.s1 - cand_delta(t.s1));
-                        }
-                    }
-                }
-            }
-            __syncwarp();
-            const unsigned kw = warp_best_key(t.s1);
-            if (kw != 0u) thr = fmaxf(thr, key_score(kw) - cand_delta(key_score(kw)));
-        };
+        // the listed blocks, kBatch per warp at a time: their loads all in flight
+        // together, one raw-logit screening threshold per block, then each lane
+        // scores its own candidates (usually none or one per batch): the exact
+        // transform (penalty) and the element's own draw
         for (int l0 = warp * kBatch; l0 < nl; l0 += kSW * kBatch) {
             // blocks whose bound no longer reaches the best found so far are skipped;
             // lane h < kBatch holds block h of the batch
@@ -1207,63 +1236,62 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const VerifyDev P) {
                 const int q = s_list[l0 + lane];
                 if (s_bnd[q] + bound_slack(s_bnd[q]) >= thw) myq = q;
             }
-            // the batch's blocks into the warp's staging, all loads in flight together
+            if (lane < kBatch) s_bq[warp][lane] = myq;
+            int qh[kBatch];
 #pragma unroll
-            for (int h = 0; h < kBatch; ++h) {
-                const int q = __shfl_sync(0xffffffffu, myq, h);
-                if (q >= 0) {
+            for (int h = 0; h < kBatch; ++h) qh[h] = __shfl_sync(0xffffffffu, myq, h);
+            uint4 r[kBatch * VPL];
 #pragma unroll
-                    for (int u = 0; u < VPL; ++u) {
-                        const int e0 = q * BLK + (u * 32 + lane) * EPV;
-                        stg[(h * VPL + u) * 32 + lane] =
-                            e0 < P.V ? load_vec<BF16>(rowp, e0, P.V, P.aligned) : make_uint4(0u, 0u, 0u, 0u);
-                    }
-                }
-            }
-            __syncwarp();
-            // the elements whose bound z / T - ln M reaches the best go to the queue (a
-            // bound of z first: a penalty above 1 only lowers it)
-            int qn = 0;
-#pragma unroll 1
-            for (int h = 0; h < kBatch; ++h) {
-                const int q = __shfl_sync(0xffffffffu, myq, h);
-                if (q < 0) continue;  // warp-uniform
-                const float lnMq = ln_fast(s_M[q]);
-                unsigned ce = 0u;
+            for (int h = 0; h < kBatch; ++h)
 #pragma unroll
                 for (int u = 0; u < VPL; ++u) {
-                    float x[EPV];
-                    unpack<BF16>(stg[(h * VPL + u) * 32 + lane], x);
+                    const int e0 = qh[h] * BLK + (u * 32 + lane) * EPV;
+                    r[h * VPL + u] = (qh[h] >= 0 && e0 < P.V) ? load_vec<BF16>(rowp, e0, P.V, P.aligned)
+                                                               : make_uint4(0u, 0u, 0u, 0u);
+                }
+            // screening thresholds (a penalty below 1 may raise a value: then every
+            // element goes to the exact test)
+            float xt[kBatch];
 #pragma unroll
-                    for (int e = 0; e < EPV; ++e) {
-                        const int k = u * EPV + e;
-                        const int v = elem_id(q, k);
-                        float zb = transform_f32<SOFTCAP, false>(x[e], false, P);
-                        if (PENALTY && P.rep < 1.0f) zb = fmaxf(zb, transform_f32<SOFTCAP, true>(x[e], true, P));
-                        zb *= P.invT;
-                        if (v < P.V && v != excl && zb - lnMq + bound_slack(zb - lnMq) >= thr) ce |= 1u << k;
+            for (int h = 0; h < kBatch; ++h)
+                xt[h] = qh[h] < 0 ? INFINITY
+                                  : ((PENALTY && P.rep < 1.0f) ? -INFINITY : raw_screen<SOFTCAP>(thr, ln_fast(s_M[qh[h]]), P));
+#pragma unroll
+            for (int i = 0; i < kBatch * VPL; ++i) stg[i * 32 + lane] = r[i];
+            unsigned long long cm = 0ull;  // bit 8 h + k: element k of my share of block h
+#pragma unroll
+            for (int h = 0; h < kBatch; ++h)
+#pragma unroll
+                for (int u = 0; u < VPL; ++u) {
+                    const uint4 rv = r[h * VPL + u];
+                    unsigned bits;
+                    if constexpr (BF16) {
+                        bits = bf16x8_ge_bits(rv, bf16x2_floor(xt[h]));
+                    } else {
+                        bits = (__uint_as_float(rv.x) >= xt[h] ? 1u : 0u) | (__uint_as_float(rv.y) >= xt[h] ? 2u : 0u) |
+                               (__uint_as_float(rv.z) >= xt[h] ? 4u : 0u) | (__uint_as_float(rv.w) >= xt[h] ? 8u : 0u);
                     }
+                    cm |= static_cast<unsigned long long>(bits) << (h * NE + u * EPV);
                 }
-                const int c = __popc(ce);
-                int incl = c;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int y2 = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += y2;
-                }
-                int at = qn + incl - c;
-                while (ce != 0u) {
-                    const int k = __ffs(ce) - 1;
-                    ce &= ce - 1u;
-                    que[at++] = make_int2(elem_id(q, k), ((h * VPL + k / EPV) * 32 + lane) * EPV + k % EPV);
-                }
-                qn += __shfl_sync(0xffffffffu, incl, 31);
-                if (qn >= 32) {
-                    flush(qn);
-                    qn = 0;
+            __syncwarp();  // the staging and the batch's block ids are visible
+            while (cm != 0ull) {
+                const int bit = __ffsll(static_cast<long long>(cm)) - 1;
+                cm &= cm - 1ull;
+                const int h = bit / NE, k = bit % NE;
+                const int q = s_bq[warp][h];
+                const int v = elem_id(q, k);
+                if (v >= P.V || v == excl) continue;
+                const float xv = elem_of_stage<BF16>(stg, ((h * VPL + k / EPV) * 32 + lane) * EPV + k % EPV);
+                const float zb = transform_f32<SOFTCAP, PENALTY>(xv, PENALTY && pen_of(v, a), P) * P.invT;
+                const float Mq = s_M[q];
+                const float lnMq = ln_fast(Mq);
+                if (zb - lnMq + bound_slack(zb - lnMq) < thr) continue;
+                const float score = zb - ln_fast(noise_exp_f32(rp, Mq, s_I[q], static_cast<uint32_t>(v)));
+                if (score >= thr) {
+                    top2_push(t, score, v);
+                    thr = fmaxf(thr, t.s1 - cand_delta(t.s1));
                 }
             }
-            if (qn > 0) flush(qn);
             __syncwarp();  // the staging is read before the next batch overwrites it
             // share the best with the other warps
             const unsigned kw = warp_best_key(t.s1);
@@ -1374,6 +1402,71 @@ __device__ __forceinline__ void build_window(const VerifyDev& P, int b, int j, i
     __syncthreads();
 }
 
+// Gumbel-max over p of row `row` (sampling position a), every id competing:
+// argmax_v (z_v / T - ln E_v), the rule an all-zero residual falls back to.
+// Whole CTA calls it; it reads the row once and draws per-id noise only
+// where a warp's running best can still be reached (E_v >= M of its block).
+// Slow by design (the case needs p <= q everywhere in floating point) but
+// exact: the top two are re-scored in fp64.  s_top: kWarps Top2 slots.
+template <bool BF16, bool SOFTCAP, bool PENALTY>
+__device__ __noinline__ int sample_p_row(const VerifyDev& P, const NoiseKey& nk, int row, int a, const int* s_win, int nw,
+                                         Top2* s_top) {
+    constexpr int EPV = ElemTraits<BF16>::EPV;
+    constexpr int BLK = 1 << kNoiseBlockShift;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const char* rowp = static_cast<const char*>(P.logits) + static_cast<size_t>(row) * P.V * ElemTraits<BF16>::SIZE;
+    const RowPhilox rp = row_philox(nk, static_cast<uint32_t>(a));
+    auto pen = [&](int v) {
+        if constexpr (!PENALTY) return false;
+        for (int t = 0; t < nw; ++t)
+            if (s_win[t] == v) return true;
+        return false;
+    };
+    Top2 t = top2_empty();
+    float thr = -INFINITY;
+    __syncthreads();  // s_top may still be read by the caller's earlier merge
+    for (int q = warp; q < P.nblk; q += kWarps) {
+        const BlockNoise bn = block_noise(nk, static_cast<uint32_t>(q), static_cast<uint32_t>(a));
+        for (int e0 = q * BLK + lane * EPV; e0 < min(P.V, (q + 1) * BLK); e0 += 32 * EPV) {
+            float x[EPV];
+            unpack<BF16>(load_vec<BF16>(rowp, e0, P.V, P.aligned), x);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) {
+                const int v = e0 + e;
+                if (v >= P.V) break;
+                float zb = transform_f32<SOFTCAP, false>(x[e], false, P);
+                if (PENALTY && P.rep < 1.0f) zb = fmaxf(zb, transform_f32<SOFTCAP, true>(x[e], true, P));
+                zb *= P.invT;
+                if (zb - bn.lnM + bound_slack(zb - bn.lnM) < thr) continue;
+                const float z = transform_f32<SOFTCAP, PENALTY>(x[e], PENALTY && pen(v), P) * P.invT;
+                const float score = z - ln_fast(noise_exp_f32(rp, bn.M, bn.I, static_cast<uint32_t>(v)));
+                top2_push(t, score, v);
+                thr = fmaxf(thr, t.s2 > -INFINITY ? t.s2 - cand_delta(t.s2) : -INFINITY);
+            }
+        }
+        const unsigned kw = warp_best_key(t.s1);
+        if (kw != 0u) thr = fmaxf(thr, key_score(kw) - cand_delta(key_score(kw)));
+    }
+    t = top2_warp_reduce(t);
+    if (lane == 0) s_top[warp] = t;
+    __syncthreads();
+    Top2 tw = lane < kWarps ? s_top[lane] : top2_empty();
+#pragma unroll
+    for (int off = kWarps / 2; off > 0; off >>= 1) tw = top2_merge(tw, top2_shfl_xor(tw, off));
+    int w = tw.i1;
+    if (tw.i2 >= 0 && tw.s2 >= tw.s1 - cand_delta(tw.s1)) {
+        double sc[2];
+        for (int h = 0; h < 2; ++h) {
+            const int id = h == 0 ? tw.i1 : tw.i2;
+            const double z = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, id),
+                                                             PENALTY && pen(id), P);
+            sc[h] = z / P.Td - log(noise_exp_f64(nk, static_cast<uint32_t>(id), static_cast<uint32_t>(a)));
+        }
+        if (better64(sc[1], tw.i2, sc[0], tw.i1)) w = tw.i2;
+    }
+    return w;  // the same value in every thread
+}
+
 template <bool BF16, bool SOFTCAP, bool PENALTY>
 __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const VerifyDev P) {
     constexpr int EPV = ElemTraits<BF16>::EPV;
@@ -1384,6 +1477,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const Veri
     __shared__ int s_nwin;
     __shared__ Top2 s_t[kWarps];
     __shared__ int s_last;
+    __shared__ int s_dec;
     __shared__ unsigned s_thr;
     __shared__ BlockNoise s_bn[NB];
     __shared__ uint16_t s_q2[kWarps * 32 * kNV * EPV];  // per-warp candidate queues (chunk offsets)
@@ -1392,6 +1486,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const Veri
     const int K1 = P.K + 1;
     const int b = blockIdx.x / P.nchunk2;
     const int c = blockIdx.x - b * P.nchunk2;
+    pdl_wait();  // the decision kernel's records
     const int need = __ldcg(&P.seqres[b].need_residual);
     if (!need) return;
     const int a = __ldcg(&P.seqres[b].a);
@@ -1552,40 +1647,46 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const Veri
         }
     }
     __syncthreads();
-    if (!s_last || warp != 0) return;
+    if (!s_last) return;  // CTA-uniform: the row's last CTA decides
     __threadfence();
-    if (lane == 0) {
-        P.seq_ticket2[b] = 0u;
-        P.row_thr[row] = 0u;  // leave the workspace zeroed
+    if (warp == 0) {
+        if (lane == 0) {
+            P.seq_ticket2[b] = 0u;
+            P.row_thr[row] = 0u;  // leave the workspace zeroed
+        }
+        const Partial* pr = P.part2 + static_cast<size_t>(b) * P.nchunk2;
+        Top2 t = top2_empty();
+        for (int cc = lane; cc < P.nchunk2; cc += 32) t = top2_merge(t, ldcg_partial(pr + cc).t);
+        t = top2_warp_reduce(t);
+        __syncwarp();
+        for (int cc = lane; cc < P.nchunk2; cc += 32) st_zero(const_cast<Partial*>(pr) + cc);
+        const int nw = PENALTY ? s_nwin : 0;
+        const bool pen1 = PENALTY && t.i1 >= 0 ? warp_in_window(t.i1, s_win, nw) : false;
+        const bool pen2 = PENALTY && t.i2 >= 0 ? warp_in_window(t.i2, s_win, nw) : false;
+        if (lane == 0) {
+            st_zero(P.rowres + row);
+            st_zero(P.seqres + b);
+            double best = -INFINITY;
+            int winner = -1;
+            for (int h = 0; h < 2; ++h) {
+                const int id = h == 0 ? t.i1 : t.i2;
+                if (id < 0) continue;
+                if (h == 1 && !(t.s2 >= t.s1 - cand_delta(t.s1))) continue;
+                const double z = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, id),
+                                                                 h == 0 ? pen1 : pen2, P);
+                const double rsd = exp(z / P.Td - lse) - static_cast<double>(qrow[id]);
+                if (!(rsd > 0.0)) continue;
+                const double score = log(rsd) - log(noise_exp_f64(nk, static_cast<uint32_t>(id), static_cast<uint32_t>(a)));
+                if (winner < 0 || better64(score, id, best, winner)) { best = score; winner = id; }
+            }
+            s_dec = winner;  // -1 for an all-zero residual
+        }
     }
-    const Partial* pr = P.part2 + static_cast<size_t>(b) * P.nchunk2;
-    Top2 t = top2_empty();
-    for (int cc = lane; cc < P.nchunk2; cc += 32) t = top2_merge(t, ldcg_partial(pr + cc).t);
-    t = top2_warp_reduce(t);
-    __syncwarp();
-    for (int cc = lane; cc < P.nchunk2; cc += 32) st_zero(const_cast<Partial*>(pr) + cc);
-    const int nw = PENALTY ? s_nwin : 0;
-    const bool pen1 = PENALTY && t.i1 >= 0 ? warp_in_window(t.i1, s_win, nw) : false;
-    const bool pen2 = PENALTY && t.i2 >= 0 ? warp_in_window(t.i2, s_win, nw) : false;
-    if (lane != 0) return;
-    const int bonus = __ldcg(&P.rowres[row].winner);
-    st_zero(P.rowres + row);
-    st_zero(P.seqres + b);
-    double best = -INFINITY;
-    int winner = -1;
-    for (int h = 0; h < 2; ++h) {
-        const int id = h == 0 ? t.i1 : t.i2;
-        if (id < 0) continue;
-        if (h == 1 && !(t.s2 >= t.s1 - cand_delta(t.s1))) continue;
-        const double z = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, id), h == 0 ? pen1 : pen2, P);
-        const double rsd = exp(z / P.Td - lse) - static_cast<double>(qrow[id]);
-        if (!(rsd > 0.0)) continue;
-        const double score = log(rsd) - log(noise_exp_f64(nk, static_cast<uint32_t>(id), static_cast<uint32_t>(a)));
-        if (winner < 0 || better64(score, id, best, winner)) { best = score; winner = id; }
-    }
-    // all-zero residual (p <= q everywhere): sample from p, the row's bonus candidate
-    if (winner < 0) winner = bonus;
-    P.out_tokens[static_cast<size_t>(b) * K1 + a] = winner;
+    __syncthreads();
+    int winner = s_dec;
+    // all-zero residual (p <= q everywhere): sample from p at row a with the same noise
+    if (winner < 0) winner = sample_p_row<BF16, SOFTCAP, PENALTY>(P, nk, row, a, s_win, PENALTY ? s_nwin : 0, s_t);
+    if (tid == 0) P.out_tokens[static_cast<size_t>(b) * K1 + a] = winner;
 }
 
 // ---------------------------------------------------------------- launch
@@ -1613,8 +1714,8 @@ cudaError_t launch_stream(const VerifyDev& P, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    verify_stream_kernel<BF16, G, C, R><<<sm_count_cached(), kPThreads, smem, s>>>(P);
-    return cudaGetLastError();
+    return launch_chained(verify_stream_kernel<BF16, G, C, R>, dim3(kK1PerSM * sm_count_cached()), dim3(kPThreads), smem, s,
+                          P);
 }
 
 template <bool BF16, bool G, bool C, bool R>
@@ -1629,15 +1730,13 @@ cudaError_t launch_seq(const VerifyDev& P, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    verify_seq_kernel<BF16, G, C, R><<<static_cast<unsigned>(P.B), kST, smem, s>>>(P);
-    return cudaGetLastError();
+    return launch_chained(verify_seq_kernel<BF16, G, C, R>, dim3(static_cast<unsigned>(P.B)), dim3(kST), smem, s, P);
 }
 
 template <bool BF16, bool C, bool R>
 cudaError_t launch_residual(const VerifyDev& P, cudaStream_t s) {
     const unsigned grid = static_cast<unsigned>(P.B) * static_cast<unsigned>(P.nchunk2);
-    verify_residual_kernel<BF16, C, R><<<grid, kThreads, 0, s>>>(P);
-    return cudaGetLastError();
+    return launch_chained(verify_residual_kernel<BF16, C, R>, dim3(grid), dim3(kThreads), 0, s, P);
 }
 
 template <bool BF16, bool G, bool C, bool R>

@@ -285,3 +285,43 @@ def test_commit_equals_append_update_draft(seed):
         np.testing.assert_array_equal(d2.cpu().numpy(), d_o)
         np.testing.assert_array_equal(k2.cpu().numpy(), k_o)
     assert sp.status_names(sp.get_status()) == ["HIST_OVERFLOW"]
+
+
+@pytest.mark.parametrize("rep", [1.0, 1.3])
+def test_all_zero_residual_falls_back_to_p(rep):
+    # q >= p everywhere (p rounded up to fp32) and q(d) = 1 at a draft of tiny p: the
+    # draft is rejected and the residual max(0, p - q) is zero everywhere, so the
+    # token is the Gumbel-max sample of p at that row (the oracle's fallback rule)
+    B, K, V, T = 4, 2, 5000, 0.7
+    g = torch.Generator().manual_seed(11)
+    logits = torch.randn(B, K + 1, V, generator=g) * 3
+    hist = torch.randint(0, V, (B, 40), generator=g, dtype=torch.int32)
+    lens = torch.full((B,), 40, dtype=torch.int32)
+    kw = dict(temperature=T, rep_penalty=rep, rep_window=16 if rep != 1.0 else 0, gate_enabled=False, seed=9, step=4)
+    op_ = ov.VerifyParams(**kw)
+    drafts = torch.zeros((B, K), dtype=torch.int32)
+    # drafts of tiny p, chosen row by row (the penalty window of row j covers the drafts before it)
+    for j in range(K):
+        zj = ov.transform_rows(logits.numpy().astype(np.float64), op_, hist.numpy(), lens.numpy(), drafts.numpy())
+        drafts[:, j] = torch.from_numpy(np.argmin(zj[:, j], axis=-1).astype(np.int32))
+    z = ov.transform_rows(logits.numpy().astype(np.float64), op_, hist.numpy(), lens.numpy(), drafts.numpy())
+    p = np.exp(ov.log_softmax(z[:, :K] / op_.f64("temperature")))
+    q = p.astype(np.float32)
+    q = np.where(q.astype(np.float64) < p, np.nextafter(q, np.float32(np.inf)), q).astype(np.float32)
+    q[np.arange(B)[:, None], np.arange(K)[None, :], drafts.numpy()] = 1.0
+    assert (q.astype(np.float64) >= p).all()
+    k = torch.full((B,), K, dtype=torch.int32)
+    dev = "cuda"
+    kv = torch.full((B,), 100, dtype=torch.int32, device=dev)
+    ema = torch.ones(B, dtype=torch.float32, device=dev)
+    out = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    acc = torch.empty((B,), dtype=torch.int32, device=dev)
+    ws = sp.spec_verify_workspace(B, K, V)
+    sp.spec_verify(logits.cuda(), drafts.cuda(), torch.from_numpy(q).cuda(), k.cuda(), hist.cuda(), lens.cuda(),
+                   sp.VerifyParams(**kw), kv, ema, out, acc, ws)
+    res = ov.spec_verify(logits.numpy(), drafts.numpy(), q, k.numpy(), hist.numpy(), lens.numpy(), op_,
+                         np.full(B, 100), np.ones(B))
+    assert (res["accept_len"] == 0).all()
+    np.testing.assert_array_equal(acc.cpu().numpy(), res["accept_len"])
+    np.testing.assert_array_equal(out.cpu().numpy(), res["out_tokens"])
+    assert sp.get_status() == 0
