@@ -30,9 +30,9 @@ template <bool BF16> struct ElemTraits;
 template <> struct ElemTraits<true> { static constexpr int EPV = 8; static constexpr int SIZE = 2; };
 template <> struct ElemTraits<false> { static constexpr int EPV = 4; static constexpr int SIZE = 4; };
 
-// One chunk of a row = one 32 KB stage of the streaming ring; the residual
+// One chunk of a row = one 64 KB stage of the streaming ring; the residual
 // pass takes 32 KB chunks, one per CTA.
-constexpr int kChunkBytes = 32768;
+constexpr int kChunkBytes = 65536;
 constexpr int kResChunkBytes = 32768;
 template <bool BF16>
 __host__ __device__ constexpr int chunk_elems() { return kChunkBytes / ElemTraits<BF16>::SIZE; }
@@ -52,9 +52,8 @@ struct __align__(32) Partial {
     int pad[2];
 };
 struct __align__(16) RowRes {
-    double lse;    // log-sum-exp of row / T (T > 0)
-    int winner;    // sampled id of this row over p (the fallback of an all-zero residual)
-    int accepted;
+    float m, S;    // the row's softmax normaliser: lse = m / T + ln S (T > 0)
+    int winner, pad;
 };
 struct __align__(16) SeqRes {
     int a, keff, need_residual, pad;
@@ -352,16 +351,16 @@ __device__ __forceinline__ uint4 mask_tail(uint4 r, int n) {
 }
 
 // ---------------------------------------------------------------- K1
-// Streaming kernel: bandwidth only.  Persistent and warp-specialised, one CTA
-// per SM; the active row-chunks of the call (rows 0..k_eff of every sequence,
-// chunks of 32 KB) are laid out row-major and split into equal contiguous
-// ranges, one per CTA.
+// Streaming kernel: bandwidth only.  Persistent and warp-specialised, kK1PerSM
+// CTAs per SM; the active row-chunks of the call (rows 0..k_eff of every
+// sequence, chunks of 64 KB) are laid out row-major and split into equal
+// contiguous ranges, one per CTA.
 //   * A producer warp walks the CTA's range and keeps up to kStages chunks in
 //     flight with cp.async.bulk into a shared-memory ring (full / empty
 //     mbarriers, bounded waits), with each chunk's row metadata and penalty
 //     bitmap.  The next sequence's drafts and history tail are fetched into
 //     registers one sequence ahead, so no global round trip stalls the copies.
-//   * Sixteen streaming warps each own a 2 KB slice of every chunk.  A warp's
+//   * Sixteen streaming warps each own a 4 KB slice of every chunk.  A warp's
 //     vector row (32 lanes x one 16-byte vector) of a bf16 chunk is one noise
 //     block (two rows for fp32): its largest raw logit goes to the workspace
 //     (packed maxima reduced across the warp).  The rows that carry an accept
@@ -373,10 +372,11 @@ __device__ __forceinline__ uint4 mask_tail(uint4 r, int n) {
 constexpr int kCWarps = 16;                    // streaming warps
 constexpr int kPWarp = kCWarps;                // producer warp index
 constexpr int kPThreads = (kCWarps + 1) * 32;  // 544
-constexpr int kK1PerSM = 2;                    // resident streaming CTAs per SM
+constexpr int kK1PerSM = 1;                    // resident streaming CTAs per SM
 constexpr int kStages = 3;                     // ring stages per CTA
-constexpr int kVL = 4;                         // 16-byte vectors per lane per chunk
+constexpr int kVL = 8;                         // 16-byte vectors per lane per chunk
 static_assert(kChunkBytes == kCWarps * 32 * kVL * 16, "stage layout");
+static_assert(kVL <= 8, "the penalty mask holds 8 vectors of a lane");
 static_assert((32 * 8) == (1 << kNoiseBlockShift), "a bf16 vector row of a warp is one noise block");
 
 template <bool PENALTY>
@@ -622,14 +622,14 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
         uint4 rv[kVL];
 #pragma unroll
         for (int i = 0; i < kVL; ++i) rv[i] = stage[ubase + i * 32 + lane];
-        // penalised elements of my lane (bit 8 i + e), only where the slice holds one
-        unsigned pmk = 0u;
+        // penalised elements of my lane (bit 8 i + e of a 64-bit mask), only where the slice holds one
+        unsigned long long pmk = 0ull;
         if constexpr (PENALTY) {
             if ((mt.penw >> warp) & 1u) {
 #pragma unroll
                 for (int i = 0; i < kVL; ++i) {
                     const int off = off0 + i * 32 * EPV;
-                    pmk |= ((bm[off >> 5] >> (off & 31)) & ((1u << EPV) - 1u)) << (8 * i);
+                    pmk |= static_cast<unsigned long long>((bm[off >> 5] >> (off & 31)) & ((1u << EPV) - 1u)) << (8 * i);
                 }
             }
         }
@@ -705,10 +705,10 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
                 }
                 if constexpr (PENALTY) {
                     // the few penalised elements: their terms are replaced by the penalised ones
-                    unsigned pw = pmk;
-                    while (pw != 0u) {
-                        const int bit = __ffs(pw) - 1;
-                        pw &= pw - 1u;
+                    unsigned long long pw = pmk;
+                    while (pw != 0ull) {
+                        const int bit = __ffsll(static_cast<long long>(pw)) - 1;
+                        pw &= pw - 1ull;
                         const float xe = elem_of_stage<BF16>(stage, off0 + (bit >> 3) * 32 * EPV + (bit & 7));
                         const float zu = transform_f32<SOFTCAP, false>(xe, false, P);
                         const float zp = transform_f32<SOFTCAP, true>(xe, true, P);
@@ -835,30 +835,33 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
 }
 
 // ---------------------------------------------------------------- K2
-// Decision kernel: one CTA of four warps per sequence.
-//   1. The accept tests (T > 0): warp w takes rows w, w + 4, ... < k_eff; the
-//      log-sum-exp of a row comes from its segment sums (fp64), and the test
-//      of d_{j+1} is taken in fp32 unless it is within 1e-4 of the boundary,
+// Decision kernel: one CTA of kSW warps per sequence, launched chained to the
+// streaming kernel (its prologue -- drafts, gate, the penalty window's table --
+// runs before the streaming kernel has finished).
+//   1. The accept tests (T > 0): warp w takes rows w, w + kSW, ... < k_eff;
+//      the log-sum-exp of a row comes from its segment sums, and the test of
+//      d_{j+1} is taken in fp32 unless it is within 1e-4 of the boundary,
 //      then in fp64.  At T = 0 every row 0..k_eff gets its argmax instead:
 //      the blocks whose largest value is within the tie margin of the best
 //      value found are read again.
 //   2. a = the first rejection (k_eff when none).
 //   3. The token at row a (T > 0): Gumbel-max over the row, draft d_{a+1}
-//      left out for a point-mass draft.  Each block's draw gives M and its
-//      slot; the bound z_max / T - ln M of every block goes to shared memory.
-//      Each warp reads again the block with its largest bound and each lane
-//      scores its largest element there, which starts the best; then only the
-//      blocks whose bound reaches the best are read again (eight per warp at
-//      once), and the elements whose own bound z / T - ln M reaches it are
-//      scored (per-id draw, E_v = M + F_v).  The two best fp32 scores are
-//      re-scored in fp64 when they are within the fp32 error of each other.
-//      With dense q the residual pass samples row a instead; this sample is
-//      its fallback for an all-zero residual.
+//      left out for a point-mass draft.  Each warp's block with the largest
+//      value is loaded first (the seed); meanwhile each block's draw gives M
+//      and its slot, and the bound z_max / T - ln M of every block goes to
+//      shared memory.  Each lane scores its largest element of the seed block,
+//      which starts the best; then only the blocks whose bound reaches the
+//      best are read again (kBatch per warp at once, screened against one
+//      raw-logit threshold per block), and each lane scores its own elements
+//      whose bound z / T - ln M reaches it (per-id draw, E_v = M + F_v).  The
+//      two best fp32 scores are re-scored in fp64 when they are within the
+//      fp32 error of each other.  With dense q a rejection's token is left to
+//      the residual pass.
 //   4. Epilogue: tokens, accept length, kv_len, EMA.
 
-constexpr int kSW = 8;                          // warps per sequence
+constexpr int kSW = 16;                         // warps per sequence
 constexpr int kST = kSW * 32;
-constexpr int kBatch = 8;                       // blocks a warp reads again at once
+constexpr int kBatch = 4;                       // blocks a warp reads again at once
 constexpr int kPenSlots = 2 * SPECNG_MAX_REP_WINDOW;
 constexpr int kPenBits = 9;
 static_assert((1 << kPenBits) == kPenSlots, "penalty table size");
@@ -915,11 +918,12 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const VerifyDev P) {
     constexpr int BLK = 1 << kNoiseBlockShift;
     constexpr int VPL = BLK / (32 * EPV);  // 16-byte vectors per lane per block (bf16 1, fp32 2)
     constexpr int NE = VPL * EPV;          // elements per lane per block
+    static_assert(kBatch * NE <= 64, "one 64-bit candidate mask per batch");
     extern __shared__ __align__(128) uint8_t s_dyn[];
     __shared__ int s_pkey[PENALTY ? kPenSlots : 1];
     __shared__ int s_ppos[PENALTY ? kPenSlots : 1];
     __shared__ int s_d[SPECNG_MAX_K + 1];
-    __shared__ double s_lse[SPECNG_MAX_K + 1];
+    __shared__ float2 s_ms[SPECNG_MAX_K + 1];
     __shared__ int s_acc[SPECNG_MAX_K + 1];
     __shared__ int s_arg[SPECNG_MAX_K + 1];
     __shared__ Top2 s_top[kSW];
@@ -1117,7 +1121,7 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const VerifyDev P) {
                     }
                 }
                 s_acc[j] = accepted;
-                s_lse[j] = (dense && !accepted) ? lse64() : 0.0;
+                s_ms[j] = make_float2(mf, Sf);
             }
         }
     }
@@ -1338,9 +1342,10 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const VerifyDev P) {
         }
         if (need) {
             RowRes rr;
-            rr.lse = s_lse[a];
-            rr.winner = y;
-            rr.accepted = 0;
+            rr.m = s_ms[a].x;
+            rr.S = s_ms[a].y;
+            rr.winner = -1;
+            rr.pad = 0;
             P.rowres[b * K1 + a] = rr;
             SeqRes sr;
             sr.a = a;
@@ -1491,8 +1496,8 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const Veri
     if (!need) return;
     const int a = __ldcg(&P.seqres[b].a);
     const int row = b * K1 + a;
-    const double lse = __ldcg(&P.rowres[row].lse);
-    const float lse_f = static_cast<float>(lse);
+    const float2 rms = __ldcg(reinterpret_cast<const float2*>(&P.rowres[row]));
+    const float lse_f = rms.x * P.invT + logf(rms.y);
     const int v0 = c * CHUNK;
     const int v1 = min(P.V, v0 + CHUNK);
     const char* rowp = static_cast<const char*>(P.logits) +
@@ -1663,11 +1668,23 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const Veri
         const int nw = PENALTY ? s_nwin : 0;
         const bool pen1 = PENALTY && t.i1 >= 0 ? warp_in_window(t.i1, s_win, nw) : false;
         const bool pen2 = PENALTY && t.i2 >= 0 ? warp_in_window(t.i2, s_win, nw) : false;
+        // fp32 decision when it is safe: the best is clear of the second by more than
+        // the fp32 error and its residual clearly positive (ln p - ln q > 1e-4, far
+        // above the fp32 error of either); otherwise both are re-scored in fp64
+        float dres = 0.0f;
+        if (lane == 0 && t.i1 >= 0) {
+            const float x1 = static_cast<float>(raw_logit_f64<BF16>(P.logits, row, P.V, t.i1));
+            dres = lp_of(x1, pen1) - logf(__ldcg(qrow + t.i1));
+        }
         if (lane == 0) {
             st_zero(P.rowres + row);
             st_zero(P.seqres + b);
             double best = -INFINITY;
             int winner = -1;
+            const bool clear2 = t.i2 < 0 || !(t.s2 >= t.s1 - cand_delta(t.s1));
+            if (t.i1 >= 0 && clear2 && dres > 1e-4f) winner = t.i1;
+            if (winner < 0) {
+            const double lse = static_cast<double>(rms.x) / P.Td + log(static_cast<double>(rms.y));
             for (int h = 0; h < 2; ++h) {
                 const int id = h == 0 ? t.i1 : t.i2;
                 if (id < 0) continue;
@@ -1678,6 +1695,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const Veri
                 if (!(rsd > 0.0)) continue;
                 const double score = log(rsd) - log(noise_exp_f64(nk, static_cast<uint32_t>(id), static_cast<uint32_t>(a)));
                 if (winner < 0 || better64(score, id, best, winner)) { best = score; winner = id; }
+            }
             }
             s_dec = winner;  // -1 for an all-zero residual
         }
