@@ -104,6 +104,9 @@ __global__ void __launch_bounds__(kNgThreads) ngram_count_kernel(const NgramDev 
 
 __device__ __forceinline__ void push_best(const NgramDev& T, const ulonglong2* pairs, ulonglong2* ctxs,
                                           uint64_t pair_key, uint64_t ctx_key, int c) {
+    // the context's home slot does not depend on the pair's value: start its
+    // fetch into L2 now, so its probe below does not wait on HBM again
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(&ctxs[mix64(ctx_key) & T.mask]));
     uint64_t pv;
     if (!find_value(pairs, T.mask, pair_key, &pv)) return;  // insert failed in the count phase
     uint64_t count = pv & 0xFFFFFFFFull;
@@ -223,6 +226,48 @@ __device__ void draft_one(const NgramDev& T, int b, const int32_t* h, int L, int
     out_k[b] = n;
 }
 
+// The same drafts as draft_one, by a whole warp: at every draft position the
+// trigram probe (lane 0) and the bigram probe (lane 1) are in flight together,
+// so a position costs one probe latency, not two.
+__device__ void draft_warp(const NgramDev& T, int b, const int32_t* h, int L, int max_k, const int32_t* k_limit,
+                           const int32_t* fallback, int32_t* out_drafts, int32_t* out_k) {
+    const int lane = threadIdx.x & 31;
+    int kmax = max_k;
+    if (k_limit != nullptr) {
+        const int kl = k_limit[b];
+        kmax = kl < 0 ? 0 : (kl < kmax ? kl : kmax);
+    }
+    int c2 = L >= 2 ? h[L - 2] : -1;
+    int c1 = L >= 1 ? h[L - 1] : -1;
+    if (lane == 0 && ((L >= 2 && !tok_ok(c2, T.V)) || (L >= 1 && !tok_ok(c1, T.V))))
+        raise_status(T.status, SPECNG_DEV_TOKEN_OOR);
+    if (!tok_ok(c2, T.V)) c2 = -1;
+    if (!tok_ok(c1, T.V)) c1 = -1;
+    int n = 0;
+    int32_t* out = out_drafts + static_cast<size_t>(b) * max_k;
+    while (n < kmax && c1 >= 0) {  // warp-uniform
+        int tok = -1;
+        uint64_t v;
+        if (lane == 0 && c2 >= 0 && find_value(T.tri_ctx, T.mask, key_tri_ctx(b, c2, c1), &v)) tok = best_token(v);
+        if (lane == 1 && find_value(T.bi_ctx, T.mask, key_bi_ctx(b, c1), &v)) tok = best_token(v);
+        const int tt = __shfl_sync(0xffffffffu, tok, 0), tb = __shfl_sync(0xffffffffu, tok, 1);
+        tok = tt >= 0 ? tt : tb;
+        if (tok < 0) break;
+        if (lane == 0) out[n] = tok;
+        ++n;
+        c2 = c1;
+        c1 = tok;
+    }
+    int nf = n;
+    if (fallback != nullptr) {
+        const int32_t* fb = fallback + static_cast<size_t>(b) * max_k;
+        for (int t = n + lane; t < kmax; t += 32) out[t] = fb[t];
+        nf = n > kmax ? n : kmax;
+    }
+    for (int t = nf + lane; t < max_k; t += 32) out[t] = -1;
+    if (lane == 0) out_k[b] = nf;
+}
+
 // One step's commit for every sequence, one warp per sequence: append the
 // emitted tokens (spec_append), index the new positions (ngram_update: pair
 // counts, then the contexts' best continuations) and draft the next step
@@ -259,47 +304,40 @@ __global__ void __launch_bounds__(kNgThreads) spec_commit_kernel(const NgramDev 
     const int idx = T.indexed[parity][b];
     if (L < idx && lane == 0) raise_status(T.status, SPECNG_DEV_HIST_SHRANK);
     const int lo = idx > 1 ? idx : 1;
-    for (int i = lo + lane; i < L; i += 32) {
-        const int c = h[i], t1 = h[i - 1];
-        if (!tok_ok(c, T.V) || !tok_ok(t1, T.V)) { raise_status(T.status, SPECNG_DEV_TOKEN_OOR); continue; }
-        int64_t slot = find_or_insert(T.bi_pair, T.mask, key_bi_pair(b, t1, c));
+    // half-warps: the bigram pairs on lanes 0..15, the trigram pairs on lanes 16..31,
+    // so the two probe chains of a position run side by side
+    const bool tri = lane >= 16;
+    for (int i = lo + (lane & 15); i < L; i += 16) {
+        if (tri && i < 2) continue;
+        const int c = h[i], t1 = h[i - 1], t2 = tri ? h[i - 2] : 0;
+        if (!tok_ok(c, T.V) || !tok_ok(t1, T.V) || (tri && !tok_ok(t2, T.V))) {
+            raise_status(T.status, SPECNG_DEV_TOKEN_OOR);
+            continue;
+        }
+        ulonglong2* tab = tri ? T.tri_pair : T.bi_pair;
+        const int64_t slot = find_or_insert(tab, T.mask, tri ? key_tri_pair(b, t2, t1, c) : key_bi_pair(b, t1, c));
         if (slot < 0) {
             raise_status(T.status, SPECNG_DEV_TABLE_FULL);
         } else {
-            unsigned* v = reinterpret_cast<unsigned*>(&T.bi_pair[slot].y);
+            unsigned* v = reinterpret_cast<unsigned*>(&tab[slot].y);
             atomicAdd(v, 1u);
             atomicMax(v + 1, static_cast<unsigned>(i));
         }
-        if (i >= 2) {
-            const int t2 = h[i - 2];
-            if (!tok_ok(t2, T.V)) { raise_status(T.status, SPECNG_DEV_TOKEN_OOR); continue; }
-            slot = find_or_insert(T.tri_pair, T.mask, key_tri_pair(b, t2, t1, c));
-            if (slot < 0) {
-                raise_status(T.status, SPECNG_DEV_TABLE_FULL);
-            } else {
-                unsigned* v = reinterpret_cast<unsigned*>(&T.tri_pair[slot].y);
-                atomicAdd(v, 1u);
-                atomicMax(v + 1, static_cast<unsigned>(i));
-            }
-        }
     }
     __syncwarp();
-    for (int i = lo + lane; i < L; i += 32) {
-        const int c = h[i], t1 = h[i - 1];
-        if (!tok_ok(c, T.V) || !tok_ok(t1, T.V)) continue;
-        push_best(T, T.bi_pair, T.bi_ctx, key_bi_pair(b, t1, c), key_bi_ctx(b, t1), c);
-        if (i >= 2) {
-            const int t2 = h[i - 2];
-            if (!tok_ok(t2, T.V)) continue;
+    for (int i = lo + (lane & 15); i < L; i += 16) {
+        if (tri && i < 2) continue;
+        const int c = h[i], t1 = h[i - 1], t2 = tri ? h[i - 2] : 0;
+        if (!tok_ok(c, T.V) || !tok_ok(t1, T.V) || (tri && !tok_ok(t2, T.V))) continue;
+        if (tri)
             push_best(T, T.tri_pair, T.tri_ctx, key_tri_pair(b, t2, t1, c), key_tri_ctx(b, t2, t1), c);
-        }
+        else
+            push_best(T, T.bi_pair, T.bi_ctx, key_bi_pair(b, t1, c), key_bi_ctx(b, t1), c);
     }
     __syncwarp();
-    if (lane == 0) {
-        T.indexed[parity ^ 1][b] = L > idx ? L : idx;
-        // ---- the next step's drafts
-        draft_one(T, b, h, L, max_k, k_limit, fallback, out_drafts, out_k);
-    }
+    if (lane == 0) T.indexed[parity ^ 1][b] = L > idx ? L : idx;
+    // ---- the next step's drafts
+    draft_warp(T, b, h, L, max_k, k_limit, fallback, out_drafts, out_k);
 }
 
 __global__ void philox_kernel(const uint4* ctr, uint32_t k0, uint32_t k1, uint4* out, int64_t n) {

@@ -912,6 +912,22 @@ static __device__ __noinline__ bool pen_lookup(const int* key, const int* pos, c
     return false;
 }
 
+// The two best fp32 sampling scores of row `row` (position a) re-scored in
+// fp64, the oracle's arithmetic: returns the winner (lower id on a tie).  Out
+// of line: it runs only for near ties, and keeps the fp64 code out of the
+// kernel's hot path.
+template <bool BF16, bool SOFTCAP, bool PENALTY>
+__device__ __noinline__ int rescore_top2_f64(const VerifyDev& P, const NoiseKey& nk, int row, int a, int i1, int i2,
+                                             bool pen1, bool pen2) {
+    double sc[2];
+    for (int h = 0; h < 2; ++h) {
+        const int id = h == 0 ? i1 : i2;
+        const double z = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, id), h == 0 ? pen1 : pen2, P);
+        sc[h] = z / P.Td - log(noise_exp_f64(nk, static_cast<uint32_t>(id), static_cast<uint32_t>(a)));
+    }
+    return better64(sc[1], i2, sc[0], i1) ? i2 : i1;
+}
+
 template <bool BF16, bool GREEDY, bool SOFTCAP, bool PENALTY>
 __global__ void __launch_bounds__(kST) verify_seq_kernel(const VerifyDev P) {
     constexpr int EPV = ElemTraits<BF16>::EPV;
@@ -1063,9 +1079,14 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const VerifyDev P) {
             const int d = s_d[j];
             const bool dv = d >= 0 && d < P.V;
             float xd = 0.0f, qdf = 1.0f;
+            double u = 0.0;
+            bool pend = false;
             if (lane == 0 && dv) {
                 xd = static_cast<float>(raw_logit_f64<BF16>(P.logits, row, P.V, d));
                 if (dense) qdf = P.q[(static_cast<size_t>(b) * P.K + j) * P.V + d];
+                // the draw and the window test need no load: they run while the loads are in flight
+                u = accept_uniform_f64(nk, static_cast<uint32_t>(j + 1));
+                pend = pen_of(d, j);
             }
             // one pass over the segment sums: a lane keeps its first kPr records in registers
             constexpr int kPr = 4;
@@ -1107,8 +1128,6 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const VerifyDev P) {
                 int accepted = 0;
                 if (dv) {
                     const double qd = static_cast<double>(qdf);
-                    const bool pend = pen_of(d, j);
-                    const double u = accept_uniform_f64(nk, static_cast<uint32_t>(j + 1));
                     const float lp = transform_f32<SOFTCAP, PENALTY>(xd, pend, P) * P.invT - lsef;
                     const float lr = logf(static_cast<float>(u)) + logf(static_cast<float>(qd));
                     if (lr < lp - 1e-4f * (1.0f + fabsf(lp))) {
@@ -1311,16 +1330,9 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const VerifyDev P) {
 #pragma unroll
             for (int off = kSW / 2; off > 0; off >>= 1) tw = top2_merge(tw, top2_shfl_xor(tw, off));
             int w = tw.i1;
-            if (lane == 0 && tw.i2 >= 0 && tw.s2 >= tw.s1 - cand_delta(tw.s1)) {
-                double sc[2];
-                for (int h = 0; h < 2; ++h) {
-                    const int id = h == 0 ? tw.i1 : tw.i2;
-                    const double z = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, id),
-                                                                     PENALTY && pen_of(id, a), P);
-                    sc[h] = z / P.Td - log(noise_exp_f64(nk, static_cast<uint32_t>(id), static_cast<uint32_t>(a)));
-                }
-                if (better64(sc[1], tw.i2, sc[0], tw.i1)) w = tw.i2;
-            }
+            if (lane == 0 && tw.i2 >= 0 && tw.s2 >= tw.s1 - cand_delta(tw.s1))
+                w = rescore_top2_f64<BF16, SOFTCAP, PENALTY>(P, nk, row, a, tw.i1, tw.i2, PENALTY && pen_of(tw.i1, a),
+                                                            PENALTY && pen_of(tw.i2, a));
             if (lane == 0) s_y = w;
         }
         __syncthreads();
