@@ -393,8 +393,55 @@ struct StageMeta {
     int pad[2];
 };
 
+// Running state of a lane's sum of exponentials: reference m (transformed
+// units), the sum s of exp((z - m) / T), and m * log2(e) / T.
+struct SumState {
+    float m, s, msc;
+};
+
+// Cold paths of the streaming warps, kept out of line so the hot loop stays
+// small in the instruction cache; both read the lane's vectors back from the
+// stage.  sum_from_stage: the lane's chunk against reference msc (after the
+// reference was raised).  sum_partial: a row's last chunk, element by
+// element with the exact transform, for vectors that pass the row's end.
+template <bool BF16, bool SOFTCAP>
+__device__ __noinline__ float sum_from_stage(const uint4* stage, int vec0, float msc, const VerifyDev& P) {
+    constexpr int EPV = ElemTraits<BF16>::EPV;
+    float add = 0.0f;
+#pragma unroll 1
+    for (int i = 0; i < kVL; ++i) {
+        float x[EPV];
+        unpack<BF16>(stage[vec0 + i * 32], x);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) add += ex2_approx(fmaf(transform_f32<SOFTCAP, false>(x[e], false, P), P.sc, -msc));
+    }
+    return add;
+}
+
+template <bool BF16, bool SOFTCAP, bool PENALTY>
+__device__ __noinline__ SumState sum_partial(const uint4* stage, int off0, int v0, int v1, unsigned long long pmk,
+                                             SumState st, const VerifyDev& P) {
+    constexpr int EPV = ElemTraits<BF16>::EPV;
+#pragma unroll 1
+    for (int i = 0; i < kVL; ++i) {
+        const int off = off0 + i * 32 * EPV;
+        const int nv = min(EPV, v1 - (v0 + off));
+#pragma unroll 1
+        for (int e = 0; e < nv; ++e) {
+            const float z = transform_f32<SOFTCAP, PENALTY>(elem_of_stage<BF16>(stage, off + e), (pmk >> (8 * i + e)) & 1ull, P);
+            if (!(st.m > -INFINITY) || (z - st.m) * P.sc > 32.0f) {
+                st.s = st.m > -INFINITY ? st.s * ex2_approx((st.m - z) * P.sc) : 0.0f;
+                st.m = z;
+                st.msc = st.m * P.sc;
+            }
+            st.s += ex2_approx(fmaf(z, P.sc, -st.msc));
+        }
+    }
+    return st;
+}
+
 template <bool BF16, bool GREEDY, bool SOFTCAP, bool PENALTY>
-__global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(const VerifyDev P) {
+__global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(const __grid_constant__ VerifyDev P) {
     constexpr int EPV = ElemTraits<BF16>::EPV;
     constexpr int CHUNK = chunk_elems<BF16>();
     constexpr int SB = kChunkBytes;
@@ -691,15 +738,7 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
                         s *= ex2_approx((m - zl) * P.sc);
                         m = zl;
                         msc = m * P.sc;
-                        add = 0.0f;
-#pragma unroll
-                        for (int i = 0; i < kVL; ++i) {
-                            float x[EPV];
-                            unpack<BF16>(rv[i], x);
-#pragma unroll
-                            for (int e = 0; e < EPV; ++e)
-                                add += ex2_approx(fmaf(transform_f32<SOFTCAP, false>(x[e], false, P), P.sc, -msc));
-                        }
+                        add = sum_from_stage<BF16, SOFTCAP>(stage, ubase + lane, msc, P);
                     }
                     s += add;
                 }
@@ -722,25 +761,10 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
                 }
             } else {
                 // partial vectors (a row's last chunk): exact transform element by element
-#pragma unroll
-                for (int i = 0; i < kVL; ++i) {
-                    const int off = off0 + i * 32 * EPV;
-                    const int nv = min(EPV, v1 - (v0 + off));
-                    if (nv <= 0) continue;
-                    float x[EPV];
-                    unpack<BF16>(rv[i], x);
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e) {
-                        if (e >= nv) break;
-                        const float z = transform_f32<SOFTCAP, PENALTY>(x[e], (pmk >> (8 * i + e)) & 1u, P);
-                        if (!(m > -INFINITY) || (z - m) * P.sc > 32.0f) {
-                            s = m > -INFINITY ? s * ex2_approx((m - z) * P.sc) : 0.0f;
-                            m = z;
-                            msc = m * P.sc;
-                        }
-                        s += ex2_approx(fmaf(z, P.sc, -msc));
-                    }
-                }
+                const SumState st = sum_partial<BF16, SOFTCAP, PENALTY>(stage, off0, v0, v1, pmk, SumState{m, s, msc}, P);
+                m = st.m;
+                s = st.s;
+                msc = st.msc;
             }
         }
         // ---- block maxima (raw logits): vector row i of the warp (rows i, i + 1 for
@@ -929,7 +953,7 @@ __device__ __noinline__ int rescore_top2_f64(const VerifyDev& P, const NoiseKey&
 }
 
 template <bool BF16, bool GREEDY, bool SOFTCAP, bool PENALTY>
-__global__ void __launch_bounds__(kST) verify_seq_kernel(const VerifyDev P) {
+__global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__ VerifyDev P) {
     constexpr int EPV = ElemTraits<BF16>::EPV;
     constexpr int BLK = 1 << kNoiseBlockShift;
     constexpr int VPL = BLK / (32 * EPV);  // 16-byte vectors per lane per block (bf16 1, fp32 2)
@@ -1485,7 +1509,7 @@ __device__ __noinline__ int sample_p_row(const VerifyDev& P, const NoiseKey& nk,
 }
 
 template <bool BF16, bool SOFTCAP, bool PENALTY>
-__global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const VerifyDev P) {
+__global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const __grid_constant__ VerifyDev P) {
     constexpr int EPV = ElemTraits<BF16>::EPV;
     constexpr int CHUNK = res_chunk_elems<BF16>();
     constexpr int NB = CHUNK >> kNoiseBlockShift;
