@@ -967,7 +967,7 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
     __shared__ int s_acc[SPECNG_MAX_K + 1];
     __shared__ int s_arg[SPECNG_MAX_K + 1];
     __shared__ Top2 s_top[kSW];
-    __shared__ unsigned s_thr;
+    __shared__ unsigned s_thr, s_thr0;
     __shared__ int s_nl;
     __shared__ int s_y;
     __shared__ int s_bq[kSW][kBatch];
@@ -989,6 +989,7 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
     }
     if (tid == 0) {
         s_thr = 0u;
+        s_thr0 = 0u;
         s_nl = 0;
     }
     if constexpr (PENALTY) {
@@ -1036,6 +1037,82 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
     };
     auto elem_id = [&](int q, int k) { return q * BLK + ((k / EPV) * 32 + lane) * EPV + (k % EPV); };
 
+    // Preparation of the sampling at row ra (T > 0): every block's draw and bound
+    // into shared memory, and each participating warp's seed score (the best of
+    // its largest element in its block with the largest value) into *thr_slot.
+    // Threads t of nt take part, whole warps; ex is the id left out.
+    const int nblk = P.nblk;
+    uint8_t* scr = nblk <= kSmemBlkCap ? s_dyn : P.blkws + static_cast<size_t>(b) * nblk * kBlkScratchBytes;
+    float* s_bnd = reinterpret_cast<float*>(scr);
+    float* s_M = s_bnd + nblk;
+    int* s_I = reinterpret_cast<int*>(s_M + nblk);
+    int* s_list = s_I + nblk;
+    uint4* stg = reinterpret_cast<uint4*>(s_dyn + k2_blk_bytes(nblk)) + warp * (kBatch * 32 * VPL);
+    auto prepare = [&](int ra, int ex, int t, int nt, unsigned* thr_slot) {
+        const float* bmx = P.bmax + static_cast<size_t>(b * K1 + ra) * nblk;
+        const char* rowp = rowp_of(b * K1 + ra);
+        const RowPhilox rpr = row_philox(nk, static_cast<uint32_t>(ra));
+        // each warp's seed: its block with the largest value (the blocks' maxima are
+        // loaded first); the seed block's load is issued before the block draws, so
+        // its latency overlaps them
+        float lb = -INFINITY;
+        int lq = -1;
+        for (int q = t; q < nblk; q += nt) {
+            const float zq = bmx[q];
+            if (zq > lb) { lb = zq; lq = q; }
+        }
+        const unsigned kq = warp_best_key(lb);
+        const unsigned own = __ballot_sync(0xffffffffu, kq != 0u && lb > -INFINITY && score_key(lb) == kq);
+        const int qs = own ? __shfl_sync(0xffffffffu, lq, __ffs(own) - 1) : -1;
+        uint4 rs[VPL];
+        if (qs >= 0) load_block(rowp, qs, rs);
+        // block draws and bounds
+        for (int q0 = t; q0 < nblk; q0 += 4 * nt) {
+            float zq[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) zq[i] = q0 + i * nt < nblk ? bmx[q0 + i * nt] : -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int q = q0 + i * nt;
+                if (q >= nblk) break;
+                const BlockNoise bn = block_noise(nk, static_cast<uint32_t>(q), static_cast<uint32_t>(ra));
+                s_bnd[q] = block_zmax<SOFTCAP, PENALTY>(zq[i], P) * P.invT - bn.lnM;
+                s_M[q] = bn.M;
+                s_I[q] = bn.I;
+            }
+        }
+        // seed: each lane scores its largest element of the warp's seed block (the
+        // seed block's draw is the same function of (row, block) as above)
+        {
+            float sc = -INFINITY;
+            if (qs >= 0) {
+                float xb = -INFINITY;
+                int vb = -1;
+#pragma unroll
+                for (int u = 0; u < VPL; ++u) {
+                    float x[EPV];
+                    unpack<BF16>(rs[u], x);
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) {
+                        const int v = elem_id(qs, u * EPV + e);
+                        if (v < P.V && v != ex && (vb < 0 || x[e] > xb)) { xb = x[e]; vb = v; }
+                    }
+                }
+                if (vb >= 0) {
+                    const BlockNoise bn = block_noise(nk, static_cast<uint32_t>(qs), static_cast<uint32_t>(ra));
+                    const float zb = transform_f32<SOFTCAP, PENALTY>(xb, PENALTY && pen_of(vb, ra), P) * P.invT;
+                    sc = zb - ln_fast(noise_exp_f32(rpr, bn.M, bn.I, static_cast<uint32_t>(vb)));
+                }
+            }
+            const unsigned kw = warp_best_key(sc);
+            if (kw != 0u && lane == 0) atomicMax(thr_slot, kw);
+        }
+    };
+    // Row 0 is sampled by this kernel whenever a = 0 and no residual pass takes it
+    // (point-mass drafts, or no draft at all): the warps without an accept test
+    // prepare it meanwhile, which takes its preparation off the critical path
+    // when the first draft is rejected.
+    const bool spec0 = !GREEDY && (!dense || keff == 0);
     // ---- 1. accept tests (T > 0) / argmax of every row (T = 0)
     for (int j = warp; j <= keff; j += kSW) {
         const int row = b * K1 + j;
@@ -1168,6 +1245,10 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
             }
         }
     }
+    if constexpr (!GREEDY) {
+        if (spec0 && warp >= keff)
+            prepare(0, keff > 0 && s_d[0] >= 0 && s_d[0] < P.V ? s_d[0] : -1, tid - 32 * keff, kST - 32 * keff, &s_thr0);
+    }
     __syncthreads();
 
     // ---- 2. acceptance length
@@ -1187,70 +1268,12 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
     } else {
         const int row = b * K1 + a;
         const int excl = (a < keff && dvalid) ? da : -1;  // point mass here: dense rejections took the branch above
-        const float* bmx = P.bmax + static_cast<size_t>(row) * P.nblk;
         const char* rowp = rowp_of(row);
-        const int nblk = P.nblk;
-        uint8_t* scr = nblk <= kSmemBlkCap ? s_dyn : P.blkws + static_cast<size_t>(b) * nblk * kBlkScratchBytes;
-        float* s_bnd = reinterpret_cast<float*>(scr);
-        float* s_M = s_bnd + nblk;
-        int* s_I = reinterpret_cast<int*>(s_M + nblk);
-        int* s_list = s_I + nblk;
-        uint4* stg = reinterpret_cast<uint4*>(s_dyn + k2_blk_bytes(nblk)) + warp * (kBatch * 32 * VPL);
         const RowPhilox rp = row_philox(nk, static_cast<uint32_t>(a));
-        // each warp's seed: its block with the largest value (the blocks' maxima are
-        // loaded first); the seed block's load is issued before the block draws, so
-        // its latency overlaps them
-        float lb = -INFINITY;
-        int lq = -1;
-        for (int q = tid; q < nblk; q += kST) {
-            const float zq = bmx[q];
-            if (zq > lb) { lb = zq; lq = q; }
-        }
-        const unsigned kq = warp_best_key(lb);
-        const unsigned own = __ballot_sync(0xffffffffu, kq != 0u && lb > -INFINITY && score_key(lb) == kq);
-        const int qs = own ? __shfl_sync(0xffffffffu, lq, __ffs(own) - 1) : -1;
-        uint4 rs[VPL];
-        if (qs >= 0) load_block(rowp, qs, rs);
-        // block draws and bounds
-        for (int q0 = tid; q0 < nblk; q0 += 4 * kST) {
-            float zq[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) zq[i] = q0 + i * kST < nblk ? bmx[q0 + i * kST] : -INFINITY;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int q = q0 + i * kST;
-                if (q >= nblk) break;
-                const BlockNoise bn = block_noise(nk, static_cast<uint32_t>(q), static_cast<uint32_t>(a));
-                s_bnd[q] = block_zmax<SOFTCAP, PENALTY>(zq[i], P) * P.invT - bn.lnM;
-                s_M[q] = bn.M;
-                s_I[q] = bn.I;
-            }
-        }
-        // seed: each lane scores its largest element of the warp's seed block (the
-        // seed block's draw is the same function of (row, block) as above)
-        {
-            float sc = -INFINITY;
-            if (qs >= 0) {
-                float xb = -INFINITY;
-                int vb = -1;
-#pragma unroll
-                for (int u = 0; u < VPL; ++u) {
-                    float x[EPV];
-                    unpack<BF16>(rs[u], x);
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e) {
-                        const int v = elem_id(qs, u * EPV + e);
-                        if (v < P.V && v != excl && (vb < 0 || x[e] > xb)) { xb = x[e]; vb = v; }
-                    }
-                }
-                if (vb >= 0) {
-                    const BlockNoise bn = block_noise(nk, static_cast<uint32_t>(qs), static_cast<uint32_t>(a));
-                    const float zb = transform_f32<SOFTCAP, PENALTY>(xb, PENALTY && pen_of(vb, a), P) * P.invT;
-                    sc = zb - ln_fast(noise_exp_f32(rp, bn.M, bn.I, static_cast<uint32_t>(vb)));
-                }
-            }
-            const unsigned kw = warp_best_key(sc);
-            if (kw != 0u && lane == 0) atomicMax(&s_thr, kw);
+        if (a == 0 && spec0) {
+            if (tid == 0) s_thr = s_thr0;  // row 0 was prepared during the accept tests
+        } else {
+            prepare(a, excl, tid, kST, &s_thr);
         }
         __syncthreads();
         float thr = -INFINITY;
