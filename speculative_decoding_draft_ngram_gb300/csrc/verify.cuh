@@ -952,6 +952,100 @@ __device__ __noinline__ int rescore_top2_f64(const VerifyDev& P, const NoiseKey&
     return better64(sc[1], i2, sc[0], i1) ? i2 : i1;
 }
 
+// The accept test u q(d) <= p(d) in fp64, the oracle's arithmetic, for a test
+// within the fp32 screen's margin of its boundary; x: the draft's raw logit,
+// (mf, Sf): the row's normaliser.  Out of line: it is rarely taken.
+template <bool SOFTCAP, bool PENALTY>
+__device__ __noinline__ int accept_f64(const VerifyDev& P, float x, bool pen, double u, double q, float mf, float Sf) {
+    const double lse = static_cast<double>(mf) / P.Td + log(static_cast<double>(Sf));
+    const double zd = transform_f64<SOFTCAP, PENALTY>(static_cast<double>(x), pen, P);
+    return u * q <= exp(zd / P.Td - lse) ? 1 : 0;
+}
+
+// Preparation of the sampling at row ra of sequence b (T > 0): every noise
+// block's draw and bound z_max / T - ln M into s_bnd / s_M / s_I, and each
+// participating warp's seed score (its largest element in its block with the
+// largest value, with the element's own draw) into *thr_slot.  Threads t of
+// nt take part, whole warps; ex is the id left out (-1: none).  Out of line:
+// the decision kernel calls it from two places and its code would otherwise
+// be there twice.
+template <bool BF16, bool SOFTCAP, bool PENALTY>
+__device__ __noinline__ void prepare_row(const VerifyDev& P, const NoiseKey& nk, int b, int ra, int ex, int t, int nt,
+                                         unsigned* thr_slot, float* s_bnd, float* s_M, int* s_I, const int* pen_key,
+                                         const int* pen_pos, const int* drafts, int nh) {
+    constexpr int EPV = ElemTraits<BF16>::EPV;
+    constexpr int BLK = 1 << kNoiseBlockShift;
+    constexpr int VPL = BLK / (32 * EPV);
+    const int lane = threadIdx.x & 31;
+    const int K1 = P.K + 1;
+    const int nblk = P.nblk;
+    const float* bmx = P.bmax + static_cast<size_t>(b * K1 + ra) * nblk;
+    const char* rowp = static_cast<const char*>(P.logits) + static_cast<size_t>(b * K1 + ra) * P.V * ElemTraits<BF16>::SIZE;
+    const RowPhilox rpr = row_philox(nk, static_cast<uint32_t>(ra));
+    // each warp's seed: its block with the largest value (the blocks' maxima are
+    // loaded first); the seed block's load is issued before the block draws, so
+    // its latency overlaps them
+    float lb = -INFINITY;
+    int lq = -1;
+    for (int q = t; q < nblk; q += nt) {
+        const float zq = bmx[q];
+        if (zq > lb) { lb = zq; lq = q; }
+    }
+    const unsigned kq = warp_best_key(lb);
+    const unsigned own = __ballot_sync(0xffffffffu, kq != 0u && lb > -INFINITY && score_key(lb) == kq);
+    const int qs = own ? __shfl_sync(0xffffffffu, lq, __ffs(own) - 1) : -1;
+    uint4 rs[VPL];
+    if (qs >= 0) {
+#pragma unroll
+        for (int u = 0; u < VPL; ++u) {
+            const int e0 = qs * BLK + (u * 32 + lane) * EPV;
+            rs[u] = e0 < P.V ? load_vec<BF16>(rowp, e0, P.V, P.aligned) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    // block draws and bounds
+    for (int q0 = t; q0 < nblk; q0 += 4 * nt) {
+        float zq[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) zq[i] = q0 + i * nt < nblk ? bmx[q0 + i * nt] : -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int q = q0 + i * nt;
+            if (q >= nblk) break;
+            const BlockNoise bn = block_noise(nk, static_cast<uint32_t>(q), static_cast<uint32_t>(ra));
+            s_bnd[q] = block_zmax<SOFTCAP, PENALTY>(zq[i], P) * P.invT - bn.lnM;
+            s_M[q] = bn.M;
+            s_I[q] = bn.I;
+        }
+    }
+    // seed: each lane scores its largest element of the warp's seed block (the
+    // seed block's draw is the same function of (row, block) as above)
+    {
+        float sc = -INFINITY;
+        if (qs >= 0) {
+            float xb = -INFINITY;
+            int vb = -1;
+#pragma unroll
+            for (int u = 0; u < VPL; ++u) {
+                float x[EPV];
+                unpack<BF16>(rs[u], x);
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) {
+                    const int v = qs * BLK + (u * 32 + lane) * EPV + e;
+                    if (v < P.V && v != ex && (vb < 0 || x[e] > xb)) { xb = x[e]; vb = v; }
+                }
+            }
+            if (vb >= 0) {
+                const BlockNoise bn = block_noise(nk, static_cast<uint32_t>(qs), static_cast<uint32_t>(ra));
+                const bool pen = PENALTY && pen_lookup(pen_key, pen_pos, drafts, nh, P.W, vb, ra);
+                const float zb = transform_f32<SOFTCAP, PENALTY>(xb, pen, P) * P.invT;
+                sc = zb - ln_fast(noise_exp_f32(rpr, bn.M, bn.I, static_cast<uint32_t>(vb)));
+            }
+        }
+        const unsigned kw = warp_best_key(sc);
+        if (kw != 0u && lane == 0) atomicMax(thr_slot, kw);
+    }
+}
+
 template <bool BF16, bool GREEDY, bool SOFTCAP, bool PENALTY>
 __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__ VerifyDev P) {
     constexpr int EPV = ElemTraits<BF16>::EPV;
@@ -1037,10 +1131,7 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
     };
     auto elem_id = [&](int q, int k) { return q * BLK + ((k / EPV) * 32 + lane) * EPV + (k % EPV); };
 
-    // Preparation of the sampling at row ra (T > 0): every block's draw and bound
-    // into shared memory, and each participating warp's seed score (the best of
-    // its largest element in its block with the largest value) into *thr_slot.
-    // Threads t of nt take part, whole warps; ex is the id left out.
+    // the sampling scratch of row a (block draws and bounds, the list of blocks)
     const int nblk = P.nblk;
     uint8_t* scr = nblk <= kSmemBlkCap ? s_dyn : P.blkws + static_cast<size_t>(b) * nblk * kBlkScratchBytes;
     float* s_bnd = reinterpret_cast<float*>(scr);
@@ -1048,66 +1139,6 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
     int* s_I = reinterpret_cast<int*>(s_M + nblk);
     int* s_list = s_I + nblk;
     uint4* stg = reinterpret_cast<uint4*>(s_dyn + k2_blk_bytes(nblk)) + warp * (kBatch * 32 * VPL);
-    auto prepare = [&](int ra, int ex, int t, int nt, unsigned* thr_slot) {
-        const float* bmx = P.bmax + static_cast<size_t>(b * K1 + ra) * nblk;
-        const char* rowp = rowp_of(b * K1 + ra);
-        const RowPhilox rpr = row_philox(nk, static_cast<uint32_t>(ra));
-        // each warp's seed: its block with the largest value (the blocks' maxima are
-        // loaded first); the seed block's load is issued before the block draws, so
-        // its latency overlaps them
-        float lb = -INFINITY;
-        int lq = -1;
-        for (int q = t; q < nblk; q += nt) {
-            const float zq = bmx[q];
-            if (zq > lb) { lb = zq; lq = q; }
-        }
-        const unsigned kq = warp_best_key(lb);
-        const unsigned own = __ballot_sync(0xffffffffu, kq != 0u && lb > -INFINITY && score_key(lb) == kq);
-        const int qs = own ? __shfl_sync(0xffffffffu, lq, __ffs(own) - 1) : -1;
-        uint4 rs[VPL];
-        if (qs >= 0) load_block(rowp, qs, rs);
-        // block draws and bounds
-        for (int q0 = t; q0 < nblk; q0 += 4 * nt) {
-            float zq[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) zq[i] = q0 + i * nt < nblk ? bmx[q0 + i * nt] : -INFINITY;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int q = q0 + i * nt;
-                if (q >= nblk) break;
-                const BlockNoise bn = block_noise(nk, static_cast<uint32_t>(q), static_cast<uint32_t>(ra));
-                s_bnd[q] = block_zmax<SOFTCAP, PENALTY>(zq[i], P) * P.invT - bn.lnM;
-                s_M[q] = bn.M;
-                s_I[q] = bn.I;
-            }
-        }
-        // seed: each lane scores its largest element of the warp's seed block (the
-        // seed block's draw is the same function of (row, block) as above)
-        {
-            float sc = -INFINITY;
-            if (qs >= 0) {
-                float xb = -INFINITY;
-                int vb = -1;
-#pragma unroll
-                for (int u = 0; u < VPL; ++u) {
-                    float x[EPV];
-                    unpack<BF16>(rs[u], x);
-#pragma unroll
-                    for (int e = 0; e < EPV; ++e) {
-                        const int v = elem_id(qs, u * EPV + e);
-                        if (v < P.V && v != ex && (vb < 0 || x[e] > xb)) { xb = x[e]; vb = v; }
-                    }
-                }
-                if (vb >= 0) {
-                    const BlockNoise bn = block_noise(nk, static_cast<uint32_t>(qs), static_cast<uint32_t>(ra));
-                    const float zb = transform_f32<SOFTCAP, PENALTY>(xb, PENALTY && pen_of(vb, ra), P) * P.invT;
-                    sc = zb - ln_fast(noise_exp_f32(rpr, bn.M, bn.I, static_cast<uint32_t>(vb)));
-                }
-            }
-            const unsigned kw = warp_best_key(sc);
-            if (kw != 0u && lane == 0) atomicMax(thr_slot, kw);
-        }
-    };
     // Row 0 is sampled by this kernel whenever a = 0 and no residual pass takes it
     // (point-mass drafts, or no draft at all): the warps without an accept test
     // prepare it meanwhile, which takes its preparation off the critical path
@@ -1224,8 +1255,6 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
             if (lane == 0) {
                 if (!(Sf > 0.0f && Sf < INFINITY && mf < INFINITY)) raise_status(P.status, SPECNG_DEV_NONFINITE);
                 const float lsef = mf * P.invT + logf(Sf);
-                // the log-sum-exp in fp64 (the oracle's precision), only where it is used
-                auto lse64 = [&]() { return static_cast<double>(mf) / P.Td + log(static_cast<double>(Sf)); };
                 int accepted = 0;
                 if (dv) {
                     const double qd = static_cast<double>(qdf);
@@ -1236,8 +1265,7 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
                     } else if (lr > lp + 1e-4f * (1.0f + fabsf(lp))) {
                         accepted = 0;
                     } else {
-                        const double zd = transform_f64<SOFTCAP, PENALTY>(static_cast<double>(xd), pend, P);
-                        accepted = u * qd <= exp(zd / P.Td - lse64());
+                        accepted = accept_f64<SOFTCAP, PENALTY>(P, xd, pend, u, qd, mf, Sf);
                     }
                 }
                 s_acc[j] = accepted;
@@ -1247,7 +1275,9 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
     }
     if constexpr (!GREEDY) {
         if (spec0 && warp >= keff)
-            prepare(0, keff > 0 && s_d[0] >= 0 && s_d[0] < P.V ? s_d[0] : -1, tid - 32 * keff, kST - 32 * keff, &s_thr0);
+            prepare_row<BF16, SOFTCAP, PENALTY>(P, nk, b, 0, keff > 0 && s_d[0] >= 0 && s_d[0] < P.V ? s_d[0] : -1,
+                                                tid - 32 * keff, kST - 32 * keff, &s_thr0, s_bnd, s_M, s_I, s_pkey, s_ppos,
+                                                s_d, nh);
     }
     __syncthreads();
 
@@ -1273,7 +1303,8 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
         if (a == 0 && spec0) {
             if (tid == 0) s_thr = s_thr0;  // row 0 was prepared during the accept tests
         } else {
-            prepare(a, excl, tid, kST, &s_thr);
+            prepare_row<BF16, SOFTCAP, PENALTY>(P, nk, b, a, excl, tid, kST, &s_thr, s_bnd, s_M, s_I, s_pkey, s_ppos, s_d,
+                                                nh);
         }
         __syncthreads();
         float thr = -INFINITY;
