@@ -32,6 +32,11 @@
  *  - No kernel waits for another block: cross-block merges use a
  *    fence + atomic ticket, and the last block to arrive does the merge.
  *    Every hash probe loop is bounded by the table capacity.
+ *  - The kernels of spec_verify, spec_append and spec_commit are launched
+ *    with programmatic stream serialisation: each may start before the
+ *    previous kernel on the stream has finished and waits (griddepcontrol)
+ *    before it reads anything that kernel may have written, so stream
+ *    order is kept for every caller.
  */
 #ifndef SPECNG_H
 #define SPECNG_H
@@ -156,7 +161,8 @@ typedef struct {
 size_t spec_verify_workspace_bytes(int B, int K, int V);
 
 /* Zero a workspace (stream-ordered).  A workspace must be zero-filled once
- * before its first spec_verify call; each call leaves it zero-filled. */
+ * before its first spec_verify call; each call leaves it ready for the next
+ * (see spec_verify's workspace argument). */
 int spec_verify_workspace_init(void* workspace, size_t workspace_bytes, cudaStream_t s);
 
 /* One verify call for B sequences with up to K drafts each.
@@ -182,8 +188,10 @@ int spec_verify_workspace_init(void* workspace, size_t workspace_bytes, cudaStre
  * workspace    device scratch of at least spec_verify_workspace_bytes(B, K, V)
  *              bytes, 256-byte aligned, zero-filled before its first use
  *              (spec_verify_workspace_init or any zero fill).  Every call
- *              leaves it zero-filled again, so later calls of any shape that
- *              fits may reuse it; one workspace per call in flight.
+ *              zeroes again the records it reads back (the rest is written
+ *              before it is read), so later calls of any shape that fits may
+ *              reuse it without another fill; one workspace per call in
+ *              flight.
  *
  * Per row: x <- c tanh(x/c) (soft cap), repetition penalty over the window
  * (each distinct id once), temperature; online max and sum of exponentials.
@@ -193,9 +201,14 @@ int spec_verify_workspace_init(void* workspace, size_t workspace_bytes, cudaStre
  * by Gumbel-max with Philox noise keyed by (seed; vocab id, row, step,
  * sequence).  T = 0: accept iff d_i is its row's argmax (lowest id on
  * ties); the emitted token is the argmax of row a.
- * Launches: two kernels (the streaming pass over the rows, then a per-row
- * merge that also runs each sequence's epilogue); three with dense q at
- * T > 0 (a residual pass over row a of the rejected sequences).
+ * Sampling noise: per block of 256 ids a block draw (the block minimum of
+ * the block's Exp(1) variates and its slot), then one draw per id (that
+ * minimum plus an Exp(1)), which leaves the variates i.i.d. Exp(1) and lets
+ * whole blocks be ruled out by the bound z_max / T - ln(minimum).
+ * Launches: two kernels (the streaming pass over the rows: block maxima and
+ * the sums of exponentials; then one CTA per sequence: accept tests,
+ * sample, epilogue); three with dense q at T > 0 (a residual pass over row a
+ * of the rejected sequences).
  * Requirements: logits 16-byte aligned for the vectorised path (any
  * alignment works, slower); B in [1, 2^20]; K in [0, 16]; V in [1, 2^30].
  * Errors: EINVAL, ESMALL, ECUDA.  Device: NONFINITE, TOKEN_OOR, BAD_K. */
