@@ -1799,6 +1799,14 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const __gr
 
 // ---------------------------------------------------------------- launch
 
+// Per-device flag for a one-time function attribute (the attribute belongs to
+// the device's context, so each device needs its own call).
+__host__ inline bool* attr_flag(bool* flags) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) dev = 0;
+    return &flags[dev];
+}
+
 __host__ inline int sm_count_cached() {
     static int cached[128] = {};
     int dev = 0;
@@ -1815,12 +1823,13 @@ template <bool BF16, bool G, bool C, bool R>
 cudaError_t launch_stream(const VerifyDev& P, cudaStream_t s) {
     // one persistent CTA per SM; the staging ring lives in dynamic shared memory
     constexpr size_t smem = k1_dyn_smem<R>();
-    static bool configured = false;
-    if (!configured) {
+    static bool configured[128] = {};
+    bool* done = attr_flag(configured);
+    if (!*done) {
         const cudaError_t e = cudaFuncSetAttribute(verify_stream_kernel<BF16, G, C, R>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        configured = true;
+        *done = true;
     }
     return launch_chained(verify_stream_kernel<BF16, G, C, R>, dim3(kK1PerSM * sm_count_cached()), dim3(kPThreads), smem, s,
                           P);
@@ -1828,15 +1837,16 @@ cudaError_t launch_stream(const VerifyDev& P, cudaStream_t s) {
 
 template <bool BF16, bool G, bool C, bool R>
 cudaError_t launch_seq(const VerifyDev& P, cudaStream_t s) {
-    // block scratch of the sampled row (when it fits), staging and candidate queues
+    // block scratch of the sampled row (when it fits) and the warps' staging
     const size_t smem = G ? 0 : k2_dyn_smem(P.nblk, BF16);
-    static bool configured = false;
-    if (!G && !configured) {
+    static bool configured[128] = {};
+    bool* done = attr_flag(configured);
+    if (!G && !*done) {
         const cudaError_t e = cudaFuncSetAttribute(verify_seq_kernel<BF16, G, C, R>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    static_cast<int>(k2_dyn_smem(kSmemBlkCap, BF16)));
         if (e != cudaSuccess) return e;
-        configured = true;
+        *done = true;
     }
     return launch_chained(verify_seq_kernel<BF16, G, C, R>, dim3(static_cast<unsigned>(P.B)), dim3(kST), smem, s, P);
 }
