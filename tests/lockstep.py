@@ -92,7 +92,7 @@ def compare(step, a_g, t_g, kv_gh, ema_gh, res, rep: Report, ids=None):
 
 
 def run_sampled(cfg: wl.Config, steps: int, sample: int, T: float | None = None, device="cuda",
-                seed: int | None = None) -> Report:
+                seed: int | None = None, ema0: float = 1.0) -> Report:
     """Full-size steps on the GPU (the whole batch, in the launch configuration
     the benchmark uses); the oracle checks a seeded sample of ``sample``
     sequences one by one (sequences are independent; their Philox streams are
@@ -107,8 +107,8 @@ def run_sampled(cfg: wl.Config, steps: int, sample: int, T: float | None = None,
     lens_o = lens_full.numpy()[ids].astype(np.int64)
     hist_g = hist_full.to(device)
     lens_g = lens_full.to(device)
-    ema_o = np.ones(len(ids), dtype=np.float64)
-    ema_g = torch.ones(B, dtype=torch.float32, device=device)
+    ema_o = np.full(len(ids), float(np.float32(ema0)), dtype=np.float64)
+    ema_g = torch.full((B,), float(np.float32(ema0)), dtype=torch.float32, device=device)
     kv_g = lens_g.clone()
     use_ngram = not cfg.dense
     table = stats = None
@@ -191,7 +191,7 @@ def run_sampled(cfg: wl.Config, steps: int, sample: int, T: float | None = None,
 
 
 def run(cfg: wl.Config, steps: int, T: float | None = None, device="cuda", seed: int | None = None,
-        oracle_chunk: int = 16) -> Report:
+        oracle_chunk: int = 16, ema0: float = 1.0) -> Report:
     """Run ``steps`` lockstep steps of cfg; raise AssertionError on a parity failure."""
     T = cfg.temperature if T is None else T
     seed = cfg.sampler_seed if seed is None else seed
@@ -202,8 +202,8 @@ def run(cfg: wl.Config, steps: int, T: float | None = None, device="cuda", seed:
     B, K, V = cfg.B, cfg.K, cfg.V
     hist_g = torch.from_numpy(hist_o.astype(np.int32)).to(device)
     lens_g = torch.from_numpy(lens_o.astype(np.int32)).to(device)
-    ema_o = np.ones(B, dtype=np.float64)
-    ema_g = torch.ones(B, dtype=torch.float32, device=device)
+    ema_o = np.full(B, float(np.float32(ema0)), dtype=np.float64)
+    ema_g = torch.full((B,), float(np.float32(ema0)), dtype=torch.float32, device=device)
     kv_o = lens_o.copy()
     kv_g = torch.from_numpy(kv_o.astype(np.int32)).to(device)
     use_ngram = not cfg.dense

@@ -50,6 +50,29 @@ def test_lockstep(name):
         assert rep.accepted > 0
 
 
+# A low starting EMA with the gate off: the EMA update runs from a state far
+# from its fixed point (and, on the boosted workloads c2 and c3, climbs back
+# during the run), and must still match the oracle's step by step.
+LOW_EMA = {
+    "c5_low_ema": (wl.get("c5", B=7, V=V_SMALL, hist_len=(1500, 1500), steps=10), 10, None),
+    "c5_low_ema_penalty_below_one": (wl.get("c5", B=4, V=V_SMALL, hist_len=(1500, 1500), rep_penalty=0.8, steps=6),
+                                     6, None),
+    "c2_low_ema_boost": (wl.get("c2", V=V_SMALL, hist_len=(512, 512), steps=16), 16, 0.6),
+    "c3_low_ema_softcap": (wl.get("c3", B=6, V=V_SMALL, hist_len=(64, 700), gate=False, steps=12), 12, None),
+}
+
+
+@pytest.mark.parametrize("name", list(LOW_EMA))
+def test_lockstep_low_starting_ema(name):
+    cfg, steps, T = LOW_EMA[name]
+    rep = lockstep.run(cfg, steps, T=T, ema0=0.1)
+    assert rep.steps == steps
+    assert rep.excused == 0, rep.notes
+    assert rep.drafted > 0
+    if name.startswith(("c2", "c3")):
+        assert rep.accepted > 0
+
+
 def test_gate_turns_sequences_off():
     cfg = wl.get("c3", B=8, V=8000, hist_len=(64, 400), boost_prob=(0.0, 0.3), steps=20)
     rep = lockstep.run(cfg, 20)
