@@ -267,6 +267,15 @@ int spec_verify_noalloc(const void* logits, int logits_dtype, int B, int K, int 
                         int32_t* kv_len, float* ema,
                         int32_t* out_tokens, int32_t* out_accept_len, cudaStream_t s);
 
+/* Measurement hook; the pages have no counterpart of it.  While
+ * after_stream_kernel is not NULL, every spec_verify call records it on its
+ * stream right after the streaming kernel, so a caller can time that kernel
+ * alone (an event recorded before the call starts the span).  While it is
+ * set, the decision kernel waits for the streaming kernel to finish instead
+ * of starting during its tail.  One process-wide setting, not thread-safe;
+ * NULL turns it off.  Always returns SPECNG_OK. */
+int specng_set_verify_marker(cudaEvent_t after_stream_kernel);
+
 /* Append the emitted tokens: history[b, lens_b + t] = out_tokens[b, t] for
  * t <= out_accept_len[b], then lens_b += out_accept_len[b] + 1.  A sequence
  * whose history would pass hist_cap tokens is left unchanged (HIST_OVERFLOW).

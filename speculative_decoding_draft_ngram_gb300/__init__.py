@@ -17,6 +17,7 @@ from .capi import (  # noqa: F401
     ngram_draft,
     ngram_update,
     philox4x32_10,
+    set_verify_marker,
     spec_append,
     spec_commit,
     spec_verify,

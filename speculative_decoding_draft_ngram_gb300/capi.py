@@ -36,7 +36,7 @@ EXPORTED = (
     "specng_ngram_create", "specng_ngram_destroy", "specng_ngram_reset", "specng_ngram_capacity",
     "ngram_update", "ngram_draft", "spec_verify_workspace_bytes", "spec_verify_workspace_init",
     "spec_verify", "spec_verify_noalloc", "spec_append", "spec_commit", "specng_get_status", "specng_strerror",
-    "specng_last_error", "specng_philox4x32_10",
+    "specng_last_error", "specng_philox4x32_10", "specng_set_verify_marker",
 )
 
 
@@ -111,6 +111,7 @@ def load() -> ctypes.CDLL:
         "spec_append": (I, [P, I64, P, I64, P, P, I, I, P]),
         "spec_commit": (I, [P, P, I64, P, I64, P, P, I, I, I, P, P, P, P, P]),
         "specng_get_status": (I, [ctypes.POINTER(ctypes.c_uint32), I]),
+        "specng_set_verify_marker": (I, [P]),
         "specng_strerror": (ctypes.c_char_p, [I]),
         "specng_last_error": (ctypes.c_char_p, []),
         "specng_philox4x32_10": (I, [P, U64, P, I64, P]),
@@ -307,6 +308,13 @@ def spec_commit(table: NgramTable, history: torch.Tensor, lens: torch.Tensor, ou
 
 
 # ---------------------------------------------------------------- diagnostics
+
+def set_verify_marker(event: Optional["torch.cuda.Event"]):
+    """Record `event` after the streaming kernel of every later spec_verify
+    call (None: stop).  The event must already exist (recorded once)."""
+    h = None if event is None else ctypes.c_void_p(event.cuda_event)
+    _check(load().specng_set_verify_marker(h), "specng_set_verify_marker")
+
 
 def get_status(clear: bool = True) -> int:
     """Device status bits (synchronises the device)."""

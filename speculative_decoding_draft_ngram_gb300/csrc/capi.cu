@@ -121,6 +121,11 @@ const char* specng_strerror(int code) {
     }
 }
 
+int specng_set_verify_marker(cudaEvent_t after_stream_kernel) {
+    verify_marker() = after_stream_kernel;
+    return SPECNG_OK;
+}
+
 int specng_get_status(uint32_t* bits, int clear) {
     if (bits == nullptr) return fail(SPECNG_EINVAL, "specng_get_status: bits is NULL");
     cudaError_t e = cudaDeviceSynchronize();

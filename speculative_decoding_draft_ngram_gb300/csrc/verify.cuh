@@ -1799,6 +1799,16 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const __gr
 
 // ---------------------------------------------------------------- launch
 
+// Event recorded on the stream between the streaming kernel and the decision
+// kernel of every spec_verify call while it is set (a measurement hook: it
+// lets a caller time the streaming kernel alone; the decision kernel then
+// starts after the streaming kernel has finished instead of overlapping its
+// tail).  One process-wide slot.
+__host__ inline cudaEvent_t& verify_marker() {
+    static cudaEvent_t marker = nullptr;
+    return marker;
+}
+
 // Per-device flag for a one-time function attribute (the attribute belongs to
 // the device's context, so each device needs its own call).
 __host__ inline bool* attr_flag(bool* flags) {
@@ -1861,6 +1871,10 @@ template <bool BF16, bool G, bool C, bool R>
 cudaError_t launch_all(const VerifyDev& P, bool dense, cudaStream_t s) {
     cudaError_t e = launch_stream<BF16, G, C, R>(P, s);
     if (e != cudaSuccess) return e;
+    if (cudaEvent_t m = verify_marker()) {
+        e = cudaEventRecord(m, s);  // measurement only: ends the streaming kernel's span
+        if (e != cudaSuccess) return e;
+    }
     e = launch_seq<BF16, G, C, R>(P, s);
     if (e != cudaSuccess || !dense || G) return e;
     return launch_residual<BF16, C, R>(P, s);
