@@ -1143,7 +1143,7 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
     // (point-mass drafts, or no draft at all): the warps without an accept test
     // prepare it meanwhile, which takes its preparation off the critical path
     // when the first draft is rejected.
-    const bool spec0 = !GREEDY && (!dense || keff == 0);
+    const bool spec0 = !GREEDY && (!dense || keff == 0) && keff < kSW;  // (needs a warp without a test)
     // ---- 1. accept tests (T > 0) / argmax of every row (T = 0)
     for (int j = warp; j <= keff; j += kSW) {
         const int row = b * K1 + j;

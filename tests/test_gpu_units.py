@@ -325,3 +325,27 @@ def test_all_zero_residual_falls_back_to_p(rep):
     np.testing.assert_array_equal(acc.cpu().numpy(), res["accept_len"])
     np.testing.assert_array_equal(out.cpu().numpy(), res["out_tokens"])
     assert sp.get_status() == 0
+
+
+def test_sixteen_drafts_every_warp_testing():
+    # K = 16: every warp of the decision kernel takes an accept test, none is free
+    # to prepare row 0 early; the row must then be prepared after the tests
+    B, K, V = 3, 16, 5000
+    g = torch.Generator().manual_seed(21)
+    logits = torch.randn(B, K + 1, V, generator=g) * 3
+    drafts = torch.randint(0, V, (B, K), generator=g, dtype=torch.int32)
+    k = torch.full((B,), K, dtype=torch.int32)
+    kw = dict(temperature=0.8, gate_enabled=False, seed=4, step=9)
+    dev = "cuda"
+    kv = torch.full((B,), 100, dtype=torch.int32, device=dev)
+    ema = torch.ones(B, dtype=torch.float32, device=dev)
+    out = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    acc = torch.empty((B,), dtype=torch.int32, device=dev)
+    ws = sp.spec_verify_workspace(B, K, V)
+    sp.spec_verify(logits.cuda(), drafts.cuda(), None, k.cuda(), None, None, sp.VerifyParams(**kw), kv, ema, out,
+                   acc, ws)
+    res = ov.spec_verify(logits.numpy(), drafts.numpy(), None, k.numpy(), np.zeros((B, 1), int), np.zeros(B, int),
+                         ov.VerifyParams(**kw), np.full(B, 100), np.ones(B))
+    np.testing.assert_array_equal(acc.cpu().numpy(), res["accept_len"])
+    np.testing.assert_array_equal(out.cpu().numpy(), res["out_tokens"])
+    assert sp.get_status() == 0
