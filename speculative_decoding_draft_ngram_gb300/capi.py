@@ -253,7 +253,7 @@ def spec_verify_noalloc(logits: torch.Tensor, drafts: Optional[torch.Tensor], dr
     """spec_verify on the library's static scratch (no workspace, nothing allocated).
 
     For callers that cannot allocate device memory where they verify; shapes
-    are limited to spec_verify_workspace_bytes(B, K, V) <= 4 MiB, and calls
+    are limited to spec_verify_workspace_bytes(B, K, V) <= 16 MiB, and calls
     on one device must not overlap (they share the scratch)."""
     if logits.dim() != 3:
         raise SpecngError("logits must be [B, K+1, V]")
