@@ -44,7 +44,6 @@ DESCR = {
     "c5": "large batch: B=256 V=151936 k_b~U{0..4} bf16 N(0,1)*4 logits, repetition penalty 1.1 over the last "
           "64 tokens, T=0.6, histories 32768 Zipf(1.05) with 64-token copied spans, n-gram update each step",
 }
-VERIFY_SRC = os.path.join(ROOT, "speculative_decoding_draft_ngram_gb300", "csrc", "verify.cuh")
 
 
 def parse():

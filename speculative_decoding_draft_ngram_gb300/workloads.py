@@ -26,7 +26,7 @@ statement; the readings taken where it is open are listed in the design doc.
 """
 from __future__ import annotations
 
-from dataclasses import dataclass, field, replace
+from dataclasses import dataclass, replace
 from typing import Optional, Tuple
 
 import numpy as np

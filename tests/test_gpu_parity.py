@@ -1,9 +1,9 @@
 """GPU parity of the whole hot path (draft -> verify -> append -> update)
 against the fp64 oracle, in lockstep, on every workload at sizes the oracle
-finishes in seconds.  V = 40000 spans three bf16 chunks (five fp32 chunks)
-with a ragged tail; V = 40001 takes the unaligned (scalar-load) path."""
+finishes in seconds.  V = 40000 spans two 64 KB chunks of the streaming
+pass in bf16 (three in fp32) with a ragged tail, and 157 noise blocks;
+V = 40001 takes the unaligned (scalar-load) path."""
 import pytest
-import torch
 
 from speculative_decoding_draft_ngram_gb300 import workloads as wl
 
