@@ -55,6 +55,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sub", action="store_true", help="skip the other workloads' verify timings")
     ap.add_argument("--cpu-sample", type=int, default=0, help="sequences in the oracle sample (0: auto)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (smaller profiler captures only)")
@@ -267,7 +268,8 @@ class Path:
             drafts, k, q = self.dsets[i], self.kfull, self.q[i]
         saved = None
         if cfg.boost is not None:
-            # target-model stand-in: it agrees with a draft w.p. rho_b
+            # target-model stand-in (not the library's work): it agrees with a draft
+            # w.p. rho_b; it runs before the step's library events
             saved = self._boost(logits, drafts, k, rowmax)
         self.params.step = s
         if ev is not None:
@@ -276,14 +278,16 @@ class Path:
                        self.acc, self.ws)
         if ev is not None:
             ev[1].record()
-        if saved is not None:
-            logits.view(-1)[saved[0]] = saved[1]
         if self.ngram:
             lim, fb = self._limits(s + 1)
             sp.spec_commit(self.table, self.hist, self.lens, self.out, self.acc, cfg.K, k_limit=lim, fallback=fb,
                            out_drafts=self.drafts, out_k=self.kbuf[s + 1])
         else:
             sp.spec_append(self.hist, self.lens, self.out, self.acc)
+        if ev is not None:
+            ev[2].record()
+        if saved is not None:
+            logits.view(-1)[saved[0]] = saved[1]
 
     def _boost(self, logits, drafts, k, rowmax=None):
         B, K1, V = logits.shape
@@ -375,6 +379,57 @@ class Path:
         return steps * cfg.B * (cfg.K + 1)
 
 
+def verify_summary(path, peak, calls=60):
+    """spec_verify alone on the workload's current state: the whole call and its
+    streaming kernel against the HBM roofline (see Path.time_verify)."""
+    cfg = path.cfg
+    v_avg_s, v_rows, k1_s = path.time_verify(calls)
+    elem = 2 if cfg.dtype == "bf16" else 4
+    call_bytes = v_rows * cfg.V * elem + cfg.B * 4 * (2 * cfg.K + 8)
+    k1_bytes = v_rows * cfg.V * elem
+    return {
+        "verify_us": v_avg_s * 1e6,
+        "rows_read_per_call": v_rows,
+        "rows_read_per_s": v_rows / v_avg_s,
+        "nominal_rows_per_s": cfg.B * (cfg.K + 1) / v_avg_s,
+        "verify_logits_gbs": call_bytes / v_avg_s / 1e9,
+        "verify_call_frac": call_bytes / v_avg_s / 1e9 / peak,
+        "stream_kernel_us": k1_s * 1e6,
+        "stream_kernel_frac": k1_bytes / k1_s / 1e9 / peak,
+    }
+
+
+# Workloads measured beside the headline (spec_verify alone, same process):
+# name -> (workload, what is timed, steps run first, gate forced open)
+SUB_WORKLOADS = {
+    "c3_gate_open": ("c3", "c3 with every sequence verifying its k drafts (gate forced open for the timing): the "
+                           "soft-capped accept rows at V=262144", 8, True),
+    "c3_steady": ("c3", "c3 after 150 steps of the whole path with the EMA gate (tau 0.1, thr 0.5) as configured",
+                  150, False),
+    "c4": ("c4", "c4 dense q: accept rows, decision and the residual pass", 8, False),
+    "c2": ("c2", "c2 latency case (B=1), T=0.6", 8, False),
+}
+
+
+def measure_sub_workloads(dev, peak, names):
+    out = {}
+    for name in names:
+        wname, what, warm, gate_open = SUB_WORKLOADS[name]
+        path = Path(wname, warm + 2 * 70 + 16, dev)
+        path.first_drafts(0)
+        for s in range(warm):
+            path.step(s, path.logits[s % path.n_sets], rowmax=path.rowmax[s % path.n_sets])
+        torch.cuda.synchronize()
+        if gate_open:
+            path.params.gate_enabled = False
+        d = {"what": what, "B": path.cfg.B, "V": path.cfg.V, "K": path.cfg.K}
+        d.update(verify_summary(path, peak))
+        out[name] = d
+        del path
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     ws, rank, local = dist_env()
     if ws > 1:
@@ -395,7 +450,7 @@ def run_ours(args):
     for s in range(args.warmup):
         path.step(s, path.logits[s % path.n_sets], rowmax=path.rowmax[s % path.n_sets])
     torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     clocks = Clocks(dev) if rank == 0 else None
@@ -419,7 +474,8 @@ def run_ours(args):
         torch.distributed.barrier()
     clk = clocks.stop((wall0, wall1)) if clocks else None
     ms = t_start.elapsed_time(t_end)
-    verify_ms = [a.elapsed_time(b) for a, b in evs]
+    verify_ms = [a.elapsed_time(b) for a, b, _ in evs]
+    library_ms = [a.elapsed_time(c) for a, _, c in evs]   # spec_verify + spec_commit / spec_append
     # rows of the timed steps only
     rows_read = path.rows_read(base + args.steps) - path.rows_read(base)
     rows_nominal = args.steps * cfg.B * (cfg.K + 1)
@@ -450,6 +506,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         ems = max_over_ranks(e0.elapsed_time(e1), dev)
         e2e = {"value": ws * e2e_steps * cfg.B * (cfg.K + 1) / (ems / 1e3), "unit": UNIT,
+               "bound": "the host-to-device copy of each step's whole logit batch [B, K+1, V] from pinned memory",
                "h2d_bytes_per_step": int(dbuf.numel() * dbuf.element_size()),
                "d2h_bytes_per_step": int(out_h.numel() * 4 + acc_h.numel() * 4), "steps": e2e_steps,
                "ms_per_step": ems / e2e_steps}
@@ -468,6 +525,10 @@ def run_ours(args):
     k1_bytes = int(v_rows * cfg.V * elem)                   # the streaming kernel reads each active row once
     k1_achieved = k1_bytes / k1_s / 1e9
     step_verify_us = statistics.mean(verify_ms) * 1e3
+    del path.logits[:]
+    torch.cuda.empty_cache()
+    subs = measure_sub_workloads(dev, peak, [n for n in SUB_WORKLOADS if SUB_WORKLOADS[n][0] != args.workload]
+                                 if not args.no_sub else [])
     traffic = ncu_traffic(args.workload)
     line = {
         "metric": METRIC,
@@ -489,6 +550,7 @@ def run_ours(args):
             "parallelism": f"dp{ws} (independent sequences per GPU)",
         },
         "rows_read_per_s": ws * rows_read / (ms_max / 1e3),
+        "library_ms_per_step": statistics.mean(library_ms),
         "verify_us": v_avg_s * 1e6,
         "verify_us_in_step": step_verify_us,
         "verify_logits_gbs": achieved,
@@ -507,6 +569,7 @@ def run_ours(args):
         },
         "gpu_launches": path.launches_per_step * args.steps,
         "e2e": e2e,
+        "workloads": subs,
         "clocks": clk,
         "device_status": sp.status_names(status),
     }
@@ -522,11 +585,12 @@ def run_ours(args):
 # ---------------------------------------------------------------- oracle arm
 
 class OracleState:
-    """A bounded sample of the workload's sequences, stepped by the oracle."""
+    """A bounded sample of the workload's sequences, stepped by the oracle
+    (worker w draws its own independent sequences: data seed + 7919 w)."""
 
-    def __init__(self, name, nseq):
+    def __init__(self, name, nseq, worker=0):
         cfg = wl.get(name)
-        cfg = wl.get(name, B=nseq, steps=max(cfg.steps, 64))
+        cfg = wl.get(name, B=nseq, steps=max(cfg.steps, 64), data_seed=cfg.data_seed + 7919 * worker)
         self.cfg = cfg
         hist, lens = wl.histories(cfg, "cpu")
         self.hist = hist.numpy().astype(np.int64)
@@ -565,43 +629,87 @@ class OracleState:
         return cfg.B * (cfg.K + 1)
 
 
-AUTO_SAMPLE = {"c2": 1, "c3": 4, "c4": 6, "c5": 8}
+AUTO_SAMPLE = {"c2": 1, "c3": 2, "c4": 3, "c5": 4}   # sequences per worker
 
 
-def cpu_baseline(name, nseq=0, steps=6):
-    """Time the oracle, as it stands, on a bounded sample of the workload."""
-    nseq = nseq or AUTO_SAMPLE[name]
-    st = OracleState(name, nseq)
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def _oracle_worker_init():
+    # one numpy thread per worker: the pool spreads the sequences over the cores
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[v] = "1"
+    torch.set_num_threads(1)
+
+
+def _oracle_worker(task):
+    """One worker's share: its own independent sequences of the workload (its
+    own data seed), stepped by the oracle; returns (rows, seconds)."""
+    name, nseq, steps, worker, warm = task
+    st = OracleState(name, nseq, worker)
+    for s in range(warm):
+        st.step(s)
     t0 = time.perf_counter()
-    rows = sum(st.step(s) for s in range(steps))
-    dt = time.perf_counter() - t0
-    return {"value": rows / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{steps} full steps (n-gram draft from the history, fp64 verify, append) of {nseq} "
-                      f"sequences of workload {name}; {rows} nominal rows in {dt:.1f} s; numpy, one thread"}
+    rows = sum(st.step(warm + s) for s in range(steps))
+    return rows, time.perf_counter() - t0
+
+
+def oracle_parallel(name, nseq_per_worker, steps, warm=0, workers=None):
+    """The oracle, as it stands, on all host cores: one process per core (spawned,
+    so no CUDA state is inherited), each stepping its own sequences.  Returns
+    (rows/s over the parallel region, workers, rows, wall seconds)."""
+    import multiprocessing as mp
+    workers = workers or (os.cpu_count() or 1)
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(workers, initializer=_oracle_worker_init) as pool:
+        pool.map(_noop, range(workers))          # workers up and their imports done
+        t0 = time.perf_counter()
+        res = pool.map(_oracle_worker, [(name, nseq_per_worker, steps, w, warm) for w in range(workers)])
+        wall = time.perf_counter() - t0
+    rows = sum(r for r, _ in res)
+    return rows / wall, workers, rows, wall
+
+
+def _noop(_):
+    return 0
+
+
+def cpu_baseline(name, nseq=0, steps=4):
+    """Time the oracle, as it stands, on a bounded sample of the workload, on every host core."""
+    nseq = nseq or AUTO_SAMPLE[name]
+    v, workers, rows, wall = oracle_parallel(name, nseq, steps)
+    return {"value": v, "unit": UNIT, "cores": workers, "kind": "oracle", "cpu_model": cpu_model(),
+            "nproc": os.cpu_count(),
+            "sample": f"{workers} worker processes (one per host core, one numpy thread each), each stepping "
+                      f"{nseq} independent sequences of workload {name} for {steps} full steps (n-gram draft "
+                      f"from the history, fp64 verify, append); {rows} nominal rows in {wall:.1f} s wall"}
 
 
 def run_reference(args):
     ws, rank, local = dist_env()
     if rank != 0:
         return
-    nseq = args.cpu_sample or 1   # one sequence per step keeps the run within minutes
-    st = OracleState(args.workload, nseq)
-    for s in range(args.warmup):
-        st.step(s)
-    t0 = time.perf_counter()
-    rows = 0
-    for s in range(args.steps):
-        rows += st.step(args.warmup + s)
-    dt = time.perf_counter() - t0
-    v = rows / dt
-    sample = (f"each step: {nseq} sequences of workload {args.workload} (n-gram draft, fp64 verify, append) "
-              f"on the host; {args.steps} timed steps")
+    nseq = args.cpu_sample or 1   # sequences per worker per step: keeps the run within minutes
+    v, workers, rows, wall = oracle_parallel(args.workload, nseq, args.steps, warm=args.warmup)
+    sample = (f"each step: {workers} worker processes (one per host core) x {nseq} sequence(s) of workload "
+              f"{args.workload} (n-gram draft, fp64 verify, append); {args.steps} timed steps after "
+              f"{args.warmup} warm-up steps; {rows} nominal rows in {wall:.1f} s wall")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": wall * 1e3 / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{args.workload}: {DESCR[args.workload]}", "sampled_sequences": nseq},
-        "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "config": {"workload": f"{args.workload}: {DESCR[args.workload]}", "sampled_sequences": nseq * workers},
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": workers, "kind": "oracle", "cpu_model": cpu_model(),
+                         "nproc": os.cpu_count(), "sample": sample},
         "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 

@@ -22,7 +22,10 @@
  *  - Every array argument is caller-owned DEVICE memory unless stated
  *    otherwise; the library never frees it.  int32 arrays are row-major.
  *  - Every call is asynchronous and ordered on the given stream; none of
- *    them synchronises except specng_get_status().
+ *    them synchronises except specng_get_status() and specng_get_counters().
+ *  - The stream must belong to the current device (make the device of the
+ *    arrays current before the call); the verify calls check this and
+ *    return EINVAL otherwise.
  *  - Return value: SPECNG_OK (0), or a negative code for an error found on
  *    the host before anything was enqueued (nothing ran in that case).
  *  - Errors found on the device (full table, out-of-range token, non-finite
@@ -83,6 +86,18 @@ extern "C" {
 #define SPECNG_NGRAM_MAX_POS  16777216  /* positions per sequence in a table (2^24) */
 #define SPECNG_STATIC_SCRATCH_BYTES 16777216 /* scratch of spec_verify_noalloc (16 MiB) */
 
+/* Diagnostic counters (specng_get_counters): how often a rarely taken exact
+ * path ran.  Every decision that floating point takes is screened in fp32
+ * with a margin and re-taken in fp64 inside the margin; these count the
+ * re-takes, so a test can tell that a planted near-tie reached the fp64
+ * code.  They are bumped only inside those cold paths. */
+#define SPECNG_DIAG_ACCEPT_F64    0 /* accept test u q <= p re-taken in fp64              */
+#define SPECNG_DIAG_SAMPLE_F64    1 /* top two Gumbel scores (point mass / bonus) in fp64 */
+#define SPECNG_DIAG_RESIDUAL_F64  2 /* dense-residual decision taken in fp64              */
+#define SPECNG_DIAG_GREEDY_F64    3 /* greedy argmax near-tie re-decided in fp64          */
+#define SPECNG_DIAG_RESIDUAL_ZERO 4 /* all-zero residual: token sampled from p            */
+#define SPECNG_DIAG_N             8
+
 /* ------------------------------------------------------------------------
  * N-gram table  [AX]: "builds bigram/trigram tables at runtime, predicts up
  * to 4 draft tokens per step".
@@ -125,8 +140,8 @@ int specng_ngram_capacity(const specng_ngram* table, int64_t* slots);
  * i >= 2, the trigram pair ((h[i-2], h[i-1]) -> h[i]) are counted, then the
  * contexts' best continuations are refreshed.  Two kernel launches.
  * Device errors: TABLE_FULL, TOKEN_OOR, COUNT_SAT, HIST_SHRANK. */
-int ngram_update(specng_ngram* table, const int32_t* history, int64_t hist_stride,
-                 const int32_t* lens, cudaStream_t s);
+int ngram_update(const int32_t* history, int64_t hist_stride, const int32_t* lens,
+                 specng_ngram* table, cudaStream_t s);
 
 /* Draft up to max_k tokens per sequence by chained lookups: the context is
  * the last two tokens of history ++ drafts so far; the trigram context is
@@ -250,8 +265,11 @@ int spec_commit(specng_ngram* table, int32_t* history, int64_t hist_stride, int3
  *   - Limit: spec_verify_workspace_bytes(B, K, V) must not exceed
  *     SPECNG_STATIC_SCRATCH_BYTES (e.g. B = 512, K = 4, V = 262144 fits);
  *     a larger shape returns SPECNG_ESMALL, with the sizes in
- *     specng_last_error(), and nothing is enqueued.  spec_verify with a
- *     caller workspace has no such limit.
+ *     specng_last_error().  spec_verify with a caller workspace has no
+ *     such limit.
+ *   - Every argument check, this one included, runs before anything is
+ *     enqueued: a call that returns an error has enqueued nothing and has
+ *     not touched the scratch.
  *   - Each call first zero-fills the part of the scratch it uses
  *     (cudaMemsetAsync on s), then enqueues the verify kernels on s.
  *   - The first call on a device looks the scratch address up
@@ -291,6 +309,13 @@ int spec_append(int32_t* history, int64_t hist_stride, int32_t* lens, int64_t hi
 /* Copy the current device's status bits to *bits (host pointer);
  * if clear != 0, reset them to 0.  Synchronises the device. */
 int specng_get_status(uint32_t* bits, int clear);
+
+/* Copy the current device's first n diagnostic counters (SPECNG_DIAG_*) to
+ * counts (host array of n); if clear != 0, reset all of them to 0.  n in
+ * [0, SPECNG_DIAG_N].  Synchronises the device.  The pages have no
+ * counterpart of this call: it exists so that tests can show which exact
+ * path a decision took. */
+int specng_get_counters(uint32_t* counts, int n, int clear);
 
 /* Static description of a return code. */
 const char* specng_strerror(int code);

@@ -29,7 +29,7 @@ What one call computes, for every sequence b of a batch (rows j = 0..K of
    accept_len = a; kv_len <- kv_len - k + a; if k_eff > 0,
    ema <- (1 - tau) * ema + tau * a / k_eff.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent (the same readings hold in the GPU library):
 * processors apply in the order soft cap -> penalty -> temperature;
 * the penalty divides positive logits by r and multiplies negative ones by
   r, once per distinct id, over the last ``rep_window`` tokens of

@@ -11,6 +11,7 @@ from .capi import (  # noqa: F401
     NgramTable,
     SpecngError,
     VerifyParams,
+    get_counters,
     get_status,
     lib_path,
     load,

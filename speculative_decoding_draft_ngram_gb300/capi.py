@@ -36,8 +36,12 @@ EXPORTED = (
     "specng_ngram_create", "specng_ngram_destroy", "specng_ngram_reset", "specng_ngram_capacity",
     "ngram_update", "ngram_draft", "spec_verify_workspace_bytes", "spec_verify_workspace_init",
     "spec_verify", "spec_verify_noalloc", "spec_append", "spec_commit", "specng_get_status", "specng_strerror",
-    "specng_last_error", "specng_philox4x32_10", "specng_set_verify_marker",
+    "specng_last_error", "specng_philox4x32_10", "specng_set_verify_marker", "specng_get_counters",
 )
+
+# Diagnostic counters (SPECNG_DIAG_*): runs of the exact (fp64) paths.
+DIAG = {"accept_f64": 0, "sample_f64": 1, "residual_f64": 2, "greedy_f64": 3, "residual_zero": 4}
+DIAG_N = 8
 
 
 class SpecngError(RuntimeError):
@@ -100,7 +104,7 @@ def load() -> ctypes.CDLL:
         "specng_ngram_destroy": (I, [P]),
         "specng_ngram_reset": (I, [P, P]),
         "specng_ngram_capacity": (I, [P, ctypes.POINTER(I64)]),
-        "ngram_update": (I, [P, P, I64, P, P]),
+        "ngram_update": (I, [P, I64, P, P, P]),
         "ngram_draft": (I, [P, P, I64, P, I, P, P, P, P, P]),
         "spec_verify_workspace_bytes": (SZ, [I, I, I]),
         "spec_verify_workspace_init": (I, [P, SZ, P]),
@@ -111,6 +115,7 @@ def load() -> ctypes.CDLL:
         "spec_append": (I, [P, I64, P, I64, P, P, I, I, P]),
         "spec_commit": (I, [P, P, I64, P, I64, P, P, I, I, I, P, P, P, P, P]),
         "specng_get_status": (I, [ctypes.POINTER(ctypes.c_uint32), I]),
+        "specng_get_counters": (I, [ctypes.POINTER(ctypes.c_uint32), I, I]),
         "specng_set_verify_marker": (I, [P]),
         "specng_strerror": (ctypes.c_char_p, [I]),
         "specng_last_error": (ctypes.c_char_p, []),
@@ -185,8 +190,10 @@ class NgramTable:
 
 def ngram_update(table: NgramTable, history: torch.Tensor, lens: torch.Tensor):
     """Index positions [indexed_b, lens_b) of every sequence (two kernels)."""
-    _check(load().ngram_update(table._h, _ptr(history, torch.int32, "history"), history.shape[1],
-                               _ptr(lens, torch.int32, "lens"), _stream(history.device)), "ngram_update")
+    with torch.cuda.device(history.device):
+        _check(load().ngram_update(_ptr(history, torch.int32, "history"), history.shape[1],
+                                   _ptr(lens, torch.int32, "lens"), table._h, _stream(history.device)),
+               "ngram_update")
 
 
 def ngram_draft(table: NgramTable, history: torch.Tensor, lens: torch.Tensor, max_k: int,
@@ -200,11 +207,12 @@ def ngram_draft(table: NgramTable, history: torch.Tensor, lens: torch.Tensor, ma
         out_drafts = torch.empty((B, max_k), dtype=torch.int32, device=history.device)
     if out_k is None:
         out_k = torch.empty((B,), dtype=torch.int32, device=history.device)
-    _check(load().ngram_draft(table._h, _ptr(history, torch.int32, "history"), history.shape[1],
-                              _ptr(lens, torch.int32, "lens"), int(max_k),
-                              _ptr(k_limit, torch.int32, "k_limit"), _ptr(fallback, torch.int32, "fallback"),
-                              _ptr(out_drafts, torch.int32, "out_drafts"),
-                              _ptr(out_k, torch.int32, "out_k"), _stream(history.device)), "ngram_draft")
+    with torch.cuda.device(history.device):
+        _check(load().ngram_draft(table._h, _ptr(history, torch.int32, "history"), history.shape[1],
+                                  _ptr(lens, torch.int32, "lens"), int(max_k),
+                                  _ptr(k_limit, torch.int32, "k_limit"), _ptr(fallback, torch.int32, "fallback"),
+                                  _ptr(out_drafts, torch.int32, "out_drafts"),
+                                  _ptr(out_k, torch.int32, "out_k"), _stream(history.device)), "ngram_draft")
     return out_drafts, out_k
 
 
@@ -235,15 +243,16 @@ def spec_verify(logits: torch.Tensor, drafts: Optional[torch.Tensor], draft_prob
     else:
         raise SpecngError(f"logits dtype {logits.dtype} unsupported (bfloat16 or float32)")
     pc = params.to_c()
-    _check(load().spec_verify(
-        _ptr(logits, None, "logits"), dt, B, K1 - 1, V,
-        _ptr(drafts, torch.int32, "drafts"), _ptr(draft_probs, torch.float32, "draft_probs"),
-        _ptr(k, torch.int32, "k"), _ptr(history, torch.int32, "history"),
-        history.shape[1] if history is not None else 0, _ptr(lens, torch.int32, "lens"),
-        ctypes.byref(pc), _ptr(kv_len, torch.int32, "kv_len"), _ptr(ema, torch.float32, "ema"),
-        _ptr(out_tokens, torch.int32, "out_tokens"), _ptr(out_accept_len, torch.int32, "out_accept_len"),
-        _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
-        _stream(logits.device)), "spec_verify")
+    with torch.cuda.device(logits.device):   # the library works on the current device
+        _check(load().spec_verify(
+            _ptr(logits, None, "logits"), dt, B, K1 - 1, V,
+            _ptr(drafts, torch.int32, "drafts"), _ptr(draft_probs, torch.float32, "draft_probs"),
+            _ptr(k, torch.int32, "k"), _ptr(history, torch.int32, "history"),
+            history.shape[1] if history is not None else 0, _ptr(lens, torch.int32, "lens"),
+            ctypes.byref(pc), _ptr(kv_len, torch.int32, "kv_len"), _ptr(ema, torch.float32, "ema"),
+            _ptr(out_tokens, torch.int32, "out_tokens"), _ptr(out_accept_len, torch.int32, "out_accept_len"),
+            _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+            _stream(logits.device)), "spec_verify")
 
 
 def spec_verify_noalloc(logits: torch.Tensor, drafts: Optional[torch.Tensor], draft_probs: Optional[torch.Tensor],
@@ -265,14 +274,15 @@ def spec_verify_noalloc(logits: torch.Tensor, drafts: Optional[torch.Tensor], dr
     else:
         raise SpecngError(f"logits dtype {logits.dtype} unsupported (bfloat16 or float32)")
     pc = params.to_c()
-    _check(load().spec_verify_noalloc(
-        _ptr(logits, None, "logits"), dt, B, K1 - 1, V,
-        _ptr(drafts, torch.int32, "drafts"), _ptr(draft_probs, torch.float32, "draft_probs"),
-        _ptr(k, torch.int32, "k"), _ptr(history, torch.int32, "history"),
-        history.shape[1] if history is not None else 0, _ptr(lens, torch.int32, "lens"),
-        ctypes.byref(pc), _ptr(kv_len, torch.int32, "kv_len"), _ptr(ema, torch.float32, "ema"),
-        _ptr(out_tokens, torch.int32, "out_tokens"), _ptr(out_accept_len, torch.int32, "out_accept_len"),
-        _stream(logits.device)), "spec_verify_noalloc")
+    with torch.cuda.device(logits.device):   # the scratch is the current device's
+        _check(load().spec_verify_noalloc(
+            _ptr(logits, None, "logits"), dt, B, K1 - 1, V,
+            _ptr(drafts, torch.int32, "drafts"), _ptr(draft_probs, torch.float32, "draft_probs"),
+            _ptr(k, torch.int32, "k"), _ptr(history, torch.int32, "history"),
+            history.shape[1] if history is not None else 0, _ptr(lens, torch.int32, "lens"),
+            ctypes.byref(pc), _ptr(kv_len, torch.int32, "kv_len"), _ptr(ema, torch.float32, "ema"),
+            _ptr(out_tokens, torch.int32, "out_tokens"), _ptr(out_accept_len, torch.int32, "out_accept_len"),
+            _stream(logits.device)), "spec_verify_noalloc")
 
 
 def spec_append(history: torch.Tensor, lens: torch.Tensor, out_tokens: torch.Tensor,
@@ -280,10 +290,11 @@ def spec_append(history: torch.Tensor, lens: torch.Tensor, out_tokens: torch.Ten
     """history[b, lens_b + t] = out_tokens[b, t] for t <= a_b; lens_b += a_b + 1 (in place)."""
     B, K1 = out_tokens.shape
     cap = history.shape[1] if hist_cap is None else int(hist_cap)
-    _check(load().spec_append(_ptr(history, torch.int32, "history"), history.shape[1],
-                              _ptr(lens, torch.int32, "lens"), cap, _ptr(out_tokens, torch.int32, "out_tokens"),
-                              _ptr(out_accept_len, torch.int32, "out_accept_len"), B, K1 - 1,
-                              _stream(history.device)), "spec_append")
+    with torch.cuda.device(history.device):
+        _check(load().spec_append(_ptr(history, torch.int32, "history"), history.shape[1],
+                                  _ptr(lens, torch.int32, "lens"), cap, _ptr(out_tokens, torch.int32, "out_tokens"),
+                                  _ptr(out_accept_len, torch.int32, "out_accept_len"), B, K1 - 1,
+                                  _stream(history.device)), "spec_append")
 
 
 def spec_commit(table: NgramTable, history: torch.Tensor, lens: torch.Tensor, out_tokens: torch.Tensor,
@@ -298,12 +309,13 @@ def spec_commit(table: NgramTable, history: torch.Tensor, lens: torch.Tensor, ou
     if out_k is None:
         out_k = torch.empty((B,), dtype=torch.int32, device=history.device)
     cap = history.shape[1] if hist_cap is None else int(hist_cap)
-    _check(load().spec_commit(table._h, _ptr(history, torch.int32, "history"), history.shape[1],
-                              _ptr(lens, torch.int32, "lens"), cap, _ptr(out_tokens, torch.int32, "out_tokens"),
-                              _ptr(out_accept_len, torch.int32, "out_accept_len"), B, K1 - 1, int(max_k),
-                              _ptr(k_limit, torch.int32, "k_limit"), _ptr(fallback, torch.int32, "fallback"),
-                              _ptr(out_drafts, torch.int32, "out_drafts"), _ptr(out_k, torch.int32, "out_k"),
-                              _stream(history.device)), "spec_commit")
+    with torch.cuda.device(history.device):
+        _check(load().spec_commit(table._h, _ptr(history, torch.int32, "history"), history.shape[1],
+                                  _ptr(lens, torch.int32, "lens"), cap, _ptr(out_tokens, torch.int32, "out_tokens"),
+                                  _ptr(out_accept_len, torch.int32, "out_accept_len"), B, K1 - 1, int(max_k),
+                                  _ptr(k_limit, torch.int32, "k_limit"), _ptr(fallback, torch.int32, "fallback"),
+                                  _ptr(out_drafts, torch.int32, "out_drafts"), _ptr(out_k, torch.int32, "out_k"),
+                                  _stream(history.device)), "spec_commit")
     return out_drafts, out_k
 
 
@@ -314,6 +326,14 @@ def set_verify_marker(event: Optional["torch.cuda.Event"]):
     call (None: stop).  The event must already exist (recorded once)."""
     h = None if event is None else ctypes.c_void_p(event.cuda_event)
     _check(load().specng_set_verify_marker(h), "specng_set_verify_marker")
+
+
+def get_counters(clear: bool = True) -> dict:
+    """Diagnostic counters of the current device (synchronises): how often each
+    exact (fp64) decision path ran since the last clear (see DIAG)."""
+    v = (ctypes.c_uint32 * DIAG_N)()
+    _check(load().specng_get_counters(v, DIAG_N, 1 if clear else 0), "specng_get_counters")
+    return {name: int(v[i]) for name, i in DIAG.items()}
 
 
 def get_status(clear: bool = True) -> int:

@@ -12,6 +12,9 @@ namespace specng {
 
 __device__ unsigned g_status_word;
 
+// Diagnostic counters of the rarely taken exact paths (SPECNG_DIAG_*).
+__device__ unsigned g_diag_counters[SPECNG_DIAG_N];
+
 // Scratch of spec_verify_noalloc: part of the library's device image, one
 // per device, so that callers without an allocator (see the header) can
 // verify.  Each call zero-fills the part it uses before its kernels run.
@@ -43,6 +46,33 @@ unsigned* status_ptr() {
         if (cudaGetSymbolAddress(&p, g_status_word) == cudaSuccess) ptrs[dev] = static_cast<unsigned*>(p);
     }
     return ptrs[dev];
+}
+
+// Device address of the diagnostic counters, looked up once per device.
+unsigned* diag_ptr() {
+    static std::mutex mu;
+    static unsigned* ptrs[128] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (ptrs[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_diag_counters) == cudaSuccess) ptrs[dev] = static_cast<unsigned*>(p);
+    }
+    return ptrs[dev];
+}
+
+// The stream must belong to the current device: the status word, the
+// counters and the static scratch are looked up on the current device.
+bool stream_on_current_device(cudaStream_t s) {
+    if (s == nullptr) return true;  // the legacy default stream follows the current device
+    int cur = -1, sd = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) return false;
+    if (cudaStreamGetDevice(s, &sd) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return cur == sd;
 }
 
 // Device address of the static verify scratch, looked up once per device
@@ -213,7 +243,7 @@ int specng_ngram_capacity(const specng_ngram* table, int64_t* slots) {
     return SPECNG_OK;
 }
 
-int ngram_update(specng_ngram* table, const int32_t* history, int64_t hist_stride, const int32_t* lens,
+int ngram_update(const int32_t* history, int64_t hist_stride, const int32_t* lens, specng_ngram* table,
                  cudaStream_t s) {
     if (table == nullptr || history == nullptr || lens == nullptr)
         return fail(SPECNG_EINVAL, "ngram_update: NULL argument");
@@ -254,51 +284,57 @@ int spec_verify_workspace_init(void* workspace, size_t workspace_bytes, cudaStre
     return SPECNG_OK;
 }
 
-int spec_verify(const void* logits, int logits_dtype, int B, int K, int V, const int32_t* drafts,
-                const float* draft_probs, const int32_t* k, const int32_t* history, int64_t hist_stride,
-                const int32_t* lens, const specng_verify_params* params, int32_t* kv_len, float* ema,
-                int32_t* out_tokens, int32_t* out_accept_len, void* workspace, size_t workspace_bytes,
-                cudaStream_t s) {
+namespace {
+
+// Host-side checks of a verify call and its kernel parameters, everything
+// but the workspace.  Nothing is enqueued here.
+int verify_setup(const char* who, const void* logits, int logits_dtype, int B, int K, int V, const int32_t* drafts,
+                 const float* draft_probs, const int32_t* k, const int32_t* history, int64_t hist_stride,
+                 const int32_t* lens, const specng_verify_params* params, int32_t* kv_len, float* ema,
+                 int32_t* out_tokens, int32_t* out_accept_len, cudaStream_t s, VerifyDev* out, bool* flags) {
+    char msg[160];
+    auto bad = [&](int code, const char* what) {
+        std::snprintf(msg, sizeof(msg), "%s: %s", who, what);
+        return fail(code, msg);
+    };
     if (logits == nullptr || k == nullptr || params == nullptr || kv_len == nullptr || ema == nullptr ||
-        out_tokens == nullptr || out_accept_len == nullptr || workspace == nullptr)
-        return fail(SPECNG_EINVAL, "spec_verify: NULL argument");
+        out_tokens == nullptr || out_accept_len == nullptr)
+        return bad(SPECNG_EINVAL, "NULL argument");
     if (logits_dtype != SPECNG_BF16 && logits_dtype != SPECNG_F32)
-        return fail(SPECNG_EINVAL, "spec_verify: logits_dtype must be SPECNG_BF16 or SPECNG_F32");
-    if (B < 1 || B > (1 << 20)) return fail(SPECNG_EINVAL, "spec_verify: B outside [1, 2^20]");
-    if (K < 0 || K > SPECNG_MAX_K) return fail(SPECNG_EINVAL, "spec_verify: K outside [0, 16]");
-    if (V < 1 || V > (1 << 30)) return fail(SPECNG_EINVAL, "spec_verify: V outside [1, 2^30]");
-    if (K > 0 && drafts == nullptr) return fail(SPECNG_EINVAL, "spec_verify: drafts is NULL with K > 0");
+        return bad(SPECNG_EINVAL, "logits_dtype must be SPECNG_BF16 or SPECNG_F32");
+    if (B < 1 || B > (1 << 20)) return bad(SPECNG_EINVAL, "B outside [1, 2^20]");
+    if (K < 0 || K > SPECNG_MAX_K) return bad(SPECNG_EINVAL, "K outside [0, 16]");
+    if (V < 1 || V > (1 << 30)) return bad(SPECNG_EINVAL, "V outside [1, 2^30]");
+    if (K > 0 && drafts == nullptr) return bad(SPECNG_EINVAL, "drafts is NULL with K > 0");
     const specng_verify_params& p = *params;
     if (!(p.temperature >= 0.0f) || !std::isfinite(p.temperature))
-        return fail(SPECNG_EINVAL, "spec_verify: temperature must be finite and >= 0");
-    if (!std::isfinite(p.softcap)) return fail(SPECNG_EINVAL, "spec_verify: softcap must be finite");
+        return bad(SPECNG_EINVAL, "temperature must be finite and >= 0");
+    if (!std::isfinite(p.softcap)) return bad(SPECNG_EINVAL, "softcap must be finite");
     if (!(p.rep_penalty > 0.0f) || !std::isfinite(p.rep_penalty))
-        return fail(SPECNG_EINVAL, "spec_verify: rep_penalty must be finite and > 0");
-    if (p.rep_window < 0 || p.rep_window > SPECNG_MAX_REP_WINDOW)
-        return fail(SPECNG_EINVAL, "spec_verify: rep_window outside [0, 256]");
+        return bad(SPECNG_EINVAL, "rep_penalty must be finite and > 0");
+    if (p.rep_window < 0 || p.rep_window > SPECNG_MAX_REP_WINDOW) return bad(SPECNG_EINVAL, "rep_window outside [0, 256]");
     if (p.gate_enabled && (!std::isfinite(p.ema_tau) || !std::isfinite(p.ema_thresh)))
-        return fail(SPECNG_EINVAL, "spec_verify: ema_tau and ema_thresh must be finite");
+        return bad(SPECNG_EINVAL, "ema_tau and ema_thresh must be finite");
     const bool penalty = p.rep_penalty != 1.0f && p.rep_window > 0;
     if (penalty && (history == nullptr || lens == nullptr || hist_stride < 1))
-        return fail(SPECNG_EINVAL, "spec_verify: history, lens and hist_stride are needed for the penalty");
-    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-        return fail(SPECNG_EALIGN, "spec_verify: workspace must be 256-byte aligned");
-    const WsLayout L = ws_layout(B, K, V);
-    if (workspace_bytes < L.total) return fail(SPECNG_ESMALL, "spec_verify: workspace too small");
+        return bad(SPECNG_EINVAL, "history, lens and hist_stride are needed for the penalty");
+    if (!stream_on_current_device(s))
+        return bad(SPECNG_EINVAL, "the stream does not belong to the current device (make its device current)");
     const bool bf16 = logits_dtype == SPECNG_BF16;
     const int chunk = bf16 ? chunk_elems<true>() : chunk_elems<false>();
     const int nchunk = (V + chunk - 1) / chunk;
     const int chunk2 = bf16 ? res_chunk_elems<true>() : res_chunk_elems<false>();
     const int nchunk2 = (V + chunk2 - 1) / chunk2;
     if (static_cast<int64_t>(B) * (K + 1) * nchunk2 > 0x7FFFFFFFLL)
-        return fail(SPECNG_EINVAL, "spec_verify: B * (K + 1) * chunks exceeds the grid limit");
+        return bad(SPECNG_EINVAL, "B * (K + 1) * chunks exceeds the grid limit");
 
     const bool greedy = p.temperature == 0.0f;
     const bool softcap = p.softcap > 0.0f;
     const bool dense = draft_probs != nullptr;
     const int epv = bf16 ? 8 : 4;
 
-    VerifyDev P{};
+    VerifyDev& P = *out;
+    P = VerifyDev{};
     P.logits = logits;
     P.B = B; P.K = K; P.V = V; P.nchunk = nchunk; P.nchunk2 = nchunk2;
     P.nblk = noise_blocks(V);
@@ -322,6 +358,14 @@ int spec_verify(const void* logits, int logits_dtype, int B, int K, int V, const
     P.nk.seq = 0;
     P.aligned = aligned16(logits) && (V % epv == 0) && (!dense || (aligned16(draft_probs) && V % 4 == 0));
     P.kv_len = kv_len; P.ema = ema; P.out_tokens = out_tokens; P.out_accept = out_accept_len;
+    P.status = status_ptr();
+    P.diag = diag_ptr();
+    flags[0] = bf16; flags[1] = greedy; flags[2] = softcap; flags[3] = penalty; flags[4] = dense;
+    return SPECNG_OK;
+}
+
+void attach_workspace(VerifyDev& P, void* workspace) {
+    const WsLayout L = ws_layout(P.B, P.K, P.V);
     char* ws = static_cast<char*>(workspace);
     P.part = reinterpret_cast<SegSum*>(ws + L.part);
     P.bmax = reinterpret_cast<float*>(ws + L.bmax);
@@ -331,20 +375,46 @@ int spec_verify(const void* logits, int logits_dtype, int B, int K, int V, const
     P.part2 = reinterpret_cast<Partial*>(ws + L.part2);
     P.row_thr = reinterpret_cast<unsigned*>(ws + L.row_thr);
     P.seq_ticket2 = reinterpret_cast<unsigned*>(ws + L.seq_ticket2);
-    P.status = status_ptr();
+}
 
-    const cudaError_t e = bf16 ? launch_verify_dtype<true>(P, greedy, softcap, penalty, dense, s)
-                               : launch_verify_dtype<false>(P, greedy, softcap, penalty, dense, s);
-    if (e != cudaSuccess) return fail_cuda(e, "spec_verify");
+int verify_launch(const VerifyDev& P, const bool* f, cudaStream_t s, const char* who) {
+    const cudaError_t e = f[0] ? launch_verify_dtype<true>(P, f[1], f[2], f[3], f[4], s)
+                               : launch_verify_dtype<false>(P, f[1], f[2], f[3], f[4], s);
+    if (e != cudaSuccess) return fail_cuda(e, who);
     return SPECNG_OK;
+}
+
+}  // namespace
+
+int spec_verify(const void* logits, int logits_dtype, int B, int K, int V, const int32_t* drafts,
+                const float* draft_probs, const int32_t* k, const int32_t* history, int64_t hist_stride,
+                const int32_t* lens, const specng_verify_params* params, int32_t* kv_len, float* ema,
+                int32_t* out_tokens, int32_t* out_accept_len, void* workspace, size_t workspace_bytes,
+                cudaStream_t s) {
+    VerifyDev P;
+    bool f[5];
+    int rc = verify_setup("spec_verify", logits, logits_dtype, B, K, V, drafts, draft_probs, k, history, hist_stride,
+                          lens, params, kv_len, ema, out_tokens, out_accept_len, s, &P, f);
+    if (rc != SPECNG_OK) return rc;
+    if (workspace == nullptr) return fail(SPECNG_EINVAL, "spec_verify: workspace is NULL");
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(SPECNG_EALIGN, "spec_verify: workspace must be 256-byte aligned");
+    if (workspace_bytes < ws_layout(B, K, V).total) return fail(SPECNG_ESMALL, "spec_verify: workspace too small");
+    attach_workspace(P, workspace);
+    return verify_launch(P, f, s, "spec_verify");
 }
 
 int spec_verify_noalloc(const void* logits, int logits_dtype, int B, int K, int V, const int32_t* drafts,
                         const float* draft_probs, const int32_t* k, const int32_t* history, int64_t hist_stride,
                         const int32_t* lens, const specng_verify_params* params, int32_t* kv_len, float* ema,
                         int32_t* out_tokens, int32_t* out_accept_len, cudaStream_t s) {
-    const size_t need = spec_verify_workspace_bytes(B, K, V);
-    if (need == 0) return fail(SPECNG_EINVAL, "spec_verify_noalloc: B, K or V out of range");
+    // every check comes before anything is enqueued on s
+    VerifyDev P;
+    bool f[5];
+    int rc = verify_setup("spec_verify_noalloc", logits, logits_dtype, B, K, V, drafts, draft_probs, k, history,
+                          hist_stride, lens, params, kv_len, ema, out_tokens, out_accept_len, s, &P, f);
+    if (rc != SPECNG_OK) return rc;
+    const size_t need = ws_layout(B, K, V).total;
     if (need > static_cast<size_t>(SPECNG_STATIC_SCRATCH_BYTES)) {
         std::snprintf(g_last_error, sizeof(g_last_error),
                       "spec_verify_noalloc: B=%d K=%d V=%d needs %zu bytes of scratch but the static scratch "
@@ -356,8 +426,8 @@ int spec_verify_noalloc(const void* logits, int logits_dtype, int B, int K, int 
     if (scratch == nullptr) return fail(SPECNG_ECUDA, "spec_verify_noalloc: scratch address lookup failed");
     const cudaError_t e = cudaMemsetAsync(scratch, 0, need, s);
     if (e != cudaSuccess) return fail_cuda(e, "spec_verify_noalloc");
-    return spec_verify(logits, logits_dtype, B, K, V, drafts, draft_probs, k, history, hist_stride, lens, params,
-                       kv_len, ema, out_tokens, out_accept_len, scratch, SPECNG_STATIC_SCRATCH_BYTES, s);
+    attach_workspace(P, scratch);
+    return verify_launch(P, f, s, "spec_verify_noalloc");
 }
 
 int spec_append(int32_t* history, int64_t hist_stride, int32_t* lens, int64_t hist_cap, const int32_t* out_tokens,
@@ -391,6 +461,22 @@ int spec_commit(specng_ngram* table, int32_t* history, int64_t hist_stride, int3
                                              out_accept_len, K, max_k, k_limit, fallback, out_drafts, out_k, s);
     if (e != cudaSuccess) return fail_cuda(e, "spec_commit");
     table->parity ^= 1;
+    return SPECNG_OK;
+}
+
+int specng_get_counters(uint32_t* counts, int n, int clear) {
+    if (counts == nullptr || n < 0 || n > SPECNG_DIAG_N) return fail(SPECNG_EINVAL, "specng_get_counters: bad argument");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return fail_cuda(e, "specng_get_counters");
+    unsigned v[SPECNG_DIAG_N] = {};
+    e = cudaMemcpyFromSymbol(v, g_diag_counters, sizeof(v));
+    if (e != cudaSuccess) return fail_cuda(e, "specng_get_counters");
+    for (int i = 0; i < n; ++i) counts[i] = v[i];
+    if (clear) {
+        const unsigned z[SPECNG_DIAG_N] = {};
+        e = cudaMemcpyToSymbol(g_diag_counters, z, sizeof(z));
+        if (e != cudaSuccess) return fail_cuda(e, "specng_get_counters");
+    }
     return SPECNG_OK;
 }
 

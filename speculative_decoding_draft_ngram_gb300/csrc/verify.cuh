@@ -98,7 +98,13 @@ struct VerifyDev {
     Partial* part2;
     unsigned* seq_ticket2;
     unsigned* status;
+    unsigned* diag;           // SPECNG_DIAG_* counters of the exact (fp64) paths
 };
+
+// Count one run of a rarely taken exact path (see SPECNG_DIAG_*).
+__device__ __forceinline__ void count_diag(const VerifyDev& P, int which) {
+    if (P.diag != nullptr) atomicAdd(P.diag + which, 1u);
+}
 // ---------------------------------------------------------------- helpers
 
 template <bool BF16>
@@ -565,6 +571,7 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
         }
         bool ok = true;
         int st = 0;
+        int issued = 0;     // items whose copy was issued (copies complete in issue order per stage)
         unsigned eph = 0u;  // parity of the empty barrier phase to wait for
         for (int n = 0; n < nwork && ok; ++n) {
             const int v0 = c * CHUNK;
@@ -581,6 +588,7 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
                 mbar_add_tx(&s_full[st], static_cast<unsigned>(v1 - v0) * ElemTraits<BF16>::SIZE);
                 bulk_g2s(s_stage + st * SB, src, static_cast<unsigned>(v1 - v0) * ElemTraits<BF16>::SIZE, &s_full[st]);
             }
+            issued = n + 1;
             StageMeta& mt = s_meta[st];
             if (lane == 0) {
                 mt.b = b; mt.j = j; mt.c = c;
@@ -635,10 +643,15 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
                 }
             }
         }
-        // the CTA stays resident until every issued copy has landed
+        // the CTA stays resident until every issued copy has landed: item n of a stage
+        // completes that stage's phase n / kStages, so the last kStages issued items
+        // (one per stage, each its stage's latest phase) are the ones to wait for; a
+        // wait that runs out raises TIMEOUT
         if (P.aligned && lane == 0) {
-            const int lo = nwork > kStages ? nwork - kStages : 0;
-            for (int n = lo; n < nwork; ++n) mbar_wait_bounded(&s_full[n % kStages], static_cast<unsigned>((n / kStages) & 1));
+            const int lo = issued > kStages ? issued - kStages : 0;
+            for (int n = lo; n < issued; ++n)
+                if (!mbar_wait_bounded(&s_full[n % kStages], static_cast<unsigned>((n / kStages) & 1)))
+                    raise_status(P.status, SPECNG_DEV_TIMEOUT);
         }
         return;
     }
@@ -1193,6 +1206,7 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
             int y = t.i1;
             if (t.i2 >= 0 && t.s2 >= t.s1 - cand_delta(t.s1)) {
                 if (lane == 0) {
+                    count_diag(P, SPECNG_DIAG_GREEDY_F64);
                     const double z1 = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, t.i1),
                                                                       PENALTY && pen_of(t.i1, j), P);
                     const double z2 = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, t.i2),
@@ -1265,6 +1279,7 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
                     } else if (lr > lp + 1e-4f * (1.0f + fabsf(lp))) {
                         accepted = 0;
                     } else {
+                        count_diag(P, SPECNG_DIAG_ACCEPT_F64);
                         accepted = accept_f64<SOFTCAP, PENALTY>(P, xd, pend, u, qd, mf, Sf);
                     }
                 }
@@ -1408,9 +1423,11 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
 #pragma unroll
             for (int off = kSW / 2; off > 0; off >>= 1) tw = top2_merge(tw, top2_shfl_xor(tw, off));
             int w = tw.i1;
-            if (lane == 0 && tw.i2 >= 0 && tw.s2 >= tw.s1 - cand_delta(tw.s1))
+            if (lane == 0 && tw.i2 >= 0 && tw.s2 >= tw.s1 - cand_delta(tw.s1)) {
+                count_diag(P, SPECNG_DIAG_SAMPLE_F64);
                 w = rescore_top2_f64<BF16, SOFTCAP, PENALTY>(P, nk, row, a, tw.i1, tw.i2, PENALTY && pen_of(tw.i1, a),
                                                             PENALTY && pen_of(tw.i2, a));
+            }
             if (lane == 0) s_y = w;
         }
         __syncthreads();
@@ -1550,6 +1567,7 @@ __device__ __noinline__ int sample_p_row(const VerifyDev& P, const NoiseKey& nk,
     for (int off = kWarps / 2; off > 0; off >>= 1) tw = top2_merge(tw, top2_shfl_xor(tw, off));
     int w = tw.i1;
     if (tw.i2 >= 0 && tw.s2 >= tw.s1 - cand_delta(tw.s1)) {
+        if (threadIdx.x == 0) count_diag(P, SPECNG_DIAG_SAMPLE_F64);
         double sc[2];
         for (int h = 0; h < 2; ++h) {
             const int id = h == 0 ? tw.i1 : tw.i2;
@@ -1774,6 +1792,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const __gr
             const bool clear2 = t.i2 < 0 || !(t.s2 >= t.s1 - cand_delta(t.s1));
             if (t.i1 >= 0 && clear2 && dres > 1e-4f) winner = t.i1;
             if (winner < 0) {
+            count_diag(P, SPECNG_DIAG_RESIDUAL_F64);
             const double lse = static_cast<double>(rms.x) / P.Td + log(static_cast<double>(rms.y));
             for (int h = 0; h < 2; ++h) {
                 const int id = h == 0 ? t.i1 : t.i2;
@@ -1793,7 +1812,10 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const __gr
     __syncthreads();
     int winner = s_dec;
     // all-zero residual (p <= q everywhere): sample from p at row a with the same noise
-    if (winner < 0) winner = sample_p_row<BF16, SOFTCAP, PENALTY>(P, nk, row, a, s_win, PENALTY ? s_nwin : 0, s_t);
+    if (winner < 0) {
+        if (tid == 0) count_diag(P, SPECNG_DIAG_RESIDUAL_ZERO);
+        winner = sample_p_row<BF16, SOFTCAP, PENALTY>(P, nk, row, a, s_win, PENALTY ? s_nwin : 0, s_t);
+    }
     if (tid == 0) P.out_tokens[static_cast<size_t>(b) * K1 + a] = winner;
 }
 

@@ -2,8 +2,9 @@
 
 Input synthesis only -- no step of the method is computed here.  The tests
 feed the same arrays to the GPU library and to the oracle; the benchmark
-uses the same recipes.  Each config follows one workload of the task
-statement; the readings taken where it is open are listed in the design doc.
+uses the same recipes.  Each config below is one synthetic workload of the
+verify path; where a recipe leaves a detail open (the boosts, the copied
+spans, the draft top-up), the choice is stated beside it.
 
   c1  tiny: B=1, V=32, K=4, fp32 logits N(0,1)*3 fresh per step, T=1, no soft
       cap; history of 256 Zipf(1.1) tokens over 32 ids with one fixed 8-token

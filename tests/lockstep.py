@@ -184,7 +184,8 @@ def run_sampled(cfg: wl.Config, steps: int, sample: int, T: float | None = None,
         rep.steps += 1
     status = sp.get_status(clear=True)
     assert status == 0, f"device status bits set: {sp.status_names(status)}"
-    assert rep.excused <= max(1, EXCUSE_RATE * rep.rows), "\n".join(rep.notes)
+    assert rep.excused <= EXCUSE_RATE * rep.rows, \
+        f"{rep.excused} excused rows out of {rep.rows} exceed 1e-5:\n" + "\n".join(rep.notes)
     if table is not None:
         table.close()
     return rep

@@ -55,7 +55,7 @@ def test_host_argument_checks(lib):
     assert lib.specng_ngram_create(ctypes.byref(t), 0, 10, 100, None) == -1
     assert lib.specng_ngram_create(ctypes.byref(t), 4, 1 << 19, 100, None) == -1
     assert b"V outside" in lib.specng_last_error()
-    assert lib.ngram_update(None, None, 8, None, None) == -1
+    assert lib.ngram_update(None, 8, None, None, None) == -1
     assert lib.ngram_draft(None, None, 8, None, 4, None, None, None, None, None) == -1
     p = capi.VerifyParams(temperature=-1.0).to_c()
     fake = ctypes.c_void_p(0x1000)

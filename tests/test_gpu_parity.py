@@ -23,6 +23,8 @@ CASES = {
     "c3_greedy_softcap": (wl.get("c3", B=4, V=V_SMALL, hist_len=(64, 700), steps=8), 8, 0.0),
     "c4_dense": (wl.get("c4", B=6, V=V_SMALL, steps=10), 10, None),
     "c4_dense_f32": (wl.get("c4", B=3, V=V_SMALL, dtype="f32", steps=6), 6, None),
+    "c4_dense_greedy": (wl.get("c4", B=6, V=V_SMALL, steps=8), 8, 0.0),
+    "c4_dense_greedy_f32": (wl.get("c4", B=3, V=V_SMALL, dtype="f32", steps=5), 5, 0.0),
     "c4_dense_softcap_penalty": (wl.get("c4", B=3, V=V_SMALL, softcap=20.0, rep_penalty=1.3,
                                         rep_window=32, steps=6), 6, None),
     "c5_penalty": (wl.get("c5", B=7, V=V_SMALL, hist_len=(1500, 1500), steps=10), 10, None),
@@ -86,10 +88,12 @@ def test_long_c1_run():
 
 
 FULL = {
-    # the benchmark's workloads at full size; the oracle checks sampled sequences
-    "c5_full": (wl.get("c5"), 2, 8),
-    "c3_full": (wl.get("c3"), 2, 6),
-    "c4_full": (wl.get("c4"), 2, 4),
+    # the benchmark's workloads at full size and launch configuration; the
+    # oracle checks sampled sequences one by one
+    "c5_full": (wl.get("c5"), 10, 8),
+    "c3_full": (wl.get("c3"), 10, 6),
+    "c4_full": (wl.get("c4"), 4, 4),
+    "c4_full_greedy": (wl.get("c4"), 3, 3),
     "c2_full_greedy": (wl.get("c2"), 3, 1),
 }
 
@@ -99,5 +103,5 @@ def test_full_size_sampled(name):
     cfg, steps, sample = FULL[name]
     T = 0.0 if name.endswith("greedy") else None
     rep = lockstep.run_sampled(cfg, steps, sample, T=T)
-    assert rep.steps == steps and rep.excused <= 1
+    assert rep.steps == steps and rep.excused == 0, rep.notes
     assert rep.drafted > 0

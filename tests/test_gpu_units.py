@@ -94,6 +94,27 @@ def test_ngram_fallback_pads_to_the_cap():
     np.testing.assert_array_equal(d.cpu().numpy(), d_o)
 
 
+def test_ngram_fallback_after_a_miss_part_way():
+    # the table indexes the prefix [1, 2, 3] while the history has grown to
+    # [1, 2, 3, 9, 1] (no update since): the chain drafts 2, 3 and then misses,
+    # so positions 2.. of the cap take fallback[b, 2:k_b] (worked by hand in
+    # tests/test_oracle_ngram.py)
+    B, V = 5, 64
+    hist = torch.full((B, 8), -1, dtype=torch.int32)
+    hist[:, :5] = torch.tensor([1, 2, 3, 9, 1], dtype=torch.int32)
+    t = sp.NgramTable(B, V, B * 8)
+    hg = hist.cuda()
+    sp.ngram_update(t, hg, torch.full((B,), 3, dtype=torch.int32, device="cuda"))
+    lens = torch.full((B,), 5, dtype=torch.int32, device="cuda")
+    fb = torch.tensor([[40, 41, 42, 43]] * B, dtype=torch.int32, device="cuda")
+    lim = torch.tensor([4, 3, 2, 1, 0], dtype=torch.int32, device="cuda")
+    d, k = sp.ngram_draft(t, hg, lens, 4, k_limit=lim, fallback=fb)
+    want = [[2, 3, 42, 43], [2, 3, 42, -1], [2, 3, -1, -1], [2, -1, -1, -1], [-1, -1, -1, -1]]
+    assert d.cpu().tolist() == want
+    assert k.cpu().tolist() == [4, 3, 2, 1, 0]
+    assert sp.get_status() == 0
+
+
 def test_ngram_large_vocab_keys():
     # ids near 2^18 exercise every key field
     rng = np.random.default_rng(9)

@@ -92,3 +92,32 @@ def test_draft_batch_limits_and_padding():
     d, n = ngram.draft_batch(h, lens, 4, k_limit=np.array([2, 4]))
     assert list(n) == [2, 4]
     assert list(d[0]) == [1, 0, -1, -1] and list(d[1]) == [3, 3, 3, 3]
+
+
+def test_fallback_fills_the_positions_after_the_first_miss():
+    # With statistics that match the history, a chain either misses at its
+    # first step or never misses (every drafted token occurs before the last
+    # position, so it has a bigram continuation).  A chain that stops part
+    # way needs statistics that lag the history: here they index the prefix
+    # [1, 2, 3] while the history has grown to [1, 2, 3, 9, 1].  Context
+    # (9, 1): no trigram, bigram 1 -> 2; context (1, 2): trigram -> 3;
+    # context (2, 3): no trigram, and 3 was never followed in the indexed
+    # prefix -> miss after two drafts.  The fallback proposals then fill
+    # positions 2.. of the per-sequence length, i.e. fallback[b, 2:k_b].
+    h = np.array([[1, 2, 3, 9, 1, -1, -1, -1]])
+    lens = np.array([5])
+    stats = [ngram.continuation_stats(h[0], 3)]
+    assert ngram.draft(h[0], 5, 4, stats[0]) == [2, 3]
+    fb = np.array([[40, 41, 42, 43]])
+    cases = {4: [2, 3, 42, 43], 3: [2, 3, 42], 2: [2, 3], 1: [2], 0: []}
+    for kb, want in cases.items():
+        d, n = ngram.draft_batch(h, lens, 4, k_limit=np.array([kb]), stats=stats, fallback=fb)
+        assert int(n[0]) == len(want), (kb, d, n)
+        assert list(d[0, :len(want)]) == want and (d[0, len(want):] == -1).all(), (kb, d)
+    # a chain that misses at its first step takes the whole cap from the fallback
+    d, n = ngram.draft_batch(np.array([[7, 8, -1, -1]]), np.array([2]), 4, k_limit=np.array([3]),
+                             fallback=np.array([[50, 51, 52, 53]]))
+    assert list(d[0]) == [50, 51, 52, -1] and int(n[0]) == 3
+    # without a fallback the chain just stops
+    d, n = ngram.draft_batch(h, lens, 4, stats=stats)
+    assert list(d[0]) == [2, 3, -1, -1] and int(n[0]) == 2
