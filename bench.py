@@ -339,7 +339,7 @@ class Path:
         rows = []
         for i in range(3, n):
             keff = k
-            if cfg.gate:
+            if self.params.gate_enabled:
                 keff = torch.where((k > 0) & ~(emas[i] >= self.params.ema_thresh), torch.zeros_like(k), k)
             rows.append(int((keff + 1).sum().item()))
         self.kv.copy_(kv0)

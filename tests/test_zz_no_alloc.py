@@ -93,6 +93,37 @@ def test_noalloc_leaves_free_device_memory_unchanged():
     assert free2 == free1, (free0, free1, free2)
 
 
+@pytest.mark.gpu
+def test_noalloc_near_the_scratch_limit():
+    # B=740, K=4, V=262144 needs over 15.5 MiB of the 16 MiB scratch; the inputs
+    # are made on the device (1.9 GB of bf16 logits), two calls in a row as above
+    B, K, V = 740, 4, 262144
+    need = sp.spec_verify_workspace_bytes(B, K, V)
+    assert 15.5 * 2**20 < need <= 16 << 20
+    dev = "cuda"
+    g = torch.Generator(device=dev).manual_seed(7)
+    logits = (torch.randn((B, K + 1, V), generator=g, device=dev) * 8).to(torch.bfloat16)
+    drafts = torch.randint(0, V, (B, K), generator=g, device=dev, dtype=torch.int32)
+    k = torch.randint(0, K + 1, (B,), generator=g, device=dev, dtype=torch.int32)
+    results = []
+    for fn, ws in ((sp.spec_verify, sp.spec_verify_workspace(B, K, V)), (sp.spec_verify_noalloc, None)):
+        kv = torch.full((B,), 900, dtype=torch.int32, device=dev)
+        ema = torch.full((B,), 0.6, dtype=torch.float32, device=dev)
+        outs = []
+        for step in (1, 2):
+            p = sp.VerifyParams(temperature=1.0, softcap=30.0, gate_enabled=True, seed=3, step=step)
+            out = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+            acc = torch.empty((B,), dtype=torch.int32, device=dev)
+            args = (logits, drafts, None, k, None, None, p, kv, ema, out, acc)
+            fn(*args, ws) if ws is not None else fn(*args)
+            outs.append((out.cpu(), acc.cpu(), kv.cpu(), ema.cpu()))
+        results.append(outs)
+    for a, b in zip(*results):
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)
+    assert sp.get_status() == 0
+
+
 def test_noalloc_rejects_shapes_beyond_the_static_scratch():
     # host-side check, before any CUDA call: runs without a GPU
     from speculative_decoding_draft_ngram_gb300 import build as b
