@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define SPECNG_API_VERSION 1
+#define SPECNG_API_VERSION 2
 
 /* Host-detected return codes. */
 #define SPECNG_OK      0
@@ -170,7 +170,18 @@ typedef struct {
     uint32_t pad_;          /* must be 0                                           */
     uint64_t seed;          /* Philox key                                          */
     uint64_t step;          /* decode step (low 32 bits enter the Philox counter)  */
+    int32_t  early_exit;    /* 1: rows past a sequence's known first rejection are
+                               not read (single-kernel schedule only); the outputs
+                               are the same, since those rows cannot change them   */
+    int32_t  schedule;      /* SPECNG_SCHEDULE_*                                   */
 } specng_verify_params;
+
+/* Kernel schedules of spec_verify (the outputs are the same under each). */
+#define SPECNG_SCHEDULE_AUTO  0  /* FUSED when B <= SPECNG_FUSED_MAX_B, else SPLIT      */
+#define SPECNG_SCHEDULE_FUSED 1  /* one persistent kernel: streaming and the decisions
+                                    of the sequences side by side (B <= 2048)         */
+#define SPECNG_SCHEDULE_SPLIT 2  /* a streaming kernel, then one CTA per sequence      */
+#define SPECNG_FUSED_MAX_B    2048
 
 /* Bytes of device workspace spec_verify needs for (B, K, V). */
 size_t spec_verify_workspace_bytes(int B, int K, int V);

@@ -60,7 +60,12 @@ class VerifyParamsC(ctypes.Structure):
         ("pad_", ctypes.c_uint32),
         ("seed", ctypes.c_uint64),
         ("step", ctypes.c_uint64),
+        ("early_exit", ctypes.c_int32),
+        ("schedule", ctypes.c_int32),
     ]
+
+
+SCHEDULE_AUTO, SCHEDULE_FUSED, SCHEDULE_SPLIT = 0, 1, 2
 
 
 @dataclass
@@ -75,11 +80,14 @@ class VerifyParams:
     gate_enabled: bool = True
     seed: int = 0
     step: int = 0
+    early_exit: bool = False      # skip the rows past a known first rejection (same outputs)
+    schedule: int = SCHEDULE_AUTO
 
     def to_c(self) -> VerifyParamsC:
         return VerifyParamsC(self.temperature, self.softcap, self.rep_penalty, int(self.rep_window),
                              self.ema_tau, self.ema_thresh, 1 if self.gate_enabled else 0, 0,
-                             int(self.seed) & 0xFFFFFFFFFFFFFFFF, int(self.step) & 0xFFFFFFFFFFFFFFFF)
+                             int(self.seed) & 0xFFFFFFFFFFFFFFFF, int(self.step) & 0xFFFFFFFFFFFFFFFF,
+                             1 if self.early_exit else 0, int(self.schedule))
 
 
 _lib = None

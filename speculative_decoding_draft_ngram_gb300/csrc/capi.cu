@@ -3,6 +3,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "ngram.cuh"
@@ -95,6 +96,7 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 struct WsLayout {
     size_t part, bmax, blkws, rowres, seqres, part2, tickets, total;
     size_t row_thr, seq_ticket2;
+    size_t row_tix, seq_state, ema_new, grid_tix;
 };
 
 // The f32 chunks are the smaller ones, so their counts bound both dtypes.
@@ -114,14 +116,28 @@ WsLayout ws_layout(int B, int K, int V) {
     L.rowres = off;  off = align256(off + rows * sizeof(RowRes));
     L.seqres = off;  off = align256(off + static_cast<size_t>(B) * sizeof(SeqRes));
     L.part2 = off;   off = align256(off + static_cast<size_t>(B) * static_cast<size_t>(max_chunks2(V)) * sizeof(Partial));
+    L.row_tix = off;    off = align256(off + rows * sizeof(unsigned long long));
+    L.seq_state = off;  off = align256(off + static_cast<size_t>(B) * sizeof(unsigned long long));
+    L.ema_new = off;    off = align256(off + static_cast<size_t>(B) * sizeof(float));
     L.tickets = off;
     L.row_thr = off;      off += rows * sizeof(unsigned);
     L.seq_ticket2 = off;  off += static_cast<size_t>(B) * sizeof(unsigned);
+    L.grid_tix = off;     off += sizeof(unsigned);
     L.total = align256(off);
     return L;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Tag of one verify call, in [1, 2^31): the single-kernel schedule's tickets
+// and state words carry it, so words left by earlier calls read as empty and
+// nothing needs clearing between calls.
+uint32_t next_epoch() {
+    static std::atomic<uint32_t> counter{0};
+    uint32_t e = 0;
+    while (e == 0) e = (counter.fetch_add(1u) + 1u) & 0x7FFFFFFFu;
+    return e;
+}
 
 }  // namespace
 }  // namespace specng
@@ -315,6 +331,11 @@ int verify_setup(const char* who, const void* logits, int logits_dtype, int B, i
     if (p.rep_window < 0 || p.rep_window > SPECNG_MAX_REP_WINDOW) return bad(SPECNG_EINVAL, "rep_window outside [0, 256]");
     if (p.gate_enabled && (!std::isfinite(p.ema_tau) || !std::isfinite(p.ema_thresh)))
         return bad(SPECNG_EINVAL, "ema_tau and ema_thresh must be finite");
+    if (p.schedule < SPECNG_SCHEDULE_AUTO || p.schedule > SPECNG_SCHEDULE_SPLIT)
+        return bad(SPECNG_EINVAL, "schedule must be SPECNG_SCHEDULE_AUTO, _FUSED or _SPLIT");
+    if (p.schedule == SPECNG_SCHEDULE_FUSED && B > SPECNG_FUSED_MAX_B)
+        return bad(SPECNG_EINVAL, "the single-kernel schedule takes B <= 2048");
+    if (p.early_exit != 0 && p.early_exit != 1) return bad(SPECNG_EINVAL, "early_exit must be 0 or 1");
     const bool penalty = p.rep_penalty != 1.0f && p.rep_window > 0;
     if (penalty && (history == nullptr || lens == nullptr || hist_stride < 1))
         return bad(SPECNG_EINVAL, "history, lens and hist_stride are needed for the penalty");
@@ -360,6 +381,9 @@ int verify_setup(const char* who, const void* logits, int logits_dtype, int B, i
     P.kv_len = kv_len; P.ema = ema; P.out_tokens = out_tokens; P.out_accept = out_accept_len;
     P.status = status_ptr();
     P.diag = diag_ptr();
+    P.fused = (p.schedule == SPECNG_SCHEDULE_FUSED || (p.schedule == SPECNG_SCHEDULE_AUTO && B <= SPECNG_FUSED_MAX_B)) ? 1 : 0;
+    P.early_exit = P.fused ? p.early_exit : 0;
+    P.epoch = next_epoch();
     flags[0] = bf16; flags[1] = greedy; flags[2] = softcap; flags[3] = penalty; flags[4] = dense;
     return SPECNG_OK;
 }
@@ -375,6 +399,10 @@ void attach_workspace(VerifyDev& P, void* workspace) {
     P.part2 = reinterpret_cast<Partial*>(ws + L.part2);
     P.row_thr = reinterpret_cast<unsigned*>(ws + L.row_thr);
     P.seq_ticket2 = reinterpret_cast<unsigned*>(ws + L.seq_ticket2);
+    P.row_tix = reinterpret_cast<unsigned long long*>(ws + L.row_tix);
+    P.seq_state = reinterpret_cast<unsigned long long*>(ws + L.seq_state);
+    P.ema_new = reinterpret_cast<float*>(ws + L.ema_new);
+    P.grid_tix = reinterpret_cast<unsigned*>(ws + L.grid_tix);
 }
 
 int verify_launch(const VerifyDev& P, const bool* f, cudaStream_t s, const char* who) {

@@ -99,6 +99,14 @@ struct VerifyDev {
     unsigned* seq_ticket2;
     unsigned* status;
     unsigned* diag;           // SPECNG_DIAG_* counters of the exact (fp64) paths
+    // single-kernel schedule
+    unsigned long long* row_tix;    // [B (K + 1)] chunks streamed per row: epoch:32 | count:32
+    unsigned long long* seq_state;  // [B] rows done / accepted this call: epoch:31 | bits:33
+    float* ema_new;                 // [B] updated EMA, copied to ema by the grid's last CTA
+    unsigned* grid_tix;             // CTAs finished
+    uint32_t epoch;                 // this call's tag, in [1, 2^31)
+    int early_exit;                 // rows past a known first rejection are not streamed
+    int fused;                      // 1: single-kernel schedule
 };
 
 // Count one run of a rarely taken exact path (see SPECNG_DIAG_*).
@@ -1819,6 +1827,12 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const __gr
     if (tid == 0) P.out_tokens[static_cast<size_t>(b) * K1 + a] = winner;
 }
 
+}  // namespace specng
+
+#include "verify_fused.cuh"
+
+namespace specng {
+
 // ---------------------------------------------------------------- launch
 
 // Event recorded on the stream between the streaming kernel and the decision
@@ -1890,7 +1904,27 @@ cudaError_t launch_residual(const VerifyDev& P, cudaStream_t s) {
 }
 
 template <bool BF16, bool G, bool C, bool R>
+cudaError_t launch_fused(const VerifyDev& P, cudaStream_t s) {
+    constexpr size_t smem = fused_dyn_smem<BF16, R>();
+    static bool configured[128] = {};
+    bool* done = attr_flag(configured);
+    if (!*done) {
+        const cudaError_t e = cudaFuncSetAttribute(verify_fused_kernel<BF16, G, C, R>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        *done = true;
+    }
+    return launch_chained(verify_fused_kernel<BF16, G, C, R>, dim3(sm_count_cached()), dim3(kFThreads), smem, s, P);
+}
+
+template <bool BF16, bool G, bool C, bool R>
 cudaError_t launch_all(const VerifyDev& P, bool dense, cudaStream_t s) {
+    if (P.fused) {
+        cudaError_t e = launch_fused<BF16, G, C, R>(P, s);
+        if (e != cudaSuccess) return e;
+        if (cudaEvent_t m = verify_marker()) e = cudaEventRecord(m, s);  // measurement only: after the one kernel
+        return e;
+    }
     cudaError_t e = launch_stream<BF16, G, C, R>(P, s);
     if (e != cudaSuccess) return e;
     if (cudaEvent_t m = verify_marker()) {

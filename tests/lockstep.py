@@ -47,9 +47,9 @@ def _oracle_params(cfg: wl.Config, T: float, step: int, seed: int) -> ov.VerifyP
                            rep_window=cfg.rep_window, gate_enabled=cfg.gate, seed=seed, step=step)
 
 
-def _gpu_params(cfg: wl.Config, T: float, step: int, seed: int) -> sp.VerifyParams:
+def _gpu_params(cfg: wl.Config, T: float, step: int, seed: int, **sched) -> sp.VerifyParams:
     return sp.VerifyParams(temperature=T, softcap=cfg.softcap, rep_penalty=cfg.rep_penalty,
-                           rep_window=cfg.rep_window, gate_enabled=cfg.gate, seed=seed, step=step)
+                           rep_window=cfg.rep_window, gate_enabled=cfg.gate, seed=seed, step=step, **sched)
 
 
 def oracle_verify(logits, drafts, q, k, hist, lens, params, kv, ema, chunk=16):
@@ -92,7 +92,7 @@ def compare(step, a_g, t_g, kv_gh, ema_gh, res, rep: Report, ids=None):
 
 
 def run_sampled(cfg: wl.Config, steps: int, sample: int, T: float | None = None, device="cuda",
-                seed: int | None = None, ema0: float = 1.0) -> Report:
+                seed: int | None = None, ema0: float = 1.0, **sched) -> Report:
     """Full-size steps on the GPU (the whole batch, in the launch configuration
     the benchmark uses); the oracle checks a seeded sample of ``sample``
     sequences one by one (sequences are independent; their Philox streams are
@@ -143,7 +143,7 @@ def run_sampled(cfg: wl.Config, steps: int, sample: int, T: float | None = None,
         kv_all = lens_g.cpu().numpy().astype(np.int64) + k.numpy()
         kv_g.copy_(torch.from_numpy(kv_all.astype(np.int32)))
         sp.spec_verify(logits.to(device), drafts.to(device), None if q is None else q.to(device), k.to(device),
-                       hist_g, lens_g, _gpu_params(cfg, T, step, seed), kv_g, ema_g, out_tok, out_acc, ws)
+                       hist_g, lens_g, _gpu_params(cfg, T, step, seed, **sched), kv_g, ema_g, out_tok, out_acc, ws)
         res = ov.spec_verify(logits[ids].double().numpy(), drafts.numpy()[ids].astype(np.int64),
                              None if q is None else q[ids].numpy(), k.numpy()[ids].astype(np.int64), hist_o,
                              lens_o, _oracle_params(cfg, T, step, seed), kv_all[ids],
@@ -192,8 +192,9 @@ def run_sampled(cfg: wl.Config, steps: int, sample: int, T: float | None = None,
 
 
 def run(cfg: wl.Config, steps: int, T: float | None = None, device="cuda", seed: int | None = None,
-        oracle_chunk: int = 16, ema0: float = 1.0) -> Report:
-    """Run ``steps`` lockstep steps of cfg; raise AssertionError on a parity failure."""
+        oracle_chunk: int = 16, ema0: float = 1.0, **sched) -> Report:
+    """Run ``steps`` lockstep steps of cfg; raise AssertionError on a parity failure.
+    ``sched``: schedule / early_exit of the GPU calls (the outputs must not depend on them)."""
     T = cfg.temperature if T is None else T
     seed = cfg.sampler_seed if seed is None else seed
     rep = Report()
@@ -250,7 +251,7 @@ def run(cfg: wl.Config, steps: int, T: float | None = None, device="cuda", seed:
                             None if q is None else q.numpy(), k.numpy().astype(np.int64), hist_o, lens_o,
                             _oracle_params(cfg, T, step, seed), kv_o, ema_o.astype(np.float32), oracle_chunk)
         sp.spec_verify(logits.to(device), drafts.to(device), None if q is None else q.to(device), k.to(device),
-                       hist_g, lens_g, _gpu_params(cfg, T, step, seed), kv_g, ema_g, out_tok, out_acc, ws)
+                       hist_g, lens_g, _gpu_params(cfg, T, step, seed, **sched), kv_g, ema_g, out_tok, out_acc, ws)
         a_g = out_acc.cpu().numpy()
         t_g = out_tok.cpu().numpy()
         kv_gh = kv_g.cpu().numpy()

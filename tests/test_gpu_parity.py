@@ -5,6 +5,7 @@ pass in bf16 (three in fp32) with a ragged tail, and 157 noise blocks;
 V = 40001 takes the unaligned (scalar-load) path."""
 import pytest
 
+import speculative_decoding_draft_ngram_gb300 as sp
 from speculative_decoding_draft_ngram_gb300 import workloads as wl
 
 import lockstep
@@ -105,3 +106,38 @@ def test_full_size_sampled(name):
     rep = lockstep.run_sampled(cfg, steps, sample, T=T)
     assert rep.steps == steps and rep.excused == 0, rep.notes
     assert rep.drafted > 0
+
+
+# The same cases under the other kernel schedule and with early exit: the
+# outputs must not depend on either (single kernel = the default for these
+# batch sizes; the two-kernel schedule; the single kernel skipping the rows
+# past a known first rejection).
+SCHEDULES = {
+    "split": dict(schedule=sp.capi.SCHEDULE_SPLIT),
+    "early_exit": dict(schedule=sp.capi.SCHEDULE_FUSED, early_exit=True),
+}
+SCHED_CASES = ["c1", "c2_greedy", "c2_t06", "c3_softcap_gate", "c3_greedy_softcap", "c4_dense", "c4_dense_greedy",
+               "c5_penalty", "c5_f32", "c5_penalty_below_one", "unaligned_v", "tiny_v", "k2_many_seqs",
+               "k0_bonus_only"]
+
+
+@pytest.mark.parametrize("sched", list(SCHEDULES))
+@pytest.mark.parametrize("name", SCHED_CASES)
+def test_lockstep_schedules(name, sched):
+    cfg, steps, T = CASES[name]
+    rep = lockstep.run(cfg, steps, T=T, **SCHEDULES[sched])
+    assert rep.steps == steps and rep.excused == 0, rep.notes
+
+
+def test_lockstep_batch_above_the_single_kernel_limit():
+    # B = 2100 > 2048 takes the two-kernel schedule under the default setting
+    cfg = wl.get("c5", B=2100, K=2, V=1000, hist_len=(200, 200), steps=3)
+    rep = lockstep.run(cfg, 3, oracle_chunk=256)
+    assert rep.steps == 3 and rep.excused == 0
+
+
+@pytest.mark.parametrize("name", ["c5_full", "c3_full"])
+def test_full_size_sampled_early_exit(name):
+    cfg, steps, sample = FULL[name]
+    rep = lockstep.run_sampled(cfg, min(steps, 4), sample, early_exit=True, schedule=sp.capi.SCHEDULE_FUSED)
+    assert rep.excused == 0, rep.notes
