@@ -130,8 +130,9 @@ def test_lockstep_schedules(name, sched):
 
 
 def test_lockstep_batch_above_the_single_kernel_limit():
-    # B = 2100 > 2048 takes the two-kernel schedule under the default setting
-    cfg = wl.get("c5", B=2100, K=2, V=1000, hist_len=(200, 200), steps=3)
+    # B = 2100 > 2048 takes the two-kernel schedule under the default setting (dense
+    # drafts: an n-gram table holds at most 512 sequences)
+    cfg = wl.get("c4", B=2100, K=2, V=1000, steps=3)
     rep = lockstep.run(cfg, 3, oracle_chunk=256)
     assert rep.steps == 3 and rep.excused == 0
 
