@@ -115,6 +115,7 @@ __device__ __forceinline__ unsigned ticket_add(unsigned long long* p, uint32_t e
 
 // Shared state of the decision group.
 struct DShared {
+    double red[kFDWarps];
     Top2 top[kFDWarps];
     unsigned thr;
     int ival[4];
@@ -283,9 +284,9 @@ __device__ __noinline__ int group_argmax(const VerifyDev& P, DShared& S, const i
 // bounds, and reads the passing ones fused_batch at a time (all loads in
 // flight), screening them against one raw-logit threshold per block before
 // the exact per-element score.  Whole group; returns the winner.
-template <bool BF16, bool SOFTCAP, bool PENALTY, bool DENSE>
+template <bool BF16, bool SOFTCAP, bool PENALTY, bool DENSE, bool EXACT = false>
 __device__ __noinline__ int group_sample(const VerifyDev& P, DShared& S, const int* pkey, const int* ppos, uint4* stg_all,
-                                         int b, int a, int ex) {
+                                         int b, int a, int ex, double lse64 = 0.0) {
     constexpr int EPV = ElemTraits<BF16>::EPV;
     constexpr int BLK = 1 << kNoiseBlockShift;
     constexpr int VPL = fused_vpl<BF16>();
@@ -307,8 +308,15 @@ __device__ __noinline__ int group_sample(const VerifyDev& P, DShared& S, const i
     float2 rms = make_float2(0.0f, 0.0f);
     if constexpr (DENSE) {
         rms = __ldcg(reinterpret_cast<const float2*>(&P.rowres[row]));
-        lse_f = rms.x * P.invT + logf(rms.y);
+        lse_f = EXACT ? static_cast<float>(lse64) : rms.x * P.invT + logf(rms.y);
     }
+    // exact residual score of id v in fp64 (the row's exact normaliser), -inf for a zero residual
+    auto exact_residual_score = [&](int v) -> double {
+        const double z = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, v), pen_of(v), P);
+        const double rsd = exp(z / P.Td - lse64) - static_cast<double>(qrow[v]);
+        if (!(rsd > 0.0)) return -INFINITY;
+        return log(rsd) - log(noise_exp_f64(nk, static_cast<uint32_t>(v), static_cast<uint32_t>(a)));
+    };
     // score of element v (raw logit x) with its own draw, or -inf when it cannot win
     auto score_of = [&](int v, float x, float Mq, int Iq, float thr) -> float {
         const float lnMq = ln_fast(Mq);
@@ -316,6 +324,11 @@ __device__ __noinline__ int group_sample(const VerifyDev& P, DShared& S, const i
         if constexpr (DENSE) {
             lw -= lse_f;
             if (lw - lnMq + bound_slack(lw - lnMq) < thr) return -INFINITY;
+            if constexpr (EXACT) {
+                // in fp64 throughout (the fp32 logarithm of a residual near zero is not
+                // accurate enough here); its fp32 rounding only orders the candidates
+                return static_cast<float>(exact_residual_score(v));
+            }
             lw = log_residual(lw, __ldg(qrow + v));
             if (!(lw > -INFINITY)) return -INFINITY;
         }
@@ -461,32 +474,55 @@ __device__ __noinline__ int group_sample(const VerifyDev& P, DShared& S, const i
                 y = rescore_top2_f64<BF16, SOFTCAP, PENALTY>(P, nk, static_cast<int>(row), a, tw.i1, tw.i2, pen_of(tw.i1),
                                                             pen_of(tw.i2));
             }
+        } else if constexpr (EXACT) {
+            // every candidate was scored in fp64: only the order of two scores within
+            // the fp32 rounding of each other is taken again
+            if (close) {
+                const double s1 = exact_residual_score(tw.i1), s2 = exact_residual_score(tw.i2);
+                y = better64(s2, tw.i2, s1, tw.i1) ? tw.i2 : tw.i1;
+            }
         } else if (y >= 0) {
             // fp32 decision when the best is clear of the second and its residual
-            // clearly positive (ln p - ln q > 1e-4); else both re-scored in fp64
+            // clearly positive (ln p - ln q > 1e-4).  Otherwise the residual's sign or
+            // the order of the two may turn on the fp32 normaliser's own error (about
+            // 1e-6), which is amplified by 1 / (1 - q / p) near p = q: the caller
+            // computes the row's exact normaliser and samples again in fp64 (-2)
             const float x1 = static_cast<float>(raw_logit_f64<BF16>(P.logits, row, P.V, tw.i1));
             const float dres = transform_f32<SOFTCAP, PENALTY>(x1, pen_of(tw.i1), P) * P.invT - lse_f - logf(qrow[tw.i1]);
-            if (close || !(dres > 1e-4f)) {
-                count_diag(P, SPECNG_DIAG_RESIDUAL_F64);
-                const double lse = static_cast<double>(rms.x) / P.Td + log(static_cast<double>(rms.y));
-                double best = -INFINITY;
-                int winner = -1;
-                for (int h = 0; h < 2; ++h) {
-                    const int id = h == 0 ? tw.i1 : tw.i2;
-                    if (id < 0 || (h == 1 && !close)) continue;
-                    const double z = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, id), pen_of(id), P);
-                    const double rsd = exp(z / P.Td - lse) - static_cast<double>(qrow[id]);
-                    if (!(rsd > 0.0)) continue;
-                    const double score = log(rsd) - log(noise_exp_f64(nk, static_cast<uint32_t>(id), static_cast<uint32_t>(a)));
-                    if (winner < 0 || better64(score, id, best, winner)) { best = score; winner = id; }
-                }
-                y = winner;
-            }
+            if (close || !(dres > 1e-4f)) y = -2;
+        } else {
+            y = -2;  // no positive residual in fp32: confirmed (or not) with the exact normaliser
         }
         S.ival[0] = y;
     }
     group_sync();
     return S.ival[0];
+}
+
+// The exact normaliser of row a of sequence b in fp64, the oracle's
+// arithmetic: lse = m + ln sum_v exp(z_v / T - m), m = the row's largest
+// transformed value / T (from the fp32 record, any reference works).  Whole
+// group; a slow full pass over the row, taken only for the rare dense
+// residual decisions that the fp32 normaliser cannot settle.
+template <bool BF16, bool SOFTCAP, bool PENALTY>
+__device__ __noinline__ double group_exact_lse(const VerifyDev& P, DShared& S, const int* pkey, const int* ppos, int b,
+                                               int a, double* s_red) {
+    const int gt = threadIdx.x - kFD0 * 32, lane = gt & 31, gw = gt >> 5;
+    const size_t row = static_cast<size_t>(b) * (P.K + 1) + a;
+    const double m = static_cast<double>(__ldcg(&P.rowres[row].m)) / P.Td;
+    double acc = 0.0;
+    for (int v = gt; v < P.V; v += kFDThreads) {
+        const bool pen = PENALTY && pen_lookup(pkey, ppos, S.d, S.nh, P.W, v, a);
+        const double z = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, v), pen, P);
+        acc += exp(z / P.Td - m);
+    }
+    acc = warp_sum_f64(acc);
+    if (lane == 0) s_red[gw] = acc;
+    group_sync();
+    double tot = 0.0;
+    for (int w = 0; w < kFDWarps; ++w) tot += s_red[w];
+    group_sync();
+    return m + log(tot);
 }
 
 // One completed row (b, j): its test or argmax, the sequence's state, and --
@@ -572,6 +608,11 @@ __device__ __noinline__ void group_row_event(const VerifyDev& P, DShared& S, int
         y = __ldcg(&P.rowres[static_cast<size_t>(b) * K1 + a].winner);
     } else if (dense && a < keff && dvalid) {
         y = group_sample<BF16, SOFTCAP, PENALTY, true>(P, S, pkey, ppos, stg, b, a, -1);
+        if (y == -2) {
+            if (gt == 0) count_diag(P, SPECNG_DIAG_RESIDUAL_F64);
+            const double lse64 = group_exact_lse<BF16, SOFTCAP, PENALTY>(P, S, pkey, ppos, b, a, S.red);
+            y = group_sample<BF16, SOFTCAP, PENALTY, true, true>(P, S, pkey, ppos, stg, b, a, -1, lse64);
+        }
         if (y < 0) {
             if (gt == 0) count_diag(P, SPECNG_DIAG_RESIDUAL_ZERO);
             y = group_sample<BF16, SOFTCAP, PENALTY, false>(P, S, pkey, ppos, stg, b, a, -1);
