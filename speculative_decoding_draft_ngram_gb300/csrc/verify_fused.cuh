@@ -448,7 +448,7 @@ __device__ __noinline__ int group_sample(const VerifyDev& P, DShared& S, const i
                 if (v >= P.V || v == ex) continue;
                 const float xv = elem_of_stage<BF16>(stg, ((h * VPL + k / EPV) * 32 + lane) * EPV + k % EPV);
                 const float score = score_of(v, xv, Mh[h], Ih[h], thr);
-                if (score >= thr) {
+                if (score > -INFINITY && score >= thr) {  // -inf: a zero weight never wins
                     top2_push(t, score, v);
                     thr = fmaxf(thr, t.s1 - cand_delta(t.s1));
                 }
