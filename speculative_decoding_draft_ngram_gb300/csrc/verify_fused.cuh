@@ -13,24 +13,24 @@
 //   * warp 16, the producer: walks this CTA's share of the call's row-chunks
 //     and keeps up to kStages of them in flight with cp.async.bulk into a
 //     shared-memory ring (as in the streaming kernel of the two-kernel
-//     schedule).  The row-chunks are ordered row index first -- every active
+//     schedule).  The rows are ordered row index first -- every active
 //     sequence's row 0, then every row 1, ... -- and dealt out round robin
-//     (chunk t to CTA t mod G), so at any moment all CTAs work near the same
-//     point of that order and a sequence's rows complete one after the
-//     other during the call, not all at its end.
-//   * warps 0..15 stream each chunk: the block maxima, and for the rows that
-//     carry an accept test the segment sum of exponentials; every chunk is
-//     its own segment.  The warp that finishes a chunk last posts a note to
-//     the decision group (shared-memory ring).
-//   * warps 17..19, the decision group: for each note it counts the chunk on
-//     its row's ticket (global, tagged with the call's epoch); the CTA whose
-//     count completes a row takes that row's decision: the accept test of
-//     d_{j+1} (T > 0; its normaliser from the row's segment sums) or the
+//     (row t to CTA t mod G), so at any moment all CTAs work near the same
+//     point of that order, a sequence's rows complete one after the other
+//     during the call, and the CTA that streams a row also decides it.
+//   * warps 0..15 stream each chunk: per noise block the bound of its
+//     sampling scores (T > 0; the block draws come from the producer) or its
+//     largest raw logit (T = 0), and for the rows that carry an accept test
+//     the sum of exponentials of the chunk.  The warp that finishes a row's
+//     last chunk hands the row to the decision group (shared-memory ring).
+//   * warps 17..19, the decision group: for each row it streamed, the accept
+//     test of d_{j+1} (T > 0; the normaliser from the chunk sums) or the
 //     row's argmax (T = 0).  The outcome is or-ed into the sequence's state
-//     word; the one update that makes a = (number accepted before the first
-//     rejection) known -- a rejection at row a with rows 0..a-1 accepted, or
-//     all k_eff drafts accepted and row k_eff streamed -- samples the token
-//     at row a and writes the sequence's outputs.
+//     word (global, tagged with the call's epoch); the one update that makes
+//     a = (number accepted before the first rejection) known -- a rejection
+//     at row a with rows 0..a-1 accepted, or all k_eff drafts accepted and
+//     row k_eff streamed -- samples the token at row a (whichever CTA
+//     streamed it) and writes the sequence's outputs.
 //   * early exit (optional): the producer skips the chunks of rows past a
 //     sequence's known first rejection; they cannot change the outputs.
 //   * the last CTA to finish (a grid ticket) writes the EMAs: every CTA
@@ -48,7 +48,7 @@ constexpr int kFD0 = kCWarps + 1;                            // its first warp
 constexpr int kFThreads = (kCWarps + 1 + kFDWarps) * 32;     // 640
 constexpr int kFDThreads = kFDWarps * 32;
 constexpr int kFusedMaxB = 2048;                             // sequences per call on this schedule
-constexpr int kNoteCap = 256;                                // chunk notes in flight per CTA
+constexpr int kNoteCap = 256;                                // streamed rows waiting for the decision group
 constexpr int kStateAcc = SPECNG_MAX_K + 1;                  // accept bits start here
 constexpr int kStateEpoch = 2 * SPECNG_MAX_K + 1;            // epoch bits start here
 constexpr unsigned long long kStateBits = (1ull << kStateEpoch) - 1ull;
@@ -98,21 +98,6 @@ __device__ __forceinline__ unsigned long long state_or(unsigned long long* p, ui
     return ~0ull;
 }
 
-// Count one completed chunk on a row ticket (epoch:32 | count:32); returns
-// the count after this one, 0 when the bounded retry loop gave up.
-__device__ __forceinline__ unsigned ticket_add(unsigned long long* p, uint32_t epoch) {
-    unsigned long long old = __ldcg(p);
-    for (int it = 0; it < (1 << 16); ++it) {
-        const unsigned long long base =
-            static_cast<uint32_t>(old >> 32) == epoch ? old : (static_cast<unsigned long long>(epoch) << 32);
-        const unsigned long long nv = base + 1ull;
-        const unsigned long long prev = atomicCAS(p, old, nv);
-        if (prev == old) return static_cast<unsigned>(nv);
-        old = prev;
-    }
-    return 0u;
-}
-
 // Shared state of the decision group.
 struct DShared {
     double red[kFDWarps];
@@ -127,11 +112,28 @@ struct DShared {
     int bq[kFDWarps][4];
 };
 
-// Drafts of sequence b into S.d and, with the penalty, its history tail into
-// the window table (token -> latest position in the tail).  Whole group.
+// Is v among the last W tokens of history[:L] ++ d_1..d_j (the penalty window
+// of row j of sequence b)?  One whole warp; S.d holds the drafts.
+__device__ __forceinline__ bool warp_window_has(const VerifyDev& P, const DShared& S, int b, int j, int v) {
+    int L = P.lens[b];
+    L = L < 0 ? 0 : (static_cast<int64_t>(L) > P.hist_stride ? static_cast<int>(P.hist_stride) : L);
+    const int nh = L < P.W ? L : P.W;
+    const int total = nh + j;
+    const int cnt = total < P.W ? total : P.W;
+    const int* tail = P.hist + static_cast<size_t>(b) * P.hist_stride + (L - nh);
+    bool f = false;
+    for (int t = (threadIdx.x & 31); t < cnt; t += 32) {
+        const int idx = total - cnt + t;
+        f |= (idx < nh ? tail[idx] : S.d[idx - nh]) == v;
+    }
+    return __any_sync(0xffffffffu, f);
+}
+
+// With the penalty: sequence b's history tail into the window table (token ->
+// latest position in the tail), for the per-element lookups of a sampling or
+// an argmax.  Whole group; S.d holds the drafts.
 template <bool PENALTY>
 __device__ __forceinline__ void group_load_seq(const VerifyDev& P, DShared& S, int* pkey, int* ppos, int b, int gt) {
-    if (gt < P.K) S.d[gt] = P.drafts[static_cast<size_t>(b) * P.K + gt];
     if constexpr (PENALTY) {
         int L = P.lens[b];
         L = L < 0 ? 0 : (static_cast<int64_t>(L) > P.hist_stride ? static_cast<int>(P.hist_stride) : L);
@@ -158,8 +160,8 @@ __device__ __forceinline__ void group_load_seq(const VerifyDev& P, DShared& S, i
         }
     } else {
         if (gt == 0) S.nh = 0;
+        group_sync();
     }
-    group_sync();
 }
 
 // The normaliser of a row from its chunks' segment sums (one warp): the
@@ -276,14 +278,17 @@ __device__ __noinline__ int group_argmax(const VerifyDev& P, DShared& S, const i
 //   DENSE = false: argmax_v (z_v / T - ln E_v) over v != ex (the point-mass
 //     residual after rejecting draft ex, or the bonus sample with ex = -1);
 //   DENSE = true: argmax_v (log max(0, p_v - q_v) - ln E_v), the residual of a
-//     rejected dense draft; returns -1 when that residual is zero everywhere.
-// log w_v - ln E_v <= z_v / T [- lse] - ln M of its block, so the blocks
-// whose bound z_max / T [- lse] - ln M cannot reach the best found so far
-// are never read again.  Seed: each warp scores its block with the largest
-// value; then each warp takes tiles of 32 blocks, computes their draws and
-// bounds, and reads the passing ones fused_batch at a time (all loads in
-// flight), screening them against one raw-logit threshold per block before
-// the exact per-element score.  Whole group; returns the winner.
+//     rejected dense draft; returns -2 when the fp32 normaliser cannot settle
+//     the decision (the caller then passes the exact one, EXACT = true), -1
+//     when the residual is zero everywhere.
+// The streaming pass stored every block's bound z_max / T - ln M of its
+// scores (log w_v - ln E_v <= z_v / T [- lse] - ln M), so only the blocks
+// whose bound reaches the best score found so far are read again.  Seed:
+// each warp scores, in its block with the largest bound, each lane's largest
+// element; then each warp walks tiles of 32 bounds and reads the passing
+// blocks fused_batch at a time (all loads in flight, the block draws made
+// meanwhile), screening them against one raw-logit threshold per block
+// before the exact per-element score.  Whole group; returns the winner.
 template <bool BF16, bool SOFTCAP, bool PENALTY, bool DENSE, bool EXACT = false>
 __device__ __noinline__ int group_sample(const VerifyDev& P, DShared& S, const int* pkey, const int* ppos, uint4* stg_all,
                                          int b, int a, int ex, double lse64 = 0.0) {
@@ -296,7 +301,7 @@ __device__ __noinline__ int group_sample(const VerifyDev& P, DShared& S, const i
     const int gt = threadIdx.x - kFD0 * 32, gw = gt >> 5, lane = gt & 31;
     const int K1 = P.K + 1;
     const size_t row = static_cast<size_t>(b) * K1 + a;
-    const float* bmx = P.bmax + row * P.nblk;
+    const float* bnd = P.bmax + row * P.nblk;
     const char* rowp = static_cast<const char*>(P.logits) + row * P.V * ElemTraits<BF16>::SIZE;
     const float* qrow = DENSE ? P.q + (static_cast<size_t>(b) * P.K + a) * P.V : nullptr;
     uint4* stg = stg_all + gw * (NB * 32 * VPL);
@@ -310,6 +315,7 @@ __device__ __noinline__ int group_sample(const VerifyDev& P, DShared& S, const i
         rms = __ldcg(reinterpret_cast<const float2*>(&P.rowres[row]));
         lse_f = EXACT ? static_cast<float>(lse64) : rms.x * P.invT + logf(rms.y);
     }
+    const float off = DENSE ? lse_f : 0.0f;  // block bounds of the residual: minus lse
     // exact residual score of id v in fp64 (the row's exact normaliser), -inf for a zero residual
     auto exact_residual_score = [&](int v) -> double {
         const double z = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, v), pen_of(v), P);
@@ -337,38 +343,61 @@ __device__ __noinline__ int group_sample(const VerifyDev& P, DShared& S, const i
     };
     if (gt == 0) S.thr = 0u;
     group_sync();
-    // ---- seed: each warp scores, in its block with the largest value, each lane's
-    //      largest element (this only sets the threshold; the pass below finds it again)
+    // ---- seed (only sets the threshold; the pass below finds its elements again):
+    //      each warp takes up to kSeed blocks with the largest bounds among its lanes'
+    //      best ones, and each lane scores its largest element of each (all loads in
+    //      flight together, the blocks' draws made meanwhile)
     {
+        constexpr int kSeed = 4;
         float lb = -INFINITY;
         int lq = -1;
         for (int q = gw + kFDWarps * lane; q < P.nblk; q += kFDThreads) {
-            const float x = __ldcg(bmx + q);
+            const float x = __ldcg(bnd + q);
             if (x > lb) { lb = x; lq = q; }
         }
-        const unsigned kq = warp_best_key(lb);
-        const unsigned own = __ballot_sync(0xffffffffu, kq != 0u && lb > -INFINITY && score_key(lb) == kq);
-        const int qs = own ? __shfl_sync(0xffffffffu, lq, __ffs(own) - 1) : -1;
+        int qs[kSeed];
+#pragma unroll
+        for (int h = 0; h < kSeed; ++h) {
+            const unsigned kq = warp_best_key(lb);
+            const unsigned own = __ballot_sync(0xffffffffu, kq != 0u && lb > -INFINITY && score_key(lb) == kq);
+            const int src = own ? __ffs(own) - 1 : -1;
+            qs[h] = src >= 0 ? __shfl_sync(0xffffffffu, lq, src) : -1;
+            if (lane == src) lb = -INFINITY;  // that lane's block is taken
+        }
+        uint4 r[kSeed * VPL];
+#pragma unroll
+        for (int h = 0; h < kSeed; ++h)
+#pragma unroll
+            for (int u = 0; u < VPL; ++u) {
+                const int e0 = qs[h] * BLK + (u * 32 + lane) * EPV;
+                r[h * VPL + u] = (qs[h] >= 0 && e0 < P.V) ? load_vec<BF16>(rowp, e0, P.V, P.aligned)
+                                                           : make_uint4(0u, 0u, 0u, 0u);
+            }
+        int myq = -1;
+#pragma unroll
+        for (int h = 0; h < kSeed; ++h)
+            if (lane == h) myq = qs[h];
+        BlockNoise mine{1.0f, 0.0f, 0, 0};
+        if (myq >= 0) mine = block_noise(nk, static_cast<uint32_t>(myq), static_cast<uint32_t>(a));
         float sc = -INFINITY;
-        if (qs >= 0) {
+#pragma unroll
+        for (int h = 0; h < kSeed; ++h) {
+            const float Mq = __shfl_sync(0xffffffffu, mine.M, h);
+            const int Iq = __shfl_sync(0xffffffffu, mine.I, h);
+            if (qs[h] < 0) continue;
             float xb = -INFINITY;
             int vb = -1;
 #pragma unroll
             for (int u = 0; u < VPL; ++u) {
-                const int e0 = qs * BLK + (u * 32 + lane) * EPV;
-                const uint4 r = e0 < P.V ? load_vec<BF16>(rowp, e0, P.V, P.aligned) : make_uint4(0u, 0u, 0u, 0u);
                 float x[EPV];
-                unpack<BF16>(r, x);
+                unpack<BF16>(r[h * VPL + u], x);
 #pragma unroll
                 for (int e = 0; e < EPV; ++e) {
-                    const int v = e0 + e;
+                    const int v = qs[h] * BLK + (u * 32 + lane) * EPV + e;
                     if (v < P.V && v != ex && (vb < 0 || x[e] > xb)) { xb = x[e]; vb = v; }
                 }
             }
-            if (vb >= 0) {
-                const BlockNoise bn = block_noise(nk, static_cast<uint32_t>(qs), static_cast<uint32_t>(a));
-                sc = score_of(vb, xb, bn.M, bn.I, -INFINITY);
-            }
+            if (vb >= 0) sc = fmaxf(sc, score_of(vb, xb, Mq, Iq, -INFINITY));
         }
         const unsigned kw = warp_best_key(sc);
         if (kw != 0u && lane == 0) atomicMax(&S.thr, kw);
@@ -380,30 +409,19 @@ __device__ __noinline__ int group_sample(const VerifyDev& P, DShared& S, const i
     // ---- the blocks whose bound reaches the best, tile by tile
     for (int q0 = gw * 32; q0 < P.nblk; q0 += kFDThreads) {
         const int q = q0 + lane;
-        float bnd = -INFINITY, Mq = 1.0f;
-        int Iq = 0;
-        if (q < P.nblk) {
-            const BlockNoise bn = block_noise(nk, static_cast<uint32_t>(q), static_cast<uint32_t>(a));
-            bnd = block_zmax<SOFTCAP, PENALTY>(__ldcg(bmx + q), P) * P.invT - (DENSE ? lse_f : 0.0f) - bn.lnM;
-            Mq = bn.M;
-            Iq = bn.I;
-        }
+        const float bq = q < P.nblk ? __ldcg(bnd + q) - off : -INFINITY;
         {
             const unsigned kc = max(*reinterpret_cast<volatile unsigned*>(&S.thr), warp_best_key(t.s1));
             if (kc != 0u) thr = fmaxf(thr, key_score(kc) - cand_delta(key_score(kc)));
         }
-        unsigned pass = __ballot_sync(0xffffffffu, q < P.nblk && bnd + bound_slack(bnd) >= thr);
+        unsigned pass = __ballot_sync(0xffffffffu, q < P.nblk && bq + bound_slack(bq) >= thr);
         while (pass != 0u) {
             int qh[NB];
-            float Mh[NB];
-            int Ih[NB];
 #pragma unroll
             for (int h = 0; h < NB; ++h) {
                 const int bit = pass ? __ffs(pass) - 1 : -1;
                 if (pass) pass &= pass - 1u;
                 qh[h] = bit >= 0 ? q0 + bit : -1;
-                Mh[h] = __shfl_sync(0xffffffffu, Mq, bit >= 0 ? bit : 0);
-                Ih[h] = __shfl_sync(0xffffffffu, Iq, bit >= 0 ? bit : 0);
             }
             uint4 r[NB * VPL];
 #pragma unroll
@@ -414,14 +432,27 @@ __device__ __noinline__ int group_sample(const VerifyDev& P, DShared& S, const i
                     r[h * VPL + u] = (qh[h] >= 0 && e0 < P.V) ? load_vec<BF16>(rowp, e0, P.V, P.aligned)
                                                                : make_uint4(0u, 0u, 0u, 0u);
                 }
+            // the batch's block draws, lane h for block h, while the loads are in flight
+            int myq = -1;
+#pragma unroll
+            for (int h = 0; h < NB; ++h)
+                if (lane == h) myq = qh[h];
+            BlockNoise mine{1.0f, 0.0f, 0, 0};
+            if (myq >= 0) mine = block_noise(nk, static_cast<uint32_t>(myq), static_cast<uint32_t>(a));
+            float Mh[NB];
+            int Ih[NB];
+#pragma unroll
+            for (int h = 0; h < NB; ++h) {
+                Mh[h] = __shfl_sync(0xffffffffu, mine.M, h);
+                Ih[h] = __shfl_sync(0xffffffffu, mine.I, h);
+            }
             // raw-logit screen per block (none when a penalty below 1 may raise a value)
             float xt[NB];
 #pragma unroll
             for (int h = 0; h < NB; ++h)
                 xt[h] = qh[h] < 0 ? INFINITY
                                   : ((PENALTY && P.rep < 1.0f) ? -INFINITY
-                                                                : raw_screen<SOFTCAP>(thr + (DENSE ? lse_f : 0.0f),
-                                                                                      ln_fast(Mh[h]), P));
+                                                                : raw_screen<SOFTCAP>(thr + off, ln_fast(Mh[h]), P));
 #pragma unroll
             for (int i = 0; i < NB * VPL; ++i) stg[i * 32 + lane] = r[i];
             unsigned long long cm = 0ull;
@@ -537,11 +568,12 @@ __device__ __noinline__ void group_row_event(const VerifyDev& P, DShared& S, int
     const bool dense = P.q != nullptr;
     NoiseKey nk = P.nk;
     nk.seq = static_cast<uint32_t>(b);
-    group_load_seq<PENALTY>(P, S, pkey, ppos, b, gt);
-    auto pen_of = [&](int v, int jj) { return PENALTY && pen_lookup(pkey, ppos, S.d, S.nh, P.W, v, jj); };
+    if (gt < P.K) S.d[gt] = P.drafts[static_cast<size_t>(b) * P.K + gt];
+    group_sync();
     // ---- the row's test (T > 0) or argmax (T = 0)
     int acc = 0;
     if constexpr (GREEDY) {
+        group_load_seq<PENALTY>(P, S, pkey, ppos, b, gt);
         const int y = group_argmax<BF16, SOFTCAP, PENALTY>(P, S, pkey, ppos, b, j);
         if (gt == 0) {
             RowRes rr;
@@ -554,6 +586,8 @@ __device__ __noinline__ void group_row_event(const VerifyDev& P, DShared& S, int
     } else if (gt < 32 && j < keff) {
         float mf, Sf;
         row_normaliser(P, row, lane, mf, Sf);
+        const int dj = S.d[j];
+        const bool pend = PENALTY && dj >= 0 && dj < P.V && warp_window_has(P, S, b, j, dj);
         if (gt == 0) {
             if (!(Sf > 0.0f && Sf < INFINITY && mf < INFINITY)) raise_status(P.status, SPECNG_DEV_NONFINITE);
             RowRes rr;
@@ -565,7 +599,6 @@ __device__ __noinline__ void group_row_event(const VerifyDev& P, DShared& S, int
                     const float xd = static_cast<float>(raw_logit_f64<BF16>(P.logits, row, P.V, d));
                     const float qdf = dense ? P.q[(static_cast<size_t>(b) * P.K + j) * P.V + d] : 1.0f;
                     const double u = accept_uniform_f64(nk, static_cast<uint32_t>(j + 1));
-                    const bool pend = pen_of(d, j);
                     const float lsef = mf * P.invT + logf(Sf);
                     const float lp = transform_f32<SOFTCAP, PENALTY>(xd, pend, P) * P.invT - lsef;
                     const float lr = logf(static_cast<float>(u)) + logf(qdf);
@@ -601,6 +634,7 @@ __device__ __noinline__ void group_row_event(const VerifyDev& P, DShared& S, int
     const int a = S.ival[1];
     if (a < 0) return;
     // ---- the token at row a, then the outputs
+    if constexpr (!GREEDY) group_load_seq<PENALTY>(P, S, pkey, ppos, b, gt);
     const int da = a < keff ? S.d[a] : -1;
     const bool dvalid = da >= 0 && da < P.V;
     int y;
@@ -662,9 +696,9 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
     __shared__ long long s_off[SPECNG_MAX_K + 2];
     __shared__ int s_hwin[PENALTY ? SPECNG_MAX_REP_WINDOW : 1];
     __shared__ int s_pdrafts[SPECNG_MAX_K + 1];
+    __shared__ float s_lnm[GREEDY ? 1 : kStages][GREEDY ? 1 : (CHUNK >> kNoiseBlockShift)];
     __shared__ unsigned s_notes[kNoteCap];
     __shared__ unsigned s_note_wr;
-    __shared__ unsigned s_note_rd;
     __shared__ int s_stream_done;
     __shared__ int s_last;
     __shared__ DShared S;
@@ -685,7 +719,6 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
         }
         mbar_init_fence();
         s_note_wr = 0u;
-        s_note_rd = 0u;
         s_stream_done = 0;
     }
     __syncthreads();
@@ -711,47 +744,52 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
         }
     }
     if (tid == 0) {
+        // s_off[j]: the first row of wave j in the order (a row is one item)
         long long off = 0;
         int W = 0;
         for (int u = 0; u <= P.K; ++u) W += s_hist[u];
         for (int j = 0; j <= P.K; ++j) {
             s_off[j] = off;
-            off += static_cast<long long>(W) * P.nchunk;
+            off += W;
             W -= s_hist[j];
         }
         s_off[P.K + 1] = off;
     }
     __syncthreads();
-    const long long N = s_off[P.K + 1];
+    const long long N = s_off[P.K + 1];  // rows of the call
     const long long G = gridDim.x;
 
     if (warp == kPWarp) {
         // ================= producer =================
         constexpr int kHW = PENALTY ? SPECNG_MAX_REP_WINDOW / 32 : 1;
+        constexpr int BPC = CHUNK >> kNoiseBlockShift;  // noise blocks per chunk
+        constexpr int NPL = GREEDY ? 1 : (BPC + 31) / 32;  // block draws per lane per chunk
         struct Item {
-            int b, j, c, L, draft;
+            int b, j, L, draft;
             unsigned long long st;
             int hw[kHW];
+            bool valid;
         };
         auto clampL = [&](int L) {
             return L < 0 ? 0 : (static_cast<int64_t>(L) > P.hist_stride ? static_cast<int>(P.hist_stride) : L);
         };
-        // item t of the order: wave, rank in the wave, chunk; the loads that do not
-        // depend on the history length are issued here
+        // row t of the order (wave j, rank r): the loads that do not depend on the
+        // history length are issued here, two rows before the row is streamed
         auto map_item = [&](long long t, Item& it) {
+            it.valid = t < N;
+            if (!it.valid) return;
             int j = 0;
             while (j < P.K && t >= s_off[j + 1]) ++j;
-            const long long tt = t - s_off[j];
-            const int r = static_cast<int>(tt / P.nchunk);
             it.j = j;
-            it.c = static_cast<int>(tt - static_cast<long long>(r) * P.nchunk);
-            it.b = s_ord[r];
+            it.b = s_ord[t - s_off[j]];
             it.L = PENALTY ? P.lens[it.b] : 0;
             it.draft = lane < P.K ? P.drafts[static_cast<size_t>(it.b) * P.K + lane] : -1;
             it.st = (P.early_exit && j > 0) ? __ldcg(P.seq_state + it.b) : 0ull;
         };
+        // the history tail of the penalty window (first used one row later)
         auto load_tail = [&](Item& it) {
             if constexpr (PENALTY) {
+                if (!it.valid) return;
                 const int L = clampL(it.L);
                 it.L = L;
                 const int nh = L < P.W ? L : P.W;
@@ -762,48 +800,68 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
                 }
             }
         };
-        long long t = blockIdx.x;
-        Item cur, nxt;
-        bool have = t < N, have_n = false;
-        if (have) {
-            map_item(t, cur);
-            load_tail(cur);
-            if (t + G < N) { map_item(t + G, nxt); have_n = true; }
-        }
         bool ok = true;
         int st = 0, n = 0, issued = 0;
         unsigned eph = 0u;
-        while (have && ok) {
-            if (have_n) load_tail(nxt);
-            const bool skip = P.early_exit && cur.j > 0 && [&] {
+        // one row into the ring, chunk by chunk (or skipped); false once the ring timed out
+        auto issue = [&](const Item& cur) -> bool {
+            if (P.early_exit && cur.j > 0) {
                 const int a = known_a(state_bits(cur.st, P.epoch), s_keff[cur.b]);
-                return a >= 0 && a < cur.j;
-            }();
-            if (!skip) {
-                const int v0 = cur.c * CHUNK;
+                if (a >= 0 && a < cur.j) return true;  // past a known first rejection
+            }
+            const int keff = s_keff[cur.b];
+            int nh = 0;
+            if constexpr (PENALTY) {
+                // the window of row j: the history tail, then d_1..d_j
+                nh = cur.L < P.W ? cur.L : P.W;
+                __syncwarp();  // the previous row's chunks have read the window
+#pragma unroll
+                for (int i = 0; i < kHW; ++i)
+                    if (lane + 32 * i < nh) s_hwin[lane + 32 * i] = cur.hw[i];
+                if (lane < keff) s_pdrafts[lane] = cur.draft;
+                __syncwarp();
+            }
+            NoiseKey nk = P.nk;
+            nk.seq = static_cast<uint32_t>(cur.b);
+            for (int c = 0; c < P.nchunk; ++c) {
+                const int v0 = c * CHUNK;
                 const int v1 = min(P.V, v0 + CHUNK);
                 const char* src = static_cast<const char*>(P.logits) +
                                   ((static_cast<size_t>(cur.b) * K1 + cur.j) * P.V + v0) * ElemTraits<BF16>::SIZE;
-                if (n >= kStages) ok = mbar_wait_bounded(&s_empty[st], eph);
-                if (!ok) { if (lane == 0) raise_status(P.status, SPECNG_DEV_TIMEOUT); break; }
+                // the chunk's block draws (ln M of each block minimum), made before the
+                // stage is free so that they do not delay it
+                float lnm[NPL];
+                if constexpr (!GREEDY) {
+                    const int blk0 = v0 >> kNoiseBlockShift;
+#pragma unroll
+                    for (int i = 0; i < NPL; ++i) {
+                        const int q = lane + 32 * i;
+                        lnm[i] = (q < BPC && blk0 + q < P.nblk)
+                                     ? block_noise(nk, static_cast<uint32_t>(blk0 + q), static_cast<uint32_t>(cur.j)).lnM
+                                     : 0.0f;
+                    }
+                }
+                if (n >= kStages && !mbar_wait_bounded(&s_empty[st], eph)) {
+                    if (lane == 0) raise_status(P.status, SPECNG_DEV_TIMEOUT);
+                    return false;
+                }
                 if (P.aligned && lane == 0) {
                     mbar_add_tx(&s_full[st], static_cast<unsigned>(v1 - v0) * ElemTraits<BF16>::SIZE);
                     bulk_g2s(s_stage + st * SB, src, static_cast<unsigned>(v1 - v0) * ElemTraits<BF16>::SIZE, &s_full[st]);
                 }
                 issued = n + 1;
-                const int keff = s_keff[cur.b];
                 StageMeta& mt = s_meta[st];
                 if (lane == 0) {
-                    mt.b = cur.b; mt.j = cur.j; mt.c = cur.c;
-                    mt.seg_end = 1;
+                    mt.b = cur.b; mt.j = cur.j; mt.c = c;
+                    mt.seg_end = c == P.nchunk - 1 ? 1 : 0;
                     mt.sum = (!GREEDY && cur.j < keff) ? 1 : 0;
                 }
-                if constexpr (PENALTY) {
-                    const int nh = cur.L < P.W ? cur.L : P.W;
+                if constexpr (!GREEDY) {
 #pragma unroll
-                    for (int i = 0; i < kHW; ++i)
-                        if (lane + 32 * i < nh) s_hwin[lane + 32 * i] = cur.hw[i];
-                    if (lane < keff) s_pdrafts[lane] = cur.draft;
+                    for (int i = 0; i < NPL; ++i)
+                        if (lane + 32 * i < BPC) s_lnm[st][lane + 32 * i] = lnm[i];
+                }
+                if constexpr (PENALTY) {
                     uint32_t* bm = s_bm + st * (CHUNK / 32);
                     for (int i = lane; i < CHUNK / 32; i += 32) bm[i] = 0u;
                     __syncwarp();
@@ -837,14 +895,26 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
                     if (n > kStages) eph ^= 1u;
                 }
             }
-            // next item
+            return true;
+        };
+        // two item slots used in turn (no copies of loads in flight): while one row
+        // is issued, the next one's history tail and the one after's lengths load
+        long long t = blockIdx.x;
+        Item A, Bn;
+        map_item(t, A);
+        load_tail(A);
+        map_item(t + G, Bn);
+        while (ok && A.valid) {
+            load_tail(Bn);
+            ok = issue(A);
             t += G;
-            have = have_n;
-            if (have) {
-                cur = nxt;
-                have_n = t + G < N;
-                if (have_n) map_item(t + G, nxt);
-            }
+            map_item(t + G, A);          // A now holds the row after Bn
+            if (!ok || !Bn.valid) break;
+            load_tail(A);
+            ok = issue(Bn);
+            t += G;
+            map_item(t + G, Bn);
+            if (!ok || !A.valid) break;
         }
         // the end of the stream: a stage whose metadata says so (its item index is n)
         bool marked = false;
@@ -976,11 +1046,17 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
                     s = ss.s;
                 }
             }
-            // block maxima (raw logits) of my vector rows
+            // per noise block of my vector rows: at T = 0 its largest raw logit; at T > 0
+            // the bound of its sampling scores, z_max / T - ln M (z_max: the transform of
+            // the largest raw logit; M: the block's noise minimum, drawn by the producer)
             {
                 const int blk0 = (v0 >> kNoiseBlockShift) + warp * (kVL / VPB);
                 float* dst = P.bmax + static_cast<size_t>(row) * P.nblk + blk0;
                 const int nb = min(kVL / VPB, P.nblk - blk0);
+                auto bound = [&](float raw, int i) {
+                    if constexpr (GREEDY) return raw;
+                    return block_zmax<SOFTCAP, PENALTY>(raw, P) * P.invT - s_lnm[st][warp * (kVL / VPB) + i];
+                };
                 if constexpr (BF16) {
                     uint32_t bw[kVL / 2];
 #pragma unroll
@@ -995,7 +1071,7 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
                     if (lane == 0) {
 #pragma unroll
                         for (int i = 0; i < kVL; ++i)
-                            if (i < nb) dst[i] = (i & 1) ? bf16hi(bw[i >> 1]) : bf16lo(bw[i >> 1]);
+                            if (i < nb) dst[i] = bound((i & 1) ? bf16hi(bw[i >> 1]) : bf16lo(bw[i >> 1]), i);
                     }
                 } else {
                     float bmv[kVL / VPB];
@@ -1012,7 +1088,7 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
                     if (lane == 0) {
 #pragma unroll
                         for (int p = 0; p < kVL / VPB; ++p)
-                            if (p < nb) dst[p] = bmv[p];
+                            if (p < nb) dst[p] = bound(bmv[p], p);
                     }
                 }
             }
@@ -1047,8 +1123,12 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
                 }
                 if (lane == 0) {
                     s_cnt[st] = 0;
+                }
+                if (lane == 0 && mt.seg_end) {
+                    // the row's last chunk: every warp has finished the row's earlier chunks
+                    // (stages are taken in order), so the whole row is streamed; hand it to
+                    // the decision group (a slot frees once the group took it)
                     __threadfence_block();
-                    // post the chunk's note (a slot frees once the decision group took it)
                     const unsigned idx = atomicAdd(&s_note_wr, 1u);
                     volatile unsigned* slot = &s_notes[idx % kNoteCap];
                     bool posted = false;
@@ -1078,62 +1158,39 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
     } else {
         // ================= decision group =================
         const int gt = tid - kFD0 * 32;
-        unsigned rd = 0u;  // next note to take (group warp 0's copy)
+        unsigned rd = 0u;  // next row (thread 0's copy)
         int idle = 0;
         for (;;) {
-            if (gt < 32) {
-                // take the notes posted so far, in order
-                const unsigned v = *reinterpret_cast<volatile unsigned*>(&s_notes[(rd + lane) % kNoteCap]);
-                const unsigned have = __ballot_sync(0xffffffffu, v != 0u);
-                const int nn = have == 0xffffffffu ? 32 : __ffs(~have) - 1;
-                int done_rows = 0;
-                if (nn > 0) {
+            if (gt == 0) {
+                int got = -1;
+                volatile unsigned* slot = &s_notes[rd % kNoteCap];
+                const unsigned v = *slot;
+                if (v != 0u) {
+                    *slot = 0u;
+                    got = static_cast<int>(v - 1u);
+                    ++rd;
                     idle = 0;
-                    int comp = 0;
-                    if (lane < nn) {
-                        *reinterpret_cast<volatile unsigned*>(&s_notes[(rd + lane) % kNoteCap]) = 0u;
-                        __threadfence();  // the chunk's records (acquired through the note) before its count
-                        const unsigned cnt = ticket_add(P.row_tix + (v - 1u), P.epoch);
-                        if (cnt == 0u) raise_status(P.status, SPECNG_DEV_TIMEOUT);
-                        comp = cnt == static_cast<unsigned>(P.nchunk);
-                    }
-                    const unsigned cb = __ballot_sync(0xffffffffu, comp != 0);
-                    if (comp) S.rows[__popc(cb & ((1u << lane) - 1u))] = static_cast<int>(v - 1u);
-                    done_rows = __popc(cb);
-                    rd += static_cast<unsigned>(nn);
-                    if (done_rows) __threadfence();  // the other CTAs' records of these rows
-                }
-                int quit = 0;
-                if (nn == 0) {
+                } else {
                     const int sd = *reinterpret_cast<volatile int*>(&s_stream_done);
-                    __threadfence_block();  // the count before the slot: a note posted before it is seen
-                    if (sd >= kCWarps) {
-                        // the streaming warps have finished: a note posted before that is
-                        // visible now; look once more before leaving
-                        const unsigned v2 = *reinterpret_cast<volatile unsigned*>(&s_notes[rd % kNoteCap]);
-                        quit = __shfl_sync(0xffffffffu, v2 == 0u ? 1 : 0, 0);
-                    } else {
-                        if (++idle > (1 << 22)) {
-                            if (lane == 0) raise_status(P.status, SPECNG_DEV_TIMEOUT);
-                            quit = 1;
-                        } else if (idle > 16) {
-                            __nanosleep(128);
-                        }
+                    __threadfence_block();  // the count before the slot: a row posted before it is seen
+                    if (sd >= kCWarps && *slot == 0u) {
+                        got = -2;
+                    } else if (++idle > (1 << 22)) {
+                        raise_status(P.status, SPECNG_DEV_TIMEOUT);
+                        got = -2;
+                    } else if (idle > 16) {
+                        __nanosleep(128);
                     }
                 }
-                if (lane == 0) {
-                    S.nrows = done_rows;
-                    S.quit = quit;
-                }
+                S.ival[2] = got;
             }
             group_sync();
-            const int nr = S.nrows;
-            const int quit = S.quit;
-            for (int i = 0; i < nr; ++i) {
-                const int row = S.rows[i];
+            const int row = S.ival[2];
+            if (row == -2) break;
+            if (row >= 0) {
+                __threadfence_block();  // the row's records, written by this CTA's streaming warps
                 group_row_event<BF16, GREEDY, SOFTCAP, PENALTY>(P, S, s_pkey, s_ppos, s_stg, s_keff, row / K1, row % K1);
             }
-            if (quit) break;
             group_sync();
         }
     }
