@@ -404,7 +404,8 @@ struct StageMeta {
     int seg_end;   // the last chunk of this row in the CTA's range
     int sum;       // the row's softmax sum is needed (accept test)
     unsigned penw; // bit w: warp w's slice holds a penalised id
-    int pad[2];
+    int dnext;     // single-kernel schedule: d_{j+1} of the row (-1: none)
+    int pend;      // single-kernel schedule: d_{j+1} is in the row's penalty window
 };
 
 // Running state of a lane's sum of exponentials: reference m (transformed

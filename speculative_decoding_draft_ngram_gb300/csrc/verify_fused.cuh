@@ -109,7 +109,7 @@ struct DShared {
     int nrows;
     int quit;
     int nh;
-    int bq[kFDWarps][4];
+    unsigned pmask[kFDWarps][16];
 };
 
 // Is v among the last W tokens of history[:L] ++ d_1..d_j (the penalty window
@@ -406,23 +406,43 @@ __device__ __noinline__ int group_sample(const VerifyDev& P, DShared& S, const i
     float thr = -INFINITY;
     if (S.thr != 0u) thr = key_score(S.thr) - cand_delta(key_score(S.thr));
     Top2 t = top2_empty();
-    // ---- the blocks whose bound reaches the best, tile by tile
-    for (int q0 = gw * 32; q0 < P.nblk; q0 += kFDThreads) {
-        const int q = q0 + lane;
-        const float bq = q < P.nblk ? __ldcg(bnd + q) - off : -INFINITY;
+    // ---- the blocks whose bound reaches the best: a warp's tiles (32 blocks each) are
+    //      taken kTG at a time -- all their bounds loaded together and compared with the
+    //      threshold (a pass mask per tile) -- then the passing blocks are read again in
+    //      batches of NB, across tiles
+    constexpr int kTG = 16;
+    const int ntiles = P.nblk > gw * 32 ? (P.nblk - gw * 32 + kFDThreads - 1) / kFDThreads : 0;
+    for (int tg = 0; tg < ntiles; tg += kTG) {
         {
+            float bpf[kTG];
+#pragma unroll
+            for (int i = 0; i < kTG; ++i) {
+                const int q = gw * 32 + (tg + i) * kFDThreads + lane;
+                bpf[i] = (tg + i < ntiles && q < P.nblk) ? __ldcg(bnd + q) - off : -INFINITY;
+            }
             const unsigned kc = max(*reinterpret_cast<volatile unsigned*>(&S.thr), warp_best_key(t.s1));
             if (kc != 0u) thr = fmaxf(thr, key_score(kc) - cand_delta(key_score(kc)));
+#pragma unroll
+            for (int i = 0; i < kTG; ++i) {
+                const unsigned msk = __ballot_sync(0xffffffffu, bpf[i] > -INFINITY && bpf[i] + bound_slack(bpf[i]) >= thr);
+                if (lane == 0) S.pmask[gw][i] = msk;
+            }
+            __syncwarp();
         }
-        unsigned pass = __ballot_sync(0xffffffffu, q < P.nblk && bq + bound_slack(bq) >= thr);
-        while (pass != 0u) {
+        int ti = 0;
+        unsigned pass = S.pmask[gw][0];
+        auto next_block = [&]() -> int {
+            while (pass == 0u && ti + 1 < kTG && tg + ti + 1 < ntiles) pass = S.pmask[gw][++ti];
+            if (pass == 0u) return -1;
+            const int bit = __ffs(pass) - 1;
+            pass &= pass - 1u;
+            return gw * 32 + (tg + ti) * kFDThreads + bit;
+        };
+        for (;;) {
             int qh[NB];
 #pragma unroll
-            for (int h = 0; h < NB; ++h) {
-                const int bit = pass ? __ffs(pass) - 1 : -1;
-                if (pass) pass &= pass - 1u;
-                qh[h] = bit >= 0 ? q0 + bit : -1;
-            }
+            for (int h = 0; h < NB; ++h) qh[h] = next_block();
+            if (qh[0] < 0) break;
             uint4 r[NB * VPL];
 #pragma unroll
             for (int h = 0; h < NB; ++h)
@@ -560,7 +580,7 @@ __device__ __noinline__ double group_exact_lse(const VerifyDev& P, DShared& S, c
 // when this update makes a known -- the token at row a and the outputs.
 template <bool BF16, bool GREEDY, bool SOFTCAP, bool PENALTY>
 __device__ __noinline__ void group_row_event(const VerifyDev& P, DShared& S, int* pkey, int* ppos, uint4* stg,
-                                             const uint8_t* s_keff, int b, int j) {
+                                             const uint8_t* s_keff, int b, int j, int dnext, int pend) {
     const int gt = threadIdx.x - kFD0 * 32, lane = gt & 31;
     const int K1 = P.K + 1;
     const size_t row = static_cast<size_t>(b) * K1 + j;
@@ -568,39 +588,39 @@ __device__ __noinline__ void group_row_event(const VerifyDev& P, DShared& S, int
     const bool dense = P.q != nullptr;
     NoiseKey nk = P.nk;
     nk.seq = static_cast<uint32_t>(b);
-    if (gt < P.K) S.d[gt] = P.drafts[static_cast<size_t>(b) * P.K + gt];
-    group_sync();
+    group_sync();  // every thread has read the arguments the loop passed through S
     // ---- the row's test (T > 0) or argmax (T = 0)
     int acc = 0;
     if constexpr (GREEDY) {
+        if (gt < P.K) S.d[gt] = P.drafts[static_cast<size_t>(b) * P.K + gt];
+        group_sync();
         group_load_seq<PENALTY>(P, S, pkey, ppos, b, gt);
         const int y = group_argmax<BF16, SOFTCAP, PENALTY>(P, S, pkey, ppos, b, j);
         if (gt == 0) {
             RowRes rr;
             rr.m = 0.0f; rr.S = 0.0f; rr.winner = y; rr.pad = 0;
             P.rowres[row] = rr;
-            const int d = j < keff ? S.d[j] : -1;
+            const int d = j < keff ? dnext : -1;
             if (j < keff && !(d >= 0 && d < P.V)) raise_status(P.status, SPECNG_DEV_TOKEN_OOR);
             acc = j < keff && d >= 0 && d < P.V && d == y;
         }
-    } else if (gt < 32 && j < keff) {
-        float mf, Sf;
-        row_normaliser(P, row, lane, mf, Sf);
-        const int dj = S.d[j];
-        const bool pend = PENALTY && dj >= 0 && dj < P.V && warp_window_has(P, S, b, j, dj);
-        if (gt == 0) {
+    } else if (gt == 0 && j < keff) {
+        // the row's normaliser: its one record (reference m, sum relative to it)
+        const float2 rec = __ldcg(reinterpret_cast<const float2*>(P.part + row * P.nchunk));
+        const float mf = rec.x, Sf = rec.y;
+        {
             if (!(Sf > 0.0f && Sf < INFINITY && mf < INFINITY)) raise_status(P.status, SPECNG_DEV_NONFINITE);
             RowRes rr;
             rr.m = mf; rr.S = Sf; rr.winner = -1; rr.pad = 0;
             P.rowres[row] = rr;
             {
-                const int d = S.d[j];
+                const int d = dnext;
                 if (d >= 0 && d < P.V) {
                     const float xd = static_cast<float>(raw_logit_f64<BF16>(P.logits, row, P.V, d));
                     const float qdf = dense ? P.q[(static_cast<size_t>(b) * P.K + j) * P.V + d] : 1.0f;
                     const double u = accept_uniform_f64(nk, static_cast<uint32_t>(j + 1));
                     const float lsef = mf * P.invT + logf(Sf);
-                    const float lp = transform_f32<SOFTCAP, PENALTY>(xd, pend, P) * P.invT - lsef;
+                    const float lp = transform_f32<SOFTCAP, PENALTY>(xd, pend != 0, P) * P.invT - lsef;
                     const float lr = logf(static_cast<float>(u)) + logf(qdf);
                     if (lr < lp - 1e-4f * (1.0f + fabsf(lp))) {
                         acc = 1;
@@ -608,7 +628,7 @@ __device__ __noinline__ void group_row_event(const VerifyDev& P, DShared& S, int
                         acc = 0;
                     } else {
                         count_diag(P, SPECNG_DIAG_ACCEPT_F64);
-                        acc = accept_f64<SOFTCAP, PENALTY>(P, xd, pend, u, static_cast<double>(qdf), mf, Sf);
+                        acc = accept_f64<SOFTCAP, PENALTY>(P, xd, pend != 0, u, static_cast<double>(qdf), mf, Sf);
                     }
                 } else {
                     raise_status(P.status, SPECNG_DEV_TOKEN_OOR);
@@ -634,7 +654,11 @@ __device__ __noinline__ void group_row_event(const VerifyDev& P, DShared& S, int
     const int a = S.ival[1];
     if (a < 0) return;
     // ---- the token at row a, then the outputs
-    if constexpr (!GREEDY) group_load_seq<PENALTY>(P, S, pkey, ppos, b, gt);
+    if constexpr (!GREEDY) {
+        if (gt < P.K) S.d[gt] = P.drafts[static_cast<size_t>(b) * P.K + gt];
+        group_sync();
+        group_load_seq<PENALTY>(P, S, pkey, ppos, b, gt);
+    }
     const int da = a < keff ? S.d[a] : -1;
     const bool dvalid = da >= 0 && da < P.V;
     int y;
@@ -698,6 +722,7 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
     __shared__ int s_pdrafts[SPECNG_MAX_K + 1];
     __shared__ float s_lnm[GREEDY ? 1 : kStages][GREEDY ? 1 : (CHUNK >> kNoiseBlockShift)];
     __shared__ unsigned s_notes[kNoteCap];
+    __shared__ int2 s_note_aux[kNoteCap];  // d_{j+1} of the row, and whether it is penalised
     __shared__ unsigned s_note_wr;
     __shared__ int s_stream_done;
     __shared__ int s_last;
@@ -821,6 +846,16 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
                 if (lane < keff) s_pdrafts[lane] = cur.draft;
                 __syncwarp();
             }
+            // the row's draft d_{j+1} (tested when the row is decided) and whether the
+            // penalty window of row j holds it
+            const int dnext = cur.j < keff ? __shfl_sync(0xffffffffu, cur.draft, cur.j) : -1;
+            int pend = 0;
+            if constexpr (PENALTY) {
+                if (dnext >= 0) {
+                    const WindowView wv{s_hwin, s_pdrafts, nh, P.W};
+                    pend = wv.warp_has(cur.j, dnext) ? 1 : 0;
+                }
+            }
             NoiseKey nk = P.nk;
             nk.seq = static_cast<uint32_t>(cur.b);
             for (int c = 0; c < P.nchunk; ++c) {
@@ -855,6 +890,8 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
                     mt.b = cur.b; mt.j = cur.j; mt.c = c;
                     mt.seg_end = c == P.nchunk - 1 ? 1 : 0;
                     mt.sum = (!GREEDY && cur.j < keff) ? 1 : 0;
+                    mt.dnext = dnext;
+                    mt.pend = pend;
                 }
                 if constexpr (!GREEDY) {
 #pragma unroll
@@ -944,6 +981,10 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
         // ================= streaming warps =================
         const int ubase = warp * (32 * kVL);
         const int off0 = ubase * EPV + lane * EPV;
+        // the lane's sum of exponentials over the row so far, against a reference m fixed
+        // at the row's first value and raised only when a value passes it by more than
+        // 2^32 in the sum's units (so the sum never waits for a chunk's maximum)
+        float m = -INFINITY, s = 0.0f, msc = 0.0f;
         int st = 0;
         unsigned fph = 0u;
         for (;;) {
@@ -986,9 +1027,7 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
                                                   fmaxf(__uint_as_float(r.z), __uint_as_float(r.w))));
                 }
             }
-            float m = -INFINITY, s = 0.0f;
             if (dosum) {
-                float msc = 0.0f;
                 if (full) {
                     float lraw;
                     if constexpr (BF16) {
@@ -1001,10 +1040,12 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
 #pragma unroll
                         for (int i = 1; i < kVL; ++i) lraw = fmaxf(lraw, __uint_as_float(hv[i]));
                     }
-                    // the lane's largest value is its reference: every term is at most 1
-                    m = SOFTCAP ? transform_f32<true, false>(lraw, false, P) : lraw;
-                    if (m > -INFINITY) {
+                    const float zl = SOFTCAP ? transform_f32<true, false>(lraw, false, P) : lraw;
+                    if (!(m > -INFINITY)) {
+                        m = zl;
                         msc = m * P.sc;
+                    }
+                    if (m > -INFINITY) {
                         float2 acc2[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
                                           make_float2(0.0f, 0.0f)};
                         const float2 sc2 = make_float2(P.sc, P.sc), nm2 = make_float2(-msc, -msc);
@@ -1020,8 +1061,16 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
                                 acc2[i & 3] = __fadd2_rn(acc2[i & 3], make_float2(ex2_approx(tt.x), ex2_approx(tt.y)));
                             }
                         }
-                        s = ((acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y)) +
-                            ((acc2[2].x + acc2[2].y) + (acc2[3].x + acc2[3].y));
+                        float add = ((acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y)) +
+                                    ((acc2[2].x + acc2[2].y) + (acc2[3].x + acc2[3].y));
+                        if ((zl - m) * P.sc > 32.0f) {
+                            // far above the reference: raise it and take the chunk again
+                            s *= ex2_approx((m - zl) * P.sc);
+                            m = zl;
+                            msc = m * P.sc;
+                            add = sum_from_stage<BF16, SOFTCAP>(stage, ubase + lane, msc, P);
+                        }
+                        s += add;
                     }
                     if constexpr (PENALTY) {
                         unsigned long long pw = pmk;
@@ -1040,10 +1089,10 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
                         }
                     }
                 } else {
-                    const SumState ss = sum_partial<BF16, SOFTCAP, PENALTY>(stage, off0, v0, v1, pmk,
-                                                                          SumState{-INFINITY, 0.0f, 0.0f}, P);
+                    const SumState ss = sum_partial<BF16, SOFTCAP, PENALTY>(stage, off0, v0, v1, pmk, SumState{m, s, msc}, P);
                     m = ss.m;
                     s = ss.s;
+                    msc = ss.msc;
                 }
             }
             // per noise block of my vector rows: at T = 0 its largest raw logit; at T > 0
@@ -1053,9 +1102,10 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
                 const int blk0 = (v0 >> kNoiseBlockShift) + warp * (kVL / VPB);
                 float* dst = P.bmax + static_cast<size_t>(row) * P.nblk + blk0;
                 const int nb = min(kVL / VPB, P.nblk - blk0);
-                auto bound = [&](float raw, int i) {
+                // lane i < nb finishes block i (all lanes hold the warp-reduced maxima)
+                auto bound = [&](float raw) {
                     if constexpr (GREEDY) return raw;
-                    return block_zmax<SOFTCAP, PENALTY>(raw, P) * P.invT - s_lnm[st][warp * (kVL / VPB) + i];
+                    return block_zmax<SOFTCAP, PENALTY>(raw, P) * P.invT - s_lnm[st][warp * (kVL / VPB) + lane];
                 };
                 if constexpr (BF16) {
                     uint32_t bw[kVL / 2];
@@ -1068,11 +1118,11 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
 #pragma unroll
                         for (int p = 0; p < kVL / 2; ++p)
                             bw[p] = as_u32(__hmax2(as_bf162(bw[p]), as_bf162(__shfl_xor_sync(0xffffffffu, bw[p], off))));
-                    if (lane == 0) {
+                    float raw = -INFINITY;
 #pragma unroll
-                        for (int i = 0; i < kVL; ++i)
-                            if (i < nb) dst[i] = bound((i & 1) ? bf16hi(bw[i >> 1]) : bf16lo(bw[i >> 1]), i);
-                    }
+                    for (int i = 0; i < kVL; ++i)
+                        if (lane == i) raw = (i & 1) ? bf16hi(bw[i >> 1]) : bf16lo(bw[i >> 1]);
+                    if (lane < nb) dst[lane] = bound(raw);
                 } else {
                     float bmv[kVL / VPB];
 #pragma unroll
@@ -1085,32 +1135,41 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
                     for (int off = 16; off > 0; off >>= 1)
 #pragma unroll
                         for (int p = 0; p < kVL / VPB; ++p) bmv[p] = fmaxf(bmv[p], __shfl_xor_sync(0xffffffffu, bmv[p], off));
-                    if (lane == 0) {
+                    float raw = -INFINITY;
 #pragma unroll
-                        for (int p = 0; p < kVL / VPB; ++p)
-                            if (p < nb) dst[p] = bound(bmv[p], p);
-                    }
+                    for (int p = 0; p < kVL / VPB; ++p)
+                        if (lane == p) raw = bmv[p];
+                    if (lane < nb) dst[lane] = bound(raw);
                 }
             }
-            // the warp's (m, s), then the chunk's record and note by the last warp
-            if (dosum) {
+            // at the row's last chunk: the warp's (m, s), then the row's record and its
+            // hand-over to the decision group by the last warp
+            const bool rec = dosum && mt.seg_end;
+            if (rec) {
+                float pm = m, ps = s;
+                if (!(pm > -INFINITY)) ps = 0.0f;
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) {
-                    const float mo = __shfl_xor_sync(0xffffffffu, m, off);
-                    const float so = __shfl_xor_sync(0xffffffffu, s, off);
-                    ms_merge(m, s, mo, so, P.sc);
+                    const float mo = __shfl_xor_sync(0xffffffffu, pm, off);
+                    const float so = __shfl_xor_sync(0xffffffffu, ps, off);
+                    ms_merge(pm, ps, mo, so, P.sc);
                 }
+                if (lane == 0) s_slot[st][warp] = SegSum{pm, ps};
+            }
+            if (mt.seg_end) {
+                m = -INFINITY;
+                s = 0.0f;
+                msc = 0.0f;
             }
             int last = 0;
             if (lane == 0) {
-                if (dosum) s_slot[st][warp] = SegSum{m, s};
                 __threadfence_block();
                 last = atomicAdd(&s_cnt[st], 1) == kCWarps - 1;
             }
             last = __shfl_sync(0xffffffffu, last, 0);
             if (last) {
                 __threadfence_block();
-                if (dosum) {
+                if (rec) {
                     const SegSum wp = lane < kCWarps ? s_slot[st][lane] : SegSum{-INFINITY, 0.0f};
                     float cm = wp.m, cs = wp.s;
 #pragma unroll
@@ -1119,7 +1178,7 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
                         const float so = __shfl_xor_sync(0xffffffffu, cs, off);
                         ms_merge(cm, cs, mo, so, P.sc);
                     }
-                    if (lane == 0) P.part[static_cast<size_t>(row) * P.nchunk + c] = SegSum{cm, cs};
+                    if (lane == 0) P.part[static_cast<size_t>(row) * P.nchunk] = SegSum{cm, cs};  // the row's one record
                 }
                 if (lane == 0) {
                     s_cnt[st] = 0;
@@ -1134,6 +1193,8 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
                     bool posted = false;
                     for (int it = 0; it < (1 << 22); ++it) {
                         if (*slot == 0u) {
+                            s_note_aux[idx % kNoteCap] = make_int2(mt.dnext, mt.pend);
+                            __threadfence_block();
                             *slot = static_cast<unsigned>(row) + 1u;
                             posted = true;
                             break;
@@ -1166,6 +1227,10 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
                 volatile unsigned* slot = &s_notes[rd % kNoteCap];
                 const unsigned v = *slot;
                 if (v != 0u) {
+                    __threadfence_block();
+                    const int2 aux = s_note_aux[rd % kNoteCap];
+                    S.ival[3] = aux.x;  // d_{j+1}
+                    S.nh = aux.y;       // its penalty flag (S.nh is reloaded before any sampling)
                     *slot = 0u;
                     got = static_cast<int>(v - 1u);
                     ++rd;
@@ -1189,7 +1254,9 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
             if (row == -2) break;
             if (row >= 0) {
                 __threadfence_block();  // the row's records, written by this CTA's streaming warps
-                group_row_event<BF16, GREEDY, SOFTCAP, PENALTY>(P, S, s_pkey, s_ppos, s_stg, s_keff, row / K1, row % K1);
+                const int dnext = S.ival[3], pend = S.nh;
+                group_row_event<BF16, GREEDY, SOFTCAP, PENALTY>(P, S, s_pkey, s_ppos, s_stg, s_keff, row / K1, row % K1,
+                                                                dnext, pend);
             }
             group_sync();
         }
