@@ -237,11 +237,10 @@ class Path:
         self.ws = sp.spec_verify_workspace(B, K, V, device)
         self.params = sp.VerifyParams(temperature=cfg.temperature, softcap=cfg.softcap, rep_penalty=cfg.rep_penalty,
                                       rep_window=cfg.rep_window, gate_enabled=cfg.gate, seed=cfg.sampler_seed)
-        # library kernels per step: spec_verify (one kernel at B <= 2048; else the streaming kernel
-        # and the per-sequence decision kernel, + the residual pass with dense q at T > 0), then
-        # spec_commit (append + index + next drafts) or, without n-gram drafts, spec_append
-        fused = cfg.B <= 2048
-        self.launches_per_step = (1 if fused else (3 if cfg.dense and cfg.temperature > 0 else 2)) + 1
+        # library kernels per step: spec_verify (the streaming kernel and the per-sequence decision
+        # kernel, + the residual pass with dense q at T > 0), then spec_commit (append + index +
+        # next drafts) or, without n-gram drafts, spec_append
+        self.launches_per_step = (3 if cfg.dense and cfg.temperature > 0 else 2) + 1
         self.g = g
 
     def _limits(self, s):
@@ -403,10 +402,10 @@ def verify_summary(path, peak, calls=60):
 # Workloads measured beside the headline (spec_verify alone, same process):
 # name -> (workload, what is timed, steps run first, gate forced open)
 SUB_WORKLOADS = {
-    "c5_split": ("c5", "c5 under the two-kernel schedule (streaming kernel, then one CTA per sequence)", 8,
-                 dict(schedule=2)),
-    "c5_early_exit": ("c5", "c5 with early exit: the rows past a known first rejection are not read (same outputs)",
-                      8, dict(early_exit=True)),
+    "c5_fused": ("c5", "c5 under the single-kernel schedule (whole rows per CTA, each row decided by the CTA "
+                       "that streamed it)", 8, dict(schedule=1)),
+    "c5_early_exit": ("c5", "c5, single-kernel schedule with early exit: the rows past a known first rejection "
+                            "are not read (same outputs)", 8, dict(schedule=1, early_exit=True)),
     "c3_gate_open": ("c3", "c3 with every sequence verifying its k drafts (gate forced open for the timing): the "
                            "soft-capped accept rows at V=262144", 8, dict(gate_enabled=False)),
     "c3_steady": ("c3", "c3 after 150 steps of the whole path with the EMA gate (tau 0.1, thr 0.5) as configured",
@@ -564,12 +563,10 @@ def run_ours(args):
         "roofline": {
             "bound": "hbm", "achieved": k1_achieved, "peak": peak, "unit": "GB/s", "frac": k1_achieved / peak,
             "traffic": traffic,
-            "kernel": ("verify_fused_kernel, spec_verify's one kernel at this batch size (streaming and the "
-                       "per-sequence decisions side by side)" if cfg.B <= 2048 else
-                       "verify_stream_kernel, the dominant kernel of spec_verify (the decision kernel and, with "
-                       "dense q, the residual pass follow it)") +
-                      "; 60 calls on rotating logit batches larger than L2 together, a CUDA event before each call "
-                      "and the library's marker event right after the (streaming) kernel",
+            "kernel": "verify_stream_kernel, the dominant kernel of spec_verify (the decision kernel and, with "
+                      "dense q, the residual pass follow it; the whole call is verify_us / verify_logits_gbs); "
+                      "60 calls on rotating logit batches larger than L2 together, a CUDA event before each call "
+                      "and the library's marker event right after the streaming kernel",
             "kernel_us": k1_s * 1e6,
             "rows_per_launch": v_rows,
             "peak_source": peak_src,

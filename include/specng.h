@@ -177,10 +177,15 @@ typedef struct {
 } specng_verify_params;
 
 /* Kernel schedules of spec_verify (the outputs are the same under each). */
-#define SPECNG_SCHEDULE_AUTO  0  /* FUSED when B <= SPECNG_FUSED_MAX_B, else SPLIT      */
-#define SPECNG_SCHEDULE_FUSED 1  /* one persistent kernel: streaming and the decisions
-                                    of the sequences side by side (B <= 2048)         */
-#define SPECNG_SCHEDULE_SPLIT 2  /* a streaming kernel, then one CTA per sequence      */
+#define SPECNG_SCHEDULE_AUTO  0  /* the two-kernel schedule (SPLIT)                     */
+#define SPECNG_SCHEDULE_FUSED 1  /* one persistent kernel (B <= 2048): every CTA streams
+                                    whole rows, row index first, and decides each row
+                                    it streamed as soon as it is streamed; the sequence
+                                    whose accept length that settles is sampled at once;
+                                    allows early exit                                  */
+#define SPECNG_SCHEDULE_SPLIT 2  /* a streaming kernel over all active rows, then one
+                                    CTA per sequence (accept tests, sample, epilogue),
+                                    + a residual pass for dense drafts at T > 0        */
 #define SPECNG_FUSED_MAX_B    2048
 
 /* Bytes of device workspace spec_verify needs for (B, K, V). */

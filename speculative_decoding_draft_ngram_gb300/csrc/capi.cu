@@ -381,7 +381,7 @@ int verify_setup(const char* who, const void* logits, int logits_dtype, int B, i
     P.kv_len = kv_len; P.ema = ema; P.out_tokens = out_tokens; P.out_accept = out_accept_len;
     P.status = status_ptr();
     P.diag = diag_ptr();
-    P.fused = (p.schedule == SPECNG_SCHEDULE_FUSED || (p.schedule == SPECNG_SCHEDULE_AUTO && B <= SPECNG_FUSED_MAX_B)) ? 1 : 0;
+    P.fused = p.schedule == SPECNG_SCHEDULE_FUSED ? 1 : 0;
     P.early_exit = P.fused ? p.early_exit : 0;
     P.epoch = next_epoch();
     flags[0] = bf16; flags[1] = greedy; flags[2] = softcap; flags[3] = penalty; flags[4] = dense;

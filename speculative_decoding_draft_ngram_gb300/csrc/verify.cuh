@@ -807,11 +807,12 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
 #pragma unroll
                     for (int p = 0; p < kVL / 2; ++p)
                         bw[p] = as_u32(__hmax2(as_bf162(bw[p]), as_bf162(__shfl_xor_sync(0xffffffffu, bw[p], off))));
-                if (lane == 0) {
+                // lane i < nb stores block i (every lane holds the warp-reduced maxima)
+                float raw = -INFINITY;
 #pragma unroll
-                    for (int i = 0; i < kVL; ++i)
-                        if (i < nb) dst[i] = (i & 1) ? bf16hi(bw[i >> 1]) : bf16lo(bw[i >> 1]);
-                }
+                for (int i = 0; i < kVL; ++i)
+                    if (lane == i) raw = (i & 1) ? bf16hi(bw[i >> 1]) : bf16lo(bw[i >> 1]);
+                if (lane < nb) dst[lane] = raw;
             } else {
                 float bm[kVL / VPB];
 #pragma unroll
@@ -824,11 +825,11 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
                 for (int off = 16; off > 0; off >>= 1)
 #pragma unroll
                     for (int p = 0; p < kVL / VPB; ++p) bm[p] = fmaxf(bm[p], __shfl_xor_sync(0xffffffffu, bm[p], off));
-                if (lane == 0) {
+                float raw = -INFINITY;
 #pragma unroll
-                    for (int p = 0; p < kVL / VPB; ++p)
-                        if (p < nb) dst[p] = bm[p];
-                }
+                for (int p = 0; p < kVL / VPB; ++p)
+                    if (lane == p) raw = bm[p];
+                if (lane < nb) dst[lane] = raw;
             }
         }
 

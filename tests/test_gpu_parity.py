@@ -109,11 +109,11 @@ def test_full_size_sampled(name):
 
 
 # The same cases under the other kernel schedule and with early exit: the
-# outputs must not depend on either (single kernel = the default for these
-# batch sizes; the two-kernel schedule; the single kernel skipping the rows
-# past a known first rejection).
+# outputs must not depend on either (the two-kernel schedule is the default;
+# the single kernel; the single kernel skipping the rows past a known first
+# rejection).
 SCHEDULES = {
-    "split": dict(schedule=sp.capi.SCHEDULE_SPLIT),
+    "fused": dict(schedule=sp.capi.SCHEDULE_FUSED),
     "early_exit": dict(schedule=sp.capi.SCHEDULE_FUSED, early_exit=True),
 }
 SCHED_CASES = ["c1", "c2_greedy", "c2_t06", "c3_softcap_gate", "c3_greedy_softcap", "c4_dense", "c4_dense_greedy",
@@ -129,15 +129,27 @@ def test_lockstep_schedules(name, sched):
     assert rep.steps == steps and rep.excused == 0, rep.notes
 
 
-def test_lockstep_batch_above_the_single_kernel_limit():
-    # B = 2100 > 2048 takes the two-kernel schedule under the default setting (dense
-    # drafts: an n-gram table holds at most 512 sequences)
+def test_lockstep_large_batch():
+    # B = 2100 sequences (dense drafts: an n-gram table holds at most 512 sequences)
     cfg = wl.get("c4", B=2100, K=2, V=1000, steps=3)
     rep = lockstep.run(cfg, 3, oracle_chunk=256)
     assert rep.steps == 3 and rep.excused == 0
 
 
-@pytest.mark.parametrize("name", ["c5_full", "c3_full"])
+def test_single_kernel_schedule_rejects_large_batches():
+    import torch
+    B, K, V = 2049, 1, 64
+    dev = "cuda"
+    p = sp.VerifyParams(temperature=1.0, gate_enabled=False, schedule=sp.capi.SCHEDULE_FUSED)
+    args = (torch.zeros((B, K + 1, V), device=dev), torch.zeros((B, K), dtype=torch.int32, device=dev), None,
+            torch.zeros(B, dtype=torch.int32, device=dev), None, None, p, torch.zeros(B, dtype=torch.int32, device=dev),
+            torch.ones(B, device=dev), torch.empty((B, K + 1), dtype=torch.int32, device=dev),
+            torch.empty(B, dtype=torch.int32, device=dev), sp.spec_verify_workspace(B, K, V))
+    with pytest.raises(sp.SpecngError, match="B <= 2048"):
+        sp.spec_verify(*args)
+
+
+@pytest.mark.parametrize("name", ["c5_full", "c3_full", "c4_full"])
 def test_full_size_sampled_early_exit(name):
     cfg, steps, sample = FULL[name]
     rep = lockstep.run_sampled(cfg, min(steps, 4), sample, early_exit=True, schedule=sp.capi.SCHEDULE_FUSED)
