@@ -126,6 +126,13 @@ int specng_ngram_create(specng_ngram** table, int B, int V, int64_t max_position
 /* Free the table (synchronises the device first).  NULL is accepted. */
 int specng_ngram_destroy(specng_ngram* table);
 
+/* Draft only on repeated evidence ([AX] note under the decode table:
+ * speculation "repeats n-gram evidence"): a context proposes its best
+ * continuation only when that continuation was seen at least min_count
+ * times (1, the default: any evidence).  A host-side setting of the table,
+ * read by ngram_draft and spec_commit.  min_count in [1, 2^22 - 1]. */
+int specng_ngram_set_min_count(specng_ngram* table, int min_count);
+
 /* Remove every entry and mark every sequence as not indexed (stream s). */
 int specng_ngram_reset(specng_ngram* table, cudaStream_t s);
 
@@ -174,6 +181,18 @@ typedef struct {
                                not read (single-kernel schedule only); the outputs
                                are the same, since those rows cannot change them   */
     int32_t  schedule;      /* SPECNG_SCHEDULE_*                                   */
+    /* Gate variants ([AX] "Performance Evidence & Results", note under the
+     * decode table: speculation "cools after partial acceptance"; the way a
+     * disabled gate opens again is left open by the page).  Both 0: the
+     * gate above alone, which stays shut once shut.                        */
+    int32_t  probe_interval;/* P > 0: a gated-off sequence verifies its drafts on
+                               the calls whose step is a multiple of P; that call
+                               updates the EMA and may open the gate again       */
+    int32_t  cool_steps;    /* C > 0: after a call with 0 < a < k_eff the sequence
+                               verifies no drafts for its next C calls            */
+    int32_t* gate_state;    /* device int32 [B], in/out: each sequence's remaining
+                               cooling calls (zero-fill before the first call);
+                               required when cool_steps > 0, else ignored         */
 } specng_verify_params;
 
 /* Kernel schedules of spec_verify (the outputs are the same under each). */
@@ -211,8 +230,10 @@ int spec_verify_workspace_init(void* workspace, size_t workspace_bytes, cudaStre
  * kv_len       int32 [B], in/out: on entry the KV length after the verify
  *              forward (committed + k[b] + 1); on exit kv_len - k[b] + a.
  * ema          fp32 [B], in/out: acceptance EMA.  Gate (when enabled):
- *              k_eff = ema >= thresh ? k : 0, read before the update; if
- *              k_eff > 0, ema <- (1 - tau) * ema + tau * a / k_eff.
+ *              k_eff = ema >= thresh ? k : 0, read before the update (a
+ *              probe step, see probe_interval, counts as open; a cooling
+ *              sequence, see cool_steps, has k_eff = 0); if k_eff > 0,
+ *              ema <- (1 - tau) * ema + tau * a / k_eff.
  * out_tokens   int32 [B, K+1]: d_1..d_a, then the residual or bonus sample,
  *              then -1.
  * out_accept_len int32 [B]: a.

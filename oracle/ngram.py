@@ -71,19 +71,26 @@ def extend_stats(stats: Tuple[Stats, Stats], tokens: Sequence[int], start: int, 
     return stats
 
 
-def best_continuation(conts: Dict[int, List[int]]):
-    """Most frequent continuation, latest occurrence breaking ties (None if empty)."""
+def best_continuation(conts: Dict[int, List[int]], min_count: int = 1):
+    """Most frequent continuation, latest occurrence breaking ties; None if there
+    is none or if it was seen fewer than ``min_count`` times."""
     best = None
     best_key = None
     for c, (count, last) in conts.items():
         key = (count, last)
         if best_key is None or key > best_key:
             best, best_key = c, key
+    if best_key is not None and best_key[0] < min_count:
+        return None
     return best
 
 
-def draft(tokens: Sequence[int], length: int, max_k: int, stats=None) -> List[int]:
-    """Chained trigram-then-bigram drafting of up to ``max_k`` tokens."""
+def draft(tokens: Sequence[int], length: int, max_k: int, stats=None, min_count: int = 1) -> List[int]:
+    """Chained trigram-then-bigram drafting of up to ``max_k`` tokens.
+
+    ``min_count`` (reading of the AX Engine page's note under the decode table:
+    speculation "repeats n-gram evidence"): a context drafts only a
+    continuation seen at least that many times; 1 drafts on any evidence."""
     if stats is None:
         stats = continuation_stats(tokens, length)
     tri, bi = stats
@@ -92,9 +99,9 @@ def draft(tokens: Sequence[int], length: int, max_k: int, stats=None) -> List[in
     while len(out) < max_k and len(ctx) >= 1:
         nxt = None
         if len(ctx) >= 2 and (ctx[-2], ctx[-1]) in tri:
-            nxt = best_continuation(tri[(ctx[-2], ctx[-1])])
+            nxt = best_continuation(tri[(ctx[-2], ctx[-1])], min_count)
         if nxt is None and ctx[-1] in bi:
-            nxt = best_continuation(bi[ctx[-1]])
+            nxt = best_continuation(bi[ctx[-1]], min_count)
         if nxt is None:
             break
         out.append(nxt)
@@ -102,7 +109,7 @@ def draft(tokens: Sequence[int], length: int, max_k: int, stats=None) -> List[in
     return out
 
 
-def draft_batch(history, lens, max_k: int, k_limit=None, stats=None, fallback=None):
+def draft_batch(history, lens, max_k: int, k_limit=None, stats=None, fallback=None, min_count: int = 1):
     """Drafts for every sequence: (drafts [B, max_k] padded with -1, counts [B]).
 
     ``stats`` optionally holds each sequence's statistics of its whole
@@ -116,7 +123,7 @@ def draft_batch(history, lens, max_k: int, k_limit=None, stats=None, fallback=No
     counts = np.zeros(B, dtype=np.int64)
     for b in range(B):
         kb = max_k if k_limit is None else max(0, min(max_k, int(k_limit[b])))
-        d = draft(history[b], int(lens[b]), kb, None if stats is None else stats[b])
+        d = draft(history[b], int(lens[b]), kb, None if stats is None else stats[b], min_count)
         if fallback is not None:
             d = d + [int(t) for t in fallback[b, len(d):kb]]
         drafts[b, :len(d)] = d

@@ -71,6 +71,8 @@ class VerifyParams:
     gate_enabled: bool = True
     seed: int = 0
     step: int = 0
+    probe_interval: int = 0   # > 0: a gated-off sequence verifies on calls with step % interval == 0
+    cool_steps: int = 0       # > 0: after a partial acceptance, no drafts for this many calls
 
     def f64(self, name: str) -> float:
         return float(np.float32(getattr(self, name)))
@@ -133,13 +135,41 @@ def log_softmax(y: np.ndarray) -> np.ndarray:
 
 # ---------------------------------------------------------------- rules
 
-def gate_k(k: np.ndarray, ema: np.ndarray, params: VerifyParams) -> np.ndarray:
-    """k_eff = k when the gate is disabled or ema >= threshold, else 0."""
+def gate_k(k: np.ndarray, ema: np.ndarray, params: VerifyParams, cool=None) -> np.ndarray:
+    """Drafts verified this call.
+
+    EMA gate (AX Engine page, "Core Technical Architecture & Methods":
+    speculation is disabled when the acceptance EMA drops below the
+    threshold): k_eff = k when the gate is disabled or ema >= threshold,
+    else 0.  Variants (same page, "Performance Evidence & Results", note
+    under the decode table: speculation "cools after partial acceptance";
+    and the re-opening of a disabled gate, which the page leaves open):
+      * re-probe: with probe_interval P > 0, a gated-off sequence verifies
+        its drafts anyway on the calls whose step is a multiple of P (the
+        update of that call can re-open the gate);
+      * cooling: a sequence whose cooling count (``cool``) is positive
+        verifies no drafts this call, whatever the gate says.
+    """
     k = np.asarray(k, dtype=np.int64)
-    if not params.gate_enabled:
-        return k
-    on = np.asarray(ema, dtype=np.float64) >= params.f64("ema_thresh")
-    return np.where(on, k, 0)
+    keff = k
+    if params.gate_enabled:
+        on = np.asarray(ema, dtype=np.float64) >= params.f64("ema_thresh")
+        if params.probe_interval > 0 and int(params.step) % int(params.probe_interval) == 0:
+            on = np.ones_like(on)
+        keff = np.where(on, k, 0)
+    if cool is not None and params.cool_steps > 0:
+        keff = np.where(np.asarray(cool) > 0, 0, keff)
+    return keff
+
+
+def cool_update(cool, a, k_eff, params: VerifyParams):
+    """Cooling count after a call: a cooling sequence counts down; otherwise a
+    partial acceptance (0 < a < k_eff) starts cool_steps calls without drafts."""
+    cool = np.asarray(cool, dtype=np.int64)
+    a = np.asarray(a, dtype=np.int64)
+    k_eff = np.asarray(k_eff, dtype=np.int64)
+    partial = (a > 0) & (a < k_eff)
+    return np.where(cool > 0, cool - 1, np.where(partial, int(params.cool_steps), 0))
 
 
 def accept_draft(u, p_d, q_d):
@@ -180,7 +210,7 @@ def ema_update(ema: np.ndarray, a: np.ndarray, k_eff: np.ndarray, params: Verify
 # ---------------------------------------------------------------- one call
 
 def spec_verify(logits, drafts, draft_probs, k, history, lens, params: VerifyParams,
-                kv_len, ema, seq_ids=None):
+                kv_len, ema, seq_ids=None, gate_state=None):
     """One verify call over a batch; returns outputs plus diagnostics.
 
     logits       [B, K+1, V]  target logits (any float dtype, widened to fp64)
@@ -190,6 +220,7 @@ def spec_verify(logits, drafts, draft_probs, k, history, lens, params: VerifyPar
     history      [B, Lcap], lens [B]: for the repetition-penalty window
     kv_len [B], ema [B]: state before the call
     seq_ids      [B]          the sequence ids that key the noise (default 0..B-1)
+    gate_state   [B] or None  cooling counts before the call (used when cool_steps > 0)
 
     Returns a dict with out_tokens [B, K+1], accept_len [B], kv_len [B],
     ema [B] (fp64), k_eff [B] and the margins used by the parity harness:
@@ -206,7 +237,8 @@ def spec_verify(logits, drafts, draft_probs, k, history, lens, params: VerifyPar
     greedy = T == 0.0
     dense = draft_probs is not None
 
-    k_eff = gate_k(k, ema, params)
+    cool = np.zeros(B, dtype=np.int64) if gate_state is None else np.asarray(gate_state, dtype=np.int64)
+    k_eff = gate_k(k, ema, params, cool if params.cool_steps > 0 else None)
     z = transform_rows(logits, params, history, lens, drafts)
     rows = np.arange(B)
 
@@ -276,6 +308,7 @@ def spec_verify(logits, drafts, draft_probs, k, history, lens, params: VerifyPar
     ema_new = ema_update(ema, a, k_eff, params)
     thresh = params.f64("ema_thresh")
     return {
+        "gate_state": cool_update(cool, a, k_eff, params) if params.cool_steps > 0 else cool,
         "out_tokens": out,
         "accept_len": a,
         "kv_len": np.asarray(kv_len, dtype=np.int64) - k + a,

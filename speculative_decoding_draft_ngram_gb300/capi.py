@@ -34,6 +34,7 @@ STATUS_BITS = {
 # Every symbol include/specng.h declares.
 EXPORTED = (
     "specng_ngram_create", "specng_ngram_destroy", "specng_ngram_reset", "specng_ngram_capacity",
+    "specng_ngram_set_min_count",
     "ngram_update", "ngram_draft", "spec_verify_workspace_bytes", "spec_verify_workspace_init",
     "spec_verify", "spec_verify_noalloc", "spec_append", "spec_commit", "specng_get_status", "specng_strerror",
     "specng_last_error", "specng_philox4x32_10", "specng_set_verify_marker", "specng_get_counters",
@@ -62,6 +63,9 @@ class VerifyParamsC(ctypes.Structure):
         ("step", ctypes.c_uint64),
         ("early_exit", ctypes.c_int32),
         ("schedule", ctypes.c_int32),
+        ("probe_interval", ctypes.c_int32),
+        ("cool_steps", ctypes.c_int32),
+        ("gate_state", ctypes.c_void_p),
     ]
 
 
@@ -82,12 +86,19 @@ class VerifyParams:
     step: int = 0
     early_exit: bool = False      # skip the rows past a known first rejection (same outputs)
     schedule: int = SCHEDULE_AUTO
+    probe_interval: int = 0       # gate variant: re-probe a gated-off sequence every this many steps
+    cool_steps: int = 0           # gate variant: no drafts for this many calls after a partial acceptance
+    gate_state: Optional[torch.Tensor] = None  # int32 [B] cooling counts (in/out), needed with cool_steps
 
     def to_c(self) -> VerifyParamsC:
+        gs = None
+        if self.gate_state is not None:
+            gs = _ptr(self.gate_state, torch.int32, "gate_state").value
         return VerifyParamsC(self.temperature, self.softcap, self.rep_penalty, int(self.rep_window),
                              self.ema_tau, self.ema_thresh, 1 if self.gate_enabled else 0, 0,
                              int(self.seed) & 0xFFFFFFFFFFFFFFFF, int(self.step) & 0xFFFFFFFFFFFFFFFF,
-                             1 if self.early_exit else 0, int(self.schedule))
+                             1 if self.early_exit else 0, int(self.schedule), int(self.probe_interval),
+                             int(self.cool_steps), gs)
 
 
 _lib = None
@@ -112,6 +123,7 @@ def load() -> ctypes.CDLL:
         "specng_ngram_destroy": (I, [P]),
         "specng_ngram_reset": (I, [P, P]),
         "specng_ngram_capacity": (I, [P, ctypes.POINTER(I64)]),
+        "specng_ngram_set_min_count": (I, [P, I]),
         "ngram_update": (I, [P, I64, P, P, P]),
         "ngram_draft": (I, [P, P, I64, P, I, P, P, P, P, P]),
         "spec_verify_workspace_bytes": (SZ, [I, I, I]),
@@ -182,6 +194,10 @@ class NgramTable:
 
     def reset(self):
         _check(load().specng_ngram_reset(self._h, _stream(self.device)), "specng_ngram_reset")
+
+    def set_min_count(self, min_count: int):
+        """Draft only continuations seen at least min_count times (1: any)."""
+        _check(load().specng_ngram_set_min_count(self._h, int(min_count)), "specng_ngram_set_min_count")
 
     def close(self):
         if self._h is not None and self._h.value:

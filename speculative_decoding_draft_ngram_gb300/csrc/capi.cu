@@ -96,7 +96,7 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 struct WsLayout {
     size_t part, bmax, blkws, rowres, seqres, part2, tickets, total;
     size_t row_thr, seq_ticket2;
-    size_t row_tix, seq_state, ema_new, grid_tix;
+    size_t row_tix, seq_state, ema_new, cool_new, grid_tix;
 };
 
 // The f32 chunks are the smaller ones, so their counts bound both dtypes.
@@ -119,6 +119,7 @@ WsLayout ws_layout(int B, int K, int V) {
     L.row_tix = off;    off = align256(off + rows * sizeof(unsigned long long));
     L.seq_state = off;  off = align256(off + static_cast<size_t>(B) * sizeof(unsigned long long));
     L.ema_new = off;    off = align256(off + static_cast<size_t>(B) * sizeof(float));
+    L.cool_new = off;   off = align256(off + static_cast<size_t>(B) * sizeof(int32_t));
     L.tickets = off;
     L.row_thr = off;      off += rows * sizeof(unsigned);
     L.seq_ticket2 = off;  off += static_cast<size_t>(B) * sizeof(unsigned);
@@ -225,6 +226,7 @@ int specng_ngram_create(specng_ngram** table, int B, int V, int64_t max_position
     t->dev.B = B;
     t->dev.V = V;
     t->dev.status = status_ptr();
+    t->dev.min_count = 1;
     e = launch_ngram_clear(t->dev, s);
     if (e != cudaSuccess) {
         cudaFree(mem);
@@ -250,6 +252,14 @@ int specng_ngram_reset(specng_ngram* table, cudaStream_t s) {
     const cudaError_t e = launch_ngram_clear(table->dev, s);
     if (e != cudaSuccess) return fail_cuda(e, "specng_ngram_reset");
     table->parity = 0;
+    return SPECNG_OK;
+}
+
+int specng_ngram_set_min_count(specng_ngram* table, int min_count) {
+    if (table == nullptr) return fail(SPECNG_EINVAL, "specng_ngram_set_min_count: table is NULL");
+    if (min_count < 1 || min_count > (1 << 22) - 1)
+        return fail(SPECNG_EINVAL, "specng_ngram_set_min_count: min_count outside [1, 2^22 - 1]");
+    table->dev.min_count = static_cast<uint64_t>(min_count);
     return SPECNG_OK;
 }
 
@@ -336,6 +346,9 @@ int verify_setup(const char* who, const void* logits, int logits_dtype, int B, i
     if (p.schedule == SPECNG_SCHEDULE_FUSED && B > SPECNG_FUSED_MAX_B)
         return bad(SPECNG_EINVAL, "the single-kernel schedule takes B <= 2048");
     if (p.early_exit != 0 && p.early_exit != 1) return bad(SPECNG_EINVAL, "early_exit must be 0 or 1");
+    if (p.probe_interval < 0) return bad(SPECNG_EINVAL, "probe_interval must be >= 0");
+    if (p.cool_steps < 0) return bad(SPECNG_EINVAL, "cool_steps must be >= 0");
+    if (p.cool_steps > 0 && p.gate_state == nullptr) return bad(SPECNG_EINVAL, "cool_steps > 0 needs gate_state");
     const bool penalty = p.rep_penalty != 1.0f && p.rep_window > 0;
     if (penalty && (history == nullptr || lens == nullptr || hist_stride < 1))
         return bad(SPECNG_EINVAL, "history, lens and hist_stride are needed for the penalty");
@@ -376,6 +389,10 @@ int verify_setup(const char* who, const void* logits, int logits_dtype, int B, i
     P.nk.k0 = static_cast<uint32_t>(p.seed);
     P.nk.k1 = static_cast<uint32_t>(p.seed >> 32);
     P.nk.step = static_cast<uint32_t>(p.step);
+    P.probe = p.probe_interval;
+    P.probe_now = p.probe_interval > 0 && p.step % static_cast<uint64_t>(p.probe_interval) == 0 ? 1 : 0;
+    P.cool = p.cool_steps;
+    P.gate_state = p.cool_steps > 0 ? p.gate_state : nullptr;
     P.nk.seq = 0;
     P.aligned = aligned16(logits) && (V % epv == 0) && (!dense || (aligned16(draft_probs) && V % 4 == 0));
     P.kv_len = kv_len; P.ema = ema; P.out_tokens = out_tokens; P.out_accept = out_accept_len;
@@ -402,6 +419,7 @@ void attach_workspace(VerifyDev& P, void* workspace) {
     P.row_tix = reinterpret_cast<unsigned long long*>(ws + L.row_tix);
     P.seq_state = reinterpret_cast<unsigned long long*>(ws + L.seq_state);
     P.ema_new = reinterpret_cast<float*>(ws + L.ema_new);
+    P.cool_new = reinterpret_cast<int32_t*>(ws + L.cool_new);
     P.grid_tix = reinterpret_cast<unsigned*>(ws + L.grid_tix);
 }
 

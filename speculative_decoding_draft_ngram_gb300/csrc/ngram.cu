@@ -211,8 +211,8 @@ __device__ void draft_one(const NgramDev& T, int b, const int32_t* h, int L, int
     while (n < kmax && c1 >= 0) {
         int tok = -1;
         uint64_t v;
-        if (c2 >= 0 && find_value(T.tri_ctx, T.mask, key_tri_ctx(b, c2, c1), &v)) tok = best_token(v);
-        if (tok < 0 && find_value(T.bi_ctx, T.mask, key_bi_ctx(b, c1), &v)) tok = best_token(v);
+        if (c2 >= 0 && find_value(T.tri_ctx, T.mask, key_tri_ctx(b, c2, c1), &v)) tok = best_token_if(v, T.min_count);
+        if (tok < 0 && find_value(T.bi_ctx, T.mask, key_bi_ctx(b, c1), &v)) tok = best_token_if(v, T.min_count);
         if (tok < 0) break;
         out[n++] = tok;
         c2 = c1;
@@ -248,8 +248,9 @@ __device__ void draft_warp(const NgramDev& T, int b, const int32_t* h, int L, in
     while (n < kmax && c1 >= 0) {  // warp-uniform
         int tok = -1;
         uint64_t v;
-        if (lane == 0 && c2 >= 0 && find_value(T.tri_ctx, T.mask, key_tri_ctx(b, c2, c1), &v)) tok = best_token(v);
-        if (lane == 1 && find_value(T.bi_ctx, T.mask, key_bi_ctx(b, c1), &v)) tok = best_token(v);
+        if (lane == 0 && c2 >= 0 && find_value(T.tri_ctx, T.mask, key_tri_ctx(b, c2, c1), &v))
+            tok = best_token_if(v, T.min_count);
+        if (lane == 1 && find_value(T.bi_ctx, T.mask, key_bi_ctx(b, c1), &v)) tok = best_token_if(v, T.min_count);
         const int tt = __shfl_sync(0xffffffffu, tok, 0), tb = __shfl_sync(0xffffffffu, tok, 1);
         tok = tt >= 0 ? tt : tb;
         if (tok < 0) break;

@@ -35,6 +35,7 @@ struct NgramDev {
     int32_t* indexed[2];      // per-sequence indexed length, double-buffered
     int B, V;
     unsigned* status;
+    uint64_t min_count;       // a context drafts only a best continuation seen this often (>= 1)
 };
 
 __device__ __forceinline__ uint64_t key_tri_pair(uint64_t b, uint64_t t2, uint64_t t1, uint64_t c) {
@@ -54,6 +55,10 @@ __device__ __forceinline__ uint64_t pack_best(uint64_t count, uint64_t last, uin
     return (count << 42) | (last << 18) | token;
 }
 __device__ __forceinline__ int best_token(uint64_t v) { return static_cast<int>(v & 0x3FFFFull); }
+// The best continuation's token when its count reaches min_count, else -1.
+__device__ __forceinline__ int best_token_if(uint64_t v, uint64_t min_count) {
+    return (v >> 42) >= min_count ? best_token(v) : -1;
+}
 
 // Slot holding key (inserted if absent), or -1 when the table is full.
 __device__ __forceinline__ int64_t find_or_insert(ulonglong2* tab, uint64_t mask, uint64_t key) {

@@ -107,6 +107,12 @@ struct VerifyDev {
     uint32_t epoch;                 // this call's tag, in [1, 2^31)
     int early_exit;                 // rows past a known first rejection are not streamed
     int fused;                      // 1: single-kernel schedule
+    // gate variants
+    int probe;                      // re-probe interval (0: none)
+    int probe_now;                  // this call's step is a multiple of it
+    int cool;                       // cooling calls after a partial acceptance (0: none)
+    int32_t* gate_state;            // [B] cooling counts, in/out (NULL when cool == 0)
+    int32_t* cool_new;              // [B] single-kernel schedule: updated counts, copied by the last CTA
 };
 
 // Count one run of a rarely taken exact path (see SPECNG_DIAG_*).
@@ -312,6 +318,23 @@ struct WindowView {
     }
 };
 
+// Drafts verified this call for a sequence with kb drafts, acceptance EMA ema
+// and cooling count cool: the EMA gate (shut below the threshold, except on a
+// re-probe step), then no drafts while cooling.
+__device__ __forceinline__ int gate_rule(const VerifyDev& P, int kb, float ema, int cool) {
+    int ke = kb;
+    if (P.gate && kb > 0 && !(ema >= P.thresh) && !P.probe_now) ke = 0;
+    if (P.cool > 0 && cool > 0) ke = 0;
+    return ke;
+}
+
+// Cooling count after the call: a cooling sequence counts down; a partial
+// acceptance (0 < a < k_eff) starts P.cool calls without drafts.
+__device__ __forceinline__ int cool_after(const VerifyDev& P, int cool, int a, int keff) {
+    if (cool > 0) return cool - 1;
+    return (a > 0 && a < keff) ? P.cool : 0;
+}
+
 __device__ __forceinline__ int gate_keff(const VerifyDev& P, int b, int* kb_out, bool flag) {
     int kb = P.k[b];
     if (kb < 0 || kb > P.K) {
@@ -319,8 +342,7 @@ __device__ __forceinline__ int gate_keff(const VerifyDev& P, int b, int* kb_out,
         kb = kb < 0 ? 0 : P.K;
     }
     if (kb_out) *kb_out = kb;
-    if (P.gate && kb > 0 && !(P.ema[b] >= P.thresh)) return 0;
-    return kb;
+    return gate_rule(P, kb, P.gate ? P.ema[b] : 1.0f, P.gate_state ? P.gate_state[b] : 0);
 }
 
 // Slack of the block bound: covers the fp32 rounding of z / T and ln M.
@@ -532,7 +554,7 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
         // ================= producer =================
         constexpr int kHW = PENALTY ? SPECNG_MAX_REP_WINDOW / 32 : 1;
         struct SeqData {
-            int k, draft, L;
+            int k, draft, L, cool;
             float ema;
             int hw[kHW];
         };
@@ -542,6 +564,7 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
         auto fetch = [&](int bq, int L, SeqData& d) {  // issues the loads; nothing waits here
             d.k = bq < P.B ? P.k[bq] : 0;
             d.ema = (P.gate && bq < P.B) ? P.ema[bq] : 1.0f;
+            d.cool = (P.gate_state != nullptr && bq < P.B) ? P.gate_state[bq] : 0;
             d.draft = (bq < P.B && lane < P.K) ? P.drafts[bq * P.K + lane] : -1;
             d.L = L;
             if constexpr (PENALTY) {
@@ -558,7 +581,7 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
         auto install = [&](const SeqData& d) {
             int kb = d.k;
             if (kb < 0 || kb > P.K) kb = kb < 0 ? 0 : P.K;
-            keff = (P.gate && kb > 0 && !(d.ema >= P.thresh)) ? 0 : kb;
+            keff = gate_rule(P, kb, d.ema, d.cool);
             if (lane < keff) s_pdrafts[lane] = d.draft;
             if constexpr (PENALTY) {
                 nh = d.L < P.W ? d.L : P.W;
@@ -1450,6 +1473,7 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
     if (tid == 0) {
         P.out_accept[b] = a;
         P.kv_len[b] = P.kv_len[b] - kb + a;
+        if (P.gate_state != nullptr) P.gate_state[b] = cool_after(P, P.gate_state[b], a, keff);
         if (keff > 0) {
             // (1 - tau) * ema + tau * a / k_eff, rounded step by step (no contraction)
             const double tau = static_cast<double>(P.tau);

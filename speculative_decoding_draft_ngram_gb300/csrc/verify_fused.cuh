@@ -33,9 +33,9 @@
 //     streamed it) and writes the sequence's outputs.
 //   * early exit (optional): the producer skips the chunks of rows past a
 //     sequence's known first rejection; they cannot change the outputs.
-//   * the last CTA to finish (a grid ticket) writes the EMAs: every CTA
-//     reads them at its start to plan the work, so none may change before all
-//     have finished.
+//   * the last CTA to finish (a grid ticket) writes the EMAs and the cooling
+//     counts: every CTA reads them at its start to plan the work, so none may
+//     change before all have finished.
 // No CTA ever waits for another: the cross-CTA steps are tickets.  Every
 // wait inside a CTA (ring barriers, the note ring, the group's poll) is
 // bounded and raises TIMEOUT when it gives up.
@@ -692,6 +692,7 @@ __device__ __noinline__ void group_row_event(const VerifyDev& P, DShared& S, int
             en = static_cast<float>(__dadd_rn(__dmul_rn(1.0 - tau, static_cast<double>(en)), __dmul_rn(tau, rate)));
         }
         P.ema_new[b] = en;
+        if (P.gate_state != nullptr) P.cool_new[b] = cool_after(P, __ldcg(P.gate_state + b), a, keff);
     }
     group_sync();
 }
@@ -1272,8 +1273,10 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
     __syncthreads();
     if (s_last) {
         __threadfence();
-        for (int b = tid; b < P.B; b += kFThreads)
+        for (int b = tid; b < P.B; b += kFThreads) {
             if (s_keff[b] > 0) P.ema[b] = __ldcg(P.ema_new + b);
+            if (P.gate_state != nullptr) P.gate_state[b] = __ldcg(P.cool_new + b);
+        }
         if (tid == 0) *P.grid_tix = 0u;
     }
 }

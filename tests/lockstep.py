@@ -42,17 +42,21 @@ class Report:
     notes: list = field(default_factory=list)
 
 
-def _oracle_params(cfg: wl.Config, T: float, step: int, seed: int) -> ov.VerifyParams:
+GATE_KEYS = ("probe_interval", "cool_steps")
+
+
+def _oracle_params(cfg: wl.Config, T: float, step: int, seed: int, **var) -> ov.VerifyParams:
     return ov.VerifyParams(temperature=T, softcap=cfg.softcap, rep_penalty=cfg.rep_penalty,
-                           rep_window=cfg.rep_window, gate_enabled=cfg.gate, seed=seed, step=step)
+                           rep_window=cfg.rep_window, gate_enabled=cfg.gate, seed=seed, step=step,
+                           **{k: v for k, v in var.items() if k in GATE_KEYS})
 
 
-def _gpu_params(cfg: wl.Config, T: float, step: int, seed: int, **sched) -> sp.VerifyParams:
+def _gpu_params(cfg: wl.Config, T: float, step: int, seed: int, **var) -> sp.VerifyParams:
     return sp.VerifyParams(temperature=T, softcap=cfg.softcap, rep_penalty=cfg.rep_penalty,
-                           rep_window=cfg.rep_window, gate_enabled=cfg.gate, seed=seed, step=step, **sched)
+                           rep_window=cfg.rep_window, gate_enabled=cfg.gate, seed=seed, step=step, **var)
 
 
-def oracle_verify(logits, drafts, q, k, hist, lens, params, kv, ema, chunk=16):
+def oracle_verify(logits, drafts, q, k, hist, lens, params, kv, ema, chunk=16, gate_state=None):
     """The oracle's verify over the batch, in chunks of sequences (same result)."""
     B = logits.shape[0]
     parts = []
@@ -60,7 +64,8 @@ def oracle_verify(logits, drafts, q, k, hist, lens, params, kv, ema, chunk=16):
         hi = min(B, lo + chunk)
         parts.append(ov.spec_verify(logits[lo:hi].astype(np.float64), drafts[lo:hi],
                                     None if q is None else q[lo:hi], k[lo:hi], hist[lo:hi], lens[lo:hi],
-                                    params, kv[lo:hi], ema[lo:hi], seq_ids=np.arange(lo, hi)))
+                                    params, kv[lo:hi], ema[lo:hi], seq_ids=np.arange(lo, hi),
+                                    gate_state=None if gate_state is None else gate_state[lo:hi]))
     return {key: np.concatenate([p[key] for p in parts]) for key in parts[0]}
 
 
@@ -192,9 +197,12 @@ def run_sampled(cfg: wl.Config, steps: int, sample: int, T: float | None = None,
 
 
 def run(cfg: wl.Config, steps: int, T: float | None = None, device="cuda", seed: int | None = None,
-        oracle_chunk: int = 16, ema0: float = 1.0, **sched) -> Report:
+        oracle_chunk: int = 16, ema0: float = 1.0, min_count: int = 1, **sched) -> Report:
     """Run ``steps`` lockstep steps of cfg; raise AssertionError on a parity failure.
-    ``sched``: schedule / early_exit of the GPU calls (the outputs must not depend on them)."""
+    ``sched``: schedule / early_exit of the GPU calls (the outputs must not depend on
+    them) and the gate variants probe_interval / cool_steps (on both sides; the
+    cooling counts are compared bit-exact every step); ``min_count``: the n-gram
+    evidence threshold of the drafts (both sides)."""
     T = cfg.temperature if T is None else T
     seed = cfg.sampler_seed if seed is None else seed
     rep = Report()
@@ -213,9 +221,14 @@ def run(cfg: wl.Config, steps: int, T: float | None = None, device="cuda", seed:
     stats = None
     if use_ngram:
         table = sp.NgramTable(B, V, B * cfg.hist_cap, device=device)
+        if min_count != 1:
+            table.set_min_count(min_count)
         sp.ngram_update(table, hist_g, lens_g)
         stats = [on.continuation_stats(hist_o[b], int(lens_o[b])) for b in range(B)]
     ws = sp.spec_verify_workspace(B, K, V, device)
+    cooling = sched.get("cool_steps", 0) > 0
+    cool_o = np.zeros(B, dtype=np.int64)
+    cool_g = torch.zeros(B, dtype=torch.int32, device=device) if cooling else None
     out_tok = torch.empty((B, K + 1), dtype=torch.int32, device=device)
     out_acc = torch.empty((B,), dtype=torch.int32, device=device)
     g = wl._gen(cfg.data_seed + 1, "cpu")
@@ -230,7 +243,7 @@ def run(cfg: wl.Config, steps: int, T: float | None = None, device="cuda", seed:
         # ---- drafts
         if use_ngram:
             d_o, k_o = on.draft_batch(hist_o, lens_o, K, k_limit=limits.numpy(), stats=stats,
-                                      fallback=None if fb is None else fb.numpy())
+                                      fallback=None if fb is None else fb.numpy(), min_count=min_count)
             d_g, k_g = sp.ngram_draft(table, hist_g, lens_g, K, k_limit=limits.to(device),
                                       fallback=None if fb is None else fb.to(device))
             d_g_h, k_g_h = d_g.cpu().numpy(), k_g.cpu().numpy()
@@ -249,9 +262,11 @@ def run(cfg: wl.Config, steps: int, T: float | None = None, device="cuda", seed:
         # ---- verify on both sides
         res = oracle_verify(logits.float().numpy(), drafts.numpy().astype(np.int64),
                             None if q is None else q.numpy(), k.numpy().astype(np.int64), hist_o, lens_o,
-                            _oracle_params(cfg, T, step, seed), kv_o, ema_o.astype(np.float32), oracle_chunk)
+                            _oracle_params(cfg, T, step, seed, **sched), kv_o, ema_o.astype(np.float32), oracle_chunk,
+                            gate_state=cool_o)
         sp.spec_verify(logits.to(device), drafts.to(device), None if q is None else q.to(device), k.to(device),
-                       hist_g, lens_g, _gpu_params(cfg, T, step, seed, **sched), kv_g, ema_g, out_tok, out_acc, ws)
+                       hist_g, lens_g, _gpu_params(cfg, T, step, seed, gate_state=cool_g, **sched), kv_g, ema_g,
+                       out_tok, out_acc, ws)
         a_g = out_acc.cpu().numpy()
         t_g = out_tok.cpu().numpy()
         kv_gh = kv_g.cpu().numpy()
@@ -265,6 +280,9 @@ def run(cfg: wl.Config, steps: int, T: float | None = None, device="cuda", seed:
         rep.drafted += int(k_eff.sum())
         rep.gated += int(((k.numpy() > 0) & (k_eff == 0)).sum())
         bad = compare(step, a_g, t_g, kv_gh, ema_gh, res, rep)
+        if cooling:
+            assert np.array_equal(cool_g.cpu().numpy(), res["gate_state"]), f"step {step}: cooling counts differ"
+            cool_o = res["gate_state"]
         # ---- commit: both sides append their own tokens
         sp.spec_append(hist_g, lens_g, out_tok, out_acc)
         for b in range(B):

@@ -154,3 +154,29 @@ def test_full_size_sampled_early_exit(name):
     cfg, steps, sample = FULL[name]
     rep = lockstep.run_sampled(cfg, min(steps, 4), sample, early_exit=True, schedule=sp.capi.SCHEDULE_FUSED)
     assert rep.excused == 0, rep.notes
+
+
+# Gate variants (re-probe, cooling after a partial acceptance) and drafts on
+# repeated n-gram evidence, on both schedules: GPU against the oracle, the
+# cooling counts bit-exact every step.
+VARIANTS = {
+    "c3_probe_cool": (wl.get("c3", B=6, V=V_SMALL, hist_len=(64, 700), steps=30), 30, None,
+                      dict(probe_interval=4, cool_steps=2)),
+    "c3_probe_low_rho": (wl.get("c3", B=8, V=8000, hist_len=(64, 400), boost_prob=(0.0, 0.3), steps=30), 30, None,
+                         dict(probe_interval=3)),
+    "c5_cool": (wl.get("c5", B=7, V=V_SMALL, hist_len=(1500, 1500), steps=12), 12, None, dict(cool_steps=3)),
+    "c2_cool_greedy": (wl.get("c2", V=V_SMALL, hist_len=(512, 512), steps=16), 16, 0.0, dict(cool_steps=1)),
+    "c1_min_count": (wl.get("c1"), 40, None, dict(min_count=2)),
+    "c5_min_count": (wl.get("c5", B=7, V=V_SMALL, hist_len=(1500, 1500), steps=8), 8, None, dict(min_count=2)),
+}
+
+
+@pytest.mark.parametrize("sched", ["split", "fused"])
+@pytest.mark.parametrize("name", list(VARIANTS))
+def test_lockstep_gate_variants(name, sched):
+    cfg, steps, T, var = VARIANTS[name]
+    extra = {} if sched == "split" else dict(schedule=sp.capi.SCHEDULE_FUSED)
+    rep = lockstep.run(cfg, steps, T=T, **var, **extra)
+    assert rep.steps == steps and rep.excused == 0, rep.notes
+    if "probe_interval" in var:
+        assert rep.gated > 0

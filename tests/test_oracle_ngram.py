@@ -121,3 +121,19 @@ def test_fallback_fills_the_positions_after_the_first_miss():
     # without a fallback the chain just stops
     d, n = ngram.draft_batch(h, lens, 4, stats=stats)
     assert list(d[0]) == [2, 3, -1, -1] and int(n[0]) == 2
+
+
+def test_min_count_needs_repeated_evidence():
+    # "repeats n-gram evidence": a context drafts only a continuation seen at least
+    # min_count times (worked by hand)
+    h = [1, 2, 3, 1, 2, 4, 1, 2]          # (1, 2) -> 3 once, 4 once; 2 -> 3 once, 4 once
+    assert ngram.draft(h, len(h), 2) == [4, 1]
+    assert ngram.draft(h, len(h), 2, min_count=2) == []
+    h = [1, 2, 3, 1, 2, 3, 1, 2]          # (1, 2) -> 3 twice, (2, 3) -> 1 twice, (3, 1) -> 2 twice
+    assert ngram.draft(h, len(h), 4, min_count=2) == [3, 1, 2, 3]
+    assert ngram.draft(h, len(h), 4, min_count=3) == []
+    # the trigram context fails the threshold, the bigram context passes it
+    h = [5, 1, 2, 9, 1, 2, 7, 3, 2, 7, 1, 2]  # (1, 2) -> 9 once, 7 once; 2 -> 9, 7, 7: 7 twice
+    assert ngram.draft(h, len(h), 1, min_count=2) == [7]
+    d, n = ngram.draft_batch(np.array([h]), np.array([len(h)]), 1, min_count=2)
+    assert list(d[0]) == [7] and int(n[0]) == 1

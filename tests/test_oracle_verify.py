@@ -187,3 +187,62 @@ def test_invalid_draft_is_rejected():
                          np.zeros(1, int), VerifyParams(temperature=1.0, gate_enabled=False), np.zeros(1),
                          np.ones(1))
     assert res["accept_len"][0] == 0 and 0 <= res["out_tokens"][0, 0] < 8
+
+
+def _gate_golden():
+    with open(os.path.join(GOLDEN, "gate_variants.json")) as f:
+        return json.load(f)
+
+
+def test_gate_reprobe_golden():
+    """Re-probing a gated-off sequence every P calls (hand-derived trajectories)."""
+    g = _gate_golden()
+    for sc in g["probe"]:
+        p = VerifyParams(ema_tau=g["tau"], ema_thresh=g["threshold"], probe_interval=sc["probe_interval"])
+        ema = np.array([g["ema0"]])
+        seen = []
+        for step, rate in enumerate(sc["acceptance_rates"]):
+            p.step = step
+            k_eff = ov.gate_k(np.array([g["k"]]), ema, p)
+            seen.append(int(k_eff[0]))
+            ema = ov.ema_update(ema, np.array([round(rate * k_eff[0])]), k_eff, p)
+        assert seen == sc["expected_k_eff"], (sc, seen)
+
+
+def test_gate_cooling_golden():
+    """No drafts for C calls after a partial acceptance (hand-derived trajectory)."""
+    g = _gate_golden()
+    for sc in g["cooling"]:
+        p = VerifyParams(ema_tau=g["tau"], ema_thresh=g["threshold"], cool_steps=sc["cool_steps"])
+        ema, cool = np.array([g["ema0"]]), np.array([0])
+        seen, cools = [], []
+        for acc in sc["accepted_when_verifying"]:
+            k_eff = ov.gate_k(np.array([g["k"]]), ema, p, cool)
+            seen.append(int(k_eff[0]))
+            a = np.array([acc if k_eff[0] > 0 else 0])
+            ema = ov.ema_update(ema, a, k_eff, p)
+            cool = ov.cool_update(cool, a, k_eff, p)
+            cools.append(int(cool[0]))
+        assert seen == sc["expected_k_eff"] and cools == sc["expected_cool_after"], (seen, cools)
+
+
+def test_gate_variants_through_spec_verify():
+    """The variants inside one whole call: a cooling sequence verifies nothing and
+    counts down, a probe step opens a gated-off sequence, the rest as before."""
+    rng = np.random.default_rng(12)
+    B, K, V = 4, 3, 16
+    logits = rng.normal(size=(B, K + 1, V)) * 2
+    drafts = rng.integers(0, V, (B, K))
+    ema = np.array([0.2, 0.2, 0.9, 0.9], dtype=np.float32)
+    cool = np.array([0, 3, 1, 0])
+    for step, probe in ((8, True), (9, False)):
+        p = VerifyParams(temperature=1.0, gate_enabled=True, seed=3, step=step, probe_interval=4, cool_steps=2)
+        res = ov.spec_verify(logits, drafts, None, np.full(B, K), np.zeros((B, 1), int), np.zeros(B, int), p,
+                             np.full(B, 50), ema, gate_state=cool)
+        want = np.array([K if probe else 0, 0, 0, K])
+        np.testing.assert_array_equal(res["k_eff"], want)
+        assert res["gate_state"][1] == 2 and res["gate_state"][2] == 0
+        a = res["accept_len"]
+        np.testing.assert_array_equal(res["kv_len"], 50 - K + a)
+        part = (a > 0) & (a < want)
+        np.testing.assert_array_equal(res["gate_state"][[0, 3]], np.where(part, 2, 0)[[0, 3]])
