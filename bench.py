@@ -56,6 +56,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sub", action="store_true", help="skip the other workloads' verify timings")
+    ap.add_argument("--schedule", default="split", choices=["split", "fused"],
+                    help="spec_verify's kernel schedule in the timed loop (default: the library's default)")
+    ap.add_argument("--early-exit", action="store_true", help="single-kernel schedule only: early exit")
     ap.add_argument("--cpu-sample", type=int, default=0, help="sequences in the oracle sample (0: auto)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (smaller profiler captures only)")
@@ -447,6 +450,10 @@ def run_ours(args):
     e2e_steps = 0 if args.no_e2e else min(args.steps, 200)
     path = Path(args.workload, 2 * total_steps + e2e_steps + 8, dev, seed_offset=rank, batch=args.batch)
     cfg = path.cfg
+    if args.schedule == "fused":
+        path.params.schedule = 1
+        path.params.early_exit = bool(args.early_exit)
+        path.launches_per_step = 2
     stream = torch.cuda.current_stream(dev)
 
     # ---- device-resident timed loop
@@ -550,6 +557,7 @@ def run_ours(args):
         "data": "synthetic",
         "config": {
             "workload": f"{args.workload}: {DESCR[args.workload]}",
+            "schedule": args.schedule + (" + early exit" if args.early_exit else ""),
             "B": cfg.B, "K": cfg.K, "V": cfg.V, "logits_dtype": cfg.dtype,
             "l2": f"inputs larger than L2: {path.n_sets} rotating logit batches of {path.set_bytes / 1e6:.0f} MB",
             "parallelism": f"dp{ws} (independent sequences per GPU)",
