@@ -380,6 +380,7 @@ int verify_setup(const char* who, const void* logits, int logits_dtype, int B, i
     P.Td = static_cast<double>(p.temperature);
     P.cap = softcap ? p.softcap : 0.0f;
     P.invcap = softcap ? 1.0f / p.softcap : 0.0f;
+    P.cap2l = softcap ? 2.0f * kLog2e / p.softcap : 0.0f;
     P.rep = p.rep_penalty;
     P.invrep = 1.0f / p.rep_penalty;
     P.W = penalty ? p.rep_window : 0;

@@ -1056,8 +1056,8 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
                             unpack<BF16>(rv[i], x);
 #pragma unroll
                             for (int e = 0; e < EPV; e += 2) {
-                                const float2 tt = __ffma2_rn(make_float2(transform_f32<SOFTCAP, false>(x[e], false, P),
-                                                                         transform_f32<SOFTCAP, false>(x[e + 1], false, P)),
+                                const float2 tt = __ffma2_rn(make_float2(sum_transform<SOFTCAP>(x[e], P),
+                                                                         sum_transform<SOFTCAP>(x[e + 1], P)),
                                                              sc2, nm2);
                                 acc2[i & 3] = __fadd2_rn(acc2[i & 3], make_float2(ex2_approx(tt.x), ex2_approx(tt.y)));
                             }
@@ -1079,8 +1079,8 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
                             const int bit = __ffsll(static_cast<long long>(pw)) - 1;
                             pw &= pw - 1ull;
                             const float xe = elem_of_stage<BF16>(stage, off0 + (bit >> 3) * 32 * EPV + (bit & 7));
-                            const float zu = transform_f32<SOFTCAP, false>(xe, false, P);
-                            const float zp = transform_f32<SOFTCAP, true>(xe, true, P);
+                            const float zu = sum_transform<SOFTCAP>(xe, P);
+                            const float zp = sum_transform_pen<SOFTCAP>(xe, P);
                             if ((zp - m) * P.sc > 32.0f) {
                                 s = m > -INFINITY ? s * ex2_approx((m - zp) * P.sc) : 0.0f;
                                 m = zp;
