@@ -77,6 +77,10 @@ extern "C" {
 #define SPECNG_DEV_TIMEOUT        0x80u /* a bounded wait for a bulk copy gave up; the call's
                                            outputs are incomplete and its workspace must be
                                            zeroed again (spec_verify_workspace_init)         */
+#define SPECNG_DEV_CHECKED_OOB   0x100u /* checked build only (compiled with SPECNG_CHECKED):
+                                           a computed index (vocabulary id, history position,
+                                           draft slot, logit element) fell outside its array;
+                                           it was clamped into range, nothing trapped        */
 
 /* Limits checked on the host. */
 #define SPECNG_MAX_K          16        /* drafts per sequence per call            */

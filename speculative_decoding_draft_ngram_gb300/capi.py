@@ -14,7 +14,10 @@ from typing import Optional
 
 import torch
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspecng.so")
+# The library to load: libspecng.so next to this file, or the build named by
+# SPECNG_LIBRARY (e.g. libspecng_checked.so, the index-checked build).
+_LIB_PATH = os.environ.get("SPECNG_LIBRARY") or os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                                                              "libspecng.so")
 
 SPECNG_OK = 0
 SPECNG_F32 = 0
@@ -29,6 +32,7 @@ STATUS_BITS = {
     0x20: "COUNT_SAT",
     0x40: "HIST_SHRANK",
     0x80: "TIMEOUT",
+    0x100: "CHECKED_OOB",
 }
 
 # Every symbol include/specng.h declares.

@@ -14,6 +14,29 @@ __device__ __forceinline__ void raise_status(unsigned* status, unsigned bit) {
     if (status != nullptr) atomicOr(status, bit);
 }
 
+// ---------------------------------------------------------------- checked build
+// Compiled with SPECNG_CHECKED, every index that is computed from data (a
+// vocabulary id, a history position, a draft slot, a logit element) is
+// checked against its array before use: one outside [0, n) sets
+// CHECKED_OOB and is clamped into range, so the access stays inside the
+// array and nothing traps.  In the normal build chk() returns its argument.
+#ifdef SPECNG_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+
+template <typename I>
+__device__ __forceinline__ I chk(I idx, I n, unsigned* status) {
+    if constexpr (kChecked) {
+        if (idx < I(0) || idx >= n) {
+            raise_status(status, SPECNG_DEV_CHECKED_OOB);
+            return idx < I(0) ? I(0) : (n > I(0) ? n - I(1) : I(0));
+        }
+    }
+    return idx;
+}
+
 // ---------------------------------------------------------------- launch chaining
 // Programmatic dependent launch (sm_90+): a kernel launched with the
 // programmatic-serialisation attribute may start before the previous kernel

@@ -116,6 +116,21 @@ struct VerifyDev {
     int32_t* cool_new;              // [B] single-kernel schedule: updated counts, copied by the last CTA
 };
 
+// Checked-build accessors (plain accesses in the normal build).
+__device__ __forceinline__ size_t chk_row(const VerifyDev& P, size_t row) {
+    return chk<size_t>(row, static_cast<size_t>(P.B) * (P.K + 1), P.status);
+}
+__device__ __forceinline__ int chk_id(const VerifyDev& P, int v) { return chk<int>(v, P.V, P.status); }
+// History token at position pos of sequence b.
+__device__ __forceinline__ int hist_at(const VerifyDev& P, int b, int64_t pos) {
+    return P.hist[static_cast<size_t>(chk<int>(b, P.B, P.status)) * P.hist_stride +
+                  chk<int64_t>(pos, P.hist_stride, P.status)];
+}
+// Draft d_{j+1} of sequence b.
+__device__ __forceinline__ int draft_at(const VerifyDev& P, int b, int j) {
+    return P.drafts[static_cast<size_t>(chk<int>(b, P.B, P.status)) * P.K + chk<int>(j, P.K, P.status)];
+}
+
 // Count one run of a rarely taken exact path (see SPECNG_DIAG_*).
 __device__ __forceinline__ void count_diag(const VerifyDev& P, int which) {
     if (P.diag != nullptr) atomicAdd(P.diag + which, 1u);
@@ -151,6 +166,21 @@ __device__ __forceinline__ uint4 load_vec(const char* rowp, int e0, int v1, bool
         }
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <bool BF16>
+__device__ __forceinline__ double raw_logit_f64(const void* logits, size_t row, int V, int id);
+// Raw logit id of row `row`, index-checked in the checked build.
+template <bool BF16>
+__device__ __forceinline__ double raw_logit_chk(const VerifyDev& P, size_t row, int id) {
+    return raw_logit_f64<BF16>(P.logits, chk_row(P, row), P.V, chk_id(P, id));
+}
+// Vector load of row elements e0.. below v1 (see load_vec), e0 checked in the checked build.
+template <bool BF16>
+__device__ __forceinline__ uint4 load_vec(const char* rowp, int e0, int v1, bool aligned);
+template <bool BF16>
+__device__ __forceinline__ uint4 load_vec_chk(const VerifyDev& P, const char* rowp, int e0, int v1) {
+    return load_vec<BF16>(rowp, chk<int>(e0, v1, P.status), v1, P.aligned);
 }
 
 template <bool BF16>
@@ -591,14 +621,14 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
             d.k = bq < P.B ? P.k[bq] : 0;
             d.ema = (P.gate && bq < P.B) ? P.ema[bq] : 1.0f;
             d.cool = (P.gate_state != nullptr && bq < P.B) ? P.gate_state[bq] : 0;
-            d.draft = (bq < P.B && lane < P.K) ? P.drafts[bq * P.K + lane] : -1;
+            d.draft = (bq < P.B && lane < P.K) ? draft_at(P, bq, lane) : -1;
             d.L = L;
             if constexpr (PENALTY) {
                 const int nh = L < P.W ? L : P.W;
 #pragma unroll
                 for (int i = 0; i < kHW; ++i) {
                     const int t = lane + 32 * i;
-                    d.hw[i] = (bq < P.B && t < nh) ? P.hist[static_cast<size_t>(bq) * P.hist_stride + (L - nh) + t] : 0;
+                    d.hw[i] = (bq < P.B && t < nh) ? hist_at(P, bq, (L - nh) + t) : 0;
                 }
             }
         };
@@ -1018,7 +1048,7 @@ __device__ __noinline__ int rescore_top2_f64(const VerifyDev& P, const NoiseKey&
     double sc[2];
     for (int h = 0; h < 2; ++h) {
         const int id = h == 0 ? i1 : i2;
-        const double z = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, id), h == 0 ? pen1 : pen2, P);
+        const double z = transform_f64<SOFTCAP, PENALTY>(raw_logit_chk<BF16>(P, row, id), h == 0 ? pen1 : pen2, P);
         sc[h] = z / P.Td - log(noise_exp_f64(nk, static_cast<uint32_t>(id), static_cast<uint32_t>(a)));
     }
     return better64(sc[1], i2, sc[0], i1) ? i2 : i1;
@@ -1071,7 +1101,7 @@ __device__ __noinline__ void prepare_row(const VerifyDev& P, const NoiseKey& nk,
 #pragma unroll
         for (int u = 0; u < VPL; ++u) {
             const int e0 = qs * BLK + (u * 32 + lane) * EPV;
-            rs[u] = e0 < P.V ? load_vec<BF16>(rowp, e0, P.V, P.aligned) : make_uint4(0u, 0u, 0u, 0u);
+            rs[u] = e0 < P.V ? load_vec_chk<BF16>(P, rowp, e0, P.V) : make_uint4(0u, 0u, 0u, 0u);
         }
     }
     // block draws and bounds
@@ -1149,7 +1179,7 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
     nk.seq = static_cast<uint32_t>(b);
     int nh = 0;
     if (tid < keff) {
-        const int d = P.drafts[b * P.K + tid];
+        const int d = draft_at(P, b, tid);
         s_d[tid] = d;
         if (!(d >= 0 && d < P.V)) raise_status(P.status, SPECNG_DEV_TOKEN_OOR);
     }
@@ -1198,7 +1228,7 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
 #pragma unroll
         for (int u = 0; u < VPL; ++u) {
             const int e0 = q * BLK + (u * 32 + lane) * EPV;
-            r[u] = e0 < P.V ? load_vec<BF16>(rowp, e0, P.V, P.aligned) : make_uint4(0u, 0u, 0u, 0u);
+            r[u] = e0 < P.V ? load_vec_chk<BF16>(P, rowp, e0, P.V) : make_uint4(0u, 0u, 0u, 0u);
         }
     };
     auto elem_id = [&](int q, int k) { return q * BLK + ((k / EPV) * 32 + lane) * EPV + (k % EPV); };
@@ -1266,9 +1296,9 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
             if (t.i2 >= 0 && t.s2 >= t.s1 - cand_delta(t.s1)) {
                 if (lane == 0) {
                     count_diag(P, SPECNG_DIAG_GREEDY_F64);
-                    const double z1 = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, t.i1),
+                    const double z1 = transform_f64<SOFTCAP, PENALTY>(raw_logit_chk<BF16>(P, row, t.i1),
                                                                       PENALTY && pen_of(t.i1, j), P);
-                    const double z2 = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, t.i2),
+                    const double z2 = transform_f64<SOFTCAP, PENALTY>(raw_logit_chk<BF16>(P, row, t.i2),
                                                                       PENALTY && pen_of(t.i2, j), P);
                     if (better64(z2, t.i2, z1, t.i1)) y = t.i2;
                 }
@@ -1287,8 +1317,8 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
             double u = 0.0;
             bool pend = false;
             if (lane == 0 && dv) {
-                xd = static_cast<float>(raw_logit_f64<BF16>(P.logits, row, P.V, d));
-                if (dense) qdf = P.q[(static_cast<size_t>(b) * P.K + j) * P.V + d];
+                xd = static_cast<float>(raw_logit_chk<BF16>(P, row, d));
+                if (dense) qdf = P.q[(static_cast<size_t>(b) * P.K + j) * P.V + chk_id(P, d)];
                 // the draw and the window test need no load: they run while the loads are in flight
                 u = accept_uniform_f64(nk, static_cast<uint32_t>(j + 1));
                 pend = pen_of(d, j);
@@ -1421,7 +1451,7 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
 #pragma unroll
                 for (int u = 0; u < VPL; ++u) {
                     const int e0 = qh[h] * BLK + (u * 32 + lane) * EPV;
-                    r[h * VPL + u] = (qh[h] >= 0 && e0 < P.V) ? load_vec<BF16>(rowp, e0, P.V, P.aligned)
+                    r[h * VPL + u] = (qh[h] >= 0 && e0 < P.V) ? load_vec_chk<BF16>(P, rowp, e0, P.V)
                                                                : make_uint4(0u, 0u, 0u, 0u);
                 }
             // screening thresholds (a penalty below 1 may raise a value: then every
@@ -1565,7 +1595,7 @@ __device__ __forceinline__ void build_window(const VerifyDev& P, int b, int j, i
     int tok = -1;
     if (tid < nw) {
         const int idx = start + tid;
-        tok = idx < L ? P.hist[static_cast<size_t>(b) * P.hist_stride + idx] : P.drafts[b * P.K + (idx - L)];
+        tok = idx < L ? hist_at(P, b, idx) : draft_at(P, b, idx - L);
         s_win[tid] = tok;
     }
     if (tid == 0) *s_nwin = nw;
@@ -1601,7 +1631,7 @@ __device__ __noinline__ int sample_p_row(const VerifyDev& P, const NoiseKey& nk,
         const BlockNoise bn = block_noise(nk, static_cast<uint32_t>(q), static_cast<uint32_t>(a));
         for (int e0 = q * BLK + lane * EPV; e0 < min(P.V, (q + 1) * BLK); e0 += 32 * EPV) {
             float x[EPV];
-            unpack<BF16>(load_vec<BF16>(rowp, e0, P.V, P.aligned), x);
+            unpack<BF16>(load_vec_chk<BF16>(P, rowp, e0, P.V), x);
 #pragma unroll
             for (int e = 0; e < EPV; ++e) {
                 const int v = e0 + e;
@@ -1631,7 +1661,7 @@ __device__ __noinline__ int sample_p_row(const VerifyDev& P, const NoiseKey& nk,
         double sc[2];
         for (int h = 0; h < 2; ++h) {
             const int id = h == 0 ? tw.i1 : tw.i2;
-            const double z = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, id),
+            const double z = transform_f64<SOFTCAP, PENALTY>(raw_logit_chk<BF16>(P, row, id),
                                                              PENALTY && pen(id), P);
             sc[h] = z / P.Td - log(noise_exp_f64(nk, static_cast<uint32_t>(id), static_cast<uint32_t>(a)));
         }
@@ -1684,7 +1714,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const __gr
 #pragma unroll
     for (int i = 0; i < kNV; ++i) {
         const int e0 = v0 + (i * kThreads + tid) * EPV;
-        rv[i] = e0 < v1 ? load_vec<BF16>(rowp, e0, v1, P.aligned) : make_uint4(0u, 0u, 0u, 0u);
+        rv[i] = e0 < v1 ? load_vec_chk<BF16>(P, rowp, e0, v1) : make_uint4(0u, 0u, 0u, 0u);
     }
     auto lp_of = [&](float x, bool pen) { return transform_f32<SOFTCAP, PENALTY>(x, pen, P) * P.invT - lse_f; };
     auto pen_at = [&](int off) -> unsigned {
@@ -1779,7 +1809,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const __gr
         const bool in = idx < nq;
         const int loc = in ? static_cast<int>(qw[idx]) : 0;
         const int v = v0 + loc;
-        const float x = in ? static_cast<float>(raw_logit_f64<BF16>(P.logits, row, P.V, v)) : 0.0f;
+        const float x = in ? static_cast<float>(raw_logit_chk<BF16>(P, row, v)) : 0.0f;
         const float qv = in ? __ldcs(qrow + v) : 0.0f;
         const bool pen = PENALTY && ((s_bm[loc >> 5] >> (loc & 31)) & 1u);
         const BlockNoise bn = s_bn[loc >> kNoiseBlockShift];
@@ -1841,7 +1871,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const __gr
         // above the fp32 error of either); otherwise both are re-scored in fp64
         float dres = 0.0f;
         if (lane == 0 && t.i1 >= 0) {
-            const float x1 = static_cast<float>(raw_logit_f64<BF16>(P.logits, row, P.V, t.i1));
+            const float x1 = static_cast<float>(raw_logit_chk<BF16>(P, row, t.i1));
             dres = lp_of(x1, pen1) - logf(__ldcg(qrow + t.i1));
         }
         if (lane == 0) {
@@ -1858,7 +1888,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const __gr
                 const int id = h == 0 ? t.i1 : t.i2;
                 if (id < 0) continue;
                 if (h == 1 && !(t.s2 >= t.s1 - cand_delta(t.s1))) continue;
-                const double z = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, id),
+                const double z = transform_f64<SOFTCAP, PENALTY>(raw_logit_chk<BF16>(P, row, id),
                                                                  h == 0 ? pen1 : pen2, P);
                 const double rsd = exp(z / P.Td - lse) - static_cast<double>(qrow[id]);
                 if (!(rsd > 0.0)) continue;

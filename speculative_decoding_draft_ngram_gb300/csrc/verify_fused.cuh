@@ -200,7 +200,7 @@ __device__ __noinline__ int group_argmax(const VerifyDev& P, DShared& S, const i
 #pragma unroll
         for (int u = 0; u < VPL; ++u) {
             const int e0 = q * BLK + (u * 32 + lane) * EPV;
-            r[u] = e0 < P.V ? load_vec<BF16>(rowp, e0, P.V, P.aligned) : make_uint4(0u, 0u, 0u, 0u);
+            r[u] = e0 < P.V ? load_vec_chk<BF16>(P, rowp, e0, P.V) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
         for (int u = 0; u < VPL; ++u) {
@@ -264,8 +264,8 @@ __device__ __noinline__ int group_argmax(const VerifyDev& P, DShared& S, const i
         int y = tw.i1;
         if (tw.i2 >= 0 && tw.s2 >= tw.s1 - cand_delta(tw.s1)) {
             count_diag(P, SPECNG_DIAG_GREEDY_F64);
-            const double z1 = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, tw.i1), pen_of(tw.i1), P);
-            const double z2 = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, tw.i2), pen_of(tw.i2), P);
+            const double z1 = transform_f64<SOFTCAP, PENALTY>(raw_logit_chk<BF16>(P, row, tw.i1), pen_of(tw.i1), P);
+            const double z2 = transform_f64<SOFTCAP, PENALTY>(raw_logit_chk<BF16>(P, row, tw.i2), pen_of(tw.i2), P);
             if (better64(z2, tw.i2, z1, tw.i1)) y = tw.i2;
         }
         S.ival[0] = y;
@@ -318,7 +318,7 @@ __device__ __noinline__ int group_sample(const VerifyDev& P, DShared& S, const i
     const float off = DENSE ? lse_f : 0.0f;  // block bounds of the residual: minus lse
     // exact residual score of id v in fp64 (the row's exact normaliser), -inf for a zero residual
     auto exact_residual_score = [&](int v) -> double {
-        const double z = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, v), pen_of(v), P);
+        const double z = transform_f64<SOFTCAP, PENALTY>(raw_logit_chk<BF16>(P, row, v), pen_of(v), P);
         const double rsd = exp(z / P.Td - lse64) - static_cast<double>(qrow[v]);
         if (!(rsd > 0.0)) return -INFINITY;
         return log(rsd) - log(noise_exp_f64(nk, static_cast<uint32_t>(v), static_cast<uint32_t>(a)));
@@ -370,7 +370,7 @@ __device__ __noinline__ int group_sample(const VerifyDev& P, DShared& S, const i
 #pragma unroll
             for (int u = 0; u < VPL; ++u) {
                 const int e0 = qs[h] * BLK + (u * 32 + lane) * EPV;
-                r[h * VPL + u] = (qs[h] >= 0 && e0 < P.V) ? load_vec<BF16>(rowp, e0, P.V, P.aligned)
+                r[h * VPL + u] = (qs[h] >= 0 && e0 < P.V) ? load_vec_chk<BF16>(P, rowp, e0, P.V)
                                                            : make_uint4(0u, 0u, 0u, 0u);
             }
         int myq = -1;
@@ -449,7 +449,7 @@ __device__ __noinline__ int group_sample(const VerifyDev& P, DShared& S, const i
 #pragma unroll
                 for (int u = 0; u < VPL; ++u) {
                     const int e0 = qh[h] * BLK + (u * 32 + lane) * EPV;
-                    r[h * VPL + u] = (qh[h] >= 0 && e0 < P.V) ? load_vec<BF16>(rowp, e0, P.V, P.aligned)
+                    r[h * VPL + u] = (qh[h] >= 0 && e0 < P.V) ? load_vec_chk<BF16>(P, rowp, e0, P.V)
                                                                : make_uint4(0u, 0u, 0u, 0u);
                 }
             // the batch's block draws, lane h for block h, while the loads are in flight
@@ -538,7 +538,7 @@ __device__ __noinline__ int group_sample(const VerifyDev& P, DShared& S, const i
             // the order of the two may turn on the fp32 normaliser's own error (about
             // 1e-6), which is amplified by 1 / (1 - q / p) near p = q: the caller
             // computes the row's exact normaliser and samples again in fp64 (-2)
-            const float x1 = static_cast<float>(raw_logit_f64<BF16>(P.logits, row, P.V, tw.i1));
+            const float x1 = static_cast<float>(raw_logit_chk<BF16>(P, row, tw.i1));
             const float dres = transform_f32<SOFTCAP, PENALTY>(x1, pen_of(tw.i1), P) * P.invT - lse_f - logf(qrow[tw.i1]);
             if (close || !(dres > 1e-4f)) y = -2;
         } else {
@@ -564,7 +564,7 @@ __device__ __noinline__ double group_exact_lse(const VerifyDev& P, DShared& S, c
     double acc = 0.0;
     for (int v = gt; v < P.V; v += kFDThreads) {
         const bool pen = PENALTY && pen_lookup(pkey, ppos, S.d, S.nh, P.W, v, a);
-        const double z = transform_f64<SOFTCAP, PENALTY>(raw_logit_f64<BF16>(P.logits, row, P.V, v), pen, P);
+        const double z = transform_f64<SOFTCAP, PENALTY>(raw_logit_chk<BF16>(P, row, v), pen, P);
         acc += exp(z / P.Td - m);
     }
     acc = warp_sum_f64(acc);
@@ -592,7 +592,7 @@ __device__ __noinline__ void group_row_event(const VerifyDev& P, DShared& S, int
     // ---- the row's test (T > 0) or argmax (T = 0)
     int acc = 0;
     if constexpr (GREEDY) {
-        if (gt < P.K) S.d[gt] = P.drafts[static_cast<size_t>(b) * P.K + gt];
+        if (gt < P.K) S.d[gt] = draft_at(P, b, gt);
         group_sync();
         group_load_seq<PENALTY>(P, S, pkey, ppos, b, gt);
         const int y = group_argmax<BF16, SOFTCAP, PENALTY>(P, S, pkey, ppos, b, j);
@@ -616,8 +616,8 @@ __device__ __noinline__ void group_row_event(const VerifyDev& P, DShared& S, int
             {
                 const int d = dnext;
                 if (d >= 0 && d < P.V) {
-                    const float xd = static_cast<float>(raw_logit_f64<BF16>(P.logits, row, P.V, d));
-                    const float qdf = dense ? P.q[(static_cast<size_t>(b) * P.K + j) * P.V + d] : 1.0f;
+                    const float xd = static_cast<float>(raw_logit_chk<BF16>(P, row, d));
+                    const float qdf = dense ? P.q[(static_cast<size_t>(b) * P.K + j) * P.V + chk_id(P, d)] : 1.0f;
                     const double u = accept_uniform_f64(nk, static_cast<uint32_t>(j + 1));
                     const float lsef = mf * P.invT + logf(Sf);
                     const float lp = transform_f32<SOFTCAP, PENALTY>(xd, pend != 0, P) * P.invT - lsef;
@@ -655,7 +655,7 @@ __device__ __noinline__ void group_row_event(const VerifyDev& P, DShared& S, int
     if (a < 0) return;
     // ---- the token at row a, then the outputs
     if constexpr (!GREEDY) {
-        if (gt < P.K) S.d[gt] = P.drafts[static_cast<size_t>(b) * P.K + gt];
+        if (gt < P.K) S.d[gt] = draft_at(P, b, gt);
         group_sync();
         group_load_seq<PENALTY>(P, S, pkey, ppos, b, gt);
     }
@@ -809,7 +809,7 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
             it.j = j;
             it.b = s_ord[t - s_off[j]];
             it.L = PENALTY ? P.lens[it.b] : 0;
-            it.draft = lane < P.K ? P.drafts[static_cast<size_t>(it.b) * P.K + lane] : -1;
+            it.draft = lane < P.K ? draft_at(P, it.b, lane) : -1;
             it.st = (P.early_exit && j > 0) ? __ldcg(P.seq_state + it.b) : 0ull;
         };
         // the history tail of the penalty window (first used one row later)
@@ -822,7 +822,7 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
 #pragma unroll
                 for (int i = 0; i < kHW; ++i) {
                     const int t = lane + 32 * i;
-                    it.hw[i] = t < nh ? P.hist[static_cast<size_t>(it.b) * P.hist_stride + (L - nh) + t] : 0;
+                    it.hw[i] = t < nh ? hist_at(P, it.b, (L - nh) + t) : 0;
                 }
             }
         };
