@@ -44,7 +44,8 @@ __host__ __device__ constexpr int noise_blocks(int V) { return (V + (1 << kNoise
 
 // Workspace records.
 struct __align__(8) SegSum {
-    float m, s;  // reference (transformed units) and sum of exp((z - m) / T) of a row segment
+    float m, s;  // reference (transformed units) and sum of exp((z - m) / T) of a row segment;
+                 // s < 0: the segment holds a value that proves the row's accept test rejects
 };
 struct __align__(32) Partial {
     float m, s;
@@ -324,6 +325,15 @@ __device__ __forceinline__ uint32_t as_u32(__nv_bfloat162 h) { return *reinterpr
 __device__ __forceinline__ __nv_bfloat162 bf16x8_max2(const uint4& r) {
     return __hmax2(__hmax2(as_bf162(r.x), as_bf162(r.y)), __hmax2(as_bf162(r.z), as_bf162(r.w)));
 }
+// The same with NaN propagated (a NaN element makes its half NaN).
+__device__ __forceinline__ __nv_bfloat162 bf16x8_max2_nan(const uint4& r) {
+    return __hmax2_nan(__hmax2_nan(as_bf162(r.x), as_bf162(r.y)), __hmax2_nan(as_bf162(r.z), as_bf162(r.w)));
+}
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+    float y;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b));
+    return y;
+}
 
 // Bit e set when element e of the vector is >= the (packed) threshold t: the
 // high byte of each compared half is gathered with byte permutes, and the four
@@ -460,6 +470,16 @@ __device__ __forceinline__ uint4 mask_tail(uint4 r, int n) {
 //     a segment reference (so the sum does not wait for each chunk's maximum);
 //     at the last chunk of a row segment the warps combine their sums into one
 //     record.
+//   * Rejection proofs (point-mass drafts): the producer gives every accept row
+//     the threshold thr = z_d - T ln u + T mg (z_d: the draft's transformed
+//     logit, read one sequence ahead, taken at its larger penalty value; u: the
+//     test's draw; mg: a margin over fp32 error).  The log-normaliser is at
+//     least z / T for every value z of the row, so a value z >= thr proves
+//     ln p(d) < ln u: the test rejects and the row's sum is not needed.  A warp
+//     that meets such a value (its lane maxima, taken at their smaller penalty
+//     value) stops adding exponentials for the rest of the segment, and the
+//     segment's record says so (s < 0).  Dense drafts keep every sum (the
+//     residual needs the rejected row's normaliser).
 
 constexpr int kCWarps = 16;                    // streaming warps
 constexpr int kPWarp = kCWarps;                // producer warp index
@@ -481,6 +501,7 @@ struct StageMeta {
     int b, j, c;
     int seg_end;   // the last chunk of this row in the CTA's range
     int sum;       // the row's softmax sum is needed (accept test)
+    float thr;     // rejection-proof threshold of the row's accept test (+inf: none)
     unsigned penw; // bit w: warp w's slice holds a penalised id
     int dnext;     // single-kernel schedule: d_{j+1} of the row (-1: none)
     int pend;      // single-kernel schedule: d_{j+1} is in the row's penalty window
@@ -492,25 +513,29 @@ struct SumState {
     float m, s, msc;
 };
 
-// Cold paths of the streaming warps, kept out of line so the hot loop stays
-// small in the instruction cache; both read the lane's vectors back from the
-// stage.  sum_from_stage: the lane's chunk against reference msc (after the
-// reference was raised).  sum_partial: a row's last chunk, element by
-// element with the exact transform, for vectors that pass the row's end.
-template <bool BF16, bool SOFTCAP>
-__device__ __noinline__ float sum_from_stage(const uint4* stage, int vec0, float msc, const VerifyDev& P) {
-    constexpr int EPV = ElemTraits<BF16>::EPV;
-    float add = 0.0f;
-#pragma unroll 1
-    for (int i = 0; i < kVL; ++i) {
-        float x[EPV];
-        unpack<BF16>(stage[vec0 + i * 32], x);
+// Element bit = 8 i + e of a lane's vectors rv[i] (register selects; taken
+// only for the few penalised elements of a slice).
+template <bool BF16>
+__device__ __forceinline__ float elem_of_regs(const uint4 (&rv)[kVL], int bit) {
+    const int i = bit >> 3, e = bit & 7;
+    uint4 r = rv[0];
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) add += ex2_approx(fmaf(transform_f32<SOFTCAP, false>(x[e], false, P), P.sc, -msc));
+    for (int t = 1; t < kVL; ++t)
+        if (i == t) r = rv[t];
+    if constexpr (BF16) {
+        const int q = e >> 1;
+        const uint32_t w = q == 0 ? r.x : q == 1 ? r.y : q == 2 ? r.z : r.w;
+        return (e & 1) ? __uint_as_float(w & 0xFFFF0000u) : __uint_as_float(w << 16);
+    } else {
+        const uint32_t w = e == 0 ? r.x : e == 1 ? r.y : e == 2 ? r.z : r.w;
+        return __uint_as_float(w);
     }
-    return add;
 }
 
+// Cold path of the streaming warps, kept out of line so the hot loop stays
+// small in the instruction cache: a row's last chunk, element by element with
+// the exact transform, for vectors that pass the row's end (reads the lane's
+// vectors back from the stage, which the warp holds until it is done).
 template <bool BF16, bool SOFTCAP, bool PENALTY>
 __device__ __noinline__ SumState sum_partial(const uint4* stage, int off0, int v0, int v1, unsigned long long pmk,
                                              SumState st, const VerifyDev& P) {
@@ -545,8 +570,11 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
     uint32_t* s_bm = reinterpret_cast<uint32_t*>(s_dyn + kStages * SB);
     __shared__ __align__(8) uint64_t s_full[kStages], s_empty[kStages];
     __shared__ StageMeta s_meta[kStages];
-    __shared__ SegSum s_slot[kStages][kCWarps];
-    __shared__ int s_cnt[kStages];
+    // segment merge slots, two per stage (by ring-cycle parity): a warp releases
+    // a stage as soon as its vectors are in registers, so the next cycle of the
+    // same stage can reach its merge before this one's last warp has read it
+    __shared__ SegSum s_slot[kStages][2][kCWarps];
+    __shared__ int s_cnt[kStages][2];
     __shared__ long long s_wsum[kPThreads / 32];
     __shared__ int s_start[3];
     __shared__ int s_hwin[PENALTY ? SPECNG_MAX_REP_WINDOW : 1];
@@ -575,7 +603,8 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&s_empty[i], kCWarps);
-            s_cnt[i] = 0;
+            s_cnt[i][0] = 0;
+            s_cnt[i][1] = 0;
         }
         mbar_init_fence();
     }
@@ -611,7 +640,7 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
         constexpr int kHW = PENALTY ? SPECNG_MAX_REP_WINDOW / 32 : 1;
         struct SeqData {
             int k, draft, L, cool;
-            float ema;
+            float ema, xd;  // xd: raw logit of the lane's draft in its row (loaded a step after draft)
             int hw[kHW];
         };
         auto clampL = [&](int L) {
@@ -632,12 +661,34 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
                 }
             }
         };
+        // proofs need a point-mass draft and T > 0
+        const bool proofs = !GREEDY && P.q == nullptr;
+        auto fetch_xd = [&](int bq, SeqData& d) {  // after d.draft has landed
+            d.xd = (proofs && bq < P.B && lane < P.K && d.draft >= 0 && d.draft < P.V)
+                       ? static_cast<float>(raw_logit_chk<BF16>(P, static_cast<size_t>(bq) * K1 + lane, d.draft))
+                       : 0.0f;
+        };
         int b = s_start[0], j = s_start[1], c = s_start[2];
         int keff = 0, nh = 0;
-        auto install = [&](const SeqData& d) {
+        float thr = INFINITY;  // lane j: row j's rejection-proof threshold
+        auto install = [&](const SeqData& d, int bq) {
             int kb = d.k;
             if (kb < 0 || kb > P.K) kb = kb < 0 ? 0 : P.K;
             keff = gate_rule(P, kb, d.ema, d.cool);
+            thr = INFINITY;
+            if (proofs && lane < keff) {
+                if (d.draft >= 0 && d.draft < P.V) {
+                    float zd = transform_f32<SOFTCAP, false>(d.xd, false, P);
+                    if constexpr (PENALTY) zd = fmaxf(zd, zd > 0.0f ? zd * P.invrep : zd * P.rep);
+                    NoiseKey nk = P.nk;
+                    nk.seq = static_cast<uint32_t>(bq);
+                    const float lu = logf(static_cast<float>(accept_uniform_f64(nk, static_cast<uint32_t>(lane + 1))));
+                    const float lp = zd * P.invT - lu;
+                    thr = zd - P.T * lu + P.T * (1e-3f + 1e-4f * fabsf(lp));
+                } else {
+                    thr = -INFINITY;  // an id outside [0, V) is rejected without a test
+                }
+            }
             if (lane < keff) s_pdrafts[lane] = d.draft;
             if constexpr (PENALTY) {
                 nh = d.L < P.W ? d.L : P.W;
@@ -653,10 +704,12 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
             const int L0 = PENALTY ? clampL(P.lens[b]) : 0;
             const int L1 = (PENALTY && b + 1 < P.B) ? clampL(P.lens[b + 1]) : 0;
             fetch(b, L0, cur);
-            install(cur);
+            fetch_xd(b, cur);
+            install(cur, b);
             fetch(b + 1, L1, nxt);
             if (PENALTY && b + 2 < P.B) Lnext2 = P.lens[b + 2];
         }
+        bool xd_due = true;  // nxt's draft logits are loaded one chunk after its drafts
         bool ok = true;
         int st = 0;
         int issued = 0;     // items whose copy was issued (copies complete in issue order per stage)
@@ -677,11 +730,17 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
                 bulk_g2s(s_stage + st * SB, src, static_cast<unsigned>(v1 - v0) * ElemTraits<BF16>::SIZE, &s_full[st]);
             }
             issued = n + 1;
+            if (xd_due) {
+                fetch_xd(b + 1, nxt);
+                xd_due = false;
+            }
             StageMeta& mt = s_meta[st];
+            const float rthr = __shfl_sync(0xffffffffu, thr, j & 31);
             if (lane == 0) {
                 mt.b = b; mt.j = j; mt.c = c;
                 mt.seg_end = (c == P.nchunk - 1 || n == nwork - 1) ? 1 : 0;
                 mt.sum = (!GREEDY && j < keff) ? 1 : 0;
+                mt.thr = j < keff ? rthr : INFINITY;
             }
             if constexpr (PENALTY) {
                 // bitmap of the penalised ids of row j in [v0, v1), and which slices hold one
@@ -723,9 +782,11 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
                     j = 0;
                     ++b;
                     if (n + 1 < nwork) {
-                        install(nxt);
+                        if (xd_due) fetch_xd(b, nxt);  // a sequence shorter than one chunk
+                        install(nxt, b);
                         const int L2 = PENALTY ? clampL(Lnext2) : 0;
                         fetch(b + 1, L2, nxt);
+                        xd_due = true;
                         if (PENALTY && b + 2 < P.B) Lnext2 = P.lens[b + 2];
                     }
                 }
@@ -751,6 +812,7 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
     const int ubase = warp * (32 * kVL);        // first 16-byte vector of my slice
     const int off0 = ubase * EPV + lane * EPV;  // chunk offset of vector 0's element 0
     float m = -INFINITY, s = 0.0f, msc = 0.0f;
+    bool proved = false;  // this warp met a value proving the segment's row rejects
     int st = 0;
     unsigned fph = 0u;  // parity of the full barrier phase to wait for
     for (int n = 0; n < nwork; ++n) {
@@ -758,7 +820,7 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
             if (lane == 0) raise_status(P.status, SPECNG_DEV_TIMEOUT);
             break;
         }
-        const StageMeta& mt = s_meta[st];
+        const StageMeta mt = s_meta[st];
         const int c = mt.c;
         const int row = mt.b * K1 + mt.j;
         const bool dosum = !GREEDY && mt.sum != 0;
@@ -781,8 +843,15 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
                 }
             }
         }
+        // Everything below works on registers, except the element-by-element sum
+        // of a slice that passes the row's end: release the stage now unless
+        // that path will read it, so the producer can refill it while this
+        // chunk's arithmetic runs.
+        const bool hold = dosum && (v0 + ubase * EPV + 32 * kVL * EPV > v1);
+        __syncwarp();
+        if (!hold && lane == 0) mbar_arrive(&s_empty[st]);
         // packed maxima of my vectors (bf16: both halves of a word hold partial maxima;
-        // fp32: the maximum); elements past the row's end count as -inf
+        // fp32: the maximum), NaN propagated; elements past the row's end count as -inf
         uint32_t hv[kVL];
 #pragma unroll
         for (int i = 0; i < kVL; ++i) {
@@ -792,27 +861,42 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
                 r = mask_tail<BF16>(r, nv);
             }
             if constexpr (BF16) {
-                hv[i] = as_u32(bf16x8_max2(r));
+                hv[i] = as_u32(bf16x8_max2_nan(r));
             } else {
-                hv[i] = __float_as_uint(fmaxf(fmaxf(__uint_as_float(r.x), __uint_as_float(r.y)),
-                                              fmaxf(__uint_as_float(r.z), __uint_as_float(r.w))));
+                hv[i] = __float_as_uint(fmax_nan(fmax_nan(__uint_as_float(r.x), __uint_as_float(r.y)),
+                                                 fmax_nan(__uint_as_float(r.z), __uint_as_float(r.w))));
             }
         }
         if (dosum) {
-            if (full) {
-                float lraw;
-                if constexpr (BF16) {
-                    uint32_t h = hv[0];
+            // the lane's largest raw logit of the chunk (NaN if it holds one)
+            float lraw;
+            if constexpr (BF16) {
+                uint32_t h = hv[0];
 #pragma unroll
-                    for (int i = 1; i < kVL; ++i) h = as_u32(__hmax2(as_bf162(h), as_bf162(hv[i])));
-                    lraw = fmaxf(bf16lo(h), bf16hi(h));
-                } else {
-                    lraw = __uint_as_float(hv[0]);
+                for (int i = 1; i < kVL; ++i) h = as_u32(__hmax2_nan(as_bf162(h), as_bf162(hv[i])));
+                lraw = fmax_nan(bf16lo(h), bf16hi(h));
+            } else {
+                lraw = __uint_as_float(hv[0]);
 #pragma unroll
-                    for (int i = 1; i < kVL; ++i) lraw = fmaxf(lraw, __uint_as_float(hv[i]));
-                }
-                const float zl = SOFTCAP ? transform_f32<true, false>(lraw, false, P) : lraw;
+                for (int i = 1; i < kVL; ++i) lraw = fmax_nan(lraw, __uint_as_float(hv[i]));
+            }
+            const bool bad = !(lraw < INFINITY);  // NaN or +inf
+            if (__any_sync(0xffffffffu, bad) && lane == 0) raise_status(P.status, SPECNG_DEV_NONFINITE);
+            const float zl = SOFTCAP ? transform_f32<true, false>(lraw, false, P) : lraw;
+            if (!proved) {
+                float zlo = zl;
+                if constexpr (PENALTY) zlo = fminf(zl, zl > 0.0f ? zl * P.invrep : zl * P.rep);
+                proved = __any_sync(0xffffffffu, !bad && zlo >= mt.thr);
+            }
+            if (proved) {
+                // the test rejects: no sum for the rest of the segment
+            } else if (full) {
                 if (!(m > -INFINITY)) {
+                    m = zl;
+                    msc = m * P.sc;
+                } else if ((zl - m) * P.sc > 32.0f) {
+                    // far above the reference: raise it before this chunk's terms
+                    s *= ex2_approx((m - zl) * P.sc);
                     m = zl;
                     msc = m * P.sc;
                 }
@@ -832,16 +916,8 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
                             acc2[i & 3] = __fadd2_rn(acc2[i & 3], make_float2(ex2_approx(t.x), ex2_approx(t.y)));
                         }
                     }
-                    float add = ((acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y)) +
-                                ((acc2[2].x + acc2[2].y) + (acc2[3].x + acc2[3].y));
-                    if ((zl - m) * P.sc > 32.0f) {
-                        // far above the reference: raise it and take the chunk again
-                        s *= ex2_approx((m - zl) * P.sc);
-                        m = zl;
-                        msc = m * P.sc;
-                        add = sum_from_stage<BF16, SOFTCAP>(stage, ubase + lane, msc, P);
-                    }
-                    s += add;
+                    s += ((acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y)) +
+                         ((acc2[2].x + acc2[2].y) + (acc2[3].x + acc2[3].y));
                 }
                 if constexpr (PENALTY) {
                     // the few penalised elements: their terms are replaced by the penalised ones
@@ -849,7 +925,7 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
                     while (pw != 0ull) {
                         const int bit = __ffsll(static_cast<long long>(pw)) - 1;
                         pw &= pw - 1ull;
-                        const float xe = elem_of_stage<BF16>(stage, off0 + (bit >> 3) * 32 * EPV + (bit & 7));
+                        const float xe = elem_of_regs<BF16>(rv, bit);
                         const float zu = sum_transform<SOFTCAP>(xe, P);
                         const float zp = sum_transform_pen<SOFTCAP>(xe, P);
                         if ((zp - m) * P.sc > 32.0f) {
@@ -913,7 +989,7 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
         }
 
         if (mt.seg_end && dosum) {
-            // ---- end of this row's segment: one record for the segment
+            // ---- end of this row's segment: one record for the segment (s < 0: proved)
             float pm = m, ps = s;
             if (!(pm > -INFINITY)) ps = 0.0f;
 #pragma unroll
@@ -922,27 +998,36 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
                 const float so = __shfl_xor_sync(0xffffffffu, ps, off);
                 ms_merge(pm, ps, mo, so, P.sc);
             }
+            if (proved) {
+                pm = 0.0f;
+                ps = -1.0f;
+            }
             int last = 0;
             if (lane == 0) {
-                s_slot[st][warp] = SegSum{pm, ps};
+                s_slot[st][fph][warp] = SegSum{pm, ps};
                 __threadfence_block();
-                last = atomicAdd(&s_cnt[st], 1) == kCWarps - 1;
+                last = atomicAdd(&s_cnt[st][fph], 1) == kCWarps - 1;
             }
             last = __shfl_sync(0xffffffffu, last, 0);
             if (last) {
                 __threadfence_block();
-                const SegSum wp = lane < kCWarps ? s_slot[st][lane] : SegSum{-INFINITY, 0.0f};
-                float cm = wp.m, cs = wp.s;
+                const SegSum wp = lane < kCWarps ? s_slot[st][fph][lane] : SegSum{-INFINITY, 0.0f};
+                const bool anyp = __any_sync(0xffffffffu, wp.s < 0.0f);
+                float cm = wp.s < 0.0f ? -INFINITY : wp.m, cs = wp.s < 0.0f ? 0.0f : wp.s;
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) {
                     const float mo = __shfl_xor_sync(0xffffffffu, cm, off);
                     const float so = __shfl_xor_sync(0xffffffffu, cs, off);
                     ms_merge(cm, cs, mo, so, P.sc);
                 }
+                if (anyp) {
+                    cm = 0.0f;
+                    cs = -1.0f;
+                }
                 if (lane == 0) {
                     // keyed by the segment's last chunk; a written record is never all-zero
                     P.part[static_cast<size_t>(row) * P.nchunk + c] = SegSum{cm, cs};
-                    s_cnt[st] = 0;
+                    s_cnt[st][fph] = 0;
                 }
             }
         }
@@ -950,9 +1035,10 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
             m = -INFINITY;
             s = 0.0f;
             msc = 0.0f;
+            proved = false;
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s_empty[st]);
+        if (hold && lane == 0) mbar_arrive(&s_empty[st]);
         if (++st == kStages) {
             st = 0;
             fph ^= 1u;
@@ -1328,6 +1414,7 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
             SegSum* pr = P.part + static_cast<size_t>(row) * P.nchunk;
             float2 pv[kPr];
             float mf = -INFINITY;
+            bool proof = false;  // a segment proved the test rejects (s < 0)
 #pragma unroll
             for (int i = 0; i < kPr; ++i) {
                 const int cc = lane + 32 * i;
@@ -1336,10 +1423,14 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
             for (int cc = lane + 32 * kPr; cc < P.nchunk; cc += 32) {
                 const float2 p = __ldcg(reinterpret_cast<const float2*>(pr + cc));
                 if (p.y != 0.0f || __float_as_uint(p.x) != 0u) mf = fmaxf(mf, p.x);
+                proof |= p.y < 0.0f;
             }
 #pragma unroll
-            for (int i = 0; i < kPr; ++i)
+            for (int i = 0; i < kPr; ++i) {
                 if (pv[i].y != 0.0f || __float_as_uint(pv[i].x) != 0u) mf = fmaxf(mf, pv[i].x);
+                proof |= pv[i].y < 0.0f;
+            }
+            proof = __any_sync(0xffffffffu, proof);
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) mf = fmaxf(mf, __shfl_xor_sync(0xffffffffu, mf, off));
             // the records' sums relative to mf (each term <= its record's sum; fp32 keeps 2^-24
@@ -1355,7 +1446,10 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) Sf += __shfl_xor_sync(0xffffffffu, Sf, off);
             for (int cc = lane; cc < P.nchunk; cc += 32) pr[cc] = SegSum{0.0f, 0.0f};  // leave the workspace zeroed
-            if (lane == 0) {
+            if (lane == 0 && proof) {
+                s_acc[j] = 0;
+                s_ms[j] = make_float2(0.0f, 0.0f);
+            } else if (lane == 0) {
                 if (!(Sf > 0.0f && Sf < INFINITY && mf < INFINITY)) raise_status(P.status, SPECNG_DEV_NONFINITE);
                 const float lsef = mf * P.invT + logf(Sf);
                 int accepted = 0;

@@ -1045,6 +1045,11 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
                     if (!(m > -INFINITY)) {
                         m = zl;
                         msc = m * P.sc;
+                    } else if ((zl - m) * P.sc > 32.0f) {
+                        // far above the reference: raise it before this chunk's terms
+                        s *= ex2_approx((m - zl) * P.sc);
+                        m = zl;
+                        msc = m * P.sc;
                     }
                     if (m > -INFINITY) {
                         float2 acc2[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
@@ -1062,16 +1067,8 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
                                 acc2[i & 3] = __fadd2_rn(acc2[i & 3], make_float2(ex2_approx(tt.x), ex2_approx(tt.y)));
                             }
                         }
-                        float add = ((acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y)) +
-                                    ((acc2[2].x + acc2[2].y) + (acc2[3].x + acc2[3].y));
-                        if ((zl - m) * P.sc > 32.0f) {
-                            // far above the reference: raise it and take the chunk again
-                            s *= ex2_approx((m - zl) * P.sc);
-                            m = zl;
-                            msc = m * P.sc;
-                            add = sum_from_stage<BF16, SOFTCAP>(stage, ubase + lane, msc, P);
-                        }
-                        s += add;
+                        s += ((acc2[0].x + acc2[0].y) + (acc2[1].x + acc2[1].y)) +
+                             ((acc2[2].x + acc2[2].y) + (acc2[3].x + acc2[3].y));
                     }
                     if constexpr (PENALTY) {
                         unsigned long long pw = pmk;
