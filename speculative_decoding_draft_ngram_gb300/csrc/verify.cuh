@@ -577,6 +577,7 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
     __shared__ int s_cnt[kStages][2];
     __shared__ long long s_wsum[kPThreads / 32];
     __shared__ int s_start[3];
+    __shared__ int s_proved_row;  // the latest row a warp of this CTA proved to reject
     __shared__ int s_hwin[PENALTY ? SPECNG_MAX_REP_WINDOW : 1];
     __shared__ int s_pdrafts[SPECNG_MAX_K + 1];
 
@@ -606,6 +607,7 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
             s_cnt[i][0] = 0;
             s_cnt[i][1] = 0;
         }
+        s_proved_row = -1;
         mbar_init_fence();
     }
     __syncthreads();
@@ -884,9 +886,12 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
             if (__any_sync(0xffffffffu, bad) && lane == 0) raise_status(P.status, SPECNG_DEV_NONFINITE);
             const float zl = SOFTCAP ? transform_f32<true, false>(lraw, false, P) : lraw;
             if (!proved) {
+                // a proof found by any warp of the CTA holds for the whole row
                 float zlo = zl;
                 if constexpr (PENALTY) zlo = fminf(zl, zl > 0.0f ? zl * P.invrep : zl * P.rep);
-                proved = __any_sync(0xffffffffu, !bad && zlo >= mt.thr);
+                const bool mine = __any_sync(0xffffffffu, !bad && zlo >= mt.thr);
+                if (mine && lane == 0) *reinterpret_cast<volatile int*>(&s_proved_row) = row;
+                proved = __any_sync(0xffffffffu, mine || *reinterpret_cast<volatile int*>(&s_proved_row) == row);
             }
             if (proved) {
                 // the test rejects: no sum for the rest of the segment
@@ -1157,10 +1162,23 @@ __device__ __noinline__ int accept_f64(const VerifyDev& P, float x, bool pen, do
 // nt take part, whole warps; ex is the id left out (-1: none).  Out of line:
 // the decision kernel calls it from two places and its code would otherwise
 // be there twice.
+// Block draws of row ra (M, slot, and -ln M in s_bnd), threads t of nt: they
+// depend on the row's key only, so the decision kernel takes row 0's before
+// the stream kernel has finished.
+static __device__ __noinline__ void draw_row_blocks(const VerifyDev& P, const NoiseKey& nk, int ra, int t, int nt, float* s_bnd,
+                                             float* s_M, int* s_I) {
+    for (int q = t; q < P.nblk; q += nt) {
+        const BlockNoise bn = block_noise(nk, static_cast<uint32_t>(q), static_cast<uint32_t>(ra));
+        s_bnd[q] = -bn.lnM;
+        s_M[q] = bn.M;
+        s_I[q] = bn.I;
+    }
+}
+
 template <bool BF16, bool SOFTCAP, bool PENALTY>
 __device__ __noinline__ void prepare_row(const VerifyDev& P, const NoiseKey& nk, int b, int ra, int ex, int t, int nt,
                                          unsigned* thr_slot, float* s_bnd, float* s_M, int* s_I, const int* pen_key,
-                                         const int* pen_pos, const int* drafts, int nh) {
+                                         const int* pen_pos, const int* drafts, int nh, bool drawn) {
     constexpr int EPV = ElemTraits<BF16>::EPV;
     constexpr int BLK = 1 << kNoiseBlockShift;
     constexpr int VPL = BLK / (32 * EPV);
@@ -1190,7 +1208,7 @@ __device__ __noinline__ void prepare_row(const VerifyDev& P, const NoiseKey& nk,
             rs[u] = e0 < P.V ? load_vec_chk<BF16>(P, rowp, e0, P.V) : make_uint4(0u, 0u, 0u, 0u);
         }
     }
-    // block draws and bounds
+    // block draws (unless drawn already) and bounds
     for (int q0 = t; q0 < nblk; q0 += 4 * nt) {
         float zq[4];
 #pragma unroll
@@ -1199,10 +1217,14 @@ __device__ __noinline__ void prepare_row(const VerifyDev& P, const NoiseKey& nk,
         for (int i = 0; i < 4; ++i) {
             const int q = q0 + i * nt;
             if (q >= nblk) break;
-            const BlockNoise bn = block_noise(nk, static_cast<uint32_t>(q), static_cast<uint32_t>(ra));
-            s_bnd[q] = block_zmax<SOFTCAP, PENALTY>(zq[i], P) * P.invT - bn.lnM;
-            s_M[q] = bn.M;
-            s_I[q] = bn.I;
+            if (drawn) {
+                s_bnd[q] += block_zmax<SOFTCAP, PENALTY>(zq[i], P) * P.invT;
+            } else {
+                const BlockNoise bn = block_noise(nk, static_cast<uint32_t>(q), static_cast<uint32_t>(ra));
+                s_bnd[q] = block_zmax<SOFTCAP, PENALTY>(zq[i], P) * P.invT - bn.lnM;
+                s_M[q] = bn.M;
+                s_I[q] = bn.I;
+            }
         }
     }
     // seed: each lane scores its largest element of the warp's seed block (the
@@ -1235,7 +1257,7 @@ __device__ __noinline__ void prepare_row(const VerifyDev& P, const NoiseKey& nk,
 }
 
 template <bool BF16, bool GREEDY, bool SOFTCAP, bool PENALTY>
-__global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__ VerifyDev P) {
+__global__ void __launch_bounds__(kST, 2) verify_seq_kernel(const __grid_constant__ VerifyDev P) {
     constexpr int EPV = ElemTraits<BF16>::EPV;
     constexpr int BLK = 1 << kNoiseBlockShift;
     constexpr int VPL = BLK / (32 * EPV);  // 16-byte vectors per lane per block (bf16 1, fp32 2)
@@ -1298,6 +1320,27 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
             }
         }
     }
+    // the sampling scratch of row a (block draws and bounds, the list of blocks)
+    const int nblk = P.nblk;
+    uint8_t* scr = nblk <= kSmemBlkCap ? s_dyn : P.blkws + static_cast<size_t>(b) * nblk * kBlkScratchBytes;
+    float* s_bnd = reinterpret_cast<float*>(scr);
+    float* s_M = s_bnd + nblk;
+    int* s_I = reinterpret_cast<int*>(s_M + nblk);
+    int* s_list = s_I + nblk;
+    // Row 0 is sampled by this kernel whenever a = 0 and no residual pass takes it
+    // (point-mass drafts, or no draft at all): its block draws are taken here, and
+    // the warps without an accept test prepare the rest of it meanwhile, which
+    // takes its preparation off the critical path when the first draft is rejected.
+    const bool spec0 = !GREEDY && (!dense || keff == 0) && keff < kSW;  // (needs a warp without a test)
+    if (spec0) draw_row_blocks(P, nk, 0, tid, kST, s_bnd, s_M, s_I);
+    // the epilogue's inputs (written by no kernel of this call before this one)
+    int kv_in = 0, gs_in = 0;
+    float ema_in = 0.0f;
+    if (tid == 0) {
+        kv_in = P.kv_len[b];
+        ema_in = P.ema[b];
+        gs_in = P.gate_state != nullptr ? P.gate_state[b] : 0;
+    }
     __syncthreads();
     // everything above reads the call's inputs only; the stream kernel's records from here on
     pdl_wait();
@@ -1319,19 +1362,7 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
     };
     auto elem_id = [&](int q, int k) { return q * BLK + ((k / EPV) * 32 + lane) * EPV + (k % EPV); };
 
-    // the sampling scratch of row a (block draws and bounds, the list of blocks)
-    const int nblk = P.nblk;
-    uint8_t* scr = nblk <= kSmemBlkCap ? s_dyn : P.blkws + static_cast<size_t>(b) * nblk * kBlkScratchBytes;
-    float* s_bnd = reinterpret_cast<float*>(scr);
-    float* s_M = s_bnd + nblk;
-    int* s_I = reinterpret_cast<int*>(s_M + nblk);
-    int* s_list = s_I + nblk;
     uint4* stg = reinterpret_cast<uint4*>(s_dyn + k2_blk_bytes(nblk)) + warp * (kBatch * 32 * VPL);
-    // Row 0 is sampled by this kernel whenever a = 0 and no residual pass takes it
-    // (point-mass drafts, or no draft at all): the warps without an accept test
-    // prepare it meanwhile, which takes its preparation off the critical path
-    // when the first draft is rejected.
-    const bool spec0 = !GREEDY && (!dense || keff == 0) && keff < kSW;  // (needs a warp without a test)
     // ---- 1. accept tests (T > 0) / argmax of every row (T = 0)
     for (int j = warp; j <= keff; j += kSW) {
         const int row = b * K1 + j;
@@ -1475,7 +1506,7 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
         if (spec0 && warp >= keff)
             prepare_row<BF16, SOFTCAP, PENALTY>(P, nk, b, 0, keff > 0 && s_d[0] >= 0 && s_d[0] < P.V ? s_d[0] : -1,
                                                 tid - 32 * keff, kST - 32 * keff, &s_thr0, s_bnd, s_M, s_I, s_pkey, s_ppos,
-                                                s_d, nh);
+                                                s_d, nh, true);
     }
     __syncthreads();
 
@@ -1502,7 +1533,7 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
             if (tid == 0) s_thr = s_thr0;  // row 0 was prepared during the accept tests
         } else {
             prepare_row<BF16, SOFTCAP, PENALTY>(P, nk, b, a, excl, tid, kST, &s_thr, s_bnd, s_M, s_I, s_pkey, s_ppos, s_d,
-                                                nh);
+                                                nh, false);
         }
         __syncthreads();
         float thr = -INFINITY;
@@ -1622,14 +1653,14 @@ __global__ void __launch_bounds__(kST) verify_seq_kernel(const __grid_constant__
         P.out_tokens[static_cast<size_t>(b) * K1 + tid] = tid < a ? s_d[tid] : (tid == a && !need ? y : -1);
     if (tid == 0) {
         P.out_accept[b] = a;
-        P.kv_len[b] = P.kv_len[b] - kb + a;
-        if (P.gate_state != nullptr) P.gate_state[b] = cool_after(P, P.gate_state[b], a, keff);
+        P.kv_len[b] = kv_in - kb + a;
+        if (P.gate_state != nullptr) P.gate_state[b] = cool_after(P, gs_in, a, keff);
         if (keff > 0) {
             // (1 - tau) * ema + tau * a / k_eff, rounded step by step (no contraction)
             const double tau = static_cast<double>(P.tau);
             const double rate = static_cast<double>(a) / static_cast<double>(keff);
             P.ema[b] = static_cast<float>(
-                __dadd_rn(__dmul_rn(1.0 - tau, static_cast<double>(P.ema[b])), __dmul_rn(tau, rate)));
+                __dadd_rn(__dmul_rn(1.0 - tau, static_cast<double>(ema_in)), __dmul_rn(tau, rate)));
         }
         if (need) {
             RowRes rr;
