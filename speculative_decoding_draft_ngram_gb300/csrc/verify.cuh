@@ -384,6 +384,28 @@ struct WindowView {
     }
 };
 
+// The EMA's rate a / k_eff in fp64 (correctly rounded, as a division gives it),
+// tabulated at compile time: a division in fp64 is a long sequence of fp64
+// operations, slow on this GPU, at the end of every sequence's decision.
+struct RateTable {
+    double v[SPECNG_MAX_K + 1][SPECNG_MAX_K + 1];  // [k_eff][a]
+};
+constexpr RateTable make_rate_table() {
+    RateTable t{};
+    for (int k = 1; k <= SPECNG_MAX_K; ++k)
+        for (int a = 0; a <= k; ++a) t.v[k][a] = static_cast<double>(a) / static_cast<double>(k);
+    return t;
+}
+__constant__ const RateTable c_rate = make_rate_table();
+__device__ __forceinline__ double ema_rate(int a, int keff) { return c_rate.v[keff][a]; }
+
+// EMA after a call with k_eff > 0 drafts and a accepted: (1 - tau) ema + tau a / k_eff,
+// each operation rounded in fp64 (no contraction), then to fp32.
+__device__ __forceinline__ float ema_update(float ema, float tau, int a, int keff) {
+    const double t = static_cast<double>(tau);
+    return static_cast<float>(__dadd_rn(__dmul_rn(1.0 - t, static_cast<double>(ema)), __dmul_rn(t, ema_rate(a, keff))));
+}
+
 // Drafts verified this call for a sequence with kb drafts, acceptance EMA ema
 // and cooling count cool: the EMA gate (shut below the threshold, except on a
 // re-probe step), then no drafts while cooling.
@@ -1078,7 +1100,8 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
 
 constexpr int kSW = 16;                         // warps per sequence
 constexpr int kST = kSW * 32;
-constexpr int kBatch = 4;                       // blocks a warp reads again at once
+// blocks a warp reads again at once (bf16 8, fp32 4: 8 KB per warp either way)
+template <bool BF16> __host__ __device__ constexpr int k2_batch() { return BF16 ? 8 : 4; }
 constexpr int kPenSlots = 2 * SPECNG_MAX_REP_WINDOW;
 constexpr int kPenBits = 9;
 static_assert((1 << kPenBits) == kPenSlots, "penalty table size");
@@ -1086,7 +1109,9 @@ static_assert(SPECNG_MAX_K + 1 <= kST, "one thread per output token");
 
 // Dynamic shared memory of the decision kernel at T > 0: the block scratch
 // (when it fits) and each warp's staging of a batch of blocks.
-__host__ __device__ constexpr size_t k2_stage_bytes(bool bf16) { return static_cast<size_t>(kSW) * kBatch * 32 * (bf16 ? 1 : 2) * 16; }
+__host__ __device__ constexpr size_t k2_stage_bytes(bool bf16) {
+    return static_cast<size_t>(kSW) * (bf16 ? k2_batch<true>() : k2_batch<false>()) * 32 * (bf16 ? 1 : 2) * 16;
+}
 __host__ __device__ inline size_t k2_blk_bytes(int nblk) {
     return nblk <= kSmemBlkCap ? (static_cast<size_t>(nblk) * kBlkScratchBytes + 15) / 16 * 16 : 0;
 }
@@ -1245,10 +1270,21 @@ __device__ __noinline__ void prepare_row(const VerifyDev& P, const NoiseKey& nk,
                 }
             }
             if (vb >= 0) {
-                const BlockNoise bn = block_noise(nk, static_cast<uint32_t>(qs), static_cast<uint32_t>(ra));
+                // drawn: the block's draw is in shared memory already (taken before this
+                // kernel waited); otherwise it is taken again here (another warp wrote it)
+                float Mq;
+                int Iq;
+                if (drawn) {
+                    Mq = s_M[qs];
+                    Iq = s_I[qs];
+                } else {
+                    const BlockNoise bn = block_noise(nk, static_cast<uint32_t>(qs), static_cast<uint32_t>(ra));
+                    Mq = bn.M;
+                    Iq = bn.I;
+                }
                 const bool pen = PENALTY && pen_lookup(pen_key, pen_pos, drafts, nh, P.W, vb, ra);
                 const float zb = transform_f32<SOFTCAP, PENALTY>(xb, pen, P) * P.invT;
-                sc = zb - ln_fast(noise_exp_f32(rpr, bn.M, bn.I, static_cast<uint32_t>(vb)));
+                sc = zb - ln_fast(noise_exp_f32(rpr, Mq, Iq, static_cast<uint32_t>(vb)));
             }
         }
         const unsigned kw = warp_best_key(sc);
@@ -1262,6 +1298,7 @@ __global__ void __launch_bounds__(kST, 2) verify_seq_kernel(const __grid_constan
     constexpr int BLK = 1 << kNoiseBlockShift;
     constexpr int VPL = BLK / (32 * EPV);  // 16-byte vectors per lane per block (bf16 1, fp32 2)
     constexpr int NE = VPL * EPV;          // elements per lane per block
+    constexpr int kBatch = k2_batch<BF16>();
     static_assert(kBatch * NE <= 64, "one 64-bit candidate mask per batch");
     extern __shared__ __align__(128) uint8_t s_dyn[];
     __shared__ int s_pkey[PENALTY ? kPenSlots : 1];
@@ -1274,7 +1311,7 @@ __global__ void __launch_bounds__(kST, 2) verify_seq_kernel(const __grid_constan
     __shared__ unsigned s_thr, s_thr0;
     __shared__ int s_nl;
     __shared__ int s_y;
-    __shared__ int s_bq[kSW][kBatch];
+    __shared__ int s_bq[kSW][8];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = blockIdx.x;
@@ -1655,13 +1692,7 @@ __global__ void __launch_bounds__(kST, 2) verify_seq_kernel(const __grid_constan
         P.out_accept[b] = a;
         P.kv_len[b] = kv_in - kb + a;
         if (P.gate_state != nullptr) P.gate_state[b] = cool_after(P, gs_in, a, keff);
-        if (keff > 0) {
-            // (1 - tau) * ema + tau * a / k_eff, rounded step by step (no contraction)
-            const double tau = static_cast<double>(P.tau);
-            const double rate = static_cast<double>(a) / static_cast<double>(keff);
-            P.ema[b] = static_cast<float>(
-                __dadd_rn(__dmul_rn(1.0 - tau, static_cast<double>(ema_in)), __dmul_rn(tau, rate)));
-        }
+        if (keff > 0) P.ema[b] = ema_update(ema_in, P.tau, a, keff);
         if (need) {
             RowRes rr;
             rr.m = s_ms[a].x;

@@ -685,12 +685,7 @@ __device__ __noinline__ void group_row_event(const VerifyDev& P, DShared& S, int
         P.out_accept[b] = a;
         P.kv_len[b] = P.kv_len[b] - kb + a;
         float en = __ldcg(P.ema + b);
-        if (keff > 0) {
-            // (1 - tau) * ema + tau * a / k_eff, rounded step by step (no contraction)
-            const double tau = static_cast<double>(P.tau);
-            const double rate = static_cast<double>(a) / static_cast<double>(keff);
-            en = static_cast<float>(__dadd_rn(__dmul_rn(1.0 - tau, static_cast<double>(en)), __dmul_rn(tau, rate)));
-        }
+        if (keff > 0) en = ema_update(en, P.tau, a, keff);
         P.ema_new[b] = en;
         if (P.gate_state != nullptr) P.cool_new[b] = cool_after(P, __ldcg(P.gate_state + b), a, keff);
     }
