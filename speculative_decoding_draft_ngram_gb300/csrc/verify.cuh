@@ -1017,17 +1017,16 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
 
         if (mt.seg_end && dosum) {
             // ---- end of this row's segment: one record for the segment (s < 0: proved)
-            float pm = m, ps = s;
-            if (!(pm > -INFINITY)) ps = 0.0f;
+            float pm = 0.0f, ps = -1.0f;  // proved: nothing to merge
+            if (!proved) {
+                pm = m;
+                ps = pm > -INFINITY ? s : 0.0f;
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float mo = __shfl_xor_sync(0xffffffffu, pm, off);
-                const float so = __shfl_xor_sync(0xffffffffu, ps, off);
-                ms_merge(pm, ps, mo, so, P.sc);
-            }
-            if (proved) {
-                pm = 0.0f;
-                ps = -1.0f;
+                for (int off = 16; off > 0; off >>= 1) {
+                    const float mo = __shfl_xor_sync(0xffffffffu, pm, off);
+                    const float so = __shfl_xor_sync(0xffffffffu, ps, off);
+                    ms_merge(pm, ps, mo, so, P.sc);
+                }
             }
             int last = 0;
             if (lane == 0) {
@@ -1040,16 +1039,16 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
                 __threadfence_block();
                 const SegSum wp = lane < kCWarps ? s_slot[st][fph][lane] : SegSum{-INFINITY, 0.0f};
                 const bool anyp = __any_sync(0xffffffffu, wp.s < 0.0f);
-                float cm = wp.s < 0.0f ? -INFINITY : wp.m, cs = wp.s < 0.0f ? 0.0f : wp.s;
+                float cm = 0.0f, cs = -1.0f;  // a proof from any warp stands for the segment
+                if (!anyp) {
+                    cm = wp.m;
+                    cs = wp.s;
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    const float mo = __shfl_xor_sync(0xffffffffu, cm, off);
-                    const float so = __shfl_xor_sync(0xffffffffu, cs, off);
-                    ms_merge(cm, cs, mo, so, P.sc);
-                }
-                if (anyp) {
-                    cm = 0.0f;
-                    cs = -1.0f;
+                    for (int off = 16; off > 0; off >>= 1) {
+                        const float mo = __shfl_xor_sync(0xffffffffu, cm, off);
+                        const float so = __shfl_xor_sync(0xffffffffu, cs, off);
+                        ms_merge(cm, cs, mo, so, P.sc);
+                    }
                 }
                 if (lane == 0) {
                     // keyed by the segment's last chunk; a written record is never all-zero
