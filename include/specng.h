@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define SPECNG_API_VERSION 2
+#define SPECNG_API_VERSION 3
 
 /* Host-detected return codes. */
 #define SPECNG_OK      0
@@ -77,6 +77,9 @@ extern "C" {
 #define SPECNG_DEV_TIMEOUT        0x80u /* a bounded wait for a bulk copy gave up; the call's
                                            outputs are incomplete and its workspace must be
                                            zeroed again (spec_verify_workspace_init)         */
+#define SPECNG_DEV_KV_SHORT      0x200u /* specng_kv_reserve could not give a sequence all the
+                                           blocks it needs: the pool ran empty or its table
+                                           row is full (it keeps what it got)             */
 #define SPECNG_DEV_CHECKED_OOB   0x100u /* checked build only (compiled with SPECNG_CHECKED):
                                            a computed index (vocabulary id, history position,
                                            draft slot, logit element) fell outside its array;
@@ -149,7 +152,8 @@ int specng_ngram_capacity(const specng_ngram* table, int64_t* slots);
  * position i in [indexed_b, lens_b) (indexed_b = lens_b of the previous
  * call, 0 after create/reset) the bigram pair (h[i-1] -> h[i]) and, when
  * i >= 2, the trigram pair ((h[i-2], h[i-1]) -> h[i]) are counted, then the
- * contexts' best continuations are refreshed.  Two kernel launches.
+ * contexts' best continuations are refreshed.  Three kernel launches (the
+ * table keeps no state on the host, so a captured call replays right).
  * Device errors: TABLE_FULL, TOKEN_OOR, COUNT_SAT, HIST_SHRANK. */
 int ngram_update(const int32_t* history, int64_t hist_stride, const int32_t* lens,
                  specng_ngram* table, cudaStream_t s);
@@ -197,6 +201,12 @@ typedef struct {
     int32_t* gate_state;    /* device int32 [B], in/out: each sequence's remaining
                                cooling calls (zero-fill before the first call);
                                required when cool_steps > 0, else ignored         */
+    const uint64_t* step_dev; /* device uint64 or NULL: when given, the kernels read
+                               the decode step from it instead of `step` (a call
+                               captured in a CUDA graph keeps its host arguments;
+                               specng_step_advance moves this counter on).  Not
+                               with the single-kernel schedule, whose state words
+                               carry a per-call tag chosen on the host (EINVAL)   */
 } specng_verify_params;
 
 /* Kernel schedules of spec_verify (the outputs are the same under each). */
@@ -342,6 +352,62 @@ int specng_set_verify_marker(cudaEvent_t after_stream_kernel);
 int spec_append(int32_t* history, int64_t hist_stride, int32_t* lens, int64_t hist_cap,
                 const int32_t* out_tokens, const int32_t* out_accept_len, int B, int K,
                 cudaStream_t s);
+
+/* ------------------------------------------------------------------------
+ * Decode-step bookkeeping  [AX] "Core Technical Architecture & Methods":
+ * the KV cache grows inside preallocated buffers, and a speculation rollback
+ * is O(1) -- only the sequence length moves (spec_verify's kv_len update);
+ * the scheduler recovers memory blocks.  Graph compilation reuses the same
+ * work across same-shape steps: a step (spec_verify, spec_commit, the KV
+ * calls below, specng_step_advance) can be captured once in a CUDA graph and
+ * replayed, with the decode step read from a device counter (step_dev).
+ * --------------------------------------------------------------------- */
+
+/* A pool of num_blocks KV blocks of block_size positions each, in the
+ * caller's preallocated KV buffers; the library keeps the bookkeeping only.
+ * All arrays are device int32 owned by the caller:
+ *   free_stack [num_blocks]: the free block ids are free_stack[0 .. *free_top)
+ *   free_top   [1]
+ *   block_table[B, max_blocks]: row b lists sequence b's blocks in position
+ *              order (position p of sequence b is in block row_b[p / block_size]),
+ *              -1 past its count
+ *   nblocks    [B]: blocks held by each sequence
+ * Sizes: num_blocks in [1, 2^30], B in [1, 2^20], max_blocks >= 1 with
+ * B * max_blocks <= 2^31 - 1, block_size >= 1. */
+typedef struct {
+    int32_t* free_stack;
+    int32_t* free_top;
+    int32_t* block_table;
+    int32_t* nblocks;
+    int32_t  num_blocks;
+    int32_t  B;
+    int32_t  max_blocks;
+    int32_t  block_size;
+} specng_kv_pool;
+
+/* Every block free, every sequence without blocks (blocks are then handed out
+ * in increasing id order by a single sequence).  One kernel launch. */
+int specng_kv_init(const specng_kv_pool* pool, cudaStream_t s);
+
+/* Sequence b takes blocks from the pool until it holds
+ * ceil((kv_len[b] + extra) / block_size) of them (capped at max_blocks), e.g.
+ * extra = K + 1 before a verify forward that writes K + 1 positions.  Which
+ * free block a sequence gets depends on the order of the device's atomics.
+ * kv_len: device int32 [B]; extra >= 0.  Device: KV_SHORT.  One launch. */
+int specng_kv_reserve(const specng_kv_pool* pool, const int32_t* kv_len, int extra, cudaStream_t s);
+
+/* Blocks past the ceil(kv_len[b] / block_size) that sequence b's positions
+ * need go back to the pool (after a rollback, the blocks that held only
+ * rejected positions).  kv_len: device int32 [B].  One launch. */
+int specng_kv_trim(const specng_kv_pool* pool, const int32_t* kv_len, cudaStream_t s);
+
+/* All blocks of the sequences with done[b] != 0 go back to the pool (a
+ * finished request).  done: device int32 [B].  One launch. */
+int specng_kv_release(const specng_kv_pool* pool, const int32_t* done, cudaStream_t s);
+
+/* *step_dev += 1 on the stream (device uint64): the next call that reads
+ * params.step_dev sees the next decode step.  One launch. */
+int specng_step_advance(uint64_t* step_dev, cudaStream_t s);
 
 /* ------------------------------------------------------------------------
  * Status and diagnostics

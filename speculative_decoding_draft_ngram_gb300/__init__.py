@@ -2,12 +2,15 @@
 n-gram drafts: device bigram/trigram tables (``ngram_update``,
 ``ngram_draft``), a single-pass Leviathan/Chen verifier with Gumbel-max
 residual / bonus sampling, kv_len rollback and an EMA gate
-(``spec_verify``), and the history append (``spec_append``).
+(``spec_verify``), the history append (``spec_append``), and the
+decode-step bookkeeping around them: a KV block pool (``KvPool``) and a
+device step counter (``step_advance``) for steps replayed from a CUDA graph.
 
 The compute runs in hand-written CUDA kernels behind the C ABI of
 ``include/specng.h`` (``libspecng.so``); this package is the thin binding.
 """
 from .capi import (  # noqa: F401
+    KvPool,
     NgramTable,
     SpecngError,
     VerifyParams,
@@ -26,4 +29,5 @@ from .capi import (  # noqa: F401
     spec_verify_workspace,
     spec_verify_workspace_bytes,
     status_names,
+    step_advance,
 )

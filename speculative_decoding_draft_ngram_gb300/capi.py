@@ -33,6 +33,7 @@ STATUS_BITS = {
     0x40: "HIST_SHRANK",
     0x80: "TIMEOUT",
     0x100: "CHECKED_OOB",
+    0x200: "KV_SHORT",
 }
 
 # Every symbol include/specng.h declares.
@@ -42,6 +43,7 @@ EXPORTED = (
     "ngram_update", "ngram_draft", "spec_verify_workspace_bytes", "spec_verify_workspace_init",
     "spec_verify", "spec_verify_noalloc", "spec_append", "spec_commit", "specng_get_status", "specng_strerror",
     "specng_last_error", "specng_philox4x32_10", "specng_set_verify_marker", "specng_get_counters",
+    "specng_kv_init", "specng_kv_reserve", "specng_kv_trim", "specng_kv_release", "specng_step_advance",
 )
 
 # Diagnostic counters (SPECNG_DIAG_*): runs of the exact (fp64) paths.
@@ -70,6 +72,20 @@ class VerifyParamsC(ctypes.Structure):
         ("probe_interval", ctypes.c_int32),
         ("cool_steps", ctypes.c_int32),
         ("gate_state", ctypes.c_void_p),
+        ("step_dev", ctypes.c_void_p),
+    ]
+
+
+class KvPoolC(ctypes.Structure):
+    _fields_ = [
+        ("free_stack", ctypes.c_void_p),
+        ("free_top", ctypes.c_void_p),
+        ("block_table", ctypes.c_void_p),
+        ("nblocks", ctypes.c_void_p),
+        ("num_blocks", ctypes.c_int32),
+        ("B", ctypes.c_int32),
+        ("max_blocks", ctypes.c_int32),
+        ("block_size", ctypes.c_int32),
     ]
 
 
@@ -93,16 +109,20 @@ class VerifyParams:
     probe_interval: int = 0       # gate variant: re-probe a gated-off sequence every this many steps
     cool_steps: int = 0           # gate variant: no drafts for this many calls after a partial acceptance
     gate_state: Optional[torch.Tensor] = None  # int32 [B] cooling counts (in/out), needed with cool_steps
+    step_dev: Optional[torch.Tensor] = None    # int64 [1] device step counter (read instead of step)
 
     def to_c(self) -> VerifyParamsC:
         gs = None
         if self.gate_state is not None:
             gs = _ptr(self.gate_state, torch.int32, "gate_state").value
+        sd = None
+        if self.step_dev is not None:
+            sd = _ptr(self.step_dev, torch.int64, "step_dev").value
         return VerifyParamsC(self.temperature, self.softcap, self.rep_penalty, int(self.rep_window),
                              self.ema_tau, self.ema_thresh, 1 if self.gate_enabled else 0, 0,
                              int(self.seed) & 0xFFFFFFFFFFFFFFFF, int(self.step) & 0xFFFFFFFFFFFFFFFF,
                              1 if self.early_exit else 0, int(self.schedule), int(self.probe_interval),
-                             int(self.cool_steps), gs)
+                             int(self.cool_steps), gs, sd)
 
 
 _lib = None
@@ -144,6 +164,11 @@ def load() -> ctypes.CDLL:
         "specng_strerror": (ctypes.c_char_p, [I]),
         "specng_last_error": (ctypes.c_char_p, []),
         "specng_philox4x32_10": (I, [P, U64, P, I64, P]),
+        "specng_kv_init": (I, [ctypes.POINTER(KvPoolC), P]),
+        "specng_kv_reserve": (I, [ctypes.POINTER(KvPoolC), P, I, P]),
+        "specng_kv_trim": (I, [ctypes.POINTER(KvPoolC), P, P]),
+        "specng_kv_release": (I, [ctypes.POINTER(KvPoolC), P, P]),
+        "specng_step_advance": (I, [P, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -345,6 +370,57 @@ def spec_commit(table: NgramTable, history: torch.Tensor, lens: torch.Tensor, ou
                                   _ptr(out_drafts, torch.int32, "out_drafts"), _ptr(out_k, torch.int32, "out_k"),
                                   _stream(history.device)), "spec_commit")
     return out_drafts, out_k
+
+
+# ---------------------------------------------------------------- decode-step bookkeeping
+
+class KvPool:
+    """Bookkeeping of a pool of KV blocks (see specng_kv_pool): the free-block
+    stack and the per-sequence block tables, as int32 device tensors."""
+
+    def __init__(self, num_blocks: int, B: int, max_blocks: int, block_size: int, device=None):
+        self.device = torch.device(device if device is not None else "cuda")
+        self.num_blocks, self.B = int(num_blocks), int(B)
+        self.max_blocks, self.block_size = int(max_blocks), int(block_size)
+        self.free_stack = torch.empty(self.num_blocks, dtype=torch.int32, device=self.device)
+        self.free_top = torch.empty(1, dtype=torch.int32, device=self.device)
+        self.block_table = torch.empty((self.B, self.max_blocks), dtype=torch.int32, device=self.device)
+        self.nblocks = torch.empty(self.B, dtype=torch.int32, device=self.device)
+        self.init()
+
+    def _c(self) -> KvPoolC:
+        return KvPoolC(self.free_stack.data_ptr(), self.free_top.data_ptr(), self.block_table.data_ptr(),
+                       self.nblocks.data_ptr(), self.num_blocks, self.B, self.max_blocks, self.block_size)
+
+    def init(self):
+        c = self._c()
+        with torch.cuda.device(self.device):
+            _check(load().specng_kv_init(ctypes.byref(c), _stream(self.device)), "specng_kv_init")
+
+    def reserve(self, kv_len: torch.Tensor, extra: int):
+        c = self._c()
+        with torch.cuda.device(self.device):
+            _check(load().specng_kv_reserve(ctypes.byref(c), _ptr(kv_len, torch.int32, "kv_len"), int(extra),
+                                            _stream(self.device)), "specng_kv_reserve")
+
+    def trim(self, kv_len: torch.Tensor):
+        c = self._c()
+        with torch.cuda.device(self.device):
+            _check(load().specng_kv_trim(ctypes.byref(c), _ptr(kv_len, torch.int32, "kv_len"),
+                                         _stream(self.device)), "specng_kv_trim")
+
+    def release(self, done: torch.Tensor):
+        c = self._c()
+        with torch.cuda.device(self.device):
+            _check(load().specng_kv_release(ctypes.byref(c), _ptr(done, torch.int32, "done"),
+                                            _stream(self.device)), "specng_kv_release")
+
+
+def step_advance(step_dev: torch.Tensor):
+    """step_dev += 1 on the current stream (int64 [1] device tensor)."""
+    with torch.cuda.device(step_dev.device):
+        _check(load().specng_step_advance(_ptr(step_dev, torch.int64, "step_dev"), _stream(step_dev.device)),
+               "specng_step_advance")
 
 
 # ---------------------------------------------------------------- diagnostics

@@ -6,6 +6,7 @@
 #include <atomic>
 #include <mutex>
 
+#include "kv.cuh"
 #include "ngram.cuh"
 #include "verify.cuh"
 
@@ -67,6 +68,14 @@ unsigned* diag_ptr() {
 // counters and the static scratch are looked up on the current device.
 bool stream_on_current_device(cudaStream_t s) {
     if (s == nullptr) return true;  // the legacy default stream follows the current device
+    // a stream being captured into a graph takes no device query (it would end the
+    // capture); a launch on another device's stream fails the capture by itself
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (cs != cudaStreamCaptureStatusNone) return true;
     int cur = -1, sd = -1;
     if (cudaGetDevice(&cur) != cudaSuccess) return false;
     if (cudaStreamGetDevice(s, &sd) != cudaSuccess) {
@@ -148,7 +157,6 @@ using namespace specng;
 struct specng_ngram {
     NgramDev dev;
     void* mem;
-    int parity;
     int grid;
 };
 
@@ -171,6 +179,75 @@ const char* specng_strerror(int code) {
 int specng_set_verify_marker(cudaEvent_t after_stream_kernel) {
     verify_marker() = after_stream_kernel;
     return SPECNG_OK;
+}
+
+namespace {
+
+int kv_view(const specng_kv_pool* pool, const char* what, specng::KvDev* out) {
+    if (pool == nullptr || pool->free_stack == nullptr || pool->free_top == nullptr || pool->block_table == nullptr ||
+        pool->nblocks == nullptr) {
+        std::snprintf(g_last_error, sizeof(g_last_error), "%s: NULL pool or pool array", what);
+        return SPECNG_EINVAL;
+    }
+    if (pool->num_blocks < 1 || pool->num_blocks > (1 << 30) || pool->B < 1 || pool->B > (1 << 20) ||
+        pool->max_blocks < 1 || pool->block_size < 1 ||
+        static_cast<int64_t>(pool->B) * pool->max_blocks > 0x7FFFFFFFLL) {
+        std::snprintf(g_last_error, sizeof(g_last_error), "%s: pool sizes out of range", what);
+        return SPECNG_EINVAL;
+    }
+    out->free_stack = pool->free_stack;
+    out->free_top = pool->free_top;
+    out->table = pool->block_table;
+    out->nblocks = pool->nblocks;
+    out->num_blocks = pool->num_blocks;
+    out->B = pool->B;
+    out->max_blocks = pool->max_blocks;
+    out->block_size = pool->block_size;
+    out->status = status_ptr();
+    return SPECNG_OK;
+}
+
+}  // namespace
+
+int specng_kv_init(const specng_kv_pool* pool, cudaStream_t s) {
+    specng::KvDev K;
+    const int rc = kv_view(pool, "specng_kv_init", &K);
+    if (rc != SPECNG_OK) return rc;
+    const cudaError_t e = launch_kv_init(K, s);
+    return e == cudaSuccess ? SPECNG_OK : fail_cuda(e, "specng_kv_init");
+}
+
+int specng_kv_reserve(const specng_kv_pool* pool, const int32_t* kv_len, int extra, cudaStream_t s) {
+    specng::KvDev K;
+    const int rc = kv_view(pool, "specng_kv_reserve", &K);
+    if (rc != SPECNG_OK) return rc;
+    if (kv_len == nullptr || extra < 0) return fail(SPECNG_EINVAL, "specng_kv_reserve: NULL kv_len or extra < 0");
+    const cudaError_t e = launch_kv_reserve(K, kv_len, extra, s);
+    return e == cudaSuccess ? SPECNG_OK : fail_cuda(e, "specng_kv_reserve");
+}
+
+int specng_kv_trim(const specng_kv_pool* pool, const int32_t* kv_len, cudaStream_t s) {
+    specng::KvDev K;
+    const int rc = kv_view(pool, "specng_kv_trim", &K);
+    if (rc != SPECNG_OK) return rc;
+    if (kv_len == nullptr) return fail(SPECNG_EINVAL, "specng_kv_trim: NULL kv_len");
+    const cudaError_t e = launch_kv_trim(K, kv_len, s);
+    return e == cudaSuccess ? SPECNG_OK : fail_cuda(e, "specng_kv_trim");
+}
+
+int specng_kv_release(const specng_kv_pool* pool, const int32_t* done, cudaStream_t s) {
+    specng::KvDev K;
+    const int rc = kv_view(pool, "specng_kv_release", &K);
+    if (rc != SPECNG_OK) return rc;
+    if (done == nullptr) return fail(SPECNG_EINVAL, "specng_kv_release: NULL done");
+    const cudaError_t e = launch_kv_release(K, done, s);
+    return e == cudaSuccess ? SPECNG_OK : fail_cuda(e, "specng_kv_release");
+}
+
+int specng_step_advance(uint64_t* step_dev, cudaStream_t s) {
+    if (step_dev == nullptr) return fail(SPECNG_EINVAL, "specng_step_advance: NULL step_dev");
+    const cudaError_t e = launch_step_advance(step_dev, s);
+    return e == cudaSuccess ? SPECNG_OK : fail_cuda(e, "specng_step_advance");
 }
 
 int specng_get_status(uint32_t* bits, int clear) {
@@ -214,7 +291,6 @@ int specng_ngram_create(specng_ngram** table, int B, int V, int64_t max_position
     specng_ngram* t = new specng_ngram();
     char* base = static_cast<char*>(mem);
     t->mem = mem;
-    t->parity = 0;
     t->grid = 2 * (sms > 0 ? sms : 1);
     t->dev.tri_pair = reinterpret_cast<ulonglong2*>(base);
     t->dev.bi_pair = reinterpret_cast<ulonglong2*>(base + table_bytes);
@@ -251,7 +327,6 @@ int specng_ngram_reset(specng_ngram* table, cudaStream_t s) {
     if (table == nullptr) return fail(SPECNG_EINVAL, "specng_ngram_reset: table is NULL");
     const cudaError_t e = launch_ngram_clear(table->dev, s);
     if (e != cudaSuccess) return fail_cuda(e, "specng_ngram_reset");
-    table->parity = 0;
     return SPECNG_OK;
 }
 
@@ -275,9 +350,8 @@ int ngram_update(const int32_t* history, int64_t hist_stride, const int32_t* len
         return fail(SPECNG_EINVAL, "ngram_update: NULL argument");
     if (hist_stride < 1 || hist_stride > SPECNG_NGRAM_MAX_POS)
         return fail(SPECNG_EINVAL, "ngram_update: hist_stride outside [1, 2^24]");
-    const cudaError_t e = launch_ngram_update(table->dev, table->parity, history, hist_stride, lens, table->grid, s);
+    const cudaError_t e = launch_ngram_update(table->dev, history, hist_stride, lens, table->grid, s);
     if (e != cudaSuccess) return fail_cuda(e, "ngram_update");
-    table->parity ^= 1;
     return SPECNG_OK;
 }
 
@@ -349,6 +423,8 @@ int verify_setup(const char* who, const void* logits, int logits_dtype, int B, i
     if (p.probe_interval < 0) return bad(SPECNG_EINVAL, "probe_interval must be >= 0");
     if (p.cool_steps < 0) return bad(SPECNG_EINVAL, "cool_steps must be >= 0");
     if (p.cool_steps > 0 && p.gate_state == nullptr) return bad(SPECNG_EINVAL, "cool_steps > 0 needs gate_state");
+    if (p.step_dev != nullptr && p.schedule == SPECNG_SCHEDULE_FUSED)
+        return bad(SPECNG_EINVAL, "step_dev is not supported by the single-kernel schedule (per-call state tags)");
     const bool penalty = p.rep_penalty != 1.0f && p.rep_window > 0;
     if (penalty && (history == nullptr || lens == nullptr || hist_stride < 1))
         return bad(SPECNG_EINVAL, "history, lens and hist_stride are needed for the penalty");
@@ -391,7 +467,8 @@ int verify_setup(const char* who, const void* logits, int logits_dtype, int B, i
     P.nk.k1 = static_cast<uint32_t>(p.seed >> 32);
     P.nk.step = static_cast<uint32_t>(p.step);
     P.probe = p.probe_interval;
-    P.probe_now = p.probe_interval > 0 && p.step % static_cast<uint64_t>(p.probe_interval) == 0 ? 1 : 0;
+    P.step64 = p.step;
+    P.step_dev = p.step_dev;
     P.cool = p.cool_steps;
     P.gate_state = p.cool_steps > 0 ? p.gate_state : nullptr;
     P.nk.seq = 0;
@@ -504,10 +581,9 @@ int spec_commit(specng_ngram* table, int32_t* history, int64_t hist_stride, int3
     if (hist_stride < 1 || hist_stride > SPECNG_NGRAM_MAX_POS)
         return fail(SPECNG_EINVAL, "spec_commit: hist_stride outside [1, 2^24]");
     if (hist_cap < 0 || hist_cap > hist_stride) return fail(SPECNG_EINVAL, "spec_commit: need 0 <= hist_cap <= hist_stride");
-    const cudaError_t e = launch_spec_commit(table->dev, table->parity, history, hist_stride, lens, hist_cap, out_tokens,
+    const cudaError_t e = launch_spec_commit(table->dev, history, hist_stride, lens, hist_cap, out_tokens,
                                              out_accept_len, K, max_k, k_limit, fallback, out_drafts, out_k, s);
     if (e != cudaSuccess) return fail_cuda(e, "spec_commit");
-    table->parity ^= 1;
     return SPECNG_OK;
 }
 

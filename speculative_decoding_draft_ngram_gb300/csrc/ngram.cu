@@ -16,7 +16,7 @@ struct NewRange {
     int* lo;          // [B]
 };
 
-__device__ void build_new_range(const NgramDev& T, int parity, const int32_t* lens, int64_t stride,
+__device__ void build_new_range(const NgramDev& T, const int32_t* lens, int64_t stride,
                                 long long* s_pref, int* s_lo, int* s_hi, bool flag) {
     __shared__ long long s_warp[kNgThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -26,7 +26,7 @@ __device__ void build_new_range(const NgramDev& T, int parity, const int32_t* le
     for (int h = 0; h < 2; ++h) {
         const int b = 2 * tid + h;
         if (b < T.B) {
-            const int idx = T.indexed[parity][b];
+            const int idx = T.indexed[0][b];
             int L = lens[b];
             if (L < 0) L = 0;
             if (static_cast<int64_t>(L) > stride) L = static_cast<int>(stride);
@@ -66,11 +66,11 @@ __device__ __forceinline__ int seq_of(const long long* s_pref, int B, long long 
 
 __device__ __forceinline__ bool tok_ok(int t, int V) { return t >= 0 && t < V; }
 
-__global__ void __launch_bounds__(kNgThreads) ngram_count_kernel(const NgramDev T, int parity, const int32_t* hist,
+__global__ void __launch_bounds__(kNgThreads) ngram_count_kernel(const NgramDev T, const int32_t* hist,
                                                                  int64_t stride, const int32_t* lens) {
     __shared__ long long s_pref[SPECNG_NGRAM_MAX_B + 1];
     __shared__ int s_lo[SPECNG_NGRAM_MAX_B], s_hi[SPECNG_NGRAM_MAX_B];
-    build_new_range(T, parity, lens, stride, s_pref, s_lo, s_hi, blockIdx.x == 0);
+    build_new_range(T, lens, stride, s_pref, s_lo, s_hi, blockIdx.x == 0);
     const long long total = s_pref[T.B];
     for (long long f = static_cast<long long>(blockIdx.x) * kNgThreads + threadIdx.x; f < total;
          f += static_cast<long long>(gridDim.x) * kNgThreads) {
@@ -117,11 +117,11 @@ __device__ __forceinline__ void push_best(const NgramDev& T, const ulonglong2* p
     atomicMax(&ctxs[slot].y, static_cast<unsigned long long>(pack_best(count, last, static_cast<uint64_t>(c))));
 }
 
-__global__ void __launch_bounds__(kNgThreads) ngram_best_kernel(const NgramDev T, int parity, const int32_t* hist,
+__global__ void __launch_bounds__(kNgThreads) ngram_best_kernel(const NgramDev T, const int32_t* hist,
                                                                 int64_t stride, const int32_t* lens) {
     __shared__ long long s_pref[SPECNG_NGRAM_MAX_B + 1];
     __shared__ int s_lo[SPECNG_NGRAM_MAX_B], s_hi[SPECNG_NGRAM_MAX_B];
-    build_new_range(T, parity, lens, stride, s_pref, s_lo, s_hi, false);
+    build_new_range(T, lens, stride, s_pref, s_lo, s_hi, false);
     const long long total = s_pref[T.B];
     for (long long f = static_cast<long long>(blockIdx.x) * kNgThreads + threadIdx.x; f < total;
          f += static_cast<long long>(gridDim.x) * kNgThreads) {
@@ -137,14 +137,20 @@ __global__ void __launch_bounds__(kNgThreads) ngram_best_kernel(const NgramDev T
             push_best(T, T.tri_pair, T.tri_ctx, key_tri_pair(b, t2, t1, c), key_tri_ctx(b, t2, t1), c);
         }
     }
-    // the next call starts from the lengths indexed now (other buffer: no
-    // block of this launch reads it)
+    // the lengths indexed now go to the second buffer (every block of this
+    // launch reads the first); the next launch copies them over
     if (blockIdx.x == 0) {
         for (int b = threadIdx.x; b < T.B; b += kNgThreads) {
-            const int idx = T.indexed[parity][b];
-            T.indexed[parity ^ 1][b] = s_hi[b] > idx ? s_hi[b] : idx;
+            const int idx = T.indexed[0][b];
+            T.indexed[1][b] = s_hi[b] > idx ? s_hi[b] : idx;
         }
     }
+}
+
+// The indexed lengths of ngram_update take effect (second buffer to first).
+// The kernels keep no state on the host, so a captured step replays right.
+__global__ void ngram_indexed_kernel(const NgramDev T) {
+    for (int b = threadIdx.x; b < T.B; b += blockDim.x) T.indexed[0][b] = T.indexed[1][b];
 }
 
 __device__ void draft_one(const NgramDev& T, int b, const int32_t* h, int L, int max_k, const int32_t* k_limit,
@@ -274,7 +280,7 @@ __device__ void draft_warp(const NgramDev& T, int b, const int32_t* h, int L, in
 // counts, then the contexts' best continuations) and draft the next step
 // (ngram_draft).  A sequence's keys belong to it alone, so the warp needs no
 // other sequence's work: __syncwarp orders its phases.
-__global__ void __launch_bounds__(kNgThreads) spec_commit_kernel(const NgramDev T, int parity, int32_t* hist,
+__global__ void __launch_bounds__(kNgThreads) spec_commit_kernel(const NgramDev T, int32_t* hist,
                                                                  int64_t stride, int32_t* lens, int64_t cap,
                                                                  const int32_t* out_tokens, const int32_t* out_accept,
                                                                  int K, int max_k, const int32_t* k_limit,
@@ -302,7 +308,7 @@ __global__ void __launch_bounds__(kNgThreads) spec_commit_kernel(const NgramDev 
     // ---- index positions [max(indexed, 1), L)
     if (L < 0) L = 0;
     if (static_cast<int64_t>(L) > stride) L = static_cast<int>(stride);
-    const int idx = T.indexed[parity][b];
+    const int idx = T.indexed[0][b];  // this warp alone reads and writes entry b
     if (L < idx && lane == 0) raise_status(T.status, SPECNG_DEV_HIST_SHRANK);
     const int lo = idx > 1 ? idx : 1;
     // half-warps: the bigram pairs on lanes 0..15, the trigram pairs on lanes 16..31,
@@ -336,7 +342,7 @@ __global__ void __launch_bounds__(kNgThreads) spec_commit_kernel(const NgramDev 
             push_best(T, T.bi_pair, T.bi_ctx, key_bi_pair(b, t1, c), key_bi_ctx(b, t1), c);
     }
     __syncwarp();
-    if (lane == 0) T.indexed[parity ^ 1][b] = L > idx ? L : idx;
+    if (lane == 0) T.indexed[0][b] = L > idx ? L : idx;
     // ---- the next step's drafts
     draft_warp(T, b, h, L, max_k, k_limit, fallback, out_drafts, out_k);
 }
@@ -349,12 +355,15 @@ __global__ void philox_kernel(const uint4* ctr, uint32_t k0, uint32_t k1, uint4*
 
 }  // namespace
 
-cudaError_t launch_ngram_update(const NgramDev& T, int parity, const int32_t* hist, int64_t stride,
+cudaError_t launch_ngram_update(const NgramDev& T, const int32_t* hist, int64_t stride,
                                 const int32_t* lens, int grid, cudaStream_t s) {
-    ngram_count_kernel<<<grid, kNgThreads, 0, s>>>(T, parity, hist, stride, lens);
+    ngram_count_kernel<<<grid, kNgThreads, 0, s>>>(T, hist, stride, lens);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    ngram_best_kernel<<<grid, kNgThreads, 0, s>>>(T, parity, hist, stride, lens);
+    ngram_best_kernel<<<grid, kNgThreads, 0, s>>>(T, hist, stride, lens);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    ngram_indexed_kernel<<<1, kNgThreads, 0, s>>>(T);
     return cudaGetLastError();
 }
 
@@ -381,12 +390,12 @@ cudaError_t launch_spec_append(int32_t* hist, int64_t stride, int32_t* lens, int
                           out_accept, B, K, status);
 }
 
-cudaError_t launch_spec_commit(const NgramDev& T, int parity, int32_t* hist, int64_t stride, int32_t* lens,
+cudaError_t launch_spec_commit(const NgramDev& T, int32_t* hist, int64_t stride, int32_t* lens,
                                int64_t cap, const int32_t* out_tokens, const int32_t* out_accept, int K, int max_k,
                                const int32_t* k_limit, const int32_t* fallback, int32_t* out_drafts, int32_t* out_k,
                                cudaStream_t s) {
     const int per = kNgThreads / 32;
-    return launch_chained(spec_commit_kernel, dim3((T.B + per - 1) / per), dim3(kNgThreads), 0, s, T, parity, hist, stride,
+    return launch_chained(spec_commit_kernel, dim3((T.B + per - 1) / per), dim3(kNgThreads), 0, s, T, hist, stride,
                           lens, cap, out_tokens, out_accept, K, max_k, k_limit, fallback, out_drafts, out_k);
 }
 

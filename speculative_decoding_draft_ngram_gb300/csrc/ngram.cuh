@@ -32,7 +32,7 @@ struct NgramDev {
     ulonglong2* tri_ctx;
     ulonglong2* bi_ctx;
     uint64_t mask;            // slots - 1 (slots a power of two)
-    int32_t* indexed[2];      // per-sequence indexed length, double-buffered
+    int32_t* indexed[2];      // per-sequence indexed length; [1]: ngram_update's new lengths until copied to [0]
     int B, V;
     unsigned* status;
     uint64_t min_count;       // a context drafts only a best continuation seen this often (>= 1)
@@ -88,7 +88,7 @@ __device__ __forceinline__ bool find_value(const ulonglong2* tab, uint64_t mask,
     return false;
 }
 
-cudaError_t launch_ngram_update(const NgramDev& T, int parity, const int32_t* hist, int64_t stride,
+cudaError_t launch_ngram_update(const NgramDev& T, const int32_t* hist, int64_t stride,
                                 const int32_t* lens, int grid, cudaStream_t s);
 cudaError_t launch_ngram_draft(const NgramDev& T, const int32_t* hist, int64_t stride, const int32_t* lens,
                                int max_k, const int32_t* k_limit, const int32_t* fallback, int32_t* out_drafts,
@@ -96,7 +96,7 @@ cudaError_t launch_ngram_draft(const NgramDev& T, const int32_t* hist, int64_t s
 cudaError_t launch_ngram_clear(const NgramDev& T, cudaStream_t s);
 cudaError_t launch_spec_append(int32_t* hist, int64_t stride, int32_t* lens, int64_t cap, const int32_t* out_tokens,
                                const int32_t* out_accept, int B, int K, unsigned* status, cudaStream_t s);
-cudaError_t launch_spec_commit(const NgramDev& T, int parity, int32_t* hist, int64_t stride, int32_t* lens,
+cudaError_t launch_spec_commit(const NgramDev& T, int32_t* hist, int64_t stride, int32_t* lens,
                                int64_t cap, const int32_t* out_tokens, const int32_t* out_accept, int K, int max_k,
                                const int32_t* k_limit, const int32_t* fallback, int32_t* out_drafts, int32_t* out_k,
                                cudaStream_t s);

@@ -111,7 +111,8 @@ struct VerifyDev {
     int fused;                      // 1: single-kernel schedule
     // gate variants
     int probe;                      // re-probe interval (0: none)
-    int probe_now;                  // this call's step is a multiple of it
+    uint64_t step64;                // the call's decode step (host argument)
+    const uint64_t* step_dev;       // device step counter, read instead when not NULL
     int cool;                       // cooling calls after a partial acceptance (0: none)
     int32_t* gate_state;            // [B] cooling counts, in/out (NULL when cool == 0)
     int32_t* cool_new;              // [B] single-kernel schedule: updated counts, copied by the last CTA
@@ -406,12 +407,28 @@ __device__ __forceinline__ float ema_update(float ema, float tau, int a, int kef
     return static_cast<float>(__dadd_rn(__dmul_rn(1.0 - t, static_cast<double>(ema)), __dmul_rn(t, ema_rate(a, keff))));
 }
 
+// The call's decode step: the device counter when one is given (a call replayed
+// from a CUDA graph keeps its host arguments), else the host argument.
+__device__ __forceinline__ uint64_t call_step(const VerifyDev& P) {
+    return P.step_dev != nullptr ? *P.step_dev : P.step64;
+}
+// The noise key of the call (the sequence field is set per use).
+__device__ __forceinline__ NoiseKey noise_key(const VerifyDev& P) {
+    NoiseKey nk = P.nk;
+    nk.step = static_cast<uint32_t>(call_step(P));
+    return nk;
+}
+// This call is a re-probe step of the gate (step a multiple of the interval).
+__device__ __forceinline__ bool probe_now(const VerifyDev& P) {
+    return P.probe > 0 && call_step(P) % static_cast<uint64_t>(P.probe) == 0;
+}
+
 // Drafts verified this call for a sequence with kb drafts, acceptance EMA ema
 // and cooling count cool: the EMA gate (shut below the threshold, except on a
 // re-probe step), then no drafts while cooling.
 __device__ __forceinline__ int gate_rule(const VerifyDev& P, int kb, float ema, int cool) {
     int ke = kb;
-    if (P.gate && kb > 0 && !(ema >= P.thresh) && !P.probe_now) ke = 0;
+    if (P.gate && kb > 0 && !(ema >= P.thresh) && !probe_now(P)) ke = 0;
     if (P.cool > 0 && cool > 0) ke = 0;
     return ke;
 }
@@ -704,7 +721,7 @@ __global__ void __launch_bounds__(kPThreads, kK1PerSM) verify_stream_kernel(cons
                 if (d.draft >= 0 && d.draft < P.V) {
                     float zd = transform_f32<SOFTCAP, false>(d.xd, false, P);
                     if constexpr (PENALTY) zd = fmaxf(zd, zd > 0.0f ? zd * P.invrep : zd * P.rep);
-                    NoiseKey nk = P.nk;
+                    NoiseKey nk = noise_key(P);
                     nk.seq = static_cast<uint32_t>(bq);
                     const float lu = logf(static_cast<float>(accept_uniform_f64(nk, static_cast<uint32_t>(lane + 1))));
                     const float lp = zd * P.invT - lu;
@@ -1319,7 +1336,7 @@ __global__ void __launch_bounds__(kST, 2) verify_seq_kernel(const __grid_constan
     int kb;
     const int keff = gate_keff(P, b, &kb, tid == 0);
     const bool dense = P.q != nullptr;
-    NoiseKey nk = P.nk;
+    NoiseKey nk = noise_key(P);
     nk.seq = static_cast<uint32_t>(b);
     int nh = 0;
     if (tid < keff) {
@@ -1856,7 +1873,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_residual_kernel(const __gr
     const char* rowp = static_cast<const char*>(P.logits) +
                        static_cast<size_t>(row) * P.V * ElemTraits<BF16>::SIZE;
     const float* qrow = P.q + (static_cast<size_t>(b) * P.K + a) * P.V;
-    NoiseKey nk = P.nk;
+    NoiseKey nk = noise_key(P);
     nk.seq = static_cast<uint32_t>(b);
     const RowPhilox rp = row_philox(nk, static_cast<uint32_t>(a));
 

@@ -305,7 +305,7 @@ __device__ __noinline__ int group_sample(const VerifyDev& P, DShared& S, const i
     const char* rowp = static_cast<const char*>(P.logits) + row * P.V * ElemTraits<BF16>::SIZE;
     const float* qrow = DENSE ? P.q + (static_cast<size_t>(b) * P.K + a) * P.V : nullptr;
     uint4* stg = stg_all + gw * (NB * 32 * VPL);
-    NoiseKey nk = P.nk;
+    NoiseKey nk = noise_key(P);
     nk.seq = static_cast<uint32_t>(b);
     const RowPhilox rp = row_philox(nk, static_cast<uint32_t>(a));
     auto pen_of = [&](int v) { return PENALTY && pen_lookup(pkey, ppos, S.d, S.nh, P.W, v, a); };
@@ -586,7 +586,7 @@ __device__ __noinline__ void group_row_event(const VerifyDev& P, DShared& S, int
     const size_t row = static_cast<size_t>(b) * K1 + j;
     const int keff = s_keff[b];
     const bool dense = P.q != nullptr;
-    NoiseKey nk = P.nk;
+    NoiseKey nk = noise_key(P);
     nk.seq = static_cast<uint32_t>(b);
     group_sync();  // every thread has read the arguments the loop passed through S
     // ---- the row's test (T > 0) or argmax (T = 0)
@@ -852,7 +852,7 @@ __global__ void __launch_bounds__(kFThreads, 1) verify_fused_kernel(const __grid
                     pend = wv.warp_has(cur.j, dnext) ? 1 : 0;
                 }
             }
-            NoiseKey nk = P.nk;
+            NoiseKey nk = noise_key(P);
             nk.seq = static_cast<uint32_t>(cur.b);
             for (int c = 0; c < P.nchunk; ++c) {
                 const int v0 = c * CHUNK;
