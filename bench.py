@@ -13,6 +13,7 @@ Prints one JSON line (rank 0).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -437,6 +438,66 @@ def measure_sub_workloads(dev, peak, names):
     return out
 
 
+def measure_graph_step(dev, name="c2", steps=200):
+    """Whole-step CUDA-graph replay against the same step launched call by call:
+    spec_verify (decode step read from a device counter) -> spec_commit ->
+    KV block trim and reserve -> step counter advance, on fixed buffers (one
+    logits batch, the drafts and counts written in place by spec_commit).
+    Returns device microseconds per step for both, over `steps` steps."""
+    import speculative_decoding_draft_ngram_gb300 as sp
+    path = Path(name, 24, dev)
+    cfg = path.cfg
+    path.first_drafts(0)
+    for s in range(8):
+        path.step(s, path.logits[s % path.n_sets], rowmax=path.rowmax[s % path.n_sets])
+    torch.cuda.synchronize()
+    logits = path.logits[0]
+    k = path.kbuf[8].clone() if path.ngram else path.kfull
+    lim, fb = path._limits(9)
+    pool = sp.KvPool(num_blocks=cfg.B * 4096, B=cfg.B, max_blocks=4096, block_size=16, device=dev)
+    pool.reserve(path.kv, cfg.K + 1)
+    step_t = torch.full((1,), 8, dtype=torch.int64, device=dev)
+    params = dataclasses.replace(path.params, step_dev=step_t)
+
+    def one():
+        sp.spec_verify(logits, path.drafts, None, k, path.hist, path.lens, params, path.kv, path.ema, path.out,
+                       path.acc, path.ws)
+        if path.ngram:
+            sp.spec_commit(path.table, path.hist, path.lens, path.out, path.acc, cfg.K, k_limit=lim, fallback=fb,
+                           out_drafts=path.drafts, out_k=k)
+        else:
+            sp.spec_append(path.hist, path.lens, path.out, path.acc)
+        pool.trim(path.kv)
+        pool.reserve(path.kv, cfg.K + 1)
+        sp.step_advance(step_t)
+
+    def timed(fn, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / n
+
+    for _ in range(3):
+        one()
+    eager_us = timed(one, steps)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        one()
+    g.replay()
+    graph_us = timed(g.replay, steps)
+    st = sp.get_status(clear=True)
+    del path
+    torch.cuda.empty_cache()
+    return {"what": f"{name}: one whole step (verify, commit, KV trim + reserve, step advance) per graph replay, "
+                    "against the same calls launched one by one",
+            "step_us_graph": graph_us, "step_us_eager": eager_us, "steps": steps,
+            "status": sp.status_names(st)}
+
+
 def run_ours(args):
     ws, rank, local = dist_env()
     if ws > 1:
@@ -541,6 +602,8 @@ def run_ours(args):
     subs = measure_sub_workloads(dev, peak, [n for n in SUB_WORKLOADS
                                              if SUB_WORKLOADS[n][0] != args.workload or SUB_WORKLOADS[n][3]]
                                  if not args.no_sub else [])
+    if not args.no_sub:
+        subs["c2_graph"] = measure_graph_step(dev, "c2")
     traffic = ncu_traffic(args.workload)
     line = {
         "metric": METRIC,
