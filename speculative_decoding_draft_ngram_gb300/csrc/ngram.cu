@@ -279,30 +279,47 @@ __device__ void draft_warp(const NgramDev& T, int b, const int32_t* h, int L, in
 // emitted tokens (spec_append), index the new positions (ngram_update: pair
 // counts, then the contexts' best continuations) and draft the next step
 // (ngram_draft).  A sequence's keys belong to it alone, so the warp needs no
-// other sequence's work: __syncwarp orders its phases.
+// other sequence's work: __syncwarp orders its phases.  The tokens around the
+// appended positions are kept in shared memory, and each pair's count and
+// latest position are updated by one 64-bit compare-and-swap whose result
+// feeds the context's best continuation at once: the state a lane produces is
+// never above the pair's final state, and pack_best grows with the count, so
+// the context's atomic maximum ends at what the final state gives.
+constexpr int kTailTok = SPECNG_MAX_K + 3;  // the two tokens before the appended ones, then those
+
 __global__ void __launch_bounds__(kNgThreads) spec_commit_kernel(const NgramDev T, int32_t* hist,
                                                                  int64_t stride, int32_t* lens, int64_t cap,
                                                                  const int32_t* out_tokens, const int32_t* out_accept,
                                                                  int K, int max_k, const int32_t* k_limit,
                                                                  const int32_t* fallback, int32_t* out_drafts,
                                                                  int32_t* out_k) {
+    __shared__ int s_tail[kNgThreads / 32][kTailTok];
     pdl_wait();  // the verify kernels' tokens
     pdl_trigger();
-    const int lane = threadIdx.x & 31;
-    const int b = blockIdx.x * (kNgThreads / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const int b = blockIdx.x * (kNgThreads / 32) + wib;
     if (b >= T.B) return;
     int32_t* h = hist + static_cast<size_t>(b) * stride;
+    int* tail = s_tail[wib];
     // ---- append
     int L = lens[b];
     const int a = out_accept[b];
+    const int L0 = L;       // first appended position (tail[2 + t] holds position L0 + t)
+    bool appended = false;  // the tail holds positions L0 - 2 .. L0 + a
     if (a < 0 || a > K) {
         if (lane == 0) raise_status(T.status, SPECNG_DEV_BAD_K);
     } else if (L < 0 || static_cast<int64_t>(L) + a + 1 > cap) {
         if (lane == 0) raise_status(T.status, SPECNG_DEV_HIST_OVERFLOW);
     } else {
-        if (lane <= a) h[L + lane] = out_tokens[static_cast<size_t>(b) * (K + 1) + lane];
+        if (lane <= a) {
+            const int t = out_tokens[static_cast<size_t>(b) * (K + 1) + lane];
+            h[L + lane] = t;
+            tail[2 + lane] = t;
+        }
+        if (lane < 2) tail[lane] = L - 2 + lane >= 0 ? h[L - 2 + lane] : -1;
         L += a + 1;
         if (lane == 0) lens[b] = L;
+        appended = true;
     }
     __syncwarp();
     // ---- index positions [max(indexed, 1), L)
@@ -311,35 +328,44 @@ __global__ void __launch_bounds__(kNgThreads) spec_commit_kernel(const NgramDev 
     const int idx = T.indexed[0][b];  // this warp alone reads and writes entry b
     if (L < idx && lane == 0) raise_status(T.status, SPECNG_DEV_HIST_SHRANK);
     const int lo = idx > 1 ? idx : 1;
+    auto tok_at = [&](int i) {  // the token at position i (the appended ones and the two before from shared memory)
+        return (appended && i >= L0 - 2 && i - (L0 - 2) < a + 3) ? tail[i - (L0 - 2)] : h[i];
+    };
     // half-warps: the bigram pairs on lanes 0..15, the trigram pairs on lanes 16..31,
     // so the two probe chains of a position run side by side
     const bool tri = lane >= 16;
     for (int i = lo + (lane & 15); i < L; i += 16) {
         if (tri && i < 2) continue;
-        const int c = h[i], t1 = h[i - 1], t2 = tri ? h[i - 2] : 0;
+        const int c = tok_at(i), t1 = tok_at(i - 1), t2 = tri ? tok_at(i - 2) : 0;
         if (!tok_ok(c, T.V) || !tok_ok(t1, T.V) || (tri && !tok_ok(t2, T.V))) {
             raise_status(T.status, SPECNG_DEV_TOKEN_OOR);
             continue;
         }
         ulonglong2* tab = tri ? T.tri_pair : T.bi_pair;
+        ulonglong2* ctxs = tri ? T.tri_ctx : T.bi_ctx;
+        const uint64_t ctx_key = tri ? key_tri_ctx(b, t2, t1) : key_bi_ctx(b, t1);
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(&ctxs[mix64(ctx_key) & T.mask]));
         const int64_t slot = find_or_insert(tab, T.mask, tri ? key_tri_pair(b, t2, t1, c) : key_bi_pair(b, t1, c));
         if (slot < 0) {
             raise_status(T.status, SPECNG_DEV_TABLE_FULL);
-        } else {
-            unsigned* v = reinterpret_cast<unsigned*>(&tab[slot].y);
-            atomicAdd(v, 1u);
-            atomicMax(v + 1, static_cast<unsigned>(i));
+            continue;
         }
-    }
-    __syncwarp();
-    for (int i = lo + (lane & 15); i < L; i += 16) {
-        if (tri && i < 2) continue;
-        const int c = h[i], t1 = h[i - 1], t2 = tri ? h[i - 2] : 0;
-        if (!tok_ok(c, T.V) || !tok_ok(t1, T.V) || (tri && !tok_ok(t2, T.V))) continue;
-        if (tri)
-            push_best(T, T.tri_pair, T.tri_ctx, key_tri_pair(b, t2, t1, c), key_tri_ctx(b, t2, t1), c);
-        else
-            push_best(T, T.bi_pair, T.bi_ctx, key_bi_pair(b, t1, c), key_bi_ctx(b, t1), c);
+        // count:32 | last:32, both at once
+        unsigned long long* vp = &tab[slot].y;
+        unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(vp), nxt;
+        for (;;) {
+            const uint64_t cnt = (cur & 0xFFFFFFFFull) + 1ull;
+            const uint64_t lst = (cur >> 32) > static_cast<uint64_t>(i) ? (cur >> 32) : static_cast<uint64_t>(i);
+            nxt = (lst << 32) | (cnt & 0xFFFFFFFFull);
+            const unsigned long long prev = atomicCAS(vp, cur, nxt);
+            if (prev == cur) break;
+            cur = prev;
+        }
+        uint64_t count = nxt & 0xFFFFFFFFull;
+        if (count > kCountMax) { raise_status(T.status, SPECNG_DEV_COUNT_SAT); count = kCountMax; }
+        const int64_t cs = find_or_insert(ctxs, T.mask, ctx_key);
+        if (cs < 0) { raise_status(T.status, SPECNG_DEV_TABLE_FULL); continue; }
+        atomicMax(&ctxs[cs].y, static_cast<unsigned long long>(pack_best(count, nxt >> 32, static_cast<uint64_t>(c))));
     }
     __syncwarp();
     if (lane == 0) T.indexed[0][b] = L > idx ? L : idx;
