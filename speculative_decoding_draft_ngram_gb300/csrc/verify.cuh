@@ -572,27 +572,51 @@ __device__ __forceinline__ float elem_of_regs(const uint4 (&rv)[kVL], int bit) {
 }
 
 // Cold path of the streaming warps, kept out of line so the hot loop stays
-// small in the instruction cache: a row's last chunk, element by element with
-// the exact transform, for vectors that pass the row's end (reads the lane's
-// vectors back from the stage, which the warp holds until it is done).
+// small in the instruction cache: a lane's vectors of a row's last chunk when
+// they pass the row's end (read back from the stage, which the warp holds
+// until it is done).  Two passes with the exact transform, a vector at a
+// time (the elements of a vector in parallel): the largest valid value fixes
+// the reference (raised as in the hot loop), then the terms of the valid
+// elements; elements past the row's end are left out.
 template <bool BF16, bool SOFTCAP, bool PENALTY>
 __device__ __noinline__ SumState sum_partial(const uint4* stage, int off0, int v0, int v1, unsigned long long pmk,
                                              SumState st, const VerifyDev& P) {
     constexpr int EPV = ElemTraits<BF16>::EPV;
+    const int nv0 = v1 - (v0 + off0);  // valid elements from my vector 0 on
+    float zm = -INFINITY;
 #pragma unroll 1
-    for (int i = 0; i < kVL; ++i) {
-        const int off = off0 + i * 32 * EPV;
-        const int nv = min(EPV, v1 - (v0 + off));
-#pragma unroll 1
-        for (int e = 0; e < nv; ++e) {
-            const float z = transform_f32<SOFTCAP, PENALTY>(elem_of_stage<BF16>(stage, off + e), (pmk >> (8 * i + e)) & 1ull, P);
-            if (!(st.m > -INFINITY) || (z - st.m) * P.sc > 32.0f) {
-                st.s = st.m > -INFINITY ? st.s * ex2_approx((st.m - z) * P.sc) : 0.0f;
-                st.m = z;
-                st.msc = st.m * P.sc;
-            }
-            st.s += ex2_approx(fmaf(z, P.sc, -st.msc));
+    for (int i = 0; i < kVL && nv0 - i * 32 * EPV > 0; ++i) {
+        float x[EPV];
+        unpack<BF16>(stage[off0 / EPV + i * 32], x);
+        const int nv = nv0 - i * 32 * EPV;
+        const unsigned pb = static_cast<unsigned>(pmk >> (8 * i));
+#pragma unroll
+        for (int e = 0; e < EPV; ++e)
+            if (e < nv) zm = fmaxf(zm, transform_f32<SOFTCAP, PENALTY>(x[e], (pb >> e) & 1u, P));
+    }
+    if (zm > -INFINITY) {
+        if (!(st.m > -INFINITY)) {
+            st.s = 0.0f;
+            st.m = zm;
+            st.msc = zm * P.sc;
+        } else if ((zm - st.m) * P.sc > 32.0f) {
+            st.s *= ex2_approx((st.m - zm) * P.sc);
+            st.m = zm;
+            st.msc = zm * P.sc;
         }
+    }
+    if (!(st.m > -INFINITY)) return st;  // no valid finite value yet
+#pragma unroll 1
+    for (int i = 0; i < kVL && nv0 - i * 32 * EPV > 0; ++i) {
+        float x[EPV];
+        unpack<BF16>(stage[off0 / EPV + i * 32], x);
+        const int nv = nv0 - i * 32 * EPV;
+        const unsigned pb = static_cast<unsigned>(pmk >> (8 * i));
+        float acc = 0.0f;
+#pragma unroll
+        for (int e = 0; e < EPV; ++e)
+            if (e < nv) acc += ex2_approx(fmaf(transform_f32<SOFTCAP, PENALTY>(x[e], (pb >> e) & 1u, P), P.sc, -st.msc));
+        st.s += acc;
     }
     return st;
 }
