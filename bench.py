@@ -438,6 +438,89 @@ def measure_sub_workloads(dev, peak, names):
     return out
 
 
+def measure_lmhead(dev, B=256, K=4, V=151936, d=2560, reps=20):
+    """Fused LM head + verify (spec_verify_lmhead) at the c5 batch shape with a
+    Qwen3-4B-sized head (d = 2560, V = 151936), no repetition penalty (the fused
+    path does not take it), T = 0.6: the whole call, the LM-head kernel alone
+    (an event after it), and for comparison the same logits from a cuBLAS
+    matmul followed by spec_verify.  Inputs: random bf16 hidden states and
+    weights (the weight, 778 MB, is larger than L2, so every call reads it
+    from HBM)."""
+    import speculative_decoding_draft_ngram_gb300 as sp
+    g = torch.Generator(device=dev).manual_seed(21)
+    hidden = torch.randn((B, K + 1, d), generator=g, device=dev).to(torch.bfloat16)
+    weight = (torch.randn((V, d), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    drafts = torch.randint(0, V, (B, K), generator=g, device=dev, dtype=torch.int32)
+    k = torch.randint(0, K + 1, (B,), generator=g, device=dev, dtype=torch.int32)
+    logits = torch.empty((B, K + 1, V), dtype=torch.bfloat16, device=dev)
+    kv = torch.full((B,), 1000, dtype=torch.int32, device=dev)
+    ema = torch.ones(B, dtype=torch.float32, device=dev)
+    out = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    acc = torch.empty((B,), dtype=torch.int32, device=dev)
+    ws_f = sp.spec_verify_lmhead_workspace(B, K, V, device=dev)
+    ws_s = sp.spec_verify_workspace(B, K, V, device=dev)
+    p = sp.VerifyParams(temperature=0.6, gate_enabled=False, seed=3, step=0)
+
+    def fused():
+        sp.spec_verify_lmhead(hidden, weight, logits, drafts, None, k, None, None, p, kv, ema, out, acc, ws_f)
+
+    def unfused():
+        torch.matmul(hidden.view(-1, d), weight.t(), out=logits.view(-1, V))
+        sp.spec_verify(logits, drafts, None, k, None, None, p, kv, ema, out, acc, ws_s)
+
+    def timed(fn, marker=False):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        m = torch.cuda.Event(enable_timing=True)
+        m.record()
+        if marker:
+            sp.set_verify_marker(m)
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(reps)]
+        first = []
+        for i in range(reps):
+            e0[i].record()
+            fn()
+            e1[i].record()
+            if marker:
+                torch.cuda.synchronize()
+                first.append(e0[i].elapsed_time(m))
+        torch.cuda.synchronize()
+        if marker:
+            sp.set_verify_marker(None)
+        call = statistics.mean(e0[i].elapsed_time(e1[i]) for i in range(reps))
+        return call, (statistics.mean(first) if first else None)
+
+    call_f, head_f = timed(fused, marker=True)
+    call_f2, _ = timed(fused)
+    call_u, _ = timed(unfused)
+    flops = 2.0 * B * (K + 1) * V * d
+    peaks = {}
+    pp = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pp):
+        with open(pp) as f:
+            peaks = json.load(f)
+    peak_tf = float(peaks.get("bf16_tflops", 1900.0))
+    st = sp.get_status(clear=True)
+    res = {
+        "what": "fused LM head (tcgen05 GEMM, bf16 logits and per-block records in its epilogue) + decision "
+                "kernel, c5 batch shape, d=2560, no penalty, T=0.6",
+        "B": B, "K": K, "V": V, "d": d,
+        "call_us": call_f2 * 1e3,
+        "lmhead_kernel_us": head_f * 1e3,
+        "lmhead_tflops": flops / (head_f * 1e-3) / 1e12,
+        "lmhead_frac_of_bf16_peak": flops / (head_f * 1e-3) / 1e12 / peak_tf,
+        "peak_bf16_tflops": peak_tf,
+        "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)" if peaks else "fallback 1.9 PF",
+        "unfused_cublas_matmul_plus_spec_verify_us": call_u * 1e3,
+        "status": sp.status_names(st),
+    }
+    del hidden, weight, logits, ws_f, ws_s
+    torch.cuda.empty_cache()
+    return res
+
+
 def measure_graph_step(dev, name="c2", steps=200):
     """Whole-step CUDA-graph replay against the same step launched call by call:
     spec_verify (decode step read from a device counter) -> spec_commit ->
@@ -611,6 +694,7 @@ def run_ours(args):
                                  if not args.no_sub else [])
     if not args.no_sub:
         subs["c2_graph"] = measure_graph_step(dev, "c2")
+        subs["c5_lmhead"] = measure_lmhead(dev)
     traffic = ncu_traffic(args.workload)
     line = {
         "metric": METRIC,

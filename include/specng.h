@@ -336,6 +336,40 @@ int spec_verify_noalloc(const void* logits, int logits_dtype, int B, int K, int 
                         int32_t* kv_len, float* ema,
                         int32_t* out_tokens, int32_t* out_accept_len, cudaStream_t s);
 
+/* Fused LM head + verify (scope row f1).  The target model's last
+ * projection and the verify of the drafts in one call: the logits of the
+ * K + 1 positions are logits = hidden W^T (SwiftLM page, Leviathan
+ * paragraph: the target scores the K drafts and the bonus position in one
+ * forward), computed on the tensor cores, and the same kernel's epilogue
+ * writes, per row and 256-id noise block, the block's largest logit and its
+ * softmax record; the decision kernel of spec_verify then runs on those
+ * records (no streaming pass over the logits), reading single logits back
+ * only where a decision needs them.  Results, as for spec_verify with
+ * logits_dtype SPECNG_BF16 and these logits.
+ *
+ * hidden       device, bf16 [B, K+1, d] row-major: the final hidden states
+ *              of the K + 1 positions (d a multiple of 64, 16-byte aligned).
+ * weight       device, bf16 [V, d] row-major: the LM head (16-byte aligned).
+ * d            hidden size, a multiple of 64 in [64, 2^20].
+ * logits       device, bf16 [B, K+1, V]: written by the call, each value the
+ *              fp32 dot product rounded to bf16 (nearest, ties to even);
+ *              V must be a multiple of 8 (16-byte rows).
+ * workspace    device scratch of at least spec_verify_lmhead_workspace_bytes
+ *              (B, K, V) bytes, 256-byte aligned, zero-filled before the
+ *              first call; the call leaves it ready for the next one.
+ * Other arguments as for spec_verify.  Not supported (SPECNG_EINVAL): the
+ * repetition penalty (rep_penalty != 1 with rep_window > 0) and the
+ * single-kernel schedule.  SPECNG_EINVAL also when the tensor maps of
+ * hidden / weight cannot be encoded (the driver lacks
+ * cuTensorMapEncodeTiled). */
+size_t spec_verify_lmhead_workspace_bytes(int B, int K, int V);
+int spec_verify_lmhead(const void* hidden, const void* weight, int d, void* logits,
+                       int B, int K, int V, const int32_t* drafts, const float* draft_probs,
+                       const int32_t* k, const int32_t* history, int64_t hist_stride,
+                       const int32_t* lens, const specng_verify_params* params,
+                       int32_t* kv_len, float* ema, int32_t* out_tokens, int32_t* out_accept_len,
+                       void* workspace, size_t workspace_bytes, cudaStream_t s);
+
 /* Measurement hook; the pages have no counterpart of it.  While
  * after_stream_kernel is not NULL, every spec_verify call records it on its
  * stream right after the streaming kernel, so a caller can time that kernel

@@ -25,6 +25,9 @@ from .capi import (  # noqa: F401
     spec_append,
     spec_commit,
     spec_verify,
+    spec_verify_lmhead,
+    spec_verify_lmhead_workspace,
+    spec_verify_lmhead_workspace_bytes,
     spec_verify_noalloc,
     spec_verify_workspace,
     spec_verify_workspace_bytes,

@@ -23,7 +23,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libspecng.so")
 LIB_CHECKED = os.path.join(PKG, "libspecng_checked.so")
-SOURCES = ["verify_bf16.cu", "verify_f32.cu", "ngram.cu", "kv.cu", "capi.cu"]
+SOURCES = ["verify_bf16.cu", "verify_f32.cu", "lmhead.cu", "ngram.cu", "kv.cu", "capi.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
 

@@ -41,7 +41,7 @@ EXPORTED = (
     "specng_ngram_create", "specng_ngram_destroy", "specng_ngram_reset", "specng_ngram_capacity",
     "specng_ngram_set_min_count",
     "ngram_update", "ngram_draft", "spec_verify_workspace_bytes", "spec_verify_workspace_init",
-    "spec_verify", "spec_verify_noalloc", "spec_append", "spec_commit", "specng_get_status", "specng_strerror",
+    "spec_verify", "spec_verify_noalloc", "spec_verify_lmhead_workspace_bytes", "spec_verify_lmhead", "spec_append", "spec_commit", "specng_get_status", "specng_strerror",
     "specng_last_error", "specng_philox4x32_10", "specng_set_verify_marker", "specng_get_counters",
     "specng_kv_init", "specng_kv_reserve", "specng_kv_trim", "specng_kv_release", "specng_step_advance",
 )
@@ -156,6 +156,9 @@ def load() -> ctypes.CDLL:
                             P, P, P, P, P, SZ, P]),
         "spec_verify_noalloc": (I, [P, I, I, I, I, P, P, P, P, I64, P, ctypes.POINTER(VerifyParamsC),
                                     P, P, P, P, P]),
+        "spec_verify_lmhead_workspace_bytes": (SZ, [I, I, I]),
+        "spec_verify_lmhead": (I, [P, P, I, P, I, I, I, P, P, P, P, I64, P, ctypes.POINTER(VerifyParamsC),
+                                   P, P, P, P, P, SZ, P]),
         "spec_append": (I, [P, I64, P, I64, P, P, I, I, P]),
         "spec_commit": (I, [P, P, I64, P, I64, P, P, I, I, I, P, P, P, P, P]),
         "specng_get_status": (I, [ctypes.POINTER(ctypes.c_uint32), I]),
@@ -336,6 +339,47 @@ def spec_verify_noalloc(logits: torch.Tensor, drafts: Optional[torch.Tensor], dr
             ctypes.byref(pc), _ptr(kv_len, torch.int32, "kv_len"), _ptr(ema, torch.float32, "ema"),
             _ptr(out_tokens, torch.int32, "out_tokens"), _ptr(out_accept_len, torch.int32, "out_accept_len"),
             _stream(logits.device)), "spec_verify_noalloc")
+
+
+def spec_verify_lmhead_workspace_bytes(B: int, K: int, V: int) -> int:
+    return int(load().spec_verify_lmhead_workspace_bytes(int(B), int(K), int(V)))
+
+
+def spec_verify_lmhead_workspace(B: int, K: int, V: int, device=None) -> torch.Tensor:
+    """A zero-filled workspace tensor for spec_verify_lmhead (allocated once, reused)."""
+    n = spec_verify_lmhead_workspace_bytes(B, K, V)
+    return torch.zeros(n, dtype=torch.uint8, device=device if device is not None else "cuda")
+
+
+def spec_verify_lmhead(hidden: torch.Tensor, weight: torch.Tensor, logits: torch.Tensor,
+                       drafts: Optional[torch.Tensor], draft_probs: Optional[torch.Tensor], k: torch.Tensor,
+                       history: Optional[torch.Tensor], lens: Optional[torch.Tensor], params: VerifyParams,
+                       kv_len: torch.Tensor, ema: torch.Tensor, out_tokens: torch.Tensor,
+                       out_accept_len: torch.Tensor, workspace: torch.Tensor):
+    """Fused LM head + verify: logits = hidden weight^T (written, bf16) and the verify of the drafts.
+
+    hidden [B, K+1, d] bf16, weight [V, d] bf16, logits [B, K+1, V] bf16 (output)."""
+    if hidden.dim() != 3 or weight.dim() != 2 or logits.dim() != 3:
+        raise SpecngError("hidden must be [B, K+1, d], weight [V, d], logits [B, K+1, V]")
+    B, K1, d = hidden.shape
+    V = weight.shape[0]
+    if weight.shape[1] != d or tuple(logits.shape) != (B, K1, V):
+        raise SpecngError("shapes of hidden, weight and logits disagree")
+    for name, t in (("hidden", hidden), ("weight", weight), ("logits", logits)):
+        if t.dtype != torch.bfloat16:
+            raise SpecngError(f"{name} must be bfloat16")
+    pc = params.to_c()
+    with torch.cuda.device(logits.device):   # the library works on the current device
+        _check(load().spec_verify_lmhead(
+            _ptr(hidden, None, "hidden"), _ptr(weight, None, "weight"), d, _ptr(logits, None, "logits"),
+            B, K1 - 1, V,
+            _ptr(drafts, torch.int32, "drafts"), _ptr(draft_probs, torch.float32, "draft_probs"),
+            _ptr(k, torch.int32, "k"), _ptr(history, torch.int32, "history"),
+            history.shape[1] if history is not None else 0, _ptr(lens, torch.int32, "lens"),
+            ctypes.byref(pc), _ptr(kv_len, torch.int32, "kv_len"), _ptr(ema, torch.float32, "ema"),
+            _ptr(out_tokens, torch.int32, "out_tokens"), _ptr(out_accept_len, torch.int32, "out_accept_len"),
+            _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+            _stream(logits.device)), "spec_verify_lmhead")
 
 
 def spec_append(history: torch.Tensor, lens: torch.Tensor, out_tokens: torch.Tensor,

@@ -112,9 +112,10 @@ struct WsLayout {
 int max_chunks(int V) { return (V + chunk_elems<false>() - 1) / chunk_elems<false>(); }
 int max_chunks2(int V) { return (V + res_chunk_elems<false>() - 1) / res_chunk_elems<false>(); }
 
-WsLayout ws_layout(int B, int K, int V) {
+// per_block: one sum record per row and noise block (the fused LM-head path)
+WsLayout ws_layout(int B, int K, int V, bool per_block = false) {
     const size_t rows = static_cast<size_t>(B) * (K + 1);
-    const size_t nch = static_cast<size_t>(max_chunks(V));
+    const size_t nch = static_cast<size_t>(per_block ? noise_blocks(V) : max_chunks(V));
     const size_t nblk = static_cast<size_t>(noise_blocks(V));
     WsLayout L{};
     size_t off = 0;
@@ -483,8 +484,8 @@ int verify_setup(const char* who, const void* logits, int logits_dtype, int B, i
     return SPECNG_OK;
 }
 
-void attach_workspace(VerifyDev& P, void* workspace) {
-    const WsLayout L = ws_layout(P.B, P.K, P.V);
+void attach_workspace(VerifyDev& P, void* workspace, bool per_block = false) {
+    const WsLayout L = ws_layout(P.B, P.K, P.V, per_block);
     char* ws = static_cast<char*>(workspace);
     P.part = reinterpret_cast<SegSum*>(ws + L.part);
     P.bmax = reinterpret_cast<float*>(ws + L.bmax);
@@ -526,6 +527,46 @@ int spec_verify(const void* logits, int logits_dtype, int B, int K, int V, const
     if (workspace_bytes < ws_layout(B, K, V).total) return fail(SPECNG_ESMALL, "spec_verify: workspace too small");
     attach_workspace(P, workspace);
     return verify_launch(P, f, s, "spec_verify");
+}
+
+size_t spec_verify_lmhead_workspace_bytes(int B, int K, int V) {
+    if (B < 1 || K < 0 || K > SPECNG_MAX_K || V < 1) return 0;
+    return ws_layout(B, K, V, true).total;
+}
+
+int spec_verify_lmhead(const void* hidden, const void* weight, int d, void* logits, int B, int K, int V,
+                       const int32_t* drafts, const float* draft_probs, const int32_t* k, const int32_t* history,
+                       int64_t hist_stride, const int32_t* lens, const specng_verify_params* params, int32_t* kv_len,
+                       float* ema, int32_t* out_tokens, int32_t* out_accept_len, void* workspace,
+                       size_t workspace_bytes, cudaStream_t s) {
+    const char* who = "spec_verify_lmhead";
+    char msg[160];
+    auto bad = [&](int code, const char* what) {
+        std::snprintf(msg, sizeof(msg), "%s: %s", who, what);
+        return fail(code, msg);
+    };
+    if (hidden == nullptr || weight == nullptr || logits == nullptr) return bad(SPECNG_EINVAL, "NULL argument");
+    if (!aligned16(hidden) || !aligned16(weight) || !aligned16(logits))
+        return bad(SPECNG_EALIGN, "hidden, weight and logits must be 16-byte aligned");
+    if (d < 64 || d % 64 != 0 || d > (1 << 20)) return bad(SPECNG_EINVAL, "d must be a multiple of 64 in [64, 2^20]");
+    if (V % 8 != 0) return bad(SPECNG_EINVAL, "V must be a multiple of 8");
+    if (params != nullptr && params->rep_penalty != 1.0f && params->rep_window > 0)
+        return bad(SPECNG_EINVAL, "the repetition penalty is not supported by the fused LM-head path");
+    if (params != nullptr && params->schedule == SPECNG_SCHEDULE_FUSED)
+        return bad(SPECNG_EINVAL, "the fused LM-head path runs the split schedule's decision kernel");
+    VerifyDev P;
+    bool f[5];
+    int rc = verify_setup(who, logits, SPECNG_BF16, B, K, V, drafts, draft_probs, k, history, hist_stride, lens, params,
+                          kv_len, ema, out_tokens, out_accept_len, s, &P, f);
+    if (rc != SPECNG_OK) return rc;
+    if (workspace == nullptr) return bad(SPECNG_EINVAL, "workspace is NULL");
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return bad(SPECNG_EALIGN, "workspace must be 256-byte aligned");
+    if (workspace_bytes < ws_layout(B, K, V, true).total) return bad(SPECNG_ESMALL, "workspace too small");
+    attach_workspace(P, workspace, true);
+    const cudaError_t e = launch_lmhead_verify(hidden, weight, d, logits, P, f[1], f[2], f[4], s);
+    if (e == cudaErrorInvalidValue) return bad(SPECNG_EINVAL, "the tensor maps of hidden / weight could not be encoded");
+    if (e != cudaSuccess) return fail_cuda(e, who);
+    return SPECNG_OK;
 }
 
 int spec_verify_noalloc(const void* logits, int logits_dtype, int B, int K, int V, const int32_t* drafts,

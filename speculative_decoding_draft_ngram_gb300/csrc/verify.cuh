@@ -109,6 +109,7 @@ struct VerifyDev {
     uint32_t epoch;                 // this call's tag, in [1, 2^31)
     int early_exit;                 // rows past a known first rejection are not streamed
     int fused;                      // 1: single-kernel schedule
+    int records_given;              // 1: the fused LM-head kernel wrote the records (no streaming pass)
     // gate variants
     int probe;                      // re-probe interval (0: none)
     uint64_t step64;                // the call's decode step (host argument)
@@ -2203,10 +2204,13 @@ cudaError_t launch_all(const VerifyDev& P, bool dense, cudaStream_t s) {
         if (cudaEvent_t m = verify_marker()) e = cudaEventRecord(m, s);  // measurement only: after the one kernel
         return e;
     }
-    cudaError_t e = launch_stream<BF16, G, C, R>(P, s);
-    if (e != cudaSuccess) return e;
+    cudaError_t e = cudaSuccess;
+    if (!P.records_given) {
+        e = launch_stream<BF16, G, C, R>(P, s);
+        if (e != cudaSuccess) return e;
+    }
     if (cudaEvent_t m = verify_marker()) {
-        e = cudaEventRecord(m, s);  // measurement only: ends the streaming kernel's span
+        e = cudaEventRecord(m, s);  // measurement only: ends the streaming (or LM-head) kernel's span
         if (e != cudaSuccess) return e;
     }
     e = launch_seq<BF16, G, C, R>(P, s);
@@ -2225,6 +2229,13 @@ cudaError_t launch_all_cr(const VerifyDev& P, bool c, bool r, bool dense, cudaSt
 template <bool BF16>
 cudaError_t launch_verify_dtype(const VerifyDev& P, bool greedy, bool softcap, bool penalty, bool dense,
                                 cudaStream_t s);
+
+// The fused LM-head kernel (logits = h W^T on the tensor cores, with the
+// per-block records in its epilogue), then the decision kernel and, for dense
+// q at T > 0, the residual pass.  cudaErrorInvalidValue: the tensor maps of
+// hidden / weight could not be encoded.
+cudaError_t launch_lmhead_verify(const void* hidden, const void* weight, int d, void* logits, VerifyDev P, bool greedy,
+                                 bool softcap, bool dense, cudaStream_t s);
 
 template <bool BF16>
 cudaError_t launch_verify_impl(const VerifyDev& P, bool greedy, bool softcap, bool penalty, bool dense,
