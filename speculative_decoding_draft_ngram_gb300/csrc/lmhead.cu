@@ -15,14 +15,19 @@
 // drafts) and of the engine's tensor path (AX Engine page, "Core Technical
 // Architecture & Methods": the forward's operations run as GPU tensor ops).
 //
-// Layout of the work: one CTA per SM, persistent, tiles of 128 rows x 256
-// vocab ids (one noise block), ordered row tile first so that the CTAs
-// running at the same time share their W tiles through L2.  Warp 0 issues
-// the TMA loads (128-byte swizzled, 64 hidden elements per stage, a 4-stage
-// ring), warp 1 owns the tensor memory (two 256-column accumulators) and one
-// of its threads issues the MMAs, warps 2-5 read an accumulator back
-// (tcgen05.ld), round it to bf16 (the logits' dtype), store it and reduce it
-// while the next tile's MMAs run.
+// Layout of the work: one CTA per SM, persistent, in clusters of two; tiles
+// of 128 rows x 256 vocab ids (one noise block).  The two CTAs of a cluster
+// take the two row tiles of a pair for the same vocab tile, and each loads
+// half of that W tile and multicasts it to both, so each SM reads a third
+// less from L2 than a lone CTA would; pairs are ordered row tiles first, so
+// the clusters running at the same time share their W tiles through L2.
+// Warp 0 issues the TMA loads (128-byte swizzled, 64 hidden elements per
+// stage, a 4-stage ring), warp 1 owns the tensor memory (two 256-column
+// accumulators) and one of its threads issues the MMAs, warps 2-5 read an
+// accumulator back (tcgen05.ld), round it to bf16 (the logits' dtype), store
+// it and reduce it while the next tile's MMAs run.  A ring stage is refilled
+// once the MMAs of both CTAs have read it (each CTA's MMA completion arrives
+// on both CTAs' barriers).
 #include <cuda.h>
 
 #include "verify.cuh"
@@ -39,10 +44,14 @@ constexpr uint32_t kHBBytes = kHN * kHK * 2;  // 32 KB
 constexpr uint32_t kHTmemCols = 2 * kHN;      // two accumulators
 static_assert(kHN == (1 << kNoiseBlockShift), "a tile's vocab range is one noise block");
 constexpr size_t kHSmem = kHStages * (kHABytes + kHBBytes) + 1024;  // + alignment slack
+constexpr int kHCl = 2;                           // CTAs of a cluster (sharing each W tile)
+constexpr uint32_t kHBHalf = kHBBytes / kHCl;     // the W rows one CTA loads for both
+constexpr uint16_t kHMask = (1u << kHCl) - 1u;    // every CTA of the cluster
 
 struct LmHeadArgs {
     CUtensorMap tmA;  // hidden [rows, d] bf16: box {64, 128}, 128-byte swizzle
-    CUtensorMap tmB;  // weight [V, d] bf16: box {64, 256}, 128-byte swizzle
+    CUtensorMap tmB;  // weight [V, d] bf16: box {64, 128} (half a tile), 128-byte swizzle
+    CUtensorMap tmC;  // logits [rows, V] bf16: box {32, 32}, no swizzle (the epilogue's stores)
     int rows, d, ntm, ntn;
     __nv_bfloat16* logits;  // [rows, V]
     VerifyDev P;
@@ -106,6 +115,48 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Loaded once and written to the same offset in every CTA of `mask`, each of
+// whose barrier at bar's offset receives the bytes.
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar,
+                                               uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%2, "
+        "%3}], [%4], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
+        : "memory");
+}
+// The barrier at bar's offset in every CTA of `mask` gets one arrival once the
+// MMAs issued so far by this thread are done.
+__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                     smem_u32(bar)),
+                 "h"(mask)
+                 : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Shared -> global tile store; the part of the box outside the tensor is not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, int x, int y, const void* src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(tm)),
+                 "r"(x), "r"(y), "r"(smem_u32(src))
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// The source of all but the last n committed stores has been read.
+template <int N>
+__device__ __forceinline__ void tma_store_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void tma_store_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, int x, int y, uint64_t* bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
@@ -126,12 +177,15 @@ __global__ void __launch_bounds__(kHThreads, 1) lmhead_verify_kernel(const __gri
     __shared__ __align__(8) uint64_t s_full[kHStages], s_empty[kHStages], s_accf[2], s_acce[2], s_done;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
+    // epilogue staging: per warp two boxes of 32 rows x 32 bf16 columns, row-major,
+    // written by the warp and stored by TMA while the next one fills
+    __shared__ __align__(128) uint4 s_ep[4][2][32 * 4];
     const VerifyDev& P = A.P;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kHStages; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_empty[i], 1);
+            mbar_init(&s_empty[i], kHCl);  // the MMA completions of both CTAs
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_accf[i], 1);
@@ -148,9 +202,13 @@ __global__ void __launch_bounds__(kHThreads, 1) lmhead_verify_kernel(const __gri
     pdl_trigger();
     tc_fence_before();
     __syncthreads();
+    cluster_sync();  // the other CTA's barriers are initialised before anything is multicast to them
     tc_fence_after();
     const uint32_t tmem = s_tmem;
-    const int ntiles = A.ntm * A.ntn;
+    const int rank = static_cast<int>(cluster_rank());
+    const int cid = blockIdx.x / kHCl, ncl = gridDim.x / kHCl;
+    const int npm = (A.ntm + kHCl - 1) / kHCl;  // row-tile pairs
+    const int npairs = npm * A.ntn;
     const int nk = A.d / kHK;
     volatile int* abort_flag = &s_abort;
     auto give_up = [&]() {
@@ -162,16 +220,18 @@ __global__ void __launch_bounds__(kHThreads, 1) lmhead_verify_kernel(const __gri
         // ================= TMA producer =================
         if (lane == 0) {
             int st = 0, it = 0;
-            for (int t = blockIdx.x; t < ntiles && !*abort_flag; t += gridDim.x) {
-                const int tm = t % A.ntm, tn = t / A.ntm;
+            for (int pr = cid; pr < npairs && !*abort_flag; pr += ncl) {
+                const int tm = kHCl * (pr % npm) + rank, tn = pr / npm;  // rows past the end read as zeros
                 for (int kb = 0; kb < nk; ++kb, ++it) {
                     if (it >= kHStages && !mbar_wait_bounded(&s_empty[st], ((it / kHStages) + 1) & 1)) {
                         give_up();
                         break;
                     }
+                    // this stage's bytes: my A tile, my half of the W tile and the other CTA's half
                     mbar_add_tx(&s_full[st], kHABytes + kHBBytes);
                     tma_load_2d(sA + st * kHABytes, &A.tmA, kb * kHK, tm * kHM, &s_full[st]);
-                    tma_load_2d(sB + st * kHBBytes, &A.tmB, kb * kHK, tn * kHN, &s_full[st]);
+                    tma_load_2d_mc(sB + st * kHBBytes + rank * kHBHalf, &A.tmB, kb * kHK, tn * kHN + rank * (kHN / kHCl),
+                                   &s_full[st], kHMask);
                     mbar_arrive(&s_full[st]);
                     if (++st == kHStages) st = 0;
                 }
@@ -186,7 +246,7 @@ __global__ void __launch_bounds__(kHThreads, 1) lmhead_verify_kernel(const __gri
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_bf16(kHM, kHN);
             int st = 0, it = 0, lt = 0;
-            for (int t = blockIdx.x; t < ntiles && !*abort_flag; t += gridDim.x, ++lt) {
+            for (int pr = cid; pr < npairs && !*abort_flag; pr += ncl, ++lt) {
                 const int b = lt & 1;
                 if (lt >= 2 && !mbar_wait_bounded(&s_acce[b], ((lt >> 1) + 1) & 1)) {
                     give_up();
@@ -205,7 +265,7 @@ __global__ void __launch_bounds__(kHThreads, 1) lmhead_verify_kernel(const __gri
 #pragma unroll
                     for (int kk = 0; kk < kHK / 16; ++kk)
                         tc_mma(dt, sdesc_k128(a0 + kk * 32), sdesc_k128(b0 + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
-                    tc_commit(&s_empty[st]);  // the stage is free once these MMAs have read it
+                    tc_commit_mc(&s_empty[st], kHMask);  // both CTAs learn when these MMAs have read the stage
                     if (++st == kHStages) st = 0;
                 }
                 if (!ok) {
@@ -224,7 +284,7 @@ __global__ void __launch_bounds__(kHThreads, 1) lmhead_verify_kernel(const __gri
         const int q = warp & 3;  // the tensor-memory lanes this warp may read: 32 q .. 32 q + 31
         const int V = P.V;
         int lt = 0;
-        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++lt) {
+        for (int pr = cid; pr < npairs; pr += ncl, ++lt) {
             const int b = lt & 1;
             if (!mbar_wait_bounded(&s_accf[b], (lt >> 1) & 1)) {
                 if (lane == 0) give_up();
@@ -232,13 +292,12 @@ __global__ void __launch_bounds__(kHThreads, 1) lmhead_verify_kernel(const __gri
             }
             if (*abort_flag) break;
             tc_fence_after();
-            const int tm = t % A.ntm, tn = t / A.ntm;
+            const int tm = kHCl * (pr % npm) + rank, tn = pr / npm;
             const int row = tm * kHM + 32 * q + lane;
             const bool live = row < A.rows;
             const int v0 = tn * kHN;
             const uint32_t tb = tmem + (static_cast<uint32_t>(32 * q) << 16) + b * kHN;
-            __nv_bfloat16* lrow = A.logits + static_cast<size_t>(live ? row : 0) * V;
-            const bool vec = (V % 8 == 0) && v0 + kHN <= V;  // whole 16-byte stores
+            const int row0 = tm * kHM + 32 * q;  // the warp's first row
             float xmax = -INFINITY, zmax = -INFINITY;
             bool bad = false;
             // pass 1: round, store, maxima
@@ -263,18 +322,16 @@ __global__ void __launch_bounds__(kHThreads, 1) lmhead_verify_kernel(const __gri
                         if (!GREEDY) zmax = fmaxf(zmax, transform_f32<SOFTCAP, false>(x1, false, P));
                     }
                 }
-                if (live) {
-                    if (vec) {
-                        uint4* dst = reinterpret_cast<uint4*>(lrow + v0 + c0);
+                // the 32 x 32 box goes out through shared memory with one TMA store
+                // (rows past the batch and ids past V are clipped by the store)
+                uint4* box = s_ep[q][(c0 >> 5) & 1];
+                if (lane == 0) tma_store_wait_read<1>();  // this buffer's previous store has read it
+                __syncwarp();
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) dst[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (v0 + c0 + i < V)
-                                reinterpret_cast<uint16_t*>(lrow)[v0 + c0 + i] = static_cast<uint16_t>(w[i >> 1] >> (16 * (i & 1)));
-                    }
-                }
+                for (int u = 0; u < 4; ++u) box[lane * 4 + u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                fence_proxy_async_smem();  // the writes are visible to the TMA unit
+                __syncwarp();
+                if (lane == 0 && row0 < A.rows && v0 + c0 < V) tma_store_2d(&A.tmC, v0 + c0, row0, box);
             }
             // pass 2 (T > 0): the block's sum of exponentials against its largest value
             float s = 0.0f;
@@ -305,8 +362,11 @@ __global__ void __launch_bounds__(kHThreads, 1) lmhead_verify_kernel(const __gri
             }
         }
     }
+    if (warp >= 2 && lane == 0) tma_store_wait_all();  // the staged logits are written out
     tc_fence_before();
     __syncthreads();
+    // neither CTA leaves while the other may still multicast into it or arrive on its barriers
+    cluster_sync();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kHTmemCols);
@@ -334,6 +394,18 @@ EncodeTiledFn encode_fn() {
 }
 
 // A [rows, d] bf16 row-major matrix as 64 x box_rows tiles with the 128-byte swizzle.
+// The logits [rows, V] bf16 as 32 x 32 boxes, no swizzle (rows of 64 bytes in shared memory).
+bool encode_store(CUtensorMap* tm, void* base, int rows, int V) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(V) * 2};
+    const cuuint32_t box[2] = {32, 32};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_k128(CUtensorMap* tm, const void* base, int rows, int d, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return false;
@@ -347,16 +419,41 @@ bool encode_k128(CUtensorMap* tm, const void* base, int rows, int d, int box_row
 }
 
 template <bool G, bool C>
-cudaError_t launch_lmhead_gc(const LmHeadArgs& A, int grid, cudaStream_t s) {
+cudaError_t launch_lmhead_gc(const LmHeadArgs& A, int npairs, cudaStream_t s) {
     static bool configured[128] = {};
+    static int max_clusters[128] = {};
     bool* done = attr_flag(configured);
+    int* mc = max_clusters + (done - configured);
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kHThreads);
+    cfg.dynamicSmemBytes = kHSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kHCl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
     if (!*done) {
-        const cudaError_t e = cudaFuncSetAttribute(lmhead_verify_kernel<G, C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   static_cast<int>(kHSmem));
+        cudaError_t e = cudaFuncSetAttribute(lmhead_verify_kernel<G, C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kHSmem));
         if (e != cudaSuccess) return e;
+        // clusters that fit on the device at once (a GPC with an odd number of free SMs
+        // leaves one idle): the persistent grid is that many, so there is one wave
+        cfg.gridDim = dim3(static_cast<unsigned>(kHCl * (sm_count_cached() / kHCl)));
+        cfg.numAttrs = 1;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, lmhead_verify_kernel<G, C>, &cfg);
+        if (e != cudaSuccess) return e;
+        *mc = n > 0 ? n : 1;
         *done = true;
     }
-    return launch_chained(lmhead_verify_kernel<G, C>, dim3(static_cast<unsigned>(grid)), dim3(kHThreads), kHSmem, s, A);
+    const int grid = kHCl * std::min(npairs, *mc);
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, lmhead_verify_kernel<G, C>, A);
 }
 
 }  // namespace
@@ -368,7 +465,8 @@ cudaError_t launch_lmhead_verify(const void* hidden, const void* weight, int d, 
                                  bool softcap, bool dense, cudaStream_t s) {
     LmHeadArgs A{};
     const int rows = P.B * (P.K + 1);
-    if (!encode_k128(&A.tmA, hidden, rows, d, kHM) || !encode_k128(&A.tmB, weight, P.V, d, kHN))
+    if (!encode_k128(&A.tmA, hidden, rows, d, kHM) || !encode_k128(&A.tmB, weight, P.V, d, kHN / kHCl) ||
+        !encode_store(&A.tmC, logits, rows, P.V))
         return cudaErrorInvalidValue;
     A.rows = rows;
     A.d = d;
@@ -378,9 +476,9 @@ cudaError_t launch_lmhead_verify(const void* hidden, const void* weight, int d, 
     P.logits = logits;
     P.nchunk = P.nblk;  // one record per row and noise block
     A.P = P;
-    const int grid = std::min(A.ntm * A.ntn, sm_count_cached());
-    cudaError_t e = greedy ? (softcap ? launch_lmhead_gc<true, true>(A, grid, s) : launch_lmhead_gc<true, false>(A, grid, s))
-                           : (softcap ? launch_lmhead_gc<false, true>(A, grid, s) : launch_lmhead_gc<false, false>(A, grid, s));
+    const int npairs = (A.ntm + kHCl - 1) / kHCl * A.ntn;
+    cudaError_t e = greedy ? (softcap ? launch_lmhead_gc<true, true>(A, npairs, s) : launch_lmhead_gc<true, false>(A, npairs, s))
+                           : (softcap ? launch_lmhead_gc<false, true>(A, npairs, s) : launch_lmhead_gc<false, false>(A, npairs, s));
     if (e != cudaSuccess) return e;
     P.records_given = 1;
     return launch_verify_dtype<true>(P, greedy, softcap, false, dense, s);
