@@ -63,6 +63,8 @@ def parse():
     ap.add_argument("--cpu-sample", type=int, default=0, help="sequences in the oracle sample (0: auto)")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (smaller profiler captures only)")
+    ap.add_argument("--lmhead-batch", type=int, default=0,
+                    help="only the fused LM head + verify measurement at this batch (profiler captures); prints its JSON")
     return ap.parse_args()
 
 
@@ -883,6 +885,11 @@ def run_reference(args):
 
 def main():
     args = parse()
+    if args.lmhead_batch > 0:
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        print(json.dumps(measure_lmhead(dev, B=args.lmhead_batch)))
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
