@@ -298,14 +298,16 @@ __global__ void __launch_bounds__(kHThreads, 1) lmhead_verify_kernel(const __gri
             const int v0 = tn * kHN;
             const uint32_t tb = tmem + (static_cast<uint32_t>(32 * q) << 16) + b * kHN;
             const int row0 = tm * kHM + 32 * q;  // the warp's first row
-            float xmax = -INFINITY, zmax = -INFINITY;
+            // one pass: round, store, maxima, and (T > 0) the sum of exponentials against
+            // the largest transformed value so far, rescaled when a chunk raises it
+            float xmax = -INFINITY, zmax = -INFINITY, s = 0.0f, msc = 0.0f;
             bool bad = false;
-            // pass 1: round, store, maxima
 #pragma unroll 1
             for (int c0 = 0; c0 < kHN; c0 += 32) {
                 uint32_t r[32];
                 tmem_ld32(tb + c0, r);
                 uint32_t w[16];
+                float cz = -INFINITY;  // the chunk's largest transformed value
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
                     const float f0 = __uint_as_float(r[i]), f1 = __uint_as_float(r[i + 1]);
@@ -315,12 +317,32 @@ __global__ void __launch_bounds__(kHThreads, 1) lmhead_verify_kernel(const __gri
                     const float x0 = __uint_as_float(h0 << 16), x1 = __uint_as_float(h1 << 16);
                     if (v0 + c0 + i < V) {
                         xmax = fmaxf(xmax, x0);
-                        if (!GREEDY) zmax = fmaxf(zmax, transform_f32<SOFTCAP, false>(x0, false, P));
+                        if (!GREEDY) cz = fmaxf(cz, transform_f32<SOFTCAP, false>(x0, false, P));
                     }
                     if (v0 + c0 + i + 1 < V) {
                         xmax = fmaxf(xmax, x1);
-                        if (!GREEDY) zmax = fmaxf(zmax, transform_f32<SOFTCAP, false>(x1, false, P));
+                        if (!GREEDY) cz = fmaxf(cz, transform_f32<SOFTCAP, false>(x1, false, P));
                     }
+                }
+                if (c0 + 32 == kHN) {
+                    // the last read of this accumulator: it may be overwritten once all four warps are here
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&s_acce[b]);
+                }
+                if (!GREEDY) {
+                    if (cz > zmax) {
+                        if (zmax > -INFINITY) s *= ex2_approx((zmax - cz) * P.sc);
+                        zmax = cz;
+                        msc = zmax * P.sc;
+                    }
+                    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float x = (i & 1) ? __uint_as_float(w[i >> 1] & 0xFFFF0000u) : __uint_as_float(w[i >> 1] << 16);
+                        if (v0 + c0 + i < V) acc[i & 3] += ex2_approx(fmaf(sum_transform<SOFTCAP>(x, P), P.sc, -msc));
+                    }
+                    s += (acc[0] + acc[1]) + (acc[2] + acc[3]);
                 }
                 // the 32 x 32 box goes out through shared memory with one TMA store
                 // (rows past the batch and ids past V are clipped by the store)
@@ -333,27 +355,6 @@ __global__ void __launch_bounds__(kHThreads, 1) lmhead_verify_kernel(const __gri
                 __syncwarp();
                 if (lane == 0 && row0 < A.rows && v0 + c0 < V) tma_store_2d(&A.tmC, v0 + c0, row0, box);
             }
-            // pass 2 (T > 0): the block's sum of exponentials against its largest value
-            float s = 0.0f;
-            if (!GREEDY) {
-                const float msc = zmax * P.sc;
-#pragma unroll 1
-                for (int c0 = 0; c0 < kHN; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(tb + c0, r);
-                    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float x = __uint_as_float(bf16_bits(__uint_as_float(r[i])) << 16);
-                        if (v0 + c0 + i < V) acc[i & 3] += ex2_approx(fmaf(sum_transform<SOFTCAP>(x, P), P.sc, -msc));
-                    }
-                    s += (acc[0] + acc[1]) + (acc[2] + acc[3]);
-                }
-            }
-            // the accumulator may be overwritten once all four warps have read it
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_acce[b]);
             if (__any_sync(0xffffffffu, bad && live) && lane == 0) raise_status(P.status, SPECNG_DEV_NONFINITE);
             if (live) {
                 const size_t rec = static_cast<size_t>(row) * P.nblk + tn;
