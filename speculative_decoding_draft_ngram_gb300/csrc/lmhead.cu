@@ -44,9 +44,8 @@ constexpr uint32_t kHBBytes = kHN * kHK * 2;  // 32 KB
 constexpr uint32_t kHTmemCols = 2 * kHN;      // two accumulators
 static_assert(kHN == (1 << kNoiseBlockShift), "a tile's vocab range is one noise block");
 constexpr size_t kHSmem = kHStages * (kHABytes + kHBBytes) + 1024;  // + alignment slack
-constexpr int kHCl = 2;                           // CTAs of a cluster (sharing each W tile)
-constexpr uint32_t kHBHalf = kHBBytes / kHCl;     // the W rows one CTA loads for both
-constexpr uint16_t kHMask = (1u << kHCl) - 1u;    // every CTA of the cluster
+// CTAs of a cluster (CL, a template parameter): 2 (each loads half of the W tile
+// for both) when the row tiles pair up, else 1 (a lone CTA loads its whole W tile).
 
 struct LmHeadArgs {
     CUtensorMap tmA;  // hidden [rows, d] bf16: box {64, 128}, 128-byte swizzle
@@ -168,8 +167,11 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* tm, in
 // A fp32 accumulator rounded to the logits' dtype (round to nearest even), as bits and as a value.
 __device__ __forceinline__ uint32_t bf16_bits(float f) { return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(f))); }
 
-template <bool GREEDY, bool SOFTCAP>
+template <int CL, bool GREEDY, bool SOFTCAP>
 __global__ void __launch_bounds__(kHThreads, 1) lmhead_verify_kernel(const __grid_constant__ LmHeadArgs A) {
+    static_assert(CL == 1 || CL == 2, "clusters of one or two CTAs");
+    constexpr uint32_t kBPart = kHBBytes / CL;    // the W rows one CTA loads (for every CTA of the cluster)
+    constexpr uint16_t kMask = (1u << CL) - 1u;   // every CTA of the cluster
     extern __shared__ uint8_t s_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(s_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* sA = smem;
@@ -185,7 +187,7 @@ __global__ void __launch_bounds__(kHThreads, 1) lmhead_verify_kernel(const __gri
     if (threadIdx.x == 0) {
         for (int i = 0; i < kHStages; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_empty[i], kHCl);  // the MMA completions of both CTAs
+            mbar_init(&s_empty[i], CL);  // the MMA completions of every CTA of the cluster
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_accf[i], 1);
@@ -206,8 +208,8 @@ __global__ void __launch_bounds__(kHThreads, 1) lmhead_verify_kernel(const __gri
     tc_fence_after();
     const uint32_t tmem = s_tmem;
     const int rank = static_cast<int>(cluster_rank());
-    const int cid = blockIdx.x / kHCl, ncl = gridDim.x / kHCl;
-    const int npm = (A.ntm + kHCl - 1) / kHCl;  // row-tile pairs
+    const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;
+    const int npm = (A.ntm + CL - 1) / CL;  // row-tile groups (pairs, or single tiles)
     const int npairs = npm * A.ntn;
     const int nk = A.d / kHK;
     volatile int* abort_flag = &s_abort;
@@ -221,7 +223,7 @@ __global__ void __launch_bounds__(kHThreads, 1) lmhead_verify_kernel(const __gri
         if (lane == 0) {
             int st = 0, it = 0;
             for (int pr = cid; pr < npairs && !*abort_flag; pr += ncl) {
-                const int tm = kHCl * (pr % npm) + rank, tn = pr / npm;  // rows past the end read as zeros
+                const int tm = CL * (pr % npm) + rank, tn = pr / npm;
                 for (int kb = 0; kb < nk; ++kb, ++it) {
                     if (it >= kHStages && !mbar_wait_bounded(&s_empty[st], ((it / kHStages) + 1) & 1)) {
                         give_up();
@@ -230,8 +232,11 @@ __global__ void __launch_bounds__(kHThreads, 1) lmhead_verify_kernel(const __gri
                     // this stage's bytes: my A tile, my half of the W tile and the other CTA's half
                     mbar_add_tx(&s_full[st], kHABytes + kHBBytes);
                     tma_load_2d(sA + st * kHABytes, &A.tmA, kb * kHK, tm * kHM, &s_full[st]);
-                    tma_load_2d_mc(sB + st * kHBBytes + rank * kHBHalf, &A.tmB, kb * kHK, tn * kHN + rank * (kHN / kHCl),
-                                   &s_full[st], kHMask);
+                    if constexpr (CL == 1)
+                        tma_load_2d(sB + st * kHBBytes, &A.tmB, kb * kHK, tn * kHN, &s_full[st]);
+                    else
+                        tma_load_2d_mc(sB + st * kHBBytes + rank * kBPart, &A.tmB, kb * kHK, tn * kHN + rank * (kHN / CL),
+                                       &s_full[st], kMask);
                     mbar_arrive(&s_full[st]);
                     if (++st == kHStages) st = 0;
                 }
@@ -265,7 +270,11 @@ __global__ void __launch_bounds__(kHThreads, 1) lmhead_verify_kernel(const __gri
 #pragma unroll
                     for (int kk = 0; kk < kHK / 16; ++kk)
                         tc_mma(dt, sdesc_k128(a0 + kk * 32), sdesc_k128(b0 + kk * 32), idesc, (kb | kk) != 0 ? 1u : 0u);
-                    tc_commit_mc(&s_empty[st], kHMask);  // both CTAs learn when these MMAs have read the stage
+                    // every CTA of the cluster learns when these MMAs have read the stage
+                    if constexpr (CL == 1)
+                        tc_commit(&s_empty[st]);
+                    else
+                        tc_commit_mc(&s_empty[st], kMask);
                     if (++st == kHStages) st = 0;
                 }
                 if (!ok) {
@@ -292,7 +301,7 @@ __global__ void __launch_bounds__(kHThreads, 1) lmhead_verify_kernel(const __gri
             }
             if (*abort_flag) break;
             tc_fence_after();
-            const int tm = kHCl * (pr % npm) + rank, tn = pr / npm;
+            const int tm = CL * (pr % npm) + rank, tn = pr / npm;
             const int row = tm * kHM + 32 * q + lane;
             const bool live = row < A.rows;
             const int v0 = tn * kHN;
@@ -419,8 +428,8 @@ bool encode_k128(CUtensorMap* tm, const void* base, int rows, int d, int box_row
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool G, bool C>
-cudaError_t launch_lmhead_gc(const LmHeadArgs& A, int npairs, cudaStream_t s) {
+template <int CL, bool G, bool C>
+cudaError_t launch_lmhead_gc(const LmHeadArgs& A, int ngroups, cudaStream_t s) {
     static bool configured[128] = {};
     static int max_clusters[128] = {};
     bool* done = attr_flag(configured);
@@ -430,31 +439,40 @@ cudaError_t launch_lmhead_gc(const LmHeadArgs& A, int npairs, cudaStream_t s) {
     cfg.dynamicSmemBytes = kHSmem;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kHCl;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = CL;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
     if (!*done) {
-        cudaError_t e = cudaFuncSetAttribute(lmhead_verify_kernel<G, C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(lmhead_verify_kernel<CL, G, C>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(kHSmem));
         if (e != cudaSuccess) return e;
-        // clusters that fit on the device at once (a GPC with an odd number of free SMs
-        // leaves one idle): the persistent grid is that many, so there is one wave
-        cfg.gridDim = dim3(static_cast<unsigned>(kHCl * (sm_count_cached() / kHCl)));
-        cfg.numAttrs = 1;
-        int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, lmhead_verify_kernel<G, C>, &cfg);
-        if (e != cudaSuccess) return e;
+        int n = sm_count_cached();  // one CTA per SM
+        if (CL > 1) {
+            // clusters that fit on the device at once (a GPC with an odd number of free SMs
+            // leaves one idle): the persistent grid is that many, so there is one wave
+            cfg.gridDim = dim3(static_cast<unsigned>(CL * (sm_count_cached() / CL)));
+            cfg.attrs = attr + 1;
+            cfg.numAttrs = 1;
+            e = cudaOccupancyMaxActiveClusters(&n, lmhead_verify_kernel<CL, G, C>, &cfg);
+            if (e != cudaSuccess) return e;
+            cfg.attrs = attr;
+        }
         *mc = n > 0 ? n : 1;
         *done = true;
     }
-    const int grid = kHCl * std::min(npairs, *mc);
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, lmhead_verify_kernel<G, C>, A);
+    cfg.gridDim = dim3(static_cast<unsigned>(CL * std::min(ngroups, *mc)));
+    cfg.numAttrs = CL > 1 ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, lmhead_verify_kernel<CL, G, C>, A);
+}
+
+template <int CL>
+cudaError_t launch_lmhead_cl(const LmHeadArgs& A, int ngroups, bool greedy, bool softcap, cudaStream_t s) {
+    if (greedy) return softcap ? launch_lmhead_gc<CL, true, true>(A, ngroups, s) : launch_lmhead_gc<CL, true, false>(A, ngroups, s);
+    return softcap ? launch_lmhead_gc<CL, false, true>(A, ngroups, s) : launch_lmhead_gc<CL, false, false>(A, ngroups, s);
 }
 
 }  // namespace
@@ -466,20 +484,21 @@ cudaError_t launch_lmhead_verify(const void* hidden, const void* weight, int d, 
                                  bool softcap, bool dense, cudaStream_t s) {
     LmHeadArgs A{};
     const int rows = P.B * (P.K + 1);
-    if (!encode_k128(&A.tmA, hidden, rows, d, kHM) || !encode_k128(&A.tmB, weight, P.V, d, kHN / kHCl) ||
-        !encode_store(&A.tmC, logits, rows, P.V))
-        return cudaErrorInvalidValue;
     A.rows = rows;
     A.d = d;
     A.ntm = (rows + kHM - 1) / kHM;
     A.ntn = (P.V + kHN - 1) / kHN;
+    const int cl = A.ntm % 2 == 0 ? 2 : 1;  // pairs of row tiles when they pair up
+    if (!encode_k128(&A.tmA, hidden, rows, d, kHM) || !encode_k128(&A.tmB, weight, P.V, d, kHN / cl) ||
+        !encode_store(&A.tmC, logits, rows, P.V))
+        return cudaErrorInvalidValue;
     A.logits = static_cast<__nv_bfloat16*>(logits);
     P.logits = logits;
     P.nchunk = P.nblk;  // one record per row and noise block
     A.P = P;
-    const int npairs = (A.ntm + kHCl - 1) / kHCl * A.ntn;
-    cudaError_t e = greedy ? (softcap ? launch_lmhead_gc<true, true>(A, npairs, s) : launch_lmhead_gc<true, false>(A, npairs, s))
-                           : (softcap ? launch_lmhead_gc<false, true>(A, npairs, s) : launch_lmhead_gc<false, false>(A, npairs, s));
+    const int ngroups = A.ntm / cl * A.ntn;
+    cudaError_t e = cl == 2 ? launch_lmhead_cl<2>(A, ngroups, greedy, softcap, s)
+                            : launch_lmhead_cl<1>(A, ngroups, greedy, softcap, s);
     if (e != cudaSuccess) return e;
     P.records_given = 1;
     return launch_verify_dtype<true>(P, greedy, softcap, false, dense, s);
