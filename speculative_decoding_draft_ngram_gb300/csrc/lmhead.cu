@@ -15,12 +15,14 @@
 // drafts) and of the engine's tensor path (AX Engine page, "Core Technical
 // Architecture & Methods": the forward's operations run as GPU tensor ops).
 //
-// Layout of the work: one CTA per SM, persistent, in clusters of two; tiles
-// of 128 rows x 256 vocab ids (one noise block).  The two CTAs of a cluster
-// take the two row tiles of a pair for the same vocab tile, and each loads
-// half of that W tile and multicasts it to both, so each SM reads a third
-// less from L2 than a lone CTA would; pairs are ordered row tiles first, so
-// the clusters running at the same time share their W tiles through L2.
+// Layout of the work: one CTA per SM, persistent; tiles of 128 rows x 256
+// vocab ids (one noise block).  When the row tiles pair up, CTAs run in
+// clusters of two: the two take the row tiles of a pair for the same vocab
+// tile, and each loads half of that W tile and multicasts it to both, so
+// each SM reads a third less from L2 than a lone CTA would (an odd number of
+// row tiles runs single CTAs, each loading its whole W tile).  Work is
+// ordered row tiles first, so the CTAs running at the same time share their
+// W tiles through L2.
 // Warp 0 issues the TMA loads (128-byte swizzled, 64 hidden elements per
 // stage, a 4-stage ring), warp 1 owns the tensor memory (two 256-column
 // accumulators) and one of its threads issues the MMAs, warps 2-5 read an
