@@ -440,6 +440,22 @@ def measure_sub_workloads(dev, peak, names):
     return out
 
 
+def step_summary(acc, k, K):
+    """Per-step metrics of the steps run after the timed loop: acc, k [steps, B]
+    (accept lengths, drafts offered).  Each call emits a + 1 tokens per sequence."""
+    a = acc.long()
+    hist = torch.bincount(a.flatten(), minlength=K + 1)[:K + 1].tolist()
+    offered = int(k.long().sum())
+    return {
+        "steps": int(a.shape[0]),
+        "accept_len_hist": hist,                                   # counts of a = 0..K over steps x sequences
+        "tokens_per_sequence_step": float((a + 1).double().mean()),
+        "tokens_per_step": float((a + 1).double().sum(1).mean()),   # the whole batch
+        "drafts_offered_per_step": float(k.long().sum(1).double().mean()),
+        "acceptance_rate": (float(a.sum()) / offered) if offered else None,
+    }
+
+
 def measure_lmhead(dev, B=256, K=4, V=151936, d=2560, reps=20):
     """Fused LM head + verify (spec_verify_lmhead) at the c5 batch shape with a
     Qwen3-4B-sized head (d = 2560, V = 151936), no repetition penalty (the fused
@@ -636,10 +652,14 @@ def run_ours(args):
     # the split of a step (events between its calls; outside the timed loop, since an
     # event between two kernels stops the next one from launching early)
     nbreak = len(evs)
+    acc_steps, k_steps = [], []   # per-step accept lengths and draft counts (outside the timed region)
     for i in range(nbreak):
         s = base + args.steps + i
+        k_steps.append((path.kbuf[s] if path.ngram else path.kfull).clone())
         path.step(s, path.logits[s % path.n_sets], evs[i], rowmax=path.rowmax[s % path.n_sets])
+        acc_steps.append(path.acc.clone())
     torch.cuda.synchronize()
+    step_metrics = step_summary(torch.stack(acc_steps).cpu(), torch.stack(k_steps).cpu(), cfg.K)
     verify_ms = [a.elapsed_time(b) for a, b, _ in evs]
     library_ms = [a.elapsed_time(c) for a, _, c in evs]   # spec_verify + spec_commit / spec_append
     rows_nominal = args.steps * cfg.B * (cfg.K + 1)
@@ -738,6 +758,7 @@ def run_ours(args):
         },
         "gpu_launches": path.launches_per_step * args.steps,
         "e2e": e2e,
+        "step_metrics": step_metrics,
         "workloads": subs,
         "clocks": clk,
         "device_status": sp.status_names(status),

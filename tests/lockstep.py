@@ -39,7 +39,18 @@ class Report:
     accepted: int = 0
     drafted: int = 0
     gated: int = 0
+    accept_hist: list = field(default_factory=list)   # counts of accept length a = 0, 1, ... (oracle side)
     notes: list = field(default_factory=list)
+
+    def count_accepts(self, a):
+        for v in np.asarray(a).ravel().tolist():
+            while len(self.accept_hist) <= v:
+                self.accept_hist.append(0)
+            self.accept_hist[v] += 1
+
+    def tokens_per_sequence_step(self) -> float:
+        n = sum(self.accept_hist)
+        return sum((i + 1) * c for i, c in enumerate(self.accept_hist)) / n if n else 0.0
 
 
 GATE_KEYS = ("probe_interval", "cool_steps")
@@ -161,6 +172,7 @@ def run_sampled(cfg: wl.Config, steps: int, sample: int, T: float | None = None,
         rep.rows_read += int((res["k_eff"] + 1).sum())
         rep.accepted += int(res["accept_len"].sum())
         rep.drafted += int(res["k_eff"].sum())
+        rep.count_accepts(res["accept_len"])
         bad = compare(step, a_g, t_g, kv_gh, ema_gh, res, rep, ids)
         sp.spec_append(hist_g, lens_g, out_tok, out_acc)
         for i in range(len(ids)):
@@ -278,6 +290,7 @@ def run(cfg: wl.Config, steps: int, T: float | None = None, device="cuda", seed:
         rep.rows_read += int((k_eff + 1).sum())
         rep.accepted += int(a_o.sum())
         rep.drafted += int(k_eff.sum())
+        rep.count_accepts(a_o)
         rep.gated += int(((k.numpy() > 0) & (k_eff == 0)).sum())
         bad = compare(step, a_g, t_g, kv_gh, ema_gh, res, rep)
         if cooling:

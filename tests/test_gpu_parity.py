@@ -51,6 +51,11 @@ def test_lockstep(name):
         assert rep.drafted > 0
     if name in ("c2_t06", "c2_greedy", "c3_softcap_gate", "c1"):
         assert rep.accepted > 0
+    # per-step metrics: one accept length per sequence and step, a + 1 tokens each
+    n = sum(rep.accept_hist)
+    assert n == rep.rows // (cfg.K + 1)
+    assert sum(i * c for i, c in enumerate(rep.accept_hist)) == rep.accepted
+    assert abs(rep.tokens_per_sequence_step() - (1 + rep.accepted / n)) < 1e-12
 
 
 # A low starting EMA with the gate off: the EMA update runs from a state far
