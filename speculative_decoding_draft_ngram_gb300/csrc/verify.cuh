@@ -1529,10 +1529,19 @@ __global__ void __launch_bounds__(kST, 2) verify_seq_kernel(const __grid_constan
                 const int cc = lane + 32 * i;
                 pv[i] = cc < P.nchunk ? __ldcg(reinterpret_cast<const float2*>(pr + cc)) : make_float2(0.0f, 0.0f);
             }
-            for (int cc = lane + 32 * kPr; cc < P.nchunk; cc += 32) {
-                const float2 p = __ldcg(reinterpret_cast<const float2*>(pr + cc));
-                if (p.y != 0.0f || __float_as_uint(p.x) != 0u) mf = fmaxf(mf, p.x);
-                proof |= p.y < 0.0f;
+            // the rest (rows of many records, e.g. one per noise block): four loads in flight
+            for (int c0 = lane + 32 * kPr; c0 < P.nchunk; c0 += 32 * kPr) {
+                float2 pb[kPr];
+#pragma unroll
+                for (int u = 0; u < kPr; ++u) {
+                    const int cc = c0 + 32 * u;
+                    pb[u] = cc < P.nchunk ? __ldcg(reinterpret_cast<const float2*>(pr + cc)) : make_float2(0.0f, 0.0f);
+                }
+#pragma unroll
+                for (int u = 0; u < kPr; ++u) {
+                    if (pb[u].y != 0.0f || __float_as_uint(pb[u].x) != 0u) mf = fmaxf(mf, pb[u].x);
+                    proof |= pb[u].y < 0.0f;
+                }
             }
 #pragma unroll
             for (int i = 0; i < kPr; ++i) {
@@ -1551,7 +1560,16 @@ __global__ void __launch_bounds__(kST, 2) verify_seq_kernel(const __grid_constan
             };
 #pragma unroll
             for (int i = 0; i < kPr; ++i) Sf += term(pv[i]);
-            for (int cc = lane + 32 * kPr; cc < P.nchunk; cc += 32) Sf += term(__ldcg(reinterpret_cast<const float2*>(pr + cc)));
+            for (int c0 = lane + 32 * kPr; c0 < P.nchunk; c0 += 32 * kPr) {
+                float2 pb[kPr];
+#pragma unroll
+                for (int u = 0; u < kPr; ++u) {
+                    const int cc = c0 + 32 * u;
+                    pb[u] = cc < P.nchunk ? __ldcg(reinterpret_cast<const float2*>(pr + cc)) : make_float2(0.0f, 0.0f);
+                }
+#pragma unroll
+                for (int u = 0; u < kPr; ++u) Sf += term(pb[u]);
+            }
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) Sf += __shfl_xor_sync(0xffffffffu, Sf, off);
             for (int cc = lane; cc < P.nchunk; cc += 32) pr[cc] = SegSum{0.0f, 0.0f};  // leave the workspace zeroed
