@@ -356,7 +356,11 @@ int spec_verify_noalloc(const void* logits, int logits_dtype, int B, int K, int 
  *              V must be a multiple of 8 (16-byte rows).
  * workspace    device scratch of at least spec_verify_lmhead_workspace_bytes
  *              (B, K, V) bytes, 256-byte aligned, zero-filled before the
- *              first call; the call leaves it ready for the next one.
+ *              first call; the call leaves it ready for the next
+ *              spec_verify_lmhead call (every record is rewritten each
+ *              call).  Its layout differs from spec_verify's: zero it again
+ *              (spec_verify_workspace_init) before a spec_verify call uses
+ *              the same buffer.
  * Other arguments as for spec_verify.  Not supported (SPECNG_EINVAL): the
  * repetition penalty (rep_penalty != 1 with rep_window > 0) and the
  * single-kernel schedule.  SPECNG_EINVAL also when the tensor maps of
