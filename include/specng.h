@@ -336,7 +336,7 @@ int spec_verify_noalloc(const void* logits, int logits_dtype, int B, int K, int 
                         int32_t* kv_len, float* ema,
                         int32_t* out_tokens, int32_t* out_accept_len, cudaStream_t s);
 
-/* Fused LM head + verify (scope row f1).  The target model's last
+/* Fused LM head + verify.  The target model's last
  * projection and the verify of the drafts in one call: the logits of the
  * K + 1 positions are logits = hidden W^T (SwiftLM page, Leviathan
  * paragraph: the target scores the K drafts and the bonus position in one
