@@ -168,3 +168,28 @@ def test_lmhead_rejects_what_it_does_not_support():
     rc = L.spec_verify_lmhead(buf, buf, 64, buf, 1, 1, 60, buf, None, buf, None, 0, None, ctypes.byref(p),
                               buf, buf, buf, buf, buf, 1 << 20, None)
     assert rc == -1  # V not a multiple of 8
+
+
+def test_lmhead_host_checks_null_alignment_schedule_and_workspace_size():
+    # host-side checks that run before any CUDA call (no GPU needed)
+    import ctypes
+    from speculative_decoding_draft_ngram_gb300 import capi
+    L = capi.load()
+    p = sp.VerifyParams(temperature=1.0).to_c()
+    ok = ctypes.c_void_p(4096)
+    bad = ctypes.c_void_p(4096 + 8)   # 8-byte aligned only
+    args = lambda h, w, d, lg: (h, w, d, lg, 1, 1, 64, ok, None, ok, None, 0, None, ctypes.byref(p),
+                                ok, ok, ok, ok, ok, 1 << 20, None)
+    assert L.spec_verify_lmhead(*args(None, ok, 64, ok)) == -1          # NULL hidden
+    assert L.spec_verify_lmhead(*args(bad, ok, 64, ok)) == -2           # SPECNG_EALIGN
+    assert L.spec_verify_lmhead(*args(ok, ok, 64, bad)) == -2
+    assert L.spec_verify_lmhead(*args(ok, ok, (1 << 20) + 64, ok)) == -1  # d out of range
+    pf = sp.VerifyParams(temperature=1.0, schedule=1).to_c()
+    a = list(args(ok, ok, 64, ok))
+    a[13] = ctypes.byref(pf)
+    assert L.spec_verify_lmhead(*a) == -1                                # single-kernel schedule
+    # the workspace: one 8-byte record per row and noise block beyond spec_verify's per-segment records
+    B, K, V = 8, 4, 151936
+    assert sp.spec_verify_lmhead_workspace_bytes(B, K, V) > sp.spec_verify_workspace_bytes(B, K, V)
+    assert sp.spec_verify_lmhead_workspace_bytes(B, K, V) % 256 == 0
+    assert sp.spec_verify_lmhead_workspace_bytes(0, K, V) == 0
