@@ -294,6 +294,7 @@ __global__ void __launch_bounds__(kHThreads, 1) lmhead_verify_kernel(const __gri
         // ================= epilogue =================
         const int q = warp & 3;  // the tensor-memory lanes this warp may read: 32 q .. 32 q + 31
         const int V = P.V;
+        int last_buf = -1;  // lane 0: staging buffer of the latest committed store (boxes past the data are skipped)
         int lt = 0;
         for (int pr = cid; pr < npairs; pr += ncl, ++lt) {
             const int b = lt & 1;
@@ -357,14 +358,25 @@ __global__ void __launch_bounds__(kHThreads, 1) lmhead_verify_kernel(const __gri
                 }
                 // the 32 x 32 box goes out through shared memory with one TMA store
                 // (rows past the batch and ids past V are clipped by the store)
-                uint4* box = s_ep[q][(c0 >> 5) & 1];
-                if (lane == 0) tma_store_wait_read<1>();  // this buffer's previous store has read it
+                const int bb = (c0 >> 5) & 1;
+                uint4* box = s_ep[q][bb];
+                // this buffer's previous store has read it: all but the latest committed store
+                // are, and the latest too when it used this buffer
+                if (lane == 0) {
+                    if (last_buf == bb)
+                        tma_store_wait_read<0>();
+                    else
+                        tma_store_wait_read<1>();
+                }
                 __syncwarp();
 #pragma unroll
                 for (int u = 0; u < 4; ++u) box[lane * 4 + u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
                 fence_proxy_async_smem();  // the writes are visible to the TMA unit
                 __syncwarp();
-                if (lane == 0 && row0 < A.rows && v0 + c0 < V) tma_store_2d(&A.tmC, v0 + c0, row0, box);
+                if (lane == 0 && row0 < A.rows && v0 + c0 < V) {
+                    tma_store_2d(&A.tmC, v0 + c0, row0, box);
+                    last_buf = bb;
+                }
             }
             if (__any_sync(0xffffffffu, bad && live) && lane == 0) raise_status(P.status, SPECNG_DEV_NONFINITE);
             if (live) {

@@ -131,6 +131,28 @@ def test_full_vocab_and_batch_sampled_sequences():
 
 
 @pytest.mark.gpu
+def test_many_row_tiles_and_a_partial_last_vocab_tile():
+    # 153 row tiles (odd: single CTAs) on 152 SMs and V = 264 (a second vocab tile of 8 ids):
+    # some CTAs run two tiles of the last vocab column one after the other, whose trailing
+    # boxes lie past V; every logit and a sample of sequences' tokens against the oracle
+    B, K, V, d = 19584, 0, 264, 64
+    g = torch.Generator().manual_seed(13)
+    hidden = _grid(g, (B, K + 1, d))
+    weight = _grid(g, (V, d))
+    drafts = np.zeros((B, 1), dtype=np.int32)
+    k = np.zeros(B, dtype=np.int32)
+    kw = dict(temperature=0.7, gate_enabled=False, seed=2, step=5)
+    logits, out, acc, kv, ema = _run_gpu(hidden, weight, drafts[:, :0], k, kw)
+    ref = ol.lm_head_logits(hidden.float().numpy(), weight.float().numpy())
+    np.testing.assert_array_equal(logits.float().cpu().numpy(), ref)
+    for b in (0, 1, 153, 19583):
+        res = ov.spec_verify(ref[b:b + 1], drafts[b:b + 1, :0], None, k[b:b + 1], np.zeros((1, 1), int),
+                             np.zeros(1, int), ov.VerifyParams(**kw), np.full(1, 100), np.ones(1), seq_ids=np.array([b]))
+        np.testing.assert_array_equal(out[b], res["out_tokens"][0])
+    assert sp.get_status() == 0
+
+
+@pytest.mark.gpu
 def test_gaussian_inputs_within_rounding():
     # the GEMM alone: fp32 accumulation, then one rounding to bf16.  Against the
     # fp64 product rounded once: one bf16 ulp (the fp32 error can move a value
