@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kHThreads, 1) lmhead_verify_kernel(const __gri
     const int rank = static_cast<int>(cluster_rank());
     const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;
     const int npm = (A.ntm + CL - 1) / CL;  // row-tile groups (pairs, or single tiles)
-    const int npairs = npm * A.ntn;
+    const int npairs = npm * A.ntn;  // work units: a row-tile group and a vocab tile
     const int nk = A.d / kHK;
     volatile int* abort_flag = &s_abort;
     auto give_up = [&]() {
@@ -231,7 +231,8 @@ __global__ void __launch_bounds__(kHThreads, 1) lmhead_verify_kernel(const __gri
                         give_up();
                         break;
                     }
-                    // this stage's bytes: my A tile, my half of the W tile and the other CTA's half
+                    // this stage's bytes: my A tile and the W tile (in a cluster of two, my half
+                    // of it and the other CTA's half, each multicast to both)
                     mbar_add_tx(&s_full[st], kHABytes + kHBBytes);
                     tma_load_2d(sA + st * kHABytes, &A.tmA, kb * kHK, tm * kHM, &s_full[st]);
                     if constexpr (CL == 1)
